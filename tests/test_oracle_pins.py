@@ -1,0 +1,402 @@
+"""Pins for the fp64 oracle: each test checks it against something other than
+itself -- brute force, a closed form, a library routine, an invariant, or a
+hand-worked value -- chosen so that a dropped term, a wrong sign, a wrong index
+or a transposed operand in the oracle fails at least one of them.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+TEMPS = (0.2, 0.7, 1.0, 1.8)   # the temperatures the RL-Kernel GPU suite exercises
+
+
+def f32(x):
+    return float(np.float32(x))
+
+
+def score_all_ids(oracle, row, temperature, top_p):
+    """Score one row once per vocabulary id (row repeated V times)."""
+    row = np.asarray(row)
+    V = row.shape[0]
+    rep = np.ascontiguousarray(np.repeat(row[None, :], V, axis=0))
+    return oracle.logprob_entropy(rep, np.arange(V, dtype=np.int32), temperature, top_p)
+
+
+# --------------------------------------------------------------------------
+# Brute force over every subset (V = 8).
+# --------------------------------------------------------------------------
+
+def brute_nucleus(z, temperature, top_p):
+    """Smallest-cardinality id set with mass >= top_p; among those the largest
+    mass; among equal masses the lexicographically smallest sorted id tuple."""
+    T = f32(temperature)
+    p = f32(top_p)
+    x = [float(v) / T for v in z]
+    mx = max(x)
+    w = [math.exp(v - mx) for v in x]
+    Z = math.fsum(w)
+    V = len(z)
+    best = None
+    for size in range(1, V + 1):
+        for ids in itertools.combinations(range(V), size):
+            mass = math.fsum(w[i] for i in ids) / Z
+            if mass >= p:
+                key = (-mass, ids)
+                if best is None or key < best[0]:
+                    best = (key, ids)
+        if best is not None:
+            break
+    S = best[1]
+    ZS = math.fsum(w[i] for i in S)
+    lp = {i: (x[i] - mx) - math.log(ZS) for i in S}
+    H = -math.fsum((w[i] / ZS) * math.log(w[i] / ZS) for i in S)
+    return set(S), lp, H
+
+
+@pytest.mark.parametrize("temperature", [0.7, 1.0])
+def test_bruteforce_v8(oracle, temperature):
+    z, _ = workloads.brute_v8(seed=0)
+    z = z.numpy()
+    checked = 0
+    for r in range(z.shape[0]):
+        lp, ent, k, gap = score_all_ids(oracle, z[r], temperature, 0.9)
+        if gap[0] < 1e-9:
+            continue
+        S, blp, bH = brute_nucleus(z[r], temperature, 0.9)
+        members = {i for i in range(8) if np.isfinite(lp[i])}
+        assert members == S
+        assert k[0] == len(S)
+        for i in range(8):
+            if i in S:
+                assert abs(lp[i] - blp[i]) < 1e-12
+            else:
+                assert lp[i] == -np.inf
+        assert abs(ent[0] - bH) < 1e-12
+        checked += 1
+    assert checked >= 12
+
+
+def test_bruteforce_ties_lower_id_first(oracle):
+    # Equal logits: the brute force prefers the lexicographically smallest id set,
+    # i.e. ties are kept lower id first.
+    z = np.array([1.0, 2.0, 2.0, 0.5, 2.0, 1.0, -1.0, 2.0], np.float32)
+    for p in (0.3, 0.5, 0.6, 0.75, 0.9, 0.97):
+        lp, ent, k, gap = score_all_ids(oracle, z, 1.0, p)
+        S, blp, bH = brute_nucleus(z, 1.0, p)
+        assert {i for i in range(8) if np.isfinite(lp[i])} == S
+        assert abs(ent[0] - bH) < 1e-12
+    # bf16 bit patterns, including -0 and +0 which rank as equal values.
+    bits = np.array([0x8000, 0x0000, 0x3F80, 0x3F80, 0x0000, 0xBF80, 0x8000, 0x3F80], np.uint16)
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    for p in (0.2, 0.45, 0.7, 0.8, 0.95):
+        lp, ent, k, gap = score_all_ids(oracle, bits, 1.0, p)
+        S, blp, bH = brute_nucleus(vals, 1.0, p)
+        assert {i for i in range(8) if np.isfinite(lp[i])} == S
+        assert abs(ent[0] - bH) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# Closed forms.
+# --------------------------------------------------------------------------
+
+def test_uniform_logits_entropy_is_log_k(oracle):
+    V = 1000
+    row = np.full(V, 0.375, np.float32)
+    # p = 0.9005: pV is not near an integer, so k* = ceil(pV) = 901 exactly.
+    lp, ent, k, gap = score_all_ids(oracle, row, 0.7, 0.9005)
+    assert k[0] == 901
+    assert abs(ent[0] - math.log(901)) < 1e-12
+    assert np.all(np.abs(lp[:901] + math.log(901)) < 1e-12)   # lower ids kept first
+    assert np.all(lp[901:] == -np.inf)
+    # top_p = 1 keeps the whole vocabulary.
+    lp, ent, k, gap = score_all_ids(oracle, row, 0.7, 1.0)
+    assert k[0] == V and gap[0] == np.inf
+    assert abs(ent[0] - math.log(V)) < 1e-12
+
+
+def test_uniform_gap_value(oracle):
+    # float32(0.9) = 0.89999997615814...: C_899 = 0.899 < p <= C_900 = 0.9.
+    row = np.zeros(1000, np.float32)
+    lp, ent, k, gap = oracle.logprob_entropy(row[None, :], np.zeros(1, np.int32), 1.0, 0.9)
+    p = f32(0.9)
+    assert k[0] == 900
+    assert abs(gap[0] - min(p - 0.899, 0.9 - p)) < 1e-15
+
+
+@pytest.mark.parametrize("temperature", TEMPS)
+def test_top_p_one_is_log_softmax(oracle, temperature):
+    z, ids = workloads.tiny(seed=0)
+    lp, ent, k, gap = oracle.logprob_entropy(z.numpy(), ids.numpy(), temperature, 1.0)
+    zz = z.double() / f32(temperature)
+    ref_lp = torch.log_softmax(zz, dim=1)
+    ref_ent = torch.special.entr(torch.softmax(zz, dim=1)).sum(dim=1)
+    sel = ref_lp[torch.arange(z.shape[0]), ids.long()].numpy()
+    assert np.max(np.abs(lp - sel)) < 1e-12
+    assert np.max(np.abs(ent - ref_ent.numpy())) < 1e-12
+    assert np.all(k == z.shape[1])
+
+
+def test_one_hot_peak(oracle):
+    V = 500
+    T = 0.7
+    row = np.zeros(V, np.float32)
+    row[123] = f32(60 * T + 1)
+    lp, ent, k, gap = score_all_ids(oracle, row, T, 0.95)
+    assert k[0] == 1
+    assert lp[123] == 0.0
+    assert ent[0] == 0.0
+    assert np.all(np.delete(lp, 123) == -np.inf)
+
+
+@pytest.mark.parametrize("a,b,alpha,beta,T,p", [
+    (5, 300, 2.0, 0.0, 0.7, 0.6),
+    (5, 300, 2.0, 0.0, 0.7, 0.95),
+    (40, 10, 1.0, 0.5, 1.0, 0.5),
+    (3, 997, 4.0, -1.0, 1.8, 0.93),
+    (7, 50, 0.25, -0.25, 0.2, 0.999),
+])
+def test_two_level_logits(oracle, a, b, alpha, beta, T, p):
+    V = a + b
+    rng = np.random.default_rng(a * 1000 + b)
+    pos = rng.permutation(V)
+    hi_ids = np.sort(pos[:a])
+    lo_ids = np.sort(pos[a:])
+    row = np.empty(V, np.float32)
+    row[hi_ids] = alpha
+    row[lo_ids] = beta
+    Tf, pf = f32(T), f32(p)
+    wb = math.exp((beta - alpha) / Tf)       # w of a low token, w of a high token is 1
+    Z = a + b * wb
+    if pf * Z <= a:
+        n_hi, n_lo = math.ceil(pf * Z), 0
+    else:
+        n_hi, n_lo = a, math.ceil((pf * Z - a) / wb)
+    ZS = n_hi + n_lo * wb
+    qa, qb = 1.0 / ZS, wb / ZS
+    H = -(n_hi * qa * math.log(qa) + (n_lo * qb * math.log(qb) if n_lo else 0.0))
+    lp, ent, k, gap = score_all_ids(oracle, row, T, p)
+    assert gap[0] > 1e-9
+    assert k[0] == n_hi + n_lo
+    assert abs(ent[0] - H) < 1e-11
+    members = set(hi_ids[:n_hi].tolist()) | set(lo_ids[:n_lo].tolist())
+    assert {i for i in range(V) if np.isfinite(lp[i])} == members
+    for i in hi_ids[:n_hi]:
+        assert abs(lp[i] - math.log(qa)) < 1e-11
+    for i in lo_ids[:n_lo]:
+        assert abs(lp[i] - math.log(qb)) < 1e-11
+
+
+# --------------------------------------------------------------------------
+# Invariants.
+# --------------------------------------------------------------------------
+
+def _small_peaked(T=6, V=2000, seed=11):
+    z, peaks = workloads.peaked_bf16(T, V, seed=seed)
+    return workloads.bf16_bits(z)
+
+
+@pytest.mark.parametrize("p", [0.5, 0.95, 1.0])
+def test_members_sum_to_one_and_entropy_bounds(oracle, p):
+    bits = _small_peaked()
+    for r in range(bits.shape[0]):
+        lp, ent, k, gap = score_all_ids(oracle, bits[r], 0.7, p)
+        fin = np.isfinite(lp)
+        assert fin.sum() == k[0]
+        assert abs(math.fsum(np.exp(lp[fin])) - 1.0) < 1e-12
+        assert -1e-12 <= ent[0] <= math.log(k[0]) + 1e-12
+
+
+def test_k_monotone_in_top_p(oracle):
+    bits = _small_peaked(T=8)
+    ids = np.zeros(bits.shape[0], np.int32)
+    prev = np.zeros(bits.shape[0], np.int64)
+    for p in np.linspace(0.05, 1.0, 40):
+        _, _, k, _ = oracle.logprob_entropy(bits, ids, 0.7, float(p))
+        assert np.all(k >= prev)
+        prev = k
+    assert np.all(prev == bits.shape[1])
+
+
+def test_shift_and_temperature_invariance(oracle):
+    rng = np.random.default_rng(5)
+    z = (rng.integers(-512, 512, size=(8, 700)) / 64.0).astype(np.float32)  # exact grid
+    ids = rng.integers(0, 700, size=8).astype(np.int32)
+    base = oracle.logprob_entropy(z, ids, 0.7, 0.9)
+    shifted = oracle.logprob_entropy(z + np.float32(3.0), ids, 0.7, 0.9)
+    assert np.array_equal(base[2], shifted[2])
+    fin = np.isfinite(base[0])
+    assert np.array_equal(fin, np.isfinite(shifted[0]))
+    assert np.max(np.abs(base[0][fin] - shifted[0][fin])) < 1e-12
+    assert np.max(np.abs(base[1] - shifted[1])) < 1e-12
+    # z / 0.5 at temperature 1 is exactly z at temperature 0.5.
+    a = oracle.logprob_entropy(z, ids, 0.5, 0.9)
+    b = oracle.logprob_entropy(z * np.float32(2.0), ids, 1.0, 0.9)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_bad_inputs_give_nan(oracle):
+    z = np.zeros((3, 10), np.float32)
+    z[1, 4] = np.inf
+    ids = np.array([2, 3, 10], np.int32)   # row 2: id out of range
+    lp, ent, k, gap = oracle.logprob_entropy(z, ids, 1.0, 0.9)
+    assert np.isfinite(lp[0]) and np.isnan(lp[1]) and np.isnan(lp[2])
+    assert np.isnan(ent[1]) and np.isnan(ent[2])
+
+
+def test_sampler_draws_from_the_nucleus(oracle):
+    bits = _small_peaked(T=64, V=1500, seed=3)
+    u = workloads.uniforms(64, seed=1)
+    ids = oracle.sample_ids(bits, 0.7, 0.95, u)
+    lp, ent, k, gap = oracle.logprob_entropy(bits, ids, 0.7, 0.95)
+    assert np.all(np.isfinite(lp))
+    # u -> 0 picks the top-ranked token (the largest logit, lowest id on ties).
+    first = oracle.sample_ids(bits, 0.7, 0.95, np.zeros(64))
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(first, np.argmax(vals, axis=1).astype(np.int32))
+
+
+# --------------------------------------------------------------------------
+# GRPO / DAPO loss: hand-worked values.
+# --------------------------------------------------------------------------
+
+def test_advantages_hand_and_library(oracle):
+    R = np.array([1, 0, 0, 1, 1, 1, 1, 1, 0.5, 0.0, 2.0, 1.5], np.float32)
+    off = np.arange(13, dtype=np.int32)   # one token per sequence
+    z = np.zeros(12, np.float32)
+    _, _, adv, _ = oracle.grpo_loss(z, z, z, z, None, R, off, 4)
+    sigma = math.sqrt(1.0 / 3.0)          # [1,0,0,1]: mean 0.5, sum sq 1, /(G-1)=1/3
+    assert abs(adv[0] - 0.5 / (sigma + 1e-6)) < 1e-12
+    assert abs(adv[1] + 0.5 / (sigma + 1e-6)) < 1e-12
+    assert abs(adv[0] - 0.866024) < 1e-6
+    assert np.all(adv[4:8] == 0.0)        # degenerate group: A = 0
+    for g in range(3):
+        r = R[4 * g:4 * g + 4].astype(np.float64)
+        ref = (r - r.mean()) / (np.std(r, ddof=1) + 1e-6)
+        assert np.max(np.abs(adv[4 * g:4 * g + 4] - ref)) < 1e-12
+
+
+def test_clipped_ratio_tis_k3_hand_values(oracle):
+    # Group [1,0,0,1]; four one-token sequences.  A = +a, -a, -a, +a.
+    a = 0.5 / (math.sqrt(1.0 / 3.0) + 1e-6)
+    ln15 = f32(math.log(1.5))
+    r15 = math.exp(ln15)                          # the ratio the float inputs give
+    ln07 = f32(math.log(0.7))
+    new = np.array([ln15, ln15, ln07, 0.0], np.float32)
+    old = np.zeros(4, np.float32)
+    ro = np.array([0.0, 0.0, 0.0, f32(-math.log(3.0))], np.float32)   # old - rollout = ln 3
+    ref = np.array([ln15, ln15 + f32(0.1), ln07, 0.0], np.float32)
+    R = np.array([1, 0, 0, 1], np.float32)
+    off = np.arange(5, dtype=np.int32)
+    loss, grad, adv, st = oracle.grpo_loss(new, old, ro, ref, None, R, off, 4,
+                                           0.2, 0.28, 2.0, 0.01)
+    # token 0: r = 1.5 > 1.28, A > 0 -> clipped term active: pg = -1.28 a, grad_pg = 0.
+    pg0 = -(1.0 + f32(0.28)) * a
+    # token 1: r = 1.5, A < 0 -> unclipped -r A is larger: pg = r a.
+    pg1 = r15 * a
+    # token 2: r = 0.7 < 0.8, A < 0 -> clipped at 1 - 0.2: pg = 0.8 a.
+    pg2 = (1.0 - f32(0.2)) * a
+    # token 3: r = 1, A > 0 -> pg = -a; TIS weight exp(ln 3) = 3 capped to 2.
+    pg3 = -a
+    d1 = float(ref[1]) - float(new[1])                     # delta = ref - new (in double)
+    k3_1 = math.exp(d1) - d1 - 1.0
+    assert abs(k3_1 - 0.0051709) < 1e-6
+    beta = f32(0.01)                                       # kl_coef as the float received
+    ell = [pg0, pg1 + beta * k3_1, pg2, 2.0 * pg3]
+    assert abs(pg0 + 1.108511) < 1e-5 and abs(pg1 - 1.299036) < 1e-5
+    assert abs(pg2 - 0.692819) < 1e-5
+    assert abs(loss - math.fsum(ell) / 4.0) < 1e-12
+    # dL/dnew: token0 clipped -> 0; token1 -r A = r a; token2 clipped -> 0;
+    # token3 unclipped: w (-r A) = 2 (-a).
+    g = [0.0, r15 * a + beta * (1.0 - math.exp(d1)), 0.0, 2.0 * (-a)]
+    assert np.max(np.abs(grad - np.array(g) / 4.0)) < 1e-12
+    assert st["clip_high_frac"] == 0.25 and st["clip_low_frac"] == 0.25
+    assert st["tis_capped_frac"] == 0.25 and abs(st["tis_mean"] - 1.25) < 1e-12
+    assert st["tokens"] == 4.0
+
+
+def test_k3_and_degenerate_group(oracle):
+    new = np.array([0.0, -0.5, -1.0], np.float32)
+    ref = new.copy()
+    R = np.ones(3, np.float32)
+    off = np.array([0, 1, 2, 3], np.int32)
+    loss, grad, adv, st = oracle.grpo_loss(new, new, new, ref, None, R, off, 3)
+    assert loss == 0.0 and np.all(adv == 0.0) and np.all(grad == 0.0)
+
+
+def test_mask_and_empty(oracle):
+    new = np.array([0.1, 0.2, 0.3, 0.4], np.float32)
+    R = np.array([1, 0], np.float32)
+    off = np.array([0, 2, 4], np.int32)
+    m0 = np.zeros(4, np.uint8)
+    loss, grad, _, st = oracle.grpo_loss(new, new, new, new, m0, R, off, 2)
+    assert loss == 0.0 and np.all(grad == 0.0) and st["tokens"] == 0.0
+    m = np.array([1, 0, 0, 1], np.uint8)
+    full, _, _, _ = oracle.grpo_loss(new, new, new, new, None, R, off, 2)
+    part, g, _, _ = oracle.grpo_loss(new, new, new, new, m, R, off, 2)
+    # r = 1, w = 1, k3 = 0 everywhere: l = -A; A = +a for seq 0, -a for seq 1.
+    a = 0.5 / (math.sqrt(0.5) + 1e-6)
+    assert abs(part - (-a + a) / 2) < 1e-12
+    assert g[1] == 0.0 and g[2] == 0.0
+
+
+def test_seq_mean_aggregation_hand(oracle):
+    # Two groups of one sequence each (G = 1 -> A = 0), lengths 1 and 3; only KL.
+    new = np.zeros(4, np.float32)
+    ref = np.array([0.1, 0.0, 0.2, -0.3], np.float32)
+    off = np.array([0, 1, 4], np.int32)
+    R = np.zeros(2, np.float32)
+    k3 = [math.exp(float(d)) - float(d) - 1.0 for d in ref.astype(np.float64)]
+    loss, _, _, _ = oracle.grpo_loss(new, new, new, ref, None, R, off, 1, kl_coef=0.5, agg=1)
+    expect = 0.5 * (k3[0] + (k3[1] + k3[2] + k3[3]) / 3.0) / 2.0
+    assert abs(loss - expect) < 1e-12
+    loss0, _, _, _ = oracle.grpo_loss(new, new, new, ref, None, R, off, 1, kl_coef=0.5, agg=0)
+    assert abs(loss0 - 0.5 * math.fsum(k3) / 4.0) < 1e-12
+
+
+@pytest.mark.parametrize("agg", [0, 1])
+def test_grad_matches_finite_differences(oracle, agg):
+    rng = np.random.default_rng(7)
+    off = np.array([0, 5, 9, 16, 20], np.int32)
+    n = 20
+    grid = 1.0 / 256.0
+    new = (rng.integers(-200, 0, n) * grid).astype(np.float32)
+    old = new + (rng.integers(-30, 30, n) * grid).astype(np.float32)
+    ro = old + (rng.integers(-60, 60, n) * grid).astype(np.float32)
+    ref = new + (rng.integers(-20, 20, n) * grid).astype(np.float32)
+    R = np.array([1.0, 0.0, 0.3, 0.9], np.float32)
+    mask = (rng.random(n) < 0.8).astype(np.uint8)
+    kw = dict(eps_low=0.2, eps_high=0.28, tis_cap=2.0, kl_coef=0.05, agg=agg)
+    _, grad, _, _ = oracle.grpo_loss(new, old, ro, ref, mask, R, off, 2, **kw)
+    h = np.float32(2.0 ** -12)
+    for t in range(n):
+        up, dn = new.copy(), new.copy()
+        up[t] += h
+        dn[t] -= h
+        lu = oracle.grpo_loss(up, old, ro, ref, mask, R, off, 2, **kw)[0]
+        ld = oracle.grpo_loss(dn, old, ro, ref, mask, R, off, 2, **kw)[0]
+        fd = (lu - ld) / (2 * float(h))
+        assert abs(fd - grad[t]) < 2e-5, (t, fd, grad[t])
+
+
+# --------------------------------------------------------------------------
+# LM-head rows.
+# --------------------------------------------------------------------------
+
+def test_lmhead_rows_against_library_matmul(oracle):
+    hidden, w, ids = workloads.lmhead_inputs(T=6, H=64, V=300, seed=4)
+    hb, wb = workloads.bf16_bits(hidden), workloads.bf16_bits(w)
+    rows = np.array([0, 2, 5], np.int64)
+    lp, ent, k = oracle.lmhead_rows(hb, wb, rows, ids.numpy(), 0.7, 1.0)
+    logits = (hidden.double() @ w.double().T) / f32(0.7)
+    ref_lp = torch.log_softmax(logits, 1)
+    ref_ent = torch.special.entr(torch.softmax(logits, 1)).sum(1)
+    for j, r in enumerate(rows):
+        assert abs(lp[j] - ref_lp[r, ids[r].long()].item()) < 1e-10
+        assert abs(ent[j] - ref_ent[r].item()) < 1e-10
+    assert np.all(k == 300)
