@@ -1,0 +1,350 @@
+"""Benchmark: tokens/s of top-p logprob + entropy at V=151936 bf16, and the
+fraction of the HBM roofline the kernel reaches.
+
+One step = one pass of the hot path (rlk_logprob_entropy: pass 1 online
+max/log-sum-exp/entropy, nucleus select, renormalisation) over one batch of
+synthetic Qwen3-8B-shaped logits: T=4096 rows, V=151936 bf16,
+temperature 0.7, top_p 0.95 (inputs 1.24 GB, larger than L2, so no flush is
+needed between steps).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+Rows are independent, so N > 1 (one process per GPU via torchrun) runs N
+replicas with no collective on the data path: weak scaling.  ``--impl
+reference`` times the fp64 CPU oracle, as it stands, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+T_ROWS = 4096
+VOCAB = 151936
+TEMPERATURE = 0.7
+TOP_P = 0.95
+ROW_BYTES = VOCAB * 2
+BYTES_PER_TOKEN = ROW_BYTES + 4 + 12     # logits row + id + (logprob, entropy, k*) outputs
+METRIC = "tokens/s for top-p logprob+entropy at V=151936 bf16; % of HBM roofline"
+KERNEL_SRC = os.path.join(ROOT, "entropy_logits_bf16_gb300", "csrc", "logprob_entropy.cu")
+PROFILE = os.path.join(ROOT, "profiles", "lpe_kernel_qwen_T4096.txt")
+WORKLOAD = (f"Qwen3-8B-shaped logits T={T_ROWS} V={VOCAB} bf16 = 3 N(0,1) + one peak U(5,15) "
+            f"per row; temperature {TEMPERATURE}, top_p {TOP_P}")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def kernel_sha():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    try:
+        kv = {}
+        with open(PROFILE) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != kernel_sha():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_workload(device, seed):
+    import workloads
+    z, peaks = workloads.peaked_bf16(T_ROWS, VOCAB, seed=seed, device=device)
+    # The selected token of each row is its peaked token: the kernel's work
+    # does not depend on which id is selected (one extra element load).
+    return z, peaks.to(torch.int32)
+
+
+def cpu_baseline(z, ids, rows=1024):
+    """The oracle, as it stands, on evenly spaced rows of the same workload."""
+    import oracle
+    import workloads
+    sel = np.linspace(0, T_ROWS - 1, rows).astype(np.int64)
+    hz = np.ascontiguousarray(workloads.bf16_bits(z)[sel])
+    hid = ids.cpu().numpy()[sel]
+    threads = oracle.default_threads()
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.logprob_entropy(hz, hid, TEMPERATURE, TOP_P, threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": rows / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} evenly spaced rows of the T={T_ROWS} workload, fp64 oracle, "
+                      f"{threads} threads, {dt:.2f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the fp64 CPU oracle timed on the host cores."""
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import workloads
+    oracle.build()
+    rows_per_step = 64
+    z, peaks = workloads.peaked_bf16(rows_per_step * 4, VOCAB, seed=1, device="cpu")
+    hz = workloads.bf16_bits(z)
+    hid = peaks.numpy().astype(np.int32)
+    threads = oracle.default_threads()
+    for i in range(args.warmup):
+        s = (i % 4) * rows_per_step
+        oracle.logprob_entropy(hz[s:s + rows_per_step], hid[s:s + rows_per_step], TEMPERATURE,
+                               TOP_P, threads=threads)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s = (i % 4) * rows_per_step
+        oracle.logprob_entropy(hz[s:s + rows_per_step], hid[s:s + rows_per_step], TEMPERATURE,
+                               TOP_P, threads=threads)
+    dt = time.perf_counter() - t0
+    value = rows_per_step * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows_per_step": rows_per_step, "V": VOCAB},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_per_step} rows per step of the same workload"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import entropy_logits_bf16_gb300 as rlk
+    rlk.build()
+    rlk.load()
+
+    z, ids = make_workload(dev, seed=1 + rank)
+    lp = torch.empty(T_ROWS, device=dev)
+    ent = torch.empty(T_ROWS, device=dev)
+    ks = torch.empty(T_ROWS, device=dev, dtype=torch.int32)
+    lib = rlk.load()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        code = lib.rlk_logprob_entropy(
+            rlk._ptr(z), 0, T_ROWS, VOCAB, VOCAB, rlk._ptr(ids), TEMPERATURE, TOP_P,
+            rlk._ptr(lp), rlk._ptr(ent), rlk._ptr(ks), None, None, 0,
+            rlk._stream(dev))
+        if code != 0:
+            raise RuntimeError(f"rlk_logprob_entropy returned {code}")
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    barrier()
+    clocks = ClockSampler(local if ws > 1 else 0)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    t_stop.record(stream)
+    barrier()
+    elapsed_ms = t_start.elapsed_time(t_stop)
+    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
+    clk = clocks.stop()
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    # end to end through the public API: pinned host logits -> device -> kernel -> host
+    host_z = torch.empty(z.shape, dtype=z.dtype, pin_memory=True)
+    host_z.copy_(z)
+    host_ids = torch.empty(ids.shape, dtype=ids.dtype, pin_memory=True)
+    host_ids.copy_(ids)
+    out_h = torch.empty(3, T_ROWS, dtype=torch.float32, pin_memory=True)
+    dz = torch.empty_like(z)
+    dids = torch.empty_like(ids)
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        dz.copy_(host_z, non_blocking=True)
+        dids.copy_(host_ids, non_blocking=True)
+        a, b, c = rlk.logprob_entropy(dz, dids, TEMPERATURE, TOP_P, out_logprob=lp,
+                                      out_entropy=ent, return_nucleus_size=True)
+        out_h[0].copy_(a, non_blocking=True)
+        out_h[1].copy_(b, non_blocking=True)
+        out_h[2].copy_(c.view(torch.float32), non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    peaks, peak_kind = measured_peaks()
+    ms_per_step = elapsed_ms / args.steps
+    value = T_ROWS * args.steps * ws / (elapsed_ms / 1e3)
+    launch_ms = sum(per_launch_ms) / len(per_launch_ms)
+    alg_bytes = BYTES_PER_TOKEN * T_ROWS
+    achieved = alg_bytes / (launch_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_ROWS, "V": VOCAB, "temperature": TEMPERATURE,
+                   "top_p": TOP_P, "global_batch": T_ROWS * ws,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "inputs (1.24 GB per GPU) larger than L2; no flush between steps"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic(), "peak_source": peak_kind,
+                     "kernel": "lpe_kernel<RowBf16, top_p<1>",
+                     "bytes_per_token": BYTES_PER_TOKEN, "tokens_per_launch": T_ROWS,
+                     "launch_ms": launch_ms},
+        "e2e": {"value": T_ROWS * ws / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(z.numel() * 2 + ids.numel() * 4),
+                "d2h_bytes_per_step": int(3 * T_ROWS * 4)},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(z, ids)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+"""Python binding of librlk (argument marshalling only).
+
+Every step of the computation runs in the CUDA kernels of ``librlk.so``; this
+module only checks tensor placement, allocates outputs with PyTorch and passes
+raw pointers plus the current CUDA stream through the C ABI declared in
+``include/rlk.h``.  There is no CPU fallback: if the library is missing or the
+tensors are not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "librlk.so")
+
+RLK_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace",
+                4: "CUDA error", 5: "timeout", 6: "bad input"}
+STATUS_BAD_TOKEN_ID = 0x1
+STATUS_NONFINITE = 0x2
+OP_LOGPROB_ENTROPY, OP_GRPO_LOSS, OP_LMHEAD = 0, 1, 2
+AGG_TOKEN_MEAN, AGG_SEQ_MEAN_TOKEN_MEAN = 0, 1
+NSTATS = 8
+STAT_NAMES = ("loss", "tokens", "clip_low_frac", "clip_high_frac", "tis_mean",
+              "tis_capped_frac", "k3_mean", "pg_mean")
+EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logprob_entropy",
+           "rlk_grpo_loss", "rlk_lmhead_logprob")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class RlkError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)} ({code})")
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def load(path: str | None = None):
+    """Load librlk.so (built in-tree by ``build()``) and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it first (entropy_logits_bf16_gb300.build())")
+        lib = ctypes.CDLL(p)
+        i64, i32, f32, vp, sz = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                 ctypes.c_void_p, ctypes.c_size_t)
+        lib.rlk_version.restype = ctypes.c_int
+        lib.rlk_status_string.argtypes = [ctypes.c_int]
+        lib.rlk_status_string.restype = ctypes.c_char_p
+        lib.rlk_workspace_size.argtypes = [ctypes.c_int, i64, i64, i64]
+        lib.rlk_workspace_size.restype = sz
+        lib.rlk_logprob_entropy.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, f32, vp,
+                                            vp, vp, vp, vp, sz, vp]
+        lib.rlk_logprob_entropy.restype = ctypes.c_int
+        lib.rlk_grpo_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, f32, f32, f32,
+                                      f32, ctypes.c_int, vp, vp, vp, vp, sz, vp]
+        lib.rlk_grpo_loss.restype = ctypes.c_int
+        lib.rlk_lmhead_logprob.argtypes = [vp, vp, i64, i64, i64, vp, f32, f32, vp, vp, vp, vp,
+                                           sz, vp]
+        lib.rlk_lmhead_logprob.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("librlk operates on CUDA tensors only")
+
+
+def _check(fn, code):
+    if code != RLK_OK:
+        raise RlkError(fn, code)
+
+
+def workspace_size(op: int, T: int, V: int, H: int = 0) -> int:
+    return int(load().rlk_workspace_size(op, T, V, H))
+
+
+def logprob_entropy(logits: torch.Tensor, token_ids: torch.Tensor, temperature: float,
+                    top_p: float, *, out_logprob=None, out_entropy=None,
+                    return_nucleus_size: bool = False, status_word: torch.Tensor | None = None):
+    """Top-p log-probability of the selected token and entropy of the retained set.
+
+    logits: CUDA [T, V] bf16 or fp32 (rows may be strided, unit stride along V);
+    token_ids: CUDA int32 [T].  Returns (logprob, entropy) fp32 [T], plus the
+    nucleus sizes int32 [T] when ``return_nucleus_size``.  ``status_word`` (CUDA
+    uint32/int32 [1]) receives the STATUS_* bits of bad rows.
+    """
+    lib = load()
+    _need_cuda(logits, token_ids)
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be 2-D with unit stride along the vocabulary")
+    if logits.dtype == torch.bfloat16:
+        dt = 0
+    elif logits.dtype == torch.float32:
+        dt = 1
+    else:
+        raise ValueError("logits must be bf16 or fp32")
+    if token_ids.dtype != torch.int32 or not token_ids.is_contiguous():
+        raise ValueError("token_ids must be contiguous int32")
+    T, V = logits.shape
+    ld = logits.stride(0) if T > 1 else V
+    dev = logits.device
+    lp = out_logprob if out_logprob is not None else torch.empty(T, device=dev, dtype=torch.float32)
+    ent = out_entropy if out_entropy is not None else torch.empty(T, device=dev, dtype=torch.float32)
+    ks = torch.empty(T, device=dev, dtype=torch.int32) if return_nucleus_size else None
+    code = lib.rlk_logprob_entropy(_ptr(logits), dt, T, V, ld, _ptr(token_ids), float(temperature),
+                                   float(top_p), _ptr(lp), _ptr(ent), _ptr(ks), _ptr(status_word),
+                                   None, 0, _stream(dev))
+    _check("rlk_logprob_entropy", code)
+    return (lp, ent, ks) if return_nucleus_size else (lp, ent)
+
+
+def grpo_loss(logp_new, logp_old, logp_rollout, logp_ref, rewards, seq_offsets, group_size, *,
+              loss_mask=None, eps_low=0.2, eps_high=0.28, tis_cap=2.0, kl_coef=0.01,
+              agg=AGG_TOKEN_MEAN, want_grad=True, want_stats=True, workspace=None):
+    """GRPO/DAPO loss with TIS and k3 KL.  Returns (loss[1], grad[T] or None,
+    stats[NSTATS] or None), all CUDA fp32 tensors."""
+    lib = load()
+    _need_cuda(logp_new, logp_old, logp_rollout, logp_ref, rewards, seq_offsets, loss_mask)
+    for t in (logp_new, logp_old, logp_rollout, logp_ref, rewards):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("log-probs and rewards must be contiguous fp32")
+    if seq_offsets.dtype != torch.int32:
+        raise ValueError("seq_offsets must be int32")
+    if loss_mask is not None and loss_mask.dtype != torch.uint8:
+        raise ValueError("loss_mask must be uint8")
+    n_seq = seq_offsets.numel() - 1
+    n_tok = logp_new.numel()
+    dev = logp_new.device
+    need = int(lib.rlk_workspace_size(OP_GRPO_LOSS, n_tok, n_seq, 0))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+    loss = torch.empty(1, device=dev, dtype=torch.float32)
+    grad = torch.empty(n_tok, device=dev, dtype=torch.float32) if want_grad else None
+    stats = torch.empty(NSTATS, device=dev, dtype=torch.float32) if want_stats else None
+    code = lib.rlk_grpo_loss(_ptr(logp_new), _ptr(logp_old), _ptr(logp_rollout), _ptr(logp_ref),
+                             _ptr(loss_mask), _ptr(rewards), _ptr(seq_offsets), n_seq,
+                             int(group_size), n_tok, float(eps_low), float(eps_high),
+                             float(tis_cap), float(kl_coef), int(agg), _ptr(loss), _ptr(grad),
+                             _ptr(stats), _ptr(workspace), workspace.numel(), _stream(dev))
+    _check("rlk_grpo_loss", code)
+    return loss, grad, stats
+
+
+def lmhead_logprob(hidden, w_vocab, token_ids, temperature, top_p=1.0, *, status_word=None,
+                   workspace=None):
+    """Fused LM-head top-p=1 log-probability and entropy (logits never stored)."""
+    lib = load()
+    _need_cuda(hidden, w_vocab, token_ids)
+    if hidden.dtype != torch.bfloat16 or w_vocab.dtype != torch.bfloat16:
+        raise ValueError("hidden and w_vocab must be bf16")
+    if not (hidden.is_contiguous() and w_vocab.is_contiguous()):
+        raise ValueError("hidden and w_vocab must be contiguous")
+    T, H = hidden.shape
+    V, H2 = w_vocab.shape
+    if H != H2:
+        raise ValueError("hidden and w_vocab disagree on H")
+    dev = hidden.device
+    need = int(lib.rlk_workspace_size(OP_LMHEAD, T, V, H))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    lp = torch.empty(T, device=dev, dtype=torch.float32)
+    ent = torch.empty(T, device=dev, dtype=torch.float32)
+    code = lib.rlk_lmhead_logprob(_ptr(hidden), _ptr(w_vocab), T, H, V, _ptr(token_ids),
+                                  float(temperature), float(top_p), _ptr(lp), _ptr(ent),
+                                  _ptr(status_word), _ptr(workspace),
+                                  0 if workspace is None else workspace.numel(), _stream(dev))
+    _check("rlk_lmhead_logprob", code)
+    return lp, ent

@@ -1,0 +1,100 @@
+// Device helpers shared by the librlk kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rlk {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Hardware base-2 exponential (PTX ex2.approx.ftz.f32; relative error ~2^-22).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// bf16 halves of a 32-bit word as fp32 (exact widening).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_val(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// Order-preserving 16-bit key of a bf16 bit pattern: key(a) < key(b) iff a < b
+// as numbers; -0 gets the key of +0, so equal values always tie.
+__device__ __forceinline__ uint32_t okey16(uint32_t b) {
+  b &= 0xFFFFu;
+  if (b == 0x8000u) b = 0u;
+  return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+}
+__device__ __forceinline__ uint32_t okey16_inverse(uint32_t k) {
+  return (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+}
+// Same for fp32 bit patterns (32-bit key).
+__device__ __forceinline__ uint32_t okey32(uint32_t b) {
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t okey32_inverse(uint32_t k) {
+  return (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+}
+
+// ---- double-float (hi + lo) arithmetic, error-free transforms in fp32 ----
+struct DF {
+  float hi, lo;
+};
+
+// Knuth's TwoSum: s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  float bp = __fsub_rn(s, a);
+  float ap = __fsub_rn(s, bp);
+  e = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
+}
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  float hi = __fadd_rn(s, e);
+  return DF{hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+
+__device__ __forceinline__ DF df_add_f(DF a, float b) {
+  float s, e;
+  two_sum(a.hi, b, s, e);
+  e = __fadd_rn(e, a.lo);
+  float hi = __fadd_rn(s, e);
+  return DF{hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+
+// a >= b for normalised double-floats.
+__device__ __forceinline__ bool df_ge(DF a, DF b) {
+  return (a.hi > b.hi) || (a.hi == b.hi && a.lo >= b.lo);
+}
+
+// (a - b) rounded to fp32 (a, b normalised; used for small differences).
+__device__ __forceinline__ float df_sub_to_f(DF a, DF b) {
+  float s, e;
+  two_sum(a.hi, -b.hi, s, e);
+  return __fadd_rn(s, __fadd_rn(e, __fsub_rn(a.lo, b.lo)));
+}
+
+// p * Z as a double-float (FMA-based exact product of the high parts).
+__device__ __forceinline__ DF df_mul_f(DF z, float p) {
+  float hi = __fmul_rn(p, z.hi);
+  float lo = __fmaf_rn(p, z.hi, -hi);
+  lo = __fmaf_rn(p, z.lo, lo);
+  float s = __fadd_rn(hi, lo);
+  return DF{s, __fsub_rn(lo, __fsub_rn(s, hi))};
+}
+
+__device__ __forceinline__ float shfl_down(float v, int d) {
+  return __shfl_down_sync(0xFFFFFFFFu, v, d);
+}
+__device__ __forceinline__ float shfl_up(float v, int d) {
+  return __shfl_up_sync(0xFFFFFFFFu, v, d);
+}
+
+}  // namespace rlk

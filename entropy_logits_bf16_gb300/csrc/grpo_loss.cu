@@ -1,0 +1,190 @@
+// rlk_grpo_loss kernels: GRPO/DAPO clipped-ratio loss with truncated
+// importance sampling (TIS) and the k3 KL estimate.
+//
+// Method: GRPO with standard-deviation-normalised group advantages and KL
+// coefficient 0.01 (RL-Kernel "ROCm sparse performance" notes); TIS clips large
+// importance ratios (LumenRL README, section "Rollout Correction"); the loss
+// backward seed is normalised before model derivatives (RL-Kernel "Qwen3-8B
+// VIME train-rollout consistency", section "Canonical topology strategy"), so
+// the gradient written here already carries the aggregation weight.
+//
+// Launches (all on the caller's stream, no atomics on floats, no inter-CTA
+// waits, every sum in a fixed order):
+//  1. seq kernel, one CTA per sequence: the sequence's advantage from its
+//     group's rewards, then per-token terms; per-sequence partial sums go to
+//     the workspace and the unscaled per-token gradient to the output.
+//  2. finalize kernel, one CTA: fixed-order sums over sequences -> loss,
+//     statistics and the gradient weights.
+//  3. scale kernel, one CTA per sequence (only when a gradient is requested).
+
+#include <math.h>
+
+#include "internal.h"
+#include "rlk.h"
+
+namespace rlk {
+namespace {
+
+constexpr int LT = 256;
+constexpr int LWARP = LT / 32;
+constexpr int NP = kLossPartials;  // partial sums per sequence, see below
+// Partial slots: 0 sum m*l, 1 sum m, 2 clip-low count, 3 clip-high count,
+// 4 sum m*w, 5 TIS-capped count, 6 sum m*k3, 7 sum m*pg.
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
+  __shared__ float s_adv;
+  __shared__ float s_red[LWARP][NP];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.group_size;
+  const float lo_b = 1.0f - a.eps_low, hi_b = 1.0f + a.eps_high;
+  for (int s = blockIdx.x; s < a.n_seq; s += gridDim.x) {
+    if (tid == 0) {
+      // Group statistics in a fixed order, in double.
+      const int s0 = (s / G) * G;
+      double sum = 0.0;
+      for (int j = 0; j < G; ++j) sum += (double)a.rewards[s0 + j];
+      const double mu = sum / G;
+      double ss = 0.0;
+      for (int j = 0; j < G; ++j) {
+        const double d = (double)a.rewards[s0 + j] - mu;
+        ss += d * d;
+      }
+      const double sigma = G > 1 ? sqrt(ss / (G - 1)) : 0.0;
+      s_adv = (float)(((double)a.rewards[s] - mu) / (sigma + 1e-6));
+    }
+    __syncthreads();
+    const float A = s_adv;
+    const int64_t t0 = a.seq_offsets[s], t1 = a.seq_offsets[s + 1];
+    float acc[NP];
+#pragma unroll
+    for (int k = 0; k < NP; ++k) acc[k] = 0.f;
+    for (int64_t t = t0 + tid; t < t1; t += LT) {
+      const float nw = a.logp_new[t], od = a.logp_old[t];
+      const float ro = a.logp_rollout[t], rf = a.logp_ref[t];
+      const float m = a.mask ? (a.mask[t] ? 1.f : 0.f) : 1.f;
+      const float r = expf(nw - od);
+      const float rc = fminf(fmaxf(r, lo_b), hi_b);
+      const float un = r * A, cl = rc * A;
+      const float pg = -fminf(un, cl);
+      const float gpg = (un <= cl) ? -un : 0.f;
+      const float raw = expf(od - ro);
+      const float w = fminf(raw, a.tis_cap);
+      const float dl = rf - nw;
+      const float em1 = expm1f(dl);
+      const float k3 = em1 - dl;
+      const float ell = w * pg + a.kl_coef * k3;
+      acc[0] += m * ell;
+      acc[1] += m;
+      acc[2] += (A < 0.f && r < lo_b) ? m : 0.f;
+      acc[3] += (A > 0.f && r > hi_b) ? m : 0.f;
+      acc[4] += m * w;
+      acc[5] += (raw > a.tis_cap) ? m : 0.f;
+      acc[6] += m * k3;
+      acc[7] += m * pg;
+      if (a.out_grad) a.out_grad[t] = m * (w * gpg - a.kl_coef * em1);
+    }
+#pragma unroll
+    for (int k = 0; k < NP; ++k) acc[k] = warp_sum(acc[k]);
+    if (lane == 0)
+      for (int k = 0; k < NP; ++k) s_red[warp][k] = acc[k];
+    __syncthreads();
+    if (tid < NP) {
+      float v = 0.f;
+      for (int w2 = 0; w2 < LWARP; ++w2) v += s_red[w2][tid];
+      a.workspace[(int64_t)s * NP + tid] = v;
+    }
+    __syncthreads();
+  }
+}
+
+// One CTA: fixed-order sums over the sequences' partials.
+__global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
+  __shared__ double s_red[LWARP][NP + 2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  double acc[NP + 2];  // NP partial sums, sum of per-sequence means, live sequences
+#pragma unroll
+  for (int k = 0; k < NP + 2; ++k) acc[k] = 0.0;
+  for (int s = tid; s < a.n_seq; s += LT) {
+    const float* p = a.workspace + (int64_t)s * NP;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) acc[k] += (double)p[k];
+    if (p[1] > 0.f) {
+      acc[NP] += (double)p[0] / (double)p[1];
+      acc[NP + 1] += 1.0;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NP + 2; ++k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[k] += __shfl_down_sync(0xFFFFFFFFu, acc[k], o);
+  }
+  if (lane == 0)
+    for (int k = 0; k < NP + 2; ++k) s_red[warp][k] = acc[k];
+  __syncthreads();
+  if (tid == 0) {
+    double t[NP + 2];
+    for (int k = 0; k < NP + 2; ++k) {
+      t[k] = 0.0;
+      for (int w2 = 0; w2 < LWARP; ++w2) t[k] += s_red[w2][k];
+    }
+    const double M = t[1];
+    double L;
+    if (a.agg == RLK_AGG_TOKEN_MEAN) L = M > 0.0 ? t[0] / M : 0.0;
+    else L = t[NP + 1] > 0.0 ? t[NP] / t[NP + 1] : 0.0;
+    *a.out_loss = (float)L;
+    if (a.out_stats) {
+      const double d = M > 0.0 ? M : 1.0;
+      a.out_stats[RLK_STAT_LOSS] = (float)L;
+      a.out_stats[RLK_STAT_TOKENS] = (float)M;
+      a.out_stats[RLK_STAT_CLIP_LOW] = (float)(t[2] / d);
+      a.out_stats[RLK_STAT_CLIP_HIGH] = (float)(t[3] / d);
+      a.out_stats[RLK_STAT_TIS_MEAN] = (float)(t[4] / d);
+      a.out_stats[RLK_STAT_TIS_CAPPED] = (float)(t[5] / d);
+      a.out_stats[RLK_STAT_K3_MEAN] = (float)(t[6] / d);
+      a.out_stats[RLK_STAT_PG_MEAN] = (float)(t[7] / d);
+    }
+    float* sc = a.workspace + (int64_t)a.n_seq * NP;
+    sc[0] = M > 0.0 ? (float)(1.0 / M) : 0.f;   // token-mean weight
+    sc[1] = (float)t[NP + 1];                     // sequences with tokens
+  }
+}
+
+// Multiply each token's unscaled gradient by its weight in the loss.
+__global__ void __launch_bounds__(LT) loss_scale_kernel(LossArgs a) {
+  const float* sc = a.workspace + (int64_t)a.n_seq * NP;
+  for (int s = blockIdx.x; s < a.n_seq; s += gridDim.x) {
+    float wgt;
+    if (a.agg == RLK_AGG_TOKEN_MEAN) {
+      wgt = sc[0];
+    } else {
+      const float ms = a.workspace[(int64_t)s * NP + 1];
+      wgt = ms > 0.f ? (float)(1.0 / ((double)ms * (double)sc[1])) : 0.f;
+    }
+    const int64_t t0 = a.seq_offsets[s], t1 = a.seq_offsets[s + 1];
+    for (int64_t t = t0 + threadIdx.x; t < t1; t += LT) a.out_grad[t] *= wgt;
+  }
+}
+
+}  // namespace
+
+size_t loss_workspace_bytes(int64_t n_seq) {
+  const size_t floats = (size_t)n_seq * NP + 4;
+  return (floats * sizeof(float) + 255) & ~(size_t)255;
+}
+
+cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t stream) {
+  const int cap = 8 * sm_count();
+  const int grid = a.n_seq < cap ? (a.n_seq > 0 ? a.n_seq : 1) : cap;
+  if (a.n_seq > 0) loss_seq_kernel<<<grid, LT, 0, stream>>>(a);
+  loss_finalize_kernel<<<1, LT, 0, stream>>>(a);
+  if (a.out_grad && a.n_seq > 0) loss_scale_kernel<<<grid, LT, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace rlk

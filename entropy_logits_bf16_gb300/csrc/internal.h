@@ -1,0 +1,60 @@
+// Internal launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rlk {
+
+struct LpeArgs {
+  const void* logits;
+  int dtype;  // 0 bf16, 1 fp32
+  int64_t T, V, ld;
+  const int32_t* ids;
+  float temperature, top_p;
+  float* out_logprob;
+  float* out_entropy;
+  int32_t* out_k;
+  uint32_t* status;
+};
+
+struct LossArgs {
+  const float *logp_new, *logp_old, *logp_rollout, *logp_ref;
+  const uint8_t* mask;
+  const float* rewards;
+  const int32_t* seq_offsets;
+  int32_t n_seq, group_size;
+  int64_t n_tok;
+  float eps_low, eps_high, tis_cap, kl_coef;
+  int agg;
+  float* out_loss;
+  float* out_grad;
+  float* out_stats;
+  float* workspace;  // per-sequence partial sums + a few scalars
+};
+
+struct LmheadArgs {
+  const void* hidden;
+  const void* w_vocab;
+  int64_t T, H, V;
+  const int32_t* ids;
+  float temperature;
+  float* out_logprob;
+  float* out_entropy;
+  uint32_t* status;
+  void* workspace;
+};
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream);
+
+constexpr int kLossPartials = 8;  // floats per sequence in the loss workspace
+size_t loss_workspace_bytes(int64_t n_seq);
+cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t stream);
+
+size_t lmhead_workspace_bytes(int64_t T, int64_t V, int64_t H);
+cudaError_t launch_lmhead(const LmheadArgs& a, cudaStream_t stream);
+
+}  // namespace rlk

@@ -1,0 +1,177 @@
+// C ABI of librlk: argument validation, workspace sizes, status strings and
+// the launches.  Host-checkable errors return before any CUDA call, so the
+// validation paths run without a GPU.
+
+#include <atomic>
+#include <cmath>
+
+#include "internal.h"
+#include "rlk.h"
+
+namespace rlk {
+
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+}  // namespace rlk
+
+namespace {
+
+bool finite_positive(float x) { return std::isfinite(x) && x > 0.0f; }
+
+}  // namespace
+
+extern "C" {
+
+int rlk_version(void) { return 100; }
+
+const char* rlk_status_string(rlk_status status) {
+  switch (status) {
+    case RLK_OK: return "ok";
+    case RLK_ERR_INVALID_ARG: return "invalid argument";
+    case RLK_ERR_UNSUPPORTED: return "unsupported";
+    case RLK_ERR_WORKSPACE: return "workspace missing or too small";
+    case RLK_ERR_CUDA: return "CUDA error";
+    case RLK_ERR_TIMEOUT: return "device wait timed out";
+    case RLK_ERR_BAD_INPUT: return "bad input data";
+  }
+  return "unknown status";
+}
+
+size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H) {
+  if (T < 0 || V < 0 || H < 0) return 0;
+  switch (op) {
+    case RLK_OP_LOGPROB_ENTROPY: return 0;
+    case RLK_OP_GRPO_LOSS: return rlk::loss_workspace_bytes(V);
+    case RLK_OP_LMHEAD: return rlk::lmhead_workspace_bytes(T, V, H);
+  }
+  return 0;
+}
+
+rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                               int64_t ld, const int32_t* token_ids, float temperature,
+                               float top_p, float* out_logprob, float* out_entropy,
+                               int32_t* out_nucleus_size, uint32_t* out_status_word,
+                               void* workspace, size_t workspace_bytes, rlk_stream stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (dtype != RLK_BF16 && dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || ld < V) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
+  if (!(top_p > 0.0f && top_p <= 1.0f)) return RLK_ERR_INVALID_ARG;
+  if (!logits || !token_ids || !out_logprob || !out_entropy) return RLK_ERR_INVALID_ARG;
+  const uintptr_t elem = dtype == RLK_BF16 ? 2u : 4u;
+  if (reinterpret_cast<uintptr_t>(logits) % elem != 0) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  rlk::LpeArgs a;
+  a.logits = logits;
+  a.dtype = dtype == RLK_BF16 ? 0 : 1;
+  a.T = T;
+  a.V = V;
+  a.ld = ld;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.top_p = top_p;
+  a.out_logprob = out_logprob;
+  a.out_entropy = out_entropy;
+  a.out_k = out_nucleus_size;
+  a.status = out_status_word;
+  return rlk::launch_logprob_entropy(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
+                         const float* logp_rollout, const float* logp_ref,
+                         const uint8_t* loss_mask, const float* rewards,
+                         const int32_t* seq_offsets, int32_t n_seq, int32_t group_size,
+                         int64_t n_tok, float eps_low, float eps_high, float tis_cap,
+                         float kl_coef, rlk_agg agg, float* out_loss,
+                         float* out_dloss_dlogp_new, float* out_stats, void* workspace,
+                         size_t workspace_bytes, rlk_stream stream) {
+  if (n_seq < 0 || group_size < 1 || n_seq % group_size != 0 || n_tok < 0)
+    return RLK_ERR_INVALID_ARG;
+  if (!(std::isfinite(eps_low) && eps_low >= 0.0f && std::isfinite(eps_high) && eps_high >= 0.0f))
+    return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(tis_cap) || !(std::isfinite(kl_coef) && kl_coef >= 0.0f))
+    return RLK_ERR_INVALID_ARG;
+  if (agg != RLK_AGG_TOKEN_MEAN && agg != RLK_AGG_SEQ_MEAN_TOKEN_MEAN) return RLK_ERR_INVALID_ARG;
+  if (!seq_offsets || !out_loss) return RLK_ERR_INVALID_ARG;
+  if (n_seq > 0 && (!logp_new || !logp_old || !logp_rollout || !logp_ref || !rewards))
+    return RLK_ERR_INVALID_ARG;
+  const size_t need = rlk::loss_workspace_bytes(n_seq);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+    return RLK_ERR_WORKSPACE;
+  rlk::LossArgs a;
+  a.logp_new = logp_new;
+  a.logp_old = logp_old;
+  a.logp_rollout = logp_rollout;
+  a.logp_ref = logp_ref;
+  a.mask = loss_mask;
+  a.rewards = rewards;
+  a.seq_offsets = seq_offsets;
+  a.n_seq = n_seq;
+  a.group_size = group_size;
+  a.n_tok = n_tok;
+  a.eps_low = eps_low;
+  a.eps_high = eps_high;
+  a.tis_cap = tis_cap;
+  a.kl_coef = kl_coef;
+  a.agg = agg;
+  a.out_loss = out_loss;
+  a.out_grad = out_dloss_dlogp_new;
+  a.out_stats = out_stats;
+  a.workspace = static_cast<float*>(workspace);
+  return rlk::launch_grpo_loss(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_lmhead_logprob(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
+                              int64_t V, const int32_t* token_ids, float temperature,
+                              float top_p, float* out_logprob, float* out_entropy,
+                              uint32_t* out_status_word, void* workspace,
+                              size_t workspace_bytes, rlk_stream stream) {
+  if (T < 0 || H < 64 || H % 64 != 0 || V < 1 || V > (int64_t(1) << 24)) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
+  if (!(top_p > 0.0f && top_p <= 1.0f)) return RLK_ERR_INVALID_ARG;
+  if (!hidden || !w_vocab || !token_ids || !out_logprob || !out_entropy) return RLK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(hidden) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(w_vocab) % 16 != 0)
+    return RLK_ERR_INVALID_ARG;
+  if (top_p != 1.0f) return RLK_ERR_UNSUPPORTED;
+  const size_t need = rlk::lmhead_workspace_bytes(T, V, H);
+  if (need > 0 && (!workspace || workspace_bytes < need ||
+                   reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
+    return RLK_ERR_WORKSPACE;
+  if (T == 0) return RLK_OK;
+  rlk::LmheadArgs a;
+  a.hidden = hidden;
+  a.w_vocab = w_vocab;
+  a.T = T;
+  a.H = H;
+  a.V = V;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.out_logprob = out_logprob;
+  a.out_entropy = out_entropy;
+  a.status = out_status_word;
+  a.workspace = workspace;
+  const cudaError_t e = rlk::launch_lmhead(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return RLK_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,216 @@
+/*
+ * rlk.h -- C ABI of librlk: top-p log-probability / entropy of sampled tokens,
+ * the GRPO/DAPO loss epilogue, and a fused LM-head variant, for one GB300 GPU.
+ *
+ * Conventions shared by every entry point
+ *  - All pointers are DEVICE pointers unless stated otherwise; scalars are
+ *    passed by value.  The caller owns every buffer.  The library never
+ *    allocates, frees or synchronises; all work is enqueued on `stream`
+ *    (a cudaStream_t; NULL means the legacy default stream).
+ *  - Host-checkable argument errors return before any launch and leave every
+ *    output untouched.  A failed launch returns RLK_ERR_CUDA.
+ *  - Data errors found on the device (a token id outside [0, V), a non-finite
+ *    logit) do not abort: the affected row's outputs become NaN and a bit is
+ *    OR-ed into *out_status_word (when given); the caller reads it back.
+ *  - Results are deterministic: bitwise identical across runs and independent
+ *    of how rows are batched (row count, row order, position in the batch).
+ *
+ * The pages this implements give semantics, not formulas:
+ *  - RL-Kernel "Qwen3-8B VIME train-rollout consistency", section "ROCm MI300X
+ *    and gfx942": temperature finite and positive; top-p in (0,1]; the
+ *    complete retained top-p set with no support cap; top-k and temperature 0
+ *    rejected, not ignored; top-p < 1 is scored by the sparse logp /
+ *    monitoring-entropy fusion over the retained support, top-p = 1 by the
+ *    full-vocabulary strict scorer.
+ *  - RL-Kernel "ROCm sparse performance" notes: temperature, softmax, sort and
+ *    top-p thresholding keep the sampler's native semantics; train and rollout
+ *    log-probabilities must be bitwise equal (fixed reduction order); GRPO
+ *    uses standard-deviation normalisation; KL coefficient 0.01.
+ *  - LumenRL README, section "Rollout Correction": truncated importance
+ *    sampling clips large ratios.
+ *  - prime-rl v0.10.0 release notes, section "1. Trainer Performance": the
+ *    loss is chunked so full logits need not exist at once.
+ */
+#ifndef RLK_H_
+#define RLK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                       /* same type as cudaStream_t */
+typedef struct CUstream_st* rlk_stream;
+
+typedef enum {
+  RLK_OK = 0,
+  RLK_ERR_INVALID_ARG = 1,   /* a host-checkable argument is invalid          */
+  RLK_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. a mode)       */
+  RLK_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required    */
+  RLK_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed          */
+  RLK_ERR_TIMEOUT = 5,       /* reserved: a bounded device wait ran out       */
+  RLK_ERR_BAD_INPUT = 6      /* reserved for host-visible data errors         */
+} rlk_status;
+
+typedef enum { RLK_BF16 = 0, RLK_F32 = 1 } rlk_dtype;
+
+typedef enum {
+  RLK_AGG_TOKEN_MEAN = 0,            /* sum(mask * l) / sum(mask) over the batch (DAPO) */
+  RLK_AGG_SEQ_MEAN_TOKEN_MEAN = 1    /* mean over sequences of each sequence's token mean */
+} rlk_agg;
+
+/* Operation ids for rlk_workspace_size. */
+enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2 };
+
+/* Bits OR-ed into *out_status_word by the kernels. */
+#define RLK_STATUS_BAD_TOKEN_ID 0x1u   /* a token id outside [0, V)          */
+#define RLK_STATUS_NONFINITE    0x2u   /* a NaN or +-inf logit in a row      */
+
+/* Slots of the loss statistics vector (float [RLK_NSTATS]); fractions and
+ * means are over tokens with mask = 1. */
+enum {
+  RLK_STAT_LOSS = 0,          /* the loss value                                 */
+  RLK_STAT_TOKENS = 1,        /* sum of the mask                                */
+  RLK_STAT_CLIP_LOW = 2,      /* fraction with A < 0 and r < 1 - eps_low        */
+  RLK_STAT_CLIP_HIGH = 3,     /* fraction with A > 0 and r > 1 + eps_high       */
+  RLK_STAT_TIS_MEAN = 4,      /* mean truncated importance weight               */
+  RLK_STAT_TIS_CAPPED = 5,    /* fraction whose weight hit the cap              */
+  RLK_STAT_K3_MEAN = 6,       /* mean k3 KL estimate                            */
+  RLK_STAT_PG_MEAN = 7,       /* mean clipped policy-gradient term              */
+  RLK_NSTATS = 8
+};
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int rlk_version(void);
+
+/* Static, NUL-terminated description of a status code; never NULL. */
+const char* rlk_status_string(rlk_status status);
+
+/* Bytes of device workspace one call of `op` needs.  Arguments per op:
+ *  RLK_OP_LOGPROB_ENTROPY: T rows, V vocabulary, H unused      -> 0
+ *  RLK_OP_GRPO_LOSS:       T packed tokens, V = n_seq, H unused
+ *  RLK_OP_LMHEAD:          T rows, V vocabulary, H hidden size
+ * Returns 0 for an unknown op or negative sizes. */
+size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H);
+
+/*
+ * rlk_logprob_entropy -- per-token top-p log-probability and entropy.
+ *
+ * For each row t of logits[T, ld] (elements; ld >= V; row-major) with
+ * selected token y = token_ids[t]:
+ *   x_i = z_i / temperature;  m = max x;  w_i = exp(x_i - m);
+ *   rank tokens by (z descending, id ascending), -0 equal to +0;
+ *   k* = V if top_p == 1, else the least k whose prefix mass reaches top_p
+ *        (sum of w over the first k ranked tokens >= top_p * sum of all w);
+ *   S = the first k* ranked tokens (the retained set), Z_S = sum_S w;
+ *   out_logprob[t] = (x_y - m) - ln Z_S if y in S, else -INFINITY;
+ *   out_entropy[t] = Shannon entropy (nats) of w / Z_S over S;
+ *   out_nucleus_size[t] = k*.
+ * (The pages fix neither the retained-set rule nor the tie order; this library
+ *  keeps a token while the mass ranked strictly ahead of it is < top_p -- the
+ *  sampler's cumulative rule -- and keeps equal logits lower id first.)
+ *
+ * Arguments
+ *  logits          device, dtype `dtype`, T x ld elements; base 2-byte (bf16)
+ *                  or 4-byte (fp32) aligned.  Read only.
+ *  dtype           RLK_BF16 or RLK_F32 (top_p < 1 with fp32 logits takes a
+ *                  slower exact path).
+ *  T, V, ld        rows, vocabulary size (1 <= V <= 2^24), row stride.
+ *  token_ids       device int32[T].
+ *  temperature     finite, > 0.   top_p: 0 < top_p <= 1.
+ *  out_logprob     device float[T].   out_entropy: device float[T].
+ *  out_nucleus_size  device int32[T] or NULL.
+ *  out_status_word device uint32[1] or NULL; bits RLK_STATUS_* are OR-ed in.
+ *  workspace, workspace_bytes  unused (0 bytes required); may be NULL/0.
+ *  stream          CUDA stream.
+ * Errors: RLK_ERR_INVALID_ARG for T < 0, V < 1, V > 2^24, ld < V, null
+ *  required pointers, a bad dtype, a non-finite or non-positive temperature,
+ *  top_p outside (0,1].  T == 0 returns RLK_OK without launching.
+ */
+rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                               int64_t ld, const int32_t* token_ids, float temperature,
+                               float top_p, float* out_logprob, float* out_entropy,
+                               int32_t* out_nucleus_size, uint32_t* out_status_word,
+                               void* workspace, size_t workspace_bytes, rlk_stream stream);
+
+/*
+ * rlk_grpo_loss -- fused GRPO/DAPO loss with TIS correction and k3 KL.
+ *
+ * Sequences are packed: sequence s holds tokens [seq_offsets[s], seq_offsets[s+1]),
+ * and groups are contiguous runs of group_size sequences (GRPO groups of
+ * responses to one prompt; RL-Kernel "ROCm sparse performance" notes: GRPO
+ * standard-deviation normalisation).  Per group g with rewards R:
+ *   A_s = (R_s - mean_g R) / (std_g R + 1e-6), std with the n-1 divisor (0 when G = 1).
+ * Per token t of sequence s (mask m_t, 1 when loss_mask is NULL):
+ *   r = exp(logp_new - logp_old);
+ *   pg = -min(r A_s, clip(r, 1 - eps_low, 1 + eps_high) A_s)      (DAPO clip-higher);
+ *   w = min(exp(logp_old - logp_rollout), tis_cap)                 (TIS; LumenRL
+ *        README "Rollout Correction"), a detached weight on pg only;
+ *   d = logp_ref - logp_new; k3 = exp(d) - d - 1;
+ *   l_t = w pg + kl_coef k3.
+ * Aggregation RLK_AGG_TOKEN_MEAN: L = sum m l / sum m (0 if sum m = 0).
+ * RLK_AGG_SEQ_MEAN_TOKEN_MEAN: L = mean over sequences with sum m > 0 of
+ *   that sequence's token mean.
+ * Gradient (if out_dloss_dlogp_new): dL/dlogp_new[t] = (weight of t in L) *
+ *   (w g_pg + kl_coef (1 - exp(d))), g_pg = -r A when the unclipped term is
+ *   the active minimum (ties count as unclipped), else 0.
+ *
+ * Arguments
+ *  logp_new, logp_old, logp_rollout, logp_ref  device float[n_tok] each, indexed by
+ *                  the packed token position (seq_offsets[0] may be > 0).
+ *  loss_mask       device uint8[n_tok] (0/1) or NULL for all ones.
+ *  rewards         device float[n_seq].
+ *  seq_offsets     device int32[n_seq + 1], non-decreasing (not checked on the host).
+ *  n_seq, group_size  n_seq >= 0, group_size >= 1, n_seq % group_size == 0.
+ *  eps_low, eps_high  >= 0 and finite; tis_cap > 0; kl_coef >= 0 and finite.
+ *  agg             an rlk_agg value.
+ *  n_tok           number of packed tokens (seq_offsets[n_seq] - seq_offsets[0]); sizes the
+ *                  workspace and the gradient.
+ *  out_loss        device float[1].
+ *  out_dloss_dlogp_new  device float[n_tok] or NULL.
+ *  out_stats       device float[RLK_NSTATS] or NULL.
+ *  workspace       device scratch of at least rlk_workspace_size(RLK_OP_GRPO_LOSS, n_tok,
+ *                  n_seq, 0) bytes, 16-byte aligned; its contents on entry do not matter.
+ */
+rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
+                         const float* logp_rollout, const float* logp_ref,
+                         const uint8_t* loss_mask, const float* rewards,
+                         const int32_t* seq_offsets, int32_t n_seq, int32_t group_size,
+                         int64_t n_tok, float eps_low, float eps_high, float tis_cap,
+                         float kl_coef, rlk_agg agg, float* out_loss,
+                         float* out_dloss_dlogp_new, float* out_stats, void* workspace,
+                         size_t workspace_bytes, rlk_stream stream);
+
+/*
+ * rlk_lmhead_logprob -- the logits path at top_p = 1 fused with the LM-head
+ * GEMM: logits = hidden[T, H] * w_vocab[V, H]^T are produced tile by tile in
+ * tensor-core accumulators and folded into the online max / sum / entropy
+ * state; they never reach memory (prime-rl v0.10.0 notes, "1. Trainer
+ * Performance": chunked loss; RL-Kernel notes: deterministic GEMM with a
+ * fixed reduction order).  Logits are the fp32 accumulations, not rounded
+ * to bf16.
+ *
+ * Arguments
+ *  hidden          device bf16 [T, H] row-major, 16-byte aligned.
+ *  w_vocab         device bf16 [V, H] row-major, 16-byte aligned.
+ *  T, H, V         T >= 0, H a positive multiple of 64, V >= 1.
+ *  token_ids       device int32[T].
+ *  temperature     finite, > 0.   top_p must be 1 (else RLK_ERR_UNSUPPORTED).
+ *  out_logprob, out_entropy  device float[T].
+ *  out_status_word device uint32[1] or NULL.
+ *  workspace       at least rlk_workspace_size(RLK_OP_LMHEAD, T, V, H) bytes, 16-byte
+ *                  aligned; contents on entry do not matter.
+ */
+rlk_status rlk_lmhead_logprob(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
+                              int64_t V, const int32_t* token_ids, float temperature,
+                              float top_p, float* out_logprob, float* out_entropy,
+                              uint32_t* out_status_word, void* workspace,
+                              size_t workspace_bytes, rlk_stream stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* RLK_H_ */

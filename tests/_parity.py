@@ -1,0 +1,48 @@
+"""Comparison helpers shared by the GPU parity tests."""
+import numpy as np
+
+LP_TOL = 2e-4      # |delta logprob| (absolute)
+ENT_TOL = 2e-4     # |delta entropy| (absolute)
+GAP_EXEMPT = 1e-6  # rows whose boundary mass gap is below this may differ in k*
+
+
+def compare_rows(oracle, logits_host, ids_host, temperature, top_p, lp, ent, k, *, ref=None,
+                 label=""):
+    """Compare GPU outputs with the oracle row by row.
+
+    Rows with gap >= GAP_EXEMPT must have the same nucleus size and outputs
+    within tolerance; rows below it are compared against the oracle evaluated
+    at the GPU's nucleus size (both memberships are correct there) and counted.
+    Returns a small report dict.
+    """
+    lp = np.asarray(lp, np.float64)
+    ent = np.asarray(ent, np.float64)
+    k = np.asarray(k, np.int64)
+    if ref is None:
+        ref = oracle.logprob_entropy(logits_host, ids_host, temperature, top_p)
+    olp, oent, ok, gap = ref
+    exempt = gap < GAP_EXEMPT
+    bad_k = (~exempt) & (k != ok)
+    assert not bad_k.any(), f"{label}: nucleus size differs at rows {np.nonzero(bad_k)[0][:10]}"
+    if exempt.any():
+        rows = np.nonzero(exempt)[0]
+        force = np.zeros_like(k)
+        force[rows] = k[rows]
+        flp, fent, _, _ = oracle.logprob_entropy(logits_host, ids_host, temperature, top_p,
+                                                 force_k=force)
+        olp = olp.copy()
+        oent = oent.copy()
+        olp[rows] = flp[rows]
+        oent[rows] = fent[rows]
+    inf_o = np.isneginf(olp)
+    inf_g = np.isneginf(lp)
+    assert np.array_equal(inf_o, inf_g), f"{label}: -inf membership differs at {np.nonzero(inf_o != inf_g)[0][:10]}"
+    fin = ~inf_o
+    dlp = np.abs(lp[fin] - olp[fin])
+    dent = np.abs(ent - oent)
+    assert np.all(np.isfinite(lp[fin])) and np.all(np.isfinite(ent)), f"{label}: non-finite output"
+    assert dlp.size == 0 or dlp.max() <= LP_TOL, f"{label}: max |dlogprob| {dlp.max():.3e}"
+    assert dent.max() <= ENT_TOL, f"{label}: max |dentropy| {dent.max():.3e}"
+    return {"rows": int(lp.size), "gap_exempt": int(exempt.sum()),
+            "max_dlp": float(dlp.max()) if dlp.size else 0.0, "max_dent": float(dent.max()),
+            "members": int(fin.sum())}

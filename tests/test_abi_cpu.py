@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point the header declares, and rejects bad arguments on the host before any
+CUDA call (these calls never touch a device)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import entropy_logits_bf16_gb300 as rlk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: validation fails first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rlk.build()
+    return rlk.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "rlk.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rlk_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(rlk.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert lib.rlk_version() >= 100
+    for code in range(7):
+        assert lib.rlk_status_string(code)
+    assert lib.rlk_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes(lib):
+    assert lib.rlk_workspace_size(rlk.OP_LOGPROB_ENTROPY, 4096, 151936, 0) == 0
+    n = lib.rlk_workspace_size(rlk.OP_GRPO_LOSS, 590000, 512, 0)
+    assert n >= 512 * 8 * 4 and n % 256 == 0
+    assert lib.rlk_workspace_size(rlk.OP_GRPO_LOSS, 1, -1, 0) == 0
+    assert lib.rlk_workspace_size(99, 1, 1, 1) == 0
+
+
+def lpe(lib, **kw):
+    args = dict(logits=FAKE, dtype=0, T=4, V=100, ld=100, ids=FAKE, temperature=0.7, top_p=0.95,
+                lp=FAKE, ent=FAKE, k=None, status=None)
+    args.update(kw)
+    return lib.rlk_logprob_entropy(args["logits"], args["dtype"], args["T"], args["V"], args["ld"],
+                                   args["ids"], args["temperature"], args["top_p"], args["lp"],
+                                   args["ent"], args["k"], args["status"], None, 0, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(temperature=0.0), dict(temperature=-1.0), dict(temperature=math.inf),
+    dict(temperature=math.nan), dict(top_p=0.0), dict(top_p=1.0000001), dict(top_p=-0.5),
+    dict(top_p=math.nan), dict(T=-1), dict(V=0), dict(V=(1 << 24) + 1), dict(ld=99),
+    dict(dtype=2), dict(logits=None), dict(ids=None), dict(lp=None), dict(ent=None),
+    dict(logits=ctypes.c_void_p(0x10001)),
+])
+def test_logprob_entropy_rejects(lib, kw):
+    assert lpe(lib, **kw) == 1
+
+
+def test_top_k_and_zero_temperature_are_rejected_not_ignored(lib):
+    # The sampling contract rejects temperature 0; there is no top-k argument at all.
+    assert lpe(lib, temperature=0.0) == 1
+    assert "top_k" not in open(os.path.join(ROOT, "include", "rlk.h")).read()
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert lpe(lib, T=0) == 0
+
+
+def loss(lib, **kw):
+    a = dict(n_seq=4, G=2, n_tok=10, el=0.2, eh=0.28, cap=2.0, kl=0.01, agg=0, ws=FAKE,
+             ws_bytes=1 << 20, offs=FAKE, out=FAKE)
+    a.update(kw)
+    return lib.rlk_grpo_loss(FAKE, FAKE, FAKE, FAKE, None, FAKE, a["offs"], a["n_seq"], a["G"],
+                             a["n_tok"], a["el"], a["eh"], a["cap"], a["kl"], a["agg"], a["out"],
+                             None, None, a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(n_seq=-1), dict(G=0), dict(n_seq=5, G=2), dict(n_tok=-1), dict(el=-0.1),
+    dict(eh=math.inf), dict(cap=0.0), dict(cap=math.nan), dict(kl=-1.0), dict(agg=7),
+    dict(offs=None), dict(out=None),
+])
+def test_grpo_loss_rejects(lib, kw):
+    assert loss(lib, **kw) == 1
+
+
+def test_grpo_loss_workspace_errors(lib):
+    assert loss(lib, ws=None) == 3
+    assert loss(lib, ws_bytes=16) == 3
+    assert loss(lib, ws=ctypes.c_void_p(0x10004)) == 3
+
+
+def test_lmhead_rejects(lib):
+    f = lib.rlk_lmhead_logprob
+    ok = dict(T=4, H=128, V=1000, temp=0.7, p=1.0)
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(FAKE, FAKE, a["T"], a["H"], a["V"], FAKE, a["temp"], a["p"], FAKE, FAKE, None,
+                 None, 0, None)
+    assert call(H=100) == 1
+    assert call(temp=0.0) == 1
+    assert call(p=1.5) == 1
+    assert call(V=0) == 1
+    assert call(p=0.9) == 2          # fused path is top_p = 1 only
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    z = torch.zeros(2, 8, dtype=torch.bfloat16)
+    ids = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        rlk.logprob_entropy(z, ids, 0.7, 0.95)

@@ -1,0 +1,111 @@
+"""GPU parity of rlk_grpo_loss (through the C ABI) against the fp64 oracle.
+
+The loss gets the same fp32 inputs on both sides; the bar is relative error
+<= 1e-4 on the loss and the statistics, and per-token gradients within
+1e-4 of the largest gradient magnitude.  Results must repeat bitwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+REL = 1e-4
+
+
+def make_batch(n_prompts, G, lo, hi, seed, cap_frac=0.05):
+    off, R = workloads.grpo_batch(n_prompts, G, lo, hi, seed)
+    n = int(off[-1])
+    rng = np.random.default_rng(seed)
+    new = np.log(rng.uniform(1e-4, 1.0, n)).astype(np.float32)
+    old, ro, ref = workloads.perturbed_logps(new, seed)
+    # a few tokens whose old/rollout ratio exceeds the TIS cap, and large ratios
+    idx = rng.choice(n, max(1, int(cap_frac * n)), replace=False)
+    ro[idx] -= np.float32(1.5)
+    idx2 = rng.choice(n, max(1, int(0.05 * n)), replace=False)
+    old[idx2] += rng.normal(0, 0.4, idx2.size).astype(np.float32)
+    return off, R, new, old, ro, ref
+
+
+def gpu_loss(rlk, off, R, new, old, ro, ref, G, mask=None, **kw):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    loss, grad, stats = rlk.grpo_loss(t(new), t(old), t(ro), t(ref), t(R), t(off), G,
+                                      loss_mask=None if mask is None else t(mask), **kw)
+    torch.cuda.synchronize()
+    return float(loss.item()), grad.cpu().numpy(), stats.cpu().numpy()
+
+
+def check(oracle, rlk, off, R, new, old, ro, ref, G, mask=None, agg=0, **kw):
+    L, g, st = gpu_loss(rlk, off, R, new, old, ro, ref, G, mask, agg=agg, **kw)
+    oL, og, _, ost = oracle.grpo_loss(new, old, ro, ref, mask, R, off, G, agg=agg,
+                                      **{k: v for k, v in kw.items()})
+    assert abs(L - oL) <= REL * max(abs(oL), 1e-6), (L, oL)
+    scale = max(np.abs(og).max(), 1e-12)
+    assert np.abs(g - og).max() <= REL * scale
+    for i, name in enumerate(rlk.STAT_NAMES):
+        assert abs(st[i] - ost[name]) <= REL * max(abs(ost[name]), 1e-3), (name, st[i], ost[name])
+    return L, oL
+
+
+@pytest.mark.parametrize("agg", [0, 1])
+def test_dapo_config_loss(cuda_lib, oracle, agg):
+    """64 prompts x group 8, lengths U{256..2048}, Bernoulli rewards, eps 0.2/0.28,
+    TIS cap 2.0, k3 coefficient 0.01."""
+    off, R, new, old, ro, ref = make_batch(64, 8, 256, 2048, seed=3)
+    L, oL = check(oracle, cuda_lib, off, R, new, old, ro, ref, 8, agg=agg, eps_low=0.2,
+                  eps_high=0.28, tis_cap=2.0, kl_coef=0.01)
+    print("loss", L, "oracle", oL)
+
+
+def test_mask_groups_and_degenerate_cases(cuda_lib, oracle):
+    off, R, new, old, ro, ref = make_batch(6, 4, 1, 40, seed=8)
+    rng = np.random.default_rng(1)
+    mask = (rng.random(int(off[-1])) < 0.7).astype(np.uint8)
+    R[:4] = 1.0                                   # a zero-variance group
+    for agg in (0, 1):
+        check(oracle, cuda_lib, off, R, new, old, ro, ref, 4, mask=mask, agg=agg)
+        check(oracle, cuda_lib, off, R, new, old, ro, ref, 1, mask=mask, agg=agg)   # G = 1
+    zero = np.zeros_like(mask)
+    L, g, st = gpu_loss(cuda_lib, off, R, new, old, ro, ref, 4, zero)
+    assert L == 0.0 and not g.any() and st[1] == 0.0
+
+
+def test_empty_batch(cuda_lib):
+    off = np.zeros(1, np.int32)
+    e = np.zeros(0, np.float32)
+    L, g, st = gpu_loss(cuda_lib, off, e, e, e, e, e, 1)
+    assert L == 0.0 and g.size == 0
+
+
+def test_loss_bitwise_repeat(cuda_lib):
+    off, R, new, old, ro, ref = make_batch(16, 8, 100, 900, seed=4)
+    a = gpu_loss(cuda_lib, off, R, new, old, ro, ref, 8)
+    for _ in range(2):
+        b = gpu_loss(cuda_lib, off, R, new, old, ro, ref, 8)
+        assert np.float32(a[0]).tobytes() == np.float32(b[0]).tobytes()
+        assert a[1].tobytes() == b[1].tobytes() and a[2].tobytes() == b[2].tobytes()
+
+
+def test_chained_logits_to_loss(cuda_lib, oracle):
+    """Qwen3-shaped logits -> GPU log-probs -> loss, against the oracle's
+    log-probs -> oracle loss.  The chained error is reported (a 2e-4 log-prob
+    error moves the ratio by about 2e-4, so it is not held to 1e-4)."""
+    off, R = workloads.grpo_batch(4, 8, 16, 96, seed=3)
+    n = int(off[-1])
+    z, _ = workloads.peaked_bf16(n, seed=3, device="cuda")
+    hz = workloads.bf16_bits(z)
+    ids_h = oracle.sample_ids(hz, 0.7, 0.95, workloads.uniforms(n, 4))
+    ids = torch.from_numpy(ids_h).cuda()
+    lp, _ = cuda_lib.logprob_entropy(z, ids, 0.7, 0.95)
+    olp, _, _, _ = oracle.logprob_entropy(hz, ids_h, 0.7, 0.95)
+    new_gpu = lp.cpu().numpy()
+    new_or = olp.astype(np.float32)
+    old, ro, ref = workloads.perturbed_logps(new_or, 5)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    loss, _, _ = cuda_lib.grpo_loss(t(new_gpu), t(old), t(ro), t(ref), t(R), t(off), 8)
+    oL, _, _, _ = oracle.grpo_loss(new_or, old, ro, ref, None, R, off, 8)
+    rel = abs(loss.item() - oL) / max(abs(oL), 1e-6)
+    print(f"chained loss {loss.item():.6f} oracle {oL:.6f} rel {rel:.2e}")
+    assert rel < 1e-2
