@@ -29,6 +29,8 @@ STAT_NAMES = ("loss", "tokens", "clip_low_frac", "clip_high_frac", "tis_mean",
               "tis_capped_frac", "k3_mean", "pg_mean")
 EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logprob_entropy",
            "rlk_grpo_loss", "rlk_lmhead_logprob")
+DEBUG_EXPORTS = ("rlk_lmhead_logits_debug",)
+STATUS_TIMEOUT = 0x4
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +73,9 @@ def load(path: str | None = None):
         lib.rlk_lmhead_logprob.argtypes = [vp, vp, i64, i64, i64, vp, f32, f32, vp, vp, vp, vp,
                                            sz, vp]
         lib.rlk_lmhead_logprob.restype = ctypes.c_int
+        lib.rlk_lmhead_logits_debug.argtypes = [vp, vp, i64, i64, i64, vp, f32, vp, vp, vp, vp,
+                                                vp, sz, vp]
+        lib.rlk_lmhead_logits_debug.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -190,3 +195,23 @@ def lmhead_logprob(hidden, w_vocab, token_ids, temperature, top_p=1.0, *, status
                                   0 if workspace is None else workspace.numel(), _stream(dev))
     _check("rlk_lmhead_logprob", code)
     return lp, ent
+
+
+def lmhead_logits_debug(hidden, w_vocab, token_ids, temperature):
+    """Validation aid: the fused LM-head path that also returns the fp32 logits
+    it computed ([T, V]); for small sizes only."""
+    lib = load()
+    _need_cuda(hidden, w_vocab, token_ids)
+    T, H = hidden.shape
+    V = w_vocab.shape[0]
+    dev = hidden.device
+    need = int(lib.rlk_workspace_size(OP_LMHEAD, T, V, H))
+    ws = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+    logits = torch.empty(T, V, device=dev, dtype=torch.float32)
+    lp = torch.empty(T, device=dev, dtype=torch.float32)
+    ent = torch.empty(T, device=dev, dtype=torch.float32)
+    code = lib.rlk_lmhead_logits_debug(_ptr(hidden), _ptr(w_vocab), T, H, V, _ptr(token_ids),
+                                       float(temperature), _ptr(logits), _ptr(lp), _ptr(ent),
+                                       None, _ptr(ws), ws.numel(), _stream(dev))
+    _check("rlk_lmhead_logits_debug", code)
+    return logits, lp, ent

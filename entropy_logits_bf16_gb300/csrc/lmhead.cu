@@ -1,22 +1,513 @@
-// rlk_lmhead_logprob: the fused LM-head path (tensor-core GEMM tiles folded
-// into the online log-sum-exp / entropy state).  Not built yet: the entry
-// point reports RLK_ERR_UNSUPPORTED.
+// rlk_lmhead_logprob: the top_p = 1 logits path fused with the LM-head GEMM.
+//
+// What is computed: logits[t, v] = sum_k hidden[t, k] W[v, k] (bf16 inputs,
+// fp32 accumulation, never rounded or stored), then for each row the
+// full-vocabulary log-probability of the selected token and the entropy at
+// temperature T (RL-Kernel "Qwen3-8B VIME train-rollout consistency", section
+// "ROCm MI300X and gfx942": the full-vocabulary strict scorer at top_p = 1;
+// prime-rl v0.10.0 notes, "1. Trainer Performance": the loss is chunked so the
+// full logits need not exist at once; RL-Kernel "ROCm sparse performance"
+// notes: a deterministic GEMM with a fixed reduction order).
+//
+// Design (sm_103a, one CTA per SM, persistent):
+//  * Work unit = (128-row tile of hidden, one of NSLICE fixed vocabulary
+//    slices).  Units are strided over the grid; the slice boundaries depend
+//    only on V, so a row's result never depends on the batch size.
+//  * warp 0: TMA producer.  Each stage holds a 128 x 64 tile of hidden and a
+//    256 x 64 tile of W (bf16, 128-byte swizzle), 4 stages in shared memory,
+//    completion tracked by mbarriers.
+//  * warp 1: allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
+//    one elected thread issues tcgen05.mma (M=128, N=256, K=16) over K, then
+//    commits to the stage's "empty" barrier and, after the last K step, to
+//    the accumulator's "full" barrier.
+//  * warps 2-5: epilogue, one TMEM lane (= one row) per thread.  tcgen05.ld
+//    brings 32 columns at a time into registers; the columns fold into an
+//    online (max, sum of 2^d as double-float, sum of 2^d d) state in column
+//    order, and the selected token's logit is captured.  The accumulator is
+//    handed back while the next tile's MMAs run into the other one.
+//  * After a unit, each row's state goes to the workspace; a combine kernel
+//    merges the NSLICE states of a row in slice order (fixed) and writes the
+//    log-probability and entropy.
+//  * Every wait on an mbarrier is bounded; on expiry the CTA raises
+//    RLK_STATUS_TIMEOUT in the status word and winds down.
 
+#include <cuda.h>
+#include <math.h>
+
+#include <atomic>
+
+#include "common.cuh"
 #include "internal.h"
+#include "rlk.h"
 
 namespace rlk {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int NSLICE = 19;
+constexpr int THREADS = 192;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SPIN_LIMIT = 1u << 22;
+constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+// Bounded wait; false when the limit ran out or another role gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023u) == 1023u && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor: K-major tile written by TMA with the
+// 128-byte swizzle; 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);   // start address
+  d |= (uint64_t)1u << 16;                   // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024u >> 4) << 32;         // stride byte offset: next 8-row group
+  d |= (uint64_t)1u << 46;                   // descriptor version
+  d |= (uint64_t)2u << 61;                   // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// ------------------------------------------------------------ row state
+struct RowState {
+  float m, hi, lo, u;
+};
+
+__device__ __forceinline__ bool state_empty(const RowState& a) {
+  return a.m == -INFINITY && a.hi == 0.f && a.lo == 0.f && a.u == 0.f;
+}
+
+__device__ __forceinline__ RowState state_merge(const RowState& a, const RowState& b, float c) {
+  if (state_empty(b)) return a;
+  if (state_empty(a)) return b;
+  const float M = fmaxf(a.m, b.m);
+  const float da = __fmul_rn(__fsub_rn(M, a.m), c);
+  const float db = __fmul_rn(__fsub_rn(M, b.m), c);
+  const float fa = (a.m == M) ? 1.f : ex2(-da);
+  const float fb = (b.m == M) ? 1.f : ex2(-db);
+  const float sa = __fadd_rn(a.hi, a.lo), sb = __fadd_rn(b.hi, b.lo);
+  RowState r;
+  r.m = M;
+  r.u = __fadd_rn(__fmul_rn(fa, __fmaf_rn(-da, sa, a.u)), __fmul_rn(fb, __fmaf_rn(-db, sb, b.u)));
+  float s, e;
+  two_sum(__fmul_rn(a.hi, fa), __fmul_rn(b.hi, fb), s, e);
+  e = __fadd_rn(e, __fadd_rn(__fmul_rn(a.lo, fa), __fmul_rn(b.lo, fb)));
+  r.hi = __fadd_rn(s, e);
+  r.lo = __fsub_rn(e, __fsub_rn(r.hi, s));
+  return r;
+}
+
+// Fold 32 consecutive logits (the first n valid) into the state.
+__device__ __forceinline__ void absorb32(RowState& st, const float (&v)[32], int n, float c) {
+  float gm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j < n) gm = fmaxf(gm, v[j]);
+  if (gm > st.m) {
+    if (st.m != -INFINITY) {
+      const float delta = __fmul_rn(__fsub_rn(gm, st.m), c);
+      const float f = ex2(-delta);
+      st.u = __fmul_rn(f, __fmaf_rn(-delta, __fadd_rn(st.hi, st.lo), st.u));
+      st.hi = __fmul_rn(st.hi, f);
+      st.lo = __fmul_rn(st.lo, f);
+    }
+    st.m = gm;
+  }
+  float w[32], d[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j < n) {
+      d[j] = __fmul_rn(__fsub_rn(v[j], st.m), c);
+      w[j] = ex2(d[j]);
+    } else {
+      d[j] = 0.f;
+      w[j] = 0.f;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) st.u = __fmaf_rn(w[j], d[j], st.u);
+#pragma unroll
+  for (int h = 16; h > 0; h >>= 1) {
+#pragma unroll
+    for (int j = 0; j < h; ++j) w[j] = __fadd_rn(w[j], w[j + h]);
+  }
+  float s, e;
+  two_sum(st.hi, w[0], s, e);
+  st.hi = s;
+  st.lo = __fadd_rn(st.lo, e);
+}
+
+struct LmParams {
+  int64_t T, V;
+  int n_mt, n_nt, n_units, k_steps;
+  const int32_t* ids;
+  float c;               // log2(e) / temperature
+  float4* part;          // [NSLICE][T] row states
+  float* zy;             // [T] the selected token's logit
+  float* debug_logits;   // [T][V] when non-null (validation aid)
+  uint32_t* status;
+};
+
+__device__ __forceinline__ void slice_bounds(int n_nt, int sl, int& nt0, int& nt1) {
+  nt0 = (int)((int64_t)sl * n_nt / NSLICE);
+  nt1 = (int)((int64_t)(sl + 1) * n_nt / NSLICE);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    lmhead_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                  const __grid_constant__ CUtensorMap tmap_b, LmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;            // 1024-aligned stage area
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
+  const uint32_t accf0 = empty0 + 8 * STAGES, acce0 = accf0 + 16;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf0 + 8 * a, 1);
+      mbar_init(acce0 + 8 * a, 4);   // one arrive per epilogue warp
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0u, issued_parity = 0u;  // per stage: used, parity of last issue
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const int mt = u / NSLICE, sl = u % NSLICE;
+        int nt0, nt1;
+        slice_bounds(p.n_nt, sl, nt0, nt1);
+        for (int nt = nt0; nt < nt1 && ok; ++nt) {
+          for (int k = 0; k < p.k_steps; ++k) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+            const uint32_t fb = full0 + 8 * stage;
+            mbar_expect_tx(fb, STAGE_BYTES);
+            const uint32_t sa = base + stage * STAGE_BYTES;
+            tma_load_2d(sa, &tmap_a, fb, k * BK, mt * BM);
+            tma_load_2d(sa + A_BYTES, &tmap_b, fb, k * BK, nt * BN);
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+      // If any role gave up, let every issued copy land before the CTA exits
+      // (each wait bounded).
+      if (!ok || *abort_flag) {
+        for (int s2 = 0; s2 < STAGES; ++s2) {
+          if (!(issued_mask & (1u << s2))) continue;
+          const uint32_t par = (issued_parity >> s2) & 1u;
+          for (uint32_t i = 0; i < SPIN_LIMIT; ++i)
+            if (mbar_try_wait(full0 + 8 * s2, par)) break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t tile = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const int sl = u % NSLICE;
+        int nt0, nt1;
+        slice_bounds(p.n_nt, sl, nt0, nt1);
+        for (int nt = nt0; nt < nt1 && ok; ++nt, ++tile) {
+          const uint32_t acc = tile & 1u, accph = (tile >> 1) & 1u;
+          if (!mbar_wait(acce0 + 8 * acc, accph ^ 1u, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + acc * BN;
+          for (int k = 0; k < p.k_steps; ++k) {
+            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = base + stage * STAGE_BYTES;
+            const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sa + A_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // advance 16 bf16 (32 bytes) along K inside the swizzle atom
+              mma_bf16(d_tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2),
+                       (k > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(empty0 + 8 * stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+          if (ok) mma_commit(accf0 + 8 * acc);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------ epilogue
+    const int q = warp & 3;                     // TMEM lane quadrant of this warp
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t tile = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+      const int mt = u / NSLICE, sl = u % NSLICE;
+      int nt0, nt1;
+      slice_bounds(p.n_nt, sl, nt0, nt1);
+      const int64_t row = (int64_t)mt * BM + q * 32 + lane;
+      const int64_t y = row < p.T ? (int64_t)p.ids[row] : -1;
+      RowState st{-INFINITY, 0.f, 0.f, 0.f};
+      float zy = 0.f;
+      bool have_zy = false;
+      for (int nt = nt0; nt < nt1; ++nt, ++tile) {
+        const uint32_t acc = tile & 1u, accph = (tile >> 1) & 1u;
+        if (!mbar_wait(accf0 + 8 * acc, accph, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          float v[32];
+          tmem_ld32(tmem + lane_base + acc * BN + ch * 32, v);
+          const int64_t col0 = (int64_t)nt * BN + ch * 32;
+          const int n = (int)(p.V - col0 < 32 ? (p.V - col0 > 0 ? p.V - col0 : 0) : 32);
+          if (n > 0) absorb32(st, v, n, p.c);
+          if (y >= col0 && y < col0 + n) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j == y) zy = v[j];
+            have_zy = true;
+          }
+          if (p.debug_logits && row < p.T) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < n) p.debug_logits[row * p.V + col0 + j] = v[j];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+      }
+      if (ok && row < p.T) {
+        p.part[(int64_t)sl * p.T + row] = make_float4(st.m, st.hi, st.lo, st.u);
+        if (have_zy) p.zy[row] = zy;
+      }
+    }
+    if (!ok && lane == 0 && p.status) atomicOr(p.status, RLK_STATUS_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// Merge each row's slice states in slice order and write the outputs.
+__global__ void __launch_bounds__(256) lmhead_combine_kernel(LmParams p, float* out_lp,
+                                                             float* out_ent, float temperature) {
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= p.T) return;
+  const int64_t y = p.ids[row];
+  if (y < 0 || y >= p.V) {
+    out_lp[row] = NAN;
+    out_ent[row] = NAN;
+    if (p.status) atomicOr(p.status, RLK_STATUS_BAD_TOKEN_ID);
+    return;
+  }
+  RowState st{-INFINITY, 0.f, 0.f, 0.f};
+  for (int sl = 0; sl < NSLICE; ++sl) {
+    const float4 s = p.part[(int64_t)sl * p.T + row];
+    st = state_merge(st, RowState{s.x, s.y, s.z, s.w}, p.c);
+  }
+  const float z = __fadd_rn(st.hi, st.lo);
+  if (!(isfinite(z) && isfinite(st.u) && isfinite(st.m))) {
+    out_lp[row] = NAN;
+    out_ent[row] = NAN;
+    if (p.status) atomicOr(p.status, RLK_STATUS_NONFINITE);
+    return;
+  }
+  const float lz = logf(z);
+  out_lp[row] = __fsub_rn(__fdiv_rn(__fsub_rn(p.zy[row], st.m), temperature), lz);
+  out_ent[row] = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, st.u), z));
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load();
+  if (f) return f;
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  f = reinterpret_cast<EncodeTiledFn>(ptr);
+  fn.store(f);
+  return f;
+}
+
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return f(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
 
 size_t lmhead_workspace_bytes(int64_t T, int64_t V, int64_t H) {
-  (void)T;
   (void)V;
   (void)H;
-  return 0;
+  const size_t b = (size_t)NSLICE * (size_t)T * sizeof(float4) + (size_t)T * sizeof(float);
+  return (b + 255) & ~(size_t)255;
+}
+
+cudaError_t launch_lmhead_impl(const LmheadArgs& a, float* debug_logits, cudaStream_t stream) {
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, a.hidden, (uint64_t)a.T, (uint64_t)a.H, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, a.w_vocab, (uint64_t)a.V, (uint64_t)a.H, BN)) return cudaErrorInvalidValue;
+  static std::atomic<int> attr_done{0};
+  if (!attr_done.load()) {
+    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done.store(1);
+  }
+  LmParams p;
+  p.T = a.T;
+  p.V = a.V;
+  p.n_mt = (int)((a.T + BM - 1) / BM);
+  p.n_nt = (int)((a.V + BN - 1) / BN);
+  p.n_units = p.n_mt * NSLICE;
+  p.k_steps = (int)(a.H / BK);
+  p.ids = a.ids;
+  p.c = (float)(1.4426950408889634 / (double)a.temperature);
+  p.part = static_cast<float4*>(a.workspace);
+  p.zy = reinterpret_cast<float*>(static_cast<char*>(a.workspace) +
+                                  (size_t)NSLICE * (size_t)a.T * sizeof(float4));
+  p.debug_logits = debug_logits;
+  p.status = a.status;
+  const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
+  lmhead_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  lmhead_combine_kernel<<<(unsigned)((a.T + 255) / 256), 256, 0, stream>>>(
+      p, a.out_logprob, a.out_entropy, a.temperature);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_lmhead(const LmheadArgs& a, cudaStream_t stream) {
-  (void)a;
-  (void)stream;
-  return cudaErrorNotSupported;
+  return launch_lmhead_impl(a, nullptr, stream);
 }
 
 }  // namespace rlk

@@ -7,6 +7,7 @@
 
 #include "internal.h"
 #include "rlk.h"
+#include "rlk_debug.h"
 
 namespace rlk {
 
@@ -71,10 +72,10 @@ rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, i
   if (T < 0 || V < 1 || V > (int64_t(1) << 24) || ld < V) return RLK_ERR_INVALID_ARG;
   if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
   if (!(top_p > 0.0f && top_p <= 1.0f)) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;   // nothing to read or write; pointers may be NULL
   if (!logits || !token_ids || !out_logprob || !out_entropy) return RLK_ERR_INVALID_ARG;
   const uintptr_t elem = dtype == RLK_BF16 ? 2u : 4u;
   if (reinterpret_cast<uintptr_t>(logits) % elem != 0) return RLK_ERR_INVALID_ARG;
-  if (T == 0) return RLK_OK;
   rlk::LpeArgs a;
   a.logits = logits;
   a.dtype = dtype == RLK_BF16 ? 0 : 1;
@@ -139,12 +140,13 @@ rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
              : RLK_ERR_CUDA;
 }
 
-rlk_status rlk_lmhead_logprob(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
-                              int64_t V, const int32_t* token_ids, float temperature,
-                              float top_p, float* out_logprob, float* out_entropy,
-                              uint32_t* out_status_word, void* workspace,
-                              size_t workspace_bytes, rlk_stream stream) {
+static rlk_status lmhead_common(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
+                                int64_t V, const int32_t* token_ids, float temperature,
+                                float top_p, float* out_logits, float* out_logprob,
+                                float* out_entropy, uint32_t* out_status_word, void* workspace,
+                                size_t workspace_bytes, rlk_stream stream) {
   if (T < 0 || H < 64 || H % 64 != 0 || V < 1 || V > (int64_t(1) << 24)) return RLK_ERR_INVALID_ARG;
+  if (T > (int64_t(1) << 30) || H > (int64_t(1) << 20)) return RLK_ERR_INVALID_ARG;
   if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
   if (!(top_p > 0.0f && top_p <= 1.0f)) return RLK_ERR_INVALID_ARG;
   if (!hidden || !w_vocab || !token_ids || !out_logprob || !out_entropy) return RLK_ERR_INVALID_ARG;
@@ -169,9 +171,31 @@ rlk_status rlk_lmhead_logprob(const void* hidden, const void* w_vocab, int64_t T
   a.out_entropy = out_entropy;
   a.status = out_status_word;
   a.workspace = workspace;
-  const cudaError_t e = rlk::launch_lmhead(a, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      rlk::launch_lmhead_impl(a, out_logits, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return RLK_ERR_UNSUPPORTED;
   return e == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_lmhead_logprob(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
+                              int64_t V, const int32_t* token_ids, float temperature,
+                              float top_p, float* out_logprob, float* out_entropy,
+                              uint32_t* out_status_word, void* workspace,
+                              size_t workspace_bytes, rlk_stream stream) {
+  return lmhead_common(hidden, w_vocab, T, H, V, token_ids, temperature, top_p, nullptr,
+                       out_logprob, out_entropy, out_status_word, workspace, workspace_bytes,
+                       stream);
+}
+
+rlk_status rlk_lmhead_logits_debug(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
+                                   int64_t V, const int32_t* token_ids, float temperature,
+                                   float* out_logits, float* out_logprob, float* out_entropy,
+                                   uint32_t* out_status_word, void* workspace,
+                                   size_t workspace_bytes, rlk_stream stream) {
+  if (!out_logits) return RLK_ERR_INVALID_ARG;
+  return lmhead_common(hidden, w_vocab, T, H, V, token_ids, temperature, 1.0f, out_logits,
+                       out_logprob, out_entropy, out_status_word, workspace, workspace_bytes,
+                       stream);
 }
 
 }  // extern "C"

@@ -67,6 +67,8 @@ enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2 };
 /* Bits OR-ed into *out_status_word by the kernels. */
 #define RLK_STATUS_BAD_TOKEN_ID 0x1u   /* a token id outside [0, V)          */
 #define RLK_STATUS_NONFINITE    0x2u   /* a NaN or +-inf logit in a row      */
+#define RLK_STATUS_TIMEOUT      0x4u   /* a bounded device wait ran out; the
+                                          call's outputs are not valid      */
 
 /* Slots of the loss statistics vector (float [RLK_NSTATS]); fractions and
  * means are over tokens with mask = 1. */
@@ -127,7 +129,8 @@ size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H);
  *  stream          CUDA stream.
  * Errors: RLK_ERR_INVALID_ARG for T < 0, V < 1, V > 2^24, ld < V, null
  *  required pointers, a bad dtype, a non-finite or non-positive temperature,
- *  top_p outside (0,1].  T == 0 returns RLK_OK without launching.
+ *  top_p outside (0,1].  T == 0 returns RLK_OK without launching (pointers
+ *  may then be NULL).
  */
 rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
                                int64_t ld, const int32_t* token_ids, float temperature,

@@ -1,7 +1,9 @@
 """Comparison helpers shared by the GPU parity tests."""
 import numpy as np
 
-LP_TOL = 2e-4      # |delta logprob| (absolute)
+LP_TOL = 2e-4      # |delta logprob| (absolute) ...
+LP_REL = 2.0 ** -22  # ... plus ~2 ulp of the fp32 output, which cannot hold 2e-4
+                     # absolute once |logprob| exceeds ~1e3 (rows of huge logits)
 ENT_TOL = 2e-4     # |delta entropy| (absolute)
 GAP_EXEMPT = 1e-6  # rows whose boundary mass gap is below this may differ in k*
 
@@ -41,7 +43,8 @@ def compare_rows(oracle, logits_host, ids_host, temperature, top_p, lp, ent, k, 
     dlp = np.abs(lp[fin] - olp[fin])
     dent = np.abs(ent - oent)
     assert np.all(np.isfinite(lp[fin])) and np.all(np.isfinite(ent)), f"{label}: non-finite output"
-    assert dlp.size == 0 or dlp.max() <= LP_TOL, f"{label}: max |dlogprob| {dlp.max():.3e}"
+    tol = LP_TOL + LP_REL * np.abs(olp[fin])
+    assert dlp.size == 0 or np.all(dlp <= tol), f"{label}: max |dlogprob| {dlp.max():.3e}"
     assert dent.max() <= ENT_TOL, f"{label}: max |dentropy| {dent.max():.3e}"
     return {"rows": int(lp.size), "gap_exempt": int(exempt.sum()),
             "max_dlp": float(dlp.max()) if dlp.size else 0.0, "max_dent": float(dent.max()),

@@ -20,16 +20,18 @@ def lib():
     return rlk.load()
 
 
-def declared_functions():
-    text = open(os.path.join(ROOT, "include", "rlk.h")).read()
+def declared_functions(header):
+    text = open(os.path.join(ROOT, "include", header)).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(rlk_[a-z_]+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(lib):
-    names = declared_functions()
+    names = declared_functions("rlk.h")
     assert set(names) == set(rlk.EXPORTS)
-    for n in names:
+    debug = declared_functions("rlk_debug.h")
+    assert set(debug) == set(rlk.DEBUG_EXPORTS)
+    for n in names + debug:
         assert hasattr(lib, n), n
 
 

@@ -173,11 +173,12 @@ def test_ties_at_the_threshold(cuda_lib, oracle):
 
 
 def test_bad_rows_give_nan_and_status(cuda_lib):
-    z, _ = workloads.peaked_bf16(6, V=3000, seed=2, device="cuda")
+    z, peaks = workloads.peaked_bf16(6, V=3000, seed=2, device="cuda")
+    z[0, int(peaks[0])] = 30.0                 # row 0: a valid row whose id is surely kept
     z[1, 5] = float("nan")
     z[2, 7] = float("inf")
     z[3, 9] = float("-inf")
-    ids = torch.tensor([0, 1, 2, 3, 3000, -1], dtype=torch.int32, device="cuda")
+    ids = torch.tensor([int(peaks[0]), 1, 2, 3, 3000, -1], dtype=torch.int32, device="cuda")
     for p in (1.0, 0.9):
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         lp, ent = cuda_lib.logprob_entropy(z, ids, 0.7, p, status_word=st)
