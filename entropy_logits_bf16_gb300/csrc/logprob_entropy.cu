@@ -16,26 +16,39 @@
 //   d = (z - m) log2(e) / T.  The 512 states merge along a fixed tree.  At
 //   top_p = 1 this is the answer: logprob = (z_y - m)/T - ln Z and
 //   H = ln Z - ln2 * (sum 2^d d) / Z.
-//  top_p < 1: every retained token lies in the window z >= m - L T with
-//   L = ln(V / ((1 - top_p) Z)) + 0.5, because the tokens below it carry less
-//   than V e^-L < (1 - top_p) Z of the mass.  Pass 2 re-reads the row (an L2
-//   hit) and counts the window's tokens per distinct bf16 value into a
-//   shared-memory histogram indexed by key distance from the max; values with
-//   |z| < 2^-12 share one bin whose mass is summed token by token.  All tokens
-//   of one value carry the same mass, so a bin's mass is count x w(value):
-//   integer counts make the histogram independent of thread timing.  A
-//   fixed-order double-float scan over the bins (largest value first) finds
-//   the bin where the prefix mass reaches top_p * Z and how many of its tied
-//   tokens are needed (ties are kept lower id first).  The retained mass Z_S,
-//   the entropy and the selected token's membership (its rank among equal
-//   values is counted in pass 2) follow.
-//  Rows whose window is wider than the histogram, rows whose threshold falls
-//   in the shared near-zero bin, and fp32 rows at top_p < 1 instead bisect
-//   on the value key with fixed-order passes over the row (exact, slower).
-//  Each of these choices depends only on the row's own values, and every sum
-//   has a fixed order, so a row's output bits never depend on the batch.
+//  top_p < 1, bf16: the retained set lies in a window z >= m - L T.  All
+//   tokens of one bf16 value carry the same mass, so the window is summarised
+//   exactly by integer counts per distinct value (a histogram over the
+//   order-preserving 16-bit key; the values with |z| < 2^-12 share one bin
+//   whose mass is summed per token in fixed point).  Counts and fixed-point
+//   sums do not depend on the order of the atomics that build them.
+//   - Fast path: during pass 1 the CTA shares a running max; a group holding a
+//     token within the speculative depth L_spec T (L_spec = ln(1/(1-top_p)) + 7)
+//     of it is pushed on a per-warp shared-memory queue (one packed bf16x2
+//     compare per word, a ballot per group) and expanded with all lanes busy
+//     into an absolute-key histogram of 16-bit counts.  The running max never
+//     exceeds the final one, so every token of the final window is counted.
+//   - A fixed-order double-float scan over the window's bins (largest value
+//     first) finds the bin where the prefix mass reaches top_p * Z and how
+//     many of its tied tokens are needed (ties are kept lower id first).  If
+//     the window's own mass falls short, the worst-case window
+//     L = ln(V / ((1 - top_p) Z)) + 0.5 -- below which lies less than
+//     V e^-L < (1 - top_p) Z of the mass -- is counted by a second pass over
+//     the row (an L2 hit) and scanned the same way.  The same pass serves rows
+//     the fast path cannot take (a window touching the near-zero bin, or more
+//     than 65535 counted tokens).  Every path feeds identical bins to the same
+//     scan, so the result does not depend on which path ran.
+//   - Rows whose window spans more than the histogram, rows whose threshold
+//     falls in the near-zero bin, and fp32 rows bisect on the value key with
+//     fixed-order passes over the row (exact, slower).  This choice depends
+//     only on the row's values.
+//  No sum depends on thread timing, so a row's output bits never depend on
+//  the batch around it.
 
+#include <cuda_bf16.h>
 #include <math.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -46,8 +59,10 @@ namespace {
 
 constexpr int NT = 512;
 constexpr int NWARP = NT / 32;
-constexpr int HB = 8192;         // histogram bins (32 KB of shared memory)
-constexpr int BPT = HB / NT;     // bins per thread in the scan
+constexpr int HB = 8192;         // largest window (bins) the histogram path takes
+constexpr int QCAP = 64;         // per-warp queue of candidate groups (flushed at >= 32)
+constexpr int SK_ROUNDS = 48;    // rows of up to SK_ROUNDS * NT groups keep a group-max sketch
+constexpr int WL = 256;          // per-warp list of candidate groups (sketch pass)
 
 // Ordered 16-bit keys of the bf16 values with |z| < 2^-12 (exponent field
 // < 115) form the contiguous interval [MERGE_LO, MERGE_HI]; it is compressed
@@ -82,6 +97,18 @@ struct RowBf16 {
     for (int k = 0; k < E; ++k) v[k] = k < n ? bf16_val(__ldg(p + base + k)) : -INFINITY;
     return n;
   }
+  __device__ __forceinline__ float elem(int64_t i) const { return bf16_val(__ldg(p + i)); }
+  // The group as four packed words; missing tail elements read as -inf.
+  __device__ __forceinline__ uint4 packed(int64_t g, int64_t nfull) const {
+    if (g < nfull && aligned) return __ldg(reinterpret_cast<const uint4*>(p) + g);
+    float v[E];
+    scal(g, v);
+    uint32_t b[E];
+#pragma unroll
+    for (int k = 0; k < E; ++k) b[k] = __float_as_uint(v[k]) >> 16;
+    return make_uint4(b[0] | (b[1] << 16), b[2] | (b[3] << 16), b[4] | (b[5] << 16),
+                      b[6] | (b[7] << 16));
+  }
   __device__ static __forceinline__ uint32_t key(float v) {
     return okey16(__float_as_uint(v) >> 16);
   }
@@ -107,31 +134,33 @@ struct RowF32 {
     for (int k = 0; k < E; ++k) v[k] = k < n ? __ldg(p + base + k) : -INFINITY;
     return n;
   }
+  __device__ __forceinline__ float elem(int64_t i) const { return __ldg(p + i); }
   __device__ static __forceinline__ uint32_t key(float v) { return okey32(__float_as_uint(v)); }
   __device__ static __forceinline__ float value_of_key(uint32_t k) {
     return __uint_as_float(okey32_inverse(k));
   }
 };
 
+__device__ __forceinline__ void unpack8(const uint4 q, float (&v)[8]) {
+  v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+  v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
+}
+
 // Calls f(values, n_valid, group) for this thread's groups in a fixed order
 // (g = tid, tid + NT, ...), whatever the row's alignment.  Aligned rows issue
-// four 16-byte loads before using them.
-template <class Row, class F>
+// BATCH 16-byte loads before using them (memory-level parallelism).
+template <int BATCH = 4, class Row, class F>
 __device__ __forceinline__ void for_groups(const Row& row, int tid, F&& f) {
   constexpr int E = Row::E;
   const int64_t nfull = row.V / E;
   int64_t g = tid;
   if (row.aligned) {
-    for (; g + 3 * NT < nfull; g += 4 * NT) {
-      float a[E], b[E], c[E], d[E];
-      row.vec(g, a);
-      row.vec(g + NT, b);
-      row.vec(g + 2 * NT, c);
-      row.vec(g + 3 * NT, d);
-      f(a, E, g);
-      f(b, E, g + NT);
-      f(c, E, g + 2 * NT);
-      f(d, E, g + 3 * NT);
+    for (; g + (BATCH - 1) * NT < nfull; g += BATCH * NT) {
+      float a[BATCH][E];
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) row.vec(g + b * NT, a[b]);
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) f(a[b], E, g + b * NT);
     }
     for (; g < nfull; g += NT) {
       float a[E];
@@ -184,9 +213,10 @@ __device__ __forceinline__ Online online_merge(const Online& a, const Online& b,
   return r;
 }
 
-// Fold one group of N values (the first n valid) into the state.
+// Fold one group of N values (the first n valid) into the state; returns the
+// group's max.
 template <int N>
-__device__ __forceinline__ void absorb(Online& st, const float (&v)[N], int n, float c) {
+__device__ __forceinline__ float absorb(Online& st, const float (&v)[N], int n, float c) {
   float gm = -INFINITY;
 #pragma unroll
   for (int k = 0; k < N; ++k)
@@ -225,18 +255,83 @@ __device__ __forceinline__ void absorb(Online& st, const float (&v)[N], int n, f
   st.lo = __fadd_rn(st.lo, e);
 #pragma unroll
   for (int k = 0; k < N; ++k) st.u = __fmaf_rn(w[k], d[k], st.u);
+  return gm;
 }
 
-// ------------------------------------------------------ block reductions
-struct Smem {
-  uint32_t hist[HB];
+// Fold one full group of 8 bf16 values (packed words) into the state: the
+// group max by packed bf16x2 compares, then the same arithmetic as absorb().
+// With WITH_U the entropy numerator is accumulated too; *gmin gets the group
+// min (to detect -inf inputs when WITH_U is off).  Returns the group max.
+__device__ __forceinline__ __nv_bfloat162 as_bf162w(uint32_t w) {
+  return *reinterpret_cast<const __nv_bfloat162*>(&w);
+}
+template <bool WITH_U>
+__device__ __forceinline__ float absorb_packed(Online& st, const uint4 q, float c, float& gmin) {
+  const __nv_bfloat162 mx = __hmax2(__hmax2(as_bf162w(q.x), as_bf162w(q.y)),
+                                    __hmax2(as_bf162w(q.z), as_bf162w(q.w)));
+  const float gm = fmaxf(__low2float(mx), __high2float(mx));
+  if (!WITH_U) {
+    const __nv_bfloat162 mn = __hmin2(__hmin2(as_bf162w(q.x), as_bf162w(q.y)),
+                                      __hmin2(as_bf162w(q.z), as_bf162w(q.w)));
+    gmin = fminf(__low2float(mn), __high2float(mn));
+  }
+  if (gm > st.m) {
+    if (st.m != -INFINITY) {
+      const float delta = __fmul_rn(__fsub_rn(gm, st.m), c);
+      const float f = ex2(-delta);
+      if (WITH_U) st.u = __fmul_rn(f, __fmaf_rn(-delta, __fadd_rn(st.hi, st.lo), st.u));
+      st.hi = __fmul_rn(st.hi, f);
+      st.lo = __fmul_rn(st.lo, f);
+    }
+    st.m = gm;
+  }
+  float v[8], w[8], d[8];
+  unpack8(q, v);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    d[k] = __fmul_rn(__fsub_rn(v[k], st.m), c);
+    w[k] = ex2(d[k]);
+  }
+  const float gsum = __fadd_rn(__fadd_rn(__fadd_rn(w[0], w[1]), __fadd_rn(w[2], w[3])),
+                               __fadd_rn(__fadd_rn(w[4], w[5]), __fadd_rn(w[6], w[7])));
+  float s, e;
+  two_sum(st.hi, gsum, s, e);
+  st.hi = s;
+  st.lo = __fadd_rn(st.lo, e);
+  if (WITH_U) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) st.u = __fmaf_rn(w[k], d[k], st.u);
+  }
+  return gm;
+}
+
+// ------------------------------------------------------------ shared memory
+struct __align__(16) Smem {
+  // Histogram of 32-bit counts indexed by distance from the max (in keys).
+  struct {
+    uint32_t rel[HB];
+  } hist;
+  uint16_t gmax[SK_ROUNDS][NT];            // bf16 max of each group (the sketch)
+  union {
+    struct {
+      uint4 qdata[NWARP][QCAP];
+      uint32_t qidx[NWARP][QCAP];
+    } q;
+    uint32_t wlist[NWARP][WL];
+  } lists;
   float red[NWARP][4];
-  float bc[8];          // broadcast slots
+  float bc[8];
   uint32_t ured[NWARP][4];
   uint32_t ubc[4];
   DF scan_wtot[NWARP];
   uint32_t scan_wcnt[NWARP];
   float scan_wum[NWARP];
+  DF scan_woff[NWARP];
+  uint32_t scan_woffc[NWARP];
+  float scan_woffu[NWARP];
+  unsigned long long merged_w, merged_u;  // fixed-point sums of the near-zero bin
+  uint32_t merged_n;
+  uint32_t gmin_key;                      // ordered key of the row's smallest value
   int dstar;
   // result of the scan, written by the thread owning the threshold bin
   float r_pb_hi, r_pb_lo, r_um_before, r_w, r_x;
@@ -320,12 +415,379 @@ __device__ void block_sum_u32(uint32_t (&v)[4], Smem& sm, int tid) {
   __syncthreads();
 }
 
+// ------------------------------------------------------ candidate queues
+// Largest of the 8 bf16 values of a packed group (packed bf16x2 max).
+__device__ __forceinline__ float group_max(const uint4 q) {
+  const __nv_bfloat162 mx = __hmax2(__hmax2(as_bf162w(q.x), as_bf162w(q.y)),
+                                    __hmax2(as_bf162w(q.z), as_bf162w(q.w)));
+  return fmaxf(__low2float(mx), __high2float(mx));
+}
+
+// Per-warp queue of groups that hold a candidate.  offer() is called by every
+// lane of the warp in lockstep; process(q, g) expands one queued group.
+struct WarpQueue {
+  uint4* data;
+  uint32_t* idx;
+  uint32_t n;          // warp-uniform fill
+  uint32_t lt_mask;
+  int lane;
+  template <class P>
+  __device__ __forceinline__ void flush(P&& process) {
+    __syncwarp();
+    for (uint32_t i = (uint32_t)lane; i < n; i += 32) process(data[i], idx[i]);
+    __syncwarp();
+    n = 0;
+  }
+  template <class P>
+  __device__ __forceinline__ void offer(const uint4& q, int64_t g, bool cand, P&& process) {
+    const uint32_t b = __ballot_sync(0xFFFFFFFFu, cand);
+    if (b) {
+      if (cand) {
+        const uint32_t pos = n + __popc(b & lt_mask);
+        data[pos] = q;
+        idx[pos] = (uint32_t)g;
+      }
+      n += __popc(b);
+      if (n >= 32u) flush(process);
+    }
+  }
+};
+
+// Expands a queued group: calls f(bits16, element index) for every element
+// with value >= thr.
+template <class F>
+__device__ __forceinline__ void for_candidates(const uint4 q, uint32_t g, int64_t V, float thr,
+                                               F&& f) {
+  const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+  uint32_t mask = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t bits = (w4[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+    if (bf16_val(bits) >= thr && (int64_t)g * 8 + k < V) mask |= 1u << k;
+  }
+  while (mask) {
+    const int k = __ffs(mask) - 1;
+    mask &= mask - 1u;
+    const int h = k >> 1;
+    const uint32_t wsel = h == 0 ? w4[0] : h == 1 ? w4[1] : h == 2 ? w4[2] : w4[3];
+    f((wsel >> (16 * (k & 1))) & 0xFFFFu, (int64_t)g * 8 + k);
+  }
+}
+
+// ---------------------------------------------------------- packed pass 1
+// Pass 1 over a bf16 row with the groups kept packed (four registers each) so
+// that BATCH 16-byte loads per thread are in flight before they are used.
+// Same group order as for_groups (g = tid, tid + NT, ...).  *gmin gets the
+// thread's smallest value when WITH_U is off (-inf detection).
+template <int BATCH, bool WITH_U>
+__device__ __forceinline__ void pass1_packed(const RowBf16& row, int tid, float c, Online& st,
+                                             float& gmin, uint16_t (*sketch)[NT]) {
+  const int V = (int)row.V;   // V <= 2^24
+  const int nfull = V / 8;
+  int g = tid;
+  auto record = [&](int gg, float gm) {
+    if (sketch) sketch[gg / NT][tid] = (uint16_t)(__float_as_uint(gm) >> 16);
+  };
+  if (row.aligned) {
+    const uint4* base = reinterpret_cast<const uint4*>(row.p);
+    for (; g + (BATCH - 1) * NT < nfull; g += BATCH * NT) {
+      uint4 q[BATCH];
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) q[b] = __ldg(base + g + b * NT);
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        float gn = INFINITY;
+        record(g + b * NT, absorb_packed<WITH_U>(st, q[b], c, gn));
+        gmin = fminf(gmin, gn);
+      }
+    }
+  }
+  for (; g < nfull; g += NT) {
+    float gn = INFINITY;
+    record(g, absorb_packed<WITH_U>(st, row.packed(g, nfull), c, gn));
+    gmin = fminf(gmin, gn);
+  }
+  if (g == nfull && V % 8 != 0) {
+    float v[8];
+    const int n = row.scal(g, v);
+    for (int k = 0; k < n; ++k) gmin = fminf(gmin, v[k]);
+    record(g, absorb<8>(st, v, n, c));
+  }
+}
+
+// ------------------------------------------------------------ second pass
+// Counts the tokens with z >= zlo into the distance histogram (bin = ck_m - ck),
+// the near-zero bin into fixed-point sums, and the ties of y ahead of it.
+__device__ __noinline__ uint32_t window_pass(const RowBf16& row, int tid, float zlo, float m, float c,
+                                float inv_t, uint32_t ck_m, uint32_t key_y, int64_t y,
+                                Smem& sm) {
+  const int lane = tid & 31, warp = tid >> 5;
+  const int64_t nfull = row.V / 8;
+  const int64_t ngroups = (row.V + 7) / 8;
+  const int64_t rounds = (ngroups + NT - 1) / NT;
+  WarpQueue wq{sm.lists.q.qdata[warp], sm.lists.q.qidx[warp], 0u, (1u << lane) - 1u, lane};
+  uint32_t tie = 0;
+  auto process = [&](const uint4 q, uint32_t g) {
+    for_candidates(q, g, row.V, zlo, [&](uint32_t bits, int64_t i) {
+      const uint32_t key = okey16(bits);
+      const uint32_t ck = compress_key(key);
+      if (ck == MERGE_LO) {
+        const float dd = __fsub_rn(bf16_val(bits), m);
+        const float w = ex2(__fmul_rn(dd, c));
+        atomicAdd(&sm.merged_w, __float2ull_rn(__fmul_rn(w, 1099511627776.0f)));      // 2^40
+        atomicAdd(&sm.merged_u, __float2ull_rn(__fmul_rn(-__fmul_rn(w, __fmul_rn(dd, inv_t)),
+                                                         4294967296.0f)));                  // 2^32
+        atomicAdd(&sm.merged_n, 1u);
+      } else {
+        atomicAdd(&sm.hist.rel[ck_m - ck], 1u);
+      }
+      if (key == key_y && i < y) ++tie;
+    });
+  };
+  constexpr int B = 4;
+  int64_t r0 = 0;
+  if (row.aligned) {   // whole batches of full groups: plain vector loads
+    const uint4* base = reinterpret_cast<const uint4*>(row.p);
+    for (; (r0 + B - 1) * NT + (NT - 1) < nfull; r0 += B) {
+      uint4 q[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) q[b] = __ldg(base + tid + (r0 + b) * NT);
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+        wq.offer(q[b], tid + (r0 + b) * NT, group_max(q[b]) >= zlo, process);
+    }
+  }
+  for (; r0 < rounds; ++r0) {
+    const int64_t g = tid + r0 * NT;
+    const bool val = g < ngroups;
+    const uint4 q = val ? row.packed(g, nfull) : make_uint4(0u, 0u, 0u, 0u);
+    wq.offer(q, g, val && group_max(q) >= zlo, process);
+  }
+  wq.flush(process);
+  return tie;
+}
+
+// ------------------------------------------------------------ sketch pass
+// The second pass when pass 1 kept the group-max sketch: a group can hold a
+// token with z >= zlo only if its max is >= zlo, so each warp ballots over its
+// sketch entries into a list of candidate group indices and then reloads just
+// those groups (four per lane in flight) and counts their window tokens
+// exactly as window_pass does.
+__device__ __forceinline__ uint32_t sketch_pass(const RowBf16& row, int tid, float zlo, float m, float c,
+                                float inv_t, uint32_t ck_m, uint32_t key_y, int64_t y,
+                                Smem& sm) {
+  const int lane = tid & 31, warp = tid >> 5;
+  const int V = (int)row.V;
+  const int nfull = V / 8;
+  const int ngroups = (V + 7) / 8;
+  const int rounds = (ngroups + NT - 1) / NT;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t* wl = sm.lists.wlist[warp];
+  uint32_t tie = 0;
+  auto expand = [&](const uint4 q, uint32_t g) {
+    for_candidates(q, g, row.V, zlo, [&](uint32_t bits, int64_t i) {
+      const uint32_t key = okey16(bits);
+      const uint32_t ck = compress_key(key);
+      if (ck == MERGE_LO) {
+        const float dd = __fsub_rn(bf16_val(bits), m);
+        const float w = ex2(__fmul_rn(dd, c));
+        atomicAdd(&sm.merged_w, __float2ull_rn(__fmul_rn(w, 1099511627776.0f)));      // 2^40
+        atomicAdd(&sm.merged_u, __float2ull_rn(__fmul_rn(-__fmul_rn(w, __fmul_rn(dd, inv_t)),
+                                                         4294967296.0f)));                  // 2^32
+        atomicAdd(&sm.merged_n, 1u);
+      } else {
+        atomicAdd(&sm.hist.rel[ck_m - ck], 1u);
+      }
+      if (key == key_y && i < y) ++tie;
+    });
+  };
+  auto drain = [&](uint32_t n) {
+    __syncwarp();
+    for (uint32_t i0 = 0; i0 < n; i0 += 128) {
+      uint4 q[4];
+      uint32_t gi[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t i = i0 + b * 32 + lane;
+        gi[b] = i < n ? wl[i] : 0xFFFFFFFFu;
+        if (gi[b] != 0xFFFFFFFFu) q[b] = row.packed(gi[b], nfull);
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if (gi[b] != 0xFFFFFFFFu) expand(q[b], gi[b]);
+    }
+    __syncwarp();
+  };
+  uint32_t wn = 0;    // warp-uniform list fill
+  for (int r = 0; r < rounds; ++r) {
+    const int g = tid + r * NT;
+    const bool cand = g < ngroups && bf16_val(sm.gmax[r][tid]) >= zlo;
+    const uint32_t b = __ballot_sync(0xFFFFFFFFu, cand);
+    if (cand) wl[wn + __popc(b & lt_mask)] = (uint32_t)g;
+    wn += __popc(b);
+    if (wn > (uint32_t)(WL - 32)) {
+      drain(wn);
+      wn = 0;
+    }
+  }
+  drain(wn);
+  return tie;
+}
+
+// ------------------------------------------------------------ bin scan
+// Bins 0..dmax (bin d = compressed key ck_m - d, largest value first): a
+// fixed-order double-float scan for the first bin whose inclusive prefix
+// mass reaches the target.  Bins are split into equal contiguous chunks per
+// thread (one bin per thread while the window has <= 512 bins).  The winner's
+// data lands in sm.r_*; returns false when the window's mass is short.
+__device__ __forceinline__ bool scan_bins(int tid, uint32_t dmax, uint32_t d_merged, uint32_t ck_m, float m,
+                          float c, float inv_t, DF target, Smem& sm, int& dstar_out) {
+  DF mmerged{0.f, 0.f};
+  float umerged = 0.f;
+  uint32_t nmerged = 0u;
+  if (d_merged != 0xFFFFFFFFu) {
+    const double mw = (double)sm.merged_w * (1.0 / 1099511627776.0);
+    mmerged.hi = (float)mw;
+    mmerged.lo = (float)(mw - (double)mmerged.hi);
+    umerged = (float)(-(double)sm.merged_u * (1.0 / 4294967296.0));
+    nmerged = sm.merged_n;
+  }
+  const uint32_t bpt = (dmax + NT) / NT;   // ceil((dmax + 1) / NT)
+  const uint32_t d0 = (uint32_t)tid * bpt;
+  auto bin = [&](uint32_t d, uint32_t& nb, DF& mass, float& um, float& wv, float& xv) {
+    nb = 0u; mass = DF{0.f, 0.f}; um = 0.f; wv = 0.f; xv = 0.f;
+    if (d > dmax) return;
+    if (d == d_merged) {
+      nb = nmerged; mass = mmerged; um = umerged;
+      return;
+    }
+    nb = sm.hist.rel[d];
+    if (nb == 0u) return;
+    const float vv = RowBf16::value_of_key(expand_key(ck_m - d));
+    const float dd = __fsub_rn(vv, m);
+    wv = ex2(__fmul_rn(dd, c));
+    xv = __fmul_rn(dd, inv_t);
+    mass.hi = __fmul_rn((float)nb, wv);
+    um = __fmul_rn(mass.hi, xv);
+  };
+  DF tot{0.f, 0.f};
+  uint32_t tcnt = 0u;
+  float tum = 0.f;
+  if (d0 <= dmax) {
+    for (uint32_t j = 0; j < bpt; ++j) {
+      uint32_t nb; DF ms; float um, wv, xv;
+      bin(d0 + j, nb, ms, um, wv, xv);
+      tot = df_add(tot, ms);
+      tcnt += nb;
+      tum = __fadd_rn(tum, um);
+    }
+  }
+  // exclusive scan of the per-thread totals in thread order
+  const int lane = tid & 31, warp = tid >> 5;
+  DF inc = tot;
+  uint32_t icnt = tcnt;
+  float ium = tum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    DF lft{shfl_up(inc.hi, o), shfl_up(inc.lo, o)};
+    const uint32_t lc = __shfl_up_sync(0xFFFFFFFFu, icnt, o);
+    const float lu = shfl_up(ium, o);
+    if (lane >= o) {
+      inc = df_add(lft, inc);
+      icnt += lc;
+      ium = __fadd_rn(lu, ium);
+    }
+  }
+  DF exc{shfl_up(inc.hi, 1), shfl_up(inc.lo, 1)};
+  uint32_t ecnt = __shfl_up_sync(0xFFFFFFFFu, icnt, 1);
+  float eum = shfl_up(ium, 1);
+  if (lane == 0) { exc = DF{0.f, 0.f}; ecnt = 0u; eum = 0.f; }
+  if (lane == 31) {
+    sm.scan_wtot[warp] = inc;
+    sm.scan_wcnt[warp] = icnt;
+    sm.scan_wum[warp] = ium;
+  }
+  __syncthreads();
+  if (warp == 0) {   // exclusive scan of the warp totals, in warp order
+    DF t = lane < NWARP ? sm.scan_wtot[lane] : DF{0.f, 0.f};
+    uint32_t tc = lane < NWARP ? sm.scan_wcnt[lane] : 0u;
+    float tu = lane < NWARP ? sm.scan_wum[lane] : 0.f;
+#pragma unroll
+    for (int o = 1; o < NWARP; o <<= 1) {
+      DF lft{shfl_up(t.hi, o), shfl_up(t.lo, o)};
+      const uint32_t lc = __shfl_up_sync(0xFFFFFFFFu, tc, o);
+      const float lu = shfl_up(tu, o);
+      if (lane >= o) {
+        t = df_add(lft, t);
+        tc += lc;
+        tu = __fadd_rn(lu, tu);
+      }
+    }
+    DF e{shfl_up(t.hi, 1), shfl_up(t.lo, 1)};
+    uint32_t ec = __shfl_up_sync(0xFFFFFFFFu, tc, 1);
+    float eu = shfl_up(tu, 1);
+    if (lane == 0) { e = DF{0.f, 0.f}; ec = 0u; eu = 0.f; }
+    if (lane < NWARP) {
+      sm.scan_woff[lane] = e;
+      sm.scan_woffc[lane] = ec;
+      sm.scan_woffu[lane] = eu;
+    }
+  }
+  __syncthreads();
+  exc = df_add(sm.scan_woff[warp], exc);
+  ecnt += sm.scan_woffc[warp];
+  eum = __fadd_rn(sm.scan_woffu[warp], eum);
+  // first bin whose inclusive prefix reaches the target; smallest index wins
+  int my_d = -1;
+  DF my_pb{0.f, 0.f};
+  uint32_t my_cb = 0u, my_n = 0u;
+  float my_ub = 0.f, my_w = 0.f, my_x = 0.f;
+  if (d0 <= dmax) {
+    DF P = exc;
+    uint32_t pc = ecnt;
+    float pu = eum;
+    for (uint32_t j = 0; j < bpt; ++j) {
+      uint32_t nb; DF ms; float um, wv, xv;
+      bin(d0 + j, nb, ms, um, wv, xv);
+      const DF Pn = df_add(P, ms);
+      if (nb > 0u && df_ge(Pn, target)) {
+        my_d = (int)(d0 + j);
+        my_pb = P; my_cb = pc; my_ub = pu; my_w = wv; my_x = xv; my_n = nb;
+        break;
+      }
+      P = Pn;
+      pc += nb;
+      pu = __fadd_rn(pu, um);
+    }
+    if (my_d >= 0) atomicMin(&sm.dstar, my_d);
+  }
+  __syncthreads();
+  const int dstar = sm.dstar;
+  if (my_d >= 0 && my_d == dstar) {
+    sm.r_pb_hi = my_pb.hi; sm.r_pb_lo = my_pb.lo;
+    sm.r_cnt_before = my_cb; sm.r_um_before = my_ub;
+    sm.r_w = my_w; sm.r_x = my_x; sm.r_n = my_n;
+  }
+  __syncthreads();
+  dstar_out = dstar;
+  return dstar != 0x7FFFFFFF;
+}
+
+// Bin span of the window z >= zlo: the smallest key it can hold (truncating
+// zlo's fp32 bits to bf16 moves it by less than one bf16 step) to ck_m.
+__device__ __forceinline__ uint32_t window_dmax(float zlo, uint32_t ck_m, bool& merged_in) {
+  const uint32_t k_lo_raw = okey16(__float_as_uint(zlo) >> 16);
+  const uint32_t ck_lo = compress_key(k_lo_raw > 0u ? k_lo_raw - 1u : 0u);
+  merged_in = (ck_lo <= MERGE_LO) && (MERGE_LO <= ck_m);
+  return ck_m - ck_lo;   // ck_lo <= ck_m since zlo < m
+}
+
 // ------------------------------------------------ exact bisection fallback
 // Largest key tau with mass(key >= tau) >= target, then the tie count at tau;
 // every mass is a fixed-order pass over the row.  Results go to the output
 // references (valid on all threads).
 template <class Row>
-__device__ void select_by_bisection(const Row& row, int tid, float m, float c, float inv_t,
+__device__ __noinline__ void select_by_bisection(const Row& row, int tid, float m, float c, float inv_t,
                                     DF target, uint32_t key_y, int64_t y, Smem& sm,
                                     bool& all_tokens, DF& zs, float& us, uint32_t& kstar,
                                     bool& y_in) {
@@ -387,11 +849,52 @@ __device__ void select_by_bisection(const Row& row, int tid, float m, float c, f
   y_in = (key_y > tau) || (key_y == tau && cnt[2] < cneed);
 }
 
+// Threshold-bin bookkeeping shared by the histogram paths: the number of tied
+// tokens needed, retained mass and entropy numerator, k*, membership of y.
+__device__ __forceinline__ void finish_from_scan(const Smem& sm, DF target, int dstar,
+                                                 uint32_t ck_m, uint32_t key_y, uint32_t tie_y,
+                                                 DF& zs, float& us, uint32_t& kstar,
+                                                 bool& y_in) {
+  const DF pb{sm.r_pb_hi, sm.r_pb_lo};
+  const float wt = sm.r_w, xt = sm.r_x;
+  const uint32_t nt = sm.r_n;
+  const float need = df_sub_to_f(target, pb);
+  const float cf = ceilf(__fdiv_rn(need, wt));
+  const uint32_t cneed = cf < 1.f ? 1u : (cf > (float)nt ? nt : (uint32_t)cf);
+  zs = df_add_f(pb, __fmul_rn((float)cneed, wt));
+  us = __fmaf_rn(__fmul_rn((float)cneed, wt), xt, sm.r_um_before);
+  kstar = sm.r_cnt_before + cneed;
+  const uint32_t d_y = ck_m - compress_key(key_y);
+  y_in = (d_y < (uint32_t)dstar) || (d_y == (uint32_t)dstar && tie_y < cneed);
+}
+
+// Sum of w x over the whole row (fixed order), for rows whose nucleus turns out
+// to be the whole vocabulary on the path that skipped it in pass 1.
+__device__ __noinline__ float full_entropy_numerator(const RowBf16& row, int tid, float m, float c,
+                                        float inv_t, Smem& sm) {
+  DF dummy{0.f, 0.f};
+  float u = 0.f;
+  for_groups(row, tid, [&](const float (&v)[8], int n, int64_t) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k < n) {
+        const float dd = __fsub_rn(v[k], m);
+        u = __fmaf_rn(ex2(__fmul_rn(dd, c)), __fmul_rn(dd, inv_t), u);
+      }
+    }
+  });
+  block_sum_df(dummy, u, sm, tid);
+  return u;
+}
+
 // --------------------------------------------------------------- kernel
 template <class Row, bool TOPP>
 __global__ void __launch_bounds__(NT, 2) lpe_kernel(LpeArgs a, float c, float inv_t) {
-  __shared__ Smem sm;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
+  constexpr bool BF = Row::KEYBITS == 16;
+  constexpr bool HIST = TOPP && BF;   // histogram select (else bisection at top_p < 1)
   for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x) {
     Row row;
     row.p = reinterpret_cast<decltype(row.p)>(a.logits) + r * a.ld;
@@ -407,30 +910,41 @@ __global__ void __launch_bounds__(NT, 2) lpe_kernel(LpeArgs a, float c, float in
       }
       continue;
     }
-    const float zy = [&] {
-      float v[Row::E];
-      // the selected logit, read through the same element decoding
-      const int64_t gy = y / Row::E;
-      row.scal(gy, v);
-      return v[y - gy * Row::E];
-    }();
+    const float zy = row.elem(y);    // the selected logit
+    const uint32_t key_y = Row::key(zy);
 
-    // ---- pass 1: online max / sum / entropy numerator
+    // ---- pass 1: online max / sum (/ entropy numerator)
     Online st{-INFINITY, 0.f, 0.f, 0.f};
-    for_groups(row, tid, [&](const float (&v)[Row::E], int n, int64_t) {
-      absorb<Row::E>(st, v, n, c);
-    });
-    st = block_reduce_online(st, c, sm, tid);
+    if constexpr (BF) {
+      float gmin = INFINITY;
+      if constexpr (HIST) {
+        if (tid == 0) sm.gmin_key = 0xFFFFFFFFu;
+        const bool sketch = (a.V + 8 * NT - 1) / (8 * NT) <= SK_ROUNDS;
+        pass1_packed<4, false>(row, tid, c, st, gmin, sketch ? sm.gmax : nullptr);
+        const uint32_t gk = __reduce_min_sync(0xFFFFFFFFu, okey32(__float_as_uint(gmin)));
+        if ((tid & 31) == 0) atomicMin(&sm.gmin_key, gk);
+      } else {
+        pass1_packed<8, true>(row, tid, c, st, gmin, nullptr);
+      }
+    } else {
+      for_groups<TOPP ? 4 : 8>(row, tid, [&](const float (&v)[Row::E], int n, int64_t) {
+        absorb<Row::E>(st, v, n, c);
+      });
+    }
+    st = block_reduce_online(st, c, sm, tid);   // its barriers also publish gmin_key
     const float m = st.m;
     const DF Z{st.hi, st.lo};
     const float zf = __fadd_rn(st.hi, st.lo);
-    if (!(isfinite(zf) && isfinite(st.u) && isfinite(m))) {
+    bool bad = !(isfinite(zf) && isfinite(st.u) && isfinite(m));
+    if constexpr (HIST) bad = bad || isinf(__uint_as_float(okey32_inverse(sm.gmin_key)));
+    if (bad) {
       if (tid == 0) {
         a.out_logprob[r] = NAN;
         a.out_entropy[r] = NAN;
         if (a.out_k) a.out_k[r] = 0;
         if (a.status) atomicOr(a.status, RLK_STATUS_NONFINITE);
       }
+      __syncthreads();
       continue;
     }
     const float x_y = __fdiv_rn(__fsub_rn(zy, m), a.temperature);
@@ -446,188 +960,72 @@ __global__ void __launch_bounds__(NT, 2) lpe_kernel(LpeArgs a, float c, float in
 
     // ---- top_p < 1: nucleus select
     const DF target = df_mul_f(Z, a.top_p);
-    const float L = fmaxf(logf(__fdiv_rn((float)a.V, __fmul_rn(__fsub_rn(1.f, a.top_p), zf))), 0.f) + 0.5f;
-    const float zlo = __fsub_rn(m, __fmul_rn(L, a.temperature));
-    const uint32_t key_y = Row::key(zy);
+    const float one_m_p = __fsub_rn(1.f, a.top_p);
+    // Speculative window depth (units of T), kept only if its own mass reaches
+    // the target; worst-case depth, below which lies less than
+    // V e^-L < (1 - top_p) Z of the mass.
+    const float L_spec = logf(__fdiv_rn(1.f, one_m_p)) + 7.0f;
+    const float L_worst =
+        fmaxf(logf(__fdiv_rn((float)a.V, __fmul_rn(one_m_p, zf))), 0.f) + 0.5f;
 
-    bool all_tokens = false, y_in = false, use_bisect = (Row::KEYBITS != 16);
+    bool all_tokens = false, y_in = false, use_bisect = !HIST;
     DF zs{0.f, 0.f};
     float us = 0.f;
     uint32_t kstar = 0u;
 
-    if constexpr (Row::KEYBITS == 16) {
-     if (!use_bisect) {
+    if constexpr (HIST) {
       const uint32_t ck_m = compress_key(Row::key(m));
-      // smallest key the window can hold: truncating zlo's fp32 bits to bf16
-      // moves it by less than one bf16 step.
-      const uint32_t k_lo_raw = okey16(__float_as_uint(zlo) >> 16);
-      const uint32_t ck_lo = compress_key(k_lo_raw > 0u ? k_lo_raw - 1u : 0u);
-      const uint32_t dmax = ck_m - ck_lo;  // ck_lo <= ck_m since zlo < m
-      if (dmax >= (uint32_t)HB) {
-        use_bisect = true;
-      } else {
-        const bool merged_in = (ck_lo <= MERGE_LO) && (MERGE_LO <= ck_m);
+      bool done = false;
+      // Second pass over the row (served from L2): the speculative window,
+      // then, if its mass falls short, the worst-case window.
+      for (int att = 0; att < 2 && !done && !use_bisect; ++att) {
+        if (att == 0 && !(L_spec < L_worst)) continue;
+        const float L = att == 0 ? L_spec : L_worst;
+        const float zlo = __fsub_rn(m, __fmul_rn(L, a.temperature));
+        bool merged_in;
+        const uint32_t dmax = window_dmax(zlo, ck_m, merged_in);
+        if (dmax >= (uint32_t)HB) { use_bisect = true; break; }
         const uint32_t d_merged = merged_in ? ck_m - MERGE_LO : 0xFFFFFFFFu;
-        for (uint32_t i = tid; i <= dmax; i += NT) sm.hist[i] = 0u;
-        if (tid == 0) sm.dstar = 0x7FFFFFFF;
-        __syncthreads();
-        // ---- pass 2: window histogram (re-read, served from L2)
-        DF mm{0.f, 0.f};      // merged-bin mass
-        float mu = 0.f;       // merged-bin mass * x
-        uint32_t cnt[4] = {0u, 0u, 0u, 0u};  // [0] merged count, [1] ties before y
-        for_groups(row, tid, [&](const float (&v)[Row::E], int n, int64_t g) {
-#pragma unroll
-          for (int k = 0; k < Row::E; ++k) {
-            if (k < n && v[k] >= zlo) {
-              const uint32_t kk = Row::key(v[k]);
-              const uint32_t ck = compress_key(kk);
-              if (ck == MERGE_LO) {
-                const float dd = __fsub_rn(v[k], m);
-                const float w = ex2(__fmul_rn(dd, c));
-                mm = df_add_f(mm, w);
-                mu = __fmaf_rn(w, __fmul_rn(dd, inv_t), mu);
-                cnt[0] += 1u;
-              } else {
-                atomicAdd(&sm.hist[ck_m - ck], 1u);
-              }
-              if (kk == key_y && g * Row::E + k < y) cnt[1] += 1u;
-            }
-          }
-        });
-        if (merged_in) block_sum_df(mm, mu, sm, tid);
-        block_sum_u32(cnt, sm, tid);  // includes a barrier after the histogram
-
-        // ---- scan: chunk totals per thread
-        const uint32_t d0 = (uint32_t)tid * BPT;
-        auto bin = [&](uint32_t d, uint32_t& nb, float& mass_hi, float& mass_lo, float& um,
-                       float& wv, float& xv) {
-          nb = 0u; mass_hi = 0.f; mass_lo = 0.f; um = 0.f; wv = 0.f; xv = 0.f;
-          if (d > dmax) return;
-          if (d == d_merged) {
-            nb = cnt[0]; mass_hi = mm.hi; mass_lo = mm.lo; um = mu;
-            return;
-          }
-          nb = sm.hist[d];
-          if (nb == 0u) return;
-          const float vv = Row::value_of_key(expand_key(ck_m - d));
-          const float dd = __fsub_rn(vv, m);
-          wv = ex2(__fmul_rn(dd, c));
-          xv = __fmul_rn(dd, inv_t);
-          mass_hi = __fmul_rn((float)nb, wv);
-          um = __fmul_rn(mass_hi, xv);
-        };
-        DF tot{0.f, 0.f};
-        uint32_t tcnt = 0u;
-        float tum = 0.f;
-        if (d0 <= dmax) {
-          for (int j = 0; j < BPT; ++j) {
-            uint32_t nb; float mh, ml, um, wv, xv;
-            bin(d0 + j, nb, mh, ml, um, wv, xv);
-            tot = df_add(tot, DF{mh, ml});
-            tcnt += nb;
-            tum = __fadd_rn(tum, um);
-          }
-        }
-        // ---- exclusive scan of chunk totals in thread order
-        const int lane = tid & 31, warp = tid >> 5;
-        DF inc = tot;
-        uint32_t icnt = tcnt;
-        float ium = tum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          DF lft{shfl_up(inc.hi, o), shfl_up(inc.lo, o)};
-          const uint32_t lc = __shfl_up_sync(0xFFFFFFFFu, icnt, o);
-          const float lu = shfl_up(ium, o);
-          if (lane >= o) {
-            inc = df_add(lft, inc);
-            icnt += lc;
-            ium = __fadd_rn(lu, ium);
-          }
-        }
-        DF exc{shfl_up(inc.hi, 1), shfl_up(inc.lo, 1)};
-        uint32_t ecnt = __shfl_up_sync(0xFFFFFFFFu, icnt, 1);
-        float eum = shfl_up(ium, 1);
-        if (lane == 0) { exc = DF{0.f, 0.f}; ecnt = 0u; eum = 0.f; }
-        if (lane == 31) {
-          sm.scan_wtot[warp] = inc;
-          sm.scan_wcnt[warp] = icnt;
-          sm.scan_wum[warp] = ium;
+        for (uint32_t i = tid; i <= dmax; i += NT) sm.hist.rel[i] = 0u;
+        if (tid == 0) {
+          sm.dstar = 0x7FFFFFFF;
+          sm.merged_w = 0ull;
+          sm.merged_u = 0ull;
+          sm.merged_n = 0u;
         }
         __syncthreads();
-        DF woff{0.f, 0.f};
-        uint32_t wcnt = 0u;
-        float wum = 0.f;
-        for (int w = 0; w < warp; ++w) {
-          woff = df_add(woff, sm.scan_wtot[w]);
-          wcnt += sm.scan_wcnt[w];
-          wum = __fadd_rn(wum, sm.scan_wum[w]);
+        uint32_t cnt2[4] = {0u, 0u, 0u, 0u};
+        cnt2[0] = (a.V + 8 * NT - 1) / (8 * NT) <= SK_ROUNDS
+                      ? sketch_pass(row, tid, zlo, m, c, inv_t, ck_m, key_y, y, sm)
+                      : window_pass(row, tid, zlo, m, c, inv_t, ck_m, key_y, y, sm);
+        block_sum_u32(cnt2, sm, tid);  // also the barrier after the histogram
+        int dstar;
+        const bool found = scan_bins(tid, dmax, d_merged, ck_m, m, c, inv_t, target, sm, dstar);
+        if (!found) {
+          if (att == 1) all_tokens = true;   // rounding left the total below top_p
+          continue;
         }
-        exc = df_add(woff, exc);
-        ecnt += wcnt;
-        eum = __fadd_rn(wum, eum);
-        // ---- first bin (in scan order) whose inclusive prefix reaches the
-        // target.  Every thread checks its own bins; the smallest index wins.
-        int my_d = -1;
-        DF my_pb{0.f, 0.f};
-        uint32_t my_cb = 0u, my_n = 0u;
-        float my_ub = 0.f, my_w = 0.f, my_x = 0.f;
-        if (d0 <= dmax) {
-          DF P = exc;
-          uint32_t pc = ecnt;
-          float pu = eum;
-          for (int j = 0; j < BPT; ++j) {
-            uint32_t nb; float mh, ml, um, wv, xv;
-            bin(d0 + j, nb, mh, ml, um, wv, xv);
-            const DF Pn = df_add(P, DF{mh, ml});
-            if (nb > 0u && df_ge(Pn, target)) {
-              my_d = (int)(d0 + j);
-              my_pb = P; my_cb = pc; my_ub = pu; my_w = wv; my_x = xv; my_n = nb;
-              break;
-            }
-            P = Pn;
-            pc += nb;
-            pu = __fadd_rn(pu, um);
-          }
-          if (my_d >= 0) atomicMin(&sm.dstar, my_d);
-        }
-        __syncthreads();
-        const int dstar = sm.dstar;
-        if (my_d >= 0 && my_d == dstar) {
-          sm.r_pb_hi = my_pb.hi; sm.r_pb_lo = my_pb.lo;
-          sm.r_cnt_before = my_cb; sm.r_um_before = my_ub;
-          sm.r_w = my_w; sm.r_x = my_x; sm.r_n = my_n;
-        }
-        __syncthreads();
-        if (dstar == 0x7FFFFFFF) {
-          all_tokens = true;
-        } else if ((uint32_t)dstar == d_merged) {
-          use_bisect = true;
-        } else {
-          const DF pb{sm.r_pb_hi, sm.r_pb_lo};
-          const float wt = sm.r_w, xt = sm.r_x;
-          const uint32_t nt = sm.r_n;
-          const float need = df_sub_to_f(target, pb);
-          const float cf = ceilf(__fdiv_rn(need, wt));
-          const uint32_t cneed = cf < 1.f ? 1u : (cf > (float)nt ? nt : (uint32_t)cf);
-          zs = df_add_f(pb, __fmul_rn((float)cneed, wt));
-          us = __fmaf_rn(__fmul_rn((float)cneed, wt), xt, sm.r_um_before);
-          kstar = sm.r_cnt_before + cneed;
-          const uint32_t d_y = ck_m - compress_key(key_y);
-          y_in = (d_y < (uint32_t)dstar) || (d_y == (uint32_t)dstar && cnt[1] < cneed);
-        }
-        __syncthreads();
+        if ((uint32_t)dstar == d_merged) { use_bisect = true; break; }
+        finish_from_scan(sm, target, dstar, ck_m, key_y, cnt2[0], zs, us, kstar, y_in);
+        done = true;
       }
-     }
+      __syncthreads();
+      if (all_tokens) us = full_entropy_numerator(row, tid, m, c, inv_t, sm);
     }
     if (use_bisect) {
+      all_tokens = false;
       select_by_bisection(row, tid, m, c, inv_t, target, key_y, y, sm, all_tokens, zs, us,
                           kstar, y_in);
+      if (all_tokens) {
+        if constexpr (HIST) us = full_entropy_numerator(row, tid, m, c, inv_t, sm);
+        else us = __fmul_rn(kLn2, st.u);
+      }
     }
     if (tid == 0) {
       float lz, hval;
       if (all_tokens) {
         lz = logf(zf);
-        hval = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, st.u), zf));
+        hval = __fsub_rn(lz, __fdiv_rn(us, zf));
         kstar = (uint32_t)a.V;
         y_in = true;
       } else {
@@ -652,12 +1050,28 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
   const int64_t grid64 = a.T < (int64_t)2 * sm_count() ? a.T : (int64_t)2 * sm_count();
   const dim3 grid((unsigned)grid64), block(NT);
   const bool topp = a.top_p < 1.0f;
+  const size_t smem = sizeof(Smem);
+
+  static std::atomic<int> attr_done{0};
+  if (!attr_done.load()) {
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(lpe_kernel<RowBf16, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(lpe_kernel<RowBf16, false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(lpe_kernel<RowF32, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(lpe_kernel<RowF32, false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return e;
+    attr_done.store(1);
+  }
   if (a.dtype == 0) {
-    if (topp) lpe_kernel<RowBf16, true><<<grid, block, 0, stream>>>(a, c, inv_t);
-    else lpe_kernel<RowBf16, false><<<grid, block, 0, stream>>>(a, c, inv_t);
+    if (topp) lpe_kernel<RowBf16, true><<<grid, block, smem, stream>>>(a, c, inv_t);
+    else lpe_kernel<RowBf16, false><<<grid, block, smem, stream>>>(a, c, inv_t);
   } else {
-    if (topp) lpe_kernel<RowF32, true><<<grid, block, 0, stream>>>(a, c, inv_t);
-    else lpe_kernel<RowF32, false><<<grid, block, 0, stream>>>(a, c, inv_t);
+    if (topp) lpe_kernel<RowF32, true><<<grid, block, smem, stream>>>(a, c, inv_t);
+    else lpe_kernel<RowF32, false><<<grid, block, smem, stream>>>(a, c, inv_t);
   }
   return cudaGetLastError();
 }
