@@ -14,6 +14,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "librlk.so")
 SOURCES = ["rlk_api.cu", "logprob_entropy.cu", "grpo_loss.cu", "lmhead.cu"]
 HEADERS = ["common.cuh", "internal.h"]
+INCLUDES = ["rlk.h", "rlk_debug.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -36,7 +37,7 @@ def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, s) for s in SOURCES + HEADERS] + [os.path.join(INCLUDE, "rlk.h")]
+    deps = [os.path.join(CSRC, s) for s in SOURCES + HEADERS] + [os.path.join(INCLUDE, h) for h in INCLUDES]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
