@@ -28,7 +28,8 @@ NSTATS = 8
 STAT_NAMES = ("loss", "tokens", "clip_low_frac", "clip_high_frac", "tis_mean",
               "tis_capped_frac", "k3_mean", "pg_mean")
 EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logprob_entropy",
-           "rlk_grpo_loss", "rlk_lmhead_logprob")
+           "rlk_grpo_loss", "rlk_lmhead_logprob", "rlk_grpo_loss_noalloc")
+NOALLOC_MAX_SEQ = 16384
 DEBUG_EXPORTS = ("rlk_lmhead_logits_debug",)
 STATUS_TIMEOUT = 0x4
 
@@ -76,6 +77,9 @@ def load(path: str | None = None):
         lib.rlk_lmhead_logits_debug.argtypes = [vp, vp, i64, i64, i64, vp, f32, vp, vp, vp, vp,
                                                 vp, sz, vp]
         lib.rlk_lmhead_logits_debug.restype = ctypes.c_int
+        lib.rlk_grpo_loss_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, f32, f32,
+                                              f32, f32, ctypes.c_int, vp, vp, vp, vp]
+        lib.rlk_grpo_loss_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 

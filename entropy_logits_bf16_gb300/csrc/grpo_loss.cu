@@ -188,3 +188,97 @@ cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace rlk
+
+// ---------------------------------------------------------------------------
+// rlk_grpo_loss_noalloc: the same loss for callers that cannot allocate device
+// memory -- a framework that has reserved the whole device for its own pool
+// (cudaMalloc would fail or take memory the pool counts on), code that runs
+// inside an allocator callback (allocating there would re-enter the
+// allocator), or a latency-critical loop that bans cudaMalloc because it may
+// synchronise the device.  The caller passes inputs and outputs only; the
+// per-sequence partial sums live in the static array below, which every GPU
+// that loads the library holds until the process exits.
+//
+// The kernels write every partial sum and every scalar before reading it, so
+// nothing in the array has to start at zero; the array keeps the last call's
+// contents.  All calls share it: calls whose work overlaps on the GPU (on
+// different streams or from different host threads) race and give wrong
+// results, so callers must serialise them.
+
+#include <atomic>
+
+namespace rlk {
+namespace {
+
+constexpr int kNoallocFloats = RLK_NOALLOC_MAX_SEQ * NP + 4;
+static __device__ __align__(256) float g_noalloc_scratch[kNoallocFloats];
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+float* noalloc_scratch(cudaError_t& err) {
+  static std::atomic<float*> cache[64];
+  int dev = -1;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  float* p = cache[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  err = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+  if (err != cudaSuccess) return nullptr;
+  p = static_cast<float*>(addr);
+  cache[dev].store(p, std::memory_order_release);
+  return p;
+}
+
+}  // namespace
+}  // namespace rlk
+
+extern "C" rlk_status rlk_grpo_loss_noalloc(
+    const float* logp_new, const float* logp_old, const float* logp_rollout,
+    const float* logp_ref, const uint8_t* loss_mask, const float* rewards,
+    const int32_t* seq_offsets, int32_t n_seq, int32_t group_size, int64_t n_tok,
+    float eps_low, float eps_high, float tis_cap, float kl_coef, rlk_agg agg, float* out_loss,
+    float* out_dloss_dlogp_new, float* out_stats, rlk_stream stream) {
+  if (n_seq < 0 || n_seq > RLK_NOALLOC_MAX_SEQ || group_size < 1 || n_seq % group_size != 0 ||
+      n_tok < 0)
+    return RLK_ERR_INVALID_ARG;
+  if (!(isfinite(eps_low) && eps_low >= 0.0f && isfinite(eps_high) && eps_high >= 0.0f))
+    return RLK_ERR_INVALID_ARG;
+  if (!(isfinite(tis_cap) && tis_cap > 0.0f) || !(isfinite(kl_coef) && kl_coef >= 0.0f))
+    return RLK_ERR_INVALID_ARG;
+  if (agg != RLK_AGG_TOKEN_MEAN && agg != RLK_AGG_SEQ_MEAN_TOKEN_MEAN) return RLK_ERR_INVALID_ARG;
+  if (!seq_offsets || !out_loss) return RLK_ERR_INVALID_ARG;
+  if (n_seq > 0 && (!logp_new || !logp_old || !logp_rollout || !logp_ref || !rewards))
+    return RLK_ERR_INVALID_ARG;
+  cudaError_t err;
+  float* scratch = rlk::noalloc_scratch(err);
+  if (!scratch) return RLK_ERR_CUDA;
+  rlk::LossArgs a;
+  a.logp_new = logp_new;
+  a.logp_old = logp_old;
+  a.logp_rollout = logp_rollout;
+  a.logp_ref = logp_ref;
+  a.mask = loss_mask;
+  a.rewards = rewards;
+  a.seq_offsets = seq_offsets;
+  a.n_seq = n_seq;
+  a.group_size = group_size;
+  a.n_tok = n_tok;
+  a.eps_low = eps_low;
+  a.eps_high = eps_high;
+  a.tis_cap = tis_cap;
+  a.kl_coef = kl_coef;
+  a.agg = agg;
+  a.out_loss = out_loss;
+  a.out_grad = out_dloss_dlogp_new;
+  a.out_stats = out_stats;
+  a.workspace = scratch;
+  return rlk::launch_grpo_loss(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}

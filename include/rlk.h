@@ -186,6 +186,38 @@ rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
                          float* out_dloss_dlogp_new, float* out_stats, void* workspace,
                          size_t workspace_bytes, rlk_stream stream);
 
+/* Largest n_seq that rlk_grpo_loss_noalloc accepts. */
+#define RLK_NOALLOC_MAX_SEQ 16384
+
+/*
+ * rlk_grpo_loss_noalloc -- rlk_grpo_loss for callers that cannot allocate
+ * device memory (the pages have no counterpart): a framework that has
+ * reserved the whole device for its own pool, code running inside an
+ * allocator callback, or a latency-critical loop that bans cudaMalloc because
+ * it may synchronise the device.  The caller passes inputs and outputs only.
+ *
+ * Scratch: a static device array of RLK_NOALLOC_MAX_SEQ * 8 + 4 floats
+ * (about 512 KB) inside the library, held by every GPU that loads the library
+ * until the process exits.  The first call on each device looks up the
+ * array's device address (with that device current); make that first call
+ * before any stream capture.  Every call overwrites what it reads, so nothing
+ * needs clearing, and the array keeps the last call's contents.  All calls
+ * share the array: calls whose work overlaps on the GPU (different streams or
+ * host threads) race and give wrong results -- serialise them.
+ *
+ * Arguments, semantics and results: as rlk_grpo_loss without the workspace.
+ * Errors: as rlk_grpo_loss; n_seq > RLK_NOALLOC_MAX_SEQ returns
+ * RLK_ERR_INVALID_ARG; a failed address lookup returns RLK_ERR_CUDA.  Never
+ * calls cudaMalloc, cudaFree or any allocating routine.
+ */
+rlk_status rlk_grpo_loss_noalloc(const float* logp_new, const float* logp_old,
+                                 const float* logp_rollout, const float* logp_ref,
+                                 const uint8_t* loss_mask, const float* rewards,
+                                 const int32_t* seq_offsets, int32_t n_seq, int32_t group_size,
+                                 int64_t n_tok, float eps_low, float eps_high, float tis_cap,
+                                 float kl_coef, rlk_agg agg, float* out_loss,
+                                 float* out_dloss_dlogp_new, float* out_stats, rlk_stream stream);
+
 /*
  * rlk_lmhead_logprob -- the logits path at top_p = 1 fused with the LM-head
  * GEMM: logits = hidden[T, H] * w_vocab[V, H]^T are produced tile by tile in
