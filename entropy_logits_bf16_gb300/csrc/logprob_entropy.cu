@@ -57,11 +57,11 @@
 namespace rlk {
 namespace {
 
-constexpr int NT = 512;
+constexpr int NT = 256;
 constexpr int NWARP = NT / 32;
-constexpr int HB = 8192;         // largest window (bins) the histogram path takes
+constexpr int HB = 4096;         // largest window (bins) the histogram path takes
 constexpr int QCAP = 64;         // per-warp queue of candidate groups (flushed at >= 32)
-constexpr int SK_ROUNDS = 48;    // rows of up to SK_ROUNDS * NT groups keep a group-max sketch
+constexpr int SK_ROUNDS = 76;    // rows of up to SK_ROUNDS * NT groups keep a group-max sketch
 constexpr int WL = 256;          // per-warp list of candidate groups (sketch pass)
 
 // Ordered 16-bit keys of the bf16 values with |z| < 2^-12 (exponent field
@@ -889,7 +889,7 @@ __device__ __noinline__ float full_entropy_numerator(const RowBf16& row, int tid
 
 // --------------------------------------------------------------- kernel
 template <class Row, bool TOPP>
-__global__ void __launch_bounds__(NT, 2) lpe_kernel(LpeArgs a, float c, float inv_t) {
+__global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float inv_t) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
@@ -1047,7 +1047,7 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
   // c = log2(e) / T rounded once; inv_t = 1 / T.
   const float c = (float)(1.4426950408889634 / (double)a.temperature);
   const float inv_t = (float)(1.0 / (double)a.temperature);
-  const int64_t grid64 = a.T < (int64_t)2 * sm_count() ? a.T : (int64_t)2 * sm_count();
+  const int64_t grid64 = a.T < (int64_t)3 * sm_count() ? a.T : (int64_t)3 * sm_count();
   const dim3 grid((unsigned)grid64), block(NT);
   const bool topp = a.top_p < 1.0f;
   const size_t smem = sizeof(Smem);
