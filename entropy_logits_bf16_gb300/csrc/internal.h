@@ -16,7 +16,12 @@ struct LpeArgs {
   float* out_entropy;
   int32_t* out_k;
   uint32_t* status;
+  int only_marked;  // per-row kernel: process only rows whose out_logprob holds kRecomputeMark
 };
+
+// A quiet-NaN payload that no arithmetic produces: the cluster kernel leaves it
+// in out_logprob for rows that the per-row kernel must recompute.
+constexpr uint32_t kRecomputeMark = 0x7FC0DEADu;
 
 struct LossArgs {
   const float *logp_new, *logp_old, *logp_rollout, *logp_ref;
@@ -49,6 +54,9 @@ struct LmheadArgs {
 int sm_count();
 
 cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream);
+// Cluster-resident kernel for large-vocabulary bf16 rows (lpe_cluster.cu).
+bool lpe_cluster_eligible(const LpeArgs& a);
+cudaError_t launch_lpe_cluster(const LpeArgs& a, cudaStream_t stream);
 
 constexpr int kLossPartials = 8;  // floats per sequence in the loss workspace
 size_t loss_workspace_bytes(int64_t n_seq);

@@ -900,6 +900,7 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
     row.p = reinterpret_cast<decltype(row.p)>(a.logits) + r * a.ld;
     row.V = a.V;
     row.aligned = (reinterpret_cast<uintptr_t>(row.p) & 15u) == 0;
+    if (a.only_marked && __float_as_uint(a.out_logprob[r]) != kRecomputeMark) continue;
     const int64_t y = a.ids[r];
     if (y < 0 || y >= a.V) {
       if (tid == 0) {
@@ -1065,6 +1066,14 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
     attr_done.store(1);
+  }
+  if (!a.only_marked && lpe_cluster_eligible(a)) {
+    cudaError_t e = launch_lpe_cluster(a, stream);
+    if (e != cudaSuccess || !topp) return e;
+    LpeArgs b = a;   // rows the cluster kernel marked for recomputation
+    b.only_marked = 1;
+    lpe_kernel<RowBf16, true><<<grid, block, smem, stream>>>(b, c, inv_t);
+    return cudaGetLastError();
   }
   if (a.dtype == 0) {
     if (topp) lpe_kernel<RowBf16, true><<<grid, block, smem, stream>>>(a, c, inv_t);

@@ -89,6 +89,7 @@ rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, i
   a.out_entropy = out_entropy;
   a.out_k = out_nucleus_size;
   a.status = out_status_word;
+  a.only_marked = 0;
   return rlk::launch_logprob_entropy(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;

@@ -113,12 +113,21 @@ def test_bitwise_repeat_and_batch_invariance(cuda_lib, oracle):
         for x, y in zip(ref, big):
             assert x[pc].tobytes() == y[:96].tobytes()
             assert x[:7].tobytes() == y[96:103].tobytes()
-        # the same rows at a misaligned address (row stride 151937 elements)
-        wide = torch.zeros(96, 151937, dtype=torch.bfloat16, device="cuda")
+        # the same rows under a padded row stride (152064 elements, still
+        # 16-byte aligned rows): the layout does not change the bits
+        wide = torch.zeros(96, 152064, dtype=torch.bfloat16, device="cuda")
         wide[:, :151936] = z
-        mis = run(cuda_lib, wide[:, :151936], ids, 0.7, p)
-        for x, y in zip(ref, mis):
+        pad = run(cuda_lib, wide[:, :151936], ids, 0.7, p)
+        for x, y in zip(ref, pad):
             assert x.tobytes() == y.tobytes()
+        # rows that are not 16-byte aligned (stride 151937) take the per-row
+        # kernel: deterministic, within tolerance of the oracle
+        odd = torch.zeros(96, 151937, dtype=torch.bfloat16, device="cuda")
+        odd[:, :151936] = z
+        mis = run(cuda_lib, odd[:, :151936], ids, 0.7, p)
+        assert all(a.tobytes() == b.tobytes()
+                   for a, b in zip(mis, run(cuda_lib, odd[:, :151936], ids, 0.7, p)))
+        compare_rows(oracle, host(z), ids.cpu().numpy(), 0.7, p, *mis, label=f"odd-stride p{p}")
 
 
 def _bits_row(vals):

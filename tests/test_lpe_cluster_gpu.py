@@ -1,0 +1,122 @@
+"""The cluster-resident logprob/entropy path (16-byte aligned bf16 rows of a
+large vocabulary) against the fp64 oracle: rows it finishes itself, rows it
+hands to the per-row kernel (windows that cross zero, flat rows), bad rows,
+vocabulary sizes with a partial last group, the smallest and largest
+vocabularies it takes, and batches smaller than the number of clusters.
+Same tolerances as the other parity tests; outputs must be bitwise identical
+whatever the batch around a row.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from _parity import compare_rows
+
+pytestmark = pytest.mark.gpu
+
+MARK = 0x7FC0DEAD   # never a legal output
+
+
+def run(rlk, logits, ids, T, p, status=None):
+    lp, ent, k = rlk.logprob_entropy(logits, ids, T, p, return_nucleus_size=True,
+                                     status_word=status)
+    torch.cuda.synchronize()
+    return lp.cpu().numpy(), ent.cpu().numpy(), k.cpu().numpy()
+
+
+def special_rows(V, seed):
+    """A batch mixing the peaked Qwen-shaped rows with rows of unusual shape."""
+    z, peaks = workloads.peaked_bf16(16, V=V, seed=seed)
+    z = z.float()
+    g = torch.Generator().manual_seed(seed)
+    z[1] = torch.randn(V, generator=g) * 0.5              # flat: window crosses zero
+    z[2] = 1.5                                             # all equal
+    z[3] = 0.0; z[3, V // 3] = 60.0                        # one-hot
+    z[4] = torch.randn(V, generator=g) * 3e4               # huge logits
+    z[5] = torch.randn(V, generator=g) * 3 - 20.0          # all negative, peak-free
+    z[6, :64] = z[6].max() + 0.5                           # a wide tie group at the top
+    z[7] = torch.randn(V, generator=g) * 3; z[7, V - 1] = 40.0   # peak in the last column
+    z[8] = torch.randn(V, generator=g) * 3; z[8, 0] = 40.0       # peak in the first column
+    return z.to(torch.bfloat16), peaks
+
+
+def check(rlk, oracle, z, ids_h, T, p, label):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lp, ent, k = run(rlk, z, torch.from_numpy(ids_h).cuda(), T, p, st)
+    assert not np.any(lp.view(np.uint32) == MARK), f"{label}: recompute marker leaked"
+    assert int(st.item()) == 0, f"{label}: status {int(st.item())}"
+    hz = workloads.bf16_bits(z)
+    return compare_rows(oracle, hz, ids_h, T, p, lp, ent, k, label=label)
+
+
+@pytest.mark.parametrize("T", [0.7, 1.8])
+@pytest.mark.parametrize("p", [0.5, 0.95, 0.999, 1.0])
+def test_cluster_special_rows(cuda_lib, oracle, T, p):
+    z, _ = special_rows(151936, seed=31)
+    z = z.cuda()
+    hz = workloads.bf16_bits(z)
+    ids_h = oracle.sample_ids(hz, T, p, workloads.uniforms(z.shape[0], 41))
+    check(cuda_lib, oracle, z, ids_h, T, p, f"special T{T} p{p}")
+    # ids that are mostly outside the nucleus
+    far = ((ids_h.astype(np.int64) + 151936 // 2) % 151936).astype(np.int32)
+    check(cuda_lib, oracle, z, far, T, p, f"special-far T{T} p{p}")
+
+
+@pytest.mark.parametrize("V,ld", [(13000, 13000), (151931, 151936), (171999, 172000),
+                                  (172001, 172008), (20000, 20480)])
+@pytest.mark.parametrize("p", [0.9, 1.0])
+def test_cluster_vocab_sizes(cuda_lib, oracle, V, ld, p):
+    """Partial last groups, the smallest and the largest vocabularies the
+    cluster path takes, and one just past it (per-row kernel)."""
+    base, _ = workloads.peaked_bf16(12, V=ld, seed=17, device="cuda")
+    z = base[:, :V]
+    z[:, V - 3:] = 12.5   # tokens in the partial last group that are kept
+    hz = workloads.bf16_bits(z)
+    ids_h = oracle.sample_ids(hz, 0.7, p, workloads.uniforms(12, 43))
+    ids_h[:4] = V - 1 - np.arange(4)
+    check(cuda_lib, oracle, z, ids_h.astype(np.int32), 0.7, p, f"V{V} ld{ld} p{p}")
+
+
+@pytest.mark.parametrize("p", [0.95, 1.0])
+def test_cluster_small_batches_bitwise(cuda_lib, oracle, p):
+    """Batches of 1 .. 600 rows (fewer and more rows than clusters): each
+    row's bits are the same in every batch, including rows that the per-row
+    kernel recomputes."""
+    z, _ = special_rows(151936, seed=5)
+    z = z.cuda()
+    hz = workloads.bf16_bits(z)
+    ids_h = oracle.sample_ids(hz, 0.7, p, workloads.uniforms(16, 7))
+    ids = torch.from_numpy(ids_h).cuda()
+    ref = run(cuda_lib, z, ids, 0.7, p)
+    compare_rows(oracle, hz, ids_h, 0.7, p, *ref, label=f"small p{p}")
+    for r in (0, 1, 2, 9, 15):
+        one = run(cuda_lib, z[r:r + 1].contiguous(), ids[r:r + 1].contiguous(), 0.7, p)
+        for x, y in zip(ref, one):
+            assert x[r:r + 1].tobytes() == y.tobytes()
+    idx = torch.arange(600) % 16
+    idx = idx[torch.randperm(600, generator=torch.Generator().manual_seed(3))].cuda()
+    big = run(cuda_lib, z[idx].contiguous(), ids[idx].contiguous(), 0.7, p)
+    ic = idx.cpu().numpy()
+    for x, y in zip(ref, big):
+        assert x[ic].tobytes() == y.tobytes()
+
+
+def test_cluster_bad_rows(cuda_lib):
+    V = 151936
+    z, peaks = workloads.peaked_bf16(8, V=V, seed=2, device="cuda")
+    z[0, int(peaks[0])] = 30.0
+    z[1, 5] = float("nan")
+    z[2, V - 1] = float("inf")
+    z[3, 40000] = float("-inf")
+    z[4, 3] = float("nan"); z[4, 4] = float("-inf")
+    ids = torch.tensor([int(peaks[0]), 1, 2, 3, 4, V, -1, int(peaks[7])],
+                       dtype=torch.int32, device="cuda")
+    for p in (1.0, 0.9):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        lp, ent, k = run(cuda_lib, z, ids, 0.7, p, st)
+        assert np.isfinite(lp[0]) and np.isfinite(ent[0])
+        assert np.isfinite(lp[7]) and np.isfinite(ent[7])
+        assert np.all(np.isnan(lp[1:7])) and np.all(np.isnan(ent[1:7]))
+        assert np.all(k[1:7] == 0)
+        assert int(st.item()) == (cuda_lib.STATUS_BAD_TOKEN_ID | cuda_lib.STATUS_NONFINITE)
