@@ -79,6 +79,7 @@ struct __align__(16) CSmem {
   float4 wpart[NSLOT][CL][NWC];    // every warp's sums, pushed to the row's finishing CTA
   uint4 wcta[NSLOT][CL];           // every CTA's (max key, min key), pushed likewise
   uint2 wmax[2][NWC];              // this CTA's warps' (max key, min key)
+  unsigned long long wpeer[2][CL][NWC];   // every warp's (row, max key), pushed to all CTAs
   uint32_t hist[NSLOT][HBC / 2];   // this CTA's window counts, two 16-bit bins a word
   uint32_t merged[HBC];            // the finishing warp's counts for the whole row
   uint16_t queue[NWC][JS * 32];    // per-warp candidate groups of one sub-chunk
@@ -122,11 +123,41 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
                "f"(v.z), "f"(v.w)
                : "memory");
 }
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(uint32_t addr) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Waits for the mbarrier phase of the given parity, suspending in hardware
+// (up to ~1 ms a try) rather than polling; gives up (returning false and
+// raising *abort) after about 2^31 clock cycles, or when *abort is raised.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(1000000u)
+        : "memory");
+    if (ok) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > (1ll << 31)) {
+      *abort = 1;
+      return false;
+    }
+  }
 }
 
 __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
@@ -496,7 +527,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
 #pragma unroll
     for (int j = 0; j < JMAX; ++j) {
       if (j % JS == 0 && j / JS < nsub) {
-        if (!mbar_wait_bounded(smem_u32(&sm.full[j / JS]), ph, &sm.abort) && a.status)
+        if (!mbar_wait_sleep(smem_u32(&sm.full[j / JS]), ph, &sm.abort) && a.status)
           atomicOr(a.status, RLK_STATUS_TIMEOUT);
       }
       const int g = tid + j * NTC;
@@ -536,9 +567,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
     // ---- the reference exponent; top_p < 1: this CTA's max and its window
     float E;
     uint32_t key_mq = 0u, key_lo = 0u;
+    bool win_empty = false;
     float zlo_k = 0.f;
     if (TOPP) {
       const uint32_t kn = __reduce_min_sync(0xFFFFFFFFu, okey32(__float_as_uint(nt)));
+      // Offer this warp's max to every CTA: a larger max than this CTA's own
+      // raises its window floor (any value between the CTA max and the row
+      // max gives a window that holds the row's; the finishing warp reads only
+      // the row window's bins, so what arrives in time does not change them).
+      if (lane < CL)
+        st_cluster_u64(map_rank(smem_u32(&sm.wpeer[ph][q][warp]), (uint32_t)lane),
+                       ((unsigned long long)(uint32_t)r << 32) | kx);
       // This row's counts go to buffer `slot`, last read two rows ago (every
       // CTA has passed the barrier that follows that read): clear it.
       for (int i = tid; i < HBC / 2; i += NTC) sm.hist[slot][i] = 0u;
@@ -547,7 +586,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
         sm.wmax[ph][warp] = make_uint2(kx, kn);
         mbar_arrive(smem_u32(&sm.cmax_bar));
       }
-      if (!mbar_wait_bounded(smem_u32(&sm.cmax_bar), ph, &sm.abort) && a.status)
+      if (!mbar_wait_sleep(smem_u32(&sm.cmax_bar), ph, &sm.abort) && a.status)
         atomicOr(a.status, RLK_STATUS_TIMEOUT);
       uint32_t km = lane < NWC ? sm.wmax[ph][lane].x : 0u;
       uint32_t kmn = lane < NWC ? sm.wmax[ph][lane].y : 0xFFFFFFFFu;
@@ -555,23 +594,43 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
       kmn = __reduce_min_sync(0xFFFFFFFFu, kmn);
       const float mq = __uint_as_float(okey32_inverse(km));
       E = __fmul_rn(mq, c);
+      // The largest warp max of this row that has reached this CTA so far.
+      uint32_t kpeer = km;
+      {
+        const uint32_t wp = smem_u32(&sm.wpeer[ph][0][0]);
+        const unsigned long long a0 = ld_relaxed_u64(wp + 8u * lane);
+        if ((uint32_t)(a0 >> 32) == (uint32_t)r) kpeer = max(kpeer, (uint32_t)a0);
+        if (lane + 32 < CL * NWC) {
+          const unsigned long long a1 = ld_relaxed_u64(wp + 8u * (lane + 32));
+          if ((uint32_t)(a1 >> 32) == (uint32_t)r) kpeer = max(kpeer, (uint32_t)a1);
+        }
+        kpeer = __reduce_max_sync(0xFFFFFFFFu, kpeer);
+      }
+      const float mfloor = __uint_as_float(okey32_inverse(kpeer));
       if (warp == 0 && lane == 0)
         st_cluster_v4(map_rank(smem_u32(&sm.wcta[slot][q]), frank),
                       make_float4(__uint_as_float(okey16(__float_as_uint(mq) >> 16)),
                                   __uint_as_float(kmn), 0.f, 0.f));
       // Window of this CTA: z >= mq - L T, at most HBC keys below its max (the
       // row's window, which is what the finishing warp reads, lies inside).
-      const float zlo = __fsub_rn(mq, __fmul_rn(L_spec, a.temperature));
+      const float zlo = __fsub_rn(mfloor, __fmul_rn(L_spec, a.temperature));
       key_mq = okey16(__float_as_uint(mq) >> 16);
       const uint32_t kl = okey16(__float_as_uint(zlo) >> 16);
       key_lo = kl > 0u ? kl - 1u : 0u;
-      if (key_lo > key_mq || key_mq - key_lo >= (uint32_t)HBC)
-        key_lo = key_mq > (uint32_t)(HBC - 1) ? key_mq - (uint32_t)(HBC - 1) : 0u;
-      zlo_k = value_of_key(key_lo);
+      if (key_lo > key_mq) {
+        win_empty = true;   // every token of this CTA lies below the row's window
+        zlo_k = INFINITY;
+      } else {
+        if (key_mq - key_lo >= (uint32_t)HBC)
+          key_lo = key_mq > (uint32_t)(HBC - 1) ? key_mq - (uint32_t)(HBC - 1) : 0u;
+        zlo_k = value_of_key(key_lo);
+      }
     } else {
       E = __fmul_rn(__uint_as_float(okey32_inverse(kx)), c);
     }
     const uint32_t key_y = okey16(__float_as_uint(zy) >> 16);
+    const uint32_t dmq = win_empty ? 0u : key_mq - key_lo;   // window: idx = key_mq - key <= dmq
+    const int32_t ycol = (int32_t)(y - col0);         // y's column within this CTA's chunk
 
     // ---- A1: S = sum 2^d (and U = sum 2^d d), d = fma(z, c, -E); window counts
     const float2 nE2 = make_float2(-E, -E);
@@ -627,10 +686,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
           for (uint32_t en = (uint32_t)lane >> 3; en < qn; en += 4) {
             const int g = sm.queue[warp][en];
             const uint32_t kk = okey16(bufh[g * 8 + k]);
-            if (kk >= key_lo && kk <= key_mq) {
-              const uint32_t idx = key_mq - kk;
-              atomicAdd(&hist[idx >> 1], 1u << (16u * (idx & 1u)));
-              if (kk == key_y && col0 + (int64_t)g * 8 + k < y) ++tie;
+            const uint32_t idx = key_mq - kk;
+            if (idx <= dmq) {
+              atomicAdd(&hist[idx >> 1], 1u << ((idx & 1u) << 4));
+              if (kk == key_y && g * 8 + k < ycol) ++tie;
             }
           }
         }
@@ -654,10 +713,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
           if (!TOPP) u2.x = __fmaf_rn(w, d, u2.x);
           if (TOPP) {
             const uint32_t kk = okey16(__float_as_uint(tv[k]) >> 16);
-            if (kk >= key_lo && kk <= key_mq) {
-              const uint32_t idx = key_mq - kk;
-              atomicAdd(&hist[idx >> 1], 1u << (16u * (idx & 1u)));
-              if (kk == key_y && col0 + (int64_t)gfull * 8 + k < y) ++tie;
+            const uint32_t idx = key_mq - kk;
+            if (!win_empty && idx <= dmq) {
+              atomicAdd(&hist[idx >> 1], 1u << ((idx & 1u) << 4));
+              if (kk == key_y && gfull * 8 + k < ycol) ++tie;
             }
           }
         }
