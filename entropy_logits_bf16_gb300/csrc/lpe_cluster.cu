@@ -524,23 +524,36 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
     uint32_t sk[(JMAX + 1) / 2];
 #pragma unroll
     for (int j = 0; j < (JMAX + 1) / 2; ++j) sk[j] = 0u;
-#pragma unroll
-    for (int j = 0; j < JMAX; ++j) {
-      if (j % JS == 0 && j / JS < nsub) {
-        if (!mbar_wait_sleep(smem_u32(&sm.full[j / JS]), ph, &sm.abort) && a.status)
-          atomicOr(a.status, RLK_STATUS_TIMEOUT);
+    auto a0_group = [&](const uint4 v, const int j) {
+      if (TOPP) {
+        const __nv_bfloat162 gm = __hmax2(__hmax2(bf2(v.x), bf2(v.y)), __hmax2(bf2(v.z), bf2(v.w)));
+        mx2 = __hmax2(mx2, gm);
+        mn2 = __hmin2(mn2, __hmin2(__hmin2(bf2(v.x), bf2(v.y)), __hmin2(bf2(v.z), bf2(v.w))));
+        const uint32_t gw = *reinterpret_cast<const uint32_t*>(&gm);
+        sk[j >> 1] |= (__float_as_uint(fmaxf(bf16_lo(gw), bf16_hi(gw))) >> 16) << (16 * (j & 1));
+      } else {
+        mx2 = __hmax2(__hmax2(mx2, bf2(v.x)), __hmax2(bf2(v.y), __hmax2(bf2(v.z), bf2(v.w))));
       }
-      const int g = tid + j * NTC;
-      if (g < gfull) {
-        const uint4 v = bufv[g];
-        if (TOPP) {
-          const __nv_bfloat162 gm = __hmax2(__hmax2(bf2(v.x), bf2(v.y)), __hmax2(bf2(v.z), bf2(v.w)));
-          mx2 = __hmax2(mx2, gm);
-          mn2 = __hmin2(mn2, __hmin2(__hmin2(bf2(v.x), bf2(v.y)), __hmin2(bf2(v.z), bf2(v.w))));
-          const uint32_t gw = *reinterpret_cast<const uint32_t*>(&gm);
-          sk[j >> 1] |= (__float_as_uint(fmaxf(bf16_lo(gw), bf16_hi(gw))) >> 16) << (16 * (j & 1));
+    };
+#pragma unroll
+    for (int s = 0; s < NSUB; ++s) {
+      if (s < nsub) {
+        if (!mbar_wait_sleep(smem_u32(&sm.full[s]), ph, &sm.abort) && a.status)
+          atomicOr(a.status, RLK_STATUS_TIMEOUT);
+        const int J1 = (s * JS + JS < JMAX) ? s * JS + JS : JMAX;
+        if (J1 * NTC <= gfull) {   // every thread's groups of this sub-chunk are whole
+          uint4 v[JS];
+#pragma unroll
+          for (int jj = 0; jj < JS; ++jj)
+            if (s * JS + jj < JMAX) v[jj] = bufv[tid + (s * JS + jj) * NTC];
+#pragma unroll
+          for (int jj = 0; jj < JS; ++jj)
+            if (s * JS + jj < JMAX) a0_group(v[jj], s * JS + jj);
         } else {
-          mx2 = __hmax2(__hmax2(mx2, bf2(v.x)), __hmax2(bf2(v.y), __hmax2(bf2(v.z), bf2(v.w))));
+#pragma unroll
+          for (int jj = 0; jj < JS; ++jj)
+            if (s * JS + jj < JMAX && tid + (s * JS + jj) * NTC < gfull)
+              a0_group(bufv[tid + (s * JS + jj) * NTC], s * JS + jj);
         }
       }
     }
@@ -643,35 +656,52 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
       if (s < nsub) {
         float2 sacc = make_float2(0.f, 0.f);
         uint32_t qn = 0u;   // warp-uniform queue fill
-#pragma unroll
-        for (int jj = 0; jj < JS; ++jj) {
-          const int j = s * JS + jj;
-          if (j >= JMAX) break;
-          const int g = tid + j * NTC;
-          const bool valid = g < gfull;
-          if (valid) {
-            const uint4 v = bufv[g];
-            const float2 d0 = __ffma2_rn(bf16x2_to_f2(v.x), c2, nE2);
-            const float2 d1 = __ffma2_rn(bf16x2_to_f2(v.y), c2, nE2);
-            const float2 d2 = __ffma2_rn(bf16x2_to_f2(v.z), c2, nE2);
-            const float2 d3 = __ffma2_rn(bf16x2_to_f2(v.w), c2, nE2);
-            const float2 w0 = make_float2(ex2(d0.x), ex2(d0.y));
-            const float2 w1 = make_float2(ex2(d1.x), ex2(d1.y));
-            const float2 w2 = make_float2(ex2(d2.x), ex2(d2.y));
-            const float2 w3 = make_float2(ex2(d3.x), ex2(d3.y));
-            sacc = __fadd2_rn(sacc, __fadd2_rn(__fadd2_rn(w0, w1), __fadd2_rn(w2, w3)));
-            if (!TOPP) {
-              u2 = __ffma2_rn(w0, d0, u2);
-              u2 = __ffma2_rn(w1, d1, u2);
-              u2 = __ffma2_rn(w2, d2, u2);
-              u2 = __ffma2_rn(w3, d3, u2);
-            }
+        auto a1_group = [&](const uint4 v) {
+          const float2 d0 = __ffma2_rn(bf16x2_to_f2(v.x), c2, nE2);
+          const float2 d1 = __ffma2_rn(bf16x2_to_f2(v.y), c2, nE2);
+          const float2 d2 = __ffma2_rn(bf16x2_to_f2(v.z), c2, nE2);
+          const float2 d3 = __ffma2_rn(bf16x2_to_f2(v.w), c2, nE2);
+          const float2 w0 = make_float2(ex2(d0.x), ex2(d0.y));
+          const float2 w1 = make_float2(ex2(d1.x), ex2(d1.y));
+          const float2 w2 = make_float2(ex2(d2.x), ex2(d2.y));
+          const float2 w3 = make_float2(ex2(d3.x), ex2(d3.y));
+          sacc = __fadd2_rn(sacc, __fadd2_rn(__fadd2_rn(w0, w1), __fadd2_rn(w2, w3)));
+          if (!TOPP) {
+            u2 = __ffma2_rn(w0, d0, u2);
+            u2 = __ffma2_rn(w1, d1, u2);
+            u2 = __ffma2_rn(w2, d2, u2);
+            u2 = __ffma2_rn(w3, d3, u2);
           }
+        };
+        auto enqueue = [&](const int j, const bool valid) {   // top_p < 1: candidate groups
+          const int g = tid + j * NTC;
+          const bool cand = valid && bf16_val((sk[j >> 1] >> (16 * (j & 1))) & 0xFFFFu) >= zlo_k;
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, cand);
+          if (cand) sm.queue[warp][qn + __popc(bal & lt_mask)] = (uint16_t)g;
+          qn += __popc(bal);
+        };
+        const int J1 = (s * JS + JS < JMAX) ? s * JS + JS : JMAX;
+        if (J1 * NTC <= gfull) {   // every thread's groups of this sub-chunk are whole
+          uint4 v[JS];
+#pragma unroll
+          for (int jj = 0; jj < JS; ++jj)
+            if (s * JS + jj < JMAX) v[jj] = bufv[tid + (s * JS + jj) * NTC];
+#pragma unroll
+          for (int jj = 0; jj < JS; ++jj)
+            if (s * JS + jj < JMAX) a1_group(v[jj]);
           if (TOPP) {
-            const bool cand = valid && bf16_val((sk[j >> 1] >> (16 * (j & 1))) & 0xFFFFu) >= zlo_k;
-            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, cand);
-            if (cand) sm.queue[warp][qn + __popc(bal & lt_mask)] = (uint16_t)g;
-            qn += __popc(bal);
+#pragma unroll
+            for (int jj = 0; jj < JS; ++jj)
+              if (s * JS + jj < JMAX) enqueue(s * JS + jj, true);
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < JS; ++jj) {
+            if (s * JS + jj < JMAX) {
+              const bool valid = tid + (s * JS + jj) * NTC < gfull;
+              if (valid) a1_group(bufv[tid + (s * JS + jj) * NTC]);
+              if (TOPP) enqueue(s * JS + jj, valid);
+            }
           }
         }
         float t, e;
