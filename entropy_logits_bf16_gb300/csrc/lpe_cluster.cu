@@ -358,6 +358,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
     sm.abort = 0;
     fence_mbar_init();
   }
+  // Shared memory keeps whatever an earlier launch left: the row-tagged warp
+  // maxima start with a tag no row has (the first cluster barrier orders this
+  // before any peer's push).
+  for (int i = tid; i < 2 * CL * NWC; i += blockDim.x) (&sm.wpeer[0][0][0])[i] = ~0ull;
   __syncthreads();
   if (tid == 0 && r0 < a.T)
     for (int s = 0; s < nsub; ++s) issue_sub(r0, s);
@@ -778,7 +782,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
 }  // namespace
 
 bool lpe_cluster_eligible(const LpeArgs& a) {
-  if (a.dtype != 0) return false;
+  if (a.dtype != 0 || a.T >= 0xFFFFFFFFll) return false;   // rows are tagged with 32 bits
   if ((reinterpret_cast<uintptr_t>(a.logits) & 15u) != 0 || (a.ld & 7) != 0) return false;
   const int64_t cw = (((a.V + CL - 1) / CL) + 7) & ~int64_t(7);
   if (a.V - (CL - 1) * cw < 8 * NTC) return false;    // every CTA gets a sizeable chunk
