@@ -325,7 +325,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
   CSmem& sm = *reinterpret_cast<CSmem*>(smem_raw);
   uint8_t* buf = smem_raw + ((sizeof(CSmem) + 127) & ~size_t(127));
   const uint4* bufv = reinterpret_cast<const uint4*>(buf);
-  const uint16_t* bufh = reinterpret_cast<const uint16_t*>(buf);
   const uint32_t buf_s = smem_u32(buf);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t q = cluster_rank();
@@ -713,17 +712,33 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
         acc.hi = t;
         acc.lo = __fadd_rn(acc.lo, e);
         if (TOPP && qn != 0u) {
-          // Expand the queued groups with every lane busy (lane = 8 entry +
-          // column) into this CTA's window counts.
+          // Count the queued groups' window tokens: one lane per group, an
+          // 8-bit mask of its tokens >= zlo_k from packed bf16 compares, one
+          // atomic per set bit.
           __syncwarp();
-          const int k = lane & 7;
-          for (uint32_t en = (uint32_t)lane >> 3; en < qn; en += 4) {
-            const int g = sm.queue[warp][en];
-            const uint32_t kk = okey16(bufh[g * 8 + k]);
-            const uint32_t idx = key_mq - kk;
-            if (idx <= dmq) {
-              atomicAdd(&hist[idx >> 1], 1u << ((idx & 1u) << 4));
-              if (kk == key_y && g * 8 + k < ycol) ++tie;
+          const __nv_bfloat162 z2 = __float2bfloat162_rn(zlo_k);   // zlo_k is a bf16 value
+          for (uint32_t e0 = 0; e0 < qn; e0 += 32) {
+            const uint32_t e = e0 + (uint32_t)lane;
+            const bool act = e < qn;
+            const int g = act ? (int)sm.queue[warp][e] : 0;
+            const uint4 v = act ? bufv[g] : make_uint4(0u, 0u, 0u, 0u);
+            uint32_t msk = 0u;
+            if (act)
+              msk = (__hge2_mask(bf2(v.x), z2) & 0x00010001u) |
+                    ((__hge2_mask(bf2(v.y), z2) & 0x00010001u) << 1) |
+                    ((__hge2_mask(bf2(v.z), z2) & 0x00010001u) << 2) |
+                    ((__hge2_mask(bf2(v.w), z2) & 0x00010001u) << 3);
+            while (msk != 0u) {
+              const int b = __ffs(msk) - 1;   // bit b: word b & 3, high half if b >= 16
+              msk &= msk - 1u;
+              const int wi = b & 3, hi = b >> 4;
+              const uint32_t wd = wi == 0 ? v.x : (wi == 1 ? v.y : (wi == 2 ? v.z : v.w));
+              const uint32_t kk = okey16(hi ? (wd >> 16) : wd);
+              const uint32_t idx = key_mq - kk;
+              if (idx <= dmq) {
+                atomicAdd(&hist[idx >> 1], 1u << ((idx & 1u) << 4));
+                if (kk == key_y && g * 8 + 2 * wi + hi < ycol) ++tie;
+              }
             }
           }
         }
