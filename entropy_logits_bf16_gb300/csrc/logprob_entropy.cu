@@ -332,6 +332,7 @@ struct __align__(16) Smem {
   unsigned long long merged_w, merged_u;  // fixed-point sums of the near-zero bin
   uint32_t merged_n;
   uint32_t gmin_key;                      // ordered key of the row's smallest value
+  uint32_t marked[NWARP];                 // recompute pass: which of the next NT rows are marked
   int dstar;
   // result of the scan, written by the thread owning the threshold bin
   float r_pb_hi, r_pb_lo, r_um_before, r_w, r_x;
@@ -895,12 +896,24 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
   const int tid = threadIdx.x;
   constexpr bool BF = Row::KEYBITS == 16;
   constexpr bool HIST = TOPP && BF;   // histogram select (else bisection at top_p < 1)
-  for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x) {
+  int64_t i_row = 0;   // this CTA's row count (the recompute pass reads its marks NT at a time)
+  for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x, ++i_row) {
+    if (a.only_marked) {
+      const int slot = (int)(i_row % NT);
+      if (slot == 0) {
+        __syncthreads();
+        const int64_t rr = r + (int64_t)tid * gridDim.x;
+        const bool mk = rr < a.T && __float_as_uint(a.out_logprob[rr]) == kRecomputeMark;
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, mk);
+        if ((tid & 31) == 0) sm.marked[tid >> 5] = bal;
+        __syncthreads();
+      }
+      if (((sm.marked[slot >> 5] >> (slot & 31)) & 1u) == 0u) continue;
+    }
     Row row;
     row.p = reinterpret_cast<decltype(row.p)>(a.logits) + r * a.ld;
     row.V = a.V;
     row.aligned = (reinterpret_cast<uintptr_t>(row.p) & 15u) == 0;
-    if (a.only_marked && __float_as_uint(a.out_logprob[r]) != kRecomputeMark) continue;
     const int64_t y = a.ids[r];
     if (y < 0 || y >= a.V) {
       if (tid == 0) {
