@@ -1,13 +1,18 @@
 """Benchmark: tokens/s of top-p logprob + entropy at V=151936 bf16, and the
 fraction of the HBM roofline the kernel reaches.
 
-One step = one pass of the hot path (rlk_logprob_entropy: pass 1 online
-max/log-sum-exp/entropy, nucleus select, renormalisation) over one batch of
-synthetic Qwen3-8B-shaped logits: T=4096 rows, V=151936 bf16,
-temperature 0.7, top_p 0.95 (inputs 1.24 GB, larger than L2, so no flush is
-needed between steps).
+One step = one pass of the hot path over one batch of synthetic
+Qwen3-8B-shaped logits (T=4096 rows, V=151936 bf16, temperature 0.7,
+top_p 0.95; inputs 1.24 GB, larger than L2, so no flush is needed between
+steps): rlk_logprob_entropy (max / log-sum-exp / entropy, nucleus select,
+renormalisation) and then rlk_grpo_loss on the step's log-probs (64 responses
+x 64 tokens in groups of 8).  The roofline figure is for the
+rlk_logprob_entropy call, timed with its own events inside the step.
 
-  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--op logits|lmhead]
+
+--op lmhead times the fused LM-head instead (its own metric and a tensor
+roofline); the default line is the benchmark's.
 
 Rows are independent, so N > 1 (one process per GPU via torchrun) runs N
 replicas with no collective on the data path: weak scaling.  ``--impl
@@ -199,12 +204,255 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+GRPO_SEQ, GRPO_LEN, GRPO_G = 64, 64, 8          # 64 responses x 64 tokens, groups of 8
+LOSS_CFG = (f"GRPO/DAPO loss on the step's log-probs: {GRPO_SEQ} sequences x {GRPO_LEN} tokens, "
+            f"group {GRPO_G}, eps 0.2/0.28, TIS cap 2.0, k3 KL 0.01, token mean")
+LM_T, LM_H = 16384, 4096
+LM_METRIC = "tokens/s for fused LM-head logprob+entropy (top_p 1) at V=151936, H=4096 bf16; % of bf16 peak"
+
+
+def timed_steps(args, ws, dev, stream, parts, barrier):
+    """W untimed steps, then K timed ones bracketed by barriers; returns
+    (elapsed_ms over all steps, per-part mean ms, clock record).  `parts` are
+    callables run in order each step, each bracketed by its own events."""
+    for _ in range(max(args.warmup, 3)):
+        for f in parts:
+            f()
+    barrier()
+    clocks = ClockSampler(dist_env()[2] if ws > 1 else 0)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
+           for _ in range(args.steps)]
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        for j, f in enumerate(parts):
+            f()
+            evs[i][j + 1].record(stream)
+    t_stop.record(stream)
+    barrier()
+    elapsed_ms = t_start.elapsed_time(t_stop)
+    part_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j in range(len(parts))]
+    clk = clocks.stop()
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    return elapsed_ms, part_ms, clk
+
+
+def run_logits(args, ws, rank, dev, barrier):
+    import entropy_logits_bf16_gb300 as rlk
+    import workloads
+    lib = rlk.load()
+    stream = torch.cuda.current_stream(dev)
+    z, ids = make_workload(dev, seed=1 + rank)
+    lp = torch.empty(T_ROWS, device=dev)
+    ent = torch.empty(T_ROWS, device=dev)
+    ks = torch.empty(T_ROWS, device=dev, dtype=torch.int32)
+
+    def logprob():
+        code = lib.rlk_logprob_entropy(
+            rlk._ptr(z), 0, T_ROWS, VOCAB, VOCAB, rlk._ptr(ids), TEMPERATURE, TOP_P,
+            rlk._ptr(lp), rlk._ptr(ent), rlk._ptr(ks), None, None, 0, rlk._stream(dev))
+        if code != 0:
+            raise RuntimeError(f"rlk_logprob_entropy returned {code}")
+
+    # the loss stage: old / rollout / reference log-probs are the first step's
+    # log-probs plus N(0, 0.01^2); rewards Bernoulli(0.5)
+    logprob()
+    torch.cuda.synchronize(dev)
+    old_h, ro_h, ref_h = workloads.perturbed_logps(lp.cpu().numpy(), 5 + rank)
+    rng = np.random.default_rng([7, rank])
+    R_h = (rng.random(GRPO_SEQ) < 0.5).astype(np.float32)
+    off_h = (np.arange(GRPO_SEQ + 1) * GRPO_LEN).astype(np.int32)
+    assert off_h[-1] == T_ROWS
+    tdev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    old, ro, ref, R, off = tdev(old_h), tdev(ro_h), tdev(ref_h), tdev(R_h), tdev(off_h)
+    loss = torch.empty(1, device=dev)
+    grad = torch.empty(T_ROWS, device=dev)
+    stats = torch.empty(8, device=dev)
+    wsb = rlk.workspace_size(1, T_ROWS, GRPO_SEQ)
+    wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+
+    def grpo(new=lp, o=old, r_=ro, f=ref, rw=R, of=off, out=loss):
+        code = lib.rlk_grpo_loss(rlk._ptr(new), rlk._ptr(o), rlk._ptr(r_), rlk._ptr(f), None,
+                                 rlk._ptr(rw), rlk._ptr(of), GRPO_SEQ, GRPO_G, T_ROWS, 0.2, 0.28,
+                                 2.0, 0.01, 0, rlk._ptr(out), rlk._ptr(grad), rlk._ptr(stats),
+                                 rlk._ptr(wsp), wsb, rlk._stream(dev))
+        if code != 0:
+            raise RuntimeError(f"rlk_grpo_loss returned {code}")
+
+    elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [logprob, grpo], barrier)
+
+    # end to end through the public API: pinned host inputs -> device -> the
+    # hot path -> the loss, log-probs and entropies back on the host
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    host = [pin(t) for t in (z, ids, old, ro, ref, R, off)]
+    dev_in = [torch.empty_like(t) for t in (z, ids, old, ro, ref, R, off)]
+    out_h = torch.empty(2 * T_ROWS + 1, dtype=torch.float32, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        for d, h in zip(dev_in, host):
+            d.copy_(h, non_blocking=True)
+        dz, dids, dold, dro, dref, dR, doff = dev_in
+        a, b = rlk.logprob_entropy(dz, dids, TEMPERATURE, TOP_P, out_logprob=lp, out_entropy=ent)
+        grpo(a, dold, dro, dref, dR, doff, loss)
+        out_h[:T_ROWS].copy_(a, non_blocking=True)
+        out_h[T_ROWS:2 * T_ROWS].copy_(b, non_blocking=True)
+        out_h[2 * T_ROWS:].copy_(loss, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    launch_ms = part_ms[0]
+    alg_bytes = BYTES_PER_TOKEN * T_ROWS
+    achieved = alg_bytes / (launch_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": T_ROWS * args.steps * ws / (elapsed_ms / 1e3), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_ROWS, "V": VOCAB, "temperature": TEMPERATURE,
+                   "top_p": TOP_P, "global_batch": T_ROWS * ws, "loss": LOSS_CFG,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "inputs (1.24 GB per GPU) larger than L2; no flush between steps",
+                   "step_ms": {"logprob_entropy": part_ms[0], "grpo_loss": part_ms[1]}},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic(), "peak_source": peak_kind,
+                     "kernel": "lpe_cluster_kernel<top_p<1> (+ the per-row recompute pass, "
+                               "timed together as one rlk_logprob_entropy call)",
+                     "bytes_per_token": BYTES_PER_TOKEN, "tokens_per_launch": T_ROWS,
+                     "launch_ms": launch_ms},
+        "e2e": {"value": T_ROWS * ws / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host)),
+                "d2h_bytes_per_step": int(out_h.numel() * 4)},
+        # cluster kernel + recompute pass + the loss's three kernels, per step
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(z, ids)
+    return line
+
+
+def run_lmhead(args, ws, rank, dev, barrier):
+    """--op lmhead: the fused LM-head (tcgen05 GEMM + online log-sum-exp
+    epilogue) on hidden [16384, 4096] and W [151936, 4096] bf16, top_p 1."""
+    import entropy_logits_bf16_gb300 as rlk
+    import workloads
+    stream = torch.cuda.current_stream(dev)
+    hidden, w, ids = workloads.lmhead_inputs(LM_T, LM_H, VOCAB, seed=4 + rank, device=dev)
+    ids = ids.to(dev).to(torch.int32)
+    wsb = rlk.workspace_size(2, LM_T, VOCAB, LM_H)
+    wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    lp = torch.empty(LM_T, device=dev)
+
+    def lm():
+        rlk.lmhead_logprob(hidden, w, ids, TEMPERATURE, workspace=wsp)
+
+    elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [lm], barrier)
+    host_h = torch.empty(hidden.shape, dtype=hidden.dtype, pin_memory=True).copy_(hidden)
+    host_i = torch.empty(ids.shape, dtype=ids.dtype, pin_memory=True).copy_(ids)
+    dh, di = torch.empty_like(hidden), torch.empty_like(ids)
+    out_h = torch.empty(2 * LM_T, dtype=torch.float32, pin_memory=True)
+
+    def e2e_step():
+        dh.copy_(host_h, non_blocking=True)
+        di.copy_(host_i, non_blocking=True)
+        a, b = rlk.lmhead_logprob(dh, w, di, TEMPERATURE, workspace=wsp)
+        out_h[:LM_T].copy_(a, non_blocking=True)
+        out_h[LM_T:].copy_(b, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    flops = 2.0 * LM_T * LM_H * VOCAB
+    achieved = flops / (part_ms[0] / 1e3) / 1e12
+    # the kernel runs back to back for seconds: the sustained (power-capped) peak
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0))
+    line = {
+        "metric": LM_METRIC, "value": LM_T * args.steps * ws / (elapsed_ms / 1e3), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"fused LM-head: hidden [{LM_T}, {LM_H}] bf16 N(0,1), W_vocab "
+                               f"[{VOCAB}, {LM_H}] bf16 N(0, 0.02^2), temperature {TEMPERATURE}, "
+                               f"top_p 1, uniform ids; logits never stored",
+                   "global_batch": LM_T * ws,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "W (1.24 GB) larger than L2; no flush between steps"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                     "kernel": "lmhead_kernel + lmhead_combine_kernel (one rlk_lmhead_logprob call)",
+                     "flops_per_launch": flops, "launch_ms": part_ms[0]},
+        "e2e": {"value": LM_T * ws / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(hidden.numel() * 2 + ids.numel() * 4),
+                "d2h_bytes_per_step": int(out_h.numel() * 4),
+                "note": "W_vocab (model state) stays resident; hidden states and ids are copied"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        rows = 32
+        sel = np.linspace(0, LM_T - 1, rows).astype(np.int64)
+        hb = workloads.bf16_bits(hidden[torch.from_numpy(sel).to(dev)])
+        wb = workloads.bf16_bits(w)
+        threads = oracle.default_threads()
+        oracle.build()
+        t0 = time.perf_counter()
+        oracle.lmhead_rows(hb, wb, np.arange(rows), ids.cpu().numpy()[sel], TEMPERATURE,
+                           threads=threads)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": rows / dt, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{rows} evenly spaced rows, fp64 oracle, {threads} threads, "
+                                          f"{dt:.2f} s"}
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--op", default="logits", choices=["logits", "lmhead"],
+                    help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused LM-head")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -222,125 +470,15 @@ def main():
     rlk.build()
     rlk.load()
 
-    z, ids = make_workload(dev, seed=1 + rank)
-    lp = torch.empty(T_ROWS, device=dev)
-    ent = torch.empty(T_ROWS, device=dev)
-    ks = torch.empty(T_ROWS, device=dev, dtype=torch.int32)
-    lib = rlk.load()
-    stream = torch.cuda.current_stream(dev)
-
-    def step():
-        code = lib.rlk_logprob_entropy(
-            rlk._ptr(z), 0, T_ROWS, VOCAB, VOCAB, rlk._ptr(ids), TEMPERATURE, TOP_P,
-            rlk._ptr(lp), rlk._ptr(ent), rlk._ptr(ks), None, None, 0,
-            rlk._stream(dev))
-        if code != 0:
-            raise RuntimeError(f"rlk_logprob_entropy returned {code}")
-
     def barrier():
         if ws > 1:
             import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
-    barrier()
-    clocks = ClockSampler(local if ws > 1 else 0)
-    clocks.start()
-    time.sleep(0.3)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    barrier()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_stop = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        evs[i][0].record(stream)
-        step()
-        evs[i][1].record(stream)
-    t_stop.record(stream)
-    barrier()
-    elapsed_ms = t_start.elapsed_time(t_stop)
-    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
-    clk = clocks.stop()
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
-
-    # end to end through the public API: pinned host logits -> device -> kernel -> host
-    host_z = torch.empty(z.shape, dtype=z.dtype, pin_memory=True)
-    host_z.copy_(z)
-    host_ids = torch.empty(ids.shape, dtype=ids.dtype, pin_memory=True)
-    host_ids.copy_(ids)
-    out_h = torch.empty(3, T_ROWS, dtype=torch.float32, pin_memory=True)
-    dz = torch.empty_like(z)
-    dids = torch.empty_like(ids)
-    e2e_steps = max(3, min(args.steps, 10))
-
-    def e2e_step():
-        dz.copy_(host_z, non_blocking=True)
-        dids.copy_(host_ids, non_blocking=True)
-        a, b, c = rlk.logprob_entropy(dz, dids, TEMPERATURE, TOP_P, out_logprob=lp,
-                                      out_entropy=ent, return_nucleus_size=True)
-        out_h[0].copy_(a, non_blocking=True)
-        out_h[1].copy_(b, non_blocking=True)
-        out_h[2].copy_(c.view(torch.float32), non_blocking=True)
-
-    e2e_step()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-
-    if rank != 0:
-        if ws > 1:
-            import torch.distributed as dist
-            dist.barrier()
-            dist.destroy_process_group()
-        return
-    peaks, peak_kind = measured_peaks()
-    ms_per_step = elapsed_ms / args.steps
-    value = T_ROWS * args.steps * ws / (elapsed_ms / 1e3)
-    launch_ms = sum(per_launch_ms) / len(per_launch_ms)
-    alg_bytes = BYTES_PER_TOKEN * T_ROWS
-    achieved = alg_bytes / (launch_ms / 1e3) / 1e9
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "T": T_ROWS, "V": VOCAB, "temperature": TEMPERATURE,
-                   "top_p": TOP_P, "global_batch": T_ROWS * ws,
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": "inputs (1.24 GB per GPU) larger than L2; no flush between steps"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": profiled_traffic(), "peak_source": peak_kind,
-                     "kernel": "lpe_cluster_kernel<top_p<1> (+ the per-row recompute pass, "
-                               "timed together as one rlk_logprob_entropy call)",
-                     "bytes_per_token": BYTES_PER_TOKEN, "tokens_per_launch": T_ROWS,
-                     "launch_ms": launch_ms},
-        "e2e": {"value": T_ROWS * ws / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(z.numel() * 2 + ids.numel() * 4),
-                "d2h_bytes_per_step": int(3 * T_ROWS * 4)},
-        "gpu_launches": 2 * args.steps,   # cluster kernel + recompute pass per call
-        "clocks": clk,
-    }
-    if ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(z, ids)
-    print(json.dumps(line), flush=True)
+    line = (run_lmhead if args.op == "lmhead" else run_logits)(args, ws, rank, dev, barrier)
+    if line is not None:
+        print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()

@@ -19,6 +19,7 @@
 
 #include <math.h>
 
+#include "common.cuh"
 #include "internal.h"
 #include "rlk.h"
 
@@ -45,18 +46,19 @@ __global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
   const float lo_b = 1.0f - a.eps_low, hi_b = 1.0f + a.eps_high;
   for (int s = blockIdx.x; s < a.n_seq; s += gridDim.x) {
     if (tid == 0) {
-      // Group statistics in a fixed order, in double.
+      // Group statistics in a fixed order: the mean as a double-float sum,
+      // then the squared deviations from it (two passes over G rewards).
       const int s0 = (s / G) * G;
-      double sum = 0.0;
-      for (int j = 0; j < G; ++j) sum += (double)a.rewards[s0 + j];
-      const double mu = sum / G;
-      double ss = 0.0;
+      DF sum{0.f, 0.f};
+      for (int j = 0; j < G; ++j) sum = df_add_f(sum, a.rewards[s0 + j]);
+      const float mu = __fdiv_rn(__fadd_rn(sum.hi, sum.lo), (float)G);
+      float ss = 0.f;
       for (int j = 0; j < G; ++j) {
-        const double d = (double)a.rewards[s0 + j] - mu;
-        ss += d * d;
+        const float d = __fsub_rn(a.rewards[s0 + j], mu);
+        ss = __fmaf_rn(d, d, ss);
       }
-      const double sigma = G > 1 ? sqrt(ss / (G - 1)) : 0.0;
-      s_adv = (float)(((double)a.rewards[s] - mu) / (sigma + 1e-6));
+      const float sigma = G > 1 ? sqrtf(__fdiv_rn(ss, (float)(G - 1))) : 0.f;
+      s_adv = __fdiv_rn(__fsub_rn(a.rewards[s], mu), __fadd_rn(sigma, 1e-6f));
     }
     __syncthreads();
     const float A = s_adv;
@@ -105,53 +107,62 @@ __global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
 
 // One CTA: fixed-order sums over the sequences' partials.
 __global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
-  __shared__ double s_red[LWARP][NP + 2];
+  // Double-float (fp32 pair) sums in a fixed order: thread t takes sequences
+  // t, t + LT, ...; then a shuffle tree per warp and one over the warps.
+  constexpr int NV = NP + 2;   // NP partial sums, sum of per-sequence means, live sequences
+  __shared__ DF s_red[LWARP][NV];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  double acc[NP + 2];  // NP partial sums, sum of per-sequence means, live sequences
+  DF acc[NV];
 #pragma unroll
-  for (int k = 0; k < NP + 2; ++k) acc[k] = 0.0;
+  for (int k = 0; k < NV; ++k) acc[k] = DF{0.f, 0.f};
   for (int s = tid; s < a.n_seq; s += LT) {
     const float* p = a.workspace + (int64_t)s * NP;
 #pragma unroll
-    for (int k = 0; k < NP; ++k) acc[k] += (double)p[k];
+    for (int k = 0; k < NP; ++k) acc[k] = df_add_f(acc[k], p[k]);
     if (p[1] > 0.f) {
-      acc[NP] += (double)p[0] / (double)p[1];
-      acc[NP + 1] += 1.0;
+      acc[NP] = df_add_f(acc[NP], __fdiv_rn(p[0], p[1]));
+      acc[NP + 1] = df_add_f(acc[NP + 1], 1.f);
     }
   }
 #pragma unroll
-  for (int k = 0; k < NP + 2; ++k) {
+  for (int k = 0; k < NV; ++k) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[k] += __shfl_down_sync(0xFFFFFFFFu, acc[k], o);
+    for (int o = 16; o > 0; o >>= 1)
+      acc[k] = df_add(acc[k], DF{shfl_down(acc[k].hi, o), shfl_down(acc[k].lo, o)});
   }
   if (lane == 0)
-    for (int k = 0; k < NP + 2; ++k) s_red[warp][k] = acc[k];
+    for (int k = 0; k < NV; ++k) s_red[warp][k] = acc[k];
   __syncthreads();
-  if (tid == 0) {
-    double t[NP + 2];
-    for (int k = 0; k < NP + 2; ++k) {
-      t[k] = 0.0;
-      for (int w2 = 0; w2 < LWARP; ++w2) t[k] += s_red[w2][k];
+  if (warp == 0) {
+    float t[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      DF v = lane < LWARP ? s_red[lane][k] : DF{0.f, 0.f};
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v = df_add(v, DF{shfl_down(v.hi, o), shfl_down(v.lo, o)});
+      t[k] = __fadd_rn(v.hi, v.lo);
     }
-    const double M = t[1];
-    double L;
-    if (a.agg == RLK_AGG_TOKEN_MEAN) L = M > 0.0 ? t[0] / M : 0.0;
-    else L = t[NP + 1] > 0.0 ? t[NP] / t[NP + 1] : 0.0;
-    *a.out_loss = (float)L;
-    if (a.out_stats) {
-      const double d = M > 0.0 ? M : 1.0;
-      a.out_stats[RLK_STAT_LOSS] = (float)L;
-      a.out_stats[RLK_STAT_TOKENS] = (float)M;
-      a.out_stats[RLK_STAT_CLIP_LOW] = (float)(t[2] / d);
-      a.out_stats[RLK_STAT_CLIP_HIGH] = (float)(t[3] / d);
-      a.out_stats[RLK_STAT_TIS_MEAN] = (float)(t[4] / d);
-      a.out_stats[RLK_STAT_TIS_CAPPED] = (float)(t[5] / d);
-      a.out_stats[RLK_STAT_K3_MEAN] = (float)(t[6] / d);
-      a.out_stats[RLK_STAT_PG_MEAN] = (float)(t[7] / d);
+    if (lane == 0) {
+      const float M = t[1];
+      float L;
+      if (a.agg == RLK_AGG_TOKEN_MEAN) L = M > 0.f ? __fdiv_rn(t[0], M) : 0.f;
+      else L = t[NP + 1] > 0.f ? __fdiv_rn(t[NP], t[NP + 1]) : 0.f;
+      *a.out_loss = L;
+      if (a.out_stats) {
+        const float d = M > 0.f ? M : 1.f;
+        a.out_stats[RLK_STAT_LOSS] = L;
+        a.out_stats[RLK_STAT_TOKENS] = M;
+        a.out_stats[RLK_STAT_CLIP_LOW] = __fdiv_rn(t[2], d);
+        a.out_stats[RLK_STAT_CLIP_HIGH] = __fdiv_rn(t[3], d);
+        a.out_stats[RLK_STAT_TIS_MEAN] = __fdiv_rn(t[4], d);
+        a.out_stats[RLK_STAT_TIS_CAPPED] = __fdiv_rn(t[5], d);
+        a.out_stats[RLK_STAT_K3_MEAN] = __fdiv_rn(t[6], d);
+        a.out_stats[RLK_STAT_PG_MEAN] = __fdiv_rn(t[7], d);
+      }
+      float* sc = a.workspace + (int64_t)a.n_seq * NP;
+      sc[0] = M > 0.f ? __fdiv_rn(1.f, M) : 0.f;   // token-mean weight
+      sc[1] = t[NP + 1];                             // sequences with tokens
     }
-    float* sc = a.workspace + (int64_t)a.n_seq * NP;
-    sc[0] = M > 0.0 ? (float)(1.0 / M) : 0.f;   // token-mean weight
-    sc[1] = (float)t[NP + 1];                     // sequences with tokens
   }
 }
 
@@ -164,7 +175,7 @@ __global__ void __launch_bounds__(LT) loss_scale_kernel(LossArgs a) {
       wgt = sc[0];
     } else {
       const float ms = a.workspace[(int64_t)s * NP + 1];
-      wgt = ms > 0.f ? (float)(1.0 / ((double)ms * (double)sc[1])) : 0.f;
+      wgt = ms > 0.f ? __fdiv_rn(1.f, __fmul_rn(ms, sc[1])) : 0.f;
     }
     const int64_t t0 = a.seq_offsets[s], t1 = a.seq_offsets[s + 1];
     for (int64_t t = t0 + threadIdx.x; t < t1; t += LT) a.out_grad[t] *= wgt;
