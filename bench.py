@@ -56,6 +56,26 @@ def dist_env():
     return ws, rank, local
 
 
+def reduce_max(x: float, dev) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: int, steps: int, ws: int, elapsed_ms: float) -> float:
+    """Units all ranks processed per second over the (max-over-ranks) elapsed time."""
+    return units_per_rank_step * steps * ws / (elapsed_ms / 1e3)
+
+
+def rank_seed(rank: int) -> int:
+    """Replicas draw different batches: rank r uses seed 1 + r."""
+    return 1 + int(rank)
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -238,12 +258,7 @@ def timed_steps(args, ws, dev, stream, parts, barrier):
     elapsed_ms = t_start.elapsed_time(t_stop)
     part_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j in range(len(parts))]
     clk = clocks.stop()
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
-    return elapsed_ms, part_ms, clk
+    return reduce_max(elapsed_ms, dev), part_ms, clk
 
 
 def run_logits(args, ws, rank, dev, barrier):
@@ -251,7 +266,7 @@ def run_logits(args, ws, rank, dev, barrier):
     import workloads
     lib = rlk.load()
     stream = torch.cuda.current_stream(dev)
-    z, ids = make_workload(dev, seed=1 + rank)
+    z, ids = make_workload(dev, seed=rank_seed(rank))
     lp = torch.empty(T_ROWS, device=dev)
     ent = torch.empty(T_ROWS, device=dev)
     ks = torch.empty(T_ROWS, device=dev, dtype=torch.int32)
@@ -317,12 +332,7 @@ def run_logits(args, ws, rank, dev, barrier):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, dev)
     if rank != 0:
         return None
     peaks, peak_kind = measured_peaks()
@@ -330,7 +340,7 @@ def run_logits(args, ws, rank, dev, barrier):
     alg_bytes = BYTES_PER_TOKEN * T_ROWS
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
     line = {
-        "metric": METRIC, "value": T_ROWS * args.steps * ws / (elapsed_ms / 1e3), "unit": "tokens/s",
+        "metric": METRIC, "value": whole_job_rate(T_ROWS, args.steps, ws, elapsed_ms), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -396,7 +406,7 @@ def run_lmhead(args, ws, rank, dev, barrier):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / n_e2e, dev)
     if rank != 0:
         return None
     peaks, peak_kind = measured_peaks()
@@ -405,7 +415,7 @@ def run_lmhead(args, ws, rank, dev, barrier):
     # the kernel runs back to back for seconds: the sustained (power-capped) peak
     peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0))
     line = {
-        "metric": LM_METRIC, "value": LM_T * args.steps * ws / (elapsed_ms / 1e3), "unit": "tokens/s",
+        "metric": LM_METRIC, "value": whole_job_rate(LM_T, args.steps, ws, elapsed_ms), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",

@@ -1,0 +1,60 @@
+"""The multi-process (N > 1) host logic of bench.py, on CPU with the gloo
+backend and world size 2.  Rows are independent, so N GPUs run N replicas of
+the hot path with no collective on the data path; what crosses ranks is the
+timing: the job's time is the slowest rank's, and the whole-job throughput
+counts every rank's rows over that time.  Each replica draws its own batch.
+"""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, ws, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    try:
+        import bench
+        env = bench.dist_env()
+        cpu = torch.device("cpu")
+        t_max = bench.reduce_max(10.0 + 3.0 * rank, cpu)      # rank 1 is the slow one
+        rate = bench.whole_job_rate(4096, 100, ws, t_max)
+        seed = bench.rank_seed(rank)
+        q.put((rank, env, t_max, rate, seed))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replica_timing_and_seeds_over_two_gloo_ranks():
+    ws = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, ws, port, q)) for r in range(ws)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(ws))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, env, t_max, rate, _ in res:
+        assert env == (ws, rank, rank)
+        assert t_max == pytest.approx(13.0)                    # max over ranks, on every rank
+        assert rate == pytest.approx(4096 * 100 * ws / 13.0e-3)
+    assert res[0][4] != res[1][4]                              # each replica its own batch
+
+
+def test_single_process_helpers():
+    import bench
+    assert bench.reduce_max(7.5, torch.device("cpu")) == 7.5   # no process group: the value itself
+    assert bench.whole_job_rate(4096, 10, 1, 5.0) == pytest.approx(4096 * 10 / 5.0e-3)
