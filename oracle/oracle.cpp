@@ -23,8 +23,12 @@
 //    importance ratios.
 //  * prime-rl v0.10.0 release notes, section "1. Trainer Performance": the
 //    loss is chunked so full logits need not exist at once (LM-head rows).
-// Readings taken where the pages are silent (nucleus rule, tie order, std
-// estimator, KL estimator, clip bounds, aggregation) are listed in the design doc.
+// Readings taken where the pages are silent: keep a token while the mass
+// ranked strictly ahead of it is below top_p (so at least one is kept); equal
+// logits are kept lower id first, -0 equal to +0; advantages use the n-1
+// standard deviation plus 1e-6; the KL term is k3 = e^d - d - 1 with
+// d = ref - new; clip bounds and the TIS cap are arguments; the loss is the
+// token mean over the batch (or the mean of per-sequence token means).
 //
 // Parity pins: brute force on V = 8, closed forms (uniform, one-hot, two-level
 // logits), top_p = 1 against a library log-softmax, invariants, hand-worked
