@@ -52,11 +52,14 @@ def _load():
             lib.oracle_logprob_entropy.argtypes = [vp, i, i64, i64, i64, vp, f32, f32, vp,
                                                    vp, vp, vp, vp, i]
             lib.oracle_sample_ids.argtypes = [vp, i, i64, i64, i64, f32, f32, vp, vp, i]
+            lib.oracle_logprob_entropy_support.argtypes = [vp, i, i64, i64, i64, vp, f32, vp, vp,
+                                                           vp, vp, vp, i]
             lib.oracle_grpo_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, f32,
                                              f32, f32, i, vp, vp, vp, vp]
             lib.oracle_lmhead_rows.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, f32, f32,
                                                vp, vp, vp, i]
             for fn in (lib.oracle_logprob_entropy, lib.oracle_sample_ids,
+                       lib.oracle_logprob_entropy_support,
                        lib.oracle_grpo_loss, lib.oracle_lmhead_rows):
                 fn.restype = ctypes.c_int
             _lib = lib
@@ -108,6 +111,31 @@ def logprob_entropy(logits, ids, temperature, top_p, force_k=None, threads=None)
     if rc:
         raise ValueError("oracle_logprob_entropy rejected its arguments")
     return lp, ent, k, gap
+
+
+def logprob_entropy_support(logits, ids, temperature, offsets, support_ids, threads=None):
+    """Score every row of ``logits`` [T, V] over a supplied retained set: row r
+    keeps the ids ``support_ids[offsets[r]:offsets[r+1]]``.  Returns (logprob,
+    entropy, status) with status 0, 1 (bad selected id), 2 (non-finite listed
+    logit) or 8 (empty list, listed id out of range, decreasing offsets)."""
+    a, dt = _logits_array(logits)
+    if a.ndim != 2:
+        raise ValueError("logits must be 2-D")
+    T, V = a.shape
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    sup = np.ascontiguousarray(support_ids, dtype=np.int32)
+    assert ids.shape == (T,) and off.shape == (T + 1,)
+    lp = np.empty(T, np.float64)
+    ent = np.empty(T, np.float64)
+    st = np.empty(T, np.int32)
+    rc = _load().oracle_logprob_entropy_support(_ptr(a), dt, T, V, V, _ptr(ids),
+                                                float(np.float32(temperature)), _ptr(off),
+                                                _ptr(sup), _ptr(lp), _ptr(ent), _ptr(st),
+                                                threads or default_threads())
+    if rc:
+        raise ValueError("oracle_logprob_entropy_support rejected its arguments")
+    return lp, ent, st
 
 
 def sample_ids(logits, temperature, top_p, u, threads=None):

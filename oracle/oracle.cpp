@@ -213,6 +213,70 @@ int oracle_logprob_entropy(const void* logits, int dtype, int64_t T, int64_t V, 
   return 0;
 }
 
+// Log-probability and entropy over a retained set supplied by the sampler
+// (the sparse path of RL-Kernel "Qwen3-8B VIME train-rollout consistency",
+// section "ROCm MI300X and gfx942", which scores the complete retained
+// support it is given).  Row r's retained set S is the list
+// sup_ids[offsets[r] .. offsets[r+1]); every listed token is kept.
+//  1. x_i = z_i / T for the listed i; m_S = max x_i over the list.
+//  2. w_i = exp(x_i - m_S), Z_S = sum over the list (compensated).
+//  3. logprob(y) = (x_y - m_S) - ln Z_S if y is listed, else -inf.
+//  4. H = -sum over the list of q_i ln q_i, q_i = w_i / Z_S, 0 ln 0 = 0.
+// A repeated id counts each time it is listed (the list is the caller's).
+// Per-row status: 1 selected id outside [0, V); 8 an empty list, a listed id
+// outside [0, V) or offsets that decrease; 2 a non-finite listed logit.  A
+// row with a status gets NaN outputs.
+int oracle_logprob_entropy_support(const void* logits, int dtype, int64_t T, int64_t V, int64_t ld,
+                                   const int32_t* ids, float temperature, const int64_t* offsets,
+                                   const int32_t* sup_ids, double* out_logprob,
+                                   double* out_entropy, int32_t* out_status, int nthreads) {
+  if (!logits || !ids || !offsets || T < 0 || V < 1 || ld < V || (dtype != 0 && dtype != 1))
+    return 1;
+  const double Td = static_cast<double>(temperature);
+  parallel_rows(T, nthreads, [&](int64_t row) {
+    double lp = kNaN, ent = kNaN;
+    int32_t st = 0;
+    const int64_t a = offsets[row], b = offsets[row + 1];
+    const int64_t y = ids[row];
+    if (y < 0 || y >= V) st = 1;
+    else if (b <= a) st = 8;
+    else {
+      for (int64_t j = a; j < b; ++j)
+        if (sup_ids[j] < 0 || sup_ids[j] >= V) st = 8;
+    }
+    if (st == 0) {
+      std::vector<double> x;
+      x.reserve(static_cast<size_t>(b - a));
+      bool y_in = false;
+      double m = -kInf;
+      for (int64_t j = a; j < b; ++j) {
+        const double z = load_logit(logits, dtype, row, ld, sup_ids[j]);
+        if (!std::isfinite(z)) st = 2;
+        x.push_back(z / Td);
+        m = std::max(m, x.back());
+        if (sup_ids[j] == y) y_in = true;
+      }
+      if (st == 0) {
+        NeumaierSum zs;
+        for (double v : x) zs.add(std::exp(v - m));
+        const double ZS = zs.value();
+        lp = y_in ? (load_logit(logits, dtype, row, ld, y) / Td - m) - std::log(ZS) : -kInf;
+        NeumaierSum h;
+        for (double v : x) {
+          const double q = std::exp(v - m) / ZS;
+          if (q > 0.0) h.add(-q * std::log(q));
+        }
+        ent = h.value();
+      }
+    }
+    if (st != 0) lp = ent = kNaN;
+    if (out_logprob) out_logprob[row] = lp;
+    if (out_entropy) out_entropy[row] = ent;
+    if (out_status) out_status[row] = st;
+  });
+  return 0;
+}
+
 // Draws one id per row from the renormalised truncated distribution by
 // inverse CDF over S in the ranking order: the first j with
 // sum_{i<=j} w_pi(i) >= u * Z_S.  u in [0,1) is supplied per row.

@@ -400,3 +400,85 @@ def test_lmhead_rows_against_library_matmul(oracle):
         assert abs(lp[j] - ref_lp[r, ids[r].long()].item()) < 1e-10
         assert abs(ent[j] - ref_ent[r].item()) < 1e-10
     assert np.all(k == 300)
+
+
+# --------------------------------------------------------------------------
+# The supplied-support scorer (retained set given by the sampler as a list).
+
+def _nucleus_lists(hz, k):
+    """The oracle's ranking (z descending, id ascending; -0 == +0) cut at k*."""
+    vals = (hz.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return [np.lexsort((np.arange(vals.shape[1]), -vals[r]))[:k[r]] for r in range(vals.shape[0])]
+
+
+@pytest.mark.parametrize("T,p", [(0.7, 0.5), (0.7, 0.95), (1.8, 0.95), (0.2, 0.9)])
+def test_support_equals_topp_nucleus(oracle, T, p):
+    """Given the top-p nucleus as its retained set -- in rank order or shuffled --
+    the supplied-support scorer reproduces the top-p scorer."""
+    z, _ = workloads.peaked_bf16(8, V=3000, seed=12)
+    hz = workloads.bf16_bits(z)
+    ids = oracle.sample_ids(hz, T, p, workloads.uniforms(8, 3))
+    lp, ent, k, _ = oracle.logprob_entropy(hz, ids, T, p)
+    lists = _nucleus_lists(hz, k)
+    rng = np.random.default_rng(5)
+    for shuffle in (False, True):
+        ls = [rng.permutation(l) if shuffle else l for l in lists]
+        off = np.concatenate([[0], np.cumsum([len(l) for l in ls])]).astype(np.int64)
+        sup = np.concatenate(ls).astype(np.int32)
+        slp, sent, st = oracle.logprob_entropy_support(hz, ids, T, off, sup)
+        assert np.all(st == 0)
+        assert np.allclose(slp, lp, rtol=0, atol=1e-11)
+        assert np.allclose(sent, ent, rtol=0, atol=1e-11)
+    # an id outside the nucleus scores -inf on both
+    far = ((ids.astype(np.int64) + 1500) % 3000).astype(np.int32)
+    lp2, _, _, _ = oracle.logprob_entropy(hz, far, T, p)
+    off = np.concatenate([[0], np.cumsum([len(l) for l in lists])]).astype(np.int64)
+    slp2, _, _ = oracle.logprob_entropy_support(hz, far, T, off, np.concatenate(lists).astype(np.int32))
+    assert np.array_equal(np.isneginf(slp2), np.isneginf(lp2))
+
+
+def test_support_closed_forms(oracle):
+    V, T = 64, 0.7
+    z = np.zeros((3, V), np.float32)
+    z[1, :10] = 2.0          # two levels: 10 tokens at 2.0, the rest at 0.0
+    z[2] = np.linspace(-3, 3, V, dtype=np.float32)
+    # row 0: uniform logits, a support of k = 7 ids -> logprob -ln 7, H = ln 7
+    s0 = np.array([3, 9, 11, 20, 33, 40, 63], np.int32)
+    # row 1: 4 ids at 2.0 and 6 ids at 0.0
+    s1 = np.array([0, 1, 2, 3, 30, 31, 32, 33, 34, 35], np.int32)
+    # row 2: a single listed id -> logprob 0, H 0
+    s2 = np.array([17], np.int32)
+    off = np.array([0, 7, 17, 18], np.int64)
+    ids = np.array([11, 31, 17], np.int32)
+    lp, ent, st = oracle.logprob_entropy_support(z, ids, T, off, np.concatenate([s0, s1, s2]))
+    assert np.all(st == 0)
+    assert lp[0] == pytest.approx(-math.log(7), abs=1e-14)
+    assert ent[0] == pytest.approx(math.log(7), abs=1e-14)
+    a = math.exp(2.0 / float(np.float32(T)))   # the float32 temperature, widened
+    Zs = 4 * a + 6
+    q_hi, q_lo = a / Zs, 1 / Zs
+    assert lp[1] == pytest.approx(math.log(q_lo), abs=1e-13)
+    assert ent[1] == pytest.approx(-(4 * q_hi * math.log(q_hi) + 6 * q_lo * math.log(q_lo)), abs=1e-13)
+    assert lp[2] == 0.0 and ent[2] == 0.0
+    # shift invariance
+    lp_s, ent_s, _ = oracle.logprob_entropy_support(z + np.float32(5.0), ids, T, off,
+                                                    np.concatenate([s0, s1, s2]))
+    assert np.allclose(lp_s, lp, atol=1e-12) and np.allclose(ent_s, ent, atol=1e-12)
+
+
+def test_support_errors(oracle):
+    V = 16
+    z = np.zeros((5, V), np.float32)
+    z[3, 2] = np.nan          # listed non-finite logit
+    z[4, 9] = np.inf          # unlisted non-finite logit: not examined
+    off = np.array([0, 0, 2, 4, 6, 8], np.int64)          # row 0: empty list
+    sup = np.array([1, 16,  1, 2,  1, 2,  1, 2], np.int32)  # row 1: id 16 out of range
+    ids = np.array([0, 1, 99, 1, 1], np.int32)             # row 2: selected id out of range
+    lp, ent, st = oracle.logprob_entropy_support(z, ids, 1.0, off, sup)
+    assert list(st) == [8, 8, 1, 2, 0]
+    assert np.all(np.isnan(lp[:4])) and np.all(np.isnan(ent[:4]))
+    assert lp[4] == pytest.approx(-math.log(2)) and ent[4] == pytest.approx(math.log(2))
+    # offsets that decrease
+    lp, ent, st = oracle.logprob_entropy_support(z[:2], ids[:2], 1.0,
+                                                 np.array([0, 3, 1], np.int64), sup[:3])
+    assert st[1] == 8 and np.isnan(lp[1])
