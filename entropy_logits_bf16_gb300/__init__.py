@@ -28,10 +28,12 @@ NSTATS = 8
 STAT_NAMES = ("loss", "tokens", "clip_low_frac", "clip_high_frac", "tis_mean",
               "tis_capped_frac", "k3_mean", "pg_mean")
 EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logprob_entropy",
-           "rlk_grpo_loss", "rlk_lmhead_logprob", "rlk_grpo_loss_noalloc")
+           "rlk_logprob_entropy_support", "rlk_grpo_loss", "rlk_lmhead_logprob",
+           "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
 DEBUG_EXPORTS = ("rlk_lmhead_logits_debug",)
 STATUS_TIMEOUT = 0x4
+STATUS_BAD_SUPPORT = 0x8
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +70,9 @@ def load(path: str | None = None):
         lib.rlk_logprob_entropy.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, f32, vp,
                                             vp, vp, vp, vp, sz, vp]
         lib.rlk_logprob_entropy.restype = ctypes.c_int
+        lib.rlk_logprob_entropy_support.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, vp,
+                                                    vp, vp, vp, vp, vp]
+        lib.rlk_logprob_entropy_support.restype = ctypes.c_int
         lib.rlk_grpo_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, f32, f32, f32,
                                       f32, ctypes.c_int, vp, vp, vp, vp, sz, vp]
         lib.rlk_grpo_loss.restype = ctypes.c_int
@@ -140,6 +145,44 @@ def logprob_entropy(logits: torch.Tensor, token_ids: torch.Tensor, temperature: 
                                    None, 0, _stream(dev))
     _check("rlk_logprob_entropy", code)
     return (lp, ent, ks) if return_nucleus_size else (lp, ent)
+
+
+def logprob_entropy_support(logits: torch.Tensor, token_ids: torch.Tensor, temperature: float,
+                            support_offsets: torch.Tensor, support_ids: torch.Tensor, *,
+                            out_logprob=None, out_entropy=None, status_word=None):
+    """Log-probability of the selected token and entropy over a retained set
+    supplied by the sampler: row t keeps the ids
+    support_ids[support_offsets[t]:support_offsets[t+1]] (CUDA int64 offsets
+    [T+1], int32 ids).  Returns (logprob, entropy) fp32 [T]."""
+    lib = load()
+    _need_cuda(logits, token_ids, support_offsets, support_ids)
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be 2-D with unit stride along the vocabulary")
+    if logits.dtype == torch.bfloat16:
+        dt = 0
+    elif logits.dtype == torch.float32:
+        dt = 1
+    else:
+        raise ValueError("logits must be bf16 or fp32")
+    if token_ids.dtype != torch.int32 or not token_ids.is_contiguous():
+        raise ValueError("token_ids must be contiguous int32")
+    if support_offsets.dtype != torch.int64 or not support_offsets.is_contiguous():
+        raise ValueError("support_offsets must be contiguous int64")
+    if support_ids.dtype != torch.int32 or not support_ids.is_contiguous():
+        raise ValueError("support_ids must be contiguous int32")
+    T, V = logits.shape
+    if support_offsets.numel() != T + 1:
+        raise ValueError("support_offsets must have T + 1 entries")
+    ld = logits.stride(0) if T > 1 else V
+    dev = logits.device
+    lp = out_logprob if out_logprob is not None else torch.empty(T, device=dev, dtype=torch.float32)
+    ent = out_entropy if out_entropy is not None else torch.empty(T, device=dev, dtype=torch.float32)
+    code = lib.rlk_logprob_entropy_support(_ptr(logits), dt, T, V, ld, _ptr(token_ids),
+                                           float(temperature), _ptr(support_offsets),
+                                           _ptr(support_ids), _ptr(lp), _ptr(ent),
+                                           _ptr(status_word), _stream(dev))
+    _check("rlk_logprob_entropy_support", code)
+    return lp, ent
 
 
 def grpo_loss(logp_new, logp_old, logp_rollout, logp_ref, rewards, seq_offsets, group_size, *,

@@ -23,6 +23,19 @@ struct LpeArgs {
 // in out_logprob for rows that the per-row kernel must recompute.
 constexpr uint32_t kRecomputeMark = 0x7FC0DEADu;
 
+struct SupportArgs {
+  const void* logits;
+  int dtype;  // 0 bf16, 1 fp32
+  int64_t T, V, ld;
+  const int32_t* ids;
+  float temperature;
+  const int64_t* offsets;   // [T + 1]
+  const int32_t* support;   // [offsets[T]]
+  float* out_logprob;
+  float* out_entropy;
+  uint32_t* status;
+};
+
 struct LossArgs {
   const float *logp_new, *logp_old, *logp_rollout, *logp_ref;
   const uint8_t* mask;
@@ -57,6 +70,8 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream);
 // Cluster-resident kernel for large-vocabulary bf16 rows (lpe_cluster.cu).
 bool lpe_cluster_eligible(const LpeArgs& a);
 cudaError_t launch_lpe_cluster(const LpeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_support(const SupportArgs& a, cudaStream_t stream);
 
 constexpr int kLossPartials = 8;  // floats per sequence in the loss workspace
 size_t loss_workspace_bytes(int64_t n_seq);

@@ -95,6 +95,38 @@ rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, i
              : RLK_ERR_CUDA;
 }
 
+rlk_status rlk_logprob_entropy_support(const void* logits, rlk_dtype dtype, int64_t T,
+                                       int64_t V, int64_t ld, const int32_t* token_ids,
+                                       float temperature, const int64_t* support_offsets,
+                                       const int32_t* support_ids, float* out_logprob,
+                                       float* out_entropy, uint32_t* out_status_word,
+                                       rlk_stream stream) {
+  if (dtype != RLK_BF16 && dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || ld < V) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;   // nothing to read or write; pointers may be NULL
+  if (!logits || !token_ids || !support_offsets || !out_logprob || !out_entropy)
+    return RLK_ERR_INVALID_ARG;
+  const uintptr_t elem = dtype == RLK_BF16 ? 2u : 4u;
+  if (reinterpret_cast<uintptr_t>(logits) % elem != 0) return RLK_ERR_INVALID_ARG;
+  rlk::SupportArgs a;
+  a.logits = logits;
+  a.dtype = dtype == RLK_BF16 ? 0 : 1;
+  a.T = T;
+  a.V = V;
+  a.ld = ld;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.offsets = support_offsets;
+  a.support = support_ids;
+  a.out_logprob = out_logprob;
+  a.out_entropy = out_entropy;
+  a.status = out_status_word;
+  return rlk::launch_support(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
 rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
                          const float* logp_rollout, const float* logp_ref,
                          const uint8_t* loss_mask, const float* rewards,

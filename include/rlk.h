@@ -69,6 +69,9 @@ enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2 };
 #define RLK_STATUS_NONFINITE    0x2u   /* a NaN or +-inf logit in a row      */
 #define RLK_STATUS_TIMEOUT      0x4u   /* a bounded device wait ran out; the
                                           call's outputs are not valid      */
+#define RLK_STATUS_BAD_SUPPORT  0x8u   /* a supplied retained set that is empty,
+                                          lists an id outside [0, V), or whose
+                                          offsets decrease                      */
 
 /* Slots of the loss statistics vector (float [RLK_NSTATS]); fractions and
  * means are over tokens with mask = 1. */
@@ -137,6 +140,50 @@ rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, i
                                float top_p, float* out_logprob, float* out_entropy,
                                int32_t* out_nucleus_size, uint32_t* out_status_word,
                                void* workspace, size_t workspace_bytes, rlk_stream stream);
+
+/*
+ * rlk_logprob_entropy_support -- per-token log-probability and entropy over a
+ * retained set supplied by the sampler.
+ *
+ * The sparse path of RL-Kernel "Qwen3-8B VIME train-rollout consistency",
+ * section "ROCm MI300X and gfx942", scores the complete retained support the
+ * sampler produced rather than recomputing it.  Row t keeps exactly the ids
+ * listed in support_ids[support_offsets[t] .. support_offsets[t+1]) (a CSR
+ * layout; any order; an id listed twice counts twice):
+ *   x_i = z_i / temperature over the listed ids;  m_S = max x;
+ *   Z_S = sum exp(x_i - m_S) over the list;
+ *   out_logprob[t] = (x_y - m_S) - ln Z_S if y is listed, else -INFINITY;
+ *   out_entropy[t] = Shannon entropy (nats) of exp(x - m_S) / Z_S over the list.
+ * Only the listed ids' logits are read.  With the list set to the top-p
+ * retained set, the outputs equal rlk_logprob_entropy's.
+ *
+ * Arguments
+ *  logits          device, dtype `dtype`, T x ld elements, as for
+ *                  rlk_logprob_entropy.  Read only.
+ *  T, V, ld        rows, vocabulary size (1 <= V <= 2^24), row stride.
+ *  token_ids       device int32[T].
+ *  temperature     finite, > 0.
+ *  support_offsets device int64[T + 1], nondecreasing (checked per row on the
+ *                  device).
+ *  support_ids     device int32[support_offsets[T]] (may be NULL when every
+ *                  row's list is empty, which is a data error per row).
+ *  out_logprob, out_entropy  device float[T].
+ *  out_status_word device uint32[1] or NULL.  A row whose selected id is out
+ *                  of range (RLK_STATUS_BAD_TOKEN_ID), whose list is empty,
+ *                  lists an id out of range or whose offsets decrease
+ *                  (RLK_STATUS_BAD_SUPPORT), or whose listed logits include
+ *                  a NaN or +-inf (RLK_STATUS_NONFINITE) gets NaN outputs.
+ *  stream          CUDA stream.
+ * Errors: RLK_ERR_INVALID_ARG for T < 0, V < 1, V > 2^24, ld < V, a bad
+ *  dtype, a non-finite or non-positive temperature, or a null required
+ *  pointer.  T == 0 returns RLK_OK without launching.
+ */
+rlk_status rlk_logprob_entropy_support(const void* logits, rlk_dtype dtype, int64_t T,
+                                       int64_t V, int64_t ld, const int32_t* token_ids,
+                                       float temperature, const int64_t* support_offsets,
+                                       const int32_t* support_ids, float* out_logprob,
+                                       float* out_entropy, uint32_t* out_status_word,
+                                       rlk_stream stream);
 
 /*
  * rlk_grpo_loss -- fused GRPO/DAPO loss with TIS correction and k3 KL.
