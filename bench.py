@@ -477,14 +477,78 @@ def run_lmhead(args, ws, rank, dev, barrier):
     return line
 
 
+SUP_METRIC = ("tokens/s for supplied-support logprob+entropy (the top-p retained set given as "
+              "CSR) at V=151936 bf16")
+
+
+def make_supports(z, top_p, temperature, chunk=256):
+    """Each row's top-p retained set (sorted by logit, lower id first on
+    ties), as CSR int64 offsets [T+1] and int32 ids, built with library sorts on
+    the device -- benchmark inputs, not the product path."""
+    offs, lists = [0], []
+    for r0 in range(0, z.shape[0], chunk):
+        x = z[r0:r0 + chunk].float() / temperature
+        order = torch.argsort(x, dim=1, descending=True, stable=True)   # ties: lower id first
+        p = torch.softmax(x, dim=1).gather(1, order)
+        c = torch.cumsum(p, dim=1)
+        k = ((c < top_p).sum(dim=1) + 1).clamp(max=z.shape[1]).cpu()
+        for i in range(x.shape[0]):
+            lists.append(order[i, :int(k[i])].to(torch.int32))
+            offs.append(offs[-1] + int(k[i]))
+    return (torch.tensor(offs, dtype=torch.int64, device=z.device), torch.cat(lists))
+
+
+def run_support(args, ws, rank, dev, barrier):
+    """--op support: rlk_logprob_entropy_support on the benchmark rows, each
+    given its own top-p retained set."""
+    import entropy_logits_bf16_gb300 as rlk
+    stream = torch.cuda.current_stream(dev)
+    z, ids = make_workload(dev, seed=rank_seed(rank))
+    off, sup = make_supports(z, TOP_P, TEMPERATURE)
+    lp = torch.empty(T_ROWS, device=dev)
+    ent = torch.empty(T_ROWS, device=dev)
+
+    def call():
+        rlk.logprob_entropy_support(z, ids, TEMPERATURE, off, sup, out_logprob=lp, out_entropy=ent)
+
+    elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [call], barrier)
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    nnz = int(sup.numel())
+    alg = nnz * (4 + 2) + T_ROWS * (8 + 4 + 8)   # listed ids + their logits, offsets, id, outputs
+    sectors = nnz * 32 + nnz * 4 + T_ROWS * 20    # each listed logit costs one 32-byte sector
+    achieved = alg / (part_ms[0] / 1e3) / 1e9
+    return {
+        "metric": SUP_METRIC, "value": whole_job_rate(T_ROWS, args.steps, ws, elapsed_ms),
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD + "; each row's top-p retained set supplied as CSR",
+                   "T": T_ROWS, "V": VOCAB, "listed_tokens": nnz,
+                   "mean_listed_per_row": nnz / T_ROWS, "global_batch": T_ROWS * ws,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peak_kind,
+                     "kernel": "support_kernel (one rlk_logprob_entropy_support call)",
+                     "algorithmic_bytes_per_launch": alg,
+                     "sector_bytes_per_launch": sectors,
+                     "sector_frac": sectors / (part_ms[0] / 1e3) / 1e9 / peaks["hbm_gbs"],
+                     "launch_ms": part_ms[0]},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="logits", choices=["logits", "lmhead"],
-                    help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused LM-head")
+    ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "support"],
+                    help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused "
+                         "LM-head; support: the supplied-support scorer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -508,7 +572,8 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    line = (run_lmhead if args.op == "lmhead" else run_logits)(args, ws, rank, dev, barrier)
+    run = {"logits": run_logits, "lmhead": run_lmhead, "support": run_support}[args.op]
+    line = run(args, ws, rank, dev, barrier)
     if line is not None:
         print(json.dumps(line), flush=True)
     if ws > 1:
