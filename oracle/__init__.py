@@ -54,12 +54,15 @@ def _load():
             lib.oracle_sample_ids.argtypes = [vp, i, i64, i64, i64, f32, f32, vp, vp, i]
             lib.oracle_logprob_entropy_support.argtypes = [vp, i, i64, i64, i64, vp, f32, vp, vp,
                                                            vp, vp, vp, i]
+            lib.oracle_logprob_entropy_support_backward.argtypes = [vp, i, i64, i64, i64, vp, f32,
+                                                                    vp, vp, vp, vp, vp, i]
             lib.oracle_grpo_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, f32,
                                              f32, f32, i, vp, vp, vp, vp]
             lib.oracle_lmhead_rows.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, f32, f32,
                                                vp, vp, vp, i]
             for fn in (lib.oracle_logprob_entropy, lib.oracle_sample_ids,
                        lib.oracle_logprob_entropy_support,
+                       lib.oracle_logprob_entropy_support_backward,
                        lib.oracle_grpo_loss, lib.oracle_lmhead_rows):
                 fn.restype = ctypes.c_int
             _lib = lib
@@ -136,6 +139,26 @@ def logprob_entropy_support(logits, ids, temperature, offsets, support_ids, thre
     if rc:
         raise ValueError("oracle_logprob_entropy_support rejected its arguments")
     return lp, ent, st
+
+
+def logprob_entropy_support_backward(logits, ids, temperature, offsets, support_ids, g_logprob=None,
+                                     g_entropy=None, threads=None):
+    """dL/dz for every listed id (aligned with ``support_ids``), the retained
+    sets held fixed, for L = sum_t g_logprob[t] logprob_t + g_entropy[t] H_t."""
+    a, dt = _logits_array(logits)
+    T, V = a.shape
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    sup = np.ascontiguousarray(support_ids, dtype=np.int32)
+    gl = None if g_logprob is None else np.ascontiguousarray(g_logprob, dtype=np.float32)
+    gh = None if g_entropy is None else np.ascontiguousarray(g_entropy, dtype=np.float32)
+    out = np.empty(int(off[-1]), np.float64)
+    rc = _load().oracle_logprob_entropy_support_backward(
+        _ptr(a), dt, T, V, V, _ptr(ids), float(np.float32(temperature)), _ptr(off), _ptr(sup),
+        _ptr(gl), _ptr(gh), _ptr(out), threads or default_threads())
+    if rc:
+        raise ValueError("oracle_logprob_entropy_support_backward rejected its arguments")
+    return out
 
 
 def sample_ids(logits, temperature, top_p, u, threads=None):

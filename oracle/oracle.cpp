@@ -277,6 +277,69 @@ int oracle_logprob_entropy_support(const void* logits, int dtype, int64_t T, int
   return 0;
 }
 
+// Gradient of the supplied-support scorer with respect to the listed logits,
+// the retained set held fixed (the sampler chose it):
+//   d logprob / d z_i = ([i = y] - q_i) / T   for listed i, when y is listed
+//                       (0 when y is not listed: its log-probability is -inf);
+//   d H / d z_i       = -q_i (ln q_i + H) / T for listed i;
+// with q_i = exp(x_i - m_S) / Z_S as in oracle_logprob_entropy_support.
+// out_grad[j] = g_lp[row] d logprob/d z_{sup_ids[j]} + g_H[row] d H/d z_{sup_ids[j]}
+// for every list position j (g_lp / g_H may be NULL, meaning 0).  Rows with
+// a status (as in the forward) get NaN gradients.
+int oracle_logprob_entropy_support_backward(const void* logits, int dtype, int64_t T, int64_t V,
+                                            int64_t ld, const int32_t* ids, float temperature,
+                                            const int64_t* offsets, const int32_t* sup_ids,
+                                            const float* g_lp, const float* g_h, double* out_grad,
+                                            int nthreads) {
+  if (!logits || !ids || !offsets || !out_grad || T < 0 || V < 1 || ld < V ||
+      (dtype != 0 && dtype != 1))
+    return 1;
+  const double Td = static_cast<double>(temperature);
+  parallel_rows(T, nthreads, [&](int64_t row) {
+    const int64_t a = offsets[row], b = offsets[row + 1];
+    const int64_t y = ids[row];
+    bool bad = y < 0 || y >= V || b <= a;
+    for (int64_t j = a; j < b && !bad; ++j)
+      if (sup_ids[j] < 0 || sup_ids[j] >= V) bad = true;
+    std::vector<double> x;
+    double m = -kInf;
+    bool y_in = false;
+    if (!bad) {
+      for (int64_t j = a; j < b; ++j) {
+        const double z = load_logit(logits, dtype, row, ld, sup_ids[j]);
+        if (!std::isfinite(z)) bad = true;
+        x.push_back(z / Td);
+        m = std::max(m, x.back());
+        if (sup_ids[j] == y) y_in = true;
+      }
+    }
+    if (bad) {
+      for (int64_t j = a; j < b; ++j) out_grad[j] = kNaN;
+      return;
+    }
+    NeumaierSum zs;
+    for (double v : x) zs.add(std::exp(v - m));
+    const double ZS = zs.value();
+    NeumaierSum h;
+    std::vector<double> q(x.size());
+    for (size_t i = 0; i < x.size(); ++i) {
+      q[i] = std::exp(x[i] - m) / ZS;
+      if (q[i] > 0.0) h.add(-q[i] * std::log(q[i]));
+    }
+    const double H = h.value();
+    const double glp = g_lp ? static_cast<double>(g_lp[row]) : 0.0;
+    const double gh = g_h ? static_cast<double>(g_h[row]) : 0.0;
+    for (int64_t j = a; j < b; ++j) {
+      const double qi = q[j - a];
+      const double dlp = y_in ? ((sup_ids[j] == y ? 1.0 : 0.0) - qi) / Td : 0.0;
+      const double lq = qi > 0.0 ? std::log(qi) : 0.0;   // q ln q -> 0 as q -> 0
+      const double dh = -qi * (lq + H) / Td;
+      out_grad[j] = glp * dlp + gh * dh;
+    }
+  });
+  return 0;
+}
+
 // Draws one id per row from the renormalised truncated distribution by
 // inverse CDF over S in the ranking order: the first j with
 // sum_{i<=j} w_pi(i) >= u * Z_S.  u in [0,1) is supplied per row.

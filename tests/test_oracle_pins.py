@@ -482,3 +482,44 @@ def test_support_errors(oracle):
     lp, ent, st = oracle.logprob_entropy_support(z[:2], ids[:2], 1.0,
                                                  np.array([0, 3, 1], np.int64), sup[:3])
     assert st[1] == 8 and np.isnan(lp[1])
+
+
+def test_support_backward_matches_finite_differences(oracle):
+    """The supplied-support gradient against central differences of the
+    (pinned) supplied-support forward, sets held fixed; plus the shift
+    invariance sum_j grad_j = 0 and the uniform closed form."""
+    rng = np.random.default_rng(9)
+    V, R, T = 12, 4, 0.7
+    z = rng.normal(0, 1.5, (R, V)).astype(np.float32)
+    lists = [np.array([0, 3, 5, 7, 11]), np.array([2, 4]), np.array([1, 6, 8, 9, 10, 3]),
+             np.array([0, 1, 2])]
+    ids = np.array([5, 4, 9, 7], np.int32)          # row 3: y not listed
+    off = np.concatenate([[0], np.cumsum([len(l) for l in lists])]).astype(np.int64)
+    sup = np.concatenate(lists).astype(np.int32)
+    gl = rng.normal(0, 1, R).astype(np.float32)
+    gh = rng.normal(0, 1, R).astype(np.float32)
+    g = oracle.logprob_entropy_support_backward(z, ids, T, off, sup, gl, gh)
+
+    def loss(zz):
+        lp, ent, _ = oracle.logprob_entropy_support(zz, ids, T, off, sup)
+        lp = np.where(np.isneginf(lp), 0.0, lp)       # y not listed: no log-prob term
+        return gl.astype(np.float64) * lp + gh.astype(np.float64) * ent
+
+    for r in range(R):
+        for jj, i in enumerate(lists[r]):
+            zp, zm = z.copy(), z.copy()
+            zp[r, i] = np.float32(z[r, i] + 1e-3)
+            zm[r, i] = np.float32(z[r, i] - 1e-3)
+            h = float(zp[r, i]) - float(zm[r, i])
+            fd = (loss(zp)[r] - loss(zm)[r]) / h
+            assert g[off[r] + jj] == pytest.approx(fd, abs=2e-6)
+        assert abs(g[off[r]:off[r + 1]].sum()) < 1e-12
+    # uniform logits over k listed ids: the entropy part vanishes
+    zu = np.zeros((1, V), np.float32)
+    lst = np.array([2, 5, 9], np.int32)
+    gu = oracle.logprob_entropy_support_backward(zu, np.array([5], np.int32), T,
+                                                 np.array([0, 3], np.int64), lst,
+                                                 np.array([1.5], np.float32), np.array([2.0], np.float32))
+    T32 = float(np.float32(T))
+    assert np.allclose(gu, [1.5 / T32 * (0 - 1 / 3), 1.5 / T32 * (1 - 1 / 3), 1.5 / T32 * (0 - 1 / 3)],
+                       atol=1e-14)
