@@ -498,29 +498,50 @@ def make_supports(z, top_p, temperature, chunk=256):
     return (torch.tensor(offs, dtype=torch.int64, device=z.device), torch.cat(lists))
 
 
-def run_support(args, ws, rank, dev, barrier):
-    """--op support: rlk_logprob_entropy_support on the benchmark rows, each
-    given its own top-p retained set."""
+SUP_BWD_METRIC = ("tokens/s for the supplied-support backward (gradient of logprob and entropy "
+                  "over the top-p retained set given as CSR) at V=151936 bf16")
+
+
+def run_support(args, ws, rank, dev, barrier, backward=False):
+    """--op support / support_backward: rlk_logprob_entropy_support, or its
+    backward, on the benchmark rows, each given its own top-p retained set."""
     import entropy_logits_bf16_gb300 as rlk
     stream = torch.cuda.current_stream(dev)
     z, ids = make_workload(dev, seed=rank_seed(rank))
     off, sup = make_supports(z, TOP_P, TEMPERATURE)
     lp = torch.empty(T_ROWS, device=dev)
     ent = torch.empty(T_ROWS, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(rank_seed(rank) + 1)
+    glp = torch.empty(T_ROWS).uniform_(-1, 1, generator=g).to(dev)
+    gh = torch.empty(T_ROWS).uniform_(-1, 1, generator=g).to(dev)
+    grad = torch.empty(sup.shape, device=dev)
 
     def call():
         rlk.logprob_entropy_support(z, ids, TEMPERATURE, off, sup, out_logprob=lp, out_entropy=ent)
 
-    elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [call], barrier)
+    def bcall():
+        rlk.logprob_entropy_support_backward(z, ids, TEMPERATURE, off, sup, glp, gh, out=grad)
+
+    elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [bcall if backward else call],
+                                           barrier)
     if rank != 0:
         return None
     peaks, peak_kind = measured_peaks()
     nnz = int(sup.numel())
-    alg = nnz * (4 + 2) + T_ROWS * (8 + 4 + 8)   # listed ids + their logits, offsets, id, outputs
-    sectors = nnz * 32 + nnz * 4 + T_ROWS * 20    # each listed logit costs one 32-byte sector
+    if backward:
+        # ids + logits read once (the second pass hits L2), gradients written,
+        # offsets, id and the two incoming gradients per row
+        alg = nnz * (4 + 2 + 4) + T_ROWS * (8 + 4 + 8)
+        sectors = nnz * 32 + nnz * 8 + T_ROWS * 20
+        kernel = "support_backward_kernel (one rlk_logprob_entropy_support_backward call)"
+    else:
+        alg = nnz * (4 + 2) + T_ROWS * (8 + 4 + 8)   # listed ids + their logits, offsets, id, outputs
+        sectors = nnz * 32 + nnz * 4 + T_ROWS * 20    # each listed logit costs one 32-byte sector
+        kernel = "support_kernel (one rlk_logprob_entropy_support call)"
     achieved = alg / (part_ms[0] / 1e3) / 1e9
     return {
-        "metric": SUP_METRIC, "value": whole_job_rate(T_ROWS, args.steps, ws, elapsed_ms),
+        "metric": SUP_BWD_METRIC if backward else SUP_METRIC,
+        "value": whole_job_rate(T_ROWS, args.steps, ws, elapsed_ms),
         "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -530,7 +551,7 @@ def run_support(args, ws, rank, dev, barrier):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peak_kind,
-                     "kernel": "support_kernel (one rlk_logprob_entropy_support call)",
+                     "kernel": kernel,
                      "algorithmic_bytes_per_launch": alg,
                      "sector_bytes_per_launch": sectors,
                      "sector_frac": sectors / (part_ms[0] / 1e3) / 1e9 / peaks["hbm_gbs"],
@@ -546,9 +567,10 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "support"],
+    ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "support", "support_backward"],
                     help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused "
-                         "LM-head; support: the supplied-support scorer")
+                         "LM-head; support: the supplied-support scorer; support_backward: its "
+                         "gradient")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -572,7 +594,8 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    run = {"logits": run_logits, "lmhead": run_lmhead, "support": run_support}[args.op]
+    run = {"logits": run_logits, "lmhead": run_lmhead, "support": run_support,
+           "support_backward": lambda *a: run_support(*a, backward=True)}[args.op]
     line = run(args, ws, rank, dev, barrier)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -28,7 +28,8 @@ NSTATS = 8
 STAT_NAMES = ("loss", "tokens", "clip_low_frac", "clip_high_frac", "tis_mean",
               "tis_capped_frac", "k3_mean", "pg_mean")
 EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logprob_entropy",
-           "rlk_logprob_entropy_support", "rlk_grpo_loss", "rlk_lmhead_logprob",
+           "rlk_logprob_entropy_support", "rlk_logprob_entropy_support_backward",
+           "rlk_grpo_loss", "rlk_lmhead_logprob",
            "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
 DEBUG_EXPORTS = ("rlk_lmhead_logits_debug",)
@@ -73,6 +74,9 @@ def load(path: str | None = None):
         lib.rlk_logprob_entropy_support.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, vp,
                                                     vp, vp, vp, vp, vp]
         lib.rlk_logprob_entropy_support.restype = ctypes.c_int
+        lib.rlk_logprob_entropy_support_backward.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp,
+                                                             f32, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logprob_entropy_support_backward.restype = ctypes.c_int
         lib.rlk_grpo_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, f32, f32, f32,
                                       f32, ctypes.c_int, vp, vp, vp, vp, sz, vp]
         lib.rlk_grpo_loss.restype = ctypes.c_int
@@ -183,6 +187,39 @@ def logprob_entropy_support(logits: torch.Tensor, token_ids: torch.Tensor, tempe
                                            _ptr(status_word), _stream(dev))
     _check("rlk_logprob_entropy_support", code)
     return lp, ent
+
+
+def logprob_entropy_support_backward(logits: torch.Tensor, token_ids: torch.Tensor,
+                                     temperature: float, support_offsets: torch.Tensor,
+                                     support_ids: torch.Tensor, grad_logprob=None,
+                                     grad_entropy=None, *, out=None, status_word=None):
+    """dL/dz for every listed id (aligned with ``support_ids``; the retained
+    sets held fixed) for L = sum grad_logprob * logprob + grad_entropy * H.
+    Returns a CUDA fp32 tensor shaped like ``support_ids``."""
+    lib = load()
+    _need_cuda(logits, token_ids, support_offsets, support_ids, grad_logprob, grad_entropy)
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be 2-D with unit stride along the vocabulary")
+    dt = {torch.bfloat16: 0, torch.float32: 1}.get(logits.dtype)
+    if dt is None:
+        raise ValueError("logits must be bf16 or fp32")
+    for t, want in ((token_ids, torch.int32), (support_offsets, torch.int64),
+                    (support_ids, torch.int32)):
+        if t.dtype != want or not t.is_contiguous():
+            raise ValueError("token_ids int32, support_offsets int64 and support_ids int32, contiguous")
+    for g in (grad_logprob, grad_entropy):
+        if g is not None and (g.dtype != torch.float32 or not g.is_contiguous()):
+            raise ValueError("gradients must be contiguous fp32")
+    T, V = logits.shape
+    ld = logits.stride(0) if T > 1 else V
+    grad = out if out is not None else torch.empty(support_ids.shape, device=logits.device,
+                                                   dtype=torch.float32)
+    code = lib.rlk_logprob_entropy_support_backward(
+        _ptr(logits), dt, T, V, ld, _ptr(token_ids), float(temperature), _ptr(support_offsets),
+        _ptr(support_ids), _ptr(grad_logprob), _ptr(grad_entropy), _ptr(grad), _ptr(status_word),
+        _stream(logits.device))
+    _check("rlk_logprob_entropy_support_backward", code)
+    return grad
 
 
 def grpo_loss(logp_new, logp_old, logp_rollout, logp_ref, rewards, seq_offsets, group_size, *,

@@ -34,6 +34,10 @@ struct SupportArgs {
   float* out_logprob;
   float* out_entropy;
   uint32_t* status;
+  // backward only
+  const float* grad_logprob;   // [T] or NULL
+  const float* grad_entropy;   // [T] or NULL
+  float* grad_support;         // [offsets[T]]
 };
 
 struct LossArgs {
@@ -72,6 +76,7 @@ bool lpe_cluster_eligible(const LpeArgs& a);
 cudaError_t launch_lpe_cluster(const LpeArgs& a, cudaStream_t stream);
 
 cudaError_t launch_support(const SupportArgs& a, cudaStream_t stream);
+cudaError_t launch_support_backward(const SupportArgs& a, cudaStream_t stream);
 
 constexpr int kLossPartials = 8;  // floats per sequence in the loss workspace
 size_t loss_workspace_bytes(int64_t n_seq);

@@ -109,7 +109,7 @@ rlk_status rlk_logprob_entropy_support(const void* logits, rlk_dtype dtype, int6
     return RLK_ERR_INVALID_ARG;
   const uintptr_t elem = dtype == RLK_BF16 ? 2u : 4u;
   if (reinterpret_cast<uintptr_t>(logits) % elem != 0) return RLK_ERR_INVALID_ARG;
-  rlk::SupportArgs a;
+  rlk::SupportArgs a{};
   a.logits = logits;
   a.dtype = dtype == RLK_BF16 ? 0 : 1;
   a.T = T;
@@ -123,6 +123,37 @@ rlk_status rlk_logprob_entropy_support(const void* logits, rlk_dtype dtype, int6
   a.out_entropy = out_entropy;
   a.status = out_status_word;
   return rlk::launch_support(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_logprob_entropy_support_backward(
+    const void* logits, rlk_dtype dtype, int64_t T, int64_t V, int64_t ld,
+    const int32_t* token_ids, float temperature, const int64_t* support_offsets,
+    const int32_t* support_ids, const float* grad_logprob, const float* grad_entropy,
+    float* grad_support, uint32_t* out_status_word, rlk_stream stream) {
+  if (dtype != RLK_BF16 && dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || ld < V) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  if (!logits || !token_ids || !support_offsets || !grad_support) return RLK_ERR_INVALID_ARG;
+  const uintptr_t elem = dtype == RLK_BF16 ? 2u : 4u;
+  if (reinterpret_cast<uintptr_t>(logits) % elem != 0) return RLK_ERR_INVALID_ARG;
+  rlk::SupportArgs a{};
+  a.logits = logits;
+  a.dtype = dtype == RLK_BF16 ? 0 : 1;
+  a.T = T;
+  a.V = V;
+  a.ld = ld;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.offsets = support_offsets;
+  a.support = support_ids;
+  a.status = out_status_word;
+  a.grad_logprob = grad_logprob;
+  a.grad_entropy = grad_entropy;
+  a.grad_support = grad_support;
+  return rlk::launch_support_backward(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
 }

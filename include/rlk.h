@@ -186,6 +186,34 @@ rlk_status rlk_logprob_entropy_support(const void* logits, rlk_dtype dtype, int6
                                        rlk_stream stream);
 
 /*
+ * rlk_logprob_entropy_support_backward -- gradient of the supplied-support
+ * scorer with respect to the listed logits.
+ *
+ * The backward of rlk_logprob_entropy_support with each row's retained set
+ * held fixed (the sampler chose it; RL-Kernel "Qwen3-8B VIME train-rollout
+ * consistency", section "ROCm MI300X and gfx942", scores that set), for the
+ * loss L = sum_t grad_logprob[t] logprob_t + grad_entropy[t] H_t:
+ *   q_i = exp(x_i - m_S) / Z_S over the listed ids (as in the forward);
+ *   grad_support[j] = dL/dz_i for i = support_ids[j]
+ *     = grad_logprob[t] ([i = y] - q_i) / T     (0 when y is not listed)
+ *       - grad_entropy[t] q_i (ln q_i + H_t) / T.
+ * Unlisted ids have zero gradient and are not written.
+ *
+ * Arguments: as rlk_logprob_entropy_support, plus
+ *  grad_logprob    device float[T] or NULL (all zero).
+ *  grad_entropy    device float[T] or NULL (all zero).
+ *  grad_support    device float[support_offsets[T]], aligned with
+ *                  support_ids; overwritten for every list position of every
+ *                  row (NaN for a row with a status).
+ * Errors: as rlk_logprob_entropy_support; grad_support may not be NULL.
+ */
+rlk_status rlk_logprob_entropy_support_backward(
+    const void* logits, rlk_dtype dtype, int64_t T, int64_t V, int64_t ld,
+    const int32_t* token_ids, float temperature, const int64_t* support_offsets,
+    const int32_t* support_ids, const float* grad_logprob, const float* grad_entropy,
+    float* grad_support, uint32_t* out_status_word, rlk_stream stream);
+
+/*
  * rlk_grpo_loss -- fused GRPO/DAPO loss with TIS correction and k3 KL.
  *
  * Sequences are packed: sequence s holds tokens [seq_offsets[s], seq_offsets[s+1]),

@@ -104,6 +104,29 @@ def test_support_empty_batch_is_a_no_op(lib):
     assert sup(lib, T=0, logits=None, ids=None, offs=None, sids=None, lp=None, ent=None) == 0
 
 
+def sup_bwd(lib, **kw):
+    args = dict(logits=FAKE, dtype=0, T=4, V=100, ld=100, ids=FAKE, temperature=0.7, offs=FAKE,
+                sids=FAKE, glp=None, gh=None, grad=FAKE)
+    args.update(kw)
+    return lib.rlk_logprob_entropy_support_backward(
+        args["logits"], args["dtype"], args["T"], args["V"], args["ld"], args["ids"],
+        args["temperature"], args["offs"], args["sids"], args["glp"], args["gh"], args["grad"],
+        None, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(temperature=0.0), dict(temperature=math.inf), dict(T=-1), dict(V=0),
+    dict(V=(1 << 24) + 1), dict(ld=99), dict(dtype=2), dict(logits=None), dict(ids=None),
+    dict(offs=None), dict(grad=None), dict(dtype=1, logits=ctypes.c_void_p(0x10002)),
+])
+def test_support_backward_rejects(lib, kw):
+    assert sup_bwd(lib, **kw) == 1
+
+
+def test_support_backward_empty_batch_is_a_no_op(lib):
+    assert sup_bwd(lib, T=0, logits=None, ids=None, offs=None, sids=None, grad=None) == 0
+
+
 def loss(lib, **kw):
     a = dict(n_seq=4, G=2, n_tok=10, el=0.2, eh=0.28, cap=2.0, kl=0.01, agg=0, ws=FAKE,
              ws_bytes=1 << 20, offs=FAKE, out=FAKE)
