@@ -56,6 +56,8 @@ def _load():
                                                            vp, vp, vp, i]
             lib.oracle_logprob_entropy_support_backward.argtypes = [vp, i, i64, i64, i64, vp, f32,
                                                                     vp, vp, vp, vp, vp, i]
+            lib.oracle_logprob_entropy_backward.argtypes = [vp, i, i64, i64, i64, vp, f32, f32,
+                                                            vp, vp, vp, vp, i]
             lib.oracle_grpo_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, f32,
                                              f32, f32, i, vp, vp, vp, vp]
             lib.oracle_lmhead_rows.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, f32, f32,
@@ -63,7 +65,7 @@ def _load():
             for fn in (lib.oracle_logprob_entropy, lib.oracle_sample_ids,
                        lib.oracle_logprob_entropy_support,
                        lib.oracle_logprob_entropy_support_backward,
-                       lib.oracle_grpo_loss, lib.oracle_lmhead_rows):
+                       lib.oracle_logprob_entropy_backward, lib.oracle_grpo_loss, lib.oracle_lmhead_rows):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -139,6 +141,27 @@ def logprob_entropy_support(logits, ids, temperature, offsets, support_ids, thre
     if rc:
         raise ValueError("oracle_logprob_entropy_support rejected its arguments")
     return lp, ent, st
+
+
+def logprob_entropy_backward(logits, ids, temperature, top_p, g_logprob=None, g_entropy=None,
+                             force_k=None, threads=None):
+    """Dense dL/dz [T, V] (fp64) of the logits path for
+    L = sum_t g_logprob[t] logprob_t + g_entropy[t] H_t, each row's retained set
+    held fixed; zero outside the set, NaN on rows with no distribution."""
+    a, dt = _logits_array(logits)
+    T, V = a.shape
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    gl = None if g_logprob is None else np.ascontiguousarray(g_logprob, dtype=np.float32)
+    gh = None if g_entropy is None else np.ascontiguousarray(g_entropy, dtype=np.float32)
+    fk = None if force_k is None else np.ascontiguousarray(force_k, dtype=np.int64)
+    out = np.empty((T, V), np.float64)
+    rc = _load().oracle_logprob_entropy_backward(
+        _ptr(a), dt, T, V, V, _ptr(ids), float(np.float32(temperature)),
+        float(np.float32(top_p)), _ptr(fk), _ptr(gl), _ptr(gh), _ptr(out),
+        threads or default_threads())
+    if rc:
+        raise ValueError("oracle_logprob_entropy_backward rejected its arguments")
+    return out
 
 
 def logprob_entropy_support_backward(logits, ids, temperature, offsets, support_ids, g_logprob=None,

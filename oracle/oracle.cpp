@@ -107,12 +107,23 @@ struct RowResult {
 //  8. gap = min(|top_p - C_{k*-1}|, |C_{k*} - top_p|), +inf when top_p >= 1.
 // force_k > 0 evaluates steps 5-7 at that k instead of k* (rows whose gap is
 // too small for the nucleus to be unique).
-RowResult score_row(const std::vector<double>& z, int64_t y, double T, double p, int64_t force_k) {
+// grad (optional, V entries): dL/dz for L = glp logprob + gh H with S held
+// fixed (S moves only where a logit crosses the boundary, so almost everywhere
+// it is locally constant):
+//  9. grad_i = 0 for i outside S; for i in S, with q_i = w_i / Z_S,
+//     grad_i = glp [y in S] ([i = y] - q_i) / T - gh q_i (ln q_i + H) / T.
+// A row with no distribution gets NaN in every entry.
+RowResult score_row(const std::vector<double>& z, int64_t y, double T, double p, int64_t force_k,
+                    double glp = 0.0, double gh = 0.0, double* grad = nullptr) {
   const int64_t V = static_cast<int64_t>(z.size());
   RowResult r{kNaN, kNaN, kNaN, 0};
+  bool bad = y < 0 || y >= V;         // selected id outside the vocabulary
   for (double v : z)
-    if (!std::isfinite(v)) return r;  // non-finite logit: no distribution
-  if (y < 0 || y >= V) return r;      // selected id outside the vocabulary
+    if (!std::isfinite(v)) bad = true;  // non-finite logit: no distribution
+  if (bad) {
+    if (grad) std::fill(grad, grad + V, kNaN);
+    return r;
+  }
 
   std::vector<double> x(V), w(V);
   double m = -kInf;
@@ -178,6 +189,19 @@ RowResult score_row(const std::vector<double>& z, int64_t y, double T, double p,
     if (q > 0.0) h.add(-q * std::log(q));
   }
   r.entropy = h.value();
+  if (grad) {
+    const double H = r.entropy;
+    for (int64_t i = 0; i < V; ++i) {
+      if (!member[i]) {
+        grad[i] = 0.0;
+        continue;
+      }
+      const double q = w[i] / ZS;
+      const double dlp = member[y] ? ((i == y ? 1.0 : 0.0) - q) / T : 0.0;
+      const double lq = q > 0.0 ? std::log(q) : 0.0;   // q ln q -> 0 as q -> 0
+      grad[i] = glp * dlp - gh * q * (lq + H) / T;
+    }
+  }
   return r;
 }
 
@@ -209,6 +233,26 @@ int oracle_logprob_entropy(const void* logits, int dtype, int64_t T, int64_t V, 
     if (out_entropy) out_entropy[row] = r.entropy;
     if (out_k) out_k[row] = r.k;
     if (out_gap) out_gap[row] = r.gap;
+  });
+  return 0;
+}
+
+// Gradient of the logits path (steps 1-9 of score_row): out_grad[T, V] (fp64,
+// dense, row stride V) = dL/dz for L = sum_t g_lp[t] logprob_t + g_h[t] H_t,
+// the retained sets held fixed.  g_lp / g_h may be NULL (zero); force_k as for
+// oracle_logprob_entropy.
+int oracle_logprob_entropy_backward(const void* logits, int dtype, int64_t T, int64_t V, int64_t ld,
+                                    const int32_t* ids, float temperature, float top_p,
+                                    const int64_t* force_k, const float* g_lp, const float* g_h,
+                                    double* out_grad, int nthreads) {
+  if (!logits || !ids || !out_grad || T < 0 || V < 1 || ld < V || (dtype != 0 && dtype != 1))
+    return 1;
+  const double Td = static_cast<double>(temperature), pd = static_cast<double>(top_p);
+  parallel_rows(T, nthreads, [&](int64_t row) {
+    std::vector<double> z = widen_row(logits, dtype, row, V, ld);
+    score_row(z, ids[row], Td, pd, force_k ? force_k[row] : 0,
+              g_lp ? static_cast<double>(g_lp[row]) : 0.0,
+              g_h ? static_cast<double>(g_h[row]) : 0.0, out_grad + row * V);
   });
   return 0;
 }

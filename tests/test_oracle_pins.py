@@ -523,3 +523,95 @@ def test_support_backward_matches_finite_differences(oracle):
     T32 = float(np.float32(T))
     assert np.allclose(gu, [1.5 / T32 * (0 - 1 / 3), 1.5 / T32 * (1 - 1 / 3), 1.5 / T32 * (0 - 1 / 3)],
                        atol=1e-14)
+
+
+def _dense_loss(oracle, z, ids, T, p, gl, gh):
+    lp, ent, k, _ = oracle.logprob_entropy(z, ids, T, p)
+    lp = np.where(np.isneginf(lp), 0.0, lp)           # y outside S: no log-prob term
+    return gl.astype(np.float64) * lp + gh.astype(np.float64) * ent, k
+
+
+@pytest.mark.parametrize("p", [0.5, 0.8, 1.0])
+def test_dense_backward_matches_finite_differences(oracle, p):
+    """The dense top-p gradient against central differences of the (pinned)
+    forward wherever a step of +-1e-3 leaves k* alone: members and non-members
+    alike (non-members must come out exactly 0)."""
+    rng = np.random.default_rng(21)
+    V, R, T = 16, 6, 0.8
+    # distinct values 0.07 apart, so a 1e-3 step never reorders the ranking
+    z = np.stack([rng.permutation(np.arange(V) * 0.07 * 3) for _ in range(R)]).astype(np.float32)
+    ids = rng.integers(0, V, R).astype(np.int32)
+    gl = rng.normal(0, 1, R).astype(np.float32)
+    gh = rng.normal(0, 1, R).astype(np.float32)
+    g = oracle.logprob_entropy_backward(z, ids, T, p, gl, gh)
+    base, k0 = _dense_loss(oracle, z, ids, T, p, gl, gh)
+    checked = 0
+    for r in range(R):
+        for i in range(V):
+            zp, zm = z.copy(), z.copy()
+            zp[r, i] = np.float32(z[r, i] + 1e-3)
+            zm[r, i] = np.float32(z[r, i] - 1e-3)
+            lp_, kp = _dense_loss(oracle, zp, ids, T, p, gl, gh)
+            lm_, km = _dense_loss(oracle, zm, ids, T, p, gl, gh)
+            if kp[r] != k0[r] or km[r] != k0[r]:
+                continue                                # the step moved the boundary
+            fd = (lp_[r] - lm_[r]) / (float(zp[r, i]) - float(zm[r, i]))
+            assert g[r, i] == pytest.approx(fd, abs=2e-6)
+            checked += 1
+        assert abs(g[r].sum()) < 1e-12                  # shift invariance
+    assert checked >= R * V * 3 // 4
+
+
+def test_dense_backward_top_p_one_is_softmax_gradient(oracle):
+    """top_p = 1, entropy weight 0: grad = g (onehot(y) - softmax(z / T)) / T,
+    the softmax from the library."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(3)
+    T = 0.7
+    z = rng.normal(0, 2, (5, 300)).astype(np.float32)
+    ids = rng.integers(0, 300, 5).astype(np.int32)
+    gl = rng.normal(0, 1, 5).astype(np.float32)
+    g = oracle.logprob_entropy_backward(z, ids, T, 1.0, gl, None)
+    T32 = float(np.float32(T))
+    q = softmax(z.astype(np.float64) / T32, axis=1)
+    onehot = np.zeros_like(q)
+    onehot[np.arange(5), ids] = 1.0
+    assert np.allclose(g, gl[:, None].astype(np.float64) * (onehot - q) / T32, atol=1e-14)
+
+
+def test_dense_backward_equals_support_backward_on_the_nucleus(oracle):
+    """Restricted to its nucleus (found here by an independent sort), the
+    dense gradient is the supplied-support gradient of that set; elsewhere 0.
+    bf16 logits with many ties, so the id order inside the boundary value
+    matters."""
+    rng = np.random.default_rng(8)
+    R, V, T, p = 6, 3000, 0.7, 0.9
+    # a 0.25 grid: every value is shared by dozens of ids
+    z = torch.from_numpy(np.round(rng.normal(0, 1, (R, V)) * 4).astype(np.float32) / 4).to(
+        torch.bfloat16)
+    hz = z.view(torch.int16).numpy().view(np.uint16)
+    vals = (hz.astype(np.uint32) << 16).view(np.float32)
+    ids = rng.integers(0, V, R).astype(np.int32)
+    gl = rng.normal(0, 1, R).astype(np.float32)
+    gh = rng.normal(0, 1, R).astype(np.float32)
+    _, _, k, gap = oracle.logprob_entropy(hz, ids, T, p)
+    g = oracle.logprob_entropy_backward(hz, ids, T, p, gl, gh)
+    lists = [np.lexsort((np.arange(V), -vals[r]))[:k[r]] for r in range(R)]
+    off = np.concatenate([[0], np.cumsum([len(l) for l in lists])]).astype(np.int64)
+    sup = np.concatenate(lists).astype(np.int32)
+    gs = oracle.logprob_entropy_support_backward(hz, ids, T, off, sup, gl, gh)
+    for r in range(R):
+        want = np.zeros(V)
+        want[lists[r]] = gs[off[r]:off[r + 1]]
+        assert np.allclose(g[r], want, rtol=1e-12, atol=1e-15)
+        t = vals[r][lists[r][-1]]
+        kept = (vals[r][lists[r]] == t).sum()
+        assert 0 < kept < (vals[r] == t).sum()          # the boundary value's ties are split
+
+
+def test_dense_backward_bad_rows_are_nan(oracle):
+    z = np.zeros((3, 10), np.float32)
+    z[1, 4] = np.inf
+    g = oracle.logprob_entropy_backward(z, np.array([0, 1, 10], np.int32), 1.0, 0.9,
+                                        np.ones(3, np.float32), np.ones(3, np.float32))
+    assert np.all(np.isfinite(g[0])) and np.all(np.isnan(g[1])) and np.all(np.isnan(g[2]))
