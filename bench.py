@@ -561,16 +561,62 @@ def run_support(args, ws, rank, dev, barrier, backward=False):
     }
 
 
+BWD_METRIC = ("tokens/s for the dense top-p backward (dL/dlogits over V=151936, bf16 logits and "
+              "gradients, retained sets from the forward)")
+
+
+def run_backward(args, ws, rank, dev, barrier):
+    """--op backward: rlk_logprob_entropy_bwd on the benchmark rows (their row
+    states saved by one forward before the timed region), bf16 gradients."""
+    import entropy_logits_bf16_gb300 as rlk
+    stream = torch.cuda.current_stream(dev)
+    z, ids = make_workload(dev, seed=rank_seed(rank))
+    state = rlk.new_row_state(T_ROWS, dev)
+    rlk.logprob_entropy(z, ids, TEMPERATURE, TOP_P, row_state=state)
+    g = torch.Generator(device="cpu").manual_seed(rank_seed(rank) + 2)
+    glp = torch.empty(T_ROWS).uniform_(-1, 1, generator=g).to(dev)
+    gh = torch.empty(T_ROWS).uniform_(-1, 1, generator=g).to(dev)
+    grad = torch.empty((T_ROWS, VOCAB), device=dev, dtype=torch.bfloat16)
+
+    def call():
+        rlk.logprob_entropy_backward(z, ids, TEMPERATURE, state, glp, gh, out=grad)
+
+    elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [call], barrier)
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    # logits read + gradients written, plus per row the state, id and two gradients
+    alg = T_ROWS * VOCAB * (2 + 2) + T_ROWS * (32 + 4 + 8)
+    achieved = alg / (part_ms[0] / 1e3) / 1e9
+    return {
+        "metric": BWD_METRIC, "value": whole_job_rate(T_ROWS, args.steps, ws, elapsed_ms),
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD + "; gradients of logprob and entropy, bf16 out",
+                   "T": T_ROWS, "V": VOCAB, "global_batch": T_ROWS * ws,
+                   "l2": "inputs larger than L2 (1.24 GB read + 1.24 GB written per step)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peak_kind,
+                     "kernel": "lpe_backward_kernel (one rlk_logprob_entropy_bwd call)",
+                     "algorithmic_bytes_per_launch": alg, "launch_ms": part_ms[0]},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "support", "support_backward"],
+    ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "support", "support_backward",
+                                                       "backward"],
                     help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused "
                          "LM-head; support: the supplied-support scorer; support_backward: its "
-                         "gradient")
+                         "gradient; backward: the dense top-p gradient")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -595,7 +641,8 @@ def main():
         torch.cuda.synchronize(dev)
 
     run = {"logits": run_logits, "lmhead": run_lmhead, "support": run_support,
-           "support_backward": lambda *a: run_support(*a, backward=True)}[args.op]
+           "support_backward": lambda *a: run_support(*a, backward=True),
+           "backward": run_backward}[args.op]
     line = run(args, ws, rank, dev, barrier)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -28,6 +28,7 @@ NSTATS = 8
 STAT_NAMES = ("loss", "tokens", "clip_low_frac", "clip_high_frac", "tis_mean",
               "tis_capped_frac", "k3_mean", "pg_mean")
 EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logprob_entropy",
+           "rlk_logprob_entropy_fwd", "rlk_logprob_entropy_bwd",
            "rlk_logprob_entropy_support", "rlk_logprob_entropy_support_backward",
            "rlk_grpo_loss", "rlk_lmhead_logprob",
            "rlk_grpo_loss_noalloc")
@@ -35,6 +36,8 @@ NOALLOC_MAX_SEQ = 16384
 DEBUG_EXPORTS = ("rlk_lmhead_logits_debug",)
 STATUS_TIMEOUT = 0x4
 STATUS_BAD_SUPPORT = 0x8
+STATUS_NO_STATE = 0x10
+ROW_STATE_WORDS = 8   # rlk_row_state: 32 bytes per row
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +74,12 @@ def load(path: str | None = None):
         lib.rlk_logprob_entropy.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, f32, vp,
                                             vp, vp, vp, vp, sz, vp]
         lib.rlk_logprob_entropy.restype = ctypes.c_int
+        lib.rlk_logprob_entropy_fwd.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, f32, vp,
+                                                vp, vp, vp, vp, vp]
+        lib.rlk_logprob_entropy_fwd.restype = ctypes.c_int
+        lib.rlk_logprob_entropy_bwd.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, vp, vp,
+                                                vp, vp, ctypes.c_int, i64, vp, vp]
+        lib.rlk_logprob_entropy_bwd.restype = ctypes.c_int
         lib.rlk_logprob_entropy_support.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, vp,
                                                     vp, vp, vp, vp, vp]
         lib.rlk_logprob_entropy_support.restype = ctypes.c_int
@@ -116,15 +125,32 @@ def workspace_size(op: int, T: int, V: int, H: int = 0) -> int:
     return int(load().rlk_workspace_size(op, T, V, H))
 
 
+def _logits_dtype(logits):
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be 2-D with unit stride along the vocabulary")
+    dt = {torch.bfloat16: 0, torch.float32: 1}.get(logits.dtype)
+    if dt is None:
+        raise ValueError("logits must be bf16 or fp32")
+    return dt
+
+
+def new_row_state(T: int, device) -> torch.Tensor:
+    """Room for the per-row state the forward saves for the backward
+    (rlk_row_state[T], 32 bytes a row)."""
+    return torch.empty((T, ROW_STATE_WORDS), dtype=torch.int32, device=device)
+
+
 def logprob_entropy(logits: torch.Tensor, token_ids: torch.Tensor, temperature: float,
                     top_p: float, *, out_logprob=None, out_entropy=None,
-                    return_nucleus_size: bool = False, status_word: torch.Tensor | None = None):
+                    return_nucleus_size: bool = False, status_word: torch.Tensor | None = None,
+                    row_state: torch.Tensor | None = None):
     """Top-p log-probability of the selected token and entropy of the retained set.
 
     logits: CUDA [T, V] bf16 or fp32 (rows may be strided, unit stride along V);
     token_ids: CUDA int32 [T].  Returns (logprob, entropy) fp32 [T], plus the
     nucleus sizes int32 [T] when ``return_nucleus_size``.  ``status_word`` (CUDA
-    uint32/int32 [1]) receives the STATUS_* bits of bad rows.
+    uint32/int32 [1]) receives the STATUS_* bits of bad rows.  ``row_state``
+    (from ``new_row_state``) receives what ``logprob_entropy_backward`` needs.
     """
     lib = load()
     _need_cuda(logits, token_ids)
@@ -144,11 +170,88 @@ def logprob_entropy(logits: torch.Tensor, token_ids: torch.Tensor, temperature: 
     lp = out_logprob if out_logprob is not None else torch.empty(T, device=dev, dtype=torch.float32)
     ent = out_entropy if out_entropy is not None else torch.empty(T, device=dev, dtype=torch.float32)
     ks = torch.empty(T, device=dev, dtype=torch.int32) if return_nucleus_size else None
-    code = lib.rlk_logprob_entropy(_ptr(logits), dt, T, V, ld, _ptr(token_ids), float(temperature),
-                                   float(top_p), _ptr(lp), _ptr(ent), _ptr(ks), _ptr(status_word),
-                                   None, 0, _stream(dev))
-    _check("rlk_logprob_entropy", code)
+    if row_state is not None:
+        _need_cuda(row_state)
+        if (row_state.dtype != torch.int32 or not row_state.is_contiguous()
+                or row_state.numel() != T * ROW_STATE_WORDS):
+            raise ValueError("row_state must come from new_row_state(T)")
+        code = lib.rlk_logprob_entropy_fwd(_ptr(logits), dt, T, V, ld, _ptr(token_ids),
+                                           float(temperature), float(top_p), _ptr(lp), _ptr(ent),
+                                           _ptr(ks), _ptr(row_state), _ptr(status_word),
+                                           _stream(dev))
+        _check("rlk_logprob_entropy_fwd", code)
+    else:
+        code = lib.rlk_logprob_entropy(_ptr(logits), dt, T, V, ld, _ptr(token_ids),
+                                       float(temperature), float(top_p), _ptr(lp), _ptr(ent),
+                                       _ptr(ks), _ptr(status_word), None, 0, _stream(dev))
+        _check("rlk_logprob_entropy", code)
     return (lp, ent, ks) if return_nucleus_size else (lp, ent)
+
+
+def logprob_entropy_backward(logits: torch.Tensor, token_ids: torch.Tensor, temperature: float,
+                             row_state: torch.Tensor, grad_logprob=None, grad_entropy=None, *,
+                             out=None, grad_dtype=None, status_word=None):
+    """dL/dlogits [T, V] for L = sum grad_logprob * logprob + grad_entropy * H,
+    each row's retained set (saved in ``row_state`` by the forward) held fixed;
+    zero outside the set.  ``grad_dtype`` (bf16 or fp32) defaults to the
+    logits' dtype; ``out`` may be a strided [T, V] tensor of that dtype."""
+    lib = load()
+    _need_cuda(logits, token_ids, row_state, grad_logprob, grad_entropy, out)
+    dt = _logits_dtype(logits)
+    if token_ids.dtype != torch.int32 or not token_ids.is_contiguous():
+        raise ValueError("token_ids must be contiguous int32")
+    T, V = logits.shape
+    if (row_state.dtype != torch.int32 or not row_state.is_contiguous()
+            or row_state.numel() != T * ROW_STATE_WORDS):
+        raise ValueError("row_state must come from new_row_state(T)")
+    for g in (grad_logprob, grad_entropy):
+        if g is not None and (g.dtype != torch.float32 or not g.is_contiguous() or g.numel() != T):
+            raise ValueError("gradients must be contiguous fp32 [T]")
+    gdt = grad_dtype or (out.dtype if out is not None else logits.dtype)
+    if out is None:
+        out = torch.empty((T, V), device=logits.device, dtype=gdt)
+    if out.dtype != gdt or out.shape != (T, V) or out.stride(1) != 1:
+        raise ValueError("out must be [T, V] of grad_dtype with unit stride along V")
+    gd = {torch.bfloat16: 0, torch.float32: 1}.get(gdt)
+    if gd is None:
+        raise ValueError("grad_dtype must be bf16 or fp32")
+    ld = logits.stride(0) if T > 1 else V
+    ldg = out.stride(0) if T > 1 else V
+    code = lib.rlk_logprob_entropy_bwd(_ptr(logits), dt, T, V, ld, _ptr(token_ids),
+                                       float(temperature), _ptr(row_state), _ptr(grad_logprob),
+                                       _ptr(grad_entropy), _ptr(out), gd, ldg, _ptr(status_word),
+                                       _stream(logits.device))
+    _check("rlk_logprob_entropy_bwd", code)
+    return out
+
+
+class _LogprobEntropy(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, logits, token_ids, temperature, top_p):
+        state = new_row_state(logits.shape[0], logits.device)
+        lp, ent = logprob_entropy(logits, token_ids, temperature, top_p, row_state=state)
+        ctx.save_for_backward(logits, token_ids, state)
+        ctx.temperature = temperature
+        ctx.set_materialize_grads(False)
+        return lp, ent
+
+    @staticmethod
+    def backward(ctx, g_lp, g_ent):
+        logits, token_ids, state = ctx.saved_tensors
+        if g_lp is None and g_ent is None:
+            return None, None, None, None
+        g = logprob_entropy_backward(
+            logits, token_ids, ctx.temperature, state,
+            None if g_lp is None else g_lp.float().contiguous(),
+            None if g_ent is None else g_ent.float().contiguous())
+        return g, None, None, None
+
+
+def logprob_entropy_autograd(logits: torch.Tensor, token_ids: torch.Tensor, temperature: float,
+                             top_p: float):
+    """``logprob_entropy`` as a differentiable op: (logprob, entropy) whose
+    backward is ``rlk_logprob_entropy_bwd`` (the retained sets held fixed)."""
+    return _LogprobEntropy.apply(logits, token_ids, temperature, top_p)
 
 
 def logprob_entropy_support(logits: torch.Tensor, token_ids: torch.Tensor, temperature: float,

@@ -6,6 +6,23 @@
 
 namespace rlk {
 
+// What the forward saves per row for the backward (the ABI's rlk_row_state,
+// 32 bytes).  With c = log2(e) / T:
+//   q_i = 2^(z_i c - E) / e^lz for i in S, and S = { i : key(z_i) > key_thr }
+//   plus the first `ties` ids (ascending) with key(z_i) == key_thr (all of
+//   them when ties == kTiesAll).  key is the order-preserving key of the
+//   logits' own type (16-bit for bf16, 32-bit for fp32).
+struct RowState {
+  float E, lz, H;
+  uint32_t key_thr, ties, flags;   // flags: kState* bits | row status << 8
+  int32_t kstar;
+  uint32_t reserved;
+};
+static_assert(sizeof(RowState) == 32, "rlk_row_state is 32 bytes");
+constexpr uint32_t kStateValid = 1u;   // the forward finished the row
+constexpr uint32_t kStateYIn = 2u;     // the selected token is in S
+constexpr uint32_t kTiesAll = 0xFFFFFFFFu;
+
 struct LpeArgs {
   const void* logits;
   int dtype;  // 0 bf16, 1 fp32
@@ -17,6 +34,22 @@ struct LpeArgs {
   int32_t* out_k;
   uint32_t* status;
   int only_marked;  // per-row kernel: process only rows whose out_logprob holds kRecomputeMark
+  RowState* state;  // [T] or NULL
+};
+
+struct LpeBwdArgs {
+  const void* logits;
+  int dtype;  // 0 bf16, 1 fp32
+  int64_t T, V, ld;
+  const int32_t* ids;
+  float temperature;
+  const RowState* state;
+  const float* grad_logprob;   // [T] or NULL
+  const float* grad_entropy;   // [T] or NULL
+  void* grad_logits;           // [T, ldg]
+  int grad_dtype;              // 0 bf16, 1 fp32
+  int64_t ldg;
+  uint32_t* status;
 };
 
 // A quiet-NaN payload that no arithmetic produces: the cluster kernel leaves it
@@ -76,6 +109,7 @@ bool lpe_cluster_eligible(const LpeArgs& a);
 cudaError_t launch_lpe_cluster(const LpeArgs& a, cudaStream_t stream);
 
 cudaError_t launch_support(const SupportArgs& a, cudaStream_t stream);
+cudaError_t launch_logprob_entropy_backward(const LpeBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_support_backward(const SupportArgs& a, cudaStream_t stream);
 
 constexpr int kLossPartials = 8;  // floats per sequence in the loss workspace

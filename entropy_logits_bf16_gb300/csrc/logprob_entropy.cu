@@ -791,7 +791,7 @@ template <class Row>
 __device__ __noinline__ void select_by_bisection(const Row& row, int tid, float m, float c, float inv_t,
                                     DF target, uint32_t key_y, int64_t y, Smem& sm,
                                     bool& all_tokens, DF& zs, float& us, uint32_t& kstar,
-                                    bool& y_in) {
+                                    bool& y_in, uint32_t& key_thr, uint32_t& ties) {
   auto mass_ge = [&](uint32_t t) -> DF {
     DF acc{0.f, 0.f};
     float dummy = 0.f;
@@ -848,6 +848,8 @@ __device__ __noinline__ void select_by_bisection(const Row& row, int tid, float 
   us = __fmaf_rn(__fmul_rn((float)cneed, wt), xt, ugt);
   kstar = cnt[0] + cneed;
   y_in = (key_y > tau) || (key_y == tau && cnt[2] < cneed);
+  key_thr = tau;
+  ties = cneed == cnt[1] ? kTiesAll : cneed;
 }
 
 // Threshold-bin bookkeeping shared by the histogram paths: the number of tied
@@ -855,7 +857,7 @@ __device__ __noinline__ void select_by_bisection(const Row& row, int tid, float 
 __device__ __forceinline__ void finish_from_scan(const Smem& sm, DF target, int dstar,
                                                  uint32_t ck_m, uint32_t key_y, uint32_t tie_y,
                                                  DF& zs, float& us, uint32_t& kstar,
-                                                 bool& y_in) {
+                                                 bool& y_in, uint32_t& key_thr, uint32_t& ties) {
   const DF pb{sm.r_pb_hi, sm.r_pb_lo};
   const float wt = sm.r_w, xt = sm.r_x;
   const uint32_t nt = sm.r_n;
@@ -865,6 +867,8 @@ __device__ __forceinline__ void finish_from_scan(const Smem& sm, DF target, int 
   zs = df_add_f(pb, __fmul_rn((float)cneed, wt));
   us = __fmaf_rn(__fmul_rn((float)cneed, wt), xt, sm.r_um_before);
   kstar = sm.r_cnt_before + cneed;
+  key_thr = expand_key(ck_m - (uint32_t)dstar);
+  ties = cneed == nt ? kTiesAll : cneed;
   const uint32_t d_y = ck_m - compress_key(key_y);
   y_in = (d_y < (uint32_t)dstar) || (d_y == (uint32_t)dstar && tie_y < cneed);
 }
@@ -886,6 +890,22 @@ __device__ __noinline__ float full_entropy_numerator(const RowBf16& row, int tid
   });
   block_sum_df(dummy, u, sm, tid);
   return u;
+}
+
+// The saved state of a finished row.  The sums here are taken relative to m
+// (w = 2^((z - m) c)); the state's reference is E = fp32(m c), so ln Z_S moves
+// by ln2 (m c - E), computed exactly by one fma.
+__device__ __forceinline__ void write_state(const LpeArgs& a, int64_t r, float m, float c, float lz,
+                                            float h, uint32_t key_thr, uint32_t ties, bool y_in,
+                                            uint32_t kstar) {
+  const float E = __fmul_rn(m, c);
+  const float lzE = __fmaf_rn(kLn2, __fmaf_rn(m, c, -E), lz);
+  a.state[r] = RowState{E, lzE, h, key_thr, ties, kStateValid | (y_in ? kStateYIn : 0u),
+                        (int32_t)kstar, 0u};
+}
+
+__device__ __forceinline__ void write_bad_state(const LpeArgs& a, int64_t r, uint32_t bit) {
+  if (a.state) a.state[r] = RowState{0.f, 0.f, 0.f, 0u, 0u, bit << 8, 0, 0u};
 }
 
 // --------------------------------------------------------------- kernel
@@ -921,6 +941,7 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
         a.out_entropy[r] = NAN;
         if (a.out_k) a.out_k[r] = 0;
         if (a.status) atomicOr(a.status, RLK_STATUS_BAD_TOKEN_ID);
+        write_bad_state(a, r, RLK_STATUS_BAD_TOKEN_ID);
       }
       continue;
     }
@@ -957,6 +978,7 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
         a.out_entropy[r] = NAN;
         if (a.out_k) a.out_k[r] = 0;
         if (a.status) atomicOr(a.status, RLK_STATUS_NONFINITE);
+        write_bad_state(a, r, RLK_STATUS_NONFINITE);
       }
       __syncthreads();
       continue;
@@ -965,9 +987,11 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
     if (!TOPP) {
       if (tid == 0) {
         const float lz = logf(zf);
+        const float h = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, st.u), zf));
         a.out_logprob[r] = __fsub_rn(x_y, lz);
-        a.out_entropy[r] = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, st.u), zf));
+        a.out_entropy[r] = h;
         if (a.out_k) a.out_k[r] = (int32_t)a.V;
+        if (a.state) write_state(a, r, m, c, lz, h, 0u, kTiesAll, true, (uint32_t)a.V);
       }
       continue;
     }
@@ -985,7 +1009,7 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
     bool all_tokens = false, y_in = false, use_bisect = !HIST;
     DF zs{0.f, 0.f};
     float us = 0.f;
-    uint32_t kstar = 0u;
+    uint32_t kstar = 0u, key_thr = 0u, ties = kTiesAll;
 
     if constexpr (HIST) {
       const uint32_t ck_m = compress_key(Row::key(m));
@@ -1020,7 +1044,8 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
           continue;
         }
         if ((uint32_t)dstar == d_merged) { use_bisect = true; break; }
-        finish_from_scan(sm, target, dstar, ck_m, key_y, cnt2[0], zs, us, kstar, y_in);
+        finish_from_scan(sm, target, dstar, ck_m, key_y, cnt2[0], zs, us, kstar, y_in, key_thr,
+                         ties);
         done = true;
       }
       __syncthreads();
@@ -1029,7 +1054,7 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
     if (use_bisect) {
       all_tokens = false;
       select_by_bisection(row, tid, m, c, inv_t, target, key_y, y, sm, all_tokens, zs, us,
-                          kstar, y_in);
+                          kstar, y_in, key_thr, ties);
       if (all_tokens) {
         if constexpr (HIST) us = full_entropy_numerator(row, tid, m, c, inv_t, sm);
         else us = __fmul_rn(kLn2, st.u);
@@ -1042,6 +1067,8 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
         hval = __fsub_rn(lz, __fdiv_rn(us, zf));
         kstar = (uint32_t)a.V;
         y_in = true;
+        key_thr = 0u;
+        ties = kTiesAll;
       } else {
         const float zsf = __fadd_rn(zs.hi, zs.lo);
         lz = logf(zsf);
@@ -1050,6 +1077,7 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
       a.out_logprob[r] = y_in ? __fsub_rn(x_y, lz) : -INFINITY;
       a.out_entropy[r] = hval;
       if (a.out_k) a.out_k[r] = (int32_t)kstar;
+      if (a.state) write_state(a, r, m, c, lz, hval, key_thr, ties, y_in, kstar);
     }
     __syncthreads();
   }

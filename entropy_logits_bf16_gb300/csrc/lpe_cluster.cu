@@ -209,6 +209,7 @@ struct ScanOut {
   uint32_t kstar;
   float lz, h;
   bool y_in;
+  uint32_t key_thr, ties;   // the boundary key and its tied tokens kept (kTiesAll: all)
 };
 
 // One warp scans the window's bins 0..dmax (distance below the max key) in a
@@ -280,7 +281,7 @@ __device__ bool warp_scan_window(int lane, uint32_t dmax, uint32_t key_m, float 
   const uint32_t bal = __ballot_sync(0xFFFFFFFFu, my_d >= 0);
   if (bal == 0u) return false;
   const int win = __ffs(bal) - 1;   // the lowest lane holds the lowest crossing bin
-  uint32_t kstar = 0u;
+  uint32_t kstar = 0u, ties = 0u;
   int y_in = 0;
   float lz = 0.f, h = 0.f;
   if (lane == win) {
@@ -292,12 +293,15 @@ __device__ bool warp_scan_window(int lane, uint32_t dmax, uint32_t key_m, float 
     const float us = __fmaf_rn(wn, dt, ub);
     const uint32_t d_y = key_m - key_y;
     kstar = cb + cneed;
+    ties = cneed == nt ? kTiesAll : cneed;
     y_in = (d_y < (uint32_t)my_d) || (d_y == (uint32_t)my_d && tie_y < cneed);
     const float zsf = __fadd_rn(zs.hi, zs.lo);
     lz = logf(zsf);
     h = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, us), zsf));
   }
   out.kstar = __shfl_sync(0xFFFFFFFFu, kstar, win);
+  out.ties = __shfl_sync(0xFFFFFFFFu, ties, win);
+  out.key_thr = key_m - (uint32_t)__shfl_sync(0xFFFFFFFFu, my_d, win);
   out.y_in = __shfl_sync(0xFFFFFFFFu, y_in, win) != 0;
   out.lz = __shfl_sync(0xFFFFFFFFu, lz, win);
   out.h = __shfl_sync(0xFFFFFFFFu, h, win);
@@ -309,6 +313,7 @@ __device__ __forceinline__ void write_bad(const LpeArgs& a, int64_t r, uint32_t 
   a.out_entropy[r] = NAN;
   if (a.out_k) a.out_k[r] = 0;
   if (a.status) atomicOr(a.status, bit);
+  if (a.state) a.state[r] = RowState{0.f, 0.f, 0.f, 0u, 0u, bit << 8, 0, 0u};
 }
 
 __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
@@ -395,9 +400,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
         write_bad(a, f.r, RLK_STATUS_NONFINITE);
       } else {
         const float lz = logf(zf);
+        const float h = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, M.u), zf));
         a.out_logprob[f.r] = __fsub_rn(__fmul_rn(kLn2, __fmaf_rn(f.zy, c, -M.e)), lz);
-        a.out_entropy[f.r] = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, M.u), zf));
+        a.out_entropy[f.r] = h;
         if (a.out_k) a.out_k[f.r] = (int32_t)a.V;
+        if (a.state)
+          a.state[f.r] = RowState{M.e, lz, h, 0u, kTiesAll, kStateValid | kStateYIn,
+                                  (int32_t)a.V, 0u};
       }
     }
   };
@@ -476,6 +485,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTB, 2)
                                      : -INFINITY;
         a.out_entropy[f.r] = so.h;
         if (a.out_k) a.out_k[f.r] = (int32_t)so.kstar;
+        if (a.state)
+          a.state[f.r] = RowState{E, so.lz, so.h, so.key_thr, so.ties,
+                                  kStateValid | (so.y_in ? kStateYIn : 0u), (int32_t)so.kstar, 0u};
       }
     }
   };

@@ -61,21 +61,23 @@ size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H) {
   return 0;
 }
 
-rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
-                               int64_t ld, const int32_t* token_ids, float temperature,
-                               float top_p, float* out_logprob, float* out_entropy,
-                               int32_t* out_nucleus_size, uint32_t* out_status_word,
-                               void* workspace, size_t workspace_bytes, rlk_stream stream) {
-  (void)workspace;
-  (void)workspace_bytes;
+namespace {
+
+rlk_status logprob_entropy_impl(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                int64_t ld, const int32_t* token_ids, float temperature,
+                                float top_p, float* out_logprob, float* out_entropy,
+                                int32_t* out_nucleus_size, rlk_row_state* out_row_state,
+                                bool need_state, uint32_t* out_status_word, rlk_stream stream) {
   if (dtype != RLK_BF16 && dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
   if (T < 0 || V < 1 || V > (int64_t(1) << 24) || ld < V) return RLK_ERR_INVALID_ARG;
   if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
   if (!(top_p > 0.0f && top_p <= 1.0f)) return RLK_ERR_INVALID_ARG;
   if (T == 0) return RLK_OK;   // nothing to read or write; pointers may be NULL
   if (!logits || !token_ids || !out_logprob || !out_entropy) return RLK_ERR_INVALID_ARG;
+  if (need_state && !out_row_state) return RLK_ERR_INVALID_ARG;
   const uintptr_t elem = dtype == RLK_BF16 ? 2u : 4u;
   if (reinterpret_cast<uintptr_t>(logits) % elem != 0) return RLK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(out_row_state) % 16u != 0) return RLK_ERR_INVALID_ARG;
   rlk::LpeArgs a;
   a.logits = logits;
   a.dtype = dtype == RLK_BF16 ? 0 : 1;
@@ -90,7 +92,69 @@ rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, i
   a.out_k = out_nucleus_size;
   a.status = out_status_word;
   a.only_marked = 0;
+  a.state = reinterpret_cast<rlk::RowState*>(out_row_state);
   return rlk::launch_logprob_entropy(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
+}  // namespace
+
+rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                               int64_t ld, const int32_t* token_ids, float temperature,
+                               float top_p, float* out_logprob, float* out_entropy,
+                               int32_t* out_nucleus_size, uint32_t* out_status_word,
+                               void* workspace, size_t workspace_bytes, rlk_stream stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  return logprob_entropy_impl(logits, dtype, T, V, ld, token_ids, temperature, top_p, out_logprob,
+                              out_entropy, out_nucleus_size, nullptr, false, out_status_word,
+                              stream);
+}
+
+rlk_status rlk_logprob_entropy_fwd(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                   int64_t ld, const int32_t* token_ids, float temperature,
+                                   float top_p, float* out_logprob, float* out_entropy,
+                                   int32_t* out_nucleus_size, rlk_row_state* out_row_state,
+                                   uint32_t* out_status_word, rlk_stream stream) {
+  return logprob_entropy_impl(logits, dtype, T, V, ld, token_ids, temperature, top_p, out_logprob,
+                              out_entropy, out_nucleus_size, out_row_state, true, out_status_word,
+                              stream);
+}
+
+rlk_status rlk_logprob_entropy_bwd(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                   int64_t ld, const int32_t* token_ids, float temperature,
+                                   const rlk_row_state* row_state, const float* grad_logprob,
+                                   const float* grad_entropy, void* grad_logits,
+                                   rlk_dtype grad_dtype, int64_t ldg, uint32_t* out_status_word,
+                                   rlk_stream stream) {
+  if (dtype != RLK_BF16 && dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
+  if (grad_dtype != RLK_BF16 && grad_dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || ld < V || ldg < V) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  if (!logits || !token_ids || !row_state || !grad_logits) return RLK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) % (dtype == RLK_BF16 ? 2u : 4u) != 0 ||
+      reinterpret_cast<uintptr_t>(grad_logits) % (grad_dtype == RLK_BF16 ? 2u : 4u) != 0 ||
+      reinterpret_cast<uintptr_t>(row_state) % 16u != 0)
+    return RLK_ERR_INVALID_ARG;
+  rlk::LpeBwdArgs a;
+  a.logits = logits;
+  a.dtype = dtype == RLK_BF16 ? 0 : 1;
+  a.T = T;
+  a.V = V;
+  a.ld = ld;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.state = reinterpret_cast<const rlk::RowState*>(row_state);
+  a.grad_logprob = grad_logprob;
+  a.grad_entropy = grad_entropy;
+  a.grad_logits = grad_logits;
+  a.grad_dtype = grad_dtype == RLK_BF16 ? 0 : 1;
+  a.ldg = ldg;
+  a.status = out_status_word;
+  return rlk::launch_logprob_entropy_backward(a, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
 }

@@ -72,6 +72,16 @@ enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2 };
 #define RLK_STATUS_BAD_SUPPORT  0x8u   /* a supplied retained set that is empty,
                                           lists an id outside [0, V), or whose
                                           offsets decrease                      */
+#define RLK_STATUS_NO_STATE     0x10u  /* a row state that no forward wrote
+                                          (rlk_logprob_entropy_bwd)           */
+
+/* What rlk_logprob_entropy_fwd saves per row for rlk_logprob_entropy_bwd:
+ * the row's log-normaliser over its retained set, its entropy and where the
+ * set's boundary lies (a value and how many of the ids tied at it are kept).
+ * Opaque, 32 bytes, 16-byte aligned in an array of T. */
+typedef struct rlk_row_state {
+  uint32_t opaque[8];
+} rlk_row_state;
 
 /* Slots of the loss statistics vector (float [RLK_NSTATS]); fractions and
  * means are over tokens with mask = 1. */
@@ -140,6 +150,64 @@ rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, i
                                float top_p, float* out_logprob, float* out_entropy,
                                int32_t* out_nucleus_size, uint32_t* out_status_word,
                                void* workspace, size_t workspace_bytes, rlk_stream stream);
+
+/*
+ * rlk_logprob_entropy_fwd -- rlk_logprob_entropy that also saves, per row,
+ * what the backward needs.
+ *
+ * Outputs and errors as rlk_logprob_entropy, plus
+ *  out_row_state   device rlk_row_state[T] (required).  Row t's state is
+ *                  written once the row is finished; a row with a status
+ *                  gets a state that marks it so.
+ */
+rlk_status rlk_logprob_entropy_fwd(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                   int64_t ld, const int32_t* token_ids, float temperature,
+                                   float top_p, float* out_logprob, float* out_entropy,
+                                   int32_t* out_nucleus_size, rlk_row_state* out_row_state,
+                                   uint32_t* out_status_word, rlk_stream stream);
+
+/*
+ * rlk_logprob_entropy_bwd -- gradient of the top-p log-probability and
+ * entropy with respect to the logits.
+ *
+ * RL-Kernel "Qwen3-8B VIME train-rollout consistency", section "ROCm MI300X
+ * and gfx942": top-p < 1 rows are scored over the complete retained set S,
+ * renormalised.  S changes only where a logit crosses its boundary, so
+ * almost everywhere it is locally constant and the gradient is that of the
+ * softmax restricted to S at temperature T.  For
+ *   L = sum_t grad_logprob[t] logprob_t + grad_entropy[t] H_t
+ * and q_i = exp(x_i - m) / Z_S over S (as in rlk_logprob_entropy):
+ *   grad_logits[t, i] = 0                                         (i not in S)
+ *   grad_logits[t, i] = (grad_logprob[t] ([i = y] - q_i) [y in S]
+ *                        - grad_entropy[t] q_i (ln q_i + H_t)) / T   (i in S).
+ * S is the one the forward selected (ties at the boundary kept lower id
+ * first), read from the saved row state.
+ *
+ * Arguments
+ *  logits, dtype, T, V, ld, token_ids, temperature
+ *                  the forward's (same values, same contents).
+ *  row_state       device rlk_row_state[T] from rlk_logprob_entropy_fwd.
+ *  grad_logprob    device float[T] or NULL (zero).
+ *  grad_entropy    device float[T] or NULL (zero).
+ *  grad_logits     device, grad_dtype, T x ldg elements (ldg >= V); every
+ *                  element of columns [0, V) is written; NaN for a row whose
+ *                  state carries a status (or that no forward wrote).
+ *  grad_dtype      RLK_BF16 (rounded to nearest) or RLK_F32.
+ *  out_status_word device uint32[1] or NULL: the status bits the forward found
+ *                  for rows it could not score, RLK_STATUS_BAD_TOKEN_ID for an
+ *                  id outside [0, V), RLK_STATUS_NO_STATE for a state no
+ *                  forward wrote.
+ *  stream          CUDA stream.
+ * Errors: RLK_ERR_INVALID_ARG for T < 0, V < 1, V > 2^24, ld < V, ldg < V,
+ *  null required pointers, bad dtypes, a misaligned logits, gradient or state
+ *  base, a non-finite or non-positive temperature.  T == 0 returns RLK_OK.
+ */
+rlk_status rlk_logprob_entropy_bwd(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                   int64_t ld, const int32_t* token_ids, float temperature,
+                                   const rlk_row_state* row_state, const float* grad_logprob,
+                                   const float* grad_entropy, void* grad_logits,
+                                   rlk_dtype grad_dtype, int64_t ldg, uint32_t* out_status_word,
+                                   rlk_stream stream);
 
 /*
  * rlk_logprob_entropy_support -- per-token log-probability and entropy over a

@@ -127,6 +127,49 @@ def test_support_backward_empty_batch_is_a_no_op(lib):
     assert sup_bwd(lib, T=0, logits=None, ids=None, offs=None, sids=None, grad=None) == 0
 
 
+def fwd(lib, **kw):
+    args = dict(logits=FAKE, dtype=0, T=4, V=100, ld=100, ids=FAKE, temperature=0.7, top_p=0.9,
+                lp=FAKE, ent=FAKE, state=FAKE)
+    args.update(kw)
+    return lib.rlk_logprob_entropy_fwd(args["logits"], args["dtype"], args["T"], args["V"],
+                                       args["ld"], args["ids"], args["temperature"], args["top_p"],
+                                       args["lp"], args["ent"], None, args["state"], None, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(state=None), dict(state=ctypes.c_void_p(0x10008)), dict(top_p=0.0), dict(top_p=1.5),
+    dict(temperature=0.0), dict(T=-1), dict(ld=99), dict(lp=None),
+])
+def test_forward_with_state_rejects(lib, kw):
+    assert fwd(lib, **kw) == 1
+
+
+def bwd(lib, **kw):
+    args = dict(logits=FAKE, dtype=0, T=4, V=100, ld=100, ids=FAKE, temperature=0.7, state=FAKE,
+                glp=None, gh=None, grad=FAKE, gdt=0, ldg=100)
+    args.update(kw)
+    return lib.rlk_logprob_entropy_bwd(args["logits"], args["dtype"], args["T"], args["V"],
+                                       args["ld"], args["ids"], args["temperature"], args["state"],
+                                       args["glp"], args["gh"], args["grad"], args["gdt"],
+                                       args["ldg"], None, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(temperature=0.0), dict(temperature=math.nan), dict(T=-1), dict(V=0),
+    dict(V=(1 << 24) + 1), dict(ld=99), dict(ldg=99), dict(dtype=2), dict(gdt=5),
+    dict(logits=None), dict(ids=None), dict(state=None), dict(grad=None),
+    dict(state=ctypes.c_void_p(0x10004)), dict(gdt=1, grad=ctypes.c_void_p(0x10002)),
+    dict(logits=ctypes.c_void_p(0x10001)),
+])
+def test_backward_rejects(lib, kw):
+    assert bwd(lib, **kw) == 1
+
+
+def test_backward_empty_batch_is_a_no_op(lib):
+    assert bwd(lib, T=0, logits=None, ids=None, state=None, grad=None) == 0
+    assert fwd(lib, T=0, logits=None, ids=None, lp=None, ent=None, state=None) == 0
+
+
 def loss(lib, **kw):
     a = dict(n_seq=4, G=2, n_tok=10, el=0.2, eh=0.28, cap=2.0, kl=0.01, agg=0, ws=FAKE,
              ws_bytes=1 << 20, offs=FAKE, out=FAKE)
