@@ -1,6 +1,7 @@
 // Device helpers shared by the librlk kernels (sm_103a).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,6 +21,9 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_val(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+// A word of two bf16 as a float2 (low half first) / as a bf16 pair.
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+__device__ __forceinline__ __nv_bfloat162 bf2(uint32_t w) { return *reinterpret_cast<__nv_bfloat162*>(&w); }
 
 // Order-preserving 16-bit key of a bf16 bit pattern: key(a) < key(b) iff a < b
 // as numbers; -0 gets the key of +0, so equal values always tie.
@@ -129,6 +133,37 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
   }
 }
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy ones (a bulk copy into a buffer that was just read).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Waits for the mbarrier phase of the given parity, suspending in hardware
+// (up to ~1 ms a try) rather than polling; gives up (returning false and
+// raising *abort) after about 2^31 clock cycles, or when *abort is raised.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(1000000u)
+        : "memory");
+    if (ok) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > (1ll << 31)) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // One-dimensional bulk copy global -> shared, completing on an mbarrier
 // (addresses 16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,

@@ -131,37 +131,7 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(uint32_t addr) {
   asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
   return v;
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
 
-// Waits for the mbarrier phase of the given parity, suspending in hardware
-// (up to ~1 ms a try) rather than polling; gives up (returning false and
-// raising *abort) after about 2^31 clock cycles, or when *abort is raised.
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort) {
-  const long long t0 = clock64();
-  for (;;) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(1000000u)
-        : "memory");
-    if (ok) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > (1ll << 31)) {
-      *abort = 1;
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
-__device__ __forceinline__ __nv_bfloat162 bf2(uint32_t w) { return *reinterpret_cast<__nv_bfloat162*>(&w); }
 __device__ __forceinline__ float value_of_key(uint32_t k) { return bf16_val(okey16_inverse(k)); }
 
 // ----------------------------------------------------------------- helpers
