@@ -84,22 +84,26 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def kernel_sha():
-    with open(KERNEL_SRC, "rb") as f:
+BWD_SRC = os.path.join(ROOT, "entropy_logits_bf16_gb300", "csrc", "lpe_backward.cu")
+BWD_PROFILE = os.path.join(ROOT, "profiles", "lpe_backward_pipe_kernel_qwen_T4096.txt")
+
+
+def kernel_sha(src=KERNEL_SRC):
+    with open(src, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic():
+def profiled_traffic(src=KERNEL_SRC, profile=PROFILE):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
     try:
         kv = {}
-        with open(PROFILE) as f:
+        with open(profile) as f:
             for line in f:
                 if ":" in line:
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_sha256_16") != kernel_sha():
+        if kv.get("kernel_source_sha256_16") != kernel_sha(src):
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
@@ -598,8 +602,9 @@ def run_backward(args, ws, rank, dev, barrier):
                    "l2": "inputs larger than L2 (1.24 GB read + 1.24 GB written per step)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peak_kind,
-                     "kernel": "lpe_backward_kernel (one rlk_logprob_entropy_bwd call)",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic(BWD_SRC, BWD_PROFILE), "peak_source": peak_kind,
+                     "kernel": "lpe_backward_pipe_kernel (one rlk_logprob_entropy_bwd call)",
                      "algorithmic_bytes_per_launch": alg, "launch_ms": part_ms[0]},
         "gpu_launches": args.steps,
         "clocks": clk,
