@@ -58,6 +58,8 @@ def _load():
                                                                     vp, vp, vp, vp, vp, i]
             lib.oracle_logprob_entropy_backward.argtypes = [vp, i, i64, i64, i64, vp, f32, f32,
                                                             vp, vp, vp, vp, i]
+            lib.oracle_policy_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i, f32, f32,
+                                               f32, f32, f32, i, f32, f32, i, i, vp, vp, vp, vp]
             lib.oracle_grpo_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, f32,
                                              f32, f32, i, vp, vp, vp, vp]
             lib.oracle_lmhead_rows.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, f32, f32,
@@ -65,7 +67,8 @@ def _load():
             for fn in (lib.oracle_logprob_entropy, lib.oracle_sample_ids,
                        lib.oracle_logprob_entropy_support,
                        lib.oracle_logprob_entropy_support_backward,
-                       lib.oracle_logprob_entropy_backward, lib.oracle_grpo_loss, lib.oracle_lmhead_rows):
+                       lib.oracle_logprob_entropy_backward, lib.oracle_policy_loss,
+                       lib.oracle_grpo_loss, lib.oracle_lmhead_rows):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -219,6 +222,40 @@ def grpo_loss(logp_new, logp_old, logp_rollout, logp_ref, mask, rewards, seq_off
     if rc:
         raise ValueError("oracle_grpo_loss rejected its arguments")
     return float(loss[0]), grad, adv, dict(zip(STAT_NAMES, stats.tolist()))
+
+
+POLICY_STAT_NAMES = STAT_NAMES + ("mask_dropped",)
+LOSS_DAPO, LOSS_IPO, LOSS_ICEPOP = 0, 1, 2
+IS_NONE, IS_TIS, IS_MIS = 0, 1, 2
+BASELINE_MEAN, BASELINE_LENGTH_WEIGHTED = 0, 1
+
+
+def policy_loss(logp_new, logp_old, logp_rollout, logp_ref, mask, rewards, seq_offsets,
+                group_size, loss_type=LOSS_DAPO, eps_low=0.2, eps_high=0.28, ipo_eps=0.3,
+                band_low=0.5, band_high=2.0, is_method=IS_TIS, is_cap=2.0, kl_coef=0.01,
+                baseline=BASELINE_MEAN, agg=0):
+    """Policy-loss variants (DAPO / IPO / IcePop; none / TIS / MIS weights;
+    mean or length-weighted baseline; token, sequence or prompt mean); returns
+    (loss, grad[T], advantages[n_seq], stats dict)."""
+    f = lambda x: np.ascontiguousarray(x, dtype=np.float32)
+    new, old, ro, rf = f(logp_new), f(logp_old), f(logp_rollout), f(logp_ref)
+    rw = f(rewards)
+    off = np.ascontiguousarray(seq_offsets, dtype=np.int32)
+    n_seq = off.shape[0] - 1
+    m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8)
+    n_tok = int(off[-1] - off[0]) if n_seq >= 0 else 0
+    loss = np.zeros(1, np.float64)
+    grad = np.empty(max(n_tok, 0), np.float64)
+    adv = np.empty(max(n_seq, 0), np.float64)
+    stats = np.empty(len(POLICY_STAT_NAMES), np.float64)
+    rc = _load().oracle_policy_loss(
+        _ptr(new), _ptr(old), _ptr(ro), _ptr(rf), _ptr(m), _ptr(rw), _ptr(off), n_seq,
+        int(group_size), int(loss_type), float(eps_low), float(eps_high), float(ipo_eps),
+        float(band_low), float(band_high), int(is_method), float(is_cap), float(kl_coef),
+        int(baseline), int(agg), _ptr(loss), _ptr(grad), _ptr(adv), _ptr(stats))
+    if rc:
+        raise ValueError("oracle_policy_loss rejected its arguments")
+    return float(loss[0]), grad, adv, dict(zip(POLICY_STAT_NAMES, stats.tolist()))
 
 
 def lmhead_rows(hidden_bits, w_bits, rows, ids, temperature, top_p=1.0, threads=None):

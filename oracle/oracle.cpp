@@ -548,6 +548,198 @@ int oracle_grpo_loss(const float* logp_new, const float* logp_old, const float* 
   return 0;
 }
 
+// Policy-loss variants.  Sources: prime-rl v0.10.0 release notes, section
+// "2. RL Algorithms" (the IPO mask |pi_train(y) - pi_infer(y)| > eps with
+// eps = 0.3 and no KL term; IcePop, which masks a token whose ratio
+// pi_train / pi_infer leaves a fixed band; a length-weighted GRPO baseline and
+// prompt-mean aggregation), LumenRL README, section "Rollout Correction" (TIS
+// clips large ratios, MIS normalises them).  pi_train(y) = exp(new) and
+// pi_infer(y) = exp(rollout).  Readings where the pages give no formula:
+//  - IPO's surrogate is the importance-weighted policy gradient against the
+//    inference policy, -rho A with rho = exp(new - rollout), on tokens the mask
+//    keeps (no clipping);
+//  - IcePop keeps the clipped (DAPO) term on tokens whose rho lies in
+//    [band_low, band_high] and drops the others;
+//  - MIS divides exp(old - rollout) by its mean over the batch's tokens with
+//    mask 1 (no cap); TIS caps it at is_cap; none uses 1;
+//  - the length-weighted baseline weights each reward by its sequence's packed
+//    length, seq_offsets[s+1] - seq_offsets[s] (the plain mean when the group
+//    has no tokens); the divisor stays the plain group standard deviation;
+//  - prompt-mean aggregation averages, over groups with sum m > 0, each
+//    group's token mean.
+// Steps:
+//  1. A_s = (R_s - b_g) / (sigma_g + 1e-6), b_g the plain or length-weighted
+//     group mean, sigma_g as in oracle_grpo_loss.
+//  2. per token: r = exp(new - old), rho = exp(new - rollout),
+//     raw = exp(old - rollout);
+//     type 0 (DAPO):   keep = 1; pg = -min(r A, clip(r) A); g = -r A if the
+//                      unclipped term is the active minimum, else 0;
+//     type 1 (IPO):    keep = [|exp(new) - exp(rollout)| <= ipo_eps];
+//                      pg = -keep rho A; g = pg;
+//     type 2 (IcePop): keep = [band_low <= rho <= band_high]; pg, g = keep x
+//                      the DAPO ones;
+//     w by is_method (0 none, 1 TIS, 2 MIS); delta = ref - new,
+//     k3 = exp(delta) - delta - 1; l = w pg + kl_coef k3;
+//     dl = w g + kl_coef (1 - exp(delta)).
+//  3. agg 0 token mean, 1 sequence mean of token means, 2 prompt (group) mean
+//     of token means.
+//  4. dL/dnew = (weight of the token in L) dl.
+// Stats: the eight of oracle_grpo_loss (clip fractions for types 0 and 2 only,
+// the capped fraction for TIS only, slot 4 the mean of w) and slot 8, the
+// fraction of mask-1 tokens the IPO / IcePop mask drops.
+int oracle_policy_loss(const float* logp_new, const float* logp_old, const float* logp_rollout,
+                       const float* logp_ref, const uint8_t* mask, const float* rewards,
+                       const int32_t* seq_offsets, int32_t n_seq, int32_t group_size, int type,
+                       float eps_low, float eps_high, float ipo_eps, float band_low,
+                       float band_high, int is_method, float is_cap, float kl_coef, int baseline,
+                       int agg, double* out_loss, double* out_grad, double* out_adv,
+                       double* out_stats) {
+  if (!logp_new || !logp_old || !logp_rollout || !logp_ref || !rewards || !seq_offsets) return 1;
+  if (n_seq < 0 || group_size < 1 || n_seq % group_size != 0) return 1;
+  if (type < 0 || type > 2 || is_method < 0 || is_method > 2 || baseline < 0 || baseline > 1 ||
+      agg < 0 || agg > 2)
+    return 1;
+  const int64_t t0 = seq_offsets[0], t1 = seq_offsets[n_seq];
+  const int64_t n_tok = t1 - t0;
+  const double el = eps_low, eh = eps_high, beta = kl_coef;
+  const int32_t n_grp = n_seq / group_size;
+
+  // 1. advantages
+  std::vector<double> A(n_seq, 0.0);
+  for (int32_t g = 0; g < n_grp; ++g) {
+    const int32_t s0 = g * group_size;
+    NeumaierSum sum;
+    for (int32_t j = 0; j < group_size; ++j) sum.add(rewards[s0 + j]);
+    const double mu = sum.value() / group_size;
+    double sigma = 0.0;
+    if (group_size > 1) {
+      NeumaierSum ss;
+      for (int32_t j = 0; j < group_size; ++j) {
+        const double d = rewards[s0 + j] - mu;
+        ss.add(d * d);
+      }
+      sigma = std::sqrt(ss.value() / (group_size - 1));
+    }
+    double b = mu;
+    if (baseline == 1) {
+      NeumaierSum lw, ln;
+      for (int32_t j = 0; j < group_size; ++j) {
+        const double len = static_cast<double>(seq_offsets[s0 + j + 1] - seq_offsets[s0 + j]);
+        lw.add(len * rewards[s0 + j]);
+        ln.add(len);
+      }
+      if (ln.value() > 0.0) b = lw.value() / ln.value();
+    }
+    for (int32_t j = 0; j < group_size; ++j) A[s0 + j] = (rewards[s0 + j] - b) / (sigma + 1e-6);
+  }
+  if (out_adv)
+    for (int32_t s = 0; s < n_seq; ++s) out_adv[s] = A[s];
+
+  // the MIS normaliser: mean of exp(old - rollout) over tokens with mask 1
+  double raw_mean = 1.0;
+  if (is_method == 2) {
+    NeumaierSum rs, ms;
+    for (int64_t t = t0; t < t1; ++t) {
+      const double m = mask ? (mask[t] ? 1.0 : 0.0) : 1.0;
+      rs.add(m * std::exp(static_cast<double>(logp_old[t]) - logp_rollout[t]));
+      ms.add(m);
+    }
+    if (ms.value() > 0.0) raw_mean = rs.value() / ms.value();
+  }
+
+  // 2. per-token terms
+  std::vector<double> ell(n_tok > 0 ? n_tok : 0), dl(n_tok > 0 ? n_tok : 0);
+  std::vector<double> msk(n_tok > 0 ? n_tok : 0);
+  NeumaierSum msum, clo, chi, wsum, tcap, k3s, pgs, dropped;
+  for (int32_t s = 0; s < n_seq; ++s) {
+    const double a = A[s];
+    for (int64_t t = seq_offsets[s]; t < seq_offsets[s + 1]; ++t) {
+      const double nw = logp_new[t], od = logp_old[t], ro = logp_rollout[t], rf = logp_ref[t];
+      const double m = mask ? (mask[t] ? 1.0 : 0.0) : 1.0;
+      const double r = std::exp(nw - od), rho = std::exp(nw - ro), raw = std::exp(od - ro);
+      double keep = 1.0, pg = 0.0, gpg = 0.0;
+      if (type == 0 || type == 2) {
+        const double rc = std::min(std::max(r, 1.0 - el), 1.0 + eh);
+        pg = -std::min(r * a, rc * a);
+        gpg = (r * a <= rc * a) ? -r * a : 0.0;
+        if (type == 2) keep = (rho >= band_low && rho <= band_high) ? 1.0 : 0.0;
+        pg *= keep;
+        gpg *= keep;
+        clo.add(m * ((a < 0.0 && r < 1.0 - el) ? 1.0 : 0.0));
+        chi.add(m * ((a > 0.0 && r > 1.0 + eh) ? 1.0 : 0.0));
+      } else {
+        keep = std::fabs(std::exp(nw) - std::exp(ro)) <= ipo_eps ? 1.0 : 0.0;
+        pg = -keep * rho * a;
+        gpg = pg;
+      }
+      double w = 1.0;
+      if (is_method == 1) {
+        w = std::min(raw, static_cast<double>(is_cap));
+        tcap.add(m * (raw > is_cap ? 1.0 : 0.0));
+      } else if (is_method == 2) {
+        w = raw / raw_mean;
+      }
+      const double delta = rf - nw;
+      const double k3 = std::exp(delta) - delta - 1.0;
+      ell[t - t0] = w * pg + beta * k3;
+      dl[t - t0] = w * gpg + beta * (1.0 - std::exp(delta));
+      msk[t - t0] = m;
+      msum.add(m);
+      wsum.add(m * w);
+      k3s.add(m * k3);
+      pgs.add(m * pg);
+      dropped.add(m * (1.0 - keep));
+    }
+  }
+
+  // 3. aggregation over units: the batch (0), sequences (1) or groups (2)
+  const int32_t per_unit = agg == 1 ? 1 : group_size;
+  const int32_t n_unit = agg == 0 ? 1 : (agg == 1 ? n_seq : n_grp);
+  std::vector<double> weight(n_tok > 0 ? n_tok : 0, 0.0);
+  std::vector<double> unit_mean(n_unit, 0.0), unit_m(n_unit, 0.0);
+  int64_t n_live = 0;
+  for (int32_t u = 0; u < n_unit; ++u) {
+    const int64_t a0 = agg == 0 ? t0 : seq_offsets[u * per_unit];
+    const int64_t a1 = agg == 0 ? t1 : seq_offsets[(u + 1) * per_unit];
+    NeumaierSum ms, ls;
+    for (int64_t t = a0; t < a1; ++t) {
+      ms.add(msk[t - t0]);
+      ls.add(msk[t - t0] * ell[t - t0]);
+    }
+    unit_m[u] = ms.value();
+    if (unit_m[u] > 0.0) {
+      unit_mean[u] = ls.value() / unit_m[u];
+      ++n_live;
+    }
+  }
+  NeumaierSum total;
+  for (int32_t u = 0; u < n_unit; ++u) {
+    if (unit_m[u] <= 0.0) continue;
+    total.add(unit_mean[u]);
+    const int64_t a0 = agg == 0 ? t0 : seq_offsets[u * per_unit];
+    const int64_t a1 = agg == 0 ? t1 : seq_offsets[(u + 1) * per_unit];
+    for (int64_t t = a0; t < a1; ++t)
+      weight[t - t0] = msk[t - t0] / unit_m[u] / static_cast<double>(n_live);
+  }
+  const double L = n_live > 0 ? total.value() / static_cast<double>(n_live) : 0.0;
+  if (out_loss) *out_loss = L;
+  if (out_grad)
+    for (int64_t i = 0; i < n_tok; ++i) out_grad[i] = weight[i] * dl[i];
+  if (out_stats) {
+    const double M = msum.value(), d = M > 0.0 ? M : 1.0;
+    out_stats[ST_LOSS] = L;
+    out_stats[ST_TOKENS] = M;
+    out_stats[ST_CLIP_LOW] = clo.value() / d;
+    out_stats[ST_CLIP_HIGH] = chi.value() / d;
+    out_stats[ST_TIS_MEAN] = wsum.value() / d;
+    out_stats[ST_TIS_CAPPED] = tcap.value() / d;
+    out_stats[ST_K3_MEAN] = k3s.value() / d;
+    out_stats[ST_PG_MEAN] = pgs.value() / d;
+    out_stats[8] = dropped.value() / d;   // dropped by the IPO / IcePop mask
+  }
+  return 0;
+}
+
 // LM-head rows: z_i = sum_k h_k W_ik in fp64 from the exact bf16 values (never
 // rounded to bf16), then the logits path above on that row.  hidden: bf16
 // [T, H]; w_vocab: bf16 [V, H] row-major.  rows[0..n_rows) selects the rows.

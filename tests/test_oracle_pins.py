@@ -615,3 +615,145 @@ def test_dense_backward_bad_rows_are_nan(oracle):
     g = oracle.logprob_entropy_backward(z, np.array([0, 1, 10], np.int32), 1.0, 0.9,
                                         np.ones(3, np.float32), np.ones(3, np.float32))
     assert np.all(np.isfinite(g[0])) and np.all(np.isnan(g[1])) and np.all(np.isnan(g[2]))
+
+
+# ---------------------------------------------------------------- loss variants
+GOLDEN = __import__("pathlib").Path(__file__).parent / "golden"
+
+
+def _loss_batch(seed=3, n_prompts=4, group=4, lo=5, hi=40):
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi, n_prompts * group)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(off[-1])
+    new = np.log(rng.uniform(0.05, 0.95, T)).astype(np.float32)
+    old = (new + rng.normal(0, 0.2, T)).astype(np.float32)
+    ro = (old + rng.normal(0, 0.3, T)).astype(np.float32)
+    rf = (new + rng.normal(0, 0.1, T)).astype(np.float32)
+    mask = (rng.uniform(size=T) > 0.15).astype(np.uint8)
+    rew = rng.integers(0, 2, n_prompts * group).astype(np.float32)
+    return new, old, ro, rf, mask, rew, off, group
+
+
+def test_policy_loss_default_config_equals_grpo_loss(oracle):
+    """Two independently written oracles: the variant loss at DAPO + TIS + mean
+    baseline equals the GRPO/DAPO loss, for both of its aggregations."""
+    new, old, ro, rf, mask, rew, off, G = _loss_batch()
+    for agg in (0, 1):
+        a = oracle.grpo_loss(new, old, ro, rf, mask, rew, off, G, agg=agg)
+        b = oracle.policy_loss(new, old, ro, rf, mask, rew, off, G, agg=agg)
+        assert b[0] == pytest.approx(a[0], rel=1e-12, abs=1e-15)
+        assert np.allclose(b[1], a[1], rtol=1e-12, atol=1e-16)
+        assert np.allclose(b[2], a[2], rtol=1e-12)
+        for k, v in a[3].items():
+            assert b[3][k] == pytest.approx(v, rel=1e-12, abs=1e-15)
+        assert b[3]["mask_dropped"] == 0.0
+
+
+def test_ipo_mask_on_the_pages_example(oracle):
+    """The IPO mask keeps the rare token that moved 6x and masks the likely
+    token that moved to 0.22x (tests/golden/ipo_mask_example.txt)."""
+    rows = [l.split() for l in (GOLDEN / "ipo_mask_example.txt").read_text().splitlines()
+            if l.strip() and not l.startswith("#")]
+    for pi_inf, pi_tr, masked, ratio in rows:
+        lp_tr = np.log(np.float32(pi_tr))
+        lp_inf = np.log(np.float32(pi_inf))
+        z = np.array([lp_tr], np.float32)
+        _, g, _, st = oracle.policy_loss(z, z, np.array([lp_inf], np.float32), z, None,
+                                         np.array([1.0], np.float32), [0, 1], 1,
+                                         loss_type=oracle.LOSS_IPO, kl_coef=0.0,
+                                         is_method=oracle.IS_NONE)
+        assert st["mask_dropped"] == float(masked)
+        assert float(np.exp(np.float64(lp_tr) - np.float64(lp_inf))) == pytest.approx(
+            float(ratio), rel=1e-6)
+
+
+def test_ipo_and_icepop_hand_values(oracle):
+    """Two one-token sequences in one group, rewards 1 and 0: A = +-0.5 /
+    (0.7071068 + 1e-6).  IPO (eps 0.3, no KL, no weight): the first token
+    (0.5 vs 0.1) is masked, the second (0.5 vs 0.4) gives -1.25 A.  IcePop
+    (band [0.5, 2]): rho = 5 is dropped, rho = 1.25 keeps the clipped term."""
+    A = 0.5 / (np.sqrt(0.5) + 1e-6)
+    new = np.log(np.array([0.5, 0.5], np.float32))
+    ro = np.log(np.array([0.1, 0.4], np.float32))
+    rho2 = float(np.exp(np.float64(new[1]) - np.float64(ro[1])))
+    L, g, adv, st = oracle.policy_loss(new, new, ro, new, None, np.array([1, 0], np.float32),
+                                       [0, 1, 2], 2, loss_type=oracle.LOSS_IPO, kl_coef=0.0,
+                                       is_method=oracle.IS_NONE)
+    assert adv == pytest.approx([A, -A], rel=1e-12)
+    assert L == pytest.approx(0.5 * rho2 * A, rel=1e-12)
+    assert g == pytest.approx([0.0, 0.5 * rho2 * A], rel=1e-12)
+    assert st["mask_dropped"] == 0.5
+    # IcePop: old = new, so r = 1 and the clipped term is -A; rho1 = 5 leaves the band
+    L2, g2, _, st2 = oracle.policy_loss(new, new, ro, new, None, np.array([1, 0], np.float32),
+                                        [0, 1, 2], 2, loss_type=oracle.LOSS_ICEPOP,
+                                        band_low=0.5, band_high=2.0, kl_coef=0.0,
+                                        is_method=oracle.IS_NONE)
+    assert L2 == pytest.approx(0.5 * A, rel=1e-12)          # only the second: -(1)(-A)
+    assert g2 == pytest.approx([0.0, 0.5 * A], rel=1e-12)
+    assert st2["mask_dropped"] == 0.5
+
+
+def test_mis_normalises_and_is_scale_invariant(oracle):
+    """MIS: w = ratio / mean ratio.  Equal ratios give the unweighted loss;
+    multiplying every ratio by one constant changes nothing."""
+    new, old, ro, rf, mask, rew, off, G = _loss_batch(seed=5)
+    flat = (old - np.float32(0.25)).astype(np.float32)       # every ratio exp(0.25)
+    a = oracle.policy_loss(new, old, flat, rf, mask, rew, off, G, is_method=oracle.IS_MIS)
+    b = oracle.policy_loss(new, old, flat, rf, mask, rew, off, G, is_method=oracle.IS_NONE)
+    assert a[0] == pytest.approx(b[0], rel=1e-6)
+    c = oracle.policy_loss(new, old, ro, rf, mask, rew, off, G, is_method=oracle.IS_MIS)
+    d = oracle.policy_loss(new, old, (ro - np.float32(0.5)).astype(np.float32), rf, mask, rew,
+                           off, G, is_method=oracle.IS_MIS)
+    assert c[0] == pytest.approx(d[0], rel=1e-5)
+    assert c[3]["tis_mean"] == pytest.approx(1.0, rel=1e-12)   # the weights average to 1
+
+
+def test_length_weighted_baseline_and_prompt_mean(oracle):
+    """Lengths 1 and 3, rewards 1 and 0: b = 0.25, sigma = 0.7071068, so
+    A = 0.75 / (sigma + 1e-6) and -0.25 / (sigma + 1e-6).  Prompt mean with one
+    group is the token mean; with groups of one it is the sequence mean."""
+    z = np.log(np.full(4, 0.5, np.float32))
+    _, _, adv, _ = oracle.policy_loss(z, z, z, z, None, np.array([1, 0], np.float32),
+                                      [0, 1, 4], 2, baseline=oracle.BASELINE_LENGTH_WEIGHTED)
+    s = np.sqrt(0.5) + 1e-6
+    assert adv == pytest.approx([0.75 / s, -0.25 / s], rel=1e-12)
+    new, old, ro, rf, mask, rew, off, G = _loss_batch(seed=7)
+    n = len(rew)
+    tok = oracle.policy_loss(new, old, ro, rf, mask, rew, off, n, agg=0)
+    one = oracle.policy_loss(new, old, ro, rf, mask, rew, off, n, agg=2)
+    assert one[0] == pytest.approx(tok[0], rel=1e-12) and np.allclose(one[1], tok[1], rtol=1e-12)
+    seq = oracle.policy_loss(new, old, ro, rf, mask, rew, off, 1, agg=1)
+    per = oracle.policy_loss(new, old, ro, rf, mask, rew, off, 1, agg=2)
+    assert per[0] == pytest.approx(seq[0], rel=1e-12) and np.allclose(per[1], seq[1], rtol=1e-12)
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(loss_type=0, is_method=2, agg=2),
+    dict(loss_type=1, is_method=0, kl_coef=0.0, agg=0),
+    dict(loss_type=1, is_method=1, kl_coef=0.02, agg=1),
+    dict(loss_type=2, is_method=1, band_low=0.6, band_high=1.8, agg=2, baseline=1),
+])
+def test_policy_loss_gradient_matches_finite_differences(oracle, cfg):
+    """dL/dnew against central differences of the loss, skipping tokens whose
+    step crosses a clip bound or a mask edge (where L is not differentiable)."""
+    new, old, ro, rf, mask, rew, off, G = _loss_batch(seed=11, n_prompts=2, group=3, lo=3, hi=9)
+    L0, g, _, _ = oracle.policy_loss(new, old, ro, rf, mask, rew, off, G, **cfg)
+    h, checked = 1e-3, 0
+    for t in range(len(new)):
+        up, dn = new.copy(), new.copy()
+        up[t] = np.float32(new[t] + h)
+        dn[t] = np.float32(new[t] - h)
+        Lp, _, _, sp = oracle.policy_loss(up, old, ro, rf, mask, rew, off, G, **cfg)
+        Lm, _, _, sm = oracle.policy_loss(dn, old, ro, rf, mask, rew, off, G, **cfg)
+        _, _, _, s0 = oracle.policy_loss(new, old, ro, rf, mask, rew, off, G, **cfg)
+        if any(sp[k] != s0[k] or sm[k] != s0[k]
+               for k in ("clip_low_frac", "clip_high_frac", "mask_dropped")):
+            continue
+        r = np.exp(np.float64(new[t]) - old[t])
+        if abs(r - 0.8) < 2e-3 or abs(r - 1.28) < 2e-3:   # at a clip bound
+            continue
+        fd = (Lp - Lm) / (float(up[t]) - float(dn[t]))
+        assert g[t] == pytest.approx(fd, rel=2e-4, abs=2e-7), t
+        checked += 1
+    assert checked >= len(new) // 2
