@@ -23,14 +23,28 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace"
 STATUS_BAD_TOKEN_ID = 0x1
 STATUS_NONFINITE = 0x2
 OP_LOGPROB_ENTROPY, OP_GRPO_LOSS, OP_LMHEAD = 0, 1, 2
-AGG_TOKEN_MEAN, AGG_SEQ_MEAN_TOKEN_MEAN = 0, 1
+AGG_TOKEN_MEAN, AGG_SEQ_MEAN_TOKEN_MEAN, AGG_PROMPT_MEAN = 0, 1, 2
+LOSS_DAPO, LOSS_IPO, LOSS_ICEPOP = 0, 1, 2
+IS_NONE, IS_TIS, IS_MIS = 0, 1, 2
+BASELINE_MEAN, BASELINE_LENGTH_WEIGHTED = 0, 1
+NSTATS_POLICY = 9
+STAT_MASK_DROPPED = 8
 NSTATS = 8
+class LossConfig(ctypes.Structure):
+    """rlk_loss_config."""
+    _fields_ = [("type", ctypes.c_int), ("eps_low", ctypes.c_float), ("eps_high", ctypes.c_float),
+                ("ipo_eps", ctypes.c_float), ("band_low", ctypes.c_float),
+                ("band_high", ctypes.c_float), ("is_method", ctypes.c_int),
+                ("is_cap", ctypes.c_float), ("kl_coef", ctypes.c_float),
+                ("baseline", ctypes.c_int), ("agg", ctypes.c_int)]
+
+
 STAT_NAMES = ("loss", "tokens", "clip_low_frac", "clip_high_frac", "tis_mean",
               "tis_capped_frac", "k3_mean", "pg_mean")
 EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logprob_entropy",
            "rlk_logprob_entropy_fwd", "rlk_logprob_entropy_bwd",
            "rlk_logprob_entropy_support", "rlk_logprob_entropy_support_backward",
-           "rlk_grpo_loss", "rlk_lmhead_logprob",
+           "rlk_grpo_loss", "rlk_policy_loss", "rlk_lmhead_logprob",
            "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
 DEBUG_EXPORTS = ("rlk_lmhead_logits_debug",)
@@ -86,6 +100,9 @@ def load(path: str | None = None):
         lib.rlk_logprob_entropy_support_backward.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp,
                                                              f32, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logprob_entropy_support_backward.restype = ctypes.c_int
+        lib.rlk_policy_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i64,
+                                        ctypes.POINTER(LossConfig), vp, vp, vp, vp, sz, vp]
+        lib.rlk_policy_loss.restype = ctypes.c_int
         lib.rlk_grpo_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, f32, f32, f32,
                                       f32, ctypes.c_int, vp, vp, vp, vp, sz, vp]
         lib.rlk_grpo_loss.restype = ctypes.c_int
@@ -354,6 +371,45 @@ def grpo_loss(logp_new, logp_old, logp_rollout, logp_ref, rewards, seq_offsets, 
                              float(tis_cap), float(kl_coef), int(agg), _ptr(loss), _ptr(grad),
                              _ptr(stats), _ptr(workspace), workspace.numel(), _stream(dev))
     _check("rlk_grpo_loss", code)
+    return loss, grad, stats
+
+
+def policy_loss(logp_new, logp_old, logp_rollout, logp_ref, rewards, seq_offsets, group_size, *,
+                loss_mask=None, loss_type=LOSS_DAPO, eps_low=0.2, eps_high=0.28, ipo_eps=0.3,
+                band_low=0.5, band_high=2.0, is_method=IS_TIS, is_cap=2.0, kl_coef=0.01,
+                baseline=BASELINE_MEAN, agg=AGG_TOKEN_MEAN, want_grad=True, want_stats=True,
+                workspace=None):
+    """rlk_policy_loss: the GRPO/DAPO loss with the IPO / IcePop policy terms,
+    none / TIS / MIS weights, a mean or length-weighted baseline and token /
+    sequence / prompt aggregation.  Returns (loss[1], grad[T] or None,
+    stats[NSTATS_POLICY] or None), CUDA fp32 tensors."""
+    lib = load()
+    _need_cuda(logp_new, logp_old, logp_rollout, logp_ref, rewards, seq_offsets, loss_mask)
+    for t in (logp_new, logp_old, logp_rollout, logp_ref, rewards):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("log-probs and rewards must be contiguous fp32")
+    if seq_offsets.dtype != torch.int32:
+        raise ValueError("seq_offsets must be int32")
+    if loss_mask is not None and loss_mask.dtype != torch.uint8:
+        raise ValueError("loss_mask must be uint8")
+    n_seq = seq_offsets.numel() - 1
+    n_tok = logp_new.numel()
+    dev = logp_new.device
+    need = int(lib.rlk_workspace_size(OP_GRPO_LOSS, n_tok, n_seq, 0))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+    cfg = LossConfig(int(loss_type), float(eps_low), float(eps_high), float(ipo_eps),
+                     float(band_low), float(band_high), int(is_method), float(is_cap),
+                     float(kl_coef), int(baseline), int(agg))
+    loss = torch.empty(1, device=dev, dtype=torch.float32)
+    grad = torch.empty(n_tok, device=dev, dtype=torch.float32) if want_grad else None
+    stats = torch.empty(NSTATS_POLICY, device=dev, dtype=torch.float32) if want_stats else None
+    code = lib.rlk_policy_loss(_ptr(logp_new), _ptr(logp_old), _ptr(logp_rollout),
+                               _ptr(logp_ref), _ptr(loss_mask), _ptr(rewards), _ptr(seq_offsets),
+                               n_seq, int(group_size), n_tok, ctypes.byref(cfg), _ptr(loss),
+                               _ptr(grad), _ptr(stats), _ptr(workspace), workspace.numel(),
+                               _stream(dev))
+    _check("rlk_policy_loss", code)
     return loss, grad, stats
 
 

@@ -11,11 +11,18 @@
 // Launches (all on the caller's stream, no atomics on floats, no inter-CTA
 // waits, every sum in a fixed order):
 //  1. seq kernel, one CTA per sequence: the sequence's advantage from its
-//     group's rewards, then per-token terms; per-sequence partial sums go to
-//     the workspace and the unscaled per-token gradient to the output.
-//  2. finalize kernel, one CTA: fixed-order sums over sequences -> loss,
-//     statistics and the gradient weights.
-//  3. scale kernel, one CTA per sequence (only when a gradient is requested).
+//     group's rewards, then per-token terms; per-sequence partial sums (and
+//     the advantage) go to the workspace.
+//  2. finalize kernel, one CTA: fixed-order sums over sequences, then over
+//     the aggregation units -> loss, statistics, the gradient weights.
+//  3. grad kernel, one CTA per sequence (only when a gradient is requested):
+//     each token's gradient, recomputed from the inputs, times its weight.
+//
+// The variants (policy term, importance weight, baseline, aggregation) follow
+// the prime-rl v0.10.0 release notes, section "2. RL Algorithms" (IPO mask
+// |pi_train(y) - pi_infer(y)| > eps; IcePop's ratio band; length-weighted
+// baseline; prompt-mean aggregation) and the LumenRL README, section "Rollout
+// Correction" (TIS caps the ratio, MIS normalises it).
 
 #include <math.h>
 
@@ -29,8 +36,12 @@ namespace {
 constexpr int LT = 256;
 constexpr int LWARP = LT / 32;
 constexpr int NP = kLossPartials;  // partial sums per sequence, see below
-// Partial slots: 0 sum m*l, 1 sum m, 2 clip-low count, 3 clip-high count,
-// 4 sum m*w, 5 TIS-capped count, 6 sum m*k3, 7 sum m*pg.
+// Partial slots: 0 sum m l (MIS: sum m kl_coef k3 only), 1 sum m, 2 clip-low
+// count, 3 clip-high count, 4 sum m w (MIS: sum m raw), 5 capped count,
+// 6 sum m k3, 7 sum m pg, 8 count dropped by the IPO / IcePop mask,
+// 9 sum m raw pg (MIS), 10 the sequence's advantage, 11 unused.
+// Scalars after the partials: 0 1 / sum m, 1 live aggregation units,
+// 2 the importance-weight scale (1 / mean raw for MIS, else 1).
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -38,16 +49,54 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// The per-token policy term: pg, its derivative in logp_new (g), the mask
+// value (keep) and the raw importance ratio exp(old - rollout).
+struct TokTerms {
+  float pg, g, keep, r, raw;
+};
+__device__ __forceinline__ TokTerms token_terms(const LossArgs& a, float A, float nw, float od,
+                                                float ro) {
+  TokTerms t;
+  t.r = expf(nw - od);
+  t.raw = expf(od - ro);
+  t.keep = 1.f;
+  if (a.loss_type == RLK_LOSS_IPO) {
+    const float rho = expf(nw - ro);
+    t.keep = fabsf(expf(nw) - expf(ro)) <= a.ipo_eps ? 1.f : 0.f;
+    t.pg = -(t.keep * rho * A);
+    t.g = t.pg;
+  } else {
+    const float rc = fminf(fmaxf(t.r, 1.0f - a.eps_low), 1.0f + a.eps_high);
+    const float un = t.r * A, cl = rc * A;
+    t.pg = -fminf(un, cl);
+    t.g = (un <= cl) ? -un : 0.f;
+    if (a.loss_type == RLK_LOSS_ICEPOP) {
+      const float rho = expf(nw - ro);
+      t.keep = (rho >= a.band_low && rho <= a.band_high) ? 1.f : 0.f;
+      t.pg *= t.keep;
+      t.g *= t.keep;
+    }
+  }
+  return t;
+}
+
+// The importance weight for everything but MIS (whose scale is known only
+// after the batch reduction).
+__device__ __forceinline__ float is_weight(const LossArgs& a, float raw) {
+  return a.is_method == RLK_IS_TIS ? fminf(raw, a.tis_cap) : 1.f;
+}
+
 __global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
   __shared__ float s_adv;
   __shared__ float s_red[LWARP][NP];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = a.group_size;
-  const float lo_b = 1.0f - a.eps_low, hi_b = 1.0f + a.eps_high;
+  const bool mis = a.is_method == RLK_IS_MIS;
   for (int s = blockIdx.x; s < a.n_seq; s += gridDim.x) {
     if (tid == 0) {
       // Group statistics in a fixed order: the mean as a double-float sum,
-      // then the squared deviations from it (two passes over G rewards).
+      // then the squared deviations from it (two passes over G rewards); the
+      // length-weighted baseline weights each reward by its packed length.
       const int s0 = (s / G) * G;
       DF sum{0.f, 0.f};
       for (int j = 0; j < G; ++j) sum = df_add_f(sum, a.rewards[s0 + j]);
@@ -58,7 +107,18 @@ __global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
         ss = __fmaf_rn(d, d, ss);
       }
       const float sigma = G > 1 ? sqrtf(__fdiv_rn(ss, (float)(G - 1))) : 0.f;
-      s_adv = __fdiv_rn(__fsub_rn(a.rewards[s], mu), __fadd_rn(sigma, 1e-6f));
+      float b = mu;
+      if (a.baseline == RLK_BASELINE_LENGTH_WEIGHTED) {
+        DF lw{0.f, 0.f};
+        float ln = 0.f;   // lengths are integers: exact in fp32 up to 2^24 tokens a group
+        for (int j = 0; j < G; ++j) {
+          const float len = (float)(a.seq_offsets[s0 + j + 1] - a.seq_offsets[s0 + j]);
+          lw = df_add_f(lw, __fmul_rn(len, a.rewards[s0 + j]));
+          ln = __fadd_rn(ln, len);
+        }
+        if (ln > 0.f) b = __fdiv_rn(__fadd_rn(lw.hi, lw.lo), ln);
+      }
+      s_adv = __fdiv_rn(__fsub_rn(a.rewards[s], b), __fadd_rn(sigma, 1e-6f));
     }
     __syncthreads();
     const float A = s_adv;
@@ -66,30 +126,33 @@ __global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
     float acc[NP];
 #pragma unroll
     for (int k = 0; k < NP; ++k) acc[k] = 0.f;
+    const float lo_b = 1.0f - a.eps_low, hi_b = 1.0f + a.eps_high;
+    const bool clipped_type = a.loss_type != RLK_LOSS_IPO;
     for (int64_t t = t0 + tid; t < t1; t += LT) {
       const float nw = a.logp_new[t], od = a.logp_old[t];
       const float ro = a.logp_rollout[t], rf = a.logp_ref[t];
       const float m = a.mask ? (a.mask[t] ? 1.f : 0.f) : 1.f;
-      const float r = expf(nw - od);
-      const float rc = fminf(fmaxf(r, lo_b), hi_b);
-      const float un = r * A, cl = rc * A;
-      const float pg = -fminf(un, cl);
-      const float gpg = (un <= cl) ? -un : 0.f;
-      const float raw = expf(od - ro);
-      const float w = fminf(raw, a.tis_cap);
+      const TokTerms tt = token_terms(a, A, nw, od, ro);
       const float dl = rf - nw;
-      const float em1 = expm1f(dl);
-      const float k3 = em1 - dl;
-      const float ell = w * pg + a.kl_coef * k3;
-      acc[0] += m * ell;
+      const float k3 = expm1f(dl) - dl;
+      if (mis) {
+        acc[0] += m * (a.kl_coef * k3);
+        acc[4] += m * tt.raw;
+        acc[9] += m * (tt.raw * tt.pg);
+      } else {
+        const float w = is_weight(a, tt.raw);
+        acc[0] += m * (w * tt.pg + a.kl_coef * k3);
+        acc[4] += m * w;
+      }
       acc[1] += m;
-      acc[2] += (A < 0.f && r < lo_b) ? m : 0.f;
-      acc[3] += (A > 0.f && r > hi_b) ? m : 0.f;
-      acc[4] += m * w;
-      acc[5] += (raw > a.tis_cap) ? m : 0.f;
+      if (clipped_type) {
+        acc[2] += (A < 0.f && tt.r < lo_b) ? m : 0.f;
+        acc[3] += (A > 0.f && tt.r > hi_b) ? m : 0.f;
+      }
+      acc[5] += (a.is_method == RLK_IS_TIS && tt.raw > a.tis_cap) ? m : 0.f;
       acc[6] += m * k3;
-      acc[7] += m * pg;
-      if (a.out_grad) a.out_grad[t] = m * (w * gpg - a.kl_coef * em1);
+      acc[7] += m * tt.pg;
+      acc[8] += m * (1.f - tt.keep);
     }
 #pragma unroll
     for (int k = 0; k < NP; ++k) acc[k] = warp_sum(acc[k]);
@@ -99,31 +162,22 @@ __global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
     if (tid < NP) {
       float v = 0.f;
       for (int w2 = 0; w2 < LWARP; ++w2) v += s_red[w2][tid];
-      a.workspace[(int64_t)s * NP + tid] = v;
+      a.workspace[(int64_t)s * NP + tid] = tid == 10 ? A : v;
     }
     __syncthreads();
   }
 }
 
-// One CTA: fixed-order sums over the sequences' partials.
-__global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
-  // Double-float (fp32 pair) sums in a fixed order: thread t takes sequences
-  // t, t + LT, ...; then a shuffle tree per warp and one over the warps.
-  constexpr int NV = NP + 2;   // NP partial sums, sum of per-sequence means, live sequences
-  __shared__ DF s_red[LWARP][NV];
+// A sequence's sum of m l, given the MIS scale (1 when not MIS).
+__device__ __forceinline__ float seq_lsum(const float* p, bool mis, float scale) {
+  return mis ? __fmaf_rn(p[9], scale, p[0]) : p[0];
+}
+
+// Fixed-order double-float reduction of NV values over the CTA; valid on
+// thread 0.
+template <int NV>
+__device__ void cta_sum_df(DF (&acc)[NV], DF (*s_red)[NV], float (&out)[NV]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  DF acc[NV];
-#pragma unroll
-  for (int k = 0; k < NV; ++k) acc[k] = DF{0.f, 0.f};
-  for (int s = tid; s < a.n_seq; s += LT) {
-    const float* p = a.workspace + (int64_t)s * NP;
-#pragma unroll
-    for (int k = 0; k < NP; ++k) acc[k] = df_add_f(acc[k], p[k]);
-    if (p[1] > 0.f) {
-      acc[NP] = df_add_f(acc[NP], __fdiv_rn(p[0], p[1]));
-      acc[NP + 1] = df_add_f(acc[NP + 1], 1.f);
-    }
-  }
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
 #pragma unroll
@@ -134,51 +188,117 @@ __global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
     for (int k = 0; k < NV; ++k) s_red[warp][k] = acc[k];
   __syncthreads();
   if (warp == 0) {
-    float t[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       DF v = lane < LWARP ? s_red[lane][k] : DF{0.f, 0.f};
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v = df_add(v, DF{shfl_down(v.hi, o), shfl_down(v.lo, o)});
-      t[k] = __fadd_rn(v.hi, v.lo);
+      out[k] = __fadd_rn(v.hi, v.lo);
     }
-    if (lane == 0) {
-      const float M = t[1];
-      float L;
-      if (a.agg == RLK_AGG_TOKEN_MEAN) L = M > 0.f ? __fdiv_rn(t[0], M) : 0.f;
-      else L = t[NP + 1] > 0.f ? __fdiv_rn(t[NP], t[NP + 1]) : 0.f;
-      *a.out_loss = L;
-      if (a.out_stats) {
-        const float d = M > 0.f ? M : 1.f;
-        a.out_stats[RLK_STAT_LOSS] = L;
-        a.out_stats[RLK_STAT_TOKENS] = M;
-        a.out_stats[RLK_STAT_CLIP_LOW] = __fdiv_rn(t[2], d);
-        a.out_stats[RLK_STAT_CLIP_HIGH] = __fdiv_rn(t[3], d);
-        a.out_stats[RLK_STAT_TIS_MEAN] = __fdiv_rn(t[4], d);
-        a.out_stats[RLK_STAT_TIS_CAPPED] = __fdiv_rn(t[5], d);
-        a.out_stats[RLK_STAT_K3_MEAN] = __fdiv_rn(t[6], d);
-        a.out_stats[RLK_STAT_PG_MEAN] = __fdiv_rn(t[7], d);
-      }
-      float* sc = a.workspace + (int64_t)a.n_seq * NP;
-      sc[0] = M > 0.f ? __fdiv_rn(1.f, M) : 0.f;   // token-mean weight
-      sc[1] = t[NP + 1];                             // sequences with tokens
+  }
+  __syncthreads();
+}
+
+// One CTA: fixed-order sums over the sequences' partials, then (the MIS scale
+// being known) over the aggregation units: the batch, sequences or groups.
+__global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
+  __shared__ DF s_red1[LWARP][NP];
+  __shared__ DF s_red2[LWARP][2];
+  __shared__ float s_t[NP];
+  const int tid = threadIdx.x;
+  DF acc[NP];
+#pragma unroll
+  for (int k = 0; k < NP; ++k) acc[k] = DF{0.f, 0.f};
+  for (int s = tid; s < a.n_seq; s += LT) {
+    const float* p = a.workspace + (int64_t)s * NP;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) acc[k] = df_add_f(acc[k], p[k]);
+  }
+  float t[NP];
+  cta_sum_df<NP>(acc, s_red1, t);
+  if (tid == 0)
+    for (int k = 0; k < NP; ++k) s_t[k] = t[k];
+  __syncthreads();
+  const bool mis = a.is_method == RLK_IS_MIS;
+  const float M = s_t[1];
+  // MIS: w = raw / (sum m raw / sum m)
+  const float scale = mis && s_t[4] > 0.f ? __fdiv_rn(M, s_t[4]) : 1.f;
+  // Aggregation units: the batch (token mean) sums every sequence's m l;
+  // sequences or groups add their own token means.
+  const int per = a.agg == RLK_AGG_PROMPT_MEAN ? a.group_size : 1;
+  const int n_unit = a.agg == RLK_AGG_TOKEN_MEAN ? a.n_seq : a.n_seq / per;
+  DF u2[2] = {DF{0.f, 0.f}, DF{0.f, 0.f}};   // sum of unit values, live units
+  for (int u = tid; u < n_unit; u += LT) {
+    float ls = 0.f, ms = 0.f;
+    for (int j = 0; j < per; ++j) {
+      const float* p = a.workspace + (int64_t)(u * per + j) * NP;
+      ls = __fadd_rn(ls, seq_lsum(p, mis, scale));
+      ms = __fadd_rn(ms, p[1]);
     }
+    if (a.agg == RLK_AGG_TOKEN_MEAN) {
+      u2[0] = df_add_f(u2[0], ls);
+    } else if (ms > 0.f) {
+      u2[0] = df_add_f(u2[0], __fdiv_rn(ls, ms));
+      u2[1] = df_add_f(u2[1], 1.f);
+    }
+  }
+  float v[2];
+  cta_sum_df<2>(u2, s_red2, v);
+  if (tid == 0) {
+    float L;
+    if (a.agg == RLK_AGG_TOKEN_MEAN) L = M > 0.f ? __fdiv_rn(v[0], M) : 0.f;
+    else L = v[1] > 0.f ? __fdiv_rn(v[0], v[1]) : 0.f;
+    *a.out_loss = L;
+    if (a.out_stats) {
+      const float d = M > 0.f ? M : 1.f;
+      a.out_stats[RLK_STAT_LOSS] = L;
+      a.out_stats[RLK_STAT_TOKENS] = M;
+      a.out_stats[RLK_STAT_CLIP_LOW] = __fdiv_rn(s_t[2], d);
+      a.out_stats[RLK_STAT_CLIP_HIGH] = __fdiv_rn(s_t[3], d);
+      a.out_stats[RLK_STAT_TIS_MEAN] = __fdiv_rn(__fmul_rn(s_t[4], scale), d);
+      a.out_stats[RLK_STAT_TIS_CAPPED] = __fdiv_rn(s_t[5], d);
+      a.out_stats[RLK_STAT_K3_MEAN] = __fdiv_rn(s_t[6], d);
+      a.out_stats[RLK_STAT_PG_MEAN] = __fdiv_rn(s_t[7], d);
+      if (a.nstats > RLK_STAT_MASK_DROPPED)
+        a.out_stats[RLK_STAT_MASK_DROPPED] = __fdiv_rn(s_t[8], d);
+    }
+    float* sc = a.workspace + (int64_t)a.n_seq * NP;
+    sc[0] = M > 0.f ? __fdiv_rn(1.f, M) : 0.f;   // token-mean weight
+    sc[1] = v[1];                                  // live sequences or groups
+    sc[2] = scale;
   }
 }
 
-// Multiply each token's unscaled gradient by its weight in the loss.
-__global__ void __launch_bounds__(LT) loss_scale_kernel(LossArgs a) {
+// Each token's gradient with its weight in the loss, recomputed from the
+// inputs (the weight and the MIS scale are known only after the reduction).
+__global__ void __launch_bounds__(LT) loss_grad_kernel(LossArgs a) {
   const float* sc = a.workspace + (int64_t)a.n_seq * NP;
+  const bool mis = a.is_method == RLK_IS_MIS;
   for (int s = blockIdx.x; s < a.n_seq; s += gridDim.x) {
+    const float* p = a.workspace + (int64_t)s * NP;
     float wgt;
     if (a.agg == RLK_AGG_TOKEN_MEAN) {
       wgt = sc[0];
     } else {
-      const float ms = a.workspace[(int64_t)s * NP + 1];
-      wgt = ms > 0.f ? __fdiv_rn(1.f, __fmul_rn(ms, sc[1])) : 0.f;
+      float mu = p[1];   // the unit's token count: the sequence's, or its group's
+      if (a.agg == RLK_AGG_PROMPT_MEAN) {
+        const int s0 = (s / a.group_size) * a.group_size;
+        mu = 0.f;
+        for (int j = 0; j < a.group_size; ++j) mu = __fadd_rn(mu, a.workspace[(int64_t)(s0 + j) * NP + 1]);
+      }
+      wgt = mu > 0.f ? __fdiv_rn(1.f, __fmul_rn(mu, sc[1])) : 0.f;
     }
+    const float A = p[10];
     const int64_t t0 = a.seq_offsets[s], t1 = a.seq_offsets[s + 1];
-    for (int64_t t = t0 + threadIdx.x; t < t1; t += LT) a.out_grad[t] *= wgt;
+    for (int64_t t = t0 + threadIdx.x; t < t1; t += LT) {
+      const float nw = a.logp_new[t], od = a.logp_old[t];
+      const float ro = a.logp_rollout[t], rf = a.logp_ref[t];
+      const float m = a.mask ? (a.mask[t] ? 1.f : 0.f) : 1.f;
+      const TokTerms tt = token_terms(a, A, nw, od, ro);
+      const float w = mis ? __fmul_rn(tt.raw, sc[2]) : is_weight(a, tt.raw);
+      const float em1 = expm1f(rf - nw);
+      a.out_grad[t] = wgt * (m * (w * tt.g - a.kl_coef * em1));
+    }
   }
 }
 
@@ -194,7 +314,7 @@ cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t stream) {
   const int grid = a.n_seq < cap ? (a.n_seq > 0 ? a.n_seq : 1) : cap;
   if (a.n_seq > 0) loss_seq_kernel<<<grid, LT, 0, stream>>>(a);
   loss_finalize_kernel<<<1, LT, 0, stream>>>(a);
-  if (a.out_grad && a.n_seq > 0) loss_scale_kernel<<<grid, LT, 0, stream>>>(a);
+  if (a.out_grad && a.n_seq > 0) loss_grad_kernel<<<grid, LT, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -262,7 +382,8 @@ extern "C" rlk_status rlk_grpo_loss_noalloc(
     return RLK_ERR_INVALID_ARG;
   if (!(isfinite(tis_cap) && tis_cap > 0.0f) || !(isfinite(kl_coef) && kl_coef >= 0.0f))
     return RLK_ERR_INVALID_ARG;
-  if (agg != RLK_AGG_TOKEN_MEAN && agg != RLK_AGG_SEQ_MEAN_TOKEN_MEAN) return RLK_ERR_INVALID_ARG;
+  if (agg != RLK_AGG_TOKEN_MEAN && agg != RLK_AGG_SEQ_MEAN_TOKEN_MEAN && agg != RLK_AGG_PROMPT_MEAN)
+    return RLK_ERR_INVALID_ARG;
   if (!seq_offsets || !out_loss) return RLK_ERR_INVALID_ARG;
   if (n_seq > 0 && (!logp_new || !logp_old || !logp_rollout || !logp_ref || !rewards))
     return RLK_ERR_INVALID_ARG;

@@ -82,6 +82,11 @@ struct LossArgs {
   int64_t n_tok;
   float eps_low, eps_high, tis_cap, kl_coef;
   int agg;
+  int loss_type = 0;     // rlk_loss_type
+  int is_method = 1;     // rlk_is_method (TIS in rlk_grpo_loss)
+  int baseline = 0;      // rlk_baseline
+  float ipo_eps = 0.f, band_low = 0.f, band_high = 0.f;
+  int nstats = 8;        // slots of out_stats the caller provides
   float* out_loss;
   float* out_grad;
   float* out_stats;
@@ -112,7 +117,7 @@ cudaError_t launch_support(const SupportArgs& a, cudaStream_t stream);
 cudaError_t launch_logprob_entropy_backward(const LpeBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_support_backward(const SupportArgs& a, cudaStream_t stream);
 
-constexpr int kLossPartials = 8;  // floats per sequence in the loss workspace
+constexpr int kLossPartials = 12;  // floats per sequence in the loss workspace
 size_t loss_workspace_bytes(int64_t n_seq);
 cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t stream);
 

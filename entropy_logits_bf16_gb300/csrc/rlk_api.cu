@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstddef>
 
 #include "internal.h"
 #include "rlk.h"
@@ -236,7 +237,8 @@ rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
     return RLK_ERR_INVALID_ARG;
   if (!finite_positive(tis_cap) || !(std::isfinite(kl_coef) && kl_coef >= 0.0f))
     return RLK_ERR_INVALID_ARG;
-  if (agg != RLK_AGG_TOKEN_MEAN && agg != RLK_AGG_SEQ_MEAN_TOKEN_MEAN) return RLK_ERR_INVALID_ARG;
+  if (agg != RLK_AGG_TOKEN_MEAN && agg != RLK_AGG_SEQ_MEAN_TOKEN_MEAN && agg != RLK_AGG_PROMPT_MEAN)
+    return RLK_ERR_INVALID_ARG;
   if (!seq_offsets || !out_loss) return RLK_ERR_INVALID_ARG;
   if (n_seq > 0 && (!logp_new || !logp_old || !logp_rollout || !logp_ref || !rewards))
     return RLK_ERR_INVALID_ARG;
@@ -259,6 +261,79 @@ rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
   a.tis_cap = tis_cap;
   a.kl_coef = kl_coef;
   a.agg = agg;
+  a.out_loss = out_loss;
+  a.out_grad = out_dloss_dlogp_new;
+  a.out_stats = out_stats;
+  a.workspace = static_cast<float*>(workspace);
+  return rlk::launch_grpo_loss(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
+// The layout the Python binding mirrors (11 four-byte fields).
+static_assert(sizeof(rlk_loss_config) == 44, "rlk_loss_config layout");
+static_assert(offsetof(rlk_loss_config, is_method) == 24 && offsetof(rlk_loss_config, agg) == 40,
+              "rlk_loss_config layout");
+
+rlk_status rlk_policy_loss(const float* logp_new, const float* logp_old,
+                           const float* logp_rollout, const float* logp_ref,
+                           const uint8_t* loss_mask, const float* rewards,
+                           const int32_t* seq_offsets, int32_t n_seq, int32_t group_size,
+                           int64_t n_tok, const rlk_loss_config* config, float* out_loss,
+                           float* out_dloss_dlogp_new, float* out_stats, void* workspace,
+                           size_t workspace_bytes, rlk_stream stream) {
+  if (!config) return RLK_ERR_INVALID_ARG;
+  const rlk_loss_config c = *config;
+  if (c.type != RLK_LOSS_DAPO && c.type != RLK_LOSS_IPO && c.type != RLK_LOSS_ICEPOP)
+    return RLK_ERR_INVALID_ARG;
+  if (c.is_method != RLK_IS_NONE && c.is_method != RLK_IS_TIS && c.is_method != RLK_IS_MIS)
+    return RLK_ERR_INVALID_ARG;
+  if (c.baseline != RLK_BASELINE_MEAN && c.baseline != RLK_BASELINE_LENGTH_WEIGHTED)
+    return RLK_ERR_INVALID_ARG;
+  if (!(std::isfinite(c.ipo_eps) && c.ipo_eps >= 0.0f)) return RLK_ERR_INVALID_ARG;
+  if (!(std::isfinite(c.band_low) && std::isfinite(c.band_high) && c.band_low >= 0.0f &&
+        c.band_low <= c.band_high))
+    return RLK_ERR_INVALID_ARG;
+  if (c.is_method == RLK_IS_TIS && !finite_positive(c.is_cap)) return RLK_ERR_INVALID_ARG;
+  // The common checks; the cap is checked above only where it is used.
+  if (n_seq < 0 || group_size < 1 || n_seq % group_size != 0 || n_tok < 0)
+    return RLK_ERR_INVALID_ARG;
+  if (!(std::isfinite(c.eps_low) && c.eps_low >= 0.0f && std::isfinite(c.eps_high) &&
+        c.eps_high >= 0.0f))
+    return RLK_ERR_INVALID_ARG;
+  if (!(std::isfinite(c.kl_coef) && c.kl_coef >= 0.0f)) return RLK_ERR_INVALID_ARG;
+  if (c.agg != RLK_AGG_TOKEN_MEAN && c.agg != RLK_AGG_SEQ_MEAN_TOKEN_MEAN &&
+      c.agg != RLK_AGG_PROMPT_MEAN)
+    return RLK_ERR_INVALID_ARG;
+  if (!seq_offsets || !out_loss) return RLK_ERR_INVALID_ARG;
+  if (n_seq > 0 && (!logp_new || !logp_old || !logp_rollout || !logp_ref || !rewards))
+    return RLK_ERR_INVALID_ARG;
+  const size_t need = rlk::loss_workspace_bytes(n_seq);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+    return RLK_ERR_WORKSPACE;
+  rlk::LossArgs a;
+  a.logp_new = logp_new;
+  a.logp_old = logp_old;
+  a.logp_rollout = logp_rollout;
+  a.logp_ref = logp_ref;
+  a.mask = loss_mask;
+  a.rewards = rewards;
+  a.seq_offsets = seq_offsets;
+  a.n_seq = n_seq;
+  a.group_size = group_size;
+  a.n_tok = n_tok;
+  a.eps_low = c.eps_low;
+  a.eps_high = c.eps_high;
+  a.tis_cap = c.is_method == RLK_IS_TIS ? c.is_cap : 1.0f;
+  a.kl_coef = c.kl_coef;
+  a.agg = c.agg;
+  a.loss_type = c.type;
+  a.is_method = c.is_method;
+  a.baseline = c.baseline;
+  a.ipo_eps = c.ipo_eps;
+  a.band_low = c.band_low;
+  a.band_high = c.band_high;
+  a.nstats = RLK_NSTATS_POLICY;
   a.out_loss = out_loss;
   a.out_grad = out_dloss_dlogp_new;
   a.out_stats = out_stats;

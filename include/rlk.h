@@ -58,8 +58,30 @@ typedef enum { RLK_BF16 = 0, RLK_F32 = 1 } rlk_dtype;
 
 typedef enum {
   RLK_AGG_TOKEN_MEAN = 0,            /* sum(mask * l) / sum(mask) over the batch (DAPO) */
-  RLK_AGG_SEQ_MEAN_TOKEN_MEAN = 1    /* mean over sequences of each sequence's token mean */
+  RLK_AGG_SEQ_MEAN_TOKEN_MEAN = 1,   /* mean over sequences of each sequence's token mean */
+  RLK_AGG_PROMPT_MEAN = 2            /* mean over groups (prompts) of each group's token mean */
 } rlk_agg;
+
+/* Policy term of rlk_policy_loss (prime-rl v0.10.0 release notes, section
+ * "2. RL Algorithms"). */
+typedef enum {
+  RLK_LOSS_DAPO = 0,     /* clipped ratio pi_new / pi_old, DAPO clip-higher      */
+  RLK_LOSS_IPO = 1,      /* -rho A on tokens with |pi_new - pi_rollout| <= ipo_eps */
+  RLK_LOSS_ICEPOP = 2    /* the DAPO term on tokens with rho in the band         */
+} rlk_loss_type;
+
+/* Rollout correction weight (LumenRL README, section "Rollout Correction"). */
+typedef enum {
+  RLK_IS_NONE = 0,       /* w = 1                                                */
+  RLK_IS_TIS = 1,        /* w = min(pi_old / pi_rollout, is_cap)                 */
+  RLK_IS_MIS = 2         /* w = (pi_old / pi_rollout) / its mean over the batch  */
+} rlk_is_method;
+
+/* GRPO advantage baseline. */
+typedef enum {
+  RLK_BASELINE_MEAN = 0,             /* the group's mean reward                    */
+  RLK_BASELINE_LENGTH_WEIGHTED = 1   /* rewards weighted by packed sequence length */
+} rlk_baseline;
 
 /* Operation ids for rlk_workspace_size. */
 enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2 };
@@ -94,7 +116,10 @@ enum {
   RLK_STAT_TIS_CAPPED = 5,    /* fraction whose weight hit the cap              */
   RLK_STAT_K3_MEAN = 6,       /* mean k3 KL estimate                            */
   RLK_STAT_PG_MEAN = 7,       /* mean clipped policy-gradient term              */
-  RLK_NSTATS = 8
+  RLK_NSTATS = 8,
+  RLK_STAT_MASK_DROPPED = 8,  /* rlk_policy_loss: fraction dropped by the IPO /
+                                 IcePop mask                                    */
+  RLK_NSTATS_POLICY = 9
 };
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -298,7 +323,7 @@ rlk_status rlk_logprob_entropy_support_backward(
  *   l_t = w pg + kl_coef k3.
  * Aggregation RLK_AGG_TOKEN_MEAN: L = sum m l / sum m (0 if sum m = 0).
  * RLK_AGG_SEQ_MEAN_TOKEN_MEAN: L = mean over sequences with sum m > 0 of
- *   that sequence's token mean.
+ *   that sequence's token mean.  RLK_AGG_PROMPT_MEAN: the same over groups.
  * Gradient (if out_dloss_dlogp_new): dL/dlogp_new[t] = (weight of t in L) *
  *   (w g_pg + kl_coef (1 - exp(d))), g_pg = -r A when the unclipped term is
  *   the active minimum (ties count as unclipped), else 0.
@@ -329,6 +354,65 @@ rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
                          float* out_dloss_dlogp_new, float* out_stats, void* workspace,
                          size_t workspace_bytes, rlk_stream stream);
 
+/*
+ * rlk_policy_loss -- rlk_grpo_loss with the pages' loss variants.
+ *
+ * prime-rl v0.10.0 release notes, section "2. RL Algorithms": IPO masks a
+ * token whose probability moved too much between the inference engine and the
+ * trainer, |pi_train(y) - pi_infer(y)| > eps (eps 0.3, no KL term); IcePop
+ * masks a token whose ratio pi_train / pi_infer leaves a fixed band; GRPO gains
+ * a length-weighted baseline and prompt-mean aggregation.  LumenRL README,
+ * section "Rollout Correction": TIS clips large importance ratios, MIS
+ * normalises them.  With pi_train(y) = exp(logp_new), pi_infer(y) =
+ * exp(logp_rollout), r = exp(new - old), rho = exp(new - rollout),
+ * raw = exp(old - rollout):
+ *   A_s = (R_s - b_g) / (std_g R + 1e-6), b_g the group mean or, with
+ *     RLK_BASELINE_LENGTH_WEIGHTED, sum_j len_j R_j / sum_j len_j over the
+ *     group (len_j = seq_offsets[j+1] - seq_offsets[j]; the plain mean when the
+ *     group is empty); std as in rlk_grpo_loss;
+ *   RLK_LOSS_DAPO:   pg = -min(r A, clip(r, 1 - eps_low, 1 + eps_high) A);
+ *   RLK_LOSS_IPO:    keep = [|exp(new) - exp(rollout)| <= ipo_eps],
+ *                    pg = -keep rho A (no clipping; d pg / d new = pg);
+ *   RLK_LOSS_ICEPOP: keep = [band_low <= rho <= band_high], pg = keep x the
+ *                    DAPO term;
+ *   w = 1 (RLK_IS_NONE), min(raw, is_cap) (TIS), raw / mean over mask-1
+ *     tokens of raw (MIS), a detached weight on pg;
+ *   l_t = w pg + kl_coef k3 (the pages' IPO setting uses kl_coef = 0);
+ *   aggregation and gradient as in rlk_grpo_loss, the mask value held fixed.
+ * (The pages give only the IPO mask as a formula; the surrogates, MIS and the
+ *  length weights above are this library's readings.)
+ *
+ * Arguments: as rlk_grpo_loss, with the scalars in *config (a host pointer,
+ *  read before the call returns) and
+ *  out_stats       device float[RLK_NSTATS_POLICY] or NULL (slot
+ *                  RLK_STAT_MASK_DROPPED: the fraction of mask-1 tokens the
+ *                  IPO / IcePop mask drops; RLK_STAT_TIS_MEAN: mean w).
+ *  workspace       as rlk_grpo_loss (rlk_workspace_size(RLK_OP_GRPO_LOSS, ...)).
+ * Errors: as rlk_grpo_loss, plus RLK_ERR_INVALID_ARG for a NULL config, an
+ *  unknown type / method / baseline / aggregation, ipo_eps not finite and
+ *  >= 0, a band that is not finite with 0 <= band_low <= band_high, or (TIS)
+ *  is_cap not finite and > 0.
+ */
+typedef struct rlk_loss_config {
+  rlk_loss_type type;
+  float eps_low, eps_high;      /* DAPO / IcePop clip bounds                    */
+  float ipo_eps;                /* IPO mask threshold                           */
+  float band_low, band_high;    /* IcePop band on rho                           */
+  rlk_is_method is_method;
+  float is_cap;                 /* TIS cap                                      */
+  float kl_coef;
+  rlk_baseline baseline;
+  rlk_agg agg;
+} rlk_loss_config;
+
+rlk_status rlk_policy_loss(const float* logp_new, const float* logp_old,
+                           const float* logp_rollout, const float* logp_ref,
+                           const uint8_t* loss_mask, const float* rewards,
+                           const int32_t* seq_offsets, int32_t n_seq, int32_t group_size,
+                           int64_t n_tok, const rlk_loss_config* config, float* out_loss,
+                           float* out_dloss_dlogp_new, float* out_stats, void* workspace,
+                           size_t workspace_bytes, rlk_stream stream);
+
 /* Largest n_seq that rlk_grpo_loss_noalloc accepts. */
 #define RLK_NOALLOC_MAX_SEQ 16384
 
@@ -339,8 +423,8 @@ rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
  * allocator callback, or a latency-critical loop that bans cudaMalloc because
  * it may synchronise the device.  The caller passes inputs and outputs only.
  *
- * Scratch: a static device array of RLK_NOALLOC_MAX_SEQ * 8 + 4 floats
- * (about 512 KB) inside the library, held by every GPU that loads the library
+ * Scratch: a static device array of RLK_NOALLOC_MAX_SEQ * 12 + 4 floats
+ * (about 768 KB) inside the library, held by every GPU that loads the library
  * until the process exits.  The first call on each device looks up the
  * array's device address (with that device current); make that first call
  * before any stream capture.  Every call overwrites what it reads, so nothing

@@ -194,6 +194,46 @@ def test_grpo_loss_workspace_errors(lib):
     assert loss(lib, ws=ctypes.c_void_p(0x10004)) == 3
 
 
+def pol(lib, **kw):
+    import entropy_logits_bf16_gb300 as rlk
+    cfg = dict(type=0, eps_low=0.2, eps_high=0.28, ipo_eps=0.3, band_low=0.5, band_high=2.0,
+               is_method=1, is_cap=2.0, kl_coef=0.01, baseline=0, agg=0)
+    args = dict(n_seq=4, group=2, n_tok=100, ws=FAKE, wsb=1 << 20, config=True)
+    for k in list(kw):
+        if k in cfg:
+            cfg[k] = kw.pop(k)
+    args.update(kw)
+    c = rlk.LossConfig(**cfg)
+    return lib.rlk_policy_loss(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, args["n_seq"],
+                               args["group"], args["n_tok"],
+                               ctypes.byref(c) if args["config"] else None, FAKE, None, None,
+                               args["ws"], args["wsb"], None)
+
+
+def test_loss_config_layout():
+    import entropy_logits_bf16_gb300 as rlk
+    assert ctypes.sizeof(rlk.LossConfig) == 44
+    assert rlk.LossConfig.is_method.offset == 24 and rlk.LossConfig.agg.offset == 40
+
+
+@pytest.mark.parametrize("kw", [
+    dict(config=False), dict(type=3), dict(type=-1), dict(is_method=3), dict(baseline=2),
+    dict(agg=3), dict(ipo_eps=-0.1), dict(ipo_eps=math.nan), dict(band_low=2.5),
+    dict(band_low=-1.0), dict(band_high=math.inf), dict(is_cap=0.0), dict(kl_coef=-1.0),
+    dict(eps_low=math.nan), dict(group=3), dict(n_seq=-2),
+])
+def test_policy_loss_rejects(lib, kw):
+    assert pol(lib, **kw) == 1
+
+
+def test_policy_loss_workspace_and_unused_cap(lib):
+    assert pol(lib, ws=None) == 3
+    assert pol(lib, wsb=16) == 3
+    # the cap is checked only where TIS uses it: these reach the workspace check
+    assert pol(lib, is_method=0, is_cap=0.0, ws=None) == 3
+    assert pol(lib, is_method=2, is_cap=-1.0, ws=None) == 3
+
+
 def test_lmhead_rejects(lib):
     f = lib.rlk_lmhead_logprob
     ok = dict(T=4, H=128, V=1000, temp=0.7, p=1.0)
