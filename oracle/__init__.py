@@ -60,6 +60,8 @@ def _load():
                                                             vp, vp, vp, vp, i]
             lib.oracle_policy_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i, f32, f32,
                                                f32, f32, f32, i, f32, f32, i, i, vp, vp, vp, vp]
+            lib.oracle_lmhead_backward.argtypes = [vp, vp, i64, i64, i64, vp, f32, f32, vp, vp,
+                                                   vp, vp, i]
             lib.oracle_grpo_loss.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, f32,
                                              f32, f32, i, vp, vp, vp, vp]
             lib.oracle_lmhead_rows.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, f32, f32,
@@ -68,7 +70,7 @@ def _load():
                        lib.oracle_logprob_entropy_support,
                        lib.oracle_logprob_entropy_support_backward,
                        lib.oracle_logprob_entropy_backward, lib.oracle_policy_loss,
-                       lib.oracle_grpo_loss, lib.oracle_lmhead_rows):
+                       lib.oracle_lmhead_backward, lib.oracle_grpo_loss, lib.oracle_lmhead_rows):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -277,3 +279,26 @@ def lmhead_rows(hidden_bits, w_bits, rows, ids, temperature, top_p=1.0, threads=
     if rc:
         raise ValueError("oracle_lmhead_rows rejected its arguments")
     return lp, ent, k
+
+
+def lmhead_backward(hidden_bits, w_bits, ids, temperature, top_p=1.0, g_logprob=None,
+                    g_entropy=None, threads=None):
+    """Gradients of the LM-head path with the retained sets held fixed:
+    (dL/dhidden [T, H], dL/dW [V, H]) in fp64."""
+    h = np.ascontiguousarray(hidden_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    T, H = h.shape
+    V, H2 = w.shape
+    assert H == H2
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    gl = None if g_logprob is None else np.ascontiguousarray(g_logprob, dtype=np.float32)
+    gh = None if g_entropy is None else np.ascontiguousarray(g_entropy, dtype=np.float32)
+    dh = np.empty((T, H), np.float64)
+    dw = np.empty((V, H), np.float64)
+    rc = _load().oracle_lmhead_backward(_ptr(h), _ptr(w), T, H, V, _ptr(ids),
+                                        float(np.float32(temperature)), float(np.float32(top_p)),
+                                        _ptr(gl), _ptr(gh), _ptr(dh), _ptr(dw),
+                                        threads or default_threads())
+    if rc:
+        raise ValueError("oracle_lmhead_backward rejected its arguments")
+    return dh, dw

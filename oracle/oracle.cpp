@@ -772,4 +772,46 @@ int oracle_lmhead_rows(const uint16_t* hidden, const uint16_t* w_vocab, int64_t 
   return 0;
 }
 
+// Gradient of the LM-head path (oracle_lmhead_rows, every row) for
+// L = sum_t g_lp[t] logprob_t + g_h[t] H_t, the retained sets held fixed:
+//  1. z = hidden W^T in fp64 from the exact bf16 values;
+//  2. dz[t, :] = the logits-path gradient of row t (score_row, step 9);
+//  3. out_dh = dz W ([T, H]); out_dw = dz^T hidden ([V, H]), each entry a
+//     plain sum over the contracted index in increasing order.
+// Rows with no distribution give NaN in their dz, so in dh and in every dw.
+int oracle_lmhead_backward(const uint16_t* hidden, const uint16_t* w_vocab, int64_t T, int64_t H,
+                           int64_t V, const int32_t* ids, float temperature, float top_p,
+                           const float* g_lp, const float* g_h, double* out_dh, double* out_dw,
+                           int nthreads) {
+  if (!hidden || !w_vocab || !ids || T < 0 || H < 1 || V < 1 || !out_dh || !out_dw) return 1;
+  const double Td = static_cast<double>(temperature), pd = static_cast<double>(top_p);
+  std::vector<double> dz(static_cast<size_t>(T) * V);
+  parallel_rows(T, nthreads, [&](int64_t row) {
+    std::vector<double> h(H), z(V);
+    for (int64_t k = 0; k < H; ++k) h[k] = bf16_to_double(hidden[row * H + k]);
+    for (int64_t i = 0; i < V; ++i) {
+      const uint16_t* wr = w_vocab + i * H;
+      double acc = 0.0;  // products of bf16 values are exact in fp64
+      for (int64_t k = 0; k < H; ++k) acc += h[k] * bf16_to_double(wr[k]);
+      z[i] = acc;
+    }
+    score_row(z, ids[row], Td, pd, 0, g_lp ? static_cast<double>(g_lp[row]) : 0.0,
+              g_h ? static_cast<double>(g_h[row]) : 0.0, dz.data() + row * V);
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < V; ++i) acc += dz[row * V + i] * bf16_to_double(w_vocab[i * H + k]);
+      out_dh[row * H + k] = acc;
+    }
+  });
+  parallel_rows(V, nthreads, [&](int64_t i) {
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t row = 0; row < T; ++row)
+        acc += dz[row * V + i] * bf16_to_double(hidden[row * H + k]);
+      out_dw[i * H + k] = acc;
+    }
+  });
+  return 0;
+}
+
 }  // extern "C"

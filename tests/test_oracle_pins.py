@@ -757,3 +757,25 @@ def test_policy_loss_gradient_matches_finite_differences(oracle, cfg):
         assert g[t] == pytest.approx(fd, rel=2e-4, abs=2e-7), t
         checked += 1
     assert checked >= len(new) // 2
+
+
+@pytest.mark.parametrize("p", [1.0, 0.9])
+def test_lmhead_backward_is_the_chain_rule(oracle, p):
+    """With small dyadic bf16 inputs every logit is exact in fp32, so the
+    (pinned) dense logits gradient of z = h W^T applies as is: dL/dh = dz W
+    and dL/dW = dz^T h, here by library matmuls in fp64."""
+    rng = np.random.default_rng(6)
+    T, H, V = 5, 16, 40
+    h = (rng.integers(-4, 5, (T, H)) / 4.0).astype(np.float32)     # multiples of 1/4
+    w = (rng.integers(-8, 9, (V, H)) / 8.0).astype(np.float32)     # multiples of 1/8
+    hb = torch.from_numpy(h).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    wb = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    z = (h.astype(np.float64) @ w.T.astype(np.float64))
+    assert np.array_equal(z.astype(np.float32).astype(np.float64), z)   # exact in fp32
+    ids = rng.integers(0, V, T).astype(np.int32)
+    gl = rng.normal(0, 1, T).astype(np.float32)
+    gh = rng.normal(0, 1, T).astype(np.float32)
+    dh, dw = oracle.lmhead_backward(hb, wb, ids, 0.7, p, gl, gh)
+    dz = oracle.logprob_entropy_backward(z.astype(np.float32), ids, 0.7, p, gl, gh)
+    assert np.allclose(dh, dz @ w.astype(np.float64), rtol=1e-12, atol=1e-14)
+    assert np.allclose(dw, dz.T @ h.astype(np.float64), rtol=1e-12, atol=1e-14)
