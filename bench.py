@@ -481,6 +481,63 @@ def run_lmhead(args, ws, rank, dev, barrier):
     return line
 
 
+LMB_METRIC = ("tokens/s for the fused LM-head backward (dL/dhidden and dL/dW at top_p 1 by "
+              "recompute) at V=151936, H=4096")
+
+
+def run_lmhead_backward(args, ws, rank, dev, barrier):
+    """--op lmhead_backward: rlk_lmhead_logprob_bwd on the LM-head benchmark
+    shape (the forward, which saves each row's log-normaliser, runs once before
+    the timed region).  Three GEMMs of 2 T V H flops each: the recompute with
+    the gradient epilogue (tcgen05) and the two weight-side products."""
+    import entropy_logits_bf16_gb300 as rlk
+    import workloads
+    stream = torch.cuda.current_stream(dev)
+    hidden, w, ids = workloads.lmhead_inputs(LM_T, LM_H, VOCAB, seed=4 + rank, device=dev)
+    ids = ids.to(dev).to(torch.int32)
+    lse = torch.empty(LM_T, device=dev)
+    _, ent = rlk.lmhead_logprob(hidden, w, ids, TEMPERATURE, out_lse=lse)
+    g = torch.Generator(device="cpu").manual_seed(rank_seed(rank) + 3)
+    glp = torch.empty(LM_T).uniform_(-1, 1, generator=g).to(dev)
+    gh = torch.empty(LM_T).uniform_(-1, 1, generator=g).to(dev)
+    dh = torch.empty((LM_T, LM_H), device=dev)
+    dw = torch.empty((VOCAB, LM_H), device=dev)
+    wsp = torch.empty(rlk.workspace_size(rlk.OP_LMHEAD_BWD, LM_T, VOCAB, LM_H), dtype=torch.uint8,
+                      device=dev)
+
+    def bwd():
+        rlk.lmhead_backward(hidden, w, ids, TEMPERATURE, lse, ent, glp, gh, grad_hidden=dh,
+                            grad_w=dw, workspace=wsp)
+
+    elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [bwd], barrier)
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    flops = 3 * 2.0 * LM_T * LM_H * VOCAB
+    achieved = flops / (part_ms[0] / 1e3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0))
+    n_chunks = (LM_T + 4095) // 4096
+    return {
+        "metric": LMB_METRIC, "value": whole_job_rate(LM_T, args.steps, ws, elapsed_ms),
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"fused LM-head backward: hidden [{LM_T}, {LM_H}] bf16 N(0,1), "
+                               f"W_vocab [{VOCAB}, {LM_H}] bf16 N(0, 0.02^2), temperature "
+                               f"{TEMPERATURE}, top_p 1; dz recomputed 4096 rows at a time",
+                   "global_batch": LM_T * ws,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "W (1.24 GB) and dW (2.49 GB) larger than L2; no flush between steps"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                     "kernel": "lmhead_kernel (gradient epilogue) + two cuBLASLt GEMMs per chunk",
+                     "flops_per_launch": flops, "launch_ms": part_ms[0]},
+        "gpu_launches": n_chunks * args.steps,
+        "library_gemms_per_step": 2 * n_chunks,
+        "clocks": clk,
+    }
+
+
 SUP_METRIC = ("tokens/s for supplied-support logprob+entropy (the top-p retained set given as "
               "CSR) at V=151936 bf16")
 
@@ -617,11 +674,12 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "support", "support_backward",
-                                                       "backward"],
+    ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "lmhead_backward", "support",
+                                                       "support_backward", "backward"],
                     help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused "
                          "LM-head; support: the supplied-support scorer; support_backward: its "
-                         "gradient; backward: the dense top-p gradient")
+                         "gradient; backward: the dense top-p gradient; lmhead_backward: the "
+                         "LM-head gradients")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -647,7 +705,7 @@ def main():
 
     run = {"logits": run_logits, "lmhead": run_lmhead, "support": run_support,
            "support_backward": lambda *a: run_support(*a, backward=True),
-           "backward": run_backward}[args.op]
+           "backward": run_backward, "lmhead_backward": run_lmhead_backward}[args.op]
     line = run(args, ws, rank, dev, barrier)
     if line is not None:
         print(json.dumps(line), flush=True)

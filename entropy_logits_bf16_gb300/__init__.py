@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace"
                 4: "CUDA error", 5: "timeout", 6: "bad input"}
 STATUS_BAD_TOKEN_ID = 0x1
 STATUS_NONFINITE = 0x2
-OP_LOGPROB_ENTROPY, OP_GRPO_LOSS, OP_LMHEAD = 0, 1, 2
+OP_LOGPROB_ENTROPY, OP_GRPO_LOSS, OP_LMHEAD, OP_LMHEAD_BWD = 0, 1, 2, 3
 AGG_TOKEN_MEAN, AGG_SEQ_MEAN_TOKEN_MEAN, AGG_PROMPT_MEAN = 0, 1, 2
 LOSS_DAPO, LOSS_IPO, LOSS_ICEPOP = 0, 1, 2
 IS_NONE, IS_TIS, IS_MIS = 0, 1, 2
@@ -44,7 +44,8 @@ STAT_NAMES = ("loss", "tokens", "clip_low_frac", "clip_high_frac", "tis_mean",
 EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logprob_entropy",
            "rlk_logprob_entropy_fwd", "rlk_logprob_entropy_bwd",
            "rlk_logprob_entropy_support", "rlk_logprob_entropy_support_backward",
-           "rlk_grpo_loss", "rlk_policy_loss", "rlk_lmhead_logprob",
+           "rlk_grpo_loss", "rlk_policy_loss", "rlk_lmhead_logprob", "rlk_lmhead_logprob_fwd",
+           "rlk_lmhead_logprob_bwd",
            "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
 DEBUG_EXPORTS = ("rlk_lmhead_logits_debug",)
@@ -109,6 +110,12 @@ def load(path: str | None = None):
         lib.rlk_lmhead_logprob.argtypes = [vp, vp, i64, i64, i64, vp, f32, f32, vp, vp, vp, vp,
                                            sz, vp]
         lib.rlk_lmhead_logprob.restype = ctypes.c_int
+        lib.rlk_lmhead_logprob_fwd.argtypes = [vp, vp, i64, i64, i64, vp, f32, f32, vp, vp, vp,
+                                               vp, vp, sz, vp]
+        lib.rlk_lmhead_logprob_fwd.restype = ctypes.c_int
+        lib.rlk_lmhead_logprob_bwd.argtypes = [vp, vp, i64, i64, i64, vp, f32, vp, vp, vp, vp, vp,
+                                               vp, ctypes.c_int, vp, sz, vp]
+        lib.rlk_lmhead_logprob_bwd.restype = ctypes.c_int
         lib.rlk_lmhead_logits_debug.argtypes = [vp, vp, i64, i64, i64, vp, f32, vp, vp, vp, vp,
                                                 vp, sz, vp]
         lib.rlk_lmhead_logits_debug.restype = ctypes.c_int
@@ -414,8 +421,10 @@ def policy_loss(logp_new, logp_old, logp_rollout, logp_ref, rewards, seq_offsets
 
 
 def lmhead_logprob(hidden, w_vocab, token_ids, temperature, top_p=1.0, *, status_word=None,
-                   workspace=None):
-    """Fused LM-head top-p=1 log-probability and entropy (logits never stored)."""
+                   workspace=None, out_lse=None):
+    """Fused LM-head top-p=1 log-probability and entropy (logits never stored).
+    ``out_lse`` (CUDA fp32 [T]) receives each row's log-normaliser for
+    ``lmhead_backward``."""
     lib = load()
     _need_cuda(hidden, w_vocab, token_ids)
     if hidden.dtype != torch.bfloat16 or w_vocab.dtype != torch.bfloat16:
@@ -432,12 +441,63 @@ def lmhead_logprob(hidden, w_vocab, token_ids, temperature, top_p=1.0, *, status
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
     lp = torch.empty(T, device=dev, dtype=torch.float32)
     ent = torch.empty(T, device=dev, dtype=torch.float32)
-    code = lib.rlk_lmhead_logprob(_ptr(hidden), _ptr(w_vocab), T, H, V, _ptr(token_ids),
-                                  float(temperature), float(top_p), _ptr(lp), _ptr(ent),
-                                  _ptr(status_word), _ptr(workspace),
-                                  0 if workspace is None else workspace.numel(), _stream(dev))
-    _check("rlk_lmhead_logprob", code)
+    wsb = 0 if workspace is None else workspace.numel()
+    if out_lse is not None:
+        _need_cuda(out_lse)
+        if out_lse.dtype != torch.float32 or out_lse.numel() != T or not out_lse.is_contiguous():
+            raise ValueError("out_lse must be contiguous fp32 [T]")
+        code = lib.rlk_lmhead_logprob_fwd(_ptr(hidden), _ptr(w_vocab), T, H, V, _ptr(token_ids),
+                                          float(temperature), float(top_p), _ptr(lp), _ptr(ent),
+                                          _ptr(out_lse), _ptr(status_word), _ptr(workspace), wsb,
+                                          _stream(dev))
+        _check("rlk_lmhead_logprob_fwd", code)
+    else:
+        code = lib.rlk_lmhead_logprob(_ptr(hidden), _ptr(w_vocab), T, H, V, _ptr(token_ids),
+                                      float(temperature), float(top_p), _ptr(lp), _ptr(ent),
+                                      _ptr(status_word), _ptr(workspace), wsb, _stream(dev))
+        _check("rlk_lmhead_logprob", code)
     return lp, ent
+
+
+def lmhead_backward(hidden, w_vocab, token_ids, temperature, lse, entropy, grad_logprob=None,
+                    grad_entropy=None, *, grad_hidden=None, grad_w=None, accumulate_grad_w=False,
+                    workspace=None):
+    """Gradients of the fused LM-head path: (dL/dhidden fp32 [T, H],
+    dL/dW fp32 [V, H]); ``lse`` and ``entropy`` from the forward."""
+    lib = load()
+    _need_cuda(hidden, w_vocab, token_ids, lse, entropy, grad_logprob, grad_entropy, grad_hidden,
+               grad_w)
+    if hidden.dtype != torch.bfloat16 or w_vocab.dtype != torch.bfloat16:
+        raise ValueError("hidden and w_vocab must be bf16")
+    if not (hidden.is_contiguous() and w_vocab.is_contiguous()):
+        raise ValueError("hidden and w_vocab must be contiguous")
+    T, H = hidden.shape
+    V, H2 = w_vocab.shape
+    if H != H2:
+        raise ValueError("hidden and w_vocab disagree on H")
+    for t in (lse, entropy, grad_logprob, grad_entropy):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != T or not t.is_contiguous()):
+            raise ValueError("lse, entropy and the gradients must be contiguous fp32 [T]")
+    dev = hidden.device
+    if grad_hidden is None:
+        grad_hidden = torch.empty((T, H), device=dev, dtype=torch.float32)
+    if grad_w is None:
+        if accumulate_grad_w:
+            raise ValueError("accumulate_grad_w needs grad_w")
+        grad_w = torch.empty((V, H), device=dev, dtype=torch.float32)
+    for t, shp in ((grad_hidden, (T, H)), (grad_w, (V, H))):
+        if t.dtype != torch.float32 or tuple(t.shape) != shp or not t.is_contiguous():
+            raise ValueError("grad_hidden / grad_w must be contiguous fp32 [T, H] / [V, H]")
+    need = int(lib.rlk_workspace_size(OP_LMHEAD_BWD, T, V, H))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=dev, dtype=torch.uint8)
+    code = lib.rlk_lmhead_logprob_bwd(_ptr(hidden), _ptr(w_vocab), T, H, V, _ptr(token_ids),
+                                      float(temperature), _ptr(lse), _ptr(entropy),
+                                      _ptr(grad_logprob), _ptr(grad_entropy), _ptr(grad_hidden),
+                                      _ptr(grad_w), int(bool(accumulate_grad_w)), _ptr(workspace),
+                                      workspace.numel(), _stream(dev))
+    _check("rlk_lmhead_logprob_bwd", code)
+    return grad_hidden, grad_w
 
 
 def lmhead_logits_debug(hidden, w_vocab, token_ids, temperature):

@@ -103,6 +103,24 @@ struct LmheadArgs {
   float* out_entropy;
   uint32_t* status;
   void* workspace;
+  float* out_lse = nullptr;   // [T] ln sum exp(z / T), for the backward
+};
+
+struct LmheadBwdArgs {
+  const void* hidden;          // bf16 [T, H]
+  const void* w_vocab;         // bf16 [V, H]
+  int64_t T, H, V;
+  const int32_t* ids;
+  float temperature;
+  const float* lse;            // [T] from the forward
+  const float* entropy;        // [T] from the forward
+  const float* grad_logprob;   // [T] or NULL
+  const float* grad_entropy;   // [T] or NULL
+  float* grad_hidden;          // fp32 [T, H]
+  float* grad_w;               // fp32 [V, H]
+  int accumulate_w;
+  void* workspace;
+  size_t workspace_bytes;
 };
 
 // Number of SMs of the current device (cached per device).
@@ -123,6 +141,9 @@ cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t stream);
 
 size_t lmhead_workspace_bytes(int64_t T, int64_t V, int64_t H);
 cudaError_t launch_lmhead(const LmheadArgs& a, cudaStream_t stream);
+size_t lmhead_bwd_workspace_bytes(int64_t T, int64_t V, int64_t H);
+// Returns cudaErrorNotSupported when cuBLASLt finds no algorithm.
+cudaError_t launch_lmhead_backward(const LmheadBwdArgs& a, cudaStream_t stream);
 // Same, also writing the fp32 logits [T, V] to debug_logits (validation aid).
 cudaError_t launch_lmhead_impl(const LmheadArgs& a, float* debug_logits, cudaStream_t stream);
 

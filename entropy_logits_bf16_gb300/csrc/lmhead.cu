@@ -35,6 +35,9 @@
 #include <math.h>
 
 #include <atomic>
+#include <mutex>
+
+#include <cublasLt.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -202,6 +205,16 @@ struct LmParams {
   float* zy;             // [T] the selected token's logit
   float* debug_logits;   // [T][V] when non-null (validation aid)
   uint32_t* status;
+  // gradient mode (grad != 0): the epilogue writes dL/dz (bf16) instead of
+  // folding row states
+  int grad;
+  const float* lse;      // [T] ln sum exp(z / T) from the forward
+  const float* ent;      // [T] entropy from the forward
+  const float* glp;      // [T] or NULL
+  const float* gh;       // [T] or NULL
+  uint16_t* dz;          // [T][ldz] bf16
+  int64_t ldz;
+  float inv_t;
 };
 
 __device__ __forceinline__ void slice_bounds(int n_nt, int sl, int& nt0, int& nt1) {
@@ -331,6 +344,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       slice_bounds(p.n_nt, sl, nt0, nt1);
       const int64_t row = (int64_t)mt * BM + q * 32 + lane;
       const int64_t y = row < p.T ? (int64_t)p.ids[row] : -1;
+      // gradient mode: dz = q (-C t - B) + A [v = y] with t = log2 q
+      // = z c - lse log2(e), A = g_lp / T, B = (g_lp + g_H H) / T,
+      // C = g_H ln2 / T
+      float gnE = 0.f, gA = 0.f, gB = 0.f, gC = 0.f;
+      if (p.grad && row < p.T) {
+        const float glp = p.glp ? p.glp[row] : 0.f, gh = p.gh ? p.gh[row] : 0.f;
+        gnE = -__fmul_rn(p.lse[row], kLog2e);
+        gA = __fmul_rn(glp, p.inv_t);
+        gB = __fmul_rn(__fmaf_rn(gh, p.ent[row], glp), p.inv_t);
+        gC = __fmul_rn(__fmul_rn(gh, kLn2), p.inv_t);
+      }
       RowState st{-INFINITY, 0.f, 0.f, 0.f};
       float zy = 0.f;
       bool have_zy = false;
@@ -344,6 +368,36 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(tmem + lane_base + acc * BN + ch * 32, v);
           const int64_t col0 = (int64_t)nt * BN + ch * 32;
           const int n = (int)(p.V - col0 < 32 ? (p.V - col0 > 0 ? p.V - col0 : 0) : 32);
+          if (p.grad) {
+            if (row < p.T && n > 0) {
+              uint32_t o[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                float g2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const float t = __fmaf_rn(v[2 * j + e], p.c, gnE);
+                  const float qv = ex2(t);
+                  g2[e] = __fmul_rn(qv, __fmaf_rn(-gC, t, -gB));
+                  if (col0 + 2 * j + e == y) g2[e] = __fadd_rn(g2[e], gA);
+                }
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(g2[0], g2[1]);
+                o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              uint16_t* dst = p.dz + row * p.ldz + col0;
+              if (n == 32) {
+                uint4* d4 = reinterpret_cast<uint4*>(dst);   // ldz % 8 == 0, col0 % 32 == 0
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  d4[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < n) dst[j] = (uint16_t)((o[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+              }
+            }
+            continue;
+          }
           if (n > 0) absorb32(st, v, n, p.c);
           if (y >= col0 && y < col0 + n) {
 #pragma unroll
@@ -361,7 +415,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(acce0 + 8 * acc);
       }
-      if (ok && row < p.T) {
+      if (ok && row < p.T && !p.grad) {
         p.part[(int64_t)sl * p.T + row] = make_float4(st.m, st.hi, st.lo, st.u);
         if (have_zy) p.zy[row] = zy;
       }
@@ -380,13 +434,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // Merge each row's slice states in slice order and write the outputs.
 __global__ void __launch_bounds__(256) lmhead_combine_kernel(LmParams p, float* out_lp,
-                                                             float* out_ent, float temperature) {
+                                                             float* out_ent, float* out_lse,
+                                                             float temperature) {
   const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= p.T) return;
   const int64_t y = p.ids[row];
   if (y < 0 || y >= p.V) {
     out_lp[row] = NAN;
     out_ent[row] = NAN;
+    if (out_lse) out_lse[row] = NAN;
     if (p.status) atomicOr(p.status, RLK_STATUS_BAD_TOKEN_ID);
     return;
   }
@@ -399,10 +455,12 @@ __global__ void __launch_bounds__(256) lmhead_combine_kernel(LmParams p, float* 
   if (!(isfinite(z) && isfinite(st.u) && isfinite(st.m))) {
     out_lp[row] = NAN;
     out_ent[row] = NAN;
+    if (out_lse) out_lse[row] = NAN;
     if (p.status) atomicOr(p.status, RLK_STATUS_NONFINITE);
     return;
   }
   const float lz = logf(z);
+  if (out_lse) out_lse[row] = __fadd_rn(__fdiv_rn(st.m, temperature), lz);
   out_lp[row] = __fsub_rn(__fdiv_rn(__fsub_rn(p.zy[row], st.m), temperature), lz);
   out_ent[row] = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, st.u), z));
 }
@@ -460,7 +518,7 @@ cudaError_t launch_lmhead_impl(const LmheadArgs& a, float* debug_logits, cudaStr
     if (e != cudaSuccess) return e;
     attr_done.store(1);
   }
-  LmParams p;
+  LmParams p{};
   p.T = a.T;
   p.V = a.V;
   p.n_mt = (int)((a.T + BM - 1) / BM);
@@ -474,13 +532,149 @@ cudaError_t launch_lmhead_impl(const LmheadArgs& a, float* debug_logits, cudaStr
                                   (size_t)NSLICE * (size_t)a.T * sizeof(float4));
   p.debug_logits = debug_logits;
   p.status = a.status;
+  p.grad = 0;
   const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
   lmhead_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   lmhead_combine_kernel<<<(unsigned)((a.T + 255) / 256), 256, 0, stream>>>(
-      p, a.out_logprob, a.out_entropy, a.temperature);
+      p, a.out_logprob, a.out_entropy, a.out_lse, a.temperature);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ backward
+// dL/dhidden = dZ W and dL/dW = dZ^T hidden, with dZ = dL/dz recomputed by
+// the GEMM above (gradient epilogue) one chunk of rows at a time, so the
+// gradient logits exist for at most kBwdRows rows (the chunked-loss layout of
+// prime-rl v0.10.0 notes, "1. Trainer Performance").  The two weight-side
+// products are plain GEMMs with transposed operands: cuBLASLt, bf16 inputs,
+// fp32 accumulation and output, with the caller's workspace.
+namespace {
+
+constexpr int64_t kBwdRows = 4096;
+constexpr size_t kLtWorkspace = (size_t)64 << 20;
+
+int64_t dz_ld(int64_t V) { return (V + 7) / 8 * 8; }   // 16-byte rows
+
+size_t dz_bytes(int64_t T, int64_t V) {
+  const int64_t rows = T < kBwdRows ? T : kBwdRows;
+  return ((size_t)rows * (size_t)dz_ld(V) * 2 + 255) & ~(size_t)255;
+}
+
+cublasLtHandle_t lt_handle() {
+  static cublasLtHandle_t h = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    if (cublasLtCreate(&h) != CUBLAS_STATUS_SUCCESS) h = nullptr;
+  });
+  return h;
+}
+
+// D[m, n] (column-major, ld ldd, fp32) = op(A) op(B) + beta D, A and B bf16
+// given by their stored column-major shapes.
+cudaError_t lt_gemm(cublasOperation_t opa, cublasOperation_t opb, int64_t m, int64_t n,
+                    int64_t k, const void* A, int64_t a_rows, int64_t a_cols, int64_t lda,
+                    const void* B, int64_t b_rows, int64_t b_cols, int64_t ldb, float* D,
+                    int64_t ldd, float beta, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)k;
+  cublasLtHandle_t h = lt_handle();
+  if (!h) return cudaErrorNotSupported;
+  cublasLtMatmulDesc_t op = nullptr;
+  cublasLtMatrixLayout_t la = nullptr, lb = nullptr, ld = nullptr;
+  cublasLtMatmulPreference_t pref = nullptr;
+  cudaError_t err = cudaErrorNotSupported;
+  cublasLtMatmulHeuristicResult_t res{};
+  int nres = 0;
+  const float alpha = 1.0f;
+  if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS) goto done;
+  if (cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &opa, sizeof(opa)) !=
+          CUBLAS_STATUS_SUCCESS ||
+      cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &opb, sizeof(opb)) !=
+          CUBLAS_STATUS_SUCCESS)
+    goto done;
+  if (cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, a_rows, a_cols, lda) != CUBLAS_STATUS_SUCCESS ||
+      cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, b_rows, b_cols, ldb) != CUBLAS_STATUS_SUCCESS ||
+      cublasLtMatrixLayoutCreate(&ld, CUDA_R_32F, m, n, ldd) != CUBLAS_STATUS_SUCCESS)
+    goto done;
+  if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS ||
+      cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
+                                           &ws_bytes, sizeof(ws_bytes)) != CUBLAS_STATUS_SUCCESS)
+    goto done;
+  if (cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, ld, ld, pref, 1, &res, &nres) !=
+          CUBLAS_STATUS_SUCCESS ||
+      nres < 1)
+    goto done;
+  err = cublasLtMatmul(h, op, &alpha, A, la, B, lb, &beta, D, ld, D, ld, &res.algo, ws, ws_bytes,
+                       stream) == CUBLAS_STATUS_SUCCESS
+            ? cudaSuccess
+            : cudaErrorLaunchFailure;
+done:
+  if (pref) cublasLtMatmulPreferenceDestroy(pref);
+  if (ld) cublasLtMatrixLayoutDestroy(ld);
+  if (lb) cublasLtMatrixLayoutDestroy(lb);
+  if (la) cublasLtMatrixLayoutDestroy(la);
+  if (op) cublasLtMatmulDescDestroy(op);
+  return err;
+}
+
+}  // namespace
+
+size_t lmhead_bwd_workspace_bytes(int64_t T, int64_t V, int64_t H) {
+  (void)H;
+  return dz_bytes(T, V) + kLtWorkspace;
+}
+
+cudaError_t launch_lmhead_backward(const LmheadBwdArgs& a, cudaStream_t stream) {
+  static std::atomic<int> attr_done{0};
+  if (!attr_done.load()) {
+    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done.store(1);
+  }
+  CUtensorMap mb;
+  if (!make_map(&mb, a.w_vocab, (uint64_t)a.V, (uint64_t)a.H, BN)) return cudaErrorInvalidValue;
+  uint16_t* dz = static_cast<uint16_t*>(a.workspace);
+  const int64_t ldz = dz_ld(a.V);
+  void* lt_ws = static_cast<char*>(a.workspace) + dz_bytes(a.T, a.V);
+  const uint16_t* hid = static_cast<const uint16_t*>(a.hidden);
+  for (int64_t r0 = 0; r0 < a.T; r0 += kBwdRows) {
+    const int64_t rows = a.T - r0 < kBwdRows ? a.T - r0 : kBwdRows;
+    CUtensorMap ma;
+    if (!make_map(&ma, hid + r0 * a.H, (uint64_t)rows, (uint64_t)a.H, BM))
+      return cudaErrorInvalidValue;
+    LmParams p{};
+    p.T = rows;
+    p.V = a.V;
+    p.n_mt = (int)((rows + BM - 1) / BM);
+    p.n_nt = (int)((a.V + BN - 1) / BN);
+    p.n_units = p.n_mt * NSLICE;
+    p.k_steps = (int)(a.H / BK);
+    p.ids = a.ids + r0;
+    p.c = (float)(1.4426950408889634 / (double)a.temperature);
+    p.inv_t = (float)(1.0 / (double)a.temperature);
+    p.grad = 1;
+    p.lse = a.lse + r0;
+    p.ent = a.entropy + r0;
+    p.glp = a.grad_logprob ? a.grad_logprob + r0 : nullptr;
+    p.gh = a.grad_entropy ? a.grad_entropy + r0 : nullptr;
+    p.dz = dz;
+    p.ldz = ldz;
+    const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
+    lmhead_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // dH[r0 : r0 + rows] = dZ W: column-major D[H, rows] = W^T[H, V] dZ^T[V, rows]
+    e = lt_gemm(CUBLAS_OP_N, CUBLAS_OP_N, a.H, rows, a.V, a.w_vocab, a.H, a.V, a.H, dz, a.V, rows,
+                ldz, a.grad_hidden + r0 * a.H, a.H, 0.0f, lt_ws, kLtWorkspace, stream);
+    if (e != cudaSuccess) return e;
+    // dW (+)= dZ^T hidden: column-major D[H, V] = hidden^T[H, rows] dZ[rows, V]
+    const float beta = (r0 > 0 || a.accumulate_w) ? 1.0f : 0.0f;
+    e = lt_gemm(CUBLAS_OP_N, CUBLAS_OP_T, a.H, a.V, rows, hid + r0 * a.H, a.H, rows, a.H, dz, a.V,
+                rows, ldz, a.grad_w, a.H, beta, lt_ws, kLtWorkspace, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_lmhead(const LmheadArgs& a, cudaStream_t stream) {

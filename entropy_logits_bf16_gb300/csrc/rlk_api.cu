@@ -58,6 +58,7 @@ size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H) {
     case RLK_OP_LOGPROB_ENTROPY: return 0;
     case RLK_OP_GRPO_LOSS: return rlk::loss_workspace_bytes(V);
     case RLK_OP_LMHEAD: return rlk::lmhead_workspace_bytes(T, V, H);
+    case RLK_OP_LMHEAD_BWD: return rlk::lmhead_bwd_workspace_bytes(T, V, H);
   }
   return 0;
 }
@@ -346,8 +347,8 @@ rlk_status rlk_policy_loss(const float* logp_new, const float* logp_old,
 static rlk_status lmhead_common(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
                                 int64_t V, const int32_t* token_ids, float temperature,
                                 float top_p, float* out_logits, float* out_logprob,
-                                float* out_entropy, uint32_t* out_status_word, void* workspace,
-                                size_t workspace_bytes, rlk_stream stream) {
+                                float* out_entropy, float* out_lse, uint32_t* out_status_word,
+                                void* workspace, size_t workspace_bytes, rlk_stream stream) {
   if (T < 0 || H < 64 || H % 64 != 0 || V < 1 || V > (int64_t(1) << 24)) return RLK_ERR_INVALID_ARG;
   if (T > (int64_t(1) << 30) || H > (int64_t(1) << 20)) return RLK_ERR_INVALID_ARG;
   if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
@@ -374,6 +375,7 @@ static rlk_status lmhead_common(const void* hidden, const void* w_vocab, int64_t
   a.out_entropy = out_entropy;
   a.status = out_status_word;
   a.workspace = workspace;
+  a.out_lse = out_lse;
   const cudaError_t e =
       rlk::launch_lmhead_impl(a, out_logits, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return RLK_ERR_UNSUPPORTED;
@@ -386,8 +388,62 @@ rlk_status rlk_lmhead_logprob(const void* hidden, const void* w_vocab, int64_t T
                               uint32_t* out_status_word, void* workspace,
                               size_t workspace_bytes, rlk_stream stream) {
   return lmhead_common(hidden, w_vocab, T, H, V, token_ids, temperature, top_p, nullptr,
-                       out_logprob, out_entropy, out_status_word, workspace, workspace_bytes,
-                       stream);
+                       out_logprob, out_entropy, nullptr, out_status_word, workspace,
+                       workspace_bytes, stream);
+}
+
+rlk_status rlk_lmhead_logprob_fwd(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
+                                  int64_t V, const int32_t* token_ids, float temperature,
+                                  float top_p, float* out_logprob, float* out_entropy,
+                                  float* out_lse, uint32_t* out_status_word, void* workspace,
+                                  size_t workspace_bytes, rlk_stream stream) {
+  if (T > 0 && !out_lse) return RLK_ERR_INVALID_ARG;
+  return lmhead_common(hidden, w_vocab, T, H, V, token_ids, temperature, top_p, nullptr,
+                       out_logprob, out_entropy, out_lse, out_status_word, workspace,
+                       workspace_bytes, stream);
+}
+
+rlk_status rlk_lmhead_logprob_bwd(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
+                                  int64_t V, const int32_t* token_ids, float temperature,
+                                  const float* lse, const float* entropy,
+                                  const float* grad_logprob, const float* grad_entropy,
+                                  float* grad_hidden, float* grad_w, int accumulate_grad_w,
+                                  void* workspace, size_t workspace_bytes, rlk_stream stream) {
+  if (T < 0 || H < 64 || H % 64 != 0 || V < 1 || V > (int64_t(1) << 24)) return RLK_ERR_INVALID_ARG;
+  if (T > (int64_t(1) << 30) || H > (int64_t(1) << 20)) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  if (!hidden || !w_vocab || !token_ids || !lse || !entropy || !grad_hidden || !grad_w)
+    return RLK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(hidden) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(w_vocab) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(grad_hidden) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(grad_w) % 16 != 0)
+    return RLK_ERR_INVALID_ARG;
+  const size_t need = rlk::lmhead_bwd_workspace_bytes(T, V, H);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return RLK_ERR_WORKSPACE;
+  rlk::LmheadBwdArgs a;
+  a.hidden = hidden;
+  a.w_vocab = w_vocab;
+  a.T = T;
+  a.H = H;
+  a.V = V;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.lse = lse;
+  a.entropy = entropy;
+  a.grad_logprob = grad_logprob;
+  a.grad_entropy = grad_entropy;
+  a.grad_hidden = grad_hidden;
+  a.grad_w = grad_w;
+  a.accumulate_w = accumulate_grad_w != 0;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  const cudaError_t e =
+      rlk::launch_lmhead_backward(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return RLK_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
 
 rlk_status rlk_lmhead_logits_debug(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
@@ -397,8 +453,8 @@ rlk_status rlk_lmhead_logits_debug(const void* hidden, const void* w_vocab, int6
                                    size_t workspace_bytes, rlk_stream stream) {
   if (!out_logits) return RLK_ERR_INVALID_ARG;
   return lmhead_common(hidden, w_vocab, T, H, V, token_ids, temperature, 1.0f, out_logits,
-                       out_logprob, out_entropy, out_status_word, workspace, workspace_bytes,
-                       stream);
+                       out_logprob, out_entropy, nullptr, out_status_word, workspace,
+                       workspace_bytes, stream);
 }
 
 }  // extern "C"

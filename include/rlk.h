@@ -84,7 +84,8 @@ typedef enum {
 } rlk_baseline;
 
 /* Operation ids for rlk_workspace_size. */
-enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2 };
+enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2,
+       RLK_OP_LMHEAD_BWD = 3 };
 
 /* Bits OR-ed into *out_status_word by the kernels. */
 #define RLK_STATUS_BAD_TOKEN_ID 0x1u   /* a token id outside [0, V)          */
@@ -132,6 +133,7 @@ const char* rlk_status_string(rlk_status status);
  *  RLK_OP_LOGPROB_ENTROPY: T rows, V vocabulary, H unused      -> 0
  *  RLK_OP_GRPO_LOSS:       T packed tokens, V = n_seq, H unused
  *  RLK_OP_LMHEAD:          T rows, V vocabulary, H hidden size
+ *  RLK_OP_LMHEAD_BWD:      the same (rlk_lmhead_logprob_bwd)
  * Returns 0 for an unknown op or negative sizes. */
 size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H);
 
@@ -470,6 +472,58 @@ rlk_status rlk_lmhead_logprob(const void* hidden, const void* w_vocab, int64_t T
                               float top_p, float* out_logprob, float* out_entropy,
                               uint32_t* out_status_word, void* workspace,
                               size_t workspace_bytes, rlk_stream stream);
+
+/*
+ * rlk_lmhead_logprob_fwd -- rlk_lmhead_logprob that also writes each row's
+ * log-normaliser for the backward.
+ *
+ * Arguments and errors as rlk_lmhead_logprob, plus
+ *  out_lse         device float[T] (required): ln sum_v exp(z_v / T) over the
+ *                  row's fp32 logits z (NaN for a row with a status).
+ */
+rlk_status rlk_lmhead_logprob_fwd(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
+                                  int64_t V, const int32_t* token_ids, float temperature,
+                                  float top_p, float* out_logprob, float* out_entropy,
+                                  float* out_lse, uint32_t* out_status_word, void* workspace,
+                                  size_t workspace_bytes, rlk_stream stream);
+
+/*
+ * rlk_lmhead_logprob_bwd -- gradients of the fused LM-head path with respect
+ * to hidden and w_vocab.
+ *
+ * For L = sum_t grad_logprob[t] logprob_t + grad_entropy[t] H_t and
+ * z = hidden w_vocab^T (fp32 accumulations of the bf16 inputs), q_v =
+ * exp(z_v / T - lse_t):
+ *   dz[t, v] = (grad_logprob[t] ([v = y_t] - q_v) - grad_entropy[t] q_v (ln q_v + H_t)) / T,
+ *   grad_hidden = dz w_vocab,   grad_w (+)= dz^T hidden.
+ * dz is recomputed by the same tensor-core GEMM as the forward, 4096 rows at a
+ * time, rounded to bf16 and kept in the workspace (so the gradient logits of at
+ * most 4096 rows exist at once: prime-rl v0.10.0 notes, "1. Trainer
+ * Performance", the chunked loss); the two weight-side products are cuBLASLt
+ * GEMMs (bf16 inputs, fp32 accumulation and outputs).  Deterministic for a
+ * given T: grad_w sums the chunks in order.
+ *
+ * Arguments
+ *  hidden, w_vocab, T, H, V, token_ids, temperature  the forward's.
+ *  lse, entropy    device float[T] from rlk_lmhead_logprob_fwd.
+ *  grad_logprob, grad_entropy  device float[T] or NULL (zero).
+ *  grad_hidden     device float[T, H] row-major, overwritten.
+ *  grad_w          device float[V, H] row-major; overwritten, or added to when
+ *                  accumulate_grad_w is non-zero.
+ *  workspace       at least rlk_workspace_size(RLK_OP_LMHEAD_BWD, T, V, H)
+ *                  bytes (4096 x V bf16 plus 64 MB), 16-byte aligned.
+ * A row whose lse is NaN (a row the forward could not score) gives NaN in its
+ * grad_hidden row and in all of grad_w.
+ * Errors: as rlk_lmhead_logprob; RLK_ERR_INVALID_ARG for a NULL lse, entropy,
+ *  grad_hidden or grad_w; RLK_ERR_UNSUPPORTED when cuBLASLt offers no
+ *  algorithm.
+ */
+rlk_status rlk_lmhead_logprob_bwd(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
+                                  int64_t V, const int32_t* token_ids, float temperature,
+                                  const float* lse, const float* entropy,
+                                  const float* grad_logprob, const float* grad_entropy,
+                                  float* grad_hidden, float* grad_w, int accumulate_grad_w,
+                                  void* workspace, size_t workspace_bytes, rlk_stream stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

@@ -248,6 +248,31 @@ def test_lmhead_rejects(lib):
     assert call(p=0.9) == 2          # fused path is top_p = 1 only
 
 
+
+def test_lmhead_fwd_bwd_reject(lib):
+    ok = dict(T=4, H=128, V=1000, temp=0.7)
+    def fwd(lse=FAKE, **kw):
+        a = dict(ok, **kw)
+        return lib.rlk_lmhead_logprob_fwd(FAKE, FAKE, a["T"], a["H"], a["V"], FAKE, a["temp"], 1.0,
+                                          FAKE, FAKE, lse, None, FAKE, 1 << 30, None)
+    assert fwd(lse=None) == 1
+    assert fwd(H=96) == 1
+    def bwd(ws=FAKE, wsb=1 << 40, **kw):
+        a = dict(dict(ok, lse=FAKE, ent=FAKE, gh=FAKE, gw=FAKE), **kw)
+        return lib.rlk_lmhead_logprob_bwd(FAKE, FAKE, a["T"], a["H"], a["V"], FAKE, a["temp"],
+                                          a["lse"], a["ent"], None, None, a["gh"], a["gw"], 0, ws,
+                                          wsb, None)
+    for kw in (dict(H=100), dict(H=0), dict(V=0), dict(T=-1), dict(temp=0.0), dict(lse=None),
+               dict(ent=None), dict(gh=None), dict(gw=None), dict(gw=ctypes.c_void_p(0x10004))):
+        assert bwd(**kw) == 1, kw
+    assert bwd(ws=None) == 3
+    assert bwd(wsb=1024) == 3
+    assert bwd(ws=ctypes.c_void_p(0x10010)) == 3      # the workspace must be 256-byte aligned
+    assert bwd(T=0, lse=None, ent=None, gh=None, gw=None, ws=None) == 0
+    need = lib.rlk_workspace_size(3, 10000, 151936, 4096)
+    assert need >= 4096 * 151936 * 2 + (64 << 20)
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     z = torch.zeros(2, 8, dtype=torch.bfloat16)
