@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace"
                 4: "CUDA error", 5: "timeout", 6: "bad input"}
 STATUS_BAD_TOKEN_ID = 0x1
 STATUS_NONFINITE = 0x2
-OP_LOGPROB_ENTROPY, OP_GRPO_LOSS, OP_LMHEAD, OP_LMHEAD_BWD = 0, 1, 2, 3
+OP_LOGPROB_ENTROPY, OP_GRPO_LOSS, OP_LMHEAD, OP_LMHEAD_BWD, OP_LMHEAD_TOPP = 0, 1, 2, 3, 4
 AGG_TOKEN_MEAN, AGG_SEQ_MEAN_TOKEN_MEAN, AGG_PROMPT_MEAN = 0, 1, 2
 LOSS_DAPO, LOSS_IPO, LOSS_ICEPOP = 0, 1, 2
 IS_NONE, IS_TIS, IS_MIS = 0, 1, 2
@@ -422,9 +422,10 @@ def policy_loss(logp_new, logp_old, logp_rollout, logp_ref, rewards, seq_offsets
 
 def lmhead_logprob(hidden, w_vocab, token_ids, temperature, top_p=1.0, *, status_word=None,
                    workspace=None, out_lse=None):
-    """Fused LM-head top-p=1 log-probability and entropy (logits never stored).
-    ``out_lse`` (CUDA fp32 [T]) receives each row's log-normaliser for
-    ``lmhead_backward``."""
+    """Fused LM-head log-probability and entropy.  At top_p = 1 the logits never
+    reach memory; at top_p < 1 they are emitted as bf16 4096 rows at a time
+    and scored by the top-p path.  ``out_lse`` (CUDA fp32 [T], top_p = 1)
+    receives each row's log-normaliser for ``lmhead_backward``."""
     lib = load()
     _need_cuda(hidden, w_vocab, token_ids)
     if hidden.dtype != torch.bfloat16 or w_vocab.dtype != torch.bfloat16:
@@ -436,7 +437,7 @@ def lmhead_logprob(hidden, w_vocab, token_ids, temperature, top_p=1.0, *, status
     if H != H2:
         raise ValueError("hidden and w_vocab disagree on H")
     dev = hidden.device
-    need = int(lib.rlk_workspace_size(OP_LMHEAD, T, V, H))
+    need = int(lib.rlk_workspace_size(OP_LMHEAD if top_p == 1.0 else OP_LMHEAD_TOPP, T, V, H))
     if workspace is None and need > 0:
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
     lp = torch.empty(T, device=dev, dtype=torch.float32)

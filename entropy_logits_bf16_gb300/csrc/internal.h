@@ -104,6 +104,7 @@ struct LmheadArgs {
   uint32_t* status;
   void* workspace;
   float* out_lse = nullptr;   // [T] ln sum exp(z / T), for the backward
+  float top_p = 1.0f;         // < 1: the chunked path (launch_lmhead_topp)
 };
 
 struct LmheadBwdArgs {
@@ -142,6 +143,8 @@ cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t stream);
 size_t lmhead_workspace_bytes(int64_t T, int64_t V, int64_t H);
 cudaError_t launch_lmhead(const LmheadArgs& a, cudaStream_t stream);
 size_t lmhead_bwd_workspace_bytes(int64_t T, int64_t V, int64_t H);
+size_t lmhead_topp_workspace_bytes(int64_t T, int64_t V, int64_t H);
+cudaError_t launch_lmhead_topp(const LmheadArgs& a, cudaStream_t stream);
 // Returns cudaErrorNotSupported when cuBLASLt finds no algorithm.
 cudaError_t launch_lmhead_backward(const LmheadBwdArgs& a, cudaStream_t stream);
 // Same, also writing the fp32 logits [T, V] to debug_logits (validation aid).

@@ -205,8 +205,8 @@ struct LmParams {
   float* zy;             // [T] the selected token's logit
   float* debug_logits;   // [T][V] when non-null (validation aid)
   uint32_t* status;
-  // gradient mode (grad != 0): the epilogue writes dL/dz (bf16) instead of
-  // folding row states
+  // gradient mode (grad == 1): the epilogue writes dL/dz (bf16) instead of
+  // folding row states; emit mode (grad == 2): it writes the logits (bf16)
   int grad;
   const float* lse;      // [T] ln sum exp(z / T) from the forward
   const float* ent;      // [T] entropy from the forward
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // = z c - lse log2(e), A = g_lp / T, B = (g_lp + g_H H) / T,
       // C = g_H ln2 / T
       float gnE = 0.f, gA = 0.f, gB = 0.f, gC = 0.f;
-      if (p.grad && row < p.T) {
+      if (p.grad == 1 && row < p.T) {
         const float glp = p.glp ? p.glp[row] : 0.f, gh = p.gh ? p.gh[row] : 0.f;
         gnE = -__fmul_rn(p.lse[row], kLog2e);
         gA = __fmul_rn(glp, p.inv_t);
@@ -373,13 +373,15 @@ __global__ void __launch_bounds__(THREADS, 1)
               uint32_t o[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                float g2[2];
+                float g2[2] = {v[2 * j], v[2 * j + 1]};
+                if (p.grad == 1) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const float t = __fmaf_rn(v[2 * j + e], p.c, gnE);
-                  const float qv = ex2(t);
-                  g2[e] = __fmul_rn(qv, __fmaf_rn(-gC, t, -gB));
-                  if (col0 + 2 * j + e == y) g2[e] = __fadd_rn(g2[e], gA);
+                  for (int e = 0; e < 2; ++e) {
+                    const float t = __fmaf_rn(v[2 * j + e], p.c, gnE);
+                    const float qv = ex2(t);
+                    g2[e] = __fmul_rn(qv, __fmaf_rn(-gC, t, -gB));
+                    if (col0 + 2 * j + e == y) g2[e] = __fadd_rn(g2[e], gA);
+                  }
                 }
                 const __nv_bfloat162 h2 = __floats2bfloat162_rn(g2[0], g2[1]);
                 o[j] = *reinterpret_cast<const uint32_t*>(&h2);
@@ -672,6 +674,66 @@ cudaError_t launch_lmhead_backward(const LmheadBwdArgs& a, cudaStream_t stream) 
     const float beta = (r0 > 0 || a.accumulate_w) ? 1.0f : 0.0f;
     e = lt_gemm(CUBLAS_OP_N, CUBLAS_OP_T, a.H, a.V, rows, hid + r0 * a.H, a.H, rows, a.H, dz, a.V,
                 rows, ldz, a.grad_w, a.H, beta, lt_ws, kLtWorkspace, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+size_t lmhead_topp_workspace_bytes(int64_t T, int64_t V, int64_t H) {
+  (void)H;
+  return dz_bytes(T, V);
+}
+
+// top_p < 1: the nucleus needs every logit of a row, so each chunk of at most
+// kBwdRows rows is emitted once as bf16 logits (the same GEMM, emit epilogue)
+// into the workspace and scored there by the top-p logits path.
+cudaError_t launch_lmhead_topp(const LmheadArgs& a, cudaStream_t stream) {
+  static std::atomic<int> attr_done{0};
+  if (!attr_done.load()) {
+    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done.store(1);
+  }
+  CUtensorMap mb;
+  if (!make_map(&mb, a.w_vocab, (uint64_t)a.V, (uint64_t)a.H, BN)) return cudaErrorInvalidValue;
+  uint16_t* zbuf = static_cast<uint16_t*>(a.workspace);
+  const int64_t ldz = dz_ld(a.V);
+  const uint16_t* hid = static_cast<const uint16_t*>(a.hidden);
+  for (int64_t r0 = 0; r0 < a.T; r0 += kBwdRows) {
+    const int64_t rows = a.T - r0 < kBwdRows ? a.T - r0 : kBwdRows;
+    CUtensorMap ma;
+    if (!make_map(&ma, hid + r0 * a.H, (uint64_t)rows, (uint64_t)a.H, BM))
+      return cudaErrorInvalidValue;
+    LmParams p{};
+    p.T = rows;
+    p.V = a.V;
+    p.n_mt = (int)((rows + BM - 1) / BM);
+    p.n_nt = (int)((a.V + BN - 1) / BN);
+    p.n_units = p.n_mt * NSLICE;
+    p.k_steps = (int)(a.H / BK);
+    p.ids = a.ids + r0;
+    p.c = (float)(1.4426950408889634 / (double)a.temperature);
+    p.grad = 2;
+    p.dz = zbuf;
+    p.ldz = ldz;
+    const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
+    lmhead_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    LpeArgs l{};
+    l.logits = zbuf;
+    l.dtype = 0;
+    l.T = rows;
+    l.V = a.V;
+    l.ld = ldz;
+    l.ids = a.ids + r0;
+    l.temperature = a.temperature;
+    l.top_p = a.top_p;
+    l.out_logprob = a.out_logprob + r0;
+    l.out_entropy = a.out_entropy + r0;
+    l.status = a.status;
+    e = launch_logprob_entropy(l, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -1032,10 +1032,22 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
           sm.merged_n = 0u;
         }
         __syncthreads();
+        // The sketch pass lists the candidate groups and reloads only those:
+        // worth it while they are sparse.  When a quarter of the groups or
+        // more are candidates (flat rows, wide nuclei) the streaming window
+        // pass is about twice as fast.  Both build the same integer counts.
+        bool use_sketch = (a.V + 8 * NT - 1) / (8 * NT) <= SK_ROUNDS;
+        if (use_sketch) {
+          const int64_t ngroups = (a.V + 7) / 8;
+          uint32_t cc[4] = {0u, 0u, 0u, 0u};
+          for (int r2 = 0; (int64_t)r2 * NT + tid < ngroups; ++r2)
+            cc[0] += bf16_val(sm.gmax[r2][tid]) >= zlo ? 1u : 0u;
+          block_sum_u32(cc, sm, tid);
+          use_sketch = (int64_t)cc[0] * 4 < ngroups;
+        }
         uint32_t cnt2[4] = {0u, 0u, 0u, 0u};
-        cnt2[0] = (a.V + 8 * NT - 1) / (8 * NT) <= SK_ROUNDS
-                      ? sketch_pass(row, tid, zlo, m, c, inv_t, ck_m, key_y, y, sm)
-                      : window_pass(row, tid, zlo, m, c, inv_t, ck_m, key_y, y, sm);
+        cnt2[0] = use_sketch ? sketch_pass(row, tid, zlo, m, c, inv_t, ck_m, key_y, y, sm)
+                             : window_pass(row, tid, zlo, m, c, inv_t, ck_m, key_y, y, sm);
         block_sum_u32(cnt2, sm, tid);  // also the barrier after the histogram
         int dstar;
         const bool found = scan_bins(tid, dmax, d_merged, ck_m, m, c, inv_t, target, sm, dstar);

@@ -59,6 +59,7 @@ size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H) {
     case RLK_OP_GRPO_LOSS: return rlk::loss_workspace_bytes(V);
     case RLK_OP_LMHEAD: return rlk::lmhead_workspace_bytes(T, V, H);
     case RLK_OP_LMHEAD_BWD: return rlk::lmhead_bwd_workspace_bytes(T, V, H);
+    case RLK_OP_LMHEAD_TOPP: return rlk::lmhead_topp_workspace_bytes(T, V, H);
   }
   return 0;
 }
@@ -357,8 +358,10 @@ static rlk_status lmhead_common(const void* hidden, const void* w_vocab, int64_t
   if (reinterpret_cast<uintptr_t>(hidden) % 16 != 0 ||
       reinterpret_cast<uintptr_t>(w_vocab) % 16 != 0)
     return RLK_ERR_INVALID_ARG;
-  if (top_p != 1.0f) return RLK_ERR_UNSUPPORTED;
-  const size_t need = rlk::lmhead_workspace_bytes(T, V, H);
+  const bool topp = top_p != 1.0f;
+  if (topp && (out_logits || out_lse)) return RLK_ERR_UNSUPPORTED;   // top_p = 1 only
+  const size_t need = topp ? rlk::lmhead_topp_workspace_bytes(T, V, H)
+                           : rlk::lmhead_workspace_bytes(T, V, H);
   if (need > 0 && (!workspace || workspace_bytes < need ||
                    reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
     return RLK_ERR_WORKSPACE;
@@ -376,8 +379,10 @@ static rlk_status lmhead_common(const void* hidden, const void* w_vocab, int64_t
   a.status = out_status_word;
   a.workspace = workspace;
   a.out_lse = out_lse;
+  a.top_p = top_p;
   const cudaError_t e =
-      rlk::launch_lmhead_impl(a, out_logits, reinterpret_cast<cudaStream_t>(stream));
+      topp ? rlk::launch_lmhead_topp(a, reinterpret_cast<cudaStream_t>(stream))
+           : rlk::launch_lmhead_impl(a, out_logits, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return RLK_ERR_UNSUPPORTED;
   return e == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
