@@ -394,20 +394,23 @@ def run_logits(args, ws, rank, dev, barrier):
     return line
 
 
-def run_lmhead(args, ws, rank, dev, barrier):
+def run_lmhead(args, ws, rank, dev, barrier, top_p=1.0):
     """--op lmhead: the fused LM-head (tcgen05 GEMM + online log-sum-exp
-    epilogue) on hidden [16384, 4096] and W [151936, 4096] bf16, top_p 1."""
+    epilogue) on hidden [16384, 4096] and W [151936, 4096] bf16, top_p 1.
+    --op lmhead_topp: the same at top_p 0.95 (bf16 logits emitted 4096 rows at
+    a time and scored by the top-p path)."""
     import entropy_logits_bf16_gb300 as rlk
     import workloads
     stream = torch.cuda.current_stream(dev)
     hidden, w, ids = workloads.lmhead_inputs(LM_T, LM_H, VOCAB, seed=4 + rank, device=dev)
     ids = ids.to(dev).to(torch.int32)
-    wsb = rlk.workspace_size(2, LM_T, VOCAB, LM_H)
+    wsb = rlk.workspace_size(rlk.OP_LMHEAD if top_p == 1.0 else rlk.OP_LMHEAD_TOPP, LM_T, VOCAB,
+                             LM_H)
     wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
     lp = torch.empty(LM_T, device=dev)
 
     def lm():
-        rlk.lmhead_logprob(hidden, w, ids, TEMPERATURE, workspace=wsp)
+        rlk.lmhead_logprob(hidden, w, ids, TEMPERATURE, top_p, workspace=wsp)
 
     elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [lm], barrier)
     host_h = torch.empty(hidden.shape, dtype=hidden.dtype, pin_memory=True).copy_(hidden)
@@ -418,7 +421,7 @@ def run_lmhead(args, ws, rank, dev, barrier):
     def e2e_step():
         dh.copy_(host_h, non_blocking=True)
         di.copy_(host_i, non_blocking=True)
-        a, b = rlk.lmhead_logprob(dh, w, di, TEMPERATURE, workspace=wsp)
+        a, b = rlk.lmhead_logprob(dh, w, di, TEMPERATURE, top_p, workspace=wsp)
         out_h[:LM_T].copy_(a, non_blocking=True)
         out_h[LM_T:].copy_(b, non_blocking=True)
 
@@ -441,19 +444,24 @@ def run_lmhead(args, ws, rank, dev, barrier):
     # the kernel runs back to back for seconds: the sustained (power-capped) peak
     peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0))
     line = {
-        "metric": LM_METRIC, "value": whole_job_rate(LM_T, args.steps, ws, elapsed_ms), "unit": "tokens/s",
+        "metric": LM_METRIC if top_p == 1.0 else LM_METRIC.replace("(top_p 1)", f"(top_p {top_p})"),
+        "value": whole_job_rate(LM_T, args.steps, ws, elapsed_ms), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"fused LM-head: hidden [{LM_T}, {LM_H}] bf16 N(0,1), W_vocab "
                                f"[{VOCAB}, {LM_H}] bf16 N(0, 0.02^2), temperature {TEMPERATURE}, "
-                               f"top_p 1, uniform ids; logits never stored",
+                               f"top_p {top_p}, uniform ids; "
+                               + ("logits never stored" if top_p == 1.0 else
+                                  "bf16 logits of 4096 rows at a time in the workspace"),
                    "global_batch": LM_T * ws,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "W (1.24 GB) larger than L2; no flush between steps"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
-                     "kernel": "lmhead_kernel + lmhead_combine_kernel (one rlk_lmhead_logprob call)",
+                     "kernel": ("lmhead_kernel + lmhead_combine_kernel" if top_p == 1.0 else
+                                "lmhead_kernel (emit) + the top-p logits path per chunk")
+                               + " (one rlk_lmhead_logprob call)",
                      "flops_per_launch": flops, "launch_ms": part_ms[0]},
         "e2e": {"value": LM_T * ws / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(hidden.numel() * 2 + ids.numel() * 4),
@@ -471,7 +479,7 @@ def run_lmhead(args, ws, rank, dev, barrier):
         threads = oracle.default_threads()
         oracle.build()
         t0 = time.perf_counter()
-        oracle.lmhead_rows(hb, wb, np.arange(rows), ids.cpu().numpy()[sel], TEMPERATURE,
+        oracle.lmhead_rows(hb, wb, np.arange(rows), ids.cpu().numpy()[sel], TEMPERATURE, top_p,
                            threads=threads)
         dt = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": rows / dt, "unit": "tokens/s", "cores": threads,
@@ -675,7 +683,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "lmhead_backward", "support",
-                                                       "support_backward", "backward"],
+                                                       "support_backward", "backward",
+                                                       "lmhead_topp"],
                     help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused "
                          "LM-head; support: the supplied-support scorer; support_backward: its "
                          "gradient; backward: the dense top-p gradient; lmhead_backward: the "
@@ -705,7 +714,8 @@ def main():
 
     run = {"logits": run_logits, "lmhead": run_lmhead, "support": run_support,
            "support_backward": lambda *a: run_support(*a, backward=True),
-           "backward": run_backward, "lmhead_backward": run_lmhead_backward}[args.op]
+           "backward": run_backward, "lmhead_backward": run_lmhead_backward,
+           "lmhead_topp": lambda *a: run_lmhead(*a, top_p=TOP_P)}[args.op]
     line = run(args, ws, rank, dev, barrier)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -85,7 +85,7 @@ typedef enum {
 
 /* Operation ids for rlk_workspace_size. */
 enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2,
-       RLK_OP_LMHEAD_BWD = 3 };
+       RLK_OP_LMHEAD_BWD = 3, RLK_OP_LMHEAD_TOPP = 4 };
 
 /* Bits OR-ed into *out_status_word by the kernels. */
 #define RLK_STATUS_BAD_TOKEN_ID 0x1u   /* a token id outside [0, V)          */
@@ -134,6 +134,7 @@ const char* rlk_status_string(rlk_status status);
  *  RLK_OP_GRPO_LOSS:       T packed tokens, V = n_seq, H unused
  *  RLK_OP_LMHEAD:          T rows, V vocabulary, H hidden size
  *  RLK_OP_LMHEAD_BWD:      the same (rlk_lmhead_logprob_bwd)
+ *  RLK_OP_LMHEAD_TOPP:     the same (rlk_lmhead_logprob with top_p < 1)
  * Returns 0 for an unknown op or negative sizes. */
 size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H);
 
@@ -448,24 +449,30 @@ rlk_status rlk_grpo_loss_noalloc(const float* logp_new, const float* logp_old,
                                  float* out_dloss_dlogp_new, float* out_stats, rlk_stream stream);
 
 /*
- * rlk_lmhead_logprob -- the logits path at top_p = 1 fused with the LM-head
- * GEMM: logits = hidden[T, H] * w_vocab[V, H]^T are produced tile by tile in
- * tensor-core accumulators and folded into the online max / sum / entropy
- * state; they never reach memory (prime-rl v0.10.0 notes, "1. Trainer
+ * rlk_lmhead_logprob -- the logits path fused with the LM-head GEMM.
+ *
+ * top_p = 1: logits = hidden[T, H] * w_vocab[V, H]^T are produced tile by
+ * tile in tensor-core accumulators and folded into the online max / sum /
+ * entropy state; they never reach memory (prime-rl v0.10.0 notes, "1. Trainer
  * Performance": chunked loss; RL-Kernel notes: deterministic GEMM with a
  * fixed reduction order).  Logits are the fp32 accumulations, not rounded
  * to bf16.
+ * top_p < 1: the nucleus needs all of a row's logits at once, so the same GEMM
+ * emits the logits of at most 4096 rows at a time, rounded to bf16 (the
+ * scorer's input type, as an unfused LM head would emit them), into the
+ * workspace, and rlk_logprob_entropy scores each chunk there.
  *
  * Arguments
  *  hidden          device bf16 [T, H] row-major, 16-byte aligned.
  *  w_vocab         device bf16 [V, H] row-major, 16-byte aligned.
  *  T, H, V         T >= 0, H a positive multiple of 64, V >= 1.
  *  token_ids       device int32[T].
- *  temperature     finite, > 0.   top_p must be 1 (else RLK_ERR_UNSUPPORTED).
+ *  temperature     finite, > 0.   top_p: 0 < top_p <= 1.
  *  out_logprob, out_entropy  device float[T].
  *  out_status_word device uint32[1] or NULL.
- *  workspace       at least rlk_workspace_size(RLK_OP_LMHEAD, T, V, H) bytes, 16-byte
- *                  aligned; contents on entry do not matter.
+ *  workspace       at least rlk_workspace_size(RLK_OP_LMHEAD, T, V, H) bytes
+ *                  (RLK_OP_LMHEAD_TOPP when top_p < 1), 16-byte aligned;
+ *                  contents on entry do not matter.
  */
 rlk_status rlk_lmhead_logprob(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
                               int64_t V, const int32_t* token_ids, float temperature,
@@ -480,6 +487,8 @@ rlk_status rlk_lmhead_logprob(const void* hidden, const void* w_vocab, int64_t T
  * Arguments and errors as rlk_lmhead_logprob, plus
  *  out_lse         device float[T] (required): ln sum_v exp(z_v / T) over the
  *                  row's fp32 logits z (NaN for a row with a status).
+ * top_p must be 1 (else RLK_ERR_UNSUPPORTED): the backward is the top_p = 1
+ * path's.
  */
 rlk_status rlk_lmhead_logprob_fwd(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
                                   int64_t V, const int32_t* token_ids, float temperature,

@@ -245,7 +245,8 @@ def test_lmhead_rejects(lib):
     assert call(temp=0.0) == 1
     assert call(p=1.5) == 1
     assert call(V=0) == 1
-    assert call(p=0.9) == 2          # fused path is top_p = 1 only
+    assert call(p=0.9) == 3          # top_p < 1 needs the chunk workspace
+    assert lib.rlk_workspace_size(4, 100, 151936, 4096) >= 100 * 151936 * 2
 
 
 
@@ -257,6 +258,8 @@ def test_lmhead_fwd_bwd_reject(lib):
                                           FAKE, FAKE, lse, None, FAKE, 1 << 30, None)
     assert fwd(lse=None) == 1
     assert fwd(H=96) == 1
+    assert lib.rlk_lmhead_logprob_fwd(FAKE, FAKE, 4, 128, 1000, FAKE, 0.7, 0.9, FAKE, FAKE, FAKE,
+                                      None, FAKE, 1 << 40, None) == 2   # the lse is top_p = 1 only
     def bwd(ws=FAKE, wsb=1 << 40, **kw):
         a = dict(dict(ok, lse=FAKE, ent=FAKE, gh=FAKE, gw=FAKE), **kw)
         return lib.rlk_lmhead_logprob_bwd(FAKE, FAKE, a["T"], a["H"], a["V"], FAKE, a["temp"],

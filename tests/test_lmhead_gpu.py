@@ -75,3 +75,28 @@ def test_lmhead_bad_ids(cuda_lib):
     lp = lp.cpu().numpy()
     assert np.isnan(lp[3]) and np.isnan(lp[5]) and np.isfinite(lp[0])
     assert int(st.item()) & cuda_lib.STATUS_BAD_TOKEN_ID
+
+
+@pytest.mark.parametrize("T,H,V,p", [(300, 256, 20000, 0.9), (4500, 128, 8192, 0.95),
+                                     (130, 4096, 151936, 0.95)])
+def test_lmhead_top_p_chunked(cuda_lib, oracle, T, H, V, p):
+    """top_p < 1: the GEMM emits bf16 logits chunk by chunk and the top-p path
+    scores them.  Against the oracle on the GEMM's own logits rounded to bf16
+    (the GEMM core is checked against a library product above), and bit for
+    bit against rlk_logprob_entropy on those logits (V % 8 == 0: same layout).
+    The second shape spans two 4096-row chunks."""
+    hidden, w, ids = workloads.lmhead_inputs(T, H, V, seed=12, device="cuda")
+    w = (w.float() * (8.0 if H <= 256 else 1.5)).to(torch.bfloat16)   # peaked enough for a nucleus
+    lp, ent = cuda_lib.lmhead_logprob(hidden, w, ids, 0.7, p)
+    logits, _, _ = cuda_lib.lmhead_logits_debug(hidden, w, ids, 0.7)
+    zb = logits.to(torch.bfloat16)
+    dlp, dent = cuda_lib.logprob_entropy(zb, ids, 0.7, p)
+    torch.cuda.synchronize()
+    assert torch.equal(lp, dlp) and torch.equal(ent, dent)
+    olp, oent, ok, gap = oracle.logprob_entropy(workloads.bf16_bits(zb), ids.cpu().numpy(), 0.7, p)
+    sure = gap > 1e-6
+    lp_, ent_ = lp.cpu().numpy().astype(np.float64), ent.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isneginf(lp_[sure]), np.isneginf(olp[sure]))
+    fin = sure & ~np.isneginf(olp)
+    assert np.all(np.abs(lp_[fin] - olp[fin]) <= 2e-4 + 2e-7 * np.abs(olp[fin]))
+    assert np.all(np.abs(ent_[sure] - oent[sure]) <= 2e-4)
