@@ -546,6 +546,44 @@ def run_lmhead_backward(args, ws, rank, dev, barrier):
     }
 
 
+CAN_METRIC = ("tokens/s for top_p=1 logprob+entropy over the canonical vocabulary partition "
+              "(virtual TP 8, padded vocabulary 152576) at V=151936 bf16")
+
+
+def run_canonical(args, ws, rank, dev, barrier):
+    """--op canonical: rlk_logprob_entropy_canonical on the benchmark rows
+    (eight virtual shards' partials, then the fixed-order combine)."""
+    import entropy_logits_bf16_gb300 as rlk
+    stream = torch.cuda.current_stream(dev)
+    z, ids = make_workload(dev, seed=rank_seed(rank))
+
+    def call():
+        rlk.logprob_entropy_canonical(z, ids, TEMPERATURE)
+
+    elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [call], barrier)
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    alg = T_ROWS * (VOCAB * 2 + 4 + 8) + 2 * T_ROWS * rlk.CANONICAL_TP * 32   # logits, ids, outputs, partials
+    achieved = alg / (part_ms[0] / 1e3) / 1e9
+    return {
+        "metric": CAN_METRIC, "value": whole_job_rate(T_ROWS, args.steps, ws, elapsed_ms),
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD.replace("top_p 0.95", "top_p 1"), "T": T_ROWS, "V": VOCAB,
+                   "virtual_tp": rlk.CANONICAL_TP, "padded_vocab": rlk.CANONICAL_VOCAB,
+                   "global_batch": T_ROWS * ws,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peak_kind,
+                     "kernel": "shard_partial_kernel + shard_combine_kernel",
+                     "algorithmic_bytes_per_launch": alg, "launch_ms": part_ms[0]},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+
+
 SUP_METRIC = ("tokens/s for supplied-support logprob+entropy (the top-p retained set given as "
               "CSR) at V=151936 bf16")
 
@@ -684,7 +722,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "lmhead_backward", "support",
                                                        "support_backward", "backward",
-                                                       "lmhead_topp"],
+                                                       "lmhead_topp", "canonical"],
                     help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused "
                          "LM-head; support: the supplied-support scorer; support_backward: its "
                          "gradient; backward: the dense top-p gradient; lmhead_backward: the "
@@ -715,7 +753,8 @@ def main():
     run = {"logits": run_logits, "lmhead": run_lmhead, "support": run_support,
            "support_backward": lambda *a: run_support(*a, backward=True),
            "backward": run_backward, "lmhead_backward": run_lmhead_backward,
-           "lmhead_topp": lambda *a: run_lmhead(*a, top_p=TOP_P)}[args.op]
+           "lmhead_topp": lambda *a: run_lmhead(*a, top_p=TOP_P),
+           "canonical": run_canonical}[args.op]
     line = run(args, ws, rank, dev, barrier)
     if line is not None:
         print(json.dumps(line), flush=True)

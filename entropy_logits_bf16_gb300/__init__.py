@@ -23,6 +23,9 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace"
 STATUS_BAD_TOKEN_ID = 0x1
 STATUS_NONFINITE = 0x2
 OP_LOGPROB_ENTROPY, OP_GRPO_LOSS, OP_LMHEAD, OP_LMHEAD_BWD, OP_LMHEAD_TOPP = 0, 1, 2, 3, 4
+OP_CANONICAL = 5
+CANONICAL_TP, CANONICAL_VOCAB = 8, 152576
+SHARD_PARTIAL_WORDS = 8   # rlk_shard_partial: 32 bytes per (shard, row)
 AGG_TOKEN_MEAN, AGG_SEQ_MEAN_TOKEN_MEAN, AGG_PROMPT_MEAN = 0, 1, 2
 LOSS_DAPO, LOSS_IPO, LOSS_ICEPOP = 0, 1, 2
 IS_NONE, IS_TIS, IS_MIS = 0, 1, 2
@@ -45,7 +48,8 @@ EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logpro
            "rlk_logprob_entropy_fwd", "rlk_logprob_entropy_bwd",
            "rlk_logprob_entropy_support", "rlk_logprob_entropy_support_backward",
            "rlk_grpo_loss", "rlk_policy_loss", "rlk_lmhead_logprob", "rlk_lmhead_logprob_fwd",
-           "rlk_lmhead_logprob_bwd",
+           "rlk_lmhead_logprob_bwd", "rlk_shard_partials", "rlk_shard_combine",
+           "rlk_logprob_entropy_canonical",
            "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
 DEBUG_EXPORTS = ("rlk_lmhead_logits_debug",)
@@ -110,6 +114,14 @@ def load(path: str | None = None):
         lib.rlk_lmhead_logprob.argtypes = [vp, vp, i64, i64, i64, vp, f32, f32, vp, vp, vp, vp,
                                            sz, vp]
         lib.rlk_lmhead_logprob.restype = ctypes.c_int
+        lib.rlk_shard_partials.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, i64, i32, vp, f32,
+                                           vp, vp]
+        lib.rlk_shard_partials.restype = ctypes.c_int
+        lib.rlk_shard_combine.argtypes = [vp, i32, i64, i64, i64, vp, f32, vp, vp, vp, vp]
+        lib.rlk_shard_combine.restype = ctypes.c_int
+        lib.rlk_logprob_entropy_canonical.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, i32,
+                                                      i64, vp, vp, vp, vp, sz, vp]
+        lib.rlk_logprob_entropy_canonical.restype = ctypes.c_int
         lib.rlk_lmhead_logprob_fwd.argtypes = [vp, vp, i64, i64, i64, vp, f32, f32, vp, vp, vp,
                                                vp, vp, sz, vp]
         lib.rlk_lmhead_logprob_fwd.restype = ctypes.c_int
@@ -519,3 +531,97 @@ def lmhead_logits_debug(hidden, w_vocab, token_ids, temperature):
                                        None, _ptr(ws), ws.numel(), _stream(dev))
     _check("rlk_lmhead_logits_debug", code)
     return logits, lp, ent
+
+
+# ------------------------------------------------------------ canonical partition
+def canonical_plan(tp_size: int, tp_rank: int, n_virtual: int = CANONICAL_TP,
+                   padded_vocab: int = CANONICAL_VOCAB):
+    """The virtual shards a physical tensor-parallel rank holds: (first shard,
+    number of shards, first global column, shard width).  Rank k of tp_size
+    holds the adjacent shards [k n, (k + 1) n), n = n_virtual / tp_size."""
+    if n_virtual % tp_size != 0 or not 0 <= tp_rank < tp_size:
+        raise ValueError("tp_size must divide the virtual degree; 0 <= tp_rank < tp_size")
+    if padded_vocab % n_virtual != 0:
+        raise ValueError("the padded vocabulary must be a multiple of the virtual degree")
+    n = n_virtual // tp_size
+    width = padded_vocab // n_virtual
+    return tp_rank * n, n, tp_rank * n * width, width
+
+
+def shard_partials(logits, token_ids, temperature, V, first_col, shard_width, n_shards):
+    """rlk_shard_partials: [n_shards, T, 8] fp32 partials of the shards whose
+    columns ``logits`` ([T, cols], unit stride along the vocabulary) holds."""
+    lib = load()
+    _need_cuda(logits, token_ids)
+    dt = _logits_dtype(logits)
+    T = logits.shape[0]
+    ld = logits.stride(0) if T > 1 else logits.shape[1]
+    out = torch.empty((n_shards, T, SHARD_PARTIAL_WORDS), device=logits.device,
+                      dtype=torch.float32)
+    code = lib.rlk_shard_partials(_ptr(logits), dt, T, int(V), ld, int(first_col),
+                                  int(shard_width), int(n_shards), _ptr(token_ids),
+                                  float(temperature), _ptr(out), _stream(logits.device))
+    _check("rlk_shard_partials", code)
+    return out
+
+
+def shard_combine(partials, token_ids, temperature, V, shard_width, *, status_word=None):
+    """rlk_shard_combine: (logprob, entropy) from all shards' partials
+    ([n_shards, T, 8], canonical order)."""
+    lib = load()
+    _need_cuda(partials, token_ids)
+    if partials.dtype != torch.float32 or not partials.is_contiguous() or partials.dim() != 3:
+        raise ValueError("partials must be contiguous fp32 [n_shards, T, 8]")
+    n_shards, T = partials.shape[0], partials.shape[1]
+    lp = torch.empty(T, device=partials.device, dtype=torch.float32)
+    ent = torch.empty(T, device=partials.device, dtype=torch.float32)
+    code = lib.rlk_shard_combine(_ptr(partials), n_shards, T, int(V), int(shard_width),
+                                 _ptr(token_ids), float(temperature), _ptr(lp), _ptr(ent),
+                                 _ptr(status_word), _stream(partials.device))
+    _check("rlk_shard_combine", code)
+    return lp, ent
+
+
+def logprob_entropy_canonical(logits, token_ids, temperature, n_virtual=CANONICAL_TP,
+                              padded_vocab=CANONICAL_VOCAB, *, status_word=None):
+    """The canonical partition on one device (top_p = 1)."""
+    lib = load()
+    _need_cuda(logits, token_ids)
+    dt = _logits_dtype(logits)
+    T, V = logits.shape
+    ld = logits.stride(0) if T > 1 else V
+    ws = torch.empty(max(int(lib.rlk_workspace_size(OP_CANONICAL, T, n_virtual, 0)), 16),
+                     device=logits.device, dtype=torch.uint8)
+    lp = torch.empty(T, device=logits.device, dtype=torch.float32)
+    ent = torch.empty(T, device=logits.device, dtype=torch.float32)
+    code = lib.rlk_logprob_entropy_canonical(_ptr(logits), dt, T, V, ld, _ptr(token_ids),
+                                             float(temperature), int(n_virtual), int(padded_vocab),
+                                             _ptr(lp), _ptr(ent), _ptr(status_word), _ptr(ws),
+                                             ws.numel(), _stream(logits.device))
+    _check("rlk_logprob_entropy_canonical", code)
+    return lp, ent
+
+
+def gather_shard_partials(local_partials, group=None):
+    """All ranks' partials ([n_local, T, 8] each) gathered in rank order, which
+    is canonical shard order: [n_local * world, T, 8].  The one exchange of the
+    vocabulary-parallel path."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    parts = [torch.empty_like(local_partials) for _ in range(world)]
+    dist.all_gather(parts, local_partials.contiguous(), group=group)
+    return torch.cat(parts, 0)
+
+
+def vocab_parallel_logprob_entropy(local_logits, token_ids, temperature, V, group=None,
+                                   n_virtual=CANONICAL_TP, padded_vocab=CANONICAL_VOCAB):
+    """Tensor-parallel top_p = 1 log-probability and entropy: this rank's
+    canonical shards -> partials -> gather in rank order -> combine.  The result
+    is bitwise the same for every tensor-parallel degree."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    rank = dist.get_rank(group) if dist.is_initialized() else 0
+    _, n, first_col, width = canonical_plan(world, rank, n_virtual, padded_vocab)
+    part = shard_partials(local_logits, token_ids, temperature, V, first_col, width, n)
+    allp = gather_shard_partials(part, group) if world > 1 else part
+    return shard_combine(allp, token_ids, temperature, V, width)

@@ -124,6 +124,33 @@ struct LmheadBwdArgs {
   size_t workspace_bytes;
 };
 
+// Canonical vocabulary partition (vocab_parallel.cu).  Shard s of the
+// partition covers global columns [s W, (s + 1) W) clipped to V; a call
+// handles n_shards adjacent shards starting at global column first_col, whose
+// columns are logits[:, 0 ...] (row stride ld).  partials: 32 bytes per
+// (shard, row), [n_shards][T].
+struct ShardArgs {
+  const void* logits;
+  int dtype;
+  int64_t T, V, ld, first_col, shard_width;
+  int n_shards;
+  const int32_t* ids;
+  float temperature;
+  void* partials;
+};
+struct ShardCombineArgs {
+  const void* partials;   // [n_shards][T], canonical order, shard 0 first
+  int n_shards;
+  int64_t T, V, shard_width;
+  const int32_t* ids;
+  float temperature;
+  float* out_logprob;
+  float* out_entropy;
+  uint32_t* status;
+};
+cudaError_t launch_shard_partials(const ShardArgs& a, cudaStream_t stream);
+cudaError_t launch_shard_combine(const ShardCombineArgs& a, cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

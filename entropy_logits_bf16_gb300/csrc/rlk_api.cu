@@ -60,6 +60,8 @@ size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H) {
     case RLK_OP_LMHEAD: return rlk::lmhead_workspace_bytes(T, V, H);
     case RLK_OP_LMHEAD_BWD: return rlk::lmhead_bwd_workspace_bytes(T, V, H);
     case RLK_OP_LMHEAD_TOPP: return rlk::lmhead_topp_workspace_bytes(T, V, H);
+    case RLK_OP_CANONICAL:
+      return V < 1 ? 0 : (size_t)V * (size_t)T * sizeof(rlk_shard_partial);
   }
   return 0;
 }
@@ -343,6 +345,90 @@ rlk_status rlk_policy_loss(const float* logp_new, const float* logp_old,
   return rlk::launch_grpo_loss(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
+}
+
+static_assert(sizeof(rlk_shard_partial) == 32, "rlk_shard_partial is 32 bytes");
+
+rlk_status rlk_shard_partials(const void* logits, rlk_dtype dtype, int64_t T, int64_t V, int64_t ld,
+                              int64_t first_col, int64_t shard_width, int32_t n_shards,
+                              const int32_t* token_ids, float temperature,
+                              rlk_shard_partial* out_partials, rlk_stream stream) {
+  if (dtype != RLK_BF16 && dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || shard_width < 1 || n_shards < 1)
+    return RLK_ERR_INVALID_ARG;
+  if (first_col < 0 || first_col % shard_width != 0) return RLK_ERR_INVALID_ARG;
+  const int64_t span = shard_width * (int64_t)n_shards;
+  int64_t cols = V - first_col < span ? V - first_col : span;   // shards of padding only: none
+  if (cols < 0) cols = 0;
+  if (ld < cols) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  if (!logits || !token_ids || !out_partials) return RLK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) % (dtype == RLK_BF16 ? 2u : 4u) != 0 ||
+      reinterpret_cast<uintptr_t>(out_partials) % 16u != 0)
+    return RLK_ERR_INVALID_ARG;
+  rlk::ShardArgs a{};
+  a.logits = logits;
+  a.dtype = dtype == RLK_BF16 ? 0 : 1;
+  a.T = T;
+  a.V = V;
+  a.ld = ld;
+  a.first_col = first_col;
+  a.shard_width = shard_width;
+  a.n_shards = n_shards;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.partials = out_partials;
+  return rlk::launch_shard_partials(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_shard_combine(const rlk_shard_partial* partials, int32_t n_shards, int64_t T,
+                             int64_t V, int64_t shard_width, const int32_t* token_ids,
+                             float temperature, float* out_logprob, float* out_entropy,
+                             uint32_t* out_status_word, rlk_stream stream) {
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || shard_width < 1 || n_shards < 1)
+    return RLK_ERR_INVALID_ARG;
+  if (shard_width * (int64_t)n_shards < V) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  if (!partials || !token_ids || !out_logprob || !out_entropy) return RLK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(partials) % 16u != 0) return RLK_ERR_INVALID_ARG;
+  rlk::ShardCombineArgs a{};
+  a.partials = partials;
+  a.n_shards = n_shards;
+  a.T = T;
+  a.V = V;
+  a.shard_width = shard_width;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.out_logprob = out_logprob;
+  a.out_entropy = out_entropy;
+  a.status = out_status_word;
+  return rlk::launch_shard_combine(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_logprob_entropy_canonical(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                         int64_t ld, const int32_t* token_ids, float temperature,
+                                         int32_t n_virtual, int64_t padded_vocab,
+                                         float* out_logprob, float* out_entropy,
+                                         uint32_t* out_status_word, void* workspace,
+                                         size_t workspace_bytes, rlk_stream stream) {
+  if (n_virtual < 1 || padded_vocab < V || padded_vocab % n_virtual != 0 || ld < V)
+    return RLK_ERR_INVALID_ARG;
+  if (T > 0 && (!workspace || workspace_bytes < (size_t)n_virtual * (size_t)T * 32u ||
+                reinterpret_cast<uintptr_t>(workspace) % 16u != 0))
+    return RLK_ERR_WORKSPACE;
+  const int64_t W = padded_vocab / n_virtual;
+  rlk_shard_partial* part = static_cast<rlk_shard_partial*>(workspace);
+  rlk_status st = rlk_shard_partials(logits, dtype, T, V, ld, 0, W, n_virtual, token_ids,
+                                     temperature, part, stream);
+  if (st != RLK_OK) return st;
+  return rlk_shard_combine(part, n_virtual, T, V, W, token_ids, temperature, out_logprob,
+                           out_entropy, out_status_word, stream);
 }
 
 static rlk_status lmhead_common(const void* hidden, const void* w_vocab, int64_t T, int64_t H,

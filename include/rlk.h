@@ -85,7 +85,7 @@ typedef enum {
 
 /* Operation ids for rlk_workspace_size. */
 enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2,
-       RLK_OP_LMHEAD_BWD = 3, RLK_OP_LMHEAD_TOPP = 4 };
+       RLK_OP_LMHEAD_BWD = 3, RLK_OP_LMHEAD_TOPP = 4, RLK_OP_CANONICAL = 5 };
 
 /* Bits OR-ed into *out_status_word by the kernels. */
 #define RLK_STATUS_BAD_TOKEN_ID 0x1u   /* a token id outside [0, V)          */
@@ -135,6 +135,7 @@ const char* rlk_status_string(rlk_status status);
  *  RLK_OP_LMHEAD:          T rows, V vocabulary, H hidden size
  *  RLK_OP_LMHEAD_BWD:      the same (rlk_lmhead_logprob_bwd)
  *  RLK_OP_LMHEAD_TOPP:     the same (rlk_lmhead_logprob with top_p < 1)
+ *  RLK_OP_CANONICAL:       T rows, V = the number of virtual shards, H unused
  * Returns 0 for an unknown op or negative sizes. */
 size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H);
 
@@ -533,6 +534,86 @@ rlk_status rlk_lmhead_logprob_bwd(const void* hidden, const void* w_vocab, int64
                                   const float* grad_logprob, const float* grad_entropy,
                                   float* grad_hidden, float* grad_w, int accumulate_grad_w,
                                   void* workspace, size_t workspace_bytes, rlk_stream stream);
+
+/*
+ * The canonical vocabulary partition (top_p = 1).
+ *
+ * RL-Kernel "Qwen3-8B VIME train-rollout consistency", section "Canonical
+ * topology strategy": a fixed virtual tensor-parallel degree of 8 and a padded
+ * vocabulary of 152576 for every physical topology; a physical rank executes
+ * its adjacent virtual shards separately and the shards are combined in the
+ * same fixed order (the selected-token log-probability included), so a
+ * topology change moves no reduction boundary.  Shard s covers vocabulary
+ * columns [s W, (s + 1) W), W = padded_vocab / n_virtual, clipped to V (the
+ * padding holds no logits).  The result equals rlk_logprob_entropy's at
+ * top_p = 1 within the parity tolerance, and is bitwise the same whatever the
+ * number of ranks the shards are spread over.
+ */
+#define RLK_CANONICAL_TP 8
+#define RLK_CANONICAL_VOCAB 152576
+
+/* One row's summary of one shard: its max, sum of exponentials and entropy
+ * numerator, and the selected logit when the selected id is in the shard.
+ * Opaque, 32 bytes. */
+typedef struct rlk_shard_partial {
+  float opaque[8];
+} rlk_shard_partial;
+
+/*
+ * rlk_shard_partials -- the partials of n_shards adjacent shards.
+ *
+ * Arguments
+ *  logits          device bf16 or fp32: the columns of shards first_col / W ..
+ *                  first_col / W + n_shards - 1, i.e. global columns
+ *                  [first_col, min(first_col + n_shards W, V)), row-major with
+ *                  row stride ld (elements).
+ *  T, V            rows; the full (unpadded) vocabulary size.
+ *  first_col       global index of the first shard's first column, a multiple
+ *                  of W (shards wholly in the padding get empty partials).
+ *  shard_width     W.
+ *  token_ids       device int32[T] (global ids).
+ *  out_partials    device rlk_shard_partial[n_shards][T] (shard-major), 16-byte
+ *                  aligned.
+ * Errors: RLK_ERR_INVALID_ARG for T < 0, V < 1, W < 1, n_shards < 1, a
+ *  first_col outside the rules above, ld below the columns given, a bad dtype,
+ *  null pointers, a non-finite or non-positive temperature.
+ */
+rlk_status rlk_shard_partials(const void* logits, rlk_dtype dtype, int64_t T, int64_t V, int64_t ld,
+                              int64_t first_col, int64_t shard_width, int32_t n_shards,
+                              const int32_t* token_ids, float temperature,
+                              rlk_shard_partial* out_partials, rlk_stream stream);
+
+/*
+ * rlk_shard_combine -- log-probability and entropy from all shards' partials,
+ * merged in shard order.
+ *
+ *  partials        device rlk_shard_partial[n_shards][T], shard 0 first (the
+ *                  ranks' outputs gathered in rank order).
+ *  n_shards, shard_width  with n_shards W >= V.
+ * Data errors as rlk_logprob_entropy (NaN outputs, RLK_STATUS_BAD_TOKEN_ID or
+ * RLK_STATUS_NONFINITE).
+ */
+rlk_status rlk_shard_combine(const rlk_shard_partial* partials, int32_t n_shards, int64_t T,
+                             int64_t V, int64_t shard_width, const int32_t* token_ids,
+                             float temperature, float* out_logprob, float* out_entropy,
+                             uint32_t* out_status_word, rlk_stream stream);
+
+/*
+ * rlk_logprob_entropy_canonical -- the whole canonical path on one device:
+ * rlk_shard_partials over all n_virtual shards (padded_vocab / n_virtual
+ * wide) into the workspace, then rlk_shard_combine.
+ *
+ *  workspace       rlk_workspace_size(RLK_OP_CANONICAL, T, n_virtual, 0) bytes,
+ *                  16-byte aligned.
+ * Errors: as the two calls; padded_vocab must be >= V and a multiple of
+ *  n_virtual.
+ */
+rlk_status rlk_logprob_entropy_canonical(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                         int64_t ld, const int32_t* token_ids, float temperature,
+                                         int32_t n_virtual, int64_t padded_vocab,
+                                         float* out_logprob, float* out_entropy,
+                                         uint32_t* out_status_word, void* workspace,
+                                         size_t workspace_bytes, rlk_stream stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

@@ -276,6 +276,33 @@ def test_lmhead_fwd_bwd_reject(lib):
     assert need >= 4096 * 151936 * 2 + (64 << 20)
 
 
+def test_canonical_rejects(lib):
+    def part(**kw):
+        a = dict(dtype=0, T=4, V=1000, ld=1000, first=0, W=125, n=8, temp=0.7, out=FAKE)
+        a.update(kw)
+        return lib.rlk_shard_partials(FAKE, a["dtype"], a["T"], a["V"], a["ld"], a["first"], a["W"],
+                                      a["n"], FAKE, a["temp"], a["out"], None)
+    for kw in (dict(W=0), dict(n=0), dict(first=-125), dict(first=100), dict(ld=999), dict(dtype=7),
+               dict(temp=0.0), dict(out=None), dict(out=ctypes.c_void_p(0x10008)), dict(V=0)):
+        assert part(**kw) == 1, kw
+    assert part(T=0, out=None) == 0
+    def comb(**kw):
+        a = dict(n=8, T=4, V=1000, W=125)
+        a.update(kw)
+        return lib.rlk_shard_combine(FAKE, a["n"], a["T"], a["V"], a["W"], FAKE, 0.7, FAKE, FAKE,
+                                     None, None)
+    assert comb(W=124) == 1                     # the shards must cover V
+    assert comb(n=0) == 1
+    def canon(**kw):
+        a = dict(n=8, P=1000, ws=FAKE, wsb=1 << 20)
+        a.update(kw)
+        return lib.rlk_logprob_entropy_canonical(FAKE, 0, 4, 1000, 1000, FAKE, 0.7, a["n"], a["P"],
+                                                 FAKE, FAKE, None, a["ws"], a["wsb"], None)
+    assert canon(P=999) == 1 and canon(P=1001) == 1 and canon(n=0) == 1
+    assert canon(ws=None) == 3 and canon(wsb=16) == 3
+    assert lib.rlk_workspace_size(5, 100, 8, 0) == 100 * 8 * 32
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     z = torch.zeros(2, 8, dtype=torch.bfloat16)

@@ -1,0 +1,96 @@
+"""The canonical vocabulary partition (virtual tensor-parallel degree 8,
+padded vocabulary 152576) through the C ABI.
+
+- Against the fp64 oracle at top_p = 1: |d logprob|, |d entropy| <= 2e-4.
+- Independence of the physical degree: splitting the eight shards over 1, 2,
+  4 or 8 "ranks" (each computing its adjacent shards' partials from its own
+  slice of the columns, then all partials combined in rank order) gives the
+  canonical single-device result bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from _parity import LP_REL, LP_TOL, ENT_TOL
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(lp, ent, olp, oent):
+    lp, ent = lp.cpu().numpy().astype(np.float64), ent.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lp - olp) <= LP_TOL + LP_REL * np.abs(olp))
+    assert np.all(np.abs(ent - oent) <= ENT_TOL)
+
+
+@pytest.mark.parametrize("T_", [0.7, 1.8])
+def test_canonical_matches_oracle(cuda_lib, oracle, T_):
+    R, V = 48, workloads.VOCAB
+    z, _ = workloads.peaked_bf16(R, V=V, seed=33, device="cuda")
+    hz = workloads.bf16_bits(z)
+    ids = torch.from_numpy(oracle.sample_ids(hz, T_, 1.0, workloads.uniforms(R, 7))).cuda()
+    lp, ent = cuda_lib.logprob_entropy_canonical(z, ids, T_)
+    torch.cuda.synchronize()
+    olp, oent, _, _ = oracle.logprob_entropy(hz, ids.cpu().numpy(), T_, 1.0)
+    _check(lp, ent, olp, oent)
+    # and within tolerance of the single-device scorer, whose boundaries differ
+    dlp, dent = cuda_lib.logprob_entropy(z, ids, T_, 1.0)
+    torch.cuda.synchronize()
+    _check(lp, ent, dlp.cpu().numpy().astype(np.float64), dent.cpu().numpy().astype(np.float64))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_physical_degree_does_not_change_the_bits(cuda_lib, dtype):
+    R, V = 40, workloads.VOCAB
+    if dtype == "bf16":
+        z, _ = workloads.peaked_bf16(R, V=V, seed=35, device="cuda")
+    else:
+        z = workloads.normal_logits_fp32(R, V, 3.0, seed=35, device="cuda")
+    ids = torch.randint(0, V, (R,), dtype=torch.int32, device="cuda")
+    ref = cuda_lib.logprob_entropy_canonical(z, ids, 0.7)
+    for tp in (1, 2, 4, 8):
+        parts = []
+        for rank in range(tp):
+            _, n, c0, w = cuda_lib.canonical_plan(tp, rank)
+            local = z[:, c0:min(c0 + n * w, V)]            # this rank's columns only
+            parts.append(cuda_lib.shard_partials(local, ids, 0.7, V, c0, w, n))
+        lp, ent = cuda_lib.shard_combine(torch.cat(parts, 0), ids, 0.7, V, w)
+        torch.cuda.synchronize()
+        assert torch.equal(lp, ref[0]) and torch.equal(ent, ref[1]), tp
+
+
+def test_padding_shards_and_small_vocabularies(cuda_lib, oracle):
+    """A vocabulary of 1000 in a padded 2048 split eight ways: the last shards
+    are padding only (empty partials); ragged shard ends; odd row stride."""
+    R, V = 24, 1000
+    base = workloads.normal_logits_fp32(R, V + 3, 2.0, seed=2, device="cuda")
+    z = base[:, :V]                                    # fp32, row stride V + 3
+    ids = torch.randint(0, V, (R,), dtype=torch.int32, device="cuda")
+    lp, ent = cuda_lib.logprob_entropy_canonical(z, ids, 0.9, 8, 2048)
+    torch.cuda.synchronize()
+    olp, oent, _, _ = oracle.logprob_entropy(z.contiguous().cpu().numpy(), ids.cpu().numpy(),
+                                             0.9, 1.0)
+    _check(lp, ent, olp, oent)
+    # rank 7 of 8 holds padding only: its partials are empty and change nothing
+    parts = []
+    for rank in range(8):
+        _, n, c0, w = cuda_lib.canonical_plan(8, rank, 8, 2048)
+        local = z[:, c0:min(c0 + n * w, V)] if c0 < V else z[:, :1]
+        parts.append(cuda_lib.shard_partials(local, ids, 0.9, V, c0, w, n))
+    lp2, ent2 = cuda_lib.shard_combine(torch.cat(parts, 0), ids, 0.9, V, w)
+    torch.cuda.synchronize()
+    assert torch.equal(lp2, lp) and torch.equal(ent2, ent)
+
+
+def test_canonical_bad_rows(cuda_lib):
+    R, V = 6, workloads.VOCAB
+    z, _ = workloads.peaked_bf16(R, V=V, seed=3, device="cuda")
+    z[2, 140000] = float("nan")        # in the last shard
+    z[3, 5] = float("-inf")
+    ids = torch.tensor([0, V, 1, 2, 3, -1], dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lp, ent = cuda_lib.logprob_entropy_canonical(z, ids, 0.7, status_word=st)
+    torch.cuda.synchronize()
+    bad = torch.isnan(lp).cpu().tolist()
+    assert bad == [False, True, True, True, False, True]
+    assert int(st.item()) == cuda_lib.STATUS_BAD_TOKEN_ID | cuda_lib.STATUS_NONFINITE

@@ -3,6 +3,10 @@ backend and world size 2.  Rows are independent, so N GPUs run N replicas of
 the hot path with no collective on the data path; what crosses ranks is the
 timing: the job's time is the slowest rank's, and the whole-job throughput
 counts every rank's rows over that time.  Each replica draws its own batch.
+
+The vocabulary-parallel (canonical partition) path has one exchange: each
+rank's shard partials are gathered in rank order; the plan of which virtual
+shards a rank holds and that gather are tested here too.
 """
 import os
 import socket
@@ -58,3 +62,54 @@ def test_single_process_helpers():
     import bench
     assert bench.reduce_max(7.5, torch.device("cpu")) == 7.5   # no process group: the value itself
     assert bench.whole_job_rate(4096, 10, 1, 5.0) == pytest.approx(4096 * 10 / 5.0e-3)
+
+
+# ------------------------------------------------ canonical vocabulary partition
+def test_canonical_plan_covers_every_shard_once():
+    import entropy_logits_bf16_gb300 as rlk
+    for tp in (1, 2, 4, 8):
+        seen = []
+        for r in range(tp):
+            s0, n, c0, w = rlk.canonical_plan(tp, r)
+            assert w == rlk.CANONICAL_VOCAB // rlk.CANONICAL_TP and c0 == s0 * w
+            seen += list(range(s0, s0 + n))
+        assert seen == list(range(rlk.CANONICAL_TP))          # adjacent, in rank order
+    with pytest.raises(ValueError):
+        rlk.canonical_plan(3, 0)
+
+
+def _gather_worker(rank, ws, port, q):
+    import torch.distributed as dist
+    import entropy_logits_bf16_gb300 as rlk
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws))
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    try:
+        s0, n, _, _ = rlk.canonical_plan(ws, rank)
+        T = 5
+        # each rank's partials carry their global shard index, so the gathered
+        # order can be read back
+        local = torch.arange(s0, s0 + n, dtype=torch.float32).view(n, 1, 1).expand(n, T, 8)
+        full = rlk.gather_shard_partials(local.contiguous())
+        q.put((rank, full[:, 0, 0].tolist(), tuple(full.shape)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_gather_shard_partials_in_canonical_order_over_two_gloo_ranks():
+    """The vocabulary-parallel exchange: every rank ends with all eight shards'
+    partials in shard order, whatever rank computed them."""
+    ws = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gather_worker, args=(r, ws, port, q)) for r in range(ws)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(ws))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for _, order, shape in res:
+        assert order == [float(s) for s in range(8)]
+        assert shape == (8, 5, 8)
