@@ -584,6 +584,48 @@ def run_canonical(args, ws, rank, dev, barrier):
     }
 
 
+SMP_METRIC = ("tokens/s for deterministic top-p sampling (inverse CDF over the retained set "
+              "in ranking order) at V=151936 bf16")
+
+
+def run_sample(args, ws, rank, dev, barrier):
+    """--op sample: rlk_sample_top_p on the benchmark rows (their retained sets
+    from one forward before the timed region), one uniform per row."""
+    import entropy_logits_bf16_gb300 as rlk
+    stream = torch.cuda.current_stream(dev)
+    z, ids = make_workload(dev, seed=rank_seed(rank))
+    state = rlk.new_row_state(T_ROWS, dev)
+    rlk.logprob_entropy(z, ids, TEMPERATURE, TOP_P, row_state=state)
+    g = torch.Generator(device="cpu").manual_seed(rank_seed(rank) + 4)
+    u = torch.rand(T_ROWS, generator=g).to(dev)
+
+    def call():
+        rlk.sample_top_p(z, TEMPERATURE, TOP_P, u, row_state=state)
+
+    elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [call], barrier)
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    alg = T_ROWS * (VOCAB * 2 + 32 + 4 + 4)   # one read of the row, the state, u, the id
+    achieved = alg / (part_ms[0] / 1e3) / 1e9
+    return {
+        "metric": SMP_METRIC, "value": whole_job_rate(T_ROWS, args.steps, ws, elapsed_ms),
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD + "; one uniform per row", "T": T_ROWS, "V": VOCAB,
+                   "global_batch": T_ROWS * ws,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peak_kind,
+                     "kernel": "sample_kernel (one rlk_sample_top_p call; rows re-read when a tie "
+                               "must be resolved)",
+                     "algorithmic_bytes_per_launch": alg, "launch_ms": part_ms[0]},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+
+
 SUP_METRIC = ("tokens/s for supplied-support logprob+entropy (the top-p retained set given as "
               "CSR) at V=151936 bf16")
 
@@ -722,7 +764,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "lmhead_backward", "support",
                                                        "support_backward", "backward",
-                                                       "lmhead_topp", "canonical"],
+                                                       "lmhead_topp", "canonical", "sample"],
                     help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused "
                          "LM-head; support: the supplied-support scorer; support_backward: its "
                          "gradient; backward: the dense top-p gradient; lmhead_backward: the "
@@ -754,7 +796,7 @@ def main():
            "support_backward": lambda *a: run_support(*a, backward=True),
            "backward": run_backward, "lmhead_backward": run_lmhead_backward,
            "lmhead_topp": lambda *a: run_lmhead(*a, top_p=TOP_P),
-           "canonical": run_canonical}[args.op]
+           "canonical": run_canonical, "sample": run_sample}[args.op]
     line = run(args, ws, rank, dev, barrier)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -49,7 +49,7 @@ EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logpro
            "rlk_logprob_entropy_support", "rlk_logprob_entropy_support_backward",
            "rlk_grpo_loss", "rlk_policy_loss", "rlk_lmhead_logprob", "rlk_lmhead_logprob_fwd",
            "rlk_lmhead_logprob_bwd", "rlk_shard_partials", "rlk_shard_combine",
-           "rlk_logprob_entropy_canonical",
+           "rlk_logprob_entropy_canonical", "rlk_sample_top_p",
            "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
 DEBUG_EXPORTS = ("rlk_lmhead_logits_debug",)
@@ -114,6 +114,8 @@ def load(path: str | None = None):
         lib.rlk_lmhead_logprob.argtypes = [vp, vp, i64, i64, i64, vp, f32, f32, vp, vp, vp, vp,
                                            sz, vp]
         lib.rlk_lmhead_logprob.restype = ctypes.c_int
+        lib.rlk_sample_top_p.argtypes = [vp, ctypes.c_int, i64, i64, i64, f32, vp, vp, vp, vp, vp]
+        lib.rlk_sample_top_p.restype = ctypes.c_int
         lib.rlk_shard_partials.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, i64, i32, vp, f32,
                                            vp, vp]
         lib.rlk_shard_partials.restype = ctypes.c_int
@@ -625,3 +627,29 @@ def vocab_parallel_logprob_entropy(local_logits, token_ids, temperature, V, grou
     part = shard_partials(local_logits, token_ids, temperature, V, first_col, width, n)
     allp = gather_shard_partials(part, group) if world > 1 else part
     return shard_combine(allp, token_ids, temperature, V, width)
+
+
+def sample_top_p(logits, temperature, top_p, uniforms, *, row_state=None, status_word=None):
+    """Deterministic top-p draw per row (rlk_sample_top_p): the id where the
+    cumulative renormalised probability over the retained set, in ranking
+    order, first reaches ``uniforms`` (CUDA fp32 [T]).  Without ``row_state``
+    the forward runs first to select the sets."""
+    lib = load()
+    _need_cuda(logits, uniforms, row_state)
+    if logits.dtype != torch.bfloat16:
+        raise ValueError("the sampler takes bf16 logits")
+    _logits_dtype(logits)
+    if uniforms.dtype != torch.float32 or not uniforms.is_contiguous():
+        raise ValueError("uniforms must be contiguous fp32")
+    T, V = logits.shape
+    if row_state is None:
+        row_state = new_row_state(T, logits.device)
+        logprob_entropy(logits, torch.zeros(T, dtype=torch.int32, device=logits.device),
+                        temperature, top_p, row_state=row_state)
+    out = torch.empty(T, dtype=torch.int32, device=logits.device)
+    ld = logits.stride(0) if T > 1 else V
+    code = lib.rlk_sample_top_p(_ptr(logits), 0, T, V, ld, float(temperature), _ptr(row_state),
+                                _ptr(uniforms), _ptr(out), _ptr(status_word),
+                                _stream(logits.device))
+    _check("rlk_sample_top_p", code)
+    return out

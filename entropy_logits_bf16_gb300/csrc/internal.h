@@ -148,6 +148,16 @@ struct ShardCombineArgs {
   float* out_entropy;
   uint32_t* status;
 };
+struct SampleArgs {
+  const void* logits;   // bf16
+  int64_t T, V, ld;
+  float temperature;
+  const RowState* state;
+  const float* uniforms;
+  int32_t* out_ids;
+  uint32_t* status;
+};
+cudaError_t launch_sample(const SampleArgs& a, cudaStream_t stream);
 cudaError_t launch_shard_partials(const ShardArgs& a, cudaStream_t stream);
 cudaError_t launch_shard_combine(const ShardCombineArgs& a, cudaStream_t stream);
 

@@ -431,6 +431,34 @@ rlk_status rlk_logprob_entropy_canonical(const void* logits, rlk_dtype dtype, in
                            out_entropy, out_status_word, stream);
 }
 
+rlk_status rlk_sample_top_p(const void* logits, rlk_dtype dtype, int64_t T, int64_t V, int64_t ld,
+                            float temperature, const rlk_row_state* row_state,
+                            const float* uniforms, int32_t* out_ids, uint32_t* out_status_word,
+                            rlk_stream stream) {
+  if (dtype != RLK_BF16 && dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || ld < V) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
+  if (dtype != RLK_BF16) return RLK_ERR_UNSUPPORTED;
+  if (T == 0) return RLK_OK;
+  if (!logits || !row_state || !uniforms || !out_ids) return RLK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) % 2u != 0 ||
+      reinterpret_cast<uintptr_t>(row_state) % 16u != 0)
+    return RLK_ERR_INVALID_ARG;
+  rlk::SampleArgs a{};
+  a.logits = logits;
+  a.T = T;
+  a.V = V;
+  a.ld = ld;
+  a.temperature = temperature;
+  a.state = reinterpret_cast<const rlk::RowState*>(row_state);
+  a.uniforms = uniforms;
+  a.out_ids = out_ids;
+  a.status = out_status_word;
+  return rlk::launch_sample(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
 static rlk_status lmhead_common(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
                                 int64_t V, const int32_t* token_ids, float temperature,
                                 float top_p, float* out_logits, float* out_logprob,

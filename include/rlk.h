@@ -536,6 +536,35 @@ rlk_status rlk_lmhead_logprob_bwd(const void* hidden, const void* w_vocab, int64
                                   void* workspace, size_t workspace_bytes, rlk_stream stream);
 
 /*
+ * rlk_sample_top_p -- deterministic top-p sampling.
+ *
+ * For each row, the id at which the cumulative renormalised probability over
+ * the retained set S, taken in ranking order (logit descending, id
+ * ascending), first reaches uniforms[t]: the first j in that order with
+ * sum_{i <= j} w_i >= u Z_S (RL-Kernel "Qwen3-8B VIME train-rollout
+ * consistency", section "ROCm MI300X and gfx942": the sampler's native
+ * temperature / softmax / sort / top-p semantics; "ROCm sparse performance"
+ * notes: deterministic top-p sampling).  S is the set the forward selected,
+ * read from the row state of rlk_logprob_entropy_fwd (whose token_ids do not
+ * affect it).  No sort: a radix descent on the 16-bit key of the bf16 logits
+ * with exact fixed-point masses (w 2^40, truncated: tokens below 2^-40 of the
+ * row maximum count with mass 0), then a scan in id order for the tie.
+ *
+ * Arguments
+ *  logits, T, V, ld, temperature  as the forward's; dtype RLK_BF16 only
+ *                  (RLK_F32: RLK_ERR_UNSUPPORTED).
+ *  row_state       device rlk_row_state[T] from rlk_logprob_entropy_fwd.
+ *  uniforms        device float[T], each in [0, 1) (clamped).
+ *  out_ids         device int32[T]; -1 for a row whose state carries a status.
+ *  out_status_word device uint32[1] or NULL (the state's status bits, or
+ *                  RLK_STATUS_NO_STATE).
+ */
+rlk_status rlk_sample_top_p(const void* logits, rlk_dtype dtype, int64_t T, int64_t V, int64_t ld,
+                            float temperature, const rlk_row_state* row_state,
+                            const float* uniforms, int32_t* out_ids, uint32_t* out_status_word,
+                            rlk_stream stream);
+
+/*
  * The canonical vocabulary partition (top_p = 1).
  *
  * RL-Kernel "Qwen3-8B VIME train-rollout consistency", section "Canonical
