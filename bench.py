@@ -477,7 +477,7 @@ def run_lmhead(args, ws, rank, dev, barrier, top_p=1.0):
     }
     if ws == 1 and not args.no_cpu_baseline:
         import oracle
-        rows = 32
+        rows = 256   # about 10 s of fp64 dot products on 16 cores
         sel = np.linspace(0, LM_T - 1, rows).astype(np.int64)
         hb = workloads.bf16_bits(hidden[torch.from_numpy(sel).to(dev)])
         wb = workloads.bf16_bits(w)
