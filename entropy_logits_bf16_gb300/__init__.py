@@ -52,7 +52,7 @@ EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logpro
            "rlk_logprob_entropy_canonical", "rlk_sample_top_p",
            "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
-DEBUG_EXPORTS = ("rlk_lmhead_logits_debug",)
+DEBUG_EXPORTS = ("rlk_lmhead_logits_debug", "rlk_debug_inject_launch_failures")
 STATUS_TIMEOUT = 0x4
 STATUS_BAD_SUPPORT = 0x8
 STATUS_NO_STATE = 0x10
@@ -116,6 +116,8 @@ def load(path: str | None = None):
         lib.rlk_lmhead_logprob.restype = ctypes.c_int
         lib.rlk_sample_top_p.argtypes = [vp, ctypes.c_int, i64, i64, i64, f32, vp, vp, vp, vp, vp]
         lib.rlk_sample_top_p.restype = ctypes.c_int
+        lib.rlk_debug_inject_launch_failures.argtypes = [ctypes.c_int]
+        lib.rlk_debug_inject_launch_failures.restype = ctypes.c_int
         lib.rlk_shard_partials.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, i64, i32, vp, f32,
                                            vp, vp]
         lib.rlk_shard_partials.restype = ctypes.c_int
@@ -653,3 +655,10 @@ def sample_top_p(logits, temperature, top_p, uniforms, *, row_state=None, status
                                 _stream(logits.device))
     _check("rlk_sample_top_p", code)
     return out
+
+
+def inject_launch_failures(n: int) -> int:
+    """Host-side fault injection: the next ``n`` entry points that would launch
+    return RLK_ERR_CUDA (raised as RlkError) without launching.  Returns the
+    count that was pending."""
+    return int(load().rlk_debug_inject_launch_failures(int(n)))

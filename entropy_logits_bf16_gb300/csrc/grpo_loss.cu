@@ -410,6 +410,7 @@ extern "C" rlk_status rlk_grpo_loss_noalloc(
   a.out_grad = out_dloss_dlogp_new;
   a.out_stats = out_stats;
   a.workspace = scratch;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_grpo_loss(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;

@@ -161,6 +161,9 @@ cudaError_t launch_sample(const SampleArgs& a, cudaStream_t stream);
 cudaError_t launch_shard_partials(const ShardArgs& a, cudaStream_t stream);
 cudaError_t launch_shard_combine(const ShardCombineArgs& a, cudaStream_t stream);
 
+// Consumes one launch failure injected by rlk_debug_inject_launch_failures.
+bool take_injected_failure();
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

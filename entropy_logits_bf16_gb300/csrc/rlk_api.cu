@@ -35,6 +35,18 @@ bool finite_positive(float x) { return std::isfinite(x) && x > 0.0f; }
 
 }  // namespace
 
+namespace rlk {
+// Launch failures injected by rlk_debug_inject_launch_failures: each public
+// entry that is about to launch takes one and returns RLK_ERR_CUDA instead.
+static std::atomic<int> g_injected_failures{0};
+bool take_injected_failure() {
+  int n = g_injected_failures.load();
+  while (n > 0)
+    if (g_injected_failures.compare_exchange_weak(n, n - 1)) return true;
+  return false;
+}
+}  // namespace rlk
+
 extern "C" {
 
 int rlk_version(void) { return 100; }
@@ -98,6 +110,7 @@ rlk_status logprob_entropy_impl(const void* logits, rlk_dtype dtype, int64_t T, 
   a.status = out_status_word;
   a.only_marked = 0;
   a.state = reinterpret_cast<rlk::RowState*>(out_row_state);
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_logprob_entropy(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
@@ -158,6 +171,7 @@ rlk_status rlk_logprob_entropy_bwd(const void* logits, rlk_dtype dtype, int64_t 
   a.grad_dtype = grad_dtype == RLK_BF16 ? 0 : 1;
   a.ldg = ldg;
   a.status = out_status_word;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_logprob_entropy_backward(a, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? RLK_OK
@@ -191,6 +205,7 @@ rlk_status rlk_logprob_entropy_support(const void* logits, rlk_dtype dtype, int6
   a.out_logprob = out_logprob;
   a.out_entropy = out_entropy;
   a.status = out_status_word;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_support(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
@@ -222,6 +237,7 @@ rlk_status rlk_logprob_entropy_support_backward(
   a.grad_logprob = grad_logprob;
   a.grad_entropy = grad_entropy;
   a.grad_support = grad_support;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_support_backward(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
@@ -269,6 +285,7 @@ rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
   a.out_grad = out_dloss_dlogp_new;
   a.out_stats = out_stats;
   a.workspace = static_cast<float*>(workspace);
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_grpo_loss(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
@@ -342,6 +359,7 @@ rlk_status rlk_policy_loss(const float* logp_new, const float* logp_old,
   a.out_grad = out_dloss_dlogp_new;
   a.out_stats = out_stats;
   a.workspace = static_cast<float*>(workspace);
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_grpo_loss(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
@@ -379,6 +397,7 @@ rlk_status rlk_shard_partials(const void* logits, rlk_dtype dtype, int64_t T, in
   a.ids = token_ids;
   a.temperature = temperature;
   a.partials = out_partials;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_shard_partials(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
@@ -406,6 +425,7 @@ rlk_status rlk_shard_combine(const rlk_shard_partial* partials, int32_t n_shards
   a.out_logprob = out_logprob;
   a.out_entropy = out_entropy;
   a.status = out_status_word;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_shard_combine(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
@@ -454,6 +474,7 @@ rlk_status rlk_sample_top_p(const void* logits, rlk_dtype dtype, int64_t T, int6
   a.uniforms = uniforms;
   a.out_ids = out_ids;
   a.status = out_status_word;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_sample(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RLK_OK
              : RLK_ERR_CUDA;
@@ -494,6 +515,7 @@ static rlk_status lmhead_common(const void* hidden, const void* w_vocab, int64_t
   a.workspace = workspace;
   a.out_lse = out_lse;
   a.top_p = top_p;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   const cudaError_t e =
       topp ? rlk::launch_lmhead_topp(a, reinterpret_cast<cudaStream_t>(stream))
            : rlk::launch_lmhead_impl(a, out_logits, reinterpret_cast<cudaStream_t>(stream));
@@ -559,10 +581,15 @@ rlk_status rlk_lmhead_logprob_bwd(const void* hidden, const void* w_vocab, int64
   a.accumulate_w = accumulate_grad_w != 0;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   const cudaError_t e =
       rlk::launch_lmhead_backward(a, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return RLK_ERR_UNSUPPORTED;
   return e == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+int rlk_debug_inject_launch_failures(int n) {
+  return rlk::g_injected_failures.exchange(n < 0 ? 0 : n);
 }
 
 rlk_status rlk_lmhead_logits_debug(const void* hidden, const void* w_vocab, int64_t T, int64_t H,

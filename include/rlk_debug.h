@@ -25,6 +25,16 @@ rlk_status rlk_lmhead_logits_debug(const void* hidden, const void* w_vocab, int6
                                    uint32_t* out_status_word, void* workspace,
                                    size_t workspace_bytes, rlk_stream stream);
 
+/*
+ * rlk_debug_inject_launch_failures -- fault injection on the host.  The next
+ * n calls of any entry point that would launch work (after their argument
+ * checks pass) return RLK_ERR_CUDA without launching anything and without
+ * touching their outputs, as a failed launch would.  n <= 0 clears the count.
+ * Returns the count that was pending.  For testing callers' error handling;
+ * nothing reaches the GPU.
+ */
+int rlk_debug_inject_launch_failures(int n);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -303,6 +303,18 @@ def test_canonical_rejects(lib):
     assert lib.rlk_workspace_size(5, 100, 8, 0) == 100 * 8 * 32
 
 
+def test_injected_launch_failures_come_before_any_launch(lib):
+    """Host-side fault injection: calls whose arguments pass validation return
+    RLK_ERR_CUDA without launching.  More failures are injected than calls are
+    made, so no call here reaches a launch with the placeholder pointers."""
+    assert lib.rlk_debug_inject_launch_failures(5) == 0
+    assert lpe(lib) == 4
+    assert sup(lib) == 4
+    assert sup_bwd(lib) == 4
+    assert lib.rlk_debug_inject_launch_failures(0) == 2      # two were left
+    assert lib.rlk_debug_inject_launch_failures(-3) == 0     # a negative count clears
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     z = torch.zeros(2, 8, dtype=torch.bfloat16)
