@@ -45,7 +45,7 @@ class LossConfig(ctypes.Structure):
 STAT_NAMES = ("loss", "tokens", "clip_low_frac", "clip_high_frac", "tis_mean",
               "tis_capped_frac", "k3_mean", "pg_mean")
 EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logprob_entropy",
-           "rlk_logprob_entropy_fwd", "rlk_logprob_entropy_bwd",
+           "rlk_logprob_entropy_fwd", "rlk_logprob_entropy_bwd", "rlk_logprob_entropy_rows",
            "rlk_logprob_entropy_support", "rlk_logprob_entropy_support_backward",
            "rlk_grpo_loss", "rlk_policy_loss", "rlk_lmhead_logprob", "rlk_lmhead_logprob_fwd",
            "rlk_lmhead_logprob_bwd", "rlk_shard_partials", "rlk_shard_combine",
@@ -56,6 +56,7 @@ DEBUG_EXPORTS = ("rlk_lmhead_logits_debug", "rlk_debug_inject_launch_failures")
 STATUS_TIMEOUT = 0x4
 STATUS_BAD_SUPPORT = 0x8
 STATUS_NO_STATE = 0x10
+STATUS_BAD_PARAM = 0x20
 ROW_STATE_WORDS = 8   # rlk_row_state: 32 bytes per row
 
 _lock = threading.Lock()
@@ -96,6 +97,9 @@ def load(path: str | None = None):
         lib.rlk_logprob_entropy_fwd.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, f32, vp,
                                                 vp, vp, vp, vp, vp]
         lib.rlk_logprob_entropy_fwd.restype = ctypes.c_int
+        lib.rlk_logprob_entropy_rows.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, vp,
+                                                 vp, vp, vp, vp, vp]
+        lib.rlk_logprob_entropy_rows.restype = ctypes.c_int
         lib.rlk_logprob_entropy_bwd.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, vp, vp,
                                                 vp, vp, ctypes.c_int, i64, vp, vp]
         lib.rlk_logprob_entropy_bwd.restype = ctypes.c_int
@@ -225,6 +229,36 @@ def logprob_entropy(logits: torch.Tensor, token_ids: torch.Tensor, temperature: 
                                        float(temperature), float(top_p), _ptr(lp), _ptr(ent),
                                        _ptr(ks), _ptr(status_word), None, 0, _stream(dev))
         _check("rlk_logprob_entropy", code)
+    return (lp, ent, ks) if return_nucleus_size else (lp, ent)
+
+
+def logprob_entropy_rows(logits: torch.Tensor, token_ids: torch.Tensor, temperatures: torch.Tensor,
+                        top_ps: torch.Tensor, *, return_nucleus_size: bool = False,
+                        status_word=None, row_state=None):
+    """``logprob_entropy`` with per-row sampling parameters (CUDA fp32 [T]
+    each).  ``row_state`` records each row's temperature for the backward and
+    the sampler."""
+    lib = load()
+    _need_cuda(logits, token_ids, temperatures, top_ps, row_state)
+    dt = _logits_dtype(logits)
+    T, V = logits.shape
+    for t in (temperatures, top_ps):
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != T:
+            raise ValueError("temperatures and top_ps must be contiguous fp32 [T]")
+    if token_ids.dtype != torch.int32 or not token_ids.is_contiguous():
+        raise ValueError("token_ids must be contiguous int32")
+    if row_state is not None and (row_state.dtype != torch.int32 or not row_state.is_contiguous()
+                                  or row_state.numel() != T * ROW_STATE_WORDS):
+        raise ValueError("row_state must come from new_row_state(T)")
+    ld = logits.stride(0) if T > 1 else V
+    dev = logits.device
+    lp = torch.empty(T, device=dev, dtype=torch.float32)
+    ent = torch.empty(T, device=dev, dtype=torch.float32)
+    ks = torch.empty(T, device=dev, dtype=torch.int32) if return_nucleus_size else None
+    code = lib.rlk_logprob_entropy_rows(_ptr(logits), dt, T, V, ld, _ptr(token_ids),
+                                        _ptr(temperatures), _ptr(top_ps), _ptr(lp), _ptr(ent),
+                                        _ptr(ks), _ptr(row_state), _ptr(status_word), _stream(dev))
+    _check("rlk_logprob_entropy_rows", code)
     return (lp, ent, ks) if return_nucleus_size else (lp, ent)
 
 
@@ -635,7 +669,8 @@ def sample_top_p(logits, temperature, top_p, uniforms, *, row_state=None, status
     """Deterministic top-p draw per row (rlk_sample_top_p): the id where the
     cumulative renormalised probability over the retained set, in ranking
     order, first reaches ``uniforms`` (CUDA fp32 [T]).  Without ``row_state``
-    the forward runs first to select the sets."""
+    the forward runs first to select the sets; ``temperature`` and ``top_p``
+    may then be CUDA fp32 [T] tensors (per-row parameters)."""
     lib = load()
     _need_cuda(logits, uniforms, row_state)
     if logits.dtype != torch.bfloat16:
@@ -646,8 +681,15 @@ def sample_top_p(logits, temperature, top_p, uniforms, *, row_state=None, status
     T, V = logits.shape
     if row_state is None:
         row_state = new_row_state(T, logits.device)
-        logprob_entropy(logits, torch.zeros(T, dtype=torch.int32, device=logits.device),
-                        temperature, top_p, row_state=row_state)
+        zeros = torch.zeros(T, dtype=torch.int32, device=logits.device)
+        if torch.is_tensor(temperature) or torch.is_tensor(top_p):   # per-row parameters
+            full = lambda v: v if torch.is_tensor(v) else torch.full(
+                (T,), float(v), device=logits.device, dtype=torch.float32)
+            logprob_entropy_rows(logits, zeros, full(temperature), full(top_p),
+                                 row_state=row_state)
+            temperature = 1.0   # each state carries its row's
+        else:
+            logprob_entropy(logits, zeros, temperature, top_p, row_state=row_state)
     out = torch.empty(T, dtype=torch.int32, device=logits.device)
     ld = logits.stride(0) if T > 1 else V
     code = lib.rlk_sample_top_p(_ptr(logits), 0, T, V, ld, float(temperature), _ptr(row_state),

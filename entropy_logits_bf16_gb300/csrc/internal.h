@@ -16,7 +16,7 @@ struct RowState {
   float E, lz, H;
   uint32_t key_thr, ties, flags;   // flags: kState* bits | row status << 8
   int32_t kstar;
-  uint32_t reserved;
+  float temperature;   // the row's own, when the forward took per-row temperatures; else 0
 };
 static_assert(sizeof(RowState) == 32, "rlk_row_state is 32 bytes");
 constexpr uint32_t kStateValid = 1u;   // the forward finished the row
@@ -35,6 +35,9 @@ struct LpeArgs {
   uint32_t* status;
   int only_marked;  // per-row kernel: process only rows whose out_logprob holds kRecomputeMark
   RowState* state;  // [T] or NULL
+  // per-row sampling parameters (NULL: the scalars above for every row)
+  const float* temps = nullptr;
+  const float* top_ps = nullptr;
 };
 
 struct LpeBwdArgs {

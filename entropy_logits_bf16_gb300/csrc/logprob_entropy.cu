@@ -897,11 +897,11 @@ __device__ __noinline__ float full_entropy_numerator(const RowBf16& row, int tid
 // by ln2 (m c - E), computed exactly by one fma.
 __device__ __forceinline__ void write_state(const LpeArgs& a, int64_t r, float m, float c, float lz,
                                             float h, uint32_t key_thr, uint32_t ties, bool y_in,
-                                            uint32_t kstar) {
+                                            uint32_t kstar, float row_t) {
   const float E = __fmul_rn(m, c);
   const float lzE = __fmaf_rn(kLn2, __fmaf_rn(m, c, -E), lz);
   a.state[r] = RowState{E, lzE, h, key_thr, ties, kStateValid | (y_in ? kStateYIn : 0u),
-                        (int32_t)kstar, 0u};
+                        (int32_t)kstar, row_t};
 }
 
 __device__ __forceinline__ void write_bad_state(const LpeArgs& a, int64_t r, uint32_t bit) {
@@ -910,7 +910,7 @@ __device__ __forceinline__ void write_bad_state(const LpeArgs& a, int64_t r, uin
 
 // --------------------------------------------------------------- kernel
 template <class Row, bool TOPP>
-__global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float inv_t) {
+__global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c0, float inv_t0) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
@@ -945,6 +945,27 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
       }
       continue;
     }
+    // The row's sampling parameters: the call's, or its own (per-row mode,
+    // with c and 1 / T formed exactly as the host forms the call's).
+    float c = c0, inv_t = inv_t0, temp = a.temperature, top_p = a.top_p, row_t = 0.f;
+    if (a.temps || a.top_ps) {
+      if (a.temps) temp = a.temps[r];
+      if (a.top_ps) top_p = a.top_ps[r];
+      if (!(isfinite(temp) && temp > 0.f && top_p > 0.f && top_p <= 1.f)) {
+        if (tid == 0) {
+          a.out_logprob[r] = NAN;
+          a.out_entropy[r] = NAN;
+          if (a.out_k) a.out_k[r] = 0;
+          if (a.status) atomicOr(a.status, RLK_STATUS_BAD_PARAM);
+          write_bad_state(a, r, RLK_STATUS_BAD_PARAM);
+        }
+        continue;
+      }
+      c = (float)(1.4426950408889634 / (double)temp);
+      inv_t = (float)(1.0 / (double)temp);
+      if (a.temps) row_t = temp;
+    }
+    const bool row_topp = TOPP && top_p < 1.0f;
     const float zy = row.elem(y);    // the selected logit
     const uint32_t key_y = Row::key(zy);
 
@@ -983,22 +1004,27 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
       __syncthreads();
       continue;
     }
-    const float x_y = __fdiv_rn(__fsub_rn(zy, m), a.temperature);
-    if (!TOPP) {
+    const float x_y = __fdiv_rn(__fsub_rn(zy, m), temp);
+    if (!row_topp) {
+      // top_p = 1 (a per-row top_p of 1 in a top-p launch has no entropy
+      // numerator from the packed pass 1: one more pass gives it)
+      float u_ln2 = __fmul_rn(kLn2, st.u);
+      if constexpr (HIST) u_ln2 = full_entropy_numerator(row, tid, m, c, inv_t, sm);
       if (tid == 0) {
         const float lz = logf(zf);
-        const float h = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, st.u), zf));
+        const float h = __fsub_rn(lz, __fdiv_rn(u_ln2, zf));
         a.out_logprob[r] = __fsub_rn(x_y, lz);
         a.out_entropy[r] = h;
         if (a.out_k) a.out_k[r] = (int32_t)a.V;
-        if (a.state) write_state(a, r, m, c, lz, h, 0u, kTiesAll, true, (uint32_t)a.V);
+        if (a.state) write_state(a, r, m, c, lz, h, 0u, kTiesAll, true, (uint32_t)a.V, row_t);
       }
+      __syncthreads();
       continue;
     }
 
     // ---- top_p < 1: nucleus select
-    const DF target = df_mul_f(Z, a.top_p);
-    const float one_m_p = __fsub_rn(1.f, a.top_p);
+    const DF target = df_mul_f(Z, top_p);
+    const float one_m_p = __fsub_rn(1.f, top_p);
     // Speculative window depth (units of T), kept only if its own mass reaches
     // the target; worst-case depth, below which lies less than
     // V e^-L < (1 - top_p) Z of the mass.
@@ -1019,7 +1045,7 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
       for (int att = 0; att < 2 && !done && !use_bisect; ++att) {
         if (att == 0 && !(L_spec < L_worst)) continue;
         const float L = att == 0 ? L_spec : L_worst;
-        const float zlo = __fsub_rn(m, __fmul_rn(L, a.temperature));
+        const float zlo = __fsub_rn(m, __fmul_rn(L, temp));
         bool merged_in;
         const uint32_t dmax = window_dmax(zlo, ck_m, merged_in);
         if (dmax >= (uint32_t)HB) { use_bisect = true; break; }
@@ -1089,7 +1115,7 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c, float in
       a.out_logprob[r] = y_in ? __fsub_rn(x_y, lz) : -INFINITY;
       a.out_entropy[r] = hval;
       if (a.out_k) a.out_k[r] = (int32_t)kstar;
-      if (a.state) write_state(a, r, m, c, lz, hval, key_thr, ties, y_in, kstar);
+      if (a.state) write_state(a, r, m, c, lz, hval, key_thr, ties, y_in, kstar, row_t);
     }
     __syncthreads();
   }
@@ -1103,7 +1129,10 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
   const float inv_t = (float)(1.0 / (double)a.temperature);
   const int64_t grid64 = a.T < (int64_t)3 * sm_count() ? a.T : (int64_t)3 * sm_count();
   const dim3 grid((unsigned)grid64), block(NT);
-  const bool topp = a.top_p < 1.0f;
+  // per-row parameters: the per-row kernel in its top-p form (rows with
+  // top_p = 1 take its all-tokens branch); the cluster kernel is scalar-only
+  const bool per_row = a.temps != nullptr || a.top_ps != nullptr;
+  const bool topp = per_row || a.top_p < 1.0f;
   const size_t smem = sizeof(Smem);
 
   static std::atomic<int> attr_done{0};
@@ -1120,7 +1149,7 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
       return e;
     attr_done.store(1);
   }
-  if (!a.only_marked && lpe_cluster_eligible(a)) {
+  if (!a.only_marked && !per_row && lpe_cluster_eligible(a)) {
     cudaError_t e = launch_lpe_cluster(a, stream);
     if (e != cudaSuccess || !topp) return e;
     LpeArgs b = a;   // rows the cluster kernel marked for recomputation

@@ -43,6 +43,18 @@ __device__ __forceinline__ uint32_t key_of(float v) {
   return okey32(__float_as_uint(v));
 }
 
+// The row's c = log2(e) / T and 1 / T: from the temperature its state
+// recorded (a forward with per-row temperatures), else the call's.
+__device__ __forceinline__ void row_consts(const RowState& st, float c0, float inv_t0, float& c,
+                                           float& inv_t) {
+  c = c0;
+  inv_t = inv_t0;
+  if (st.temperature > 0.f) {
+    c = (float)(1.4426950408889634 / (double)st.temperature);
+    inv_t = (float)(1.0 / (double)st.temperature);
+  }
+}
+
 // 16 logits from id i0 (vector loads when the whole run is inside the row and
 // the row is 16-byte aligned; ids past V read as -inf and are never members).
 template <bool BF>
@@ -129,7 +141,7 @@ __device__ __forceinline__ uint32_t lowest_bits(uint32_t m, int n) {
 }
 
 template <bool BF, bool BO>
-__global__ void __launch_bounds__(NTB, 4) lpe_backward_kernel(LpeBwdArgs a, float c, float inv_t) {
+__global__ void __launch_bounds__(NTB, 4) lpe_backward_kernel(LpeBwdArgs a, float c0, float inv_t0) {
   __shared__ uint32_t s_wt[2][NWB];   // per-warp tie counts of a step (double-buffered)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t per_step = (int64_t)NTB * EPT;
@@ -156,6 +168,8 @@ __global__ void __launch_bounds__(NTB, 4) lpe_backward_kernel(LpeBwdArgs a, floa
       for (int64_t s = 0; s < nstep; ++s) store16<BO>(grow, vout, (s * NTB + tid) * EPT, a.V, g);
       continue;
     }
+    float c, inv_t;
+    row_consts(st, c0, inv_t0, c, inv_t);
     const float glp = (st.flags & kStateYIn) && a.grad_logprob ? a.grad_logprob[r] : 0.f;
     const float gh = a.grad_entropy ? a.grad_entropy[r] : 0.f;
     const float lz2 = __fmul_rn(st.lz, kLog2e);
@@ -255,7 +269,7 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
 }
 
 template <bool BO>
-__global__ void __launch_bounds__(PT, 3) lpe_backward_pipe_kernel(LpeBwdArgs a, float c, float inv_t) {
+__global__ void __launch_bounds__(PT, 3) lpe_backward_pipe_kernel(LpeBwdArgs a, float c0, float inv_t0) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   PSmem& sm = *reinterpret_cast<PSmem*>(smem_raw);
   uint8_t* ring = smem_raw + RING_OFF;
@@ -291,7 +305,7 @@ __global__ void __launch_bounds__(PT, 3) lpe_backward_pipe_kernel(LpeBwdArgs a, 
   //   grad = q (-C t - B) + A [i = y],
   // A = g_lp / T, B = (g_lp + g_H H) / T, C = g_H ln2 / T.
   float thr_v = 0.f, thr_up = 0.f, A = 0.f;   // the boundary value and the next bf16 above it
-  float2 c2 = make_float2(c, c), nE2 = c2, nB2 = c2, nC2 = c2;
+  float2 c2 = make_float2(c0, c0), nE2 = c2, nB2 = c2, nC2 = c2;
   uint32_t carry = 0u, phase = 0u;
   for (int64_t g = 0; g < G; ++g) {
     const int64_t ch = g % nch;
@@ -306,6 +320,9 @@ __global__ void __launch_bounds__(PT, 3) lpe_backward_pipe_kernel(LpeBwdArgs a, 
         if (bits == 0u) bits = RLK_STATUS_NO_STATE;
         atomicOr(a.status, bits);
       }
+      float c, inv_t;
+      row_consts(st, c0, inv_t0, c, inv_t);
+      c2 = make_float2(c, c);
       const float glp = good && (st.flags & kStateYIn) && a.grad_logprob ? a.grad_logprob[r] : 0.f;
       const float gh = good && a.grad_entropy ? a.grad_entropy[r] : 0.f;
       const float eref = __fadd_rn(st.E, __fmul_rn(st.lz, kLog2e));

@@ -95,7 +95,7 @@ rlk_status logprob_entropy_impl(const void* logits, rlk_dtype dtype, int64_t T, 
   const uintptr_t elem = dtype == RLK_BF16 ? 2u : 4u;
   if (reinterpret_cast<uintptr_t>(logits) % elem != 0) return RLK_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(out_row_state) % 16u != 0) return RLK_ERR_INVALID_ARG;
-  rlk::LpeArgs a;
+  rlk::LpeArgs a{};
   a.logits = logits;
   a.dtype = dtype == RLK_BF16 ? 0 : 1;
   a.T = T;
@@ -117,6 +117,44 @@ rlk_status logprob_entropy_impl(const void* logits, rlk_dtype dtype, int64_t T, 
 }
 
 }  // namespace
+
+rlk_status rlk_logprob_entropy_rows(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                    int64_t ld, const int32_t* token_ids,
+                                    const float* temperatures, const float* top_ps,
+                                    float* out_logprob, float* out_entropy,
+                                    int32_t* out_nucleus_size, rlk_row_state* out_row_state,
+                                    uint32_t* out_status_word, rlk_stream stream) {
+  if (dtype != RLK_BF16 && dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || ld < V) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  if (!logits || !token_ids || !temperatures || !top_ps || !out_logprob || !out_entropy)
+    return RLK_ERR_INVALID_ARG;
+  const uintptr_t elem = dtype == RLK_BF16 ? 2u : 4u;
+  if (reinterpret_cast<uintptr_t>(logits) % elem != 0 ||
+      reinterpret_cast<uintptr_t>(out_row_state) % 16u != 0)
+    return RLK_ERR_INVALID_ARG;
+  rlk::LpeArgs a{};
+  a.logits = logits;
+  a.dtype = dtype == RLK_BF16 ? 0 : 1;
+  a.T = T;
+  a.V = V;
+  a.ld = ld;
+  a.ids = token_ids;
+  a.temperature = 1.0f;   // placeholders: every row reads its own
+  a.top_p = 1.0f;
+  a.out_logprob = out_logprob;
+  a.out_entropy = out_entropy;
+  a.out_k = out_nucleus_size;
+  a.status = out_status_word;
+  a.only_marked = 0;
+  a.state = reinterpret_cast<rlk::RowState*>(out_row_state);
+  a.temps = temperatures;
+  a.top_ps = top_ps;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
+  return rlk::launch_logprob_entropy(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
 
 rlk_status rlk_logprob_entropy(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
                                int64_t ld, const int32_t* token_ids, float temperature,

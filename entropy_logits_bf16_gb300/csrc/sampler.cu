@@ -127,7 +127,7 @@ __device__ void scan256(MSmem& sm, unsigned long long base, unsigned long long t
   }
 }
 
-__global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c) {
+__global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
   __shared__ MSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ngroups = (a.V + 7) / 8;
@@ -141,6 +141,9 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c) {
       }
       continue;
     }
+    // the row's c: from the temperature its state recorded, else the call's
+    const float c = st.temperature > 0.f ? (float)(1.4426950408889634 / (double)st.temperature)
+                                         : c0;
     const uint16_t* p = reinterpret_cast<const uint16_t*>(a.logits) + r * a.ld;
     const bool vec = (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
     const uint32_t thr = st.key_thr;

@@ -97,6 +97,9 @@ enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2,
                                           offsets decrease                      */
 #define RLK_STATUS_NO_STATE     0x10u  /* a row state that no forward wrote
                                           (rlk_logprob_entropy_bwd)           */
+#define RLK_STATUS_BAD_PARAM    0x20u  /* a per-row temperature that is not
+                                          finite and > 0, or a per-row top_p
+                                          outside (0, 1]                      */
 
 /* What rlk_logprob_entropy_fwd saves per row for rlk_logprob_entropy_bwd:
  * the row's log-normaliser over its retained set, its entropy and where the
@@ -196,6 +199,35 @@ rlk_status rlk_logprob_entropy_fwd(const void* logits, rlk_dtype dtype, int64_t 
                                    uint32_t* out_status_word, rlk_stream stream);
 
 /*
+ * rlk_logprob_entropy_rows -- rlk_logprob_entropy_fwd with sampling parameters
+ * per row.
+ *
+ * The pages' samplers have no fixed sampling parameter (RL-Kernel "ROCm
+ * sparse performance" notes) and test per-row top-p: a batch may mix
+ * requests.  Row t uses temperatures[t] and top_ps[t]; c = log2(e) / T and
+ * 1 / T are formed per row exactly as the scalar call forms them, so rows
+ * with equal parameters give the scalar call's results on the same kernel
+ * (at top_p = 1 the entropy numerator is summed in another order: equal
+ * within rounding).
+ * These rows run on the per-row kernel (the cluster-resident kernel is for
+ * one parameter pair per call).
+ *
+ * Arguments as rlk_logprob_entropy_fwd, with
+ *  temperatures, top_ps  device float[T] (required).
+ *  out_row_state   device rlk_row_state[T] or NULL; a state records its row's
+ *                  temperature, which rlk_logprob_entropy_bwd and
+ *                  rlk_sample_top_p then use for that row.
+ * A row whose temperature is not finite and > 0 or whose top_p lies outside
+ * (0, 1] gets NaN outputs and RLK_STATUS_BAD_PARAM.
+ */
+rlk_status rlk_logprob_entropy_rows(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                    int64_t ld, const int32_t* token_ids,
+                                    const float* temperatures, const float* top_ps,
+                                    float* out_logprob, float* out_entropy,
+                                    int32_t* out_nucleus_size, rlk_row_state* out_row_state,
+                                    uint32_t* out_status_word, rlk_stream stream);
+
+/*
  * rlk_logprob_entropy_bwd -- gradient of the top-p log-probability and
  * entropy with respect to the logits.
  *
@@ -214,7 +246,9 @@ rlk_status rlk_logprob_entropy_fwd(const void* logits, rlk_dtype dtype, int64_t 
  *
  * Arguments
  *  logits, dtype, T, V, ld, token_ids, temperature
- *                  the forward's (same values, same contents).
+ *                  the forward's (same values, same contents); a row whose
+ *                  state recorded its own temperature (rlk_logprob_entropy_rows)
+ *                  uses that one.
  *  row_state       device rlk_row_state[T] from rlk_logprob_entropy_fwd.
  *  grad_logprob    device float[T] or NULL (zero).
  *  grad_entropy    device float[T] or NULL (zero).
@@ -551,8 +585,9 @@ rlk_status rlk_lmhead_logprob_bwd(const void* hidden, const void* w_vocab, int64
  * row maximum count with mass 0), then a scan in id order for the tie.
  *
  * Arguments
- *  logits, T, V, ld, temperature  as the forward's; dtype RLK_BF16 only
- *                  (RLK_F32: RLK_ERR_UNSUPPORTED).
+ *  logits, T, V, ld, temperature  as the forward's (a row whose state
+ *                  recorded its own temperature uses that one); dtype RLK_BF16
+ *                  only (RLK_F32: RLK_ERR_UNSUPPORTED).
  *  row_state       device rlk_row_state[T] from rlk_logprob_entropy_fwd.
  *  uniforms        device float[T], each in [0, 1) (clamped).
  *  out_ids         device int32[T]; -1 for a row whose state carries a status.
