@@ -151,7 +151,9 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
     float u = a.uniforms[r];
     u = u < 0.f ? 0.f : (u < 1.f ? u : 0.99999994f);
     // the 16-bit key k of each element of group g, through f(k, z, index)
-    auto for_row = [&](auto&& f) {
+    // (groups whose largest value is below `gate` hold no token the pass wants:
+    // one packed max skips them)
+    auto for_row = [&](float gate, auto&& f) {
       for (int64_t g = tid; g < ngroups; g += NTM) {
         uint32_t w4[4];
         if (vec && g * 8 + 8 <= a.V) {
@@ -166,6 +168,9 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
             w4[h] = lo | (hi << 16);
           }
         }
+        const __nv_bfloat162 m2 = __hmax2(__hmax2(bf2(w4[0]), bf2(w4[1])),
+                                          __hmax2(bf2(w4[2]), bf2(w4[3])));
+        if (fmaxf(__low2float(m2), __high2float(m2)) < gate) continue;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int64_t i = g * 8 + e;
@@ -177,6 +182,7 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
     };
     const float zt = bf16_val(okey16_inverse(thr));
     const uint64_t w_thr = thr == 0u ? 0ull : fixed_w(zt, c, E);
+    const float gate = thr == 0u ? -INFINITY : zt;   // members are z >= the boundary value
     uint32_t key_sel = 0u, n_sel = 0u, need = 1u;
     bool have = false;          // key_sel / need found (block-uniform)
     int32_t direct_id = -1;     // direct mode, need == 1: the answer
@@ -196,7 +202,7 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
           sm.dsel = 0x7FFFFFFF;
         }
         __syncthreads();
-        for_row([&](uint32_t k, float z, int64_t i) {
+        for_row(gate, [&](uint32_t k, float z, int64_t i) {
           if (k < thr) return;
           const uint32_t d = k - thr;
           if (d >= (uint32_t)NBD) {
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
     }
     if (tid == 0) sm.n_thr = 0u;
     __syncthreads();
-    for_row([&](uint32_t k, float z, int64_t) {
+    for_row(gate, [&](uint32_t k, float z, int64_t) {
       if (k < thr) return;
       atomicAdd(&sm.cnt[k >> 8], 1u);
       atomicAdd(&sm.mass[k >> 8], fixed_w(z, c, E));
@@ -330,7 +336,7 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
       sm.cnt[i] = 0u;
     }
     __syncthreads();
-    for_row([&](uint32_t k, float z, int64_t) {
+    for_row(gate, [&](uint32_t k, float z, int64_t) {
       if (k < thr || (int)(k >> 8) != hi_bin) return;
       atomicAdd(&sm.cnt[k & 255u], 1u);
       atomicAdd(&sm.mass[k & 255u], fixed_w(z, c, E));
@@ -366,25 +372,36 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
     }
     __syncthreads();
     // ---- pass 3: the need-th id (ascending) holding key_sel
+    const __nv_bfloat162 sel2 = bf2(okey16_inverse(key_sel) * 0x10001u);
+    // Each step covers 4 NTM groups: thread t takes the four consecutive
+    // groups 4 t .. 4 t + 3 of the step (ids stay in thread order).
+    constexpr int GPS = 4;
     uint32_t carry = 0u;
-    for (int64_t g0 = 0; g0 < ngroups; g0 += NTM) {
-      const int64_t g = g0 + tid;
-      uint32_t mm = 0u;   // matches in this thread's group (bit e)
-      if (g < ngroups) {
+    for (int64_t g0 = 0; g0 < ngroups; g0 += (int64_t)GPS * NTM) {
+      const int64_t gb = g0 + (int64_t)GPS * tid;
+      uint32_t mm = 0u;   // bit 8 j + e: element e of group gb + j holds key_sel
+#pragma unroll
+      for (int j = 0; j < GPS; ++j) {
+        const int64_t g = gb + j;
+        if (g >= ngroups) break;
         if (vec && g * 8 + 8 <= a.V) {
+          // equal values <=> equal keys (-0 == +0; a valid row holds no NaN)
           const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + g);
           const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (okey16((w4[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) == key_sel) mm |= 1u << e;
+          for (int h = 0; h < 4; ++h) {
+            const uint32_t eq = __heq2_mask(bf2(w4[h]), sel2);
+            mm |= ((eq & 1u) | ((eq >> 15) & 2u)) << (8 * j + 2 * h);
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int64_t i = g * 8 + e;
-            if (i < a.V && okey16(__ldg(p + i)) == key_sel) mm |= 1u << e;
+            if (i < a.V && okey16(__ldg(p + i)) == key_sel) mm |= 1u << (8 * j + e);
           }
         }
       }
+      const int64_t g = gb;   // ids: gb * 8 + bit
       const uint32_t n = (uint32_t)__popc(mm);
       uint32_t inc = n;
 #pragma unroll
