@@ -41,6 +41,8 @@ constexpr int NWM = NTM / 32;
 constexpr float kFix = 1099511627776.0f;   // 2^40
 
 constexpr int NBD = 2048;   // direct mode: members' keys within NBD of the boundary key
+// the direct-mode scan gives each thread exactly 8 consecutive bins
+static_assert(NBD == 8 * NTM, "direct-mode bins: 8 per thread");
 
 struct MSmem {
   union {
