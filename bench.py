@@ -86,6 +86,8 @@ def measured_peaks():
 
 BWD_SRC = os.path.join(ROOT, "entropy_logits_bf16_gb300", "csrc", "lpe_backward.cu")
 BWD_PROFILE = os.path.join(ROOT, "profiles", "lpe_backward_pipe_kernel_qwen_T4096.txt")
+CSRC = os.path.join(ROOT, "entropy_logits_bf16_gb300", "csrc")
+PROFILES = os.path.join(ROOT, "profiles")
 
 
 def kernel_sha(src=KERNEL_SRC):
@@ -581,8 +583,11 @@ def run_canonical(args, ws, rank, dev, barrier):
                    "global_batch": T_ROWS * ws,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peak_kind,
-                     "kernel": "shard_partial_kernel + shard_combine_kernel",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic(os.path.join(CSRC, "vocab_parallel.cu"),
+                                                 os.path.join(PROFILES, "shard_partial_kernel_qwen_T4096.txt")),
+                     "peak_source": peak_kind,
+                     "kernel": "shard_partial_kernel + shard_combine_kernel (traffic: the partial kernel)",
                      "algorithmic_bytes_per_launch": alg, "launch_ms": part_ms[0]},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
@@ -704,7 +709,12 @@ def run_support(args, ws, rank, dev, barrier, backward=False):
                    "mean_listed_per_row": nnz / T_ROWS, "global_batch": T_ROWS * ws,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peak_kind,
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic(
+                         os.path.join(CSRC, "support.cu"),
+                         os.path.join(PROFILES, ("support_backward_kernel_qwen_T4096.txt" if backward
+                                                 else "support_kernel_qwen_T4096.txt"))),
+                     "peak_source": peak_kind,
                      "kernel": kernel,
                      "algorithmic_bytes_per_launch": alg,
                      "sector_bytes_per_launch": sectors,
