@@ -49,6 +49,7 @@ EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logpro
            "rlk_logprob_entropy_support", "rlk_logprob_entropy_support_backward",
            "rlk_grpo_loss", "rlk_policy_loss", "rlk_lmhead_logprob", "rlk_lmhead_logprob_fwd",
            "rlk_lmhead_logprob_bwd", "rlk_shard_partials", "rlk_shard_combine",
+           "rlk_shard_partials_support",
            "rlk_logprob_entropy_canonical", "rlk_sample_top_p",
            "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
@@ -125,6 +126,9 @@ def load(path: str | None = None):
         lib.rlk_shard_partials.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, i64, i32, vp, f32,
                                            vp, vp]
         lib.rlk_shard_partials.restype = ctypes.c_int
+        lib.rlk_shard_partials_support.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, i64, i32,
+                                                   vp, f32, vp, vp, vp, vp]
+        lib.rlk_shard_partials_support.restype = ctypes.c_int
         lib.rlk_shard_combine.argtypes = [vp, i32, i64, i64, i64, vp, f32, vp, vp, vp, vp]
         lib.rlk_shard_combine.restype = ctypes.c_int
         lib.rlk_logprob_entropy_canonical.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, i32,
@@ -600,6 +604,27 @@ def shard_partials(logits, token_ids, temperature, V, first_col, shard_width, n_
                                   int(shard_width), int(n_shards), _ptr(token_ids),
                                   float(temperature), _ptr(out), _stream(logits.device))
     _check("rlk_shard_partials", code)
+    return out
+
+
+def shard_partials_support(logits, token_ids, temperature, V, first_col, shard_width, n_shards,
+                           support_offsets, support_ids):
+    """rlk_shard_partials_support: [n_shards, T, 8] partials of a supplied
+    retained set (CSR over global ids) restricted to this rank's shards."""
+    lib = load()
+    _need_cuda(logits, token_ids, support_offsets, support_ids)
+    dt = _logits_dtype(logits)
+    if support_offsets.dtype != torch.int64 or support_ids.dtype != torch.int32:
+        raise ValueError("support_offsets int64, support_ids int32")
+    T = logits.shape[0]
+    ld = logits.stride(0) if T > 1 else logits.shape[1]
+    out = torch.empty((n_shards, T, SHARD_PARTIAL_WORDS), device=logits.device,
+                      dtype=torch.float32)
+    code = lib.rlk_shard_partials_support(_ptr(logits), dt, T, int(V), ld, int(first_col),
+                                          int(shard_width), int(n_shards), _ptr(token_ids),
+                                          float(temperature), _ptr(support_offsets),
+                                          _ptr(support_ids), _ptr(out), _stream(logits.device))
+    _check("rlk_shard_partials_support", code)
     return out
 
 

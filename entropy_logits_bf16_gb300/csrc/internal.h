@@ -140,6 +140,9 @@ struct ShardArgs {
   const int32_t* ids;
   float temperature;
   void* partials;
+  // supplied retained set (shard_support_partial_kernel): CSR over global ids
+  const int64_t* offsets = nullptr;
+  const int32_t* support = nullptr;
 };
 struct ShardCombineArgs {
   const void* partials;   // [n_shards][T], canonical order, shard 0 first
@@ -163,6 +166,7 @@ struct SampleArgs {
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t stream);
 cudaError_t launch_shard_partials(const ShardArgs& a, cudaStream_t stream);
 cudaError_t launch_shard_combine(const ShardCombineArgs& a, cudaStream_t stream);
+cudaError_t launch_shard_support_partials(const ShardArgs& a, cudaStream_t stream);
 
 // Consumes one launch failure injected by rlk_debug_inject_launch_failures.
 bool take_injected_failure();

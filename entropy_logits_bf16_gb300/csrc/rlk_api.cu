@@ -441,6 +441,47 @@ rlk_status rlk_shard_partials(const void* logits, rlk_dtype dtype, int64_t T, in
              : RLK_ERR_CUDA;
 }
 
+rlk_status rlk_shard_partials_support(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                      int64_t ld, int64_t first_col, int64_t shard_width,
+                                      int32_t n_shards, const int32_t* token_ids,
+                                      float temperature, const int64_t* support_offsets,
+                                      const int32_t* support_ids,
+                                      rlk_shard_partial* out_partials, rlk_stream stream) {
+  if (dtype != RLK_BF16 && dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || shard_width < 1 || n_shards < 1)
+    return RLK_ERR_INVALID_ARG;
+  if (first_col < 0 || first_col % shard_width != 0) return RLK_ERR_INVALID_ARG;
+  const int64_t span = shard_width * (int64_t)n_shards;
+  int64_t cols = V - first_col < span ? V - first_col : span;
+  if (cols < 0) cols = 0;
+  if (ld < cols) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature)) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  if (!logits || !token_ids || !support_offsets || !out_partials) return RLK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) % (dtype == RLK_BF16 ? 2u : 4u) != 0 ||
+      reinterpret_cast<uintptr_t>(out_partials) % 16u != 0)
+    return RLK_ERR_INVALID_ARG;
+  rlk::ShardArgs a{};
+  a.logits = logits;
+  a.dtype = dtype == RLK_BF16 ? 0 : 1;
+  a.T = T;
+  a.V = V;
+  a.ld = ld;
+  a.first_col = first_col;
+  a.shard_width = shard_width;
+  a.n_shards = n_shards;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.partials = out_partials;
+  a.offsets = support_offsets;
+  a.support = support_ids;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
+  return rlk::launch_shard_support_partials(a, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
 rlk_status rlk_shard_combine(const rlk_shard_partial* partials, int32_t n_shards, int64_t T,
                              int64_t V, int64_t shard_width, const int32_t* token_ids,
                              float temperature, float* out_logprob, float* out_entropy,

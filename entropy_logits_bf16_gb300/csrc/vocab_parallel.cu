@@ -209,7 +209,87 @@ __global__ void __launch_bounds__(NTP) shard_partial_kernel(ShardArgs a, float c
       }
       float4* o = reinterpret_cast<float4*>(a.partials) + 2 * ((int64_t)s * a.T + r);
       o[0] = make_float4(st.m, st.hi, st.lo, st.u);
-      o[1] = make_float4(zy, 0.f, 0.f, 0.f);
+      o[1] = make_float4(zy, isnan(zy) ? 0.f : 1.f, 0.f, 0.f);   // every column is in S
+    }
+  }
+}
+
+// Fold one value into a lane's state.
+__device__ __forceinline__ void part_absorb1(Part& st, float z, float c) {
+  if (!isfinite(z)) {
+    st.u = NAN;
+    return;
+  }
+  if (z > st.m) {
+    if (st.m != -INFINITY) {
+      const float delta = __fmul_rn(__fsub_rn(z, st.m), c);
+      const float f = ex2(-delta);
+      st.u = __fmul_rn(f, __fmaf_rn(-delta, __fadd_rn(st.hi, st.lo), st.u));
+      st.hi = __fmul_rn(st.hi, f);
+      st.lo = __fmul_rn(st.lo, f);
+    }
+    st.m = z;
+  }
+  const float d = __fmul_rn(__fsub_rn(z, st.m), c);
+  const float w = ex2(d);
+  float s, e;
+  two_sum(st.hi, w, s, e);
+  st.hi = s;
+  st.lo = __fadd_rn(st.lo, e);
+  st.u = __fmaf_rn(w, d, st.u);
+}
+
+// The retained set supplied by the sampler (CSR), under the same partition:
+// one warp per (row, shard); lane l takes list positions l, l + 32, ... and
+// keeps those in the shard's columns.  The list's checks (empty, decreasing
+// offsets, an id outside [0, V)) are the row's, made by every shard alike.
+__global__ void __launch_bounds__(NTP) shard_support_partial_kernel(ShardArgs a, float c) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t n_pairs = a.T * (int64_t)a.n_shards;
+  const int64_t nwarps = (int64_t)gridDim.x * NWP;
+  for (int64_t pr = (int64_t)blockIdx.x * NWP + warp; pr < n_pairs; pr += nwarps) {
+    const int64_t r = pr / a.n_shards;
+    const int s = (int)(pr % a.n_shards);
+    const int64_t g0 = a.first_col + (int64_t)s * a.shard_width;   // global columns [g0, g1)
+    int64_t g1 = g0 + a.shard_width;
+    if (g1 > a.V) g1 = a.V;
+    const int64_t j0 = a.offsets[r], j1 = a.offsets[r + 1];
+    const int64_t y = a.ids[r];
+    Part st{-INFINITY, 0.f, 0.f, 0.f};
+    uint32_t bad = j1 <= j0 ? RLK_STATUS_BAD_SUPPORT : 0u;
+    bool y_here = false;
+    for (int64_t j = j0 + lane; j < j1; j += 32) {
+      const int64_t id = a.support[j];
+      if (id < 0 || id >= a.V) {
+        bad |= RLK_STATUS_BAD_SUPPORT;
+        continue;
+      }
+      if (id < g0 || id >= g1) continue;
+      const int64_t col = (id - a.first_col);
+      const float z = a.dtype == 0
+                          ? bf16_val(__ldg(reinterpret_cast<const uint16_t*>(a.logits) + r * a.ld + col))
+                          : __ldg(reinterpret_cast<const float*>(a.logits) + r * a.ld + col);
+      part_absorb1(st, z, c);
+      if (id == y) y_here = true;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const Part x{shfl_down(st.m, o), shfl_down(st.hi, o), shfl_down(st.lo, o), shfl_down(st.u, o)};
+      st = part_merge(st, x, c);
+    }
+    bad = __reduce_or_sync(0xFFFFFFFFu, bad);
+    y_here = __any_sync(0xFFFFFFFFu, y_here);
+    if (lane == 0) {
+      float zy = NAN;
+      if (y_here) {
+        const int64_t col = y - a.first_col;
+        zy = a.dtype == 0
+                 ? bf16_val(reinterpret_cast<const uint16_t*>(a.logits)[r * a.ld + col])
+                 : reinterpret_cast<const float*>(a.logits)[r * a.ld + col];
+      }
+      float4* o = reinterpret_cast<float4*>(a.partials) + 2 * ((int64_t)s * a.T + r);
+      o[0] = make_float4(st.m, st.hi, st.lo, st.u);
+      o[1] = make_float4(zy, y_here ? 1.f : 0.f, __uint_as_float(bad), 0.f);
     }
   }
 }
@@ -231,17 +311,23 @@ __global__ void __launch_bounds__(256) shard_combine_kernel(ShardCombineArgs a, 
     const float4 q = p[2 * ((int64_t)s * a.T + r)];
     st = part_merge(st, Part{q.x, q.y, q.z, q.w}, c);
   }
+  uint32_t bad = 0u;   // status bits the shards raised (a supplied list's checks)
+  for (int s = 0; s < a.n_shards; ++s) bad |= __float_as_uint(p[2 * ((int64_t)s * a.T + r) + 1].z);
   const int ys = (int)(y / a.shard_width);
-  const float zy = ys < a.n_shards ? p[2 * ((int64_t)ys * a.T + r) + 1].x : NAN;
+  const float4 py = ys < a.n_shards ? p[2 * ((int64_t)ys * a.T + r) + 1] : make_float4(NAN, 0.f, 0.f, 0.f);
+  const bool y_in = py.y > 0.5f;   // the selected id is in the scored set
   const float zf = __fadd_rn(st.hi, st.lo);
-  if (!(isfinite(zf) && isfinite(st.u) && isfinite(st.m) && isfinite(zy))) {
+  if (!bad && !(isfinite(zf) && isfinite(st.u) && isfinite(st.m) && (!y_in || isfinite(py.x))))
+    bad = RLK_STATUS_NONFINITE;
+  if (bad) {
     a.out_logprob[r] = NAN;
     a.out_entropy[r] = NAN;
-    if (a.status) atomicOr(a.status, RLK_STATUS_NONFINITE);
+    if (a.status) atomicOr(a.status, bad);
     return;
   }
   const float lz = logf(zf);
-  a.out_logprob[r] = __fsub_rn(__fdiv_rn(__fsub_rn(zy, st.m), a.temperature), lz);
+  a.out_logprob[r] = y_in ? __fsub_rn(__fdiv_rn(__fsub_rn(py.x, st.m), a.temperature), lz)
+                          : -INFINITY;
   a.out_entropy[r] = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, st.u), zf));
 }
 
@@ -253,6 +339,15 @@ cudaError_t launch_shard_partials(const ShardArgs& a, cudaStream_t stream) {
   const int64_t blocks = (n_pairs + NWP - 1) / NWP;
   const int64_t cap = (int64_t)8 * sm_count();
   shard_partial_kernel<<<(unsigned)(blocks < cap ? blocks : cap), NTP, 0, stream>>>(a, c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_support_partials(const ShardArgs& a, cudaStream_t stream) {
+  const float c = (float)(1.4426950408889634 / (double)a.temperature);
+  const int64_t n_pairs = a.T * (int64_t)a.n_shards;
+  const int64_t blocks = (n_pairs + NWP - 1) / NWP;
+  const int64_t cap = (int64_t)8 * sm_count();
+  shard_support_partial_kernel<<<(unsigned)(blocks < cap ? blocks : cap), NTP, 0, stream>>>(a, c);
   return cudaGetLastError();
 }
 

@@ -648,6 +648,27 @@ rlk_status rlk_shard_partials(const void* logits, rlk_dtype dtype, int64_t T, in
                               rlk_shard_partial* out_partials, rlk_stream stream);
 
 /*
+ * rlk_shard_partials_support -- rlk_shard_partials over a retained set
+ * supplied by the sampler (CSR, as rlk_logprob_entropy_support): the top_p < 1
+ * rows of the pages' sparse path under the canonical partition.  Each shard
+ * folds the listed ids that fall in its columns; combined by
+ * rlk_shard_combine, the result is rlk_logprob_entropy_support's, and
+ * bitwise the same for any number of ranks.  Every shard checks the row's
+ * list (empty, decreasing offsets, an id outside [0, V)) and the combine
+ * reports RLK_STATUS_BAD_SUPPORT for it; a selected id that is not listed
+ * gives a log-probability of -inf.
+ *
+ * Arguments as rlk_shard_partials, plus support_offsets (device int64[T + 1])
+ * and support_ids (device int32[support_offsets[T]], global ids).
+ */
+rlk_status rlk_shard_partials_support(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                      int64_t ld, int64_t first_col, int64_t shard_width,
+                                      int32_t n_shards, const int32_t* token_ids,
+                                      float temperature, const int64_t* support_offsets,
+                                      const int32_t* support_ids,
+                                      rlk_shard_partial* out_partials, rlk_stream stream);
+
+/*
  * rlk_shard_combine -- log-probability and entropy from all shards' partials,
  * merged in shard order.
  *
@@ -655,7 +676,8 @@ rlk_status rlk_shard_partials(const void* logits, rlk_dtype dtype, int64_t T, in
  *                  ranks' outputs gathered in rank order).
  *  n_shards, shard_width  with n_shards W >= V.
  * Data errors as rlk_logprob_entropy (NaN outputs, RLK_STATUS_BAD_TOKEN_ID or
- * RLK_STATUS_NONFINITE).
+ * RLK_STATUS_NONFINITE), plus the status bits the partials carry
+ * (RLK_STATUS_BAD_SUPPORT from rlk_shard_partials_support).
  */
 rlk_status rlk_shard_combine(const rlk_shard_partial* partials, int32_t n_shards, int64_t T,
                              int64_t V, int64_t shard_width, const int32_t* token_ids,

@@ -19,7 +19,9 @@ pytestmark = pytest.mark.gpu
 
 def _check(lp, ent, olp, oent):
     lp, ent = lp.cpu().numpy().astype(np.float64), ent.cpu().numpy().astype(np.float64)
-    assert np.all(np.abs(lp - olp) <= LP_TOL + LP_REL * np.abs(olp))
+    assert np.array_equal(np.isneginf(lp), np.isneginf(olp))     # -inf: y outside the set
+    fin = ~np.isneginf(olp)
+    assert np.all(np.abs(lp[fin] - olp[fin]) <= LP_TOL + LP_REL * np.abs(olp[fin]))
     assert np.all(np.abs(ent - oent) <= ENT_TOL)
 
 
@@ -94,3 +96,54 @@ def test_canonical_bad_rows(cuda_lib):
     bad = torch.isnan(lp).cpu().tolist()
     assert bad == [False, True, True, True, False, True]
     assert int(st.item()) == cuda_lib.STATUS_BAD_TOKEN_ID | cuda_lib.STATUS_NONFINITE
+
+
+def _csr(lists):
+    off = np.concatenate([[0], np.cumsum([len(l) for l in lists])]).astype(np.int64)
+    return off, np.concatenate(lists).astype(np.int32)
+
+
+def test_supplied_support_under_the_partition(cuda_lib, oracle):
+    """top_p < 1 rows as the sampler ships them (a retained set per row), under
+    the canonical partition: against the supplied-support oracle, and the same
+    bits for 1, 2, 4 and 8 emulated ranks.  Rows whose selected id is not
+    listed get -inf; a bad list is flagged."""
+    R, V = 32, workloads.VOCAB
+    z, _ = workloads.peaked_bf16(R, V=V, seed=61, device="cuda")
+    hz = workloads.bf16_bits(z)
+    ids = oracle.sample_ids(hz, 0.7, 0.95, workloads.uniforms(R, 9))
+    _, _, k, _ = oracle.logprob_entropy(hz, ids, 0.7, 0.95)
+    vals = (hz.astype(np.uint32) << 16).view(np.float32)
+    rng = np.random.default_rng(3)
+    lists = [rng.permutation(np.lexsort((np.arange(V), -vals[r]))[:k[r]]) for r in range(R)]
+    ids[5] = np.setdiff1d(np.arange(V), lists[5])[0]          # not listed
+    off, sup = _csr(lists)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    tid = d(ids)
+    ref = None
+    for tp in (1, 2, 4, 8):
+        parts = []
+        for rank in range(tp):
+            _, n, c0, w = cuda_lib.canonical_plan(tp, rank)
+            local = z[:, c0:min(c0 + n * w, V)]
+            parts.append(cuda_lib.shard_partials_support(local, tid, 0.7, V, c0, w, n, d(off),
+                                                         d(sup)))
+        lp, ent = cuda_lib.shard_combine(torch.cat(parts, 0), tid, 0.7, V, w)
+        torch.cuda.synchronize()
+        if ref is None:
+            ref = (lp, ent)
+        else:
+            assert torch.equal(lp, ref[0]) and torch.equal(ent, ref[1]), tp
+    olp, oent, st = oracle.logprob_entropy_support(hz, ids, 0.7, off, sup)
+    _check(ref[0], ref[1], olp, oent)
+    assert np.isneginf(ref[0].cpu().numpy()[5]) and np.isneginf(olp[5])
+    # a bad list: an empty row and an id out of range
+    lists2 = [lists[0], np.array([], np.int64), np.array([3, V + 7])]
+    off2, sup2 = _csr(lists2)
+    stw = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p2 = cuda_lib.shard_partials_support(z[:3].contiguous(), tid[:3].contiguous(), 0.7, V, 0,
+                                         19072, 8, d(off2), d(sup2))
+    lp2, _ = cuda_lib.shard_combine(p2, tid[:3].contiguous(), 0.7, V, 19072, status_word=stw)
+    torch.cuda.synchronize()
+    assert torch.isnan(lp2).cpu().tolist() == [False, True, True]
+    assert int(stw.item()) == cuda_lib.STATUS_BAD_SUPPORT
