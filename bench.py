@@ -627,7 +627,10 @@ def run_sample(args, ws, rank, dev, barrier):
                    "global_batch": T_ROWS * ws,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peak_kind,
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic(os.path.join(CSRC, "sampler.cu"),
+                                                 os.path.join(PROFILES, "sample_kernel_qwen_T4096.txt")),
+                     "peak_source": peak_kind,
                      "kernel": "sample_kernel (one rlk_sample_top_p call; rows re-read when a tie "
                                "must be resolved)",
                      "algorithmic_bytes_per_launch": alg, "launch_ms": part_ms[0]},
