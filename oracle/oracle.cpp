@@ -797,10 +797,14 @@ int oracle_lmhead_backward(const uint16_t* hidden, const uint16_t* w_vocab, int6
     }
     score_row(z, ids[row], Td, pd, 0, g_lp ? static_cast<double>(g_lp[row]) : 0.0,
               g_h ? static_cast<double>(g_h[row]) : 0.0, dz.data() + row * V);
-    for (int64_t k = 0; k < H; ++k) {
-      double acc = 0.0;
-      for (int64_t i = 0; i < V; ++i) acc += dz[row * V + i] * bf16_to_double(w_vocab[i * H + k]);
-      out_dh[row * H + k] = acc;
+    // every out_dh[row, k] accumulates over i = 0, 1, ..., V-1 from 0; the
+    // vocabulary loop is outermost so that W is read row by row
+    double* dh = out_dh + row * H;
+    for (int64_t k = 0; k < H; ++k) dh[k] = 0.0;
+    for (int64_t i = 0; i < V; ++i) {
+      const double d = dz[row * V + i];
+      const uint16_t* wr = w_vocab + i * H;
+      for (int64_t k = 0; k < H; ++k) dh[k] += d * bf16_to_double(wr[k]);
     }
   });
   parallel_rows(V, nthreads, [&](int64_t i) {

@@ -6,6 +6,10 @@
 2. The fused outputs against the fp64 oracle (exact dot products, logits never
    rounded to bf16) on sampled rows: |dlogprob|, |dentropy| <= 2e-4.
 3. Bitwise repeatability and batch-size invariance.
+4. top_p < 1 (logits emitted as bf16 and scored by the top-p path): bit for
+   bit the scorer's outputs on the GEMM's own logits, and against the oracle
+   on inputs whose product is exact in fp32, where the oracle's bf16 logits
+   are a CPU library product rounded to nearest even.
 """
 import numpy as np
 import pytest
@@ -79,24 +83,49 @@ def test_lmhead_bad_ids(cuda_lib):
 
 @pytest.mark.parametrize("T,H,V,p", [(300, 256, 20000, 0.9), (4500, 128, 8192, 0.95),
                                      (130, 4096, 151936, 0.95)])
-def test_lmhead_top_p_chunked(cuda_lib, oracle, T, H, V, p):
+def test_lmhead_top_p_chunked_same_bits_as_the_scorer(cuda_lib, T, H, V, p):
     """top_p < 1: the GEMM emits bf16 logits chunk by chunk and the top-p path
-    scores them.  Against the oracle on the GEMM's own logits rounded to bf16
-    (the GEMM core is checked against a library product above), and bit for
-    bit against rlk_logprob_entropy on those logits (V % 8 == 0: same layout).
-    The second shape spans two 4096-row chunks."""
+    scores them; the outputs are bit for bit those of rlk_logprob_entropy on
+    the GEMM's own logits rounded to bf16 (V % 8 == 0: same layout).  The
+    second shape spans two 4096-row chunks."""
     hidden, w, ids = workloads.lmhead_inputs(T, H, V, seed=12, device="cuda")
     w = (w.float() * (8.0 if H <= 256 else 1.5)).to(torch.bfloat16)   # peaked enough for a nucleus
     lp, ent = cuda_lib.lmhead_logprob(hidden, w, ids, 0.7, p)
     logits, _, _ = cuda_lib.lmhead_logits_debug(hidden, w, ids, 0.7)
-    zb = logits.to(torch.bfloat16)
-    dlp, dent = cuda_lib.logprob_entropy(zb, ids, 0.7, p)
+    dlp, dent = cuda_lib.logprob_entropy(logits.to(torch.bfloat16), ids, 0.7, p)
     torch.cuda.synchronize()
     assert torch.equal(lp, dlp) and torch.equal(ent, dent)
-    olp, oent, ok, gap = oracle.logprob_entropy(workloads.bf16_bits(zb), ids.cpu().numpy(), 0.7, p)
+
+
+@pytest.mark.parametrize("T,H,V,p,s,L", [(300, 256, 20000, 0.9, 7, 7),
+                                         (4500, 128, 8192, 0.95, 2, 1),
+                                         (130, 4096, 151936, 0.95, 4, 1)])
+def test_lmhead_top_p_against_oracle(cuda_lib, oracle, T, H, V, p, s, L):
+    """top_p < 1 against the oracle on inputs whose product is exact in fp32
+    in any summation order (hidden in {-L..L}, W in {-L..L} 2^-s): the
+    oracle's logits are a CPU library product of the same bf16 values,
+    rounded to bf16 to nearest even as the emit step rounds (a fifth of the
+    logits of the first shape need rounding; the others fit bf16); then the
+    fp64 logits path.  Nothing on the oracle side comes from the GPU.  The
+    full-vocabulary shape has broad rows (median nucleus ~3000): rows whose
+    boundary gap is below 1e-6 are not compared."""
+    hidden, w, ids = workloads.lmhead_grid_inputs(T, H, V, seed=14, wshift=s, levels=L,
+                                                  device="cuda")
+    z = hidden.cpu().double() @ w.cpu().double().T                  # exact
+    hz = workloads.bf16_bits(z.float().to(torch.bfloat16))          # z is exact in fp32
+    ids_h = ids.cpu().numpy()
+    drawn = oracle.sample_ids(hz, 0.7, p, workloads.uniforms(T, 21))
+    ids_h[T // 4:] = drawn[T // 4:]                                 # a quarter keep uniform ids
+    ids = torch.from_numpy(ids_h).cuda()
+    lp, ent = cuda_lib.lmhead_logprob(hidden, w, ids, 0.7, p)
+    torch.cuda.synchronize()
+    olp, oent, ok, gap = oracle.logprob_entropy(hz, ids_h, 0.7, p)
     sure = gap > 1e-6
+    assert sure.mean() > 0.75
     lp_, ent_ = lp.cpu().numpy().astype(np.float64), ent.cpu().numpy().astype(np.float64)
     assert np.array_equal(np.isneginf(lp_[sure]), np.isneginf(olp[sure]))
     fin = sure & ~np.isneginf(olp)
     assert np.all(np.abs(lp_[fin] - olp[fin]) <= 2e-4 + 2e-7 * np.abs(olp[fin]))
     assert np.all(np.abs(ent_[sure] - oent[sure]) <= 2e-4)
+    assert np.median(ok) > 1                                        # real nuclei, not one token
+    assert fin.sum() > T // 2                       # most ids drawn inside the nucleus

@@ -163,3 +163,28 @@ def lmhead_inputs(T: int, H: int, V: int, seed: int = 4, device="cpu"):
         g = _gen(seed + 500, r // 8192, device)
         w[r:r + n] = (torch.randn(8192, H, generator=g, device=device)[:n] * 0.02).to(torch.bfloat16)
     return hidden, w, uniform_ids(T, V, seed, device)
+
+
+def lmhead_grid_inputs(T: int, H: int, V: int, seed: int = 6, wshift: int = 4, levels: int = 1,
+                       device="cpu"):
+    """hidden and W on small integer grids: hidden uniform in {-L, ..., L},
+    W uniform in {-L, ..., L} * 2^-wshift (L = levels), ids uniform.  Every
+    partial sum of a dot product is a multiple of 2^-wshift of magnitude at
+    most H L^2 2^-wshift (below 2^24 of those steps here), exact in fp32
+    whatever the summation order, so a tensor-core product and a library
+    product give the same logits bit for bit.  z has standard deviation
+    sqrt(H) (L (L + 1) / 3) 2^-wshift; once |z| 2^wshift passes 256 the
+    logits no longer fit bf16 and rounding them is exercised."""
+    hidden = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    for r in range(0, T, BLOCK_ROWS):
+        n = min(BLOCK_ROWS, T - r)
+        g = _gen(seed, r // BLOCK_ROWS, device)
+        hidden[r:r + n] = torch.randint(-levels, levels + 1, (BLOCK_ROWS, H), generator=g,
+                                        device=device)[:n].to(torch.bfloat16)
+    w = torch.empty(V, H, dtype=torch.bfloat16, device=device)
+    for r in range(0, V, 8192):
+        n = min(8192, V - r)
+        g = _gen(seed + 700, r // 8192, device)
+        w[r:r + n] = (torch.randint(-levels, levels + 1, (8192, H), generator=g,
+                                    device=device)[:n].float() * 2.0 ** -wshift).to(torch.bfloat16)
+    return hidden, w, uniform_ids(T, V, seed, device)
