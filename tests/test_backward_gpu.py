@@ -2,8 +2,10 @@
 the top-p log-probability and entropy, retained sets held fixed) through the
 C ABI against the fp64 oracle.
 
-The oracle evaluates each row at the forward's own k* (force_k), so both
-sides hold the same set even on rows whose boundary gap is below rounding;
+The forward's k* is checked against the oracle's (equal, or on rows whose
+boundary gap is below rounding, one the oracle selects at a top_p within
+1e-6); the oracle then evaluates each row at that k* (force_k), so both
+sides hold the same set;
 the set itself is checked exactly: every id outside it (found here by an
 independent sort) must get a gradient of exactly 0.
 
@@ -17,6 +19,7 @@ import pytest
 import torch
 
 import workloads
+from _parity import check_nucleus_sizes
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +75,7 @@ def test_backward_matches_oracle_bf16(cuda_lib, oracle, T, p, V, pad):
     glp, gh = rng.uniform(-3, 3, R), rng.uniform(-3, 3, R)
     out = torch.full((R, V + 7), 123.0, device="cuda")[:, :V] if pad else None
     g, k, _ = _run(cuda_lib, z, ids, T, p, glp, gh, out=out)
+    check_nucleus_sizes(oracle, hz, ids, T, p, k)
     og = oracle.logprob_entropy_backward(hz, ids, T, p, glp.astype(np.float32),
                                          gh.astype(np.float32), force_k=k)
     _check(g, og, _vals(hz), k, label=f"V{V} pad{pad}")
@@ -92,6 +96,7 @@ def test_backward_full_vocab_cluster_rows(cuda_lib, oracle, p):
     ids = oracle.sample_ids(hz, T, p, workloads.uniforms(R, 5))
     glp, gh = rng.uniform(-2, 2, R), rng.uniform(-2, 2, R)
     g, k, _ = _run(cuda_lib, z, ids, T, p, glp, gh)
+    check_nucleus_sizes(oracle, hz, ids, T, p, k)
     og = oracle.logprob_entropy_backward(hz, ids, T, p, glp.astype(np.float32),
                                          gh.astype(np.float32), force_k=k)
     _check(g, og, _vals(hz), k, label="cluster fp32 grads")
@@ -112,6 +117,7 @@ def test_backward_fp32_logits(cuda_lib, oracle, p):
     ids = oracle.sample_ids(hz, T, p, workloads.uniforms(R, 9))
     glp, gh = rng.uniform(-3, 3, R), rng.uniform(-3, 3, R)
     g, k, _ = _run(cuda_lib, z, ids, T, p, glp, gh)
+    check_nucleus_sizes(oracle, hz, ids, T, p, k)
     og = oracle.logprob_entropy_backward(hz, ids, T, p, glp.astype(np.float32),
                                          gh.astype(np.float32), force_k=k)
     _check(g, og, hz, k, label="fp32 logits")
@@ -129,6 +135,7 @@ def test_backward_split_ties_at_the_boundary(cuda_lib, oracle):
     ids = rng.integers(0, V, R).astype(np.int32)
     glp, gh = rng.uniform(-1, 1, R), rng.uniform(-1, 1, R)
     g, k, st = _run(cuda_lib, z, ids, T, p, glp, gh)
+    check_nucleus_sizes(oracle, hz, ids, T, p, k)
     og = oracle.logprob_entropy_backward(hz, ids, T, p, glp.astype(np.float32),
                                          gh.astype(np.float32), force_k=k)
     _check(g, og, vals, k, label="split ties")

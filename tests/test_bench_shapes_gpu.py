@@ -16,7 +16,7 @@ import torch
 
 import bench
 import workloads
-from _parity import ENT_TOL, LP_REL, LP_TOL
+from _parity import ENT_TOL, LP_REL, LP_TOL, check_nucleus_sizes
 from test_backward_gpu import _check as check_dense_grad
 from test_sampler_gpu import _check as check_draws
 
@@ -59,6 +59,7 @@ def test_dense_backward_bench_shape(cuda_lib, oracle, batch):
     rows = _rows(3 * 152, extra=(455, 911, 912, 3000))
     tr = torch.from_numpy(rows).cuda()
     hz = workloads.bf16_bits(z[tr])
+    check_nucleus_sizes(oracle, hz, ids.cpu().numpy()[rows], TEMP, P, k[rows])
     og = oracle.logprob_entropy_backward(hz, ids.cpu().numpy()[rows], TEMP, P,
                                          glp.numpy()[rows], gh.numpy()[rows], force_k=k[rows])
     vals = (hz.astype(np.uint32) << 16).view(np.float32)

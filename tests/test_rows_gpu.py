@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import workloads
-from _parity import LP_REL, LP_TOL, ENT_TOL, GAP_EXEMPT
+from _parity import LP_REL, LP_TOL, ENT_TOL, GAP_EXEMPT, check_nucleus_sizes
 
 pytestmark = pytest.mark.gpu
 
@@ -94,6 +94,7 @@ def test_backward_and_sampler_follow_each_rows_temperature(cuda_lib, oracle):
     idn = ids.cpu().numpy()
     for i, (T_, p) in enumerate(PAIRS):
         rows = np.arange(i, R, len(PAIRS))
+        check_nucleus_sizes(oracle, hz[rows], idn[rows], T_, p, k[rows])
         og = oracle.logprob_entropy_backward(hz[rows], idn[rows], T_, p, glp[rows], gh[rows],
                                              force_k=k[rows])
         err = np.abs(g[rows] - og)
