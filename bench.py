@@ -210,15 +210,28 @@ def run_reference(args):
     hz = workloads.bf16_bits(z)
     hid = peaks.numpy().astype(np.int32)
     threads = oracle.default_threads()
-    for i in range(args.warmup):
+    # the loss stage on each step's log-probs, as in the device step: the
+    # sample's 64 tokens as 8 responses of 8 tokens in one group of 8;
+    # old / rollout / reference log-probs from the first sample's plus N(0, 0.01^2)
+    n_seq = rows_per_step // 8
+    off_h = (np.arange(n_seq + 1) * 8).astype(np.int32)
+    R_h = (np.random.default_rng(7).random(n_seq) < 0.5).astype(np.float32)
+    lp0, _, _, _ = oracle.logprob_entropy(hz[:rows_per_step], hid[:rows_per_step], TEMPERATURE,
+                                          TOP_P, threads=threads)
+    old_h, ro_h, ref_h = workloads.perturbed_logps(lp0.astype(np.float32), 5)
+
+    def step(i):
         s = (i % 4) * rows_per_step
-        oracle.logprob_entropy(hz[s:s + rows_per_step], hid[s:s + rows_per_step], TEMPERATURE,
-                               TOP_P, threads=threads)
+        lp, _, _, _ = oracle.logprob_entropy(hz[s:s + rows_per_step], hid[s:s + rows_per_step],
+                                             TEMPERATURE, TOP_P, threads=threads)
+        new = np.where(np.isfinite(lp), lp, old_h).astype(np.float32)
+        oracle.grpo_loss(new, old_h, ro_h, ref_h, None, R_h, off_h, 8)
+
+    for i in range(args.warmup):
+        step(i)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        s = (i % 4) * rows_per_step
-        oracle.logprob_entropy(hz[s:s + rows_per_step], hid[s:s + rows_per_step], TEMPERATURE,
-                               TOP_P, threads=threads)
+        step(i)
     dt = time.perf_counter() - t0
     value = rows_per_step * args.steps / dt
     line = {
@@ -228,7 +241,8 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "rows_per_step": rows_per_step, "V": VOCAB},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{rows_per_step} rows per step of the same workload"},
+                         "sample": f"{rows_per_step} rows per step of the same workload, then "
+                                   f"the loss on their log-probs"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
