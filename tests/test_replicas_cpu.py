@@ -113,3 +113,35 @@ def test_gather_shard_partials_in_canonical_order_over_two_gloo_ranks():
     for _, order, shape in res:
         assert order == [float(s) for s in range(8)]
         assert shape == (8, 5, 8)
+
+
+# ------------------------------------------------ the reference arm (the oracle on host cores)
+def _bench(args, env=None):
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    e = dict(os.environ)
+    e.update(env or {})
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], cwd=root, env=e,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_prints_the_contract_line():
+    import bench
+    (line,) = _bench(["--impl", "reference", "--steps", "1", "--warmup", "1"])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["steps"] == 1 and line["warmup"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    assert _bench(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1"],
+                  env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
