@@ -3,9 +3,10 @@ inputs ``bench.py`` builds, the calls it times), checked on sampled rows
 against the fp64 oracle, which computes a row on its own.
 
 The rows sampled include the first and the last, and rows on both sides of
-the grid-stride boundaries of the persistent kernels (760 CTAs for the
-sampler, 456 for the dense backward, 4096-row chunks for the LM-head), so the
-state a CTA carries from one row to the next is exercised.  Where the oracle
+the grid-stride boundaries of the persistent kernels on a 152-SM part (760
+CTAs for the sampler, 456 for the dense backward, 2432 for the supplied-support
+kernels, 4096-row chunks for the LM-head), so the state a CTA carries from one
+row to the next is exercised.  Where the oracle
 cannot compute one output alone (a row of dL/dW sums over all 16,384 tokens),
 a property that holds at any size stands in.  Tolerances are those of the
 per-leg tests.
@@ -94,7 +95,7 @@ def test_supplied_support_bench_shape(cuda_lib, oracle, batch):
     gh = torch.empty(T).uniform_(-1, 1, generator=g)
     grad = cuda_lib.logprob_entropy_support_backward(z, ids, TEMP, off, sup, glp.cuda(), gh.cuda())
     torch.cuda.synchronize()
-    rows = _rows(8 * 152, extra=range(0, T, 331))
+    rows = _rows(16 * 152, extra=range(0, T, 331))
     off_h, sup_h = off.cpu().numpy(), sup.cpu().numpy()
     o, s = _sub_csr(off_h, sup_h, rows)
     hz = workloads.bf16_bits(z[torch.from_numpy(rows).cuda()])
