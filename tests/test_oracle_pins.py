@@ -261,6 +261,44 @@ def test_sampler_draws_from_the_nucleus(oracle):
     assert np.array_equal(first, np.argmax(vals, axis=1).astype(np.int32))
 
 
+@pytest.mark.parametrize("T_,p", [(1.3, 0.95), (0.7, 0.6)])
+def test_sampler_frequencies_are_the_nucleus_masses(oracle, T_, p):
+    """One bf16 row (ties included) drawn at N evenly spaced u: each id's share
+    of the draws is its renormalised mass exp(logprob) from the scorer to within
+    1/N (each id owns an interval of u of that length), 0 off the nucleus; and
+    as u grows the drawn ids follow the ranking order (logit descending, lower
+    id first on ties) of a library sort."""
+    V, N = 300, 4000
+    bits = workloads.bf16_bits(workloads.normal_logits_fp32(1, V, 2.0, seed=9).to(torch.bfloat16))[0]
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    assert len(np.unique(vals)) < V                         # the row has ties
+    u = (np.arange(N) + 0.5) / N
+    ids = oracle.sample_ids(np.ascontiguousarray(np.repeat(bits[None, :], N, axis=0)), T_, p, u)
+    lp, _, k, _ = score_all_ids(oracle, bits, T_, p)
+    q = np.where(np.isfinite(lp), np.exp(lp), 0.0)
+    assert 1 < k[0] < V
+    freq = np.bincount(ids, minlength=V) / N
+    assert np.all(np.abs(freq - q) <= 1.0 / N + 1e-12)
+    order = np.lexsort((np.arange(V), -vals.astype(np.float64)))
+    rank = np.empty(V, np.int64)
+    rank[order] = np.arange(V)
+    assert np.all(np.diff(rank[ids]) >= 0)
+
+
+def test_sampler_uniform_row_closed_form(oracle):
+    """V = 32 equal logits, top_p = 1/4: the nucleus is ids 0..7 (every mass
+    1/32, exact), and u in the j-th eighth draws id j."""
+    rows = np.zeros((8, 32), np.float32)
+    ids = oracle.sample_ids(rows, 1.0, 0.25, (np.arange(8) + 0.5) / 8)
+    assert list(ids) == list(range(8))
+    ids = oracle.sample_ids(rows[:2], 1.0, 0.25, np.array([0.0, 0.999999]))
+    assert list(ids) == [0, 7]
+    # u on a boundary: the cumulative mass of ids 0..2 is exactly 3/8, so
+    # u = 3/8 is reached at id 2 (the first token whose cumulative reaches u)
+    ids = oracle.sample_ids(rows[:3], 1.0, 0.25, np.array([1 / 8, 3 / 8, 7 / 8]))
+    assert list(ids) == [0, 2, 6]
+
+
 # --------------------------------------------------------------------------
 # GRPO / DAPO loss: hand-worked values.
 # --------------------------------------------------------------------------
