@@ -749,13 +749,19 @@ def test_mis_normalises_and_is_scale_invariant(oracle):
 
 def test_length_weighted_baseline_and_prompt_mean(oracle):
     """Lengths 1 and 3, rewards 1 and 0: b = 0.25, sigma = 0.7071068, so
-    A = 0.75 / (sigma + 1e-6) and -0.25 / (sigma + 1e-6).  Prompt mean with one
+    A = 0.75 / (sigma + 1e-6) and -0.25 / (sigma + 1e-6); rewards 0 and 1:
+    b = 0.75.  Prompt mean with one
     group is the token mean; with groups of one it is the sequence mean."""
     z = np.log(np.full(4, 0.5, np.float32))
     _, _, adv, _ = oracle.policy_loss(z, z, z, z, None, np.array([1, 0], np.float32),
                                       [0, 1, 4], 2, baseline=oracle.BASELINE_LENGTH_WEIGHTED)
     s = np.sqrt(0.5) + 1e-6
     assert adv == pytest.approx([0.75 / s, -0.25 / s], rel=1e-12)
+    # rewards 0 and 1 on lengths 1 and 3: b = (1 * 0 + 3 * 1) / 4 = 0.75 (the
+    # unweighted sum of rewards over the total length would give 0.25)
+    _, _, adv, _ = oracle.policy_loss(z, z, z, z, None, np.array([0, 1], np.float32),
+                                      [0, 1, 4], 2, baseline=oracle.BASELINE_LENGTH_WEIGHTED)
+    assert adv == pytest.approx([-0.75 / s, 0.25 / s], rel=1e-12)
     new, old, ro, rf, mask, rew, off, G = _loss_batch(seed=7)
     n = len(rew)
     tok = oracle.policy_loss(new, old, ro, rf, mask, rew, off, n, agg=0)
