@@ -659,7 +659,8 @@ rlk_status rlk_shard_partials(const void* logits, rlk_dtype dtype, int64_t T, in
  * gives a log-probability of -inf.
  *
  * Arguments as rlk_shard_partials, plus support_offsets (device int64[T + 1])
- * and support_ids (device int32[support_offsets[T]], global ids).
+ * and support_ids (device int32[support_offsets[T]], global ids; may be NULL
+ * only when every row's list is empty, which is a data error per row).
  */
 rlk_status rlk_shard_partials_support(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
                                       int64_t ld, int64_t first_col, int64_t shard_width,

@@ -321,3 +321,64 @@ def test_binding_refuses_cpu_tensors(lib):
     ids = torch.zeros(2, dtype=torch.int32)
     with pytest.raises(ValueError):
         rlk.logprob_entropy(z, ids, 0.7, 0.95)
+
+
+@pytest.fixture
+def armed(lib):
+    """Host-side fault injection armed for the test: a call whose arguments
+    the host checks pass returns RLK_ERR_CUDA instead of launching, so the
+    placeholder pointers below can never reach a device."""
+    lib.rlk_debug_inject_launch_failures(1000)
+    yield
+    lib.rlk_debug_inject_launch_failures(0)
+
+
+def test_rows_rejects(lib, armed):
+    def rows(**kw):
+        a = dict(logits=FAKE, dtype=0, T=4, V=100, ld=100, ids=FAKE, temps=FAKE, tops=FAKE,
+                 lp=FAKE, ent=FAKE, state=None)
+        a.update(kw)
+        return lib.rlk_logprob_entropy_rows(a["logits"], a["dtype"], a["T"], a["V"], a["ld"],
+                                            a["ids"], a["temps"], a["tops"], a["lp"], a["ent"],
+                                            None, a["state"], None, None)
+    for kw in (dict(dtype=3), dict(T=-1), dict(V=0), dict(V=(1 << 24) + 1), dict(ld=99),
+               dict(logits=None), dict(ids=None), dict(temps=None), dict(tops=None),
+               dict(lp=None), dict(ent=None), dict(logits=ctypes.c_void_p(0x10001)),
+               dict(dtype=1, logits=ctypes.c_void_p(0x10002)),
+               dict(state=ctypes.c_void_p(0x10008))):
+        assert rows(**kw) == 1, kw
+    assert rows(T=0, logits=None, ids=None, temps=None, tops=None, lp=None, ent=None) == 0
+    assert rows() == 4 and rows(state=ctypes.c_void_p(0x10010)) == 4   # checks passed: injected
+
+
+def test_sample_top_p_rejects(lib, armed):
+    def smp(**kw):
+        a = dict(logits=FAKE, dtype=0, T=4, V=100, ld=100, temp=0.7, state=FAKE, u=FAKE,
+                 out=FAKE)
+        a.update(kw)
+        return lib.rlk_sample_top_p(a["logits"], a["dtype"], a["T"], a["V"], a["ld"], a["temp"],
+                                    a["state"], a["u"], a["out"], None, None)
+    for kw in (dict(dtype=3), dict(T=-1), dict(V=0), dict(ld=99), dict(temp=0.0),
+               dict(temp=math.inf), dict(temp=math.nan), dict(logits=None), dict(state=None),
+               dict(u=None), dict(out=None), dict(logits=ctypes.c_void_p(0x10001)),
+               dict(state=ctypes.c_void_p(0x10008))):
+        assert smp(**kw) == 1, kw
+    assert smp(dtype=1) == 2                                  # fp32 logits: not supported
+    assert smp(T=0, logits=None, state=None, u=None, out=None) == 0
+    assert smp() == 4                                          # checks passed: injected
+
+
+def test_shard_partials_support_rejects(lib, armed):
+    def part(**kw):
+        a = dict(dtype=0, T=4, V=1000, ld=1000, first=0, W=125, n=8, temp=0.7, off=FAKE,
+                 out=FAKE)
+        a.update(kw)
+        return lib.rlk_shard_partials_support(FAKE, a["dtype"], a["T"], a["V"], a["ld"],
+                                              a["first"], a["W"], a["n"], FAKE, a["temp"],
+                                              a["off"], FAKE, a["out"], None)
+    for kw in (dict(W=0), dict(n=0), dict(first=-125), dict(first=100), dict(ld=999),
+               dict(dtype=7), dict(temp=0.0), dict(off=None), dict(out=None),
+               dict(out=ctypes.c_void_p(0x10008)), dict(V=0)):
+        assert part(**kw) == 1, kw
+    assert part(T=0, off=None, out=None) == 0
+    assert part() == 4                                         # checks passed: injected
