@@ -7,7 +7,6 @@
   sentinel; after the call the sentinel must be intact outside the output
   (no write lands outside what the ABI says is written).
 """
-import numpy as np
 import pytest
 import torch
 
