@@ -145,3 +145,17 @@ def test_reference_arm_prints_the_contract_line():
 def test_reference_arm_runs_on_rank_zero_only():
     assert _bench(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1"],
                   env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
+
+
+def test_peaks_file_and_fallback(tmp_path, monkeypatch):
+    import json
+    import bench
+    peaks, kind = bench.measured_peaks()
+    if os.path.exists(os.path.join(bench.ROOT, "MEASURED_PEAKS.json")):
+        assert kind == "measured" and peaks["hbm_gbs"] > 0
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))          # no file there
+    peaks, kind = bench.measured_peaks()
+    assert kind == "fallback"
+    assert peaks == {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 1.0, "bf16_tflops": 2.0}))
+    assert bench.measured_peaks() == ({"hbm_gbs": 1.0, "bf16_tflops": 2.0}, "measured")
