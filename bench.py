@@ -240,10 +240,14 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "rows_per_step": rows_per_step, "V": VOCAB},
+        "config": {"workload": WORKLOAD, "T": T_ROWS, "V": VOCAB, "temperature": TEMPERATURE,
+                   "top_p": TOP_P, "global_batch": T_ROWS, "loss": LOSS_CFG,
+                   "parallelism": "host cores, rank 0 only",
+                   "rows_per_step": rows_per_step},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows_per_step} rows per step of the same workload, then "
-                                   f"the loss on their log-probs"},
+                                   f"the loss on their log-probs ({n_seq} responses x 8 tokens, "
+                                   f"groups of 8)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
