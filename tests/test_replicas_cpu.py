@@ -96,10 +96,10 @@ def _gather_worker(rank, ws, port, q):
         dist.destroy_process_group()
 
 
-def test_gather_shard_partials_in_canonical_order_over_two_gloo_ranks():
+@pytest.mark.parametrize("ws", [2, 4])
+def test_gather_shard_partials_in_canonical_order_over_gloo_ranks(ws):
     """The vocabulary-parallel exchange: every rank ends with all eight shards'
-    partials in shard order, whatever rank computed them."""
-    ws = 2
+    partials in shard order, whatever rank computed them (TP 2 and TP 4)."""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
