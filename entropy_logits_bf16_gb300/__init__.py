@@ -53,7 +53,8 @@ EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logpro
            "rlk_logprob_entropy_canonical", "rlk_sample_top_p",
            "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
-DEBUG_EXPORTS = ("rlk_lmhead_logits_debug", "rlk_debug_inject_launch_failures")
+DEBUG_EXPORTS = ("rlk_lmhead_logits_debug", "rlk_debug_inject_launch_failures",
+                 "rlk_debug_set_wait_limit", "rlk_debug_withhold_copy")
 STATUS_TIMEOUT = 0x4
 STATUS_BAD_SUPPORT = 0x8
 STATUS_NO_STATE = 0x10
@@ -123,6 +124,10 @@ def load(path: str | None = None):
         lib.rlk_sample_top_p.restype = ctypes.c_int
         lib.rlk_debug_inject_launch_failures.argtypes = [ctypes.c_int]
         lib.rlk_debug_inject_launch_failures.restype = ctypes.c_int
+        lib.rlk_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
+        lib.rlk_debug_set_wait_limit.restype = ctypes.c_longlong
+        lib.rlk_debug_withhold_copy.argtypes = [ctypes.c_longlong]
+        lib.rlk_debug_withhold_copy.restype = ctypes.c_int
         lib.rlk_shard_partials.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, i64, i32, vp, f32,
                                            vp, vp]
         lib.rlk_shard_partials.restype = ctypes.c_int
@@ -729,3 +734,17 @@ def inject_launch_failures(n: int) -> int:
     return RLK_ERR_CUDA (raised as RlkError) without launching.  Returns the
     count that was pending."""
     return int(load().rlk_debug_inject_launch_failures(int(n)))
+
+
+def set_wait_limit(cycles: int) -> int:
+    """Debug: the clock cycles a bounded device wait may take before it gives
+    up (<= 0 restores the default of about a second).  Returns the previous
+    limit."""
+    return int(load().rlk_debug_set_wait_limit(int(cycles)))
+
+
+def withhold_copy(stage: int) -> None:
+    """Debug: the next scorer (or LM-head forward) launch skips the bulk copy
+    of the given stage in its first CTA, so the wait on it runs out; < 0
+    clears it."""
+    load().rlk_debug_withhold_copy(int(stage))

@@ -39,7 +39,8 @@ constexpr int NP = kLossPartials;  // partial sums per sequence, see below
 // Partial slots: 0 sum m l (MIS: sum m kl_coef k3 only), 1 sum m, 2 clip-low
 // count, 3 clip-high count, 4 sum m w (MIS: sum m raw), 5 capped count,
 // 6 sum m k3, 7 sum m pg, 8 count dropped by the IPO / IcePop mask,
-// 9 sum m raw pg (MIS), 10 the sequence's advantage, 11 unused.
+// 9 sum m raw pg (MIS), 10 the sequence's advantage, 11 1 when the
+// sequence's offsets are out of order or outside the n_tok packed tokens.
 // Scalars after the partials: 0 1 / sum m, 1 live aggregation units,
 // 2 the importance-weight scale (1 / mean raw for MIS, else 1).
 
@@ -86,6 +87,20 @@ __device__ __forceinline__ float is_weight(const LossArgs& a, float raw) {
   return a.is_method == RLK_IS_TIS ? fminf(raw, a.tis_cap) : 1.f;
 }
 
+// Sequence s's packed tokens [t0, t1), clamped to the n_tok tokens that start
+// at seq_offsets[0]; returns whether the offsets were valid (non-decreasing
+// and inside that range).  Invalid offsets make the loss NaN, and no token
+// outside the range is read or written.
+__device__ __forceinline__ bool seq_range(const LossArgs& a, int s, int64_t& t0, int64_t& t1) {
+  const int64_t base = a.seq_offsets[0], lim = base + a.n_tok;
+  t0 = a.seq_offsets[s];
+  t1 = a.seq_offsets[s + 1];
+  const bool ok = t0 >= base && t1 >= t0 && t1 <= lim;
+  t0 = t0 < base ? base : (t0 > lim ? lim : t0);
+  t1 = t1 < t0 ? t0 : (t1 > lim ? lim : t1);
+  return ok;
+}
+
 __global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
   __shared__ float s_adv;
   __shared__ float s_red[LWARP][NP];
@@ -122,7 +137,8 @@ __global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
     }
     __syncthreads();
     const float A = s_adv;
-    const int64_t t0 = a.seq_offsets[s], t1 = a.seq_offsets[s + 1];
+    int64_t t0, t1;
+    const bool range_ok = seq_range(a, s, t0, t1);
     float acc[NP];
 #pragma unroll
     for (int k = 0; k < NP; ++k) acc[k] = 0.f;
@@ -162,7 +178,7 @@ __global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
     if (tid < NP) {
       float v = 0.f;
       for (int w2 = 0; w2 < LWARP; ++w2) v += s_red[w2][tid];
-      a.workspace[(int64_t)s * NP + tid] = tid == 10 ? A : v;
+      a.workspace[(int64_t)s * NP + tid] = tid == 10 ? A : (tid == 11 ? (range_ok ? 0.f : 1.f) : v);
     }
     __syncthreads();
   }
@@ -248,9 +264,11 @@ __global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
     float L;
     if (a.agg == RLK_AGG_TOKEN_MEAN) L = M > 0.f ? __fdiv_rn(v[0], M) : 0.f;
     else L = v[1] > 0.f ? __fdiv_rn(v[0], v[1]) : 0.f;
+    const bool bad_offsets = s_t[11] != 0.f;   // some sequence's offsets were invalid
+    if (bad_offsets) L = NAN;
     *a.out_loss = L;
     if (a.out_stats) {
-      const float d = M > 0.f ? M : 1.f;
+      const float d = bad_offsets ? NAN : (M > 0.f ? M : 1.f);
       a.out_stats[RLK_STAT_LOSS] = L;
       a.out_stats[RLK_STAT_TOKENS] = M;
       a.out_stats[RLK_STAT_CLIP_LOW] = __fdiv_rn(s_t[2], d);
@@ -263,8 +281,8 @@ __global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
         a.out_stats[RLK_STAT_MASK_DROPPED] = __fdiv_rn(s_t[8], d);
     }
     float* sc = a.workspace + (int64_t)a.n_seq * NP;
-    sc[0] = M > 0.f ? __fdiv_rn(1.f, M) : 0.f;   // token-mean weight
-    sc[1] = v[1];                                  // live sequences or groups
+    sc[0] = bad_offsets ? NAN : (M > 0.f ? __fdiv_rn(1.f, M) : 0.f);   // token-mean weight
+    sc[1] = bad_offsets ? NAN : v[1];                                    // live sequences or groups
     sc[2] = scale;
   }
 }
@@ -289,7 +307,8 @@ __global__ void __launch_bounds__(LT) loss_grad_kernel(LossArgs a) {
       wgt = mu > 0.f ? __fdiv_rn(1.f, __fmul_rn(mu, sc[1])) : 0.f;
     }
     const float A = p[10];
-    const int64_t t0 = a.seq_offsets[s], t1 = a.seq_offsets[s + 1];
+    int64_t t0, t1;
+    seq_range(a, s, t0, t1);
     for (int64_t t = t0 + threadIdx.x; t < t1; t += LT) {
       const float nw = a.logp_new[t], od = a.logp_old[t];
       const float ro = a.logp_rollout[t], rf = a.logp_ref[t];
@@ -375,40 +394,16 @@ extern "C" rlk_status rlk_grpo_loss_noalloc(
     const int32_t* seq_offsets, int32_t n_seq, int32_t group_size, int64_t n_tok,
     float eps_low, float eps_high, float tis_cap, float kl_coef, rlk_agg agg, float* out_loss,
     float* out_dloss_dlogp_new, float* out_stats, rlk_stream stream) {
-  if (n_seq < 0 || n_seq > RLK_NOALLOC_MAX_SEQ || group_size < 1 || n_seq % group_size != 0 ||
-      n_tok < 0)
-    return RLK_ERR_INVALID_ARG;
-  if (!(isfinite(eps_low) && eps_low >= 0.0f && isfinite(eps_high) && eps_high >= 0.0f))
-    return RLK_ERR_INVALID_ARG;
-  if (!(isfinite(tis_cap) && tis_cap > 0.0f) || !(isfinite(kl_coef) && kl_coef >= 0.0f))
-    return RLK_ERR_INVALID_ARG;
-  if (agg != RLK_AGG_TOKEN_MEAN && agg != RLK_AGG_SEQ_MEAN_TOKEN_MEAN && agg != RLK_AGG_PROMPT_MEAN)
-    return RLK_ERR_INVALID_ARG;
-  if (!seq_offsets || !out_loss) return RLK_ERR_INVALID_ARG;
-  if (n_seq > 0 && (!logp_new || !logp_old || !logp_rollout || !logp_ref || !rewards))
-    return RLK_ERR_INVALID_ARG;
+  if (n_seq > RLK_NOALLOC_MAX_SEQ) return RLK_ERR_INVALID_ARG;
+  rlk::LossArgs a;
+  const int st = rlk::grpo_loss_args(logp_new, logp_old, logp_rollout, logp_ref, loss_mask,
+                                     rewards, seq_offsets, n_seq, group_size, n_tok, eps_low,
+                                     eps_high, tis_cap, kl_coef, (int)agg, out_loss,
+                                     out_dloss_dlogp_new, out_stats, a);
+  if (st != RLK_OK) return (rlk_status)st;
   cudaError_t err;
   float* scratch = rlk::noalloc_scratch(err);
   if (!scratch) return RLK_ERR_CUDA;
-  rlk::LossArgs a;
-  a.logp_new = logp_new;
-  a.logp_old = logp_old;
-  a.logp_rollout = logp_rollout;
-  a.logp_ref = logp_ref;
-  a.mask = loss_mask;
-  a.rewards = rewards;
-  a.seq_offsets = seq_offsets;
-  a.n_seq = n_seq;
-  a.group_size = group_size;
-  a.n_tok = n_tok;
-  a.eps_low = eps_low;
-  a.eps_high = eps_high;
-  a.tis_cap = tis_cap;
-  a.kl_coef = kl_coef;
-  a.agg = agg;
-  a.out_loss = out_loss;
-  a.out_grad = out_dloss_dlogp_new;
-  a.out_stats = out_stats;
   a.workspace = scratch;
   if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_grpo_loss(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess

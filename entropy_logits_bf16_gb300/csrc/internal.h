@@ -178,12 +178,28 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream);
 // Cluster-resident kernel for large-vocabulary bf16 rows (lpe_cluster.cu).
 bool lpe_cluster_eligible(const LpeArgs& a);
 cudaError_t launch_lpe_cluster(const LpeArgs& a, cudaStream_t stream);
+// Streaming kernel for every bf16 batch of a large vocabulary (lpe_stream.cu).
+// wait_limit: clock cycles a device wait may take; withhold: a debug stage
+// index the first CTA never issues (-1: none).
+bool lpe_stream_eligible(const LpeArgs& a);
+cudaError_t launch_lpe_stream(const LpeArgs& a, cudaStream_t stream, long long wait_limit,
+                              long long withhold);
+// Debug settings of the bounded device waits (rlk_debug.h).
+long long debug_wait_limit();       // clock cycles (default about 2^31)
+long long debug_take_withheld();    // the stage to withhold in the next launch, or -1
 
 cudaError_t launch_support(const SupportArgs& a, cudaStream_t stream);
 cudaError_t launch_logprob_entropy_backward(const LpeBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_support_backward(const SupportArgs& a, cudaStream_t stream);
 
 constexpr int kLossPartials = 12;  // floats per sequence in the loss workspace
+// Checks rlk_grpo_loss's arguments (all but the workspace) and fills a; returns
+// an rlk_status value.  Shared by rlk_grpo_loss and rlk_grpo_loss_noalloc.
+int grpo_loss_args(const float* logp_new, const float* logp_old, const float* logp_rollout,
+                   const float* logp_ref, const uint8_t* loss_mask, const float* rewards,
+                   const int32_t* seq_offsets, int32_t n_seq, int32_t group_size, int64_t n_tok,
+                   float eps_low, float eps_high, float tis_cap, float kl_coef, int agg,
+                   float* out_loss, float* out_grad, float* out_stats, LossArgs& a);
 size_t loss_workspace_bytes(int64_t n_seq);
 cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t stream);
 

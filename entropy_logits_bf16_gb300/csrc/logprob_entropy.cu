@@ -1129,8 +1129,8 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
   const float inv_t = (float)(1.0 / (double)a.temperature);
   const int64_t grid64 = a.T < (int64_t)3 * sm_count() ? a.T : (int64_t)3 * sm_count();
   const dim3 grid((unsigned)grid64), block(NT);
-  // per-row parameters: the per-row kernel in its top-p form (rows with
-  // top_p = 1 take its all-tokens branch); the cluster kernel is scalar-only
+  // per-row parameters: the kernels' top-p form (rows with top_p = 1 take
+  // its all-tokens branch)
   const bool per_row = a.temps != nullptr || a.top_ps != nullptr;
   const bool topp = per_row || a.top_p < 1.0f;
   const size_t smem = sizeof(Smem);
@@ -1149,10 +1149,10 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
       return e;
     attr_done.store(1);
   }
-  if (!a.only_marked && !per_row && lpe_cluster_eligible(a)) {
-    cudaError_t e = launch_lpe_cluster(a, stream);
+  if (!a.only_marked && lpe_stream_eligible(a)) {
+    cudaError_t e = launch_lpe_stream(a, stream, debug_wait_limit(), debug_take_withheld());
     if (e != cudaSuccess || !topp) return e;
-    LpeArgs b = a;   // rows the cluster kernel marked for recomputation
+    LpeArgs b = a;   // rows the streaming kernel marked for recomputation
     b.only_marked = 1;
     lpe_kernel<RowBf16, true><<<grid, block, smem, stream>>>(b, c, inv_t);
     return cudaGetLastError();

@@ -1,0 +1,945 @@
+// Streaming rlk_logprob_entropy kernel for bf16 rows of a large vocabulary
+// (every bf16 batch with 14,848 <= V <= 174,080, whatever its row stride or
+// alignment, and whichever entry point -- scalar or per-row parameters -- so a
+// row gets one set of bits from every call that scores it).
+//
+// What is computed: the temperature-scaled, top-p-truncated, renormalised
+// log-probability of the selected token and the Shannon entropy of the
+// retained distribution, following RL-Kernel "Qwen3-8B VIME train-rollout
+// consistency", section "ROCm MI300X and gfx942" (sparse logp /
+// monitoring-entropy fusion over the complete retained top-p support, the
+// full-vocabulary scorer at top_p = 1) and the RL-Kernel "ROCm sparse
+// performance" notes (the sampler's temperature / top-p semantics, a fixed
+// reduction order so recomputed log-probabilities are bitwise reproducible).
+//
+// One CTA of 1024 threads per SM; CTA b scores rows b, b + grid, ...  Warp
+// roles, pipelined over rows:
+//  * the producer (warp 29): one thread streams each row through a ring of
+//    four shared-memory stages with cp.async.bulk (one unit of 16 logits = 32
+//    bytes per compute thread per stage), and forms each row's parameters
+//    (c = log2(e) / T exactly as the host forms it);
+//  * the compute warps (0-28): thread t owns the units t, t + 928, ... of a
+//    row and keeps one running state: an integer reference E_t,
+//    S = sum 2^d as a double-float and U = sum 2^d d with d = fma(z, c, -E_t)
+//    (one rounding).  A unit's max comes first (packed bf16x2 max); the
+//    reference moves up (by an exact power of two) only when a unit's max
+//    exceeds it by more than LAZY, so the exponentials run against a fixed
+//    reference almost always.  At top_p < 1 each unit's max also goes to a
+//    sketch.  At the end of a row the thread's state goes to shared memory and
+//    the next row starts at once;
+//  * the merge warp (30), one row behind: merges the 928 thread states in a
+//    fixed order (rescaling to E = ceil(m c), m the row max: exact powers of
+//    two) and decides the row: at top_p = 1 its answer; at top_p < 1 the
+//    window z >= m - L T (L = ln(1/(1-top_p)) + 7) in which the retained set
+//    must lie.  All tokens of one bf16 value carry the same mass, so the
+//    window is summarised exactly by integer counts per distinct value;
+//  * side work of the compute warps: while they stream the next row, each
+//    thread tests its own units' sketch entries of the finished row against
+//    the window, reads every unit that reaches it once more (staged into its
+//    own shared-memory slot by cp.async one stage ahead, so the warp never
+//    waits on the load; the row streamed through L2 microseconds earlier) and
+//    counts its window tokens per key with shared-memory atomics (integer
+//    counts do not depend on the atomics' order);
+//  * the scan warp (31): one warp scans the counts largest value first in a
+//    fixed-order double-float prefix: the bin where the retained mass reaches
+//    top_p Z, how many of its tied tokens are needed (lower ids first), Z_S
+//    and the entropy numerator; it writes every row's outputs.
+//  * Rows this path does not finish -- a window wider than the histogram (one
+//    that crosses zero) or a window whose mass falls short of the target --
+//    get a marker in out_logprob and are recomputed by the per-row kernel
+//    launched right after.  The choice depends only on the row's own values;
+//    every sum runs in a fixed order; so a row's output bits never depend on
+//    the batch around it, nor on the layout of the batch (aligned rows stream
+//    through the ring, other rows are read with scalar loads into the same
+//    units, with the same arithmetic).
+//
+// Every wait is bounded: a wait that runs out raises RLK_STATUS_TIMEOUT and an
+// abort flag; every role then stops waiting, the rows not yet finished get
+// NaN outputs, the producer lets the copies it issued land, and the kernel
+// returns.
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+#include "rlk.h"
+
+namespace rlk {
+namespace {
+
+constexpr int NWC = 29;                  // compute warps
+constexpr int NTC = NWC * 32;            // compute threads
+constexpr int WPROD = NWC;               // producer warp
+constexpr int WMRG = NWC + 1;            // merge warp
+constexpr int WSCN = NWC + 2;            // scan warp
+constexpr int NTB = (NWC + 3) * 32;
+static_assert(NTB == 1024, "one 1024-thread CTA per SM");
+constexpr int UNIT = 16;                 // logits per unit (32 bytes)
+constexpr int NSTAGE = 4;                // ring stages
+constexpr int STAGE_BYTES = NTC * 32;    // one unit per compute thread
+constexpr int HBC = 2048;                // window bins (keys below the row max)
+constexpr int NRP = 16;                  // row-parameter slots
+constexpr float LAZY = 4.0f;             // re-base when a unit's max exceeds E_t by this (base 2)
+constexpr int64_t V_MIN = (int64_t)UNIT * NTC;
+constexpr int64_t V_MAX = 174080;        // the sketch's share of shared memory (10,880 units)
+static_assert((V_MAX / UNIT + NTC - 1) / NTC <= 32, "a thread's units of a row fit a 32-bit mask");
+
+struct RowParam {
+  float c, temp, top_p, row_t;   // row_t: the row's own temperature (per-row calls), else 0
+  uint32_t bad;                  // the row's parameters are invalid (RLK_STATUS_BAD_PARAM)
+  uint32_t pad[3];
+};
+
+// What the merge warp decides for a row.
+enum : uint32_t { REC_DONE = 0, REC_COUNT = 1, REC_MARK = 2, REC_BAD = 3 };
+struct RowRec {
+  uint32_t mode, bad_bit;
+  uint32_t zf2;          // window floor, a bf16 value in both halves
+  uint32_t key_m, dmax, key_y;
+  int32_t y;
+  float E, c, U, zy, top_p, row_t;
+  float zhi, zlo;        // Z as a double-float
+  float lp, ent, lz;     // REC_DONE: the outputs and ln Z
+  int32_t kstar;
+};
+
+struct __align__(16) Ctrl {
+  unsigned long long full[NSTAGE];
+  unsigned long long empty[NSTAGE];
+  unsigned long long rowpub[2];     // compute warps -> merge warp: a row's states written
+  unsigned long long floorpub[2];   // merge warp -> compute warps, scan warp: the row's record
+  unsigned long long counted[2];    // compute warps -> scan warp: the row's window counted
+  unsigned long long hclear[2];     // scan warp -> merge warp: the row's counts consumed
+  RowParam rp[NRP];
+  RowRec rec[2];
+  uint32_t wkey[2][NWC];
+  uint32_t tie[2];
+  int abort;
+};
+
+struct Geom {
+  int nunits;     // ceil(V / 16)
+  int nfull;      // V / 16: units whose 16 logits all exist
+  int nst;        // stages per row: ceil(nunits / NTC)
+  int tma;        // rows stream through the ring (16-byte aligned rows)
+  uint32_t tma_bytes;   // bytes of a row the ring copies: floor(V / 8) * 16
+  uint32_t off_part, off_hist, off_slot, off_sk, skb, off_ring;
+  long long wait_limit;   // clock cycles a wait may take before it gives up
+  long long withhold;     // debug: the stage CTA 0 never issues (-1: none)
+};
+
+__host__ __device__ constexpr uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ helpers
+
+// 2^n for an integer-valued n <= 0 (-inf gives 0), exactly.
+__device__ __forceinline__ float exp2_int(float n) {
+  return n >= -126.f ? __int_as_float(((int)n + 127) << 23) : 0.f;
+}
+
+// Waits for the mbarrier phase of the given parity, suspending in hardware.
+// Gives up after `limit` clock cycles (raising the abort flag and the status
+// bit) or at once when the abort flag is up.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort,
+                                           long long limit, uint32_t* status) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(100000u)
+        : "memory");
+    if (ok) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit) {
+      *abort = 1;
+      if (status) atomicOr(status, RLK_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float value_of_key(uint32_t k) { return bf16_val(okey16_inverse(k)); }
+__device__ __forceinline__ uint32_t key_of(float v) { return okey16(__float_as_uint(v) >> 16); }
+
+// The running state of one compute thread for one row.
+struct Acc {
+  float E;      // reference (integer-valued, or -inf before the first unit)
+  DF S;         // sum 2^d
+  float2 U;     // sum 2^d d (two packed lanes)
+  float mx;     // largest logit seen
+};
+
+// Moves the reference up to En (> E): every sum scales by 2^(E - En), exactly.
+__device__ __forceinline__ void rebase(Acc& st, float En) {
+  if (st.E == -INFINITY) {
+    st.E = En;
+    return;
+  }
+  const float n = __fsub_rn(st.E, En);   // integer, < 0
+  const float f = exp2_int(n);
+  st.U.x = __fmul_rn(f, __fmaf_rn(n, st.S.hi, st.U.x));
+  st.U.y = __fmul_rn(f, st.U.y);
+  st.S.hi = __fmul_rn(st.S.hi, f);
+  st.S.lo = __fmul_rn(st.S.lo, f);
+  st.E = En;
+}
+
+// Folds a unit's 16 logits into the state and returns the unit's max.  The
+// words w[0..7] hold the logits in the order the thread reads them (two bf16
+// a word, low half first).  MASKED: only the logits whose bit is set in vmask
+// (bit j: half j & 1 of word j >> 1) exist -- the row's last, partial unit.
+template <bool MASKED>
+__device__ __forceinline__ float absorb_unit(Acc& st, const uint32_t (&w)[8], float c,
+                                             uint32_t vmask = 0xFFFFu) {
+  uint32_t wm[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    wm[k] = w[k];
+    if (MASKED) {   // absent logits read as -inf for the max
+      if (!((vmask >> (2 * k)) & 1u)) wm[k] = (wm[k] & 0xFFFF0000u) | 0xFF80u;
+      if (!((vmask >> (2 * k + 1)) & 1u)) wm[k] = (wm[k] & 0xFFFFu) | 0xFF800000u;
+    }
+  }
+  const __nv_bfloat162 m01 = __hmax2(bf2(wm[0]), bf2(wm[1])), m23 = __hmax2(bf2(wm[2]), bf2(wm[3]));
+  const __nv_bfloat162 m45 = __hmax2(bf2(wm[4]), bf2(wm[5])), m67 = __hmax2(bf2(wm[6]), bf2(wm[7]));
+  const __nv_bfloat162 mm = __hmax2(__hmax2(m01, m23), __hmax2(m45, m67));
+  const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mm);
+  const float gm = fmaxf(bf16_lo(mw), bf16_hi(mw));
+  st.mx = fmaxf(st.mx, gm);
+  // rare after a row's first units (E = -inf before the first: always taken)
+  if (__fmaf_rn(gm, c, -st.E) > LAZY) rebase(st, ceilf(__fmul_rn(gm, c)));
+  const float2 c2 = make_float2(c, c);
+  const float2 nE2 = make_float2(-st.E, -st.E);
+  // Two halves of four words: sum ((e0+e1)+(e2+e3)) + ((e4+e5)+(e6+e7)) and
+  // U += e_k d_k for k = 0..7 in order.
+  float2 sh[2];
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    float2 d[4], e[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int k = 4 * hf + i;
+      d[i] = __ffma2_rn(bf16x2_to_f2(w[k]), c2, nE2);
+      e[i] = make_float2(ex2(d[i].x), ex2(d[i].y));
+      if (MASKED) {
+        if (!((vmask >> (2 * k)) & 1u)) { d[i].x = 0.f; e[i].x = 0.f; }
+        if (!((vmask >> (2 * k + 1)) & 1u)) { d[i].y = 0.f; e[i].y = 0.f; }
+      }
+    }
+    sh[hf] = __fadd2_rn(__fadd2_rn(e[0], e[1]), __fadd2_rn(e[2], e[3]));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) st.U = __ffma2_rn(e[i], d[i], st.U);
+  }
+  const float2 s = __fadd2_rn(sh[0], sh[1]);
+  float t, r;
+  two_sum(st.S.hi, __fadd_rn(s.x, s.y), t, r);
+  st.S.hi = t;
+  st.S.lo = __fadd_rn(st.S.lo, r);
+  return gm;
+}
+
+// The 8 words of unit u of a row read with scalar loads (any alignment);
+// absent logits (beyond V) read as -inf (the stream masks them besides).
+__device__ __forceinline__ void load_unit_scalar(const uint16_t* row, int64_t V, int u, int h,
+                                                 uint32_t (&w)[8]) {
+  const int64_t c0 = (int64_t)u * UNIT;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int hh = half == 0 ? h : 1 - h;   // the half read first goes to words 0..3
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i0 = c0 + hh * 8 + 2 * k;
+      const uint32_t lo = i0 < V ? (uint32_t)__ldg(row + i0) : 0xFF80u;
+      const uint32_t hi = i0 + 1 < V ? (uint32_t)__ldg(row + i0 + 1) : 0xFF80u;
+      w[half * 4 + k] = lo | (hi << 16);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- the scan
+struct ScanOut {
+  uint32_t kstar;
+  float lz, h;
+  bool y_in;
+  uint32_t key_thr, ties;
+};
+
+// One warp scans the window's bins 0..dmax (distance below the max key) in a
+// fixed order, largest value first: the first bin whose inclusive prefix mass
+// reaches the target, how many of its tied tokens are needed (lower ids
+// first), Z_S and the entropy numerator.  Lane l owns the contiguous bins
+// [l b, (l+1) b).  Returns false (on every lane) when the window's mass falls
+// short; else the results are valid on every lane.
+__device__ bool warp_scan_window(int lane, uint32_t dmax, uint32_t key_m, float c, float E,
+                                 DF target, const uint32_t* hist, uint32_t key_y, uint32_t tie_y,
+                                 ScanOut& out) {
+  const uint32_t bpl = (dmax + 32u) / 32u;
+  const uint32_t d0 = (uint32_t)lane * bpl;
+  auto bin = [&](uint32_t d, uint32_t& nb, float& mass, float& um, float& wv, float& dv) {
+    nb = 0u; mass = 0.f; um = 0.f; wv = 0.f; dv = 0.f;
+    if (d > dmax) return;
+    nb = hist[d];
+    if (nb == 0u) return;
+    dv = __fmaf_rn(value_of_key(key_m - d), c, -E);
+    wv = ex2(dv);
+    mass = __fmul_rn((float)nb, wv);
+    um = __fmul_rn(mass, dv);
+  };
+  DF tot{0.f, 0.f};
+  uint32_t tcnt = 0u;
+  float tum = 0.f;
+  for (uint32_t j = 0; j < bpl; ++j) {
+    uint32_t nb; float ms, um, wv, dv;
+    bin(d0 + j, nb, ms, um, wv, dv);
+    tot = df_add_f(tot, ms);
+    tcnt += nb;
+    tum = __fadd_rn(tum, um);
+  }
+  DF inc = tot;
+  uint32_t icnt = tcnt;
+  float ium = tum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF lft{shfl_up(inc.hi, o), shfl_up(inc.lo, o)};
+    const uint32_t lc = __shfl_up_sync(0xFFFFFFFFu, icnt, o);
+    const float lu = shfl_up(ium, o);
+    if (lane >= o) {
+      inc = df_add(lft, inc);
+      icnt += lc;
+      ium = __fadd_rn(lu, ium);
+    }
+  }
+  DF P{shfl_up(inc.hi, 1), shfl_up(inc.lo, 1)};
+  uint32_t pc = __shfl_up_sync(0xFFFFFFFFu, icnt, 1);
+  float pu = shfl_up(ium, 1);
+  if (lane == 0) { P = DF{0.f, 0.f}; pc = 0u; pu = 0.f; }
+  int my_d = -1;
+  DF pb{0.f, 0.f};
+  uint32_t cb = 0u, nt = 0u;
+  float ub = 0.f, wt = 0.f, dt = 0.f;
+  for (uint32_t j = 0; j < bpl; ++j) {
+    uint32_t nb; float ms, um, wv, dv;
+    bin(d0 + j, nb, ms, um, wv, dv);
+    const DF Pn = df_add_f(P, ms);
+    if (nb > 0u && df_ge(Pn, target)) {
+      my_d = (int)(d0 + j);
+      pb = P; cb = pc; ub = pu; wt = wv; dt = dv; nt = nb;
+      break;
+    }
+    P = Pn;
+    pc += nb;
+    pu = __fadd_rn(pu, um);
+  }
+  const uint32_t bal = __ballot_sync(0xFFFFFFFFu, my_d >= 0);
+  if (bal == 0u) return false;
+  const int win = __ffs(bal) - 1;   // the lowest lane holds the lowest crossing bin
+  uint32_t kstar = 0u, ties = 0u;
+  int y_in = 0;
+  float lz = 0.f, h = 0.f;
+  if (lane == win) {
+    const float need = df_sub_to_f(target, pb);
+    const float cf = ceilf(__fdiv_rn(need, wt));
+    const uint32_t cneed = cf < 1.f ? 1u : (cf > (float)nt ? nt : (uint32_t)cf);
+    const float wn = __fmul_rn((float)cneed, wt);
+    const DF zs = df_add_f(pb, wn);
+    const float us = __fmaf_rn(wn, dt, ub);
+    const uint32_t d_y = key_m - key_y;
+    kstar = cb + cneed;
+    ties = cneed == nt ? kTiesAll : cneed;
+    y_in = (d_y < (uint32_t)my_d) || (d_y == (uint32_t)my_d && tie_y < cneed);
+    const float zsf = __fadd_rn(zs.hi, zs.lo);
+    lz = logf(zsf);
+    h = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, us), zsf));
+  }
+  out.kstar = __shfl_sync(0xFFFFFFFFu, kstar, win);
+  out.ties = __shfl_sync(0xFFFFFFFFu, ties, win);
+  out.key_thr = key_m - (uint32_t)__shfl_sync(0xFFFFFFFFu, my_d, win);
+  out.y_in = __shfl_sync(0xFFFFFFFFu, y_in, win) != 0;
+  out.lz = __shfl_sync(0xFFFFFFFFu, lz, win);
+  out.h = __shfl_sync(0xFFFFFFFFu, h, win);
+  return true;
+}
+
+__device__ __forceinline__ void write_bad(const LpeArgs& a, int64_t r, uint32_t bit) {
+  a.out_logprob[r] = NAN;
+  a.out_entropy[r] = NAN;
+  if (a.out_k) a.out_k[r] = 0;
+  if (a.status && bit) atomicOr(a.status, bit);
+  if (a.state) a.state[r] = RowState{0.f, 0.f, 0.f, 0u, 0u, bit << 8, 0, 0u};
+}
+
+// wait_phase with a fast path: one suspending try first (the phase has
+// usually completed or completes within the hardware's suspend window).
+__device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          long long limit, uint32_t* status) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(100000u)
+      : "memory");
+  if (ok) return true;
+  return wait_phase(bar, parity, abort, limit, status);
+}
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool test_phase(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned); the
+// commit of this thread's copies and the wait for all of them.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Puts unit u of a row into a thread's 32-byte slot: asynchronously for a
+// whole unit of a 16-byte aligned row, else with scalar loads (absent logits
+// beyond V read as -inf, so they never reach a window).
+__device__ __forceinline__ void stage_unit(const uint16_t* row, int64_t V, int u, bool aligned_full,
+                                           uint4* slot) {
+  if (aligned_full) {
+    const uint4* q = reinterpret_cast<const uint4*>(row) + 2 * u;
+    cp_async16(smem_u32(slot), q);
+    cp_async16(smem_u32(slot + 1), q + 1);
+    cp_async_commit();
+  } else {
+    uint32_t w[8];
+    load_unit_scalar(row, V, u, 0, w);
+    slot[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    slot[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// Counts the tokens of unit u (its 16 logits in slot) that reach the window
+// floor into hist (bins below key_m), and the tokens tied with the selected
+// one (key_y) that precede it.  Absent logits of a partial unit read as -inf.
+__device__ __forceinline__ void count_unit(const uint4* slot, int u, uint32_t zf2w, uint32_t key_m,
+                                           uint32_t key_y, int32_t y, uint32_t* hist,
+                                           uint32_t& tie) {
+  const uint4 v0 = slot[0], v1 = slot[1];
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  const __nv_bfloat162 zf2 = bf2(zf2w);
+  uint32_t msk = 0u;   // bit e: logit e of the unit reaches the floor
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t hm = __hge2_mask(bf2(w[k]), zf2);
+    msk |= ((hm & 1u) | ((hm >> 15) & 2u)) << (2 * k);
+  }
+  const uint16_t* e16 = reinterpret_cast<const uint16_t*>(slot);
+  const int32_t col0 = u * UNIT;
+  while (msk) {
+    const int el = __ffs(msk) - 1;
+    msk &= msk - 1u;
+    const uint32_t kk = okey16(e16[el]);
+    atomicAdd(&hist[key_m - kk], 1u);
+    tie += (kk == key_y && col0 + el < y) ? 1u : 0u;
+  }
+}
+
+// --------------------------------------------------------------- kernel
+template <bool TOPP, bool TMA>
+__global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, float c0) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem);
+  float* part = reinterpret_cast<float*>(smem + g.off_part);         // [2][3][NTC]: E, S, U
+  uint32_t* hist0 = reinterpret_cast<uint32_t*>(smem + g.off_hist);  // [2][HBC]
+  uint4* slots = reinterpret_cast<uint4*>(smem + g.off_slot);        // [NTC][2]: staged units
+  uint8_t* skb = smem + g.off_sk;                                     // [2][skb]
+  uint8_t* ring = smem + g.off_ring;                                  // [NSTAGE][STAGE_BYTES]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint16_t* logits = reinterpret_cast<const uint16_t*>(a.logits);
+  volatile int* abort = &ctl.abort;
+
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(smem_u32(&ctl.full[s]), 1u);
+      mbar_init(smem_u32(&ctl.empty[s]), (uint32_t)NWC);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl.rowpub[b]), (uint32_t)NWC);
+      mbar_init(smem_u32(&ctl.floorpub[b]), 1u);
+      mbar_init(smem_u32(&ctl.counted[b]), (uint32_t)NWC);
+      mbar_init(smem_u32(&ctl.hclear[b]), 1u);
+      ctl.tie[b] = 0u;
+    }
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  for (int i = tid; i < 2 * HBC; i += NTB) hist0[i] = 0u;
+  __syncthreads();
+
+  if (warp < NWC) {
+    // ------------------------------------------------------ compute warps
+    const int t = tid;
+    const int h = (lane >> 2) & 1;   // the half of its unit a thread reads first (bank spread)
+    uint32_t gs = 0;   // stages consumed (ring slot gs % NSTAGE, phase gs / NSTAGE)
+    int it = 0;
+    // Side work: the window count of the previous row, done by the warp as a
+    // whole.  Its candidate units (sketched max >= the window floor) are
+    // listed in the warp's own sketch entries of that row (each lane has read
+    // its entries first), then counted 32 at a time: a round's units are
+    // staged into the lanes' shared-memory slots by cp.async at one stage and
+    // counted at the next, so no lane waits on a load and no warp runs the
+    // count for a single lane.
+    int sw = 0;                // 0 none, 1 waiting for the record, 2 counting, 3 done
+    int sw_b = 0;
+    uint32_t sw_par = 0u, tie = 0u;
+    int sw_tot = 0, sw_q = 0;
+    bool sw_pend = false, sw_mine = false;
+    const uint16_t* sw_row = logits;
+    uint32_t rc_zf2 = 0u, rc_key_m = 0u, rc_key_y = 0u;   // the record fields the count needs
+    int32_t rc_y = 0;
+    uint4* myslot = slots + 2 * t;
+    auto list_at = [&](int k) -> uint16_t* {   // entry k of this warp's list
+      uint16_t* sk = reinterpret_cast<uint16_t*>(skb + (size_t)sw_b * g.skb);
+      return sk + (warp * 32 + (k & 31) + (k >> 5) * NTC);
+    };
+    auto side_start = [&](bool block) {   // sw == 1: read the record once it is published
+      const uint32_t bar = smem_u32(&ctl.floorpub[sw_b]);
+      bool ready = block ? wait_phase(bar, sw_par, abort, g.wait_limit, a.status)
+                         : test_phase(bar, sw_par);
+      ready = __shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0) != 0;
+      if (!ready) {
+        if (block) sw = 3;   // the wait ran out: nothing to count
+        return;
+      }
+      if (ctl.rec[sw_b].mode != REC_COUNT || *abort) {
+        sw = 3;
+        return;
+      }
+      rc_zf2 = ctl.rec[sw_b].zf2;
+      rc_key_m = ctl.rec[sw_b].key_m;
+      rc_key_y = ctl.rec[sw_b].key_y;
+      rc_y = ctl.rec[sw_b].y;
+      const uint16_t* sk = reinterpret_cast<const uint16_t*>(skb + (size_t)sw_b * g.skb);
+      const float zf = bf16_lo(rc_zf2);
+      uint32_t cm = 0u;
+      for (int j = 0; j < g.nst; ++j) {
+        const int u = t + j * NTC;
+        if (u < g.nunits && bf16_val(sk[u]) >= zf) cm |= 1u << j;
+      }
+      const int n = __popc(cm);
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      sw_tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      __syncwarp();   // every lane has read its sketch entries
+      int k = incl - n;
+      while (cm) {
+        const int j = __ffs(cm) - 1;
+        cm &= cm - 1u;
+        *list_at(k++) = (uint16_t)(t + j * NTC);
+      }
+      __syncwarp();
+      sw_q = 0;
+      sw_pend = false;
+      sw = 2;
+    };
+    auto side_step = [&]() {   // sw == 2: count the round staged a stage ago, stage the next
+      if (sw_pend) {
+        cp_async_wait_all();
+        if (sw_mine)
+          count_unit(myslot, (int)*list_at(sw_q - 32 + lane), rc_zf2, rc_key_m, rc_key_y, rc_y,
+                     hist0 + sw_b * HBC, tie);
+        sw_pend = false;
+      }
+      if (sw_q < sw_tot) {
+        const int k = sw_q + lane;
+        sw_mine = k < sw_tot;
+        if (sw_mine) {
+          const int u = (int)*list_at(k);
+          stage_unit(sw_row, a.V, u, TMA && u < g.nfull, myslot);
+        }
+        sw_q += 32;
+        sw_pend = true;
+      } else {
+        sw = 3;
+      }
+    };
+    auto side_finish = [&]() {   // end of a row: complete the side work and report it
+      if (sw == 1) side_start(true);
+      while (sw == 2) side_step();
+      uint32_t wt = tie;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wt += __shfl_down_sync(0xFFFFFFFFu, wt, o);
+      if (lane == 0 && wt) atomicAdd(&ctl.tie[sw_b], wt);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.counted[sw_b]));
+    };
+
+    for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x, ++it) {
+      const int b = it & 1;
+      Acc st{-INFINITY, DF{0.f, 0.f}, make_float2(0.f, 0.f), -INFINITY};
+      float c = 0.f;
+      const uint16_t* row = logits + r * a.ld;
+      uint16_t* sk = reinterpret_cast<uint16_t*>(skb + (size_t)b * g.skb);
+      // One stage: wait for the slot, fold this thread's unit (whole units
+      // on every stage but the last), release the slot, then side work.
+      auto stage = [&](int s, bool last) {
+        const uint32_t slot = gs & (NSTAGE - 1);
+        const bool ok = wait_full(smem_u32(&ctl.full[slot]), (gs / NSTAGE) & 1u, abort, g.wait_limit,
+                                  a.status);
+        const int u = t + s * NTC;
+        if (ok && (!last || u < g.nunits)) {
+          uint32_t w[8];
+          float gm;
+          if (!last || u < g.nfull) {
+            if (TMA) {
+              const uint4* q = reinterpret_cast<const uint4*>(ring + slot * STAGE_BYTES) + 2 * t;
+              const uint4 v0 = q[h], v1 = q[1 - h];
+              w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+              w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+            } else {
+              load_unit_scalar(row, a.V, u, h, w);
+            }
+            gm = absorb_unit<false>(st, w, c);
+          } else {
+            // the row's last, partial unit: slot j of the words holds logit
+            // 8 * (j < 8 ? h : 1 - h) + (j & 7) of the unit
+            load_unit_scalar(row, a.V, u, h, w);
+            const int nv = (int)(a.V - (int64_t)u * UNIT);   // 1..15 logits exist
+            uint32_t vm = 0u;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (8 * (j < 8 ? h : 1 - h) + (j & 7) < nv) vm |= 1u << j;
+            gm = absorb_unit<true>(st, w, c, vm);
+          }
+          if (TOPP) sk[u] = (uint16_t)(__float_as_uint(gm) >> 16);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl.empty[slot]));
+        ++gs;
+        if (TOPP) {
+          if (sw == 1 && !last) side_start(false);
+          if (sw == 2) side_step();
+        }
+      };
+      // The row's parameters are published with its first stage.
+      {
+        const uint32_t slot = gs & (NSTAGE - 1);
+        wait_full(smem_u32(&ctl.full[slot]), (gs / NSTAGE) & 1u, abort, g.wait_limit, a.status);
+        c = ctl.rp[it % NRP].c;
+      }
+      for (int s = 0; s + 1 < g.nst; ++s) stage(s, false);
+      stage(g.nst - 1, true);
+      if (TOPP && it > 0) side_finish();
+      // The state buffer was last read by the merge warp two rows ago (at
+      // top_p < 1 the side work above has already waited for that).
+      if (!TOPP && it >= 2)
+        wait_phase(smem_u32(&ctl.floorpub[b]), (uint32_t)(((it - 2) >> 1) & 1), abort, g.wait_limit,
+                   a.status);
+      float* pb = part + b * 3 * NTC;
+      pb[t] = st.E;
+      pb[NTC + t] = __fadd_rn(st.S.hi, st.S.lo);
+      pb[2 * NTC + t] = __fadd_rn(st.U.x, st.U.y);
+      const uint32_t kx = __reduce_max_sync(0xFFFFFFFFu, okey32(__float_as_uint(st.mx)));
+      if (lane == 0) ctl.wkey[b][warp] = kx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.rowpub[b]));
+      if (TOPP) {   // this row's side work runs during the next row
+        sw = 1;
+        sw_b = b;
+        sw_par = (uint32_t)((it >> 1) & 1);
+        sw_row = row;
+        tie = 0u;
+      }
+    }
+    if (TOPP && it > 0) side_finish();
+  } else if (warp == WPROD) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    uint32_t gs = 0;
+    int it = 0;
+    int issued[NSTAGE];   // parity of the last copy issued on a slot (-1: none pending)
+    for (int s = 0; s < NSTAGE; ++s) issued[s] = -1;
+    const bool per_row = a.temps || a.top_ps;
+    for (int64_t r = blockIdx.x; r < a.T && !*abort; r += gridDim.x, ++it) {
+      RowParam p{c0, a.temperature, a.top_p, 0.f, 0u, {0u, 0u, 0u}};
+      if (per_row) {
+        if (a.temps) p.temp = a.temps[r];
+        if (a.top_ps) p.top_p = a.top_ps[r];
+        p.bad = !(isfinite(p.temp) && p.temp > 0.f && p.top_p > 0.f && p.top_p <= 1.f);
+        p.c = p.bad ? 1.f : (float)(1.4426950408889634 / (double)p.temp);
+        if (a.temps) p.row_t = p.temp;
+      }
+      ctl.rp[it % NRP] = p;
+      const char* src = reinterpret_cast<const char*>(logits + r * a.ld);
+      for (int s = 0; s < g.nst; ++s, ++gs) {
+        const uint32_t slot = gs & (NSTAGE - 1);
+        // Once a wait of this CTA has run out no further copy is issued: the
+        // consumers may have left a slot unread.
+        if (gs >= NSTAGE &&
+            !wait_phase(smem_u32(&ctl.empty[slot]), ((gs / NSTAGE) - 1) & 1u, abort,
+                        g.wait_limit, a.status))
+          break;
+        if (*abort) break;
+        if (blockIdx.x == 0 && (long long)gs == g.withhold) continue;   // debug: a copy never issued
+        const uint32_t bar = smem_u32(&ctl.full[slot]);
+        const uint32_t b0 = (uint32_t)s * STAGE_BYTES;
+        uint32_t bytes = 0u;
+        if (TMA && b0 < g.tma_bytes) bytes = min((uint32_t)STAGE_BYTES, g.tma_bytes - b0);
+        if (bytes) {
+          mbar_expect_tx(bar, bytes);
+          bulk_copy_g2s(smem_u32(ring + slot * STAGE_BYTES), src + b0, bytes, bar);
+          issued[slot] = (int)((gs / NSTAGE) & 1);
+        } else {
+          mbar_arrive(bar);
+          issued[slot] = -1;
+        }
+      }
+    }
+    // Let every copy this thread issued land before the CTA may exit.
+    volatile int never = 0;
+    for (int s = 0; s < NSTAGE; ++s)
+      if (issued[s] >= 0)
+        wait_phase(smem_u32(&ctl.full[s]), (uint32_t)issued[s], &never, g.wait_limit, a.status);
+  } else if (warp == WMRG) {
+    // ---------------------------------------------------------- merge warp
+    int it = 0;
+    for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x, ++it) {
+      const int b = it & 1;
+      const uint32_t par = (uint32_t)((it >> 1) & 1);
+      // A row is trusted only if no wait of this CTA has run out (the compute
+      // warps still publish rows after an abort, without having read them).
+      const bool waited = wait_phase(smem_u32(&ctl.rowpub[b]), par, abort, g.wait_limit, a.status);
+      const bool ok = __shfl_sync(0xFFFFFFFFu, (waited && !*abort) ? 1 : 0, 0) != 0;
+      const RowParam p = ctl.rp[it % NRP];
+      const int64_t y = a.ids[r];
+      const bool bad_id = y < 0 || y >= a.V;
+      const uint16_t* row = logits + r * a.ld;
+      const float zy = bad_id ? 0.f : bf16_val(__ldg(row + y));
+      uint32_t km = lane < NWC ? ctl.wkey[b][lane] : 0u;
+      km = __reduce_max_sync(0xFFFFFFFFu, km);
+      const float m = __uint_as_float(okey32_inverse(km));
+      const float c = p.c;
+      const float E = ceilf(__fmul_rn(m, c));
+      // Merge the thread states in a fixed order.
+      DF Z{0.f, 0.f};
+      float U = 0.f;
+      if (ok) {
+        // Lane l takes the states 4 l .. 4 l + 3 of every block of 128 into
+        // four accumulators (independent chains), merged in a fixed order.
+        const float4* pE = reinterpret_cast<const float4*>(part + b * 3 * NTC);
+        const float4* pS = reinterpret_cast<const float4*>(part + b * 3 * NTC + NTC);
+        const float4* pU = reinterpret_cast<const float4*>(part + b * 3 * NTC + 2 * NTC);
+        DF z4[4] = {DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}};
+        float u4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int q = lane; q < NTC / 4; q += 32) {
+          const float4 e4 = pE[q], s4 = pS[q], v4 = pU[q];
+          const float ev[4] = {e4.x, e4.y, e4.z, e4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w},
+                      uv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (sv[k] == 0.f && uv[k] == 0.f) continue;
+            const float n = __fsub_rn(ev[k], E);
+            const float f = exp2_int(n);
+            z4[k] = df_add_f(z4[k], __fmul_rn(sv[k], f));
+            u4[k] = __fmaf_rn(f, __fmaf_rn(n, sv[k], uv[k]), u4[k]);
+          }
+        }
+        Z = df_add(df_add(z4[0], z4[1]), df_add(z4[2], z4[3]));
+        U = __fadd_rn(__fadd_rn(u4[0], u4[1]), __fadd_rn(u4[2], u4[3]));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const DF x{shfl_down(Z.hi, o), shfl_down(Z.lo, o)};
+        const float ux = shfl_down(U, o);
+        Z = df_add(Z, x);
+        U = __fadd_rn(U, ux);
+      }
+      RowRec rc{};
+      if (lane == 0) {
+        const float zf = __fadd_rn(Z.hi, Z.lo);
+        const bool nonfinite = !(isfinite(zf) && isfinite(U) && isfinite(m) && isfinite(E));
+        const bool topp = TOPP && p.top_p < 1.0f;
+        rc.E = E; rc.c = c; rc.U = U; rc.zy = zy; rc.top_p = p.top_p; rc.row_t = p.row_t;
+        rc.zhi = Z.hi; rc.zlo = Z.lo;
+        rc.y = (int32_t)y;
+        if (!ok) { rc.mode = REC_BAD; rc.bad_bit = 0u; }
+        else if (p.bad) { rc.mode = REC_BAD; rc.bad_bit = RLK_STATUS_BAD_PARAM; }
+        else if (bad_id) { rc.mode = REC_BAD; rc.bad_bit = RLK_STATUS_BAD_TOKEN_ID; }
+        else if (nonfinite) { rc.mode = REC_BAD; rc.bad_bit = RLK_STATUS_NONFINITE; }
+        else if (!topp) {
+          rc.mode = REC_DONE;
+          const float lz = logf(zf);
+          rc.lp = __fsub_rn(__fmul_rn(kLn2, __fmaf_rn(zy, c, -E)), lz);
+          rc.ent = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, U), zf));
+          rc.lz = lz;
+          rc.kstar = (int32_t)a.V;
+        } else {
+          // The window z >= m - L T as keys [key_lo, key_m].
+          const float L_spec = logf(__fdiv_rn(1.f, __fsub_rn(1.f, p.top_p))) + 7.0f;
+          const float zlo = __fsub_rn(m, __fmul_rn(L_spec, p.temp));
+          const uint32_t key_m = key_of(m);
+          const uint32_t kl = key_of(zlo);
+          const uint32_t key_lo = kl > 0u ? kl - 1u : 0u;
+          const uint32_t dmax = key_m - key_lo;
+          if (key_lo <= key_m && dmax < (uint32_t)HBC) {
+            rc.mode = REC_COUNT;
+            const uint32_t fb = okey16_inverse(key_lo);
+            rc.zf2 = fb | (fb << 16);
+            rc.key_m = key_m;
+            rc.dmax = dmax;
+            rc.key_y = key_of(zy);
+          } else {
+            rc.mode = REC_MARK;
+          }
+        }
+      }
+      // The record buffer and the counts of this buffer were last used two
+      // rows ago: wait until the scan warp is done with them.
+      if (it >= 2)
+        wait_phase(smem_u32(&ctl.hclear[b]), (uint32_t)(((it - 2) >> 1) & 1), abort, g.wait_limit,
+                   a.status);
+      if (lane == 0) {
+        if (*abort && rc.mode != REC_BAD) { rc.mode = REC_BAD; rc.bad_bit = 0u; }
+        ctl.rec[b] = rc;
+        mbar_arrive(smem_u32(&ctl.floorpub[b]));
+      }
+      __syncwarp();
+    }
+  } else if (warp == WSCN) {
+    // ----------------------------------------------------------- scan warp
+    int it = 0;
+    for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x, ++it) {
+      const int b = it & 1;
+      const uint32_t par = (uint32_t)((it >> 1) & 1);
+      bool ok = wait_phase(smem_u32(&ctl.floorpub[b]), par, abort, g.wait_limit, a.status);
+      const RowRec rc = ctl.rec[b];
+      // every row's count phase completes (the compute warps report each one)
+      if (TOPP) ok = wait_phase(smem_u32(&ctl.counted[b]), par, abort, g.wait_limit, a.status) && ok;
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      uint32_t* hist = hist0 + b * HBC;
+      if (!ok || *abort) {
+        if (lane == 0) write_bad(a, r, 0u);
+      } else if (rc.mode == REC_BAD) {
+        if (lane == 0) write_bad(a, r, rc.bad_bit);
+      } else if (rc.mode == REC_DONE) {
+        if (lane == 0) {
+          a.out_logprob[r] = rc.lp;
+          a.out_entropy[r] = rc.ent;
+          if (a.out_k) a.out_k[r] = rc.kstar;
+          if (a.state)
+            a.state[r] = RowState{rc.E, rc.lz, rc.ent, 0u, kTiesAll, kStateValid | kStateYIn,
+                                  rc.kstar, rc.row_t};
+        }
+      } else if (rc.mode == REC_MARK) {
+        if (lane == 0) a.out_logprob[r] = __uint_as_float(kRecomputeMark);
+      } else {
+        ScanOut so{};
+        const DF Z{rc.zhi, rc.zlo};
+        const bool found = warp_scan_window(lane, rc.dmax, rc.key_m, rc.c, rc.E,
+                                            df_mul_f(Z, rc.top_p), hist, rc.key_y, ctl.tie[b], so);
+        if (lane == 0) {
+          if (!found) {
+            a.out_logprob[r] = __uint_as_float(kRecomputeMark);
+          } else {
+            a.out_logprob[r] = so.y_in
+                                   ? __fsub_rn(__fmul_rn(kLn2, __fmaf_rn(rc.zy, rc.c, -rc.E)), so.lz)
+                                   : -INFINITY;
+            a.out_entropy[r] = so.h;
+            if (a.out_k) a.out_k[r] = (int32_t)so.kstar;
+            if (a.state)
+              a.state[r] = RowState{rc.E, so.lz, so.h, so.key_thr, so.ties,
+                                    kStateValid | (so.y_in ? kStateYIn : 0u), (int32_t)so.kstar,
+                                    rc.row_t};
+          }
+        }
+      }
+      if (TOPP && rc.mode == REC_COUNT) {
+        __syncwarp();
+        for (uint32_t d = (uint32_t)lane; d <= rc.dmax; d += 32u) hist[d] = 0u;
+        if (lane == 0) ctl.tie[b] = 0u;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.hclear[b]));
+    }
+  }
+}
+
+}  // namespace
+
+bool lpe_stream_eligible(const LpeArgs& a) {
+  return a.dtype == 0 && a.V >= V_MIN && a.V <= V_MAX;
+}
+
+cudaError_t launch_lpe_stream(const LpeArgs& a, cudaStream_t stream, long long wait_limit,
+                              long long withhold) {
+  Geom g{};
+  g.nunits = (int)((a.V + UNIT - 1) / UNIT);
+  g.nfull = (int)(a.V / UNIT);
+  g.nst = (g.nunits + NTC - 1) / NTC;
+  g.tma = ((reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0 && (a.ld & 7) == 0) ? 1 : 0;
+  g.tma_bytes = (uint32_t)((a.V / 8) * 16);
+  uint32_t off = align_up((uint32_t)sizeof(Ctrl), 128);
+  g.off_part = off;
+  off += 2u * 3u * NTC * 4u;
+  g.off_hist = off;
+  off += 2u * HBC * 4u;
+  g.off_slot = off;
+  off += NTC * 32u;
+  g.skb = align_up((uint32_t)g.nunits * 2u, 16);
+  g.off_sk = off;
+  off += 2u * g.skb;
+  off = align_up(off, 128);
+  g.off_ring = off;
+  off += NSTAGE * STAGE_BYTES;
+  const size_t smem = off;
+  g.wait_limit = wait_limit;
+  g.withhold = withhold;
+  const float c = (float)(1.4426950408889634 / (double)a.temperature);
+  const bool topp = a.temps || a.top_ps || a.top_p < 1.0f;
+
+  // The shared-memory attribute is set once per device and variant.
+  static std::atomic<int> attr[64][4];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int vi = (topp ? 2 : 0) + (g.tma ? 1 : 0);
+  const void* fns[4] = {(const void*)lpe_stream_kernel<false, false>, (const void*)lpe_stream_kernel<false, true>,
+                        (const void*)lpe_stream_kernel<true, false>, (const void*)lpe_stream_kernel<true, true>};
+  const int smax = (int)(align_up(align_up((uint32_t)sizeof(Ctrl), 128) + 2u * 3u * NTC * 4u +
+                                      2u * HBC * 4u + NTC * 32u +
+                                      2u * align_up((uint32_t)(V_MAX / UNIT) * 2u, 16),
+                                  128) +
+                         NSTAGE * STAGE_BYTES);
+  if (dev < 0 || dev >= 64 || attr[dev][vi].load() < smax) {
+    if ((e = cudaFuncSetAttribute(fns[vi], cudaFuncAttributeMaxDynamicSharedMemorySize, smax)) !=
+        cudaSuccess)
+      return e;
+    if (dev >= 0 && dev < 64) attr[dev][vi].store(smax);
+  }
+  const int nsm = sm_count();
+  const int64_t grid = a.T < (int64_t)nsm ? a.T : (int64_t)nsm;
+  switch (vi) {
+    case 0: lpe_stream_kernel<false, false><<<(unsigned)grid, NTB, smem, stream>>>(a, g, c); break;
+    case 1: lpe_stream_kernel<false, true><<<(unsigned)grid, NTB, smem, stream>>>(a, g, c); break;
+    case 2: lpe_stream_kernel<true, false><<<(unsigned)grid, NTB, smem, stream>>>(a, g, c); break;
+    default: lpe_stream_kernel<true, true><<<(unsigned)grid, NTB, smem, stream>>>(a, g, c); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace rlk

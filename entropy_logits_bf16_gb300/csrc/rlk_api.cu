@@ -45,11 +45,67 @@ bool take_injected_failure() {
     if (g_injected_failures.compare_exchange_weak(n, n - 1)) return true;
   return false;
 }
+
+// Bounded device waits: the limit in clock cycles (about a second at the
+// GB300's clocks by default) and a debug stage that the next launch of the
+// streaming scorer withholds (rlk_debug_withhold_copy).
+constexpr long long kDefaultWaitLimit = 1ll << 31;
+static std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+static std::atomic<long long> g_withhold{-1};
+long long debug_wait_limit() { return g_wait_limit.load(); }
+long long debug_take_withheld() { return g_withhold.exchange(-1); }
+
+int grpo_loss_args(const float* logp_new, const float* logp_old, const float* logp_rollout,
+                   const float* logp_ref, const uint8_t* loss_mask, const float* rewards,
+                   const int32_t* seq_offsets, int32_t n_seq, int32_t group_size, int64_t n_tok,
+                   float eps_low, float eps_high, float tis_cap, float kl_coef, int agg,
+                   float* out_loss, float* out_grad, float* out_stats, LossArgs& a) {
+  if (n_seq < 0 || group_size < 1 || n_seq % group_size != 0 || n_tok < 0)
+    return RLK_ERR_INVALID_ARG;
+  if (!(std::isfinite(eps_low) && eps_low >= 0.0f && std::isfinite(eps_high) && eps_high >= 0.0f))
+    return RLK_ERR_INVALID_ARG;
+  if (!(std::isfinite(tis_cap) && tis_cap > 0.0f) || !(std::isfinite(kl_coef) && kl_coef >= 0.0f))
+    return RLK_ERR_INVALID_ARG;
+  if (agg != RLK_AGG_TOKEN_MEAN && agg != RLK_AGG_SEQ_MEAN_TOKEN_MEAN && agg != RLK_AGG_PROMPT_MEAN)
+    return RLK_ERR_INVALID_ARG;
+  if (!seq_offsets || !out_loss) return RLK_ERR_INVALID_ARG;
+  if (n_seq > 0 && (!logp_new || !logp_old || !logp_rollout || !logp_ref || !rewards))
+    return RLK_ERR_INVALID_ARG;
+  a = LossArgs{};
+  a.logp_new = logp_new;
+  a.logp_old = logp_old;
+  a.logp_rollout = logp_rollout;
+  a.logp_ref = logp_ref;
+  a.mask = loss_mask;
+  a.rewards = rewards;
+  a.seq_offsets = seq_offsets;
+  a.n_seq = n_seq;
+  a.group_size = group_size;
+  a.n_tok = n_tok;
+  a.eps_low = eps_low;
+  a.eps_high = eps_high;
+  a.tis_cap = tis_cap;
+  a.kl_coef = kl_coef;
+  a.agg = agg;
+  a.out_loss = out_loss;
+  a.out_grad = out_grad;
+  a.out_stats = out_stats;
+  return RLK_OK;
+}
 }  // namespace rlk
 
 extern "C" {
 
 int rlk_version(void) { return 100; }
+
+long long rlk_debug_set_wait_limit(long long cycles) {
+  return rlk::g_wait_limit.exchange(cycles > 0 ? cycles : rlk::kDefaultWaitLimit);
+}
+
+int rlk_debug_withhold_copy(long long stage) {
+  rlk::g_withhold.store(stage >= 0 ? stage : -1);
+  return 0;
+}
 
 const char* rlk_status_string(rlk_status status) {
   switch (status) {
@@ -289,39 +345,15 @@ rlk_status rlk_grpo_loss(const float* logp_new, const float* logp_old,
                          float kl_coef, rlk_agg agg, float* out_loss,
                          float* out_dloss_dlogp_new, float* out_stats, void* workspace,
                          size_t workspace_bytes, rlk_stream stream) {
-  if (n_seq < 0 || group_size < 1 || n_seq % group_size != 0 || n_tok < 0)
-    return RLK_ERR_INVALID_ARG;
-  if (!(std::isfinite(eps_low) && eps_low >= 0.0f && std::isfinite(eps_high) && eps_high >= 0.0f))
-    return RLK_ERR_INVALID_ARG;
-  if (!finite_positive(tis_cap) || !(std::isfinite(kl_coef) && kl_coef >= 0.0f))
-    return RLK_ERR_INVALID_ARG;
-  if (agg != RLK_AGG_TOKEN_MEAN && agg != RLK_AGG_SEQ_MEAN_TOKEN_MEAN && agg != RLK_AGG_PROMPT_MEAN)
-    return RLK_ERR_INVALID_ARG;
-  if (!seq_offsets || !out_loss) return RLK_ERR_INVALID_ARG;
-  if (n_seq > 0 && (!logp_new || !logp_old || !logp_rollout || !logp_ref || !rewards))
-    return RLK_ERR_INVALID_ARG;
+  rlk::LossArgs a;
+  const int st = rlk::grpo_loss_args(logp_new, logp_old, logp_rollout, logp_ref, loss_mask,
+                                     rewards, seq_offsets, n_seq, group_size, n_tok, eps_low,
+                                     eps_high, tis_cap, kl_coef, (int)agg, out_loss,
+                                     out_dloss_dlogp_new, out_stats, a);
+  if (st != RLK_OK) return (rlk_status)st;
   const size_t need = rlk::loss_workspace_bytes(n_seq);
   if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
     return RLK_ERR_WORKSPACE;
-  rlk::LossArgs a;
-  a.logp_new = logp_new;
-  a.logp_old = logp_old;
-  a.logp_rollout = logp_rollout;
-  a.logp_ref = logp_ref;
-  a.mask = loss_mask;
-  a.rewards = rewards;
-  a.seq_offsets = seq_offsets;
-  a.n_seq = n_seq;
-  a.group_size = group_size;
-  a.n_tok = n_tok;
-  a.eps_low = eps_low;
-  a.eps_high = eps_high;
-  a.tis_cap = tis_cap;
-  a.kl_coef = kl_coef;
-  a.agg = agg;
-  a.out_loss = out_loss;
-  a.out_grad = out_dloss_dlogp_new;
-  a.out_stats = out_stats;
   a.workspace = static_cast<float*>(workspace);
   if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
   return rlk::launch_grpo_loss(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess

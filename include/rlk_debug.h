@@ -35,6 +35,29 @@ rlk_status rlk_lmhead_logits_debug(const void* hidden, const void* w_vocab, int6
  */
 int rlk_debug_inject_launch_failures(int n);
 
+/*
+ * rlk_debug_set_wait_limit -- the number of clock cycles any bounded device
+ * wait of the logprob/entropy scorer and the LM-head kernel may take before
+ * it gives up (default 2^31, about a second).  A wait that runs out sets
+ * RLK_STATUS_TIMEOUT in the call's status word, the rows the kernel has not
+ * finished get NaN outputs, copies already issued are allowed to land, and
+ * the kernel returns, so the context stays usable.  cycles <= 0 restores the
+ * default.  Returns the previous limit.  Not thread-safe with respect to
+ * concurrent launches.
+ */
+long long rlk_debug_set_wait_limit(long long cycles);
+
+/*
+ * rlk_debug_withhold_copy -- makes the next rlk_logprob_entropy launch (and
+ * the next LM-head forward launch) skip one of the bulk copies of its first
+ * CTA: the stage with the given index in that CTA's sequence, for which no
+ * copy is issued and no arrival made.  The wait on it then runs out (after
+ * the limit set above), which exercises the expiry path; nothing is left in
+ * flight.  stage < 0 clears it.  The setting is consumed by one launch.
+ * Returns 0.
+ */
+int rlk_debug_withhold_copy(long long stage);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif
