@@ -194,7 +194,7 @@ __device__ __forceinline__ void rebase(Acc& st, float En) {
 // words w[0..7] hold the logits in the order the thread reads them (two bf16
 // a word, low half first).  MASKED: only the logits whose bit is set in vmask
 // (bit j: half j & 1 of word j >> 1) exist -- the row's last, partial unit.
-template <bool MASKED>
+template <bool MASKED, bool UNIFORM = false>
 __device__ __forceinline__ float absorb_unit(Acc& st, const uint32_t (&w)[8], float c,
                                              uint32_t vmask = 0xFFFFu) {
   uint32_t wm[8];
@@ -213,7 +213,14 @@ __device__ __forceinline__ float absorb_unit(Acc& st, const uint32_t (&w)[8], fl
   const float gm = fmaxf(bf16_lo(mw), bf16_hi(mw));
   st.mx = fmaxf(st.mx, gm);
   // rare after a row's first units (E = -inf before the first: always taken)
-  if (__fmaf_rn(gm, c, -st.E) > LAZY) rebase(st, ceilf(__fmul_rn(gm, c)));
+  const bool up = __fmaf_rn(gm, c, -st.E) > LAZY;
+  if (UNIFORM) {   // every lane is here: one warp-uniform test guards the rare re-base
+    if (__any_sync(0xFFFFFFFFu, up)) {
+      if (up) rebase(st, ceilf(__fmul_rn(gm, c)));
+    }
+  } else if (up) {
+    rebase(st, ceilf(__fmul_rn(gm, c)));
+  }
   const float2 c2 = make_float2(c, c);
   const float2 nE2 = make_float2(-st.E, -st.E);
   // Two halves of four words: sum ((e0+e1)+(e2+e3)) + ((e4+e5)+(e6+e7)) and
@@ -389,6 +396,20 @@ __device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, volatil
   return wait_phase(bar, parity, abort, limit, status);
 }
 
+// wait_full for a whole warp, its lanes agreeing on the result.
+__device__ __forceinline__ bool wait_full_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               long long limit, uint32_t* status) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(100000u)
+      : "memory");
+  if (__all_sync(0xFFFFFFFFu, ok != 0u)) return true;
+  return __all_sync(0xFFFFFFFFu, wait_phase(bar, parity, abort, limit, status));
+}
+
 // Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool test_phase(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -438,12 +459,27 @@ __device__ __forceinline__ void count_unit(const uint4* slot, int u, uint32_t zf
   const uint4 v0 = slot[0], v1 = slot[1];
   const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
   const __nv_bfloat162 zf2 = bf2(zf2w);
-  uint32_t msk = 0u;   // bit e: logit e of the unit reaches the floor
+  uint32_t hm[8], cnt = 0u;   // per word: 0xFFFF in each half that reaches the floor
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const uint32_t hm = __hge2_mask(bf2(w[k]), zf2);
-    msk |= ((hm & 1u) | ((hm >> 15) & 2u)) << (2 * k);
+    hm[k] = __hge2_mask(bf2(w[k]), zf2);
+    cnt += hm[k] & 0x00010001u;
   }
+  if ((cnt & 0xFFFFu) + (cnt >> 16) == 1u) {
+    // The unit's only token in the window is its max (the usual case).
+    const __nv_bfloat162 m01 = __hmax2(bf2(w[0]), bf2(w[1])), m23 = __hmax2(bf2(w[2]), bf2(w[3]));
+    const __nv_bfloat162 m45 = __hmax2(bf2(w[4]), bf2(w[5])), m67 = __hmax2(bf2(w[6]), bf2(w[7]));
+    const __nv_bfloat162 mm = __hmax2(__hmax2(m01, m23), __hmax2(m45, m67));
+    const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mm);
+    const uint32_t kk = okey16(__float_as_uint(fmaxf(bf16_lo(mw), bf16_hi(mw))) >> 16);
+    if (kk != key_y) {
+      atomicAdd(&hist[key_m - kk], 1u);
+      return;
+    }
+  }
+  uint32_t msk = 0u;   // bit e: logit e of the unit reaches the floor
+#pragma unroll
+  for (int k = 0; k < 8; ++k) msk |= ((hm[k] & 1u) | ((hm[k] >> 15) & 2u)) << (2 * k);
   const uint16_t* e16 = reinterpret_cast<const uint16_t*>(slot);
   const int32_t col0 = u * UNIT;
   while (msk) {
@@ -472,7 +508,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(smem_u32(&ctl.full[s]), 1u);
-      mbar_init(smem_u32(&ctl.empty[s]), (uint32_t)NWC);
+      mbar_init(smem_u32(&ctl.empty[s]), (uint32_t)NTC);   // every compute lane releases
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl.rowpub[b]), (uint32_t)NWC);
@@ -505,6 +541,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
     uint32_t sw_par = 0u, tie = 0u;
     int sw_tot = 0, sw_q = 0;
     bool sw_pend = false, sw_mine = false;
+    int sw_u = 0;   // the unit this lane staged for the pending round
     const uint16_t* sw_row = logits;
     uint32_t rc_zf2 = 0u, rc_key_m = 0u, rc_key_y = 0u;   // the record fields the count needs
     int32_t rc_y = 0;
@@ -561,16 +598,15 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       if (sw_pend) {
         cp_async_wait_all();
         if (sw_mine)
-          count_unit(myslot, (int)*list_at(sw_q - 32 + lane), rc_zf2, rc_key_m, rc_key_y, rc_y,
-                     hist0 + sw_b * HBC, tie);
+          count_unit(myslot, sw_u, rc_zf2, rc_key_m, rc_key_y, rc_y, hist0 + sw_b * HBC, tie);
         sw_pend = false;
       }
       if (sw_q < sw_tot) {
         const int k = sw_q + lane;
         sw_mine = k < sw_tot;
         if (sw_mine) {
-          const int u = (int)*list_at(k);
-          stage_unit(sw_row, a.V, u, TMA && u < g.nfull, myslot);
+          sw_u = (int)*list_at(k);
+          stage_unit(sw_row, a.V, sw_u, TMA && sw_u < g.nfull, myslot);
         }
         sw_q += 32;
         sw_pend = true;
@@ -599,7 +635,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       // on every stage but the last), release the slot, then side work.
       auto stage = [&](int s, bool last) {
         const uint32_t slot = gs & (NSTAGE - 1);
-        const bool ok = wait_full(smem_u32(&ctl.full[slot]), (gs / NSTAGE) & 1u, abort, g.wait_limit,
+        const bool ok = wait_full_warp(smem_u32(&ctl.full[slot]), (gs / NSTAGE) & 1u, abort, g.wait_limit,
                                   a.status);
         const int u = t + s * NTC;
         if (ok && (!last || u < g.nunits)) {
@@ -614,7 +650,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
             } else {
               load_unit_scalar(row, a.V, u, h, w);
             }
-            gm = absorb_unit<false>(st, w, c);
+            gm = last ? absorb_unit<false>(st, w, c) : absorb_unit<false, true>(st, w, c);
           } else {
             // the row's last, partial unit: slot j of the words holds logit
             // 8 * (j < 8 ? h : 1 - h) + (j & 7) of the unit
@@ -628,8 +664,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
           }
           if (TOPP) sk[u] = (uint16_t)(__float_as_uint(gm) >> 16);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl.empty[slot]));
+        mbar_arrive(smem_u32(&ctl.empty[slot]));   // this lane is done with the slot
         ++gs;
         if (TOPP) {
           if (sw == 1 && !last) side_start(false);
