@@ -43,10 +43,13 @@ TOP_P = 0.95
 ROW_BYTES = VOCAB * 2
 BYTES_PER_TOKEN = ROW_BYTES + 4 + 12     # logits row + id + (logprob, entropy, k*) outputs
 METRIC = "tokens/s for top-p logprob+entropy at V=151936 bf16; % of HBM roofline"
-KERNEL_SRC = os.path.join(ROOT, "entropy_logits_bf16_gb300", "csrc", "lpe_cluster.cu")
-PROFILE = os.path.join(ROOT, "profiles", "lpe_cluster_kernel_qwen_T4096.txt")
+KERNEL_SRC = os.path.join(ROOT, "entropy_logits_bf16_gb300", "csrc", "lpe_stream.cu")
+PROFILE = os.path.join(ROOT, "profiles", "lpe_stream_kernel_qwen_T4096.txt")
 WORKLOAD = (f"Qwen3-8B-shaped logits T={T_ROWS} V={VOCAB} bf16 = 3 N(0,1) + one peak U(5,15) "
-            f"per row; temperature {TEMPERATURE}, top_p {TOP_P}")
+            f"per row; temperature {TEMPERATURE}, top_p {TOP_P}; ids drawn from each row's "
+            f"truncated distribution")
+HBM_NOMINAL_GBS = 7900.0      # GB300 HBM3e nominal bandwidth
+BF16_NOMINAL_TFLOPS = 2250.0  # GB300 dense bf16 nominal
 
 
 def dist_env():
@@ -168,12 +171,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def sampled_ids(z, seed, temperature=TEMPERATURE, top_p=TOP_P):
+    """Each row's selected id drawn from its temperature-scaled, top-p-truncated,
+    renormalised distribution (the library's deterministic sampler, whose draws
+    are tested against the oracle's inverse-CDF sampler), with seeded uniforms.
+    Runs before any timed region."""
+    import entropy_logits_bf16_gb300 as rlk
+    import workloads
+    u = torch.from_numpy(np.ascontiguousarray(workloads.uniforms(z.shape[0], seed),
+                                              dtype=np.float32)).to(z.device)
+    return rlk.sample_top_p(z, temperature, top_p, u)
+
+
 def make_workload(device, seed):
     import workloads
-    z, peaks = workloads.peaked_bf16(T_ROWS, VOCAB, seed=seed, device=device)
-    # The selected token of each row is its peaked token: the kernel's work
-    # does not depend on which id is selected (one extra element load).
-    return z, peaks.to(torch.int32)
+    z, _ = workloads.peaked_bf16(T_ROWS, VOCAB, seed=seed, device=device)
+    return z, sampled_ids(z, 1000 + seed)
 
 
 def cpu_baseline(z, ids, min_seconds=10.0, max_reps=8):
@@ -209,7 +222,7 @@ def run_reference(args):
     rows_per_step = 64
     z, peaks = workloads.peaked_bf16(rows_per_step * 4, VOCAB, seed=1, device="cpu")
     hz = workloads.bf16_bits(z)
-    hid = peaks.numpy().astype(np.int32)
+    hid = oracle.sample_ids(hz, TEMPERATURE, TOP_P, workloads.uniforms(hz.shape[0], 1001))
     threads = oracle.default_threads()
     # the loss stage on each step's log-probs, as in the device step: the
     # sample's 64 tokens as 8 responses of 8 tokens in one group of 8;
@@ -240,10 +253,15 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "T": T_ROWS, "V": VOCAB, "temperature": TEMPERATURE,
-                   "top_p": TOP_P, "global_batch": T_ROWS, "loss": LOSS_CFG,
-                   "parallelism": "host cores, rank 0 only",
-                   "rows_per_step": rows_per_step},
+        "config": {"workload": WORKLOAD, "T": rows_per_step, "V": VOCAB,
+                   "temperature": TEMPERATURE, "top_p": TOP_P, "global_batch": rows_per_step,
+                   "loss": (f"GRPO/DAPO loss on the step's log-probs: {n_seq} sequences x 8 tokens, "
+                            f"group 8, eps 0.2/0.28, TIS cap 2.0, k3 KL 0.01, token mean"),
+                   "parallelism": "host cores, rank 0 only", "rows_per_step": rows_per_step,
+                   "same_config": False,
+                   "same_config_reason": (f"the fp64 oracle scores {rows_per_step} rows of the "
+                                          f"{T_ROWS}-row device workload per step (a bounded "
+                                          f"sample), then an {n_seq} x 8-token loss")},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows_per_step} rows per step of the same workload, then "
                                    f"the loss on their log-probs ({n_seq} responses x 8 tokens, "
@@ -385,6 +403,20 @@ def run_logits(args, ws, rank, dev, barrier):
     e1.record(stream)
     barrier()
     e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, dev)
+    cpu_line = cpu_baseline(z, ids) if (ws == 1 and rank == 0 and not args.no_cpu_baseline) else None
+    h2d_bytes = int(sum(t.numel() * t.element_size() for t in host))
+    legs = None
+    if not args.no_legs:   # every rank runs them (their timings cross ranks)
+        del z, dev_in, host
+        torch.cuda.empty_cache()
+        legs = {}
+        for name, fn in (("long_response_zipf_stress", lambda: leg_zipf(args, ws, rank, dev, barrier, 1.0)),
+                         ("long_response_zipf_calibrated",
+                          lambda: leg_zipf(args, ws, rank, dev, barrier, None)),
+                         ("grpo_packed_591k", lambda: leg_grpo(args, ws, rank, dev, barrier)),
+                         ("fused_lmhead", lambda: leg_lmhead(args, ws, rank, dev, barrier))):
+            legs[name] = fn()
+            torch.cuda.empty_cache()
     if rank != 0:
         return None
     peaks, peak_kind = measured_peaks()
@@ -401,26 +433,249 @@ def run_logits(args, ws, rank, dev, barrier):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "inputs (1.24 GB per GPU) larger than L2; no flush between steps",
                    "step_ms": {"logprob_entropy": part_ms[0], "grpo_loss": part_ms[1]}},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": profiled_traffic(), "peak_source": peak_kind,
-                     "kernel": "lpe_cluster_kernel<top_p<1> (+ the per-row recompute pass, "
-                               "timed together as one rlk_logprob_entropy call)",
-                     "bytes_per_token": BYTES_PER_TOKEN, "tokens_per_launch": T_ROWS,
-                     "launch_ms": launch_ms},
+        "roofline": hbm_roofline(achieved, peaks, peak_kind, launch_ms, clk,
+                                 kernel="lpe_stream_kernel<top_p<1> (+ the per-row recompute pass, "
+                                        "timed together as one rlk_logprob_entropy call)",
+                                 traffic=profiled_traffic(), bytes_per_token=BYTES_PER_TOKEN,
+                                 tokens_per_launch=T_ROWS),
         "e2e": {"value": T_ROWS * ws / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host)),
+                "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": int(out_h.numel() * 4)},
-        # cluster kernel + recompute pass + the loss's three kernels, per step
+        # streaming kernel + recompute pass + the loss's three kernels, per step
         "gpu_launches": 5 * args.steps,
         "clocks": clk,
     }
-    if ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(z, ids)
+    if cpu_line is not None:
+        line["cpu_baseline"] = cpu_line
+    if legs is not None:
+        line["legs"] = legs
     return line
 
 
-def run_lmhead(args, ws, rank, dev, barrier, top_p=1.0):
+def hbm_roofline(achieved, peaks, peak_kind, launch_ms, clk, **extra):
+    """The HBM roofline entry: the fraction of the measured copy bandwidth
+    (the task's denominator), with the nominal HBM3e bandwidth and the clock
+    the launch ran at beside it."""
+    r = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+         "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_kind,
+         "peak_nominal": HBM_NOMINAL_GBS, "frac_of_nominal": achieved / HBM_NOMINAL_GBS,
+         "launch_ms": launch_ms}
+    r.setdefault("traffic", None)
+    r.update(extra)
+    if clk:
+        r["sm_mhz_median"] = clk["sm_mhz"]
+        r["launch_ms_x_sm_ghz"] = launch_ms * clk["sm_mhz"] / 1e3
+    return r
+
+
+def leg_args(args, steps):
+    class A:
+        pass
+    a = A()
+    a.steps = min(args.steps, steps)
+    a.warmup = max(args.warmup, 3)
+    a.no_cpu_baseline = args.no_cpu_baseline
+    return a
+
+
+def leg_zipf(args, ws, rank, dev, barrier, kappa):
+    """Long-response batch: 8 responses x 6912 tokens (T = 55,296 rows), V =
+    151,936 bf16 rows with Zipf-tilted means, temperature 0.7, top_p 0.95, ids
+    drawn from the truncated distributions.  kappa None: the calibrated rows
+    (nucleus sizes 1 to ~5000); 1.0: the wider stress rows.  Rows the streaming
+    kernel hands to the per-row kernel are counted from the row state (the
+    per-row kernel's reference exponent is not an integer)."""
+    import entropy_logits_bf16_gb300 as rlk
+    import workloads
+    rows = 8 * 6912
+    k = workloads.ZIPF_KAPPA_CALIBRATED if kappa is None else kappa
+    z, _ = workloads.zipf_bf16(rows, seed=2 + 100 * rank, kappa=k, sigma=workloads.ZIPF_SIGMA,
+                               device=dev)
+    ids = sampled_ids(z, 2000 + rank)
+    lp = torch.empty(rows, device=dev)
+    ent = torch.empty(rows, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def f():
+        rlk.logprob_entropy(z, ids, TEMPERATURE, TOP_P, out_logprob=lp, out_entropy=ent)
+
+    la = leg_args(args, 5)
+    elapsed_ms, part_ms, clk = timed_steps(la, ws, dev, stream, [f], barrier)
+    st = rlk.new_row_state(rows, dev)
+    _, _, ks = rlk.logprob_entropy(z, ids, TEMPERATURE, TOP_P, row_state=st, return_nucleus_size=True)
+    E = st[:, 0].contiguous().view(torch.float32)
+    recomputed = float((E != torch.floor(E)).float().mean().item())
+    kq = torch.quantile(ks.float()[::7], torch.tensor([0.0, 0.5, 0.9, 0.99, 1.0], device=dev)).tolist()
+    peaks, peak_kind = measured_peaks()
+    achieved = rows * BYTES_PER_TOKEN / (part_ms[0] / 1e3) / 1e9
+    out = {"metric": "tokens/s", "value": whole_job_rate(rows, la.steps, ws, elapsed_ms),
+           "unit": "tokens/s", "steps": la.steps, "ms_per_step": elapsed_ms / la.steps,
+           "config": {"workload": (f"long-response batch 8 x 6912 = {rows} rows, V={VOCAB} bf16, "
+                                   f"z = bf16(-kappa s ln rank + sigma N(0,1)), s ~ U(0.8,1.4), "
+                                   f"kappa {k}, sigma {workloads.ZIPF_SIGMA}, temperature "
+                                   f"{TEMPERATURE}, top_p {TOP_P}; ids from the truncated "
+                                   f"distribution; boundary ties not injected"),
+                      "T": rows, "V": VOCAB, "kappa": k, "sigma": workloads.ZIPF_SIGMA,
+                      "nucleus_size_quantiles_0_50_90_99_100": [round(x) for x in kq],
+                      "rows_recomputed_by_per_row_kernel": recomputed,
+                      "l2": "inputs (16.8 GB) larger than L2"},
+           "roofline": hbm_roofline(achieved, peaks, peak_kind, part_ms[0], clk,
+                                    kernel="one rlk_logprob_entropy call (streaming kernel + "
+                                           "per-row recompute pass)",
+                                    bytes_per_token=BYTES_PER_TOKEN, tokens_per_launch=rows),
+           "clocks": clk}
+    if ws == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        sel = np.linspace(0, rows - 1, 96).astype(np.int64)
+        sel_t = torch.from_numpy(sel).to(dev)
+        hz = workloads.bf16_bits(z[sel_t])
+        hid = ids[sel_t].cpu().numpy()
+        threads = oracle.default_threads()
+        oracle.build()
+        t0 = time.perf_counter()
+        oracle.logprob_entropy(hz, hid, TEMPERATURE, TOP_P, threads=threads)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": len(sel) / dt, "unit": "tokens/s", "cores": threads,
+                               "kind": "oracle",
+                               "sample": f"{len(sel)} evenly spaced rows, fp64 oracle, {threads} "
+                                         f"threads, {dt:.2f} s"}
+    del z
+    return out
+
+
+def leg_grpo(args, ws, rank, dev, barrier):
+    """GRPO/DAPO batch: 64 prompts x group 8, response lengths U{256..2048}
+    packed (591,145 tokens at seed 3), logits as the Qwen3-shaped rows scored
+    16,384 rows at a time (each chunk regenerated from the seeded generator
+    before its scorer call, outside the timed events), then the loss over all
+    tokens with old / rollout / reference log-probs = the first pass's
+    log-probs + N(0, 0.01^2).  Timed: the scorer calls and the loss."""
+    import entropy_logits_bf16_gb300 as rlk
+    import workloads
+    off_h, R_h = workloads.grpo_batch(64, 8, 256, 2048, seed=3)
+    n = int(off_h[-1])
+    CH = 16384
+    chunks = [(c0, min(CH, n - c0)) for c0 in range(0, n, CH)]
+    lp = torch.empty(n, device=dev)
+    ent = torch.empty(n, device=dev)
+    ids_all = torch.empty(n, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def chunk(c0, cn):
+        z, _ = workloads.peaked_bf16(cn, VOCAB, seed=3 + 100 * rank, device=dev, row0=c0)
+        return z
+
+    for c0, cn in chunks:   # ids from each chunk's truncated distributions, and a first pass
+        z = chunk(c0, cn)
+        ids_all[c0:c0 + cn] = sampled_ids(z, 3000 + c0 + rank)
+        rlk.logprob_entropy(z, ids_all[c0:c0 + cn], TEMPERATURE, TOP_P,
+                            out_logprob=lp[c0:c0 + cn], out_entropy=ent[c0:c0 + cn])
+        del z
+    lp_h = lp.cpu().numpy()
+    finite = np.isfinite(lp_h)
+    old_h, ro_h, ref_h = workloads.perturbed_logps(np.where(finite, lp_h, -20.0), 9 + rank)
+    tdev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    old, ro, ref, R, off = tdev(old_h), tdev(ro_h), tdev(ref_h), tdev(R_h), tdev(off_h)
+    n_seq = len(R_h)
+    wsb = rlk.workspace_size(1, n, n_seq)
+    wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    loss = torch.empty(1, device=dev)
+    grad = torch.empty(n, device=dev)
+    new = torch.empty(n, device=dev)
+
+    lib = rlk.load()
+    stats = torch.empty(8, device=dev)
+
+    def run_loss():
+        torch.where(torch.isfinite(lp), lp, old, out=new)
+        code = lib.rlk_grpo_loss(rlk._ptr(new), rlk._ptr(old), rlk._ptr(ro), rlk._ptr(ref), None,
+                                 rlk._ptr(R), rlk._ptr(off), n_seq, 8, n, 0.2, 0.28, 2.0, 0.01, 0,
+                                 rlk._ptr(loss), rlk._ptr(grad), rlk._ptr(stats), rlk._ptr(wsp),
+                                 wsb, rlk._stream(dev))
+        if code != 0:
+            raise RuntimeError(f"rlk_grpo_loss returned {code}")
+
+    steps = min(args.steps, 2)
+    score_ms, loss_ms = [], []
+    clocks = ClockSampler(dist_env()[2] if ws > 1 else 0)
+    for it in range(steps + 1):
+        if it == 1:
+            clocks.start()
+        t_sc = 0.0
+        for c0, cn in chunks:
+            z = chunk(c0, cn)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            e0.record(stream)
+            rlk.logprob_entropy(z, ids_all[c0:c0 + cn], TEMPERATURE, TOP_P,
+                                out_logprob=lp[c0:c0 + cn], out_entropy=ent[c0:c0 + cn])
+            e1.record(stream)
+            barrier()
+            t_sc += e0.elapsed_time(e1)
+            del z
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run_loss()
+        e1.record(stream)
+        barrier()
+        if it > 0:
+            score_ms.append(t_sc)
+            loss_ms.append(e0.elapsed_time(e1))
+    clk = clocks.stop()
+    sc = reduce_max(sum(score_ms) / steps, dev)
+    ls = reduce_max(sum(loss_ms) / steps, dev)
+    peaks, peak_kind = measured_peaks()
+    achieved = n * BYTES_PER_TOKEN / (sc / 1e3) / 1e9
+    out = {"metric": "tokens/s", "value": n * ws / ((sc + ls) / 1e3), "unit": "tokens/s",
+           "steps": steps, "ms_per_step": sc + ls,
+           "step_ms": {"logprob_entropy_all_chunks": sc, "grpo_loss": ls},
+           "config": {"workload": (f"GRPO/DAPO: 64 prompts x group 8, lengths U{{256..2048}} packed "
+                                   f"({n} tokens, seed 3); Qwen3-shaped logits V={VOCAB} bf16 "
+                                   f"scored {CH} rows at a time ({len(chunks)} chunks, "
+                                   f"regenerated outside the timed events); rewards "
+                                   f"Bernoulli(0.5); old/rollout/ref = new + N(0, 0.01^2); "
+                                   f"eps 0.2/0.28, TIS cap 2.0, k3 KL 0.01, token mean"),
+                      "tokens": n, "sequences": n_seq, "chunk_rows": CH},
+           "roofline": hbm_roofline(achieved, peaks, peak_kind, sc, clk,
+                                    kernel="the rlk_logprob_entropy calls over all chunks",
+                                    bytes_per_token=BYTES_PER_TOKEN, tokens_per_launch=n),
+           "loss_roofline_note": "the loss reads ~21 B a token and is launch/latency-bound",
+           "clocks": clk}
+    if ws == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.default_threads()
+        oracle.build()
+        z = chunk(0, CH)
+        sel = np.arange(0, CH, 256)
+        sel_t = torch.from_numpy(sel).to(dev)
+        hz = workloads.bf16_bits(z[sel_t])
+        hid = ids_all[sel_t].cpu().numpy()
+        del z
+        t0 = time.perf_counter()
+        oracle.logprob_entropy(hz, hid, TEMPERATURE, TOP_P, threads=threads)
+        t_rows = (time.perf_counter() - t0) / len(sel)
+        new_h = np.where(finite, lp_h, old_h).astype(np.float32)
+        t0 = time.perf_counter()
+        oracle.grpo_loss(new_h, old_h, ro_h, ref_h, None, R_h, off_h, 8)
+        t_loss = time.perf_counter() - t0
+        est = n * t_rows + t_loss
+        out["cpu_baseline"] = {"value": n / est, "unit": "tokens/s", "cores": threads,
+                               "kind": "oracle",
+                               "sample": (f"{len(sel)} rows (every 256th of the first chunk) "
+                                          f"scored at {t_rows * 1e3:.1f} ms a row on {threads} "
+                                          f"threads, extrapolated to all {n} rows, plus the "
+                                          f"loss over all tokens ({t_loss:.2f} s)")}
+    return out
+
+
+def leg_lmhead(args, ws, rank, dev, barrier):
+    """The fused LM-head (config 5) at top_p 1, as --op lmhead, without the
+    end-to-end copy."""
+    line = run_lmhead(leg_args(args, 5), ws, rank, dev, barrier, top_p=1.0, leg=True)
+    return line
+
+
+def run_lmhead(args, ws, rank, dev, barrier, top_p=1.0, leg=False):
     """--op lmhead: the fused LM-head (tcgen05 GEMM + online log-sum-exp
     epilogue) on hidden [16384, 4096] and W [151936, 4096] bf16, top_p 1.
     --op lmhead_topp: the same at top_p 0.95 (bf16 logits emitted 4096 rows at
@@ -439,6 +694,44 @@ def run_lmhead(args, ws, rank, dev, barrier, top_p=1.0):
         rlk.lmhead_logprob(hidden, w, ids, TEMPERATURE, top_p, workspace=wsp)
 
     elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [lm], barrier)
+    if leg:
+        peaks, peak_kind = measured_peaks()
+        flops = 2.0 * LM_T * LM_H * VOCAB
+        achieved = flops / (part_ms[0] / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0))
+        out = {"metric": "tokens/s", "value": whole_job_rate(LM_T, args.steps, ws, elapsed_ms),
+               "unit": "tokens/s", "steps": args.steps, "ms_per_step": elapsed_ms / args.steps,
+               "config": {"workload": f"fused LM-head: hidden [{LM_T}, {LM_H}] bf16 N(0,1), W_vocab "
+                                      f"[{VOCAB}, {LM_H}] bf16 N(0, 0.02^2), temperature "
+                                      f"{TEMPERATURE}, top_p 1, uniform ids; logits never stored"},
+               "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                            "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_kind,
+                            "peak_kind": "bf16 sustained (cuBLAS bf16 GEMM back to back)",
+                            "peak_nominal": BF16_NOMINAL_TFLOPS,
+                            "frac_of_nominal": achieved / BF16_NOMINAL_TFLOPS,
+                            "kernel": "lmhead_kernel + lmhead_combine_kernel",
+                            "flops_per_launch": flops, "launch_ms": part_ms[0]},
+               "clocks": clk}
+        if clk:
+            out["roofline"]["sm_mhz_median"] = clk["sm_mhz"]
+        if ws == 1 and rank == 0 and not args.no_cpu_baseline:
+            import oracle
+            rows = 64
+            sel = np.linspace(0, LM_T - 1, rows).astype(np.int64)
+            hb = workloads.bf16_bits(hidden[torch.from_numpy(sel).to(dev)])
+            wb = workloads.bf16_bits(w)
+            threads = oracle.default_threads()
+            oracle.build()
+            t0 = time.perf_counter()
+            oracle.lmhead_rows(hb, wb, np.arange(rows), ids.cpu().numpy()[sel], TEMPERATURE, 1.0,
+                               threads=threads)
+            dt = time.perf_counter() - t0
+            out["cpu_baseline"] = {"value": rows / dt, "unit": "tokens/s", "cores": threads,
+                                   "kind": "oracle",
+                                   "sample": f"{rows} evenly spaced rows, fp64 oracle, {threads} "
+                                             f"threads, {dt:.2f} s"}
+        del hidden, w
+        return out
     host_h = torch.empty(hidden.shape, dtype=hidden.dtype, pin_memory=True).copy_(hidden)
     host_i = torch.empty(ids.shape, dtype=ids.dtype, pin_memory=True).copy_(ids)
     dh, di = torch.empty_like(hidden), torch.empty_like(ids)
@@ -807,6 +1100,8 @@ def main():
                          "gradient; backward: the dense top-p gradient; lmhead_backward: the "
                          "LM-head gradients")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-legs", action="store_true",
+                    help="logits only: skip the long-response, packed GRPO and LM-head legs")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

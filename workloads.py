@@ -92,6 +92,15 @@ def peaked_bf16(T: int, V: int = VOCAB, seed: int = 1, device="cpu", row0: int =
     return out, peaks
 
 
+# The long-response configuration's rows, calibrated so that their nucleus
+# sizes at temperature 0.7 / top_p 0.95 span 1 to ~5000 (tests/golden/
+# zipf_calibration.py, whose output zipf_calibration.txt records the
+# candidates and the histogram).  kappa = 1.0 gives a wider stress batch
+# (nuclei up to ~34,000 tokens).
+ZIPF_KAPPA_CALIBRATED = 1.15
+ZIPF_SIGMA = 0.5
+
+
 def zipf_bf16(T: int, V: int = VOCAB, seed: int = 2, kappa: float = 1.0, sigma: float = 0.5,
               device="cpu"):
     """Long-response rows with Zipf-tilted means.
