@@ -12,7 +12,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "librlk.so")
-SOURCES = ["rlk_api.cu", "logprob_entropy.cu", "lpe_cluster.cu", "lpe_stream.cu", "lpe_backward.cu", "support.cu", "vocab_parallel.cu", "sampler.cu", "grpo_loss.cu", "lmhead.cu"]
+SOURCES = ["rlk_api.cu", "logprob_entropy.cu", "lpe_stream.cu", "lpe_backward.cu", "support.cu", "vocab_parallel.cu", "sampler.cu", "grpo_loss.cu", "lmhead.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 INCLUDES = ["rlk.h", "rlk_debug.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -55,7 +55,7 @@ struct LpeBwdArgs {
   uint32_t* status;
 };
 
-// A quiet-NaN payload that no arithmetic produces: the cluster kernel leaves it
+// A quiet-NaN payload that no arithmetic produces: the streaming kernel leaves it
 // in out_logprob for rows that the per-row kernel must recompute.
 constexpr uint32_t kRecomputeMark = 0x7FC0DEADu;
 
@@ -175,9 +175,6 @@ bool take_injected_failure();
 int sm_count();
 
 cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream);
-// Cluster-resident kernel for large-vocabulary bf16 rows (lpe_cluster.cu).
-bool lpe_cluster_eligible(const LpeArgs& a);
-cudaError_t launch_lpe_cluster(const LpeArgs& a, cudaStream_t stream);
 // Streaming kernel for every bf16 batch of a large vocabulary (lpe_stream.cu).
 // wait_limit: clock cycles a device wait may take; withhold: a debug stage
 // index the first CTA never issues (-1: none).

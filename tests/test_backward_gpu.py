@@ -84,8 +84,8 @@ def test_backward_matches_oracle_bf16(cuda_lib, oracle, T, p, V, pad):
 
 
 @pytest.mark.parametrize("p", [0.95, 0.6, 1.0])
-def test_backward_full_vocab_cluster_rows(cuda_lib, oracle, p):
-    """V = 151936 bf16: the cluster kernel's states (and the per-row
+def test_backward_full_vocab_stream_rows(cuda_lib, oracle, p):
+    """V = 151936 bf16: the streaming kernel's states (and the per-row
     recompute pass's), tie rows included; bf16 and fp32 gradients."""
     V, R, T = 151936, 24, 0.7
     rng = np.random.default_rng(17)
@@ -99,12 +99,12 @@ def test_backward_full_vocab_cluster_rows(cuda_lib, oracle, p):
     check_nucleus_sizes(oracle, hz, ids, T, p, k)
     og = oracle.logprob_entropy_backward(hz, ids, T, p, glp.astype(np.float32),
                                          gh.astype(np.float32), force_k=k)
-    _check(g, og, _vals(hz), k, label="cluster fp32 grads")
+    _check(g, og, _vals(hz), k, label="stream fp32 grads")
     gb, _, _ = _run(cuda_lib, z, ids, T, p, glp, gh, grad_dtype=torch.bfloat16)
     assert gb.dtype == torch.bfloat16
     # bf16 gradients are the fp32 ones rounded to nearest
     assert torch.equal(gb, g.to(torch.bfloat16))
-    _check(gb, og, _vals(hz), k, rel=2.0 ** -8, label="cluster bf16 grads")
+    _check(gb, og, _vals(hz), k, rel=2.0 ** -8, label="stream bf16 grads")
 
 
 @pytest.mark.parametrize("p", [0.9, 1.0])

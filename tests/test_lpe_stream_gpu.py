@@ -1,8 +1,8 @@
-"""The cluster-resident logprob/entropy path (16-byte aligned bf16 rows of a
-large vocabulary) against the fp64 oracle: rows it finishes itself, rows it
-hands to the per-row kernel (windows that cross zero, flat rows), bad rows,
-vocabulary sizes with a partial last group, the smallest and largest
-vocabularies it takes, and batches smaller than the number of clusters.
+"""The streaming logprob/entropy path (bf16 rows of a large vocabulary)
+against the fp64 oracle: rows it finishes itself, rows it hands to the
+per-row kernel (windows that cross zero, flat rows), bad rows, vocabulary
+sizes with a partial last unit, the smallest and largest vocabularies it
+takes and one just past them, and batches smaller than the number of SMs.
 Same tolerances as the other parity tests; outputs must be bitwise identical
 whatever the batch around a row.
 """
@@ -52,7 +52,7 @@ def check(rlk, oracle, z, ids_h, T, p, label):
 
 @pytest.mark.parametrize("T", [0.7, 1.8])
 @pytest.mark.parametrize("p", [0.5, 0.95, 0.999, 1.0])
-def test_cluster_special_rows(cuda_lib, oracle, T, p):
+def test_stream_special_rows(cuda_lib, oracle, T, p):
     z, _ = special_rows(151936, seed=31)
     z = z.cuda()
     hz = workloads.bf16_bits(z)
@@ -63,12 +63,13 @@ def test_cluster_special_rows(cuda_lib, oracle, T, p):
     check(cuda_lib, oracle, z, far, T, p, f"special-far T{T} p{p}")
 
 
-@pytest.mark.parametrize("V,ld", [(13000, 13000), (151931, 151936), (171999, 172000),
-                                  (172001, 172008), (20000, 20480)])
+@pytest.mark.parametrize("V,ld", [(14847, 14848), (14848, 14848), (151931, 151936),
+                                  (174080, 174080), (174081, 174088), (20000, 20480)])
 @pytest.mark.parametrize("p", [0.9, 1.0])
-def test_cluster_vocab_sizes(cuda_lib, oracle, V, ld, p):
-    """Partial last groups, the smallest and the largest vocabularies the
-    cluster path takes, and one just past it (per-row kernel)."""
+def test_stream_vocab_sizes(cuda_lib, oracle, V, ld, p):
+    """Partial last units, the smallest and the largest vocabularies the
+    streaming path takes (14,848 and 174,080) and one just outside each (the
+    per-row kernel), padded row strides."""
     base, _ = workloads.peaked_bf16(12, V=ld, seed=17, device="cuda")
     z = base[:, :V]
     z[:, V - 3:] = 12.5   # tokens in the partial last group that are kept
@@ -79,8 +80,8 @@ def test_cluster_vocab_sizes(cuda_lib, oracle, V, ld, p):
 
 
 @pytest.mark.parametrize("p", [0.95, 1.0])
-def test_cluster_small_batches_bitwise(cuda_lib, oracle, p):
-    """Batches of 1 .. 600 rows (fewer and more rows than clusters): each
+def test_stream_small_batches_bitwise(cuda_lib, oracle, p):
+    """Batches of 1 .. 600 rows (fewer and more rows than SMs): each
     row's bits are the same in every batch, including rows that the per-row
     kernel recomputes."""
     z, _ = special_rows(151936, seed=5)
@@ -102,7 +103,7 @@ def test_cluster_small_batches_bitwise(cuda_lib, oracle, p):
         assert x[ic].tobytes() == y.tobytes()
 
 
-def test_cluster_bad_rows(cuda_lib):
+def test_stream_bad_rows(cuda_lib):
     V = 151936
     z, peaks = workloads.peaked_bf16(8, V=V, seed=2, device="cuda")
     z[0, int(peaks[0])] = 30.0
