@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
     if (a.out_stats) {
       const float d = bad_offsets ? NAN : (M > 0.f ? M : 1.f);
       a.out_stats[RLK_STAT_LOSS] = L;
-      a.out_stats[RLK_STAT_TOKENS] = M;
+      a.out_stats[RLK_STAT_TOKENS] = bad_offsets ? NAN : M;
       a.out_stats[RLK_STAT_CLIP_LOW] = __fdiv_rn(s_t[2], d);
       a.out_stats[RLK_STAT_CLIP_HIGH] = __fdiv_rn(s_t[3], d);
       a.out_stats[RLK_STAT_TIS_MEAN] = __fdiv_rn(__fmul_rn(s_t[4], scale), d);

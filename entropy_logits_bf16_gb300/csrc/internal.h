@@ -173,6 +173,10 @@ bool take_injected_failure();
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+// Slot 0..63 of the current device for per-device once-only state (kernel
+// attributes, occupancy), or -1 (no device / more than 64 devices: the
+// callers then redo the work on every call).
+int device_slot();
 
 cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream);
 // Streaming kernel for every bf16 batch of a large vocabulary (lpe_stream.cu).

@@ -60,15 +60,27 @@ constexpr uint32_t SPIN_LIMIT = 1u << 22;
 constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 
 // ------------------------------------------------------------ PTX wrappers
-// Bounded wait; false when the limit ran out or another role gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
+// Bounded wait: false when `limit` clock cycles ran out (the abort flag is
+// then raised) or another role gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023u) == 1023u && *abort) return false;
+    if ((i & 255u) == 255u) {
+      if (*abort) return false;
+      if (clock64() - t0 > limit) {
+        *abort = 1;
+        return false;
+      }
+    }
   }
-  *abort = 1;
-  return false;
 }
+
+// The row-state marker of a slice that a timed-out CTA never finished: a
+// negative sum, which no data produces; the combine turns it into NaN rows.
+constexpr float kTimedOutSum = -1.0f;
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y) {
   asm volatile(
@@ -215,6 +227,8 @@ struct LmParams {
   uint16_t* dz;          // [T][ldz] bf16
   int64_t ldz;
   float inv_t;
+  long long wait_limit;  // clock cycles a wait may take
+  long long withhold;    // debug: the k-step copy the first CTA never issues (-1: none)
 };
 
 __device__ __forceinline__ void slice_bounds(int n_nt, int sl, int& nt0, int& nt1) {
@@ -230,11 +244,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;            // 1024-aligned stage area
   uint8_t* base_ptr = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
-  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2]
+  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], then the
+  // abort flag, the TMEM address and the drain barrier of an aborted MMA issuer
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
   const uint32_t accf0 = empty0 + 8 * STAGES, acce0 = accf0 + 16;
+  const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -246,6 +262,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(accf0 + 8 * a, 1);
       mbar_init(acce0 + 8 * a, 4);   // one arrive per epilogue warp
     }
+    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -268,14 +285,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0u, issued_parity = 0u;  // per stage: used, parity of last issue
+      long long n_issue = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
         const int mt = u / NSLICE, sl = u % NSLICE;
         int nt0, nt1;
         slice_bounds(p.n_nt, sl, nt0, nt1);
         for (int nt = nt0; nt < nt1 && ok; ++nt) {
-          for (int k = 0; k < p.k_steps; ++k) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+          for (int k = 0; k < p.k_steps; ++k, ++n_issue) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.wait_limit)) { ok = false; break; }
+            if (*abort_flag) { ok = false; break; }
+            if (blockIdx.x == 0 && n_issue == p.withhold) {   // debug: a copy never issued
+              if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+              continue;
+            }
             const uint32_t fb = full0 + 8 * stage;
             mbar_expect_tx(fb, STAGE_BYTES);
             const uint32_t sa = base + stage * STAGE_BYTES;
@@ -311,11 +334,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         slice_bounds(p.n_nt, sl, nt0, nt1);
         for (int nt = nt0; nt < nt1 && ok; ++nt, ++tile) {
           const uint32_t acc = tile & 1u, accph = (tile >> 1) & 1u;
-          if (!mbar_wait(acce0 + 8 * acc, accph ^ 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(acce0 + 8 * acc, accph ^ 1u, abort_flag, p.wait_limit)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem + acc * BN;
           for (int k = 0; k < p.k_steps; ++k) {
-            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.wait_limit)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = base + stage * STAGE_BYTES;
             const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sa + A_BYTES);
@@ -331,6 +354,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (ok) mma_commit(accf0 + 8 * acc);
         }
       }
+      if (!ok) {
+        // Let every MMA already issued finish before TMEM is freed (bounded).
+        mma_commit(drain_bar);
+        for (uint32_t i = 0; i < SPIN_LIMIT; ++i)
+          if (mbar_try_wait(drain_bar, 0u)) break;
+      }
     }
   } else {
     // ------------------------------------------------------ epilogue
@@ -338,7 +367,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t tile = 0;
     bool ok = true;
+    int u_fail = p.n_units;
     for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+      u_fail = u;
       const int mt = u / NSLICE, sl = u % NSLICE;
       int nt0, nt1;
       slice_bounds(p.n_nt, sl, nt0, nt1);
@@ -360,7 +391,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool have_zy = false;
       for (int nt = nt0; nt < nt1; ++nt, ++tile) {
         const uint32_t acc = tile & 1u, accph = (tile >> 1) & 1u;
-        if (!mbar_wait(accf0 + 8 * acc, accph, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(accf0 + 8 * acc, accph, abort_flag, p.wait_limit)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
         for (int ch = 0; ch < BN / 32; ++ch) {
@@ -421,8 +452,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         p.part[(int64_t)sl * p.T + row] = make_float4(st.m, st.hi, st.lo, st.u);
         if (have_zy) p.zy[row] = zy;
       }
+      if (ok) u_fail = p.n_units;
     }
-    if (!ok && lane == 0 && p.status) atomicOr(p.status, RLK_STATUS_TIMEOUT);
+    if (!ok) {
+      // A wait ran out: every unit this CTA has not finished is marked, so
+      // its rows come out NaN instead of normal-looking values.
+      for (int u = u_fail; u < p.n_units; u += gridDim.x) {
+        const int64_t row = (int64_t)(u / NSLICE) * BM + q * 32 + lane;
+        if (row >= p.T) continue;
+        if (!p.grad) {
+          p.part[(int64_t)(u % NSLICE) * p.T + row] = make_float4(0.f, kTimedOutSum, 0.f, 0.f);
+        } else {   // NaN logits or gradients: every result built on them is NaN
+          int nt0, nt1;
+          slice_bounds(p.n_nt, u % NSLICE, nt0, nt1);
+          const int64_t c1 = (int64_t)nt1 * BN < p.V ? (int64_t)nt1 * BN : p.V;
+          for (int64_t col = (int64_t)nt0 * BN; col < c1; ++col) p.dz[row * p.ldz + col] = 0x7FC0u;
+        }
+      }
+      if (lane == 0 && p.status) atomicOr(p.status, RLK_STATUS_TIMEOUT);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -449,9 +497,17 @@ __global__ void __launch_bounds__(256) lmhead_combine_kernel(LmParams p, float* 
     return;
   }
   RowState st{-INFINITY, 0.f, 0.f, 0.f};
+  bool timed_out = false;
   for (int sl = 0; sl < NSLICE; ++sl) {
     const float4 s = p.part[(int64_t)sl * p.T + row];
+    timed_out = timed_out || s.y == kTimedOutSum;
     st = state_merge(st, RowState{s.x, s.y, s.z, s.w}, p.c);
+  }
+  if (timed_out) {   // the kernel has set RLK_STATUS_TIMEOUT
+    out_lp[row] = NAN;
+    out_ent[row] = NAN;
+    if (out_lse) out_lse[row] = NAN;
+    return;
   }
   const float z = __fadd_rn(st.hi, st.lo);
   if (!(isfinite(z) && isfinite(st.u) && isfinite(st.m))) {
@@ -509,17 +565,22 @@ size_t lmhead_workspace_bytes(int64_t T, int64_t V, int64_t H) {
   return (b + 255) & ~(size_t)255;
 }
 
+// The kernel's shared-memory attribute, once per device.
+cudaError_t set_lmhead_smem() {
+  static std::atomic<int> done[64];
+  const int ds = device_slot();
+  if (ds >= 0 && done[ds].load()) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SMEM_BYTES);
+  if (e == cudaSuccess && ds >= 0) done[ds].store(1);
+  return e;
+}
+
 cudaError_t launch_lmhead_impl(const LmheadArgs& a, float* debug_logits, cudaStream_t stream) {
   CUtensorMap ma, mb;
   if (!make_map(&ma, a.hidden, (uint64_t)a.T, (uint64_t)a.H, BM)) return cudaErrorInvalidValue;
   if (!make_map(&mb, a.w_vocab, (uint64_t)a.V, (uint64_t)a.H, BN)) return cudaErrorInvalidValue;
-  static std::atomic<int> attr_done{0};
-  if (!attr_done.load()) {
-    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done.store(1);
-  }
+  if (cudaError_t e = set_lmhead_smem(); e != cudaSuccess) return e;
   LmParams p{};
   p.T = a.T;
   p.V = a.V;
@@ -535,6 +596,8 @@ cudaError_t launch_lmhead_impl(const LmheadArgs& a, float* debug_logits, cudaStr
   p.debug_logits = debug_logits;
   p.status = a.status;
   p.grad = 0;
+  p.wait_limit = debug_wait_limit();
+  p.withhold = debug_take_withheld();
   const int grid = p.n_units < sm_count() ? p.n_units : sm_count();
   lmhead_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
   cudaError_t e = cudaGetLastError();
@@ -627,13 +690,7 @@ size_t lmhead_bwd_workspace_bytes(int64_t T, int64_t V, int64_t H) {
 }
 
 cudaError_t launch_lmhead_backward(const LmheadBwdArgs& a, cudaStream_t stream) {
-  static std::atomic<int> attr_done{0};
-  if (!attr_done.load()) {
-    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done.store(1);
-  }
+  if (cudaError_t e = set_lmhead_smem(); e != cudaSuccess) return e;
   CUtensorMap mb;
   if (!make_map(&mb, a.w_vocab, (uint64_t)a.V, (uint64_t)a.H, BN)) return cudaErrorInvalidValue;
   uint16_t* dz = static_cast<uint16_t*>(a.workspace);
@@ -655,7 +712,9 @@ cudaError_t launch_lmhead_backward(const LmheadBwdArgs& a, cudaStream_t stream) 
     p.ids = a.ids + r0;
     p.c = (float)(1.4426950408889634 / (double)a.temperature);
     p.inv_t = (float)(1.0 / (double)a.temperature);
-    p.grad = 1;
+    p.grad = 1;   // no status word: a timed-out tile leaves NaN gradients
+    p.wait_limit = debug_wait_limit();
+    p.withhold = -1;
     p.lse = a.lse + r0;
     p.ent = a.entropy + r0;
     p.glp = a.grad_logprob ? a.grad_logprob + r0 : nullptr;
@@ -688,13 +747,7 @@ size_t lmhead_topp_workspace_bytes(int64_t T, int64_t V, int64_t H) {
 // kBwdRows rows is emitted once as bf16 logits (the same GEMM, emit epilogue)
 // into the workspace and scored there by the top-p logits path.
 cudaError_t launch_lmhead_topp(const LmheadArgs& a, cudaStream_t stream) {
-  static std::atomic<int> attr_done{0};
-  if (!attr_done.load()) {
-    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done.store(1);
-  }
+  if (cudaError_t e = set_lmhead_smem(); e != cudaSuccess) return e;
   CUtensorMap mb;
   if (!make_map(&mb, a.w_vocab, (uint64_t)a.V, (uint64_t)a.H, BN)) return cudaErrorInvalidValue;
   uint16_t* zbuf = static_cast<uint16_t*>(a.workspace);
@@ -715,6 +768,9 @@ cudaError_t launch_lmhead_topp(const LmheadArgs& a, cudaStream_t stream) {
     p.ids = a.ids + r0;
     p.c = (float)(1.4426950408889634 / (double)a.temperature);
     p.grad = 2;
+    p.status = a.status;
+    p.wait_limit = debug_wait_limit();
+    p.withhold = -1;
     p.dz = zbuf;
     p.ldz = ldz;
     const int grid = p.n_units < sm_count() ? p.n_units : sm_count();

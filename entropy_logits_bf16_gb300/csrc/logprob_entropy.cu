@@ -1135,8 +1135,9 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
   const bool topp = per_row || a.top_p < 1.0f;
   const size_t smem = sizeof(Smem);
 
-  static std::atomic<int> attr_done{0};
-  if (!attr_done.load()) {
+  static std::atomic<int> attr_done[64];   // once per device
+  const int ds = device_slot();
+  if (ds < 0 || !attr_done[ds].load()) {
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(lpe_kernel<RowBf16, true>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
@@ -1147,7 +1148,7 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
         (e = cudaFuncSetAttribute(lpe_kernel<RowF32, false>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
-    attr_done.store(1);
+    if (ds >= 0) attr_done[ds].store(1);
   }
   if (!a.only_marked && lpe_stream_eligible(a)) {
     cudaError_t e = launch_lpe_stream(a, stream, debug_wait_limit(), debug_take_withheld());

@@ -511,9 +511,10 @@ __global__ void __launch_bounds__(PT, 3) lpe_backward_pipe_kernel(LpeBwdArgs a, 
 
 template <bool BO>
 cudaError_t launch_pipe(const LpeBwdArgs& a, float c, float inv_t, cudaStream_t stream) {
-  static std::atomic<int> per_sm{0};
+  static std::atomic<int> per_sm[64];   // resident CTAs per SM, per device
   const int smem = RING_OFF + NSTG * (int)STG;
-  int occ = per_sm.load();
+  const int ds = device_slot();
+  int occ = ds >= 0 ? per_sm[ds].load() : 0;
   if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(lpe_backward_pipe_kernel<BO>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -521,7 +522,7 @@ cudaError_t launch_pipe(const LpeBwdArgs& a, float c, float inv_t, cudaStream_t 
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lpe_backward_pipe_kernel<BO>, PT, smem);
     if (e != cudaSuccess) return e;
     occ = occ < 1 ? 1 : occ;
-    per_sm.store(occ);
+    if (ds >= 0) per_sm[ds].store(occ);
   }
   const int64_t cap = (int64_t)occ * sm_count();
   const dim3 grid((unsigned)(a.T < cap ? a.T : cap)), block(PT);
@@ -538,14 +539,15 @@ bool pipe_eligible(const LpeBwdArgs& a) {
 
 template <bool BF, bool BO>
 cudaError_t launch_typed(const LpeBwdArgs& a, float c, float inv_t, cudaStream_t stream) {
-  static std::atomic<int> per_sm{0};   // resident CTAs per SM (one GPU type per process)
-  int occ = per_sm.load();
+  static std::atomic<int> per_sm[64];   // resident CTAs per SM, per device
+  const int ds = device_slot();
+  int occ = ds >= 0 ? per_sm[ds].load() : 0;
   if (occ == 0) {
     const cudaError_t e =
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lpe_backward_kernel<BF, BO>, NTB, 0);
     if (e != cudaSuccess) return e;
     occ = occ < 1 ? 1 : occ;
-    per_sm.store(occ);
+    if (ds >= 0) per_sm[ds].store(occ);
   }
   const int64_t cap = (int64_t)occ * sm_count();
   const dim3 grid((unsigned)(a.T < cap ? a.T : cap)), block(NTB);

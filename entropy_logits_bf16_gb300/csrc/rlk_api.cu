@@ -27,6 +27,12 @@ int sm_count() {
   return n;
 }
 
+int device_slot() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  return dev;
+}
+
 }  // namespace rlk
 
 namespace {

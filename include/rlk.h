@@ -91,7 +91,9 @@ enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2,
 #define RLK_STATUS_BAD_TOKEN_ID 0x1u   /* a token id outside [0, V)          */
 #define RLK_STATUS_NONFINITE    0x2u   /* a NaN or +-inf logit in a row      */
 #define RLK_STATUS_TIMEOUT      0x4u   /* a bounded device wait ran out; the
-                                          call's outputs are not valid      */
+                                          rows the kernel had not finished
+                                          get NaN outputs (rows finished
+                                          before it are valid)              */
 #define RLK_STATUS_BAD_SUPPORT  0x8u   /* a supplied retained set that is empty,
                                           lists an id outside [0, V), or whose
                                           offsets decrease                      */
@@ -367,16 +369,21 @@ rlk_status rlk_logprob_entropy_support_backward(
  *   the active minimum (ties count as unclipped), else 0.
  *
  * Arguments
- *  logp_new, logp_old, logp_rollout, logp_ref  device float[n_tok] each, indexed by
- *                  the packed token position (seq_offsets[0] may be > 0).
+ *  logp_new, logp_old, logp_rollout, logp_ref  device float arrays indexed by the
+ *                  packed token position t, seq_offsets[0] <= t < seq_offsets[0] + n_tok
+ *                  (seq_offsets[0] may be > 0: pass the base of the packed batch).
  *  loss_mask       device uint8[n_tok] (0/1) or NULL for all ones.
  *  rewards         device float[n_seq].
- *  seq_offsets     device int32[n_seq + 1], non-decreasing (not checked on the host).
+ *  seq_offsets     device int32[n_seq + 1], non-decreasing and within
+ *                  [seq_offsets[0], seq_offsets[0] + n_tok] (checked on the device:
+ *                  otherwise every sequence's range is clamped to the n_tok tokens, no
+ *                  token outside them is read or written, and the loss, the
+ *                  statistics and the gradient come out NaN).
  *  n_seq, group_size  n_seq >= 0, group_size >= 1, n_seq % group_size == 0.
  *  eps_low, eps_high  >= 0 and finite; tis_cap > 0; kl_coef >= 0 and finite.
  *  agg             an rlk_agg value.
- *  n_tok           number of packed tokens (seq_offsets[n_seq] - seq_offsets[0]); sizes the
- *                  workspace and the gradient.
+ *  n_tok           number of packed tokens (seq_offsets[n_seq] - seq_offsets[0]): the
+ *                  extent of the per-token arrays and of the gradient.
  *  out_loss        device float[1].
  *  out_dloss_dlogp_new  device float[n_tok] or NULL.
  *  out_stats       device float[RLK_NSTATS] or NULL.
@@ -464,8 +471,10 @@ rlk_status rlk_policy_loss(const float* logp_new, const float* logp_old,
  * Scratch: a static device array of RLK_NOALLOC_MAX_SEQ * 12 + 4 floats
  * (about 768 KB) inside the library, held by every GPU that loads the library
  * until the process exits.  The first call on each device looks up the
- * array's device address (with that device current); make that first call
- * before any stream capture.  Every call overwrites what it reads, so nothing
+ * array's device address (with that device current) and caches it for the
+ * life of the process; make that first call before any stream capture.  A
+ * cudaDeviceReset of that device frees the array behind the cached address:
+ * do not call this entry point on a device after resetting it.  Every call overwrites what it reads, so nothing
  * needs clearing, and the array keeps the last call's contents.  All calls
  * share the array: calls whose work overlaps on the GPU (different streams or
  * host threads) race and give wrong results -- serialise them.

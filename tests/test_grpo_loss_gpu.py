@@ -121,3 +121,47 @@ def test_chained_logits_to_loss(cuda_lib, oracle):
     err = abs(loss.item() - oL)
     print(f"chained loss {loss.item():.6f} oracle {oL:.6f} |diff| {err:.2e} bound {tol:.2e}")
     assert err <= tol
+
+
+@pytest.mark.parametrize("case", ["decreasing", "past_end", "before_base"])
+def test_bad_offsets_give_nan_and_stay_in_range(cuda_lib, case):
+    """seq_offsets that decrease or leave the n_tok packed tokens: the loss,
+    the statistics and the gradient come out NaN, and no gradient is written
+    outside the n_tok tokens (canaries on both sides of the buffer)."""
+    import ctypes
+    lib = cuda_lib.load()
+    off, R, new, old, ro, ref = make_batch(4, 4, 8, 40, seed=23)
+    n = int(off[-1])
+    bad = off.copy()
+    if case == "decreasing":
+        bad[5] = bad[3] - 1
+    elif case == "past_end":
+        bad[-1] = n + 50
+    else:
+        bad[2] = -7
+    pad = 64
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    tn, to, tr, tf, tR, toff = t(new), t(old), t(ro), t(ref), t(R), t(bad)
+    gbuf = torch.full((n + 2 * pad,), 12345.0, device="cuda")
+    grad = gbuf[pad:pad + n]
+    loss = torch.zeros(1, device="cuda")
+    stats = torch.zeros(cuda_lib.NSTATS, device="cuda")
+    n_seq = off.size - 1
+    wsb = cuda_lib.workspace_size(1, n, n_seq)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    p = lambda x: ctypes.c_void_p(x.data_ptr())
+    code = lib.rlk_grpo_loss(p(tn), p(to), p(tr), p(tf), None, p(tR), p(toff), n_seq, 4, n, 0.2,
+                             0.28, 2.0, 0.01, 0, p(loss), p(grad), p(stats), p(ws), wsb,
+                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0
+    torch.cuda.synchronize()
+    assert np.isnan(loss.item())
+    assert np.all(np.isnan(stats.cpu().numpy()))
+    g = gbuf.cpu().numpy()
+    assert np.all(g[:pad] == 12345.0) and np.all(g[pad + n:] == 12345.0)
+    written = g[pad:pad + n]
+    assert np.all(np.isnan(written) | (written == 12345.0))
+    # the same call with valid offsets is finite again
+    loss2, _, _ = cuda_lib.grpo_loss(tn, to, tr, tf, tR, t(off), 4)
+    torch.cuda.synchronize()
+    assert np.isfinite(loss2.item())

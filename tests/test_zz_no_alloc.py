@@ -5,9 +5,11 @@ framework that has reserved the whole device for its own pool, code running
 inside an allocator callback, or a loop that bans cudaMalloc because it may
 synchronise the device.  Its scratch lives in a static device array of the
 library.  The test checks it against rlk_grpo_loss (caller-supplied
-workspace) on the same inputs, within the loss tests' tolerance, on two calls
-in a row (the second one reuses the array the first left behind), and that
-sizes beyond the array's limit are refused.  This file is collected last so a
+workspace) on the same inputs for every aggregation, on two calls in a row
+(the second one reuses the array the first left behind).  Both run the same
+three kernels in the same order on the same inputs, so the loss, the
+gradient and the statistics must be bitwise equal.  Sizes beyond the array's
+limit must be refused.  This file is collected last so a
 run that stops at the first failure has run every other test already.
 """
 import ctypes
@@ -19,8 +21,6 @@ import torch
 import workloads
 
 pytestmark = pytest.mark.gpu
-
-REL = 1e-4
 
 
 def _ptr(t):
@@ -40,7 +40,8 @@ def test_noalloc_matches_workspace_entry_point(cuda_lib):
     tn, to, tr, tf, tR, toff, tm = t(new), t(old), t(ro), t(ref), t(R), t(off), t(mask)
     n_seq = off.size - 1
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    for agg in (0, 1):
+    bits = lambda t: t.cpu().contiguous().view(torch.int32).numpy()
+    for agg in (0, 1, 2):
         ref_loss, ref_grad, ref_stats = cuda_lib.grpo_loss(tn, to, tr, tf, tR, toff, 8,
                                                            loss_mask=tm, agg=agg)
         torch.cuda.synchronize()
@@ -54,12 +55,10 @@ def test_noalloc_matches_workspace_entry_point(cuda_lib):
                                              stream)
             assert code == 0
             torch.cuda.synchronize()
-            L, RL = loss.item(), ref_loss.item()
-            assert abs(L - RL) <= REL * max(abs(RL), 1e-6)
-            g, rg = grad.cpu().numpy(), ref_grad.cpu().numpy()
-            assert np.abs(g - rg).max() <= REL * max(np.abs(rg).max(), 1e-12)
-            s, rs = stats.cpu().numpy(), ref_stats.cpu().numpy()
-            assert np.all(np.abs(s - rs) <= REL * np.maximum(np.abs(rs), 1e-3))
+            assert np.isfinite(loss.item())
+            assert np.array_equal(bits(loss), bits(ref_loss)), f"agg {agg}: loss bits differ"
+            assert np.array_equal(bits(grad), bits(ref_grad)), f"agg {agg}: gradient bits differ"
+            assert np.array_equal(bits(stats), bits(ref_stats)), f"agg {agg}: statistics differ"
 
 
 def test_noalloc_refuses_sizes_beyond_its_array(cuda_lib):
