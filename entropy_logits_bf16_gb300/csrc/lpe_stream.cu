@@ -1,5 +1,5 @@
 // Streaming rlk_logprob_entropy kernel for bf16 rows of a large vocabulary
-// (every bf16 batch with 14,848 <= V <= 174,080, whatever its row stride or
+// (every bf16 batch with 14,336 <= V <= 174,080, whatever its row stride or
 // alignment, and whichever entry point -- scalar or per-row parameters -- so a
 // row gets one set of bits from every call that scores it).
 //
@@ -14,36 +14,43 @@
 //
 // One CTA of 1024 threads per SM; CTA b scores rows b, b + grid, ...  Warp
 // roles, pipelined over rows:
-//  * the producer (warp 29): one thread streams each row through a ring of
+//  * the producer (warp 28): one thread streams each row through a ring of
 //    four shared-memory stages with cp.async.bulk (one unit of 16 logits = 32
 //    bytes per compute thread per stage), and forms each row's parameters
 //    (c = log2(e) / T exactly as the host forms it);
-//  * the compute warps (0-28): thread t owns the units t, t + 928, ... of a
+//  * the compute warps (0-27): thread t owns the units t, t + 896, ... of a
 //    row and keeps one running state: an integer reference E_t,
 //    S = sum 2^d as a double-float and U = sum 2^d d with d = fma(z, c, -E_t)
 //    (one rounding).  A unit's max comes first (packed bf16x2 max); the
 //    reference moves up (by an exact power of two) only when a unit's max
 //    exceeds it by more than LAZY, so the exponentials run against a fixed
-//    reference almost always.  At top_p < 1 each unit's max also goes to a
-//    sketch.  At the end of a row the thread's state goes to shared memory and
-//    the next row starts at once;
-//  * the merge warp (30), one row behind: merges the 928 thread states in a
+//    reference almost always.  At top_p < 1 each unit's largest and second
+//    largest logits also go to a sketch.  At the end of a row each warp
+//    merges its 32 thread states in a fixed order, writes the warp state to
+//    shared memory and starts the next row at once;
+//  * the merge warp (29), one row behind: merges the 28 warp states in a
 //    fixed order (rescaling to E = ceil(m c), m the row max: exact powers of
 //    two) and decides the row: at top_p = 1 its answer; at top_p < 1 the
 //    window z >= m - L T (L = ln(1/(1-top_p)) + 7) in which the retained set
 //    must lie.  All tokens of one bf16 value carry the same mass, so the
 //    window is summarised exactly by integer counts per distinct value;
-//  * side work of the compute warps: while they stream the next row, each
-//    thread tests its own units' sketch entries of the finished row against
-//    the window, reads every unit that reaches it once more (staged into its
-//    own shared-memory slot by cp.async one stage ahead, so the warp never
-//    waits on the load; the row streamed through L2 microseconds earlier) and
-//    counts its window tokens per key with shared-memory atomics (integer
-//    counts do not depend on the atomics' order);
-//  * the scan warp (31): one warp scans the counts largest value first in a
-//    fixed-order double-float prefix: the bin where the retained mass reaches
-//    top_p Z, how many of its tied tokens are needed (lower ids first), Z_S
-//    and the entropy numerator; it writes every row's outputs.
+//  * side work of the compute warps, at the end of the next row: the threads
+//    test the sketch of the finished row against the window.  A unit whose
+//    largest logit reaches the window and whose second largest does not holds
+//    one window token, its max, counted from the sketch alone.  A unit with
+//    more has its two largest counted from the sketch and is listed.  Tokens
+//    are counted per key with shared-memory atomics (integer counts do not
+//    depend on the atomics' order);
+//  * the scan warps (30 and 31, alternate rows): the counts are now exact for
+//    every token but the third and later largest of listed units.  A first
+//    scan over them, largest value first, bounds the crossing from below; the
+//    listed units whose second largest logit reaches that bound, and the
+//    selected token's unit, are read once more and their remaining tokens
+//    above it counted, which makes every count above the bound exact.  The
+//    final scan (a fixed-order double-float prefix) finds the bin where the
+//    retained mass reaches top_p Z, how many of its tied tokens are needed
+//    (lower ids first), Z_S and the entropy numerator; the warp writes the
+//    row's outputs.
 //  * Rows this path does not finish -- a window wider than the histogram (one
 //    that crosses zero) or a window whose mass falls short of the target --
 //    get a marker in out_logprob and are recomputed by the per-row kernel
@@ -70,12 +77,12 @@
 namespace rlk {
 namespace {
 
-constexpr int NWC = 29;                  // compute warps
+constexpr int NWC = 28;                  // compute warps
 constexpr int NTC = NWC * 32;            // compute threads
 constexpr int WPROD = NWC;               // producer warp
 constexpr int WMRG = NWC + 1;            // merge warp
-constexpr int WSCN = NWC + 2;            // scan warp
-constexpr int NTB = (NWC + 3) * 32;
+constexpr int WSCN = NWC + 2;            // scan warps (two: even and odd rows of the CTA)
+constexpr int NTB = (NWC + 4) * 32;
 static_assert(NTB == 1024, "one 1024-thread CTA per SM");
 constexpr int UNIT = 16;                 // logits per unit (32 bytes)
 constexpr int NSTAGE = 4;                // ring stages
@@ -86,6 +93,9 @@ constexpr float LAZY = 4.0f;             // re-base when a unit's max exceeds E_
 constexpr int64_t V_MIN = (int64_t)UNIT * NTC;
 constexpr int64_t V_MAX = 174080;        // the sketch's share of shared memory (10,880 units)
 static_assert((V_MAX / UNIT + NTC - 1) / NTC <= 32, "a thread's units of a row fit a 32-bit mask");
+constexpr uint32_t PART_BYTES = 2u * 4u * 32u * 4u;   // [2][4][32] warp states
+constexpr int NSTM = (int)((V_MAX / UNIT + NTC - 1) / NTC);   // a thread's units of a row, at most
+constexpr uint32_t LCAP = 1500;          // units with two or more window tokens listed per row
 
 struct RowParam {
   float c, temp, top_p, row_t;   // row_t: the row's own temperature (per-row calls), else 0
@@ -117,6 +127,7 @@ struct __align__(16) Ctrl {
   RowRec rec[2];
   uint32_t wkey[2][NWC];
   uint32_t tie[2];
+  uint32_t lcnt[2];                 // units listed for the scan warp (may exceed LCAP)
   int abort;
 };
 
@@ -126,7 +137,7 @@ struct Geom {
   int nst;        // stages per row: ceil(nunits / NTC)
   int tma;        // rows stream through the ring (16-byte aligned rows)
   uint32_t tma_bytes;   // bytes of a row the ring copies: floor(V / 8) * 16
-  uint32_t off_part, off_hist, off_slot, off_sk, skb, off_ring;
+  uint32_t off_part, off_hist, off_list, off_sk, skb, off_ring;
   long long wait_limit;   // clock cycles a wait may take before it gives up
   long long withhold;     // debug: the stage CTA 0 never issues (-1: none)
 };
@@ -190,13 +201,24 @@ __device__ __forceinline__ void rebase(Acc& st, float En) {
   st.E = En;
 }
 
+__device__ __forceinline__ uint32_t u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+// Merges two (largest, second largest) pairs of bf16x2 lanes.
+__device__ __forceinline__ void top2_merge(__nv_bfloat162& a1, __nv_bfloat162& b1, __nv_bfloat162 a2,
+                                           __nv_bfloat162 b2) {
+  b1 = __hmax2(__hmin2(a1, a2), __hmax2(b1, b2));
+  a1 = __hmax2(a1, a2);
+}
+
 // Folds a unit's 16 logits into the state and returns the unit's max.  The
 // words w[0..7] hold the logits in the order the thread reads them (two bf16
 // a word, low half first).  MASKED: only the logits whose bit is set in vmask
 // (bit j: half j & 1 of word j >> 1) exist -- the row's last, partial unit.
-template <bool MASKED, bool UNIFORM = false>
+// TOP2: *ent receives the unit's sketch entry, its largest logit (low half)
+// and its second largest (high half; -inf for a unit of one logit), as bf16.
+template <bool MASKED, bool UNIFORM = false, bool TOP2 = false>
 __device__ __forceinline__ float absorb_unit(Acc& st, const uint32_t (&w)[8], float c,
-                                             uint32_t vmask = 0xFFFFu) {
+                                             uint32_t vmask = 0xFFFFu, uint32_t* ent = nullptr) {
   uint32_t wm[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
@@ -206,11 +228,30 @@ __device__ __forceinline__ float absorb_unit(Acc& st, const uint32_t (&w)[8], fl
       if (!((vmask >> (2 * k + 1)) & 1u)) wm[k] = (wm[k] & 0xFFFFu) | 0xFF800000u;
     }
   }
-  const __nv_bfloat162 m01 = __hmax2(bf2(wm[0]), bf2(wm[1])), m23 = __hmax2(bf2(wm[2]), bf2(wm[3]));
-  const __nv_bfloat162 m45 = __hmax2(bf2(wm[4]), bf2(wm[5])), m67 = __hmax2(bf2(wm[6]), bf2(wm[7]));
-  const __nv_bfloat162 mm = __hmax2(__hmax2(m01, m23), __hmax2(m45, m67));
-  const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mm);
-  const float gm = fmaxf(bf16_lo(mw), bf16_hi(mw));
+  float gm;
+  if (TOP2) {
+    // tournament: (max, second) per bf16x2 lane over the 8 words, then across the lanes
+    __nv_bfloat162 A[4], B[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      A[k] = __hmax2(bf2(wm[2 * k]), bf2(wm[2 * k + 1]));
+      B[k] = __hmin2(bf2(wm[2 * k]), bf2(wm[2 * k + 1]));
+    }
+    top2_merge(A[0], B[0], A[1], B[1]);
+    top2_merge(A[2], B[2], A[3], B[3]);
+    top2_merge(A[0], B[0], A[2], B[2]);
+    const __nv_bfloat162 As = bf2(__byte_perm(u32(A[0]), 0u, 0x1032));
+    const __nv_bfloat162 Bs = bf2(__byte_perm(u32(B[0]), 0u, 0x1032));
+    top2_merge(A[0], B[0], As, Bs);   // both lanes now hold the unit's pair
+    *ent = __byte_perm(u32(A[0]), u32(B[0]), 0x5410);
+    gm = bf16_lo(u32(A[0]));
+  } else {
+    const __nv_bfloat162 m01 = __hmax2(bf2(wm[0]), bf2(wm[1])), m23 = __hmax2(bf2(wm[2]), bf2(wm[3]));
+    const __nv_bfloat162 m45 = __hmax2(bf2(wm[4]), bf2(wm[5])), m67 = __hmax2(bf2(wm[6]), bf2(wm[7]));
+    const __nv_bfloat162 mm = __hmax2(__hmax2(m01, m23), __hmax2(m45, m67));
+    const uint32_t mw = u32(mm);
+    gm = fmaxf(bf16_lo(mw), bf16_hi(mw));
+  }
   st.mx = fmaxf(st.mx, gm);
   // rare after a row's first units (E = -inf before the first: always taken)
   const bool up = __fmaf_rn(gm, c, -st.E) > LAZY;
@@ -422,73 +463,87 @@ __device__ __forceinline__ bool test_phase(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
-// 16-byte asynchronous copy global -> shared (both 16-byte aligned); the
-// commit of this thread's copies and the wait for all of them.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-// Puts unit u of a row into a thread's 32-byte slot: asynchronously for a
-// whole unit of a 16-byte aligned row, else with scalar loads (absent logits
-// beyond V read as -inf, so they never reach a window).
-__device__ __forceinline__ void stage_unit(const uint16_t* row, int64_t V, int u, bool aligned_full,
-                                           uint4* slot) {
+// Counts the tokens of unit u of a row that reach the window floor (zf2w, a
+// bf16 value in both halves) into hist (bins below key_m); ny receives how
+// many carry key_y.  The unit is read again (whole with two 16-byte loads from
+// a 16-byte aligned row, else with scalar loads; absent logits read as -inf).
+__device__ __forceinline__ void count_unit(const uint16_t* row, int64_t V, int u, bool aligned_full,
+                                           uint32_t zf2w, uint32_t key_m, uint32_t key_y,
+                                           uint32_t* hist, uint32_t& ny) {
+  uint32_t w[8];
   if (aligned_full) {
     const uint4* q = reinterpret_cast<const uint4*>(row) + 2 * u;
-    cp_async16(smem_u32(slot), q);
-    cp_async16(smem_u32(slot + 1), q + 1);
-    cp_async_commit();
+    const uint4 v0 = __ldg(q), v1 = __ldg(q + 1);
+    w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+    w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
   } else {
-    uint32_t w[8];
     load_unit_scalar(row, V, u, 0, w);
-    slot[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    slot[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  const __nv_bfloat162 zf2 = bf2(zf2w);
+  ny = 0u;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t hm = __hge2_mask(bf2(w[k]), zf2);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      if ((hm >> (16 * hf)) & 1u) {
+        const uint32_t kk = okey16((w[k] >> (16 * hf)) & 0xFFFFu);
+        atomicAdd(&hist[key_m - kk], 1u);
+        ny += kk == key_y ? 1u : 0u;
+      }
+    }
   }
 }
 
-// Counts the tokens of unit u (its 16 logits in slot) that reach the window
-// floor into hist (bins below key_m), and the tokens tied with the selected
-// one (key_y) that precede it.  Absent logits of a partial unit read as -inf.
-__device__ __forceinline__ void count_unit(const uint4* slot, int u, uint32_t zf2w, uint32_t key_m,
-                                           uint32_t key_y, int32_t y, uint32_t* hist,
-                                           uint32_t& tie) {
-  const uint4 v0 = slot[0], v1 = slot[1];
-  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-  const __nv_bfloat162 zf2 = bf2(zf2w);
-  uint32_t hm[8], cnt = 0u;   // per word: 0xFFFF in each half that reaches the floor
+// The scan warp's second look at a listed unit (two or more window tokens,
+// whose two largest logits the sketch already counted): reads the unit again
+// (whole with two 16-byte loads from a 16-byte aligned row, else with scalar
+// loads; absent logits beyond V read as -inf) and adds its other tokens whose
+// key reaches the one of kv (a bf16 value in both halves).  Returns how many
+// were added; ny receives how many of them carry key_y.
+__device__ __forceinline__ uint32_t recount_unit(const uint16_t* row, int64_t V, int u, bool aligned_full,
+                                                 uint32_t kv2w, uint32_t key_m, uint32_t key_y,
+                                                 uint32_t* hist, uint32_t& ny) {
+  uint32_t w[8];
+  if (aligned_full) {
+    const uint4* q = reinterpret_cast<const uint4*>(row) + 2 * u;
+    const uint4 v0 = __ldg(q), v1 = __ldg(q + 1);
+    w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+    w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+  } else {
+    load_unit_scalar(row, V, u, 0, w);
+  }
+  const __nv_bfloat162 kv2 = bf2(kv2w);
+  uint32_t n = 0u;
+  ny = 0u;
+  float m1 = -INFINITY, m2 = -INFINITY;   // the unit's two largest logits
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    hm[k] = __hge2_mask(bf2(w[k]), zf2);
-    cnt += hm[k] & 0x00010001u;
-  }
-  if ((cnt & 0xFFFFu) + (cnt >> 16) == 1u) {
-    // The unit's only token in the window is its max (the usual case).
-    const __nv_bfloat162 m01 = __hmax2(bf2(w[0]), bf2(w[1])), m23 = __hmax2(bf2(w[2]), bf2(w[3]));
-    const __nv_bfloat162 m45 = __hmax2(bf2(w[4]), bf2(w[5])), m67 = __hmax2(bf2(w[6]), bf2(w[7]));
-    const __nv_bfloat162 mm = __hmax2(__hmax2(m01, m23), __hmax2(m45, m67));
-    const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mm);
-    const uint32_t kk = okey16(__float_as_uint(fmaxf(bf16_lo(mw), bf16_hi(mw))) >> 16);
-    if (kk != key_y) {
-      atomicAdd(&hist[key_m - kk], 1u);
-      return;
+    const uint32_t hm = __hge2_mask(bf2(w[k]), kv2);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const uint32_t bits = (w[k] >> (16 * hf)) & 0xFFFFu;
+      const float f = bf16_lo(bits);
+      if (f > m1) {
+        m2 = m1;
+        m1 = f;
+      } else {
+        m2 = fmaxf(m2, f);
+      }
+      if ((hm >> (16 * hf)) & 1u) {
+        const uint32_t kk = okey16(bits);
+        atomicAdd(&hist[key_m - kk], 1u);
+        ++n;
+        ny += kk == key_y ? 1u : 0u;
+      }
     }
   }
-  uint32_t msk = 0u;   // bit e: logit e of the unit reaches the floor
-#pragma unroll
-  for (int k = 0; k < 8; ++k) msk |= ((hm[k] & 1u) | ((hm[k] >> 15) & 2u)) << (2 * k);
-  const uint16_t* e16 = reinterpret_cast<const uint16_t*>(slot);
-  const int32_t col0 = u * UNIT;
-  while (msk) {
-    const int el = __ffs(msk) - 1;
-    msk &= msk - 1u;
-    const uint32_t kk = okey16(e16[el]);
-    atomicAdd(&hist[key_m - kk], 1u);
-    tie += (kk == key_y && col0 + el < y) ? 1u : 0u;
-  }
+  // the two largest were counted from the sketch
+  const uint32_t k1 = key_of(m1), k2 = key_of(m2);
+  atomicAdd(&hist[key_m - k1], 0xFFFFFFFFu);
+  atomicAdd(&hist[key_m - k2], 0xFFFFFFFFu);
+  ny -= (k1 == key_y ? 1u : 0u) + (k2 == key_y ? 1u : 0u);
+  return n - 2u;
 }
 
 // --------------------------------------------------------------- kernel
@@ -496,10 +551,9 @@ template <bool TOPP, bool TMA>
 __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, float c0) {
   extern __shared__ __align__(128) uint8_t smem[];
   Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem);
-  float* part = reinterpret_cast<float*>(smem + g.off_part);         // [2][3][NTC]: E, S, U
+  float* part = reinterpret_cast<float*>(smem + g.off_part);         // [2][4][32]: E, S hi, S lo, U
   uint32_t* hist0 = reinterpret_cast<uint32_t*>(smem + g.off_hist);  // [2][HBC]
-  uint4* slots = reinterpret_cast<uint4*>(smem + g.off_slot);        // [NTC][2]: staged units
-  uint8_t* skb = smem + g.off_sk;                                     // [2][skb]
+  uint8_t* skb = smem + g.off_sk;                                     // [2][skb]: u32 per unit
   uint8_t* ring = smem + g.off_ring;                                  // [NSTAGE][STAGE_BYTES]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint16_t* logits = reinterpret_cast<const uint16_t*>(a.logits);
@@ -516,6 +570,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       mbar_init(smem_u32(&ctl.counted[b]), (uint32_t)NWC);
       mbar_init(smem_u32(&ctl.hclear[b]), 1u);
       ctl.tie[b] = 0u;
+      ctl.lcnt[b] = 0u;
     }
     ctl.abort = 0;
     fence_mbar_init();
@@ -529,100 +584,108 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
     const int h = (lane >> 2) & 1;   // the half of its unit a thread reads first (bank spread)
     uint32_t gs = 0;   // stages consumed (ring slot gs % NSTAGE, phase gs / NSTAGE)
     int it = 0;
-    // Side work: the window count of the previous row, done by the warp as a
-    // whole.  Its candidate units (sketched max >= the window floor) are
-    // listed in the warp's own sketch entries of that row (each lane has read
-    // its entries first), then counted 32 at a time: a round's units are
-    // staged into the lanes' shared-memory slots by cp.async at one stage and
-    // counted at the next, so no lane waits on a load and no warp runs the
-    // count for a single lane.
-    int sw = 0;                // 0 none, 1 waiting for the record, 2 counting, 3 done
-    int sw_b = 0;
-    uint32_t sw_par = 0u, tie = 0u;
-    int sw_tot = 0, sw_q = 0;
-    bool sw_pend = false, sw_mine = false;
-    int sw_u = 0;   // the unit this lane staged for the pending round
-    const uint16_t* sw_row = logits;
-    uint32_t rc_zf2 = 0u, rc_key_m = 0u, rc_key_y = 0u;   // the record fields the count needs
-    int32_t rc_y = 0;
-    uint4* myslot = slots + 2 * t;
-    auto list_at = [&](int k) -> uint16_t* {   // entry k of this warp's list
-      uint16_t* sk = reinterpret_cast<uint16_t*>(skb + (size_t)sw_b * g.skb);
-      return sk + (warp * 32 + (k & 31) + (k >> 5) * NTC);
-    };
-    auto side_start = [&](bool block) {   // sw == 1: read the record once it is published
-      const uint32_t bar = smem_u32(&ctl.floorpub[sw_b]);
-      bool ready = block ? wait_phase(bar, sw_par, abort, g.wait_limit, a.status)
-                         : test_phase(bar, sw_par);
+    // Side work: the window count of the previous row, done by each warp at
+    // the end of a row.  Each lane tests the sketch entries of its own units
+    // of that row (only the thread that wrote an entry reads it: a warp may
+    // already be a few stages into the next row, writing the other buffer's
+    // entries of its own units).  A unit whose largest logit reaches the
+    // window floor but whose second largest does not holds exactly one window
+    // token, its max, counted from the sketch.  A unit with two or more window
+    // tokens has its two largest counted the same way and is listed for the
+    // scan warp, which reads again only the listed units whose second largest
+    // logit reaches the crossing (units the list has no room for are read
+    // again here and counted whole).  The selected token's unit is left to the
+    // scan warp (its ties need positions).
+    auto side_row = [&](int rs) {   // rs: the side row's place in this CTA's sequence
+      const int sb = rs & 1;
+      const uint32_t par = (uint32_t)((rs >> 1) & 1);
+      bool ready = wait_phase(smem_u32(&ctl.floorpub[sb]), par, abort, g.wait_limit, a.status);
       ready = __shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0) != 0;
-      if (!ready) {
-        if (block) sw = 3;   // the wait ran out: nothing to count
-        return;
-      }
-      if (ctl.rec[sw_b].mode != REC_COUNT || *abort) {
-        sw = 3;
-        return;
-      }
-      rc_zf2 = ctl.rec[sw_b].zf2;
-      rc_key_m = ctl.rec[sw_b].key_m;
-      rc_key_y = ctl.rec[sw_b].key_y;
-      rc_y = ctl.rec[sw_b].y;
-      const uint16_t* sk = reinterpret_cast<const uint16_t*>(skb + (size_t)sw_b * g.skb);
-      const float zf = bf16_lo(rc_zf2);
-      uint32_t cm = 0u;
-      for (int j = 0; j < g.nst; ++j) {
-        const int u = t + j * NTC;
-        if (u < g.nunits && bf16_val(sk[u]) >= zf) cm |= 1u << j;
-      }
-      const int n = __popc(cm);
-      int incl = n;
+      uint32_t tie = 0u;
+      if (ready && ctl.rec[sb].mode == REC_COUNT && !*abort) {
+        const uint32_t zf2w = ctl.rec[sb].zf2;
+        const __nv_bfloat162 zf2 = bf2(zf2w);
+        const uint32_t key_m = ctl.rec[sb].key_m, key_y = ctl.rec[sb].key_y;
+        const int uy = ctl.rec[sb].y >> 4;
+        uint32_t* hist = hist0 + sb * HBC;
+        const uint32_t* sk = reinterpret_cast<const uint32_t*>(skb + (size_t)sb * g.skb);
+        uint32_t sm = 0u, cm = 0u;   // bit j: unit t + j NTC holds one / several window tokens
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      sw_tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      __syncwarp();   // every lane has read its sketch entries
-      int k = incl - n;
-      while (cm) {
-        const int j = __ffs(cm) - 1;
-        cm &= cm - 1u;
-        *list_at(k++) = (uint16_t)(t + j * NTC);
-      }
-      __syncwarp();
-      sw_q = 0;
-      sw_pend = false;
-      sw = 2;
-    };
-    auto side_step = [&]() {   // sw == 2: count the round staged a stage ago, stage the next
-      if (sw_pend) {
-        cp_async_wait_all();
-        if (sw_mine)
-          count_unit(myslot, sw_u, rc_zf2, rc_key_m, rc_key_y, rc_y, hist0 + sw_b * HBC, tie);
-        sw_pend = false;
-      }
-      if (sw_q < sw_tot) {
-        const int k = sw_q + lane;
-        sw_mine = k < sw_tot;
-        if (sw_mine) {
-          sw_u = (int)*list_at(k);
-          stage_unit(sw_row, a.V, sw_u, TMA && sw_u < g.nfull, myslot);
+        for (int j = 0; j < NSTM; ++j) {
+          const int u = t + j * NTC;
+          if (u < g.nunits) {
+            const uint32_t mk = __hge2_mask(bf2(sk[u]), zf2);
+            if ((mk & 1u) && u != uy) {
+              if (mk >> 16) cm |= 1u << j;
+              else sm |= 1u << j;
+            }
+          }
         }
-        sw_q += 32;
-        sw_pend = true;
-      } else {
-        sw = 3;
-      }
-    };
-    auto side_finish = [&]() {   // end of a row: complete the side work and report it
-      if (sw == 1) side_start(true);
-      while (sw == 2) side_step();
-      uint32_t wt = tie;
+        // Candidates are handed out warp-densely, one per lane and round:
+        // candidate k of the warp belongs to the lane whose inclusive count
+        // first exceeds k, as that lane's (k - exclusive count)-th set bit.
+        const int ns = __popc(sm), nc = __popc(cm);
+        int is = ns, ic = nc;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) wt += __shfl_down_sync(0xFFFFFFFFu, wt, o);
-      if (lane == 0 && wt) atomicAdd(&ctl.tie[sw_b], wt);
+        for (int o = 1; o < 32; o <<= 1) {
+          const int vs = __shfl_up_sync(0xFFFFFFFFu, is, o), vc = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+          if (lane >= o) { is += vs; ic += vc; }
+        }
+        const int tot_s = __shfl_sync(0xFFFFFFFFu, is, 31), tot_c = __shfl_sync(0xFFFFFFFFu, ic, 31);
+        auto pick = [&](int k, int incl, int n, uint32_t mask) -> int {   // the unit, or -1
+          int L = 0;
+#pragma unroll
+          for (int st = 16; st > 0; st >>= 1) {
+            const int v = __shfl_sync(0xFFFFFFFFu, incl, L + st - 1);
+            if (v <= k) L += st;
+          }
+          const int x = __shfl_sync(0xFFFFFFFFu, incl - n, L);
+          const uint32_t mL = __shfl_sync(0xFFFFFFFFu, mask, L);
+          if (L > 31) return -1;
+          const int j = (int)__fns(mL, 0u, k - x + 1);
+          return warp * 32 + L + j * NTC;
+        };
+        for (int k0 = 0; k0 < tot_s; k0 += 32) {
+          const int k = k0 + lane;
+          const int u = pick(k, is, ns, sm);
+          if (k < tot_s) {
+            const uint32_t kk = okey16(sk[u] & 0xFFFFu);
+            atomicAdd(&hist[key_m - kk], 1u);
+            tie += (kk == key_y && u < uy) ? 1u : 0u;
+          }
+        }
+        if (tot_c) {
+          uint32_t base = 0u;
+          if (lane == 0) base = atomicAdd(&ctl.lcnt[sb], (uint32_t)tot_c);
+          base = __shfl_sync(0xFFFFFFFFu, base, 0);
+          uint32_t* lst = reinterpret_cast<uint32_t*>(smem + g.off_list) + sb * LCAP;
+          const uint16_t* srow = logits + (int64_t)(blockIdx.x + (int64_t)rs * gridDim.x) * a.ld;
+          for (int k0 = 0; k0 < tot_c; k0 += 32) {
+            const int k = k0 + lane;
+            const int u = pick(k, ic, nc, cm);
+            if (k < tot_c) {
+              const uint32_t idx = base + (uint32_t)k;
+              if (idx < LCAP) {
+                const uint32_t e = sk[u];
+                const uint32_t kg = okey16(e & 0xFFFFu), k2 = okey16(e >> 16);
+                atomicAdd(&hist[key_m - kg], 1u);
+                atomicAdd(&hist[key_m - k2], 1u);
+                if (u < uy) tie += (kg == key_y ? 1u : 0u) + (k2 == key_y ? 1u : 0u);
+                lst[idx] = (uint32_t)u | (e & 0xFFFF0000u);
+              } else {   // no room in the list: counted whole here
+                uint32_t ny;
+                count_unit(srow, a.V, u, TMA && u < g.nfull, zf2w, key_m, key_y, hist, ny);
+                if (u < uy) tie += ny;
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) tie += __shfl_down_sync(0xFFFFFFFFu, tie, o);
+      if (lane == 0 && tie) atomicAdd(&ctl.tie[sb], tie);
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl.counted[sw_b]));
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.counted[sb]));
     };
 
     for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x, ++it) {
@@ -630,7 +693,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       Acc st{-INFINITY, DF{0.f, 0.f}, make_float2(0.f, 0.f), -INFINITY};
       float c = 0.f;
       const uint16_t* row = logits + r * a.ld;
-      uint16_t* sk = reinterpret_cast<uint16_t*>(skb + (size_t)b * g.skb);
+      uint32_t* sk = reinterpret_cast<uint32_t*>(skb + (size_t)b * g.skb);
       // One stage: wait for the slot, fold this thread's unit (whole units
       // on every stage but the last), release the slot, then side work.
       auto stage = [&](int s, bool last) {
@@ -640,7 +703,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
         const int u = t + s * NTC;
         if (ok && (!last || u < g.nunits)) {
           uint32_t w[8];
-          float gm;
+          uint32_t ent = 0u;
           if (!last || u < g.nfull) {
             if (TMA) {
               const uint4* q = reinterpret_cast<const uint4*>(ring + slot * STAGE_BYTES) + 2 * t;
@@ -650,7 +713,8 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
             } else {
               load_unit_scalar(row, a.V, u, h, w);
             }
-            gm = last ? absorb_unit<false>(st, w, c) : absorb_unit<false, true>(st, w, c);
+            if (last) absorb_unit<false, false, TOPP>(st, w, c, 0xFFFFu, &ent);
+            else absorb_unit<false, true, TOPP>(st, w, c, 0xFFFFu, &ent);
           } else {
             // the row's last, partial unit: slot j of the words holds logit
             // 8 * (j < 8 ? h : 1 - h) + (j & 7) of the unit
@@ -660,16 +724,12 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               if (8 * (j < 8 ? h : 1 - h) + (j & 7) < nv) vm |= 1u << j;
-            gm = absorb_unit<true>(st, w, c, vm);
+            absorb_unit<true, false, TOPP>(st, w, c, vm, &ent);
           }
-          if (TOPP) sk[u] = (uint16_t)(__float_as_uint(gm) >> 16);
+          if (TOPP) sk[u] = ent;
         }
         mbar_arrive(smem_u32(&ctl.empty[slot]));   // this lane is done with the slot
         ++gs;
-        if (TOPP) {
-          if (sw == 1 && !last) side_start(false);
-          if (sw == 2) side_step();
-        }
       };
       // The row's parameters are published with its first stage.
       {
@@ -679,29 +739,51 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       }
       for (int s = 0; s + 1 < g.nst; ++s) stage(s, false);
       stage(g.nst - 1, true);
-      if (TOPP && it > 0) side_finish();
+      // The previous row's side work, by every warp at once: the producer
+      // meanwhile fills the ring's stages for the next row.
+      if (TOPP && it > 0) side_row(it - 1);
+      // Merge the warp's 32 thread states in a fixed order: rescale to the
+      // warp's largest reference (exact powers of two), then a shuffle tree.
+      // (At top_p < 1 the side work above has waited for the previous row's
+      // record, so the merge warp is done with this row's state buffer.)
+      float Ew = st.E;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Ew = fmaxf(Ew, __shfl_xor_sync(0xFFFFFFFFu, Ew, o));
+      DF ws_s{0.f, 0.f};
+      float ws_u = 0.f;
+      {
+        const float n = __fsub_rn(st.E, Ew);
+        const float f = exp2_int(n);
+        if (f != 0.f) {
+          ws_s = DF{__fmul_rn(st.S.hi, f), __fmul_rn(st.S.lo, f)};
+          ws_u = __fmul_rn(f, __fmaf_rn(n, __fadd_rn(st.S.hi, st.S.lo), __fadd_rn(st.U.x, st.U.y)));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const DF x{shfl_down(ws_s.hi, o), shfl_down(ws_s.lo, o)};
+        const float ux = shfl_down(ws_u, o);
+        ws_s = df_add(ws_s, x);
+        ws_u = __fadd_rn(ws_u, ux);
+      }
       // The state buffer was last read by the merge warp two rows ago (at
       // top_p < 1 the side work above has already waited for that).
       if (!TOPP && it >= 2)
         wait_phase(smem_u32(&ctl.floorpub[b]), (uint32_t)(((it - 2) >> 1) & 1), abort, g.wait_limit,
                    a.status);
-      float* pb = part + b * 3 * NTC;
-      pb[t] = st.E;
-      pb[NTC + t] = __fadd_rn(st.S.hi, st.S.lo);
-      pb[2 * NTC + t] = __fadd_rn(st.U.x, st.U.y);
       const uint32_t kx = __reduce_max_sync(0xFFFFFFFFu, okey32(__float_as_uint(st.mx)));
-      if (lane == 0) ctl.wkey[b][warp] = kx;
+      if (lane == 0) {
+        float* pb = part + b * 4 * 32;
+        pb[warp] = Ew;
+        pb[32 + warp] = ws_s.hi;
+        pb[64 + warp] = ws_s.lo;
+        pb[96 + warp] = ws_u;
+        ctl.wkey[b][warp] = kx;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl.rowpub[b]));
-      if (TOPP) {   // this row's side work runs during the next row
-        sw = 1;
-        sw_b = b;
-        sw_par = (uint32_t)((it >> 1) & 1);
-        sw_row = row;
-        tie = 0u;
-      }
     }
-    if (TOPP && it > 0) side_finish();
+    if (TOPP && it > 0) side_row(it - 1);
   } else if (warp == WPROD) {
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
@@ -770,32 +852,19 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       const float m = __uint_as_float(okey32_inverse(km));
       const float c = p.c;
       const float E = ceilf(__fmul_rn(m, c));
-      // Merge the thread states in a fixed order.
+      // Merge the warp states in a fixed order: lane l takes warp l's state,
+      // rescaled to E (exact powers of two), then a shuffle tree.
       DF Z{0.f, 0.f};
       float U = 0.f;
-      if (ok) {
-        // Lane l takes the states 4 l .. 4 l + 3 of every block of 128 into
-        // four accumulators (independent chains), merged in a fixed order.
-        const float4* pE = reinterpret_cast<const float4*>(part + b * 3 * NTC);
-        const float4* pS = reinterpret_cast<const float4*>(part + b * 3 * NTC + NTC);
-        const float4* pU = reinterpret_cast<const float4*>(part + b * 3 * NTC + 2 * NTC);
-        DF z4[4] = {DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}, DF{0.f, 0.f}};
-        float u4[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int q = lane; q < NTC / 4; q += 32) {
-          const float4 e4 = pE[q], s4 = pS[q], v4 = pU[q];
-          const float ev[4] = {e4.x, e4.y, e4.z, e4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w},
-                      uv[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if (sv[k] == 0.f && uv[k] == 0.f) continue;
-            const float n = __fsub_rn(ev[k], E);
-            const float f = exp2_int(n);
-            z4[k] = df_add_f(z4[k], __fmul_rn(sv[k], f));
-            u4[k] = __fmaf_rn(f, __fmaf_rn(n, sv[k], uv[k]), u4[k]);
-          }
+      if (ok && lane < NWC) {
+        const float* pb = part + b * 4 * 32;
+        const float n = __fsub_rn(pb[lane], E);
+        const float f = exp2_int(n);
+        if (f != 0.f) {
+          const float shi = pb[32 + lane], slo = pb[64 + lane];
+          Z = DF{__fmul_rn(shi, f), __fmul_rn(slo, f)};
+          U = __fmul_rn(f, __fmaf_rn(n, __fadd_rn(shi, slo), pb[96 + lane]));
         }
-        Z = df_add(df_add(z4[0], z4[1]), df_add(z4[2], z4[3]));
-        U = __fadd_rn(__fadd_rn(u4[0], u4[1]), __fadd_rn(u4[2], u4[3]));
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -855,14 +924,23 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       }
       __syncwarp();
     }
-  } else if (warp == WSCN) {
-    // ----------------------------------------------------------- scan warp
-    int it = 0;
-    for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x, ++it) {
+  } else {
+    // ---------------------------------------------------------- scan warps
+    // Warp WSCN + s finishes the CTA's rows it = s, s + 2, ... (buffer s), so
+    // each has two rows' time for one.
+    const int s0 = warp - WSCN;
+    int it = s0;
+    for (int64_t r = blockIdx.x + (int64_t)s0 * gridDim.x; r < a.T; r += 2 * (int64_t)gridDim.x, it += 2) {
       const int b = it & 1;
       const uint32_t par = (uint32_t)((it >> 1) & 1);
       bool ok = wait_phase(smem_u32(&ctl.floorpub[b]), par, abort, g.wait_limit, a.status);
       const RowRec rc = ctl.rec[b];
+      const uint16_t* row = logits + r * a.ld;
+      // The selected token's unit, read while the compute warps count.
+      const bool counting = TOPP && rc.mode == REC_COUNT;
+      uint32_t ybits = 0xFF80u;
+      const int64_t ypos = (int64_t)(rc.y & ~15) + lane;
+      if (ok && counting && lane < UNIT && ypos >= 0 && ypos < a.V) ybits = __ldg(row + ypos);
       // every row's count phase completes (the compute warps report each one)
       if (TOPP) ok = wait_phase(smem_u32(&ctl.counted[b]), par, abort, g.wait_limit, a.status) && ok;
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
@@ -883,10 +961,64 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       } else if (rc.mode == REC_MARK) {
         if (lane == 0) a.out_logprob[r] = __uint_as_float(kRecomputeMark);
       } else {
-        ScanOut so{};
+        // The counts so far are exact for every token but the third and
+        // later largest of the listed units.  A first scan on them bounds the
+        // crossing from below; the listed units whose second largest logit
+        // reaches that bound are read again and their other tokens above it
+        // added; a second scan then sees exact counts above the bound.
         const DF Z{rc.zhi, rc.zlo};
-        const bool found = warp_scan_window(lane, rc.dmax, rc.key_m, rc.c, rc.E,
-                                            df_mul_f(Z, rc.top_p), hist, rc.key_y, ctl.tie[b], so);
+        const DF target = df_mul_f(Z, rc.top_p);
+        uint32_t ty = 0u;
+        if (lane < UNIT && bf16_lo(ybits) >= bf16_lo(rc.zf2)) {
+          const uint32_t kk = okey16(ybits);
+          atomicAdd(&hist[rc.key_m - kk], 1u);
+          ty = (kk == rc.key_y && ypos < rc.y) ? 1u : 0u;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ty += __shfl_xor_sync(0xFFFFFFFFu, ty, o);
+        uint32_t tie_all = ctl.tie[b] + ty;
+        __syncwarp();
+        ScanOut so{};
+        bool found = warp_scan_window(lane, rc.dmax, rc.key_m, rc.c, rc.E, target, hist, rc.key_y,
+                                      tie_all, so);
+        // (units beyond the list's room were counted whole by the compute warps)
+        const uint32_t ncx = ctl.lcnt[b] < LCAP ? ctl.lcnt[b] : LCAP;
+        if (ncx > 0u) {
+          const uint32_t kap = found ? so.key_thr : rc.key_m - rc.dmax;
+          const uint32_t kvb = okey16_inverse(kap);
+          const uint32_t* lst = reinterpret_cast<const uint32_t*>(smem + g.off_list) + b * LCAP;
+          const int uy = rc.y >> 4;
+          uint32_t* lstw = reinterpret_cast<uint32_t*>(smem + g.off_list) + b * LCAP;
+          // keep the listed units whose second largest reaches kap (in place, in order)
+          uint32_t nneed = 0u;
+          for (uint32_t k0 = 0u; k0 < ncx; k0 += 32u) {
+            const uint32_t k = k0 + (uint32_t)lane;
+            const uint32_t item = k < ncx ? lst[k] : 0u;
+            const bool need = k < ncx && okey16(item >> 16) >= kap;
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, need);
+            __syncwarp();
+            if (need) lstw[nneed + __popc(bal & ((1u << lane) - 1u))] = item;
+            nneed += __popc(bal);
+          }
+          __syncwarp();
+          uint32_t added = 0u, tx = 0u;
+          for (uint32_t k = (uint32_t)lane; k < nneed; k += 32u) {
+            const uint32_t item = lstw[k];
+            const int u = (int)(item & 0xFFFFu);
+            uint32_t ny;
+            added += recount_unit(row, a.V, u, TMA && u < g.nfull, kvb | (kvb << 16), rc.key_m,
+                                  rc.key_y, hist, ny);
+            if (u < uy) tx += ny;
+          }
+          if (__any_sync(0xFFFFFFFFu, added != 0u)) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) tx += __shfl_xor_sync(0xFFFFFFFFu, tx, o);
+            tie_all += tx;
+            __syncwarp();
+            found = warp_scan_window(lane, rc.dmax, rc.key_m, rc.c, rc.E, target, hist, rc.key_y,
+                                     tie_all, so);
+          }
+        }
         if (lane == 0) {
           if (!found) {
             a.out_logprob[r] = __uint_as_float(kRecomputeMark);
@@ -906,7 +1038,10 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       if (TOPP && rc.mode == REC_COUNT) {
         __syncwarp();
         for (uint32_t d = (uint32_t)lane; d <= rc.dmax; d += 32u) hist[d] = 0u;
-        if (lane == 0) ctl.tie[b] = 0u;
+        if (lane == 0) {
+          ctl.tie[b] = 0u;
+          ctl.lcnt[b] = 0u;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl.hclear[b]));
@@ -915,6 +1050,13 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
 }
 
 }  // namespace
+
+constexpr uint32_t kSmemMax =
+    align_up(align_up((uint32_t)sizeof(Ctrl), 128) + PART_BYTES + 2u * HBC * 4u + 2u * LCAP * 4u +
+                 2u * align_up((uint32_t)(V_MAX / UNIT) * 4u, 16),
+             128) +
+    NSTAGE * STAGE_BYTES;
+static_assert(kSmemMax <= 232448u, "shared memory of one CTA");
 
 bool lpe_stream_eligible(const LpeArgs& a) {
   return a.dtype == 0 && a.V >= V_MIN && a.V <= V_MAX;
@@ -930,12 +1072,12 @@ cudaError_t launch_lpe_stream(const LpeArgs& a, cudaStream_t stream, long long w
   g.tma_bytes = (uint32_t)((a.V / 8) * 16);
   uint32_t off = align_up((uint32_t)sizeof(Ctrl), 128);
   g.off_part = off;
-  off += 2u * 3u * NTC * 4u;
+  off += PART_BYTES;
   g.off_hist = off;
   off += 2u * HBC * 4u;
-  g.off_slot = off;
-  off += NTC * 32u;
-  g.skb = align_up((uint32_t)g.nunits * 2u, 16);
+  g.off_list = off;
+  off += 2u * LCAP * 4u;
+  g.skb = align_up((uint32_t)g.nunits * 4u, 16);
   g.off_sk = off;
   off += 2u * g.skb;
   off = align_up(off, 128);
@@ -955,11 +1097,7 @@ cudaError_t launch_lpe_stream(const LpeArgs& a, cudaStream_t stream, long long w
   const int vi = (topp ? 2 : 0) + (g.tma ? 1 : 0);
   const void* fns[4] = {(const void*)lpe_stream_kernel<false, false>, (const void*)lpe_stream_kernel<false, true>,
                         (const void*)lpe_stream_kernel<true, false>, (const void*)lpe_stream_kernel<true, true>};
-  const int smax = (int)(align_up(align_up((uint32_t)sizeof(Ctrl), 128) + 2u * 3u * NTC * 4u +
-                                      2u * HBC * 4u + NTC * 32u +
-                                      2u * align_up((uint32_t)(V_MAX / UNIT) * 2u, 16),
-                                  128) +
-                         NSTAGE * STAGE_BYTES);
+  const int smax = (int)kSmemMax;
   if (dev < 0 || dev >= 64 || attr[dev][vi].load() < smax) {
     if ((e = cudaFuncSetAttribute(fns[vi], cudaFuncAttributeMaxDynamicSharedMemorySize, smax)) !=
         cudaSuccess)

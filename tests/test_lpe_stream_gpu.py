@@ -63,12 +63,12 @@ def test_stream_special_rows(cuda_lib, oracle, T, p):
     check(cuda_lib, oracle, z, far, T, p, f"special-far T{T} p{p}")
 
 
-@pytest.mark.parametrize("V,ld", [(14847, 14848), (14848, 14848), (151931, 151936),
+@pytest.mark.parametrize("V,ld", [(14335, 14336), (14336, 14336), (151931, 151936),
                                   (174080, 174080), (174081, 174088), (20000, 20480)])
 @pytest.mark.parametrize("p", [0.9, 1.0])
 def test_stream_vocab_sizes(cuda_lib, oracle, V, ld, p):
     """Partial last units, the smallest and the largest vocabularies the
-    streaming path takes (14,848 and 174,080) and one just outside each (the
+    streaming path takes (14,336 and 174,080) and one just outside each (the
     per-row kernel), padded row strides."""
     base, _ = workloads.peaked_bf16(12, V=ld, seed=17, device="cuda")
     z = base[:, :V]
