@@ -184,9 +184,13 @@ struct Acc {
   DF S;         // sum 2^d
   float2 U;     // sum 2^d d (two packed lanes)
   float mx;     // largest logit seen
+  uint32_t mn;  // without U: smallest logit seen per bf16x2 lane (a -inf logit makes the row
+                // non-finite, which U would otherwise show as NaN)
 };
 
 // Moves the reference up to En (> E): every sum scales by 2^(E - En), exactly.
+// NOU: U is not kept (it stays 0).
+template <bool NOU = false>
 __device__ __forceinline__ void rebase(Acc& st, float En) {
   if (st.E == -INFINITY) {
     st.E = En;
@@ -194,8 +198,10 @@ __device__ __forceinline__ void rebase(Acc& st, float En) {
   }
   const float n = __fsub_rn(st.E, En);   // integer, < 0
   const float f = exp2_int(n);
-  st.U.x = __fmul_rn(f, __fmaf_rn(n, st.S.hi, st.U.x));
-  st.U.y = __fmul_rn(f, st.U.y);
+  if (!NOU) {
+    st.U.x = __fmul_rn(f, __fmaf_rn(n, st.S.hi, st.U.x));
+    st.U.y = __fmul_rn(f, st.U.y);
+  }
   st.S.hi = __fmul_rn(st.S.hi, f);
   st.S.lo = __fmul_rn(st.S.lo, f);
   st.E = En;
@@ -216,7 +222,9 @@ __device__ __forceinline__ void top2_merge(__nv_bfloat162& a1, __nv_bfloat162& b
 // (bit j: half j & 1 of word j >> 1) exist -- the row's last, partial unit.
 // TOP2: *ent receives the unit's sketch entry, its largest logit (low half)
 // and its second largest (high half; -inf for a unit of one logit), as bf16.
-template <bool MASKED, bool UNIFORM = false, bool TOP2 = false>
+// NOU: U is not kept -- a row at top_p < 1 takes its entropy from the
+// retained set's counts, not from the whole row.
+template <bool MASKED, bool UNIFORM = false, bool TOP2 = false, bool NOU = false>
 __device__ __forceinline__ float absorb_unit(Acc& st, const uint32_t (&w)[8], float c,
                                              uint32_t vmask = 0xFFFFu, uint32_t* ent = nullptr) {
   uint32_t wm[8];
@@ -236,6 +244,21 @@ __device__ __forceinline__ float absorb_unit(Acc& st, const uint32_t (&w)[8], fl
     for (int k = 0; k < 4; ++k) {
       A[k] = __hmax2(bf2(wm[2 * k]), bf2(wm[2 * k + 1]));
       B[k] = __hmin2(bf2(wm[2 * k]), bf2(wm[2 * k + 1]));
+    }
+    if (NOU) {
+      if (MASKED) {   // absent logits read as +inf for the min
+        uint32_t mn = 0x7F807F80u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint32_t v = w[k];
+          if (!((vmask >> (2 * k)) & 1u)) v = (v & 0xFFFF0000u) | 0x7F80u;
+          if (!((vmask >> (2 * k + 1)) & 1u)) v = (v & 0xFFFFu) | 0x7F800000u;
+          mn = u32(__hmin2(bf2(mn), bf2(v)));
+        }
+        st.mn = u32(__hmin2(bf2(st.mn), bf2(mn)));
+      } else {
+        st.mn = u32(__hmin2(bf2(st.mn), __hmin2(__hmin2(B[0], B[1]), __hmin2(B[2], B[3]))));
+      }
     }
     top2_merge(A[0], B[0], A[1], B[1]);
     top2_merge(A[2], B[2], A[3], B[3]);
@@ -257,10 +280,10 @@ __device__ __forceinline__ float absorb_unit(Acc& st, const uint32_t (&w)[8], fl
   const bool up = __fmaf_rn(gm, c, -st.E) > LAZY;
   if (UNIFORM) {   // every lane is here: one warp-uniform test guards the rare re-base
     if (__any_sync(0xFFFFFFFFu, up)) {
-      if (up) rebase(st, ceilf(__fmul_rn(gm, c)));
+      if (up) rebase<NOU>(st, ceilf(__fmul_rn(gm, c)));
     }
   } else if (up) {
-    rebase(st, ceilf(__fmul_rn(gm, c)));
+    rebase<NOU>(st, ceilf(__fmul_rn(gm, c)));
   }
   const float2 c2 = make_float2(c, c);
   const float2 nE2 = make_float2(-st.E, -st.E);
@@ -282,7 +305,8 @@ __device__ __forceinline__ float absorb_unit(Acc& st, const uint32_t (&w)[8], fl
     }
     sh[hf] = __fadd2_rn(__fadd2_rn(e[0], e[1]), __fadd2_rn(e[2], e[3]));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) st.U = __ffma2_rn(e[i], d[i], st.U);
+    for (int i = 0; i < 4; ++i)
+      if (!NOU) st.U = __ffma2_rn(e[i], d[i], st.U);
   }
   const float2 s = __fadd2_rn(sh[0], sh[1]);
   float t, r;
@@ -449,18 +473,6 @@ __device__ __forceinline__ bool wait_full_warp(uint32_t bar, uint32_t parity, vo
       : "memory");
   if (__all_sync(0xFFFFFFFFu, ok != 0u)) return true;
   return __all_sync(0xFFFFFFFFu, wait_phase(bar, parity, abort, limit, status));
-}
-
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool test_phase(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0u;
 }
 
 // Counts the tokens of unit u of a row that reach the window floor (zf2w, a
@@ -690,8 +702,9 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
 
     for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x, ++it) {
       const int b = it & 1;
-      Acc st{-INFINITY, DF{0.f, 0.f}, make_float2(0.f, 0.f), -INFINITY};
+      Acc st{-INFINITY, DF{0.f, 0.f}, make_float2(0.f, 0.f), -INFINITY, 0x7F807F80u};
       float c = 0.f;
+      bool nou = false;   // a row at top_p < 1: U is not needed
       const uint16_t* row = logits + r * a.ld;
       uint32_t* sk = reinterpret_cast<uint32_t*>(skb + (size_t)b * g.skb);
       // One stage: wait for the slot, fold this thread's unit (whole units
@@ -713,8 +726,13 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
             } else {
               load_unit_scalar(row, a.V, u, h, w);
             }
-            if (last) absorb_unit<false, false, TOPP>(st, w, c, 0xFFFFu, &ent);
-            else absorb_unit<false, true, TOPP>(st, w, c, 0xFFFFu, &ent);
+            if (nou) {
+              if (last) absorb_unit<false, false, TOPP, true>(st, w, c, 0xFFFFu, &ent);
+              else absorb_unit<false, true, TOPP, true>(st, w, c, 0xFFFFu, &ent);
+            } else {
+              if (last) absorb_unit<false, false, TOPP>(st, w, c, 0xFFFFu, &ent);
+              else absorb_unit<false, true, TOPP>(st, w, c, 0xFFFFu, &ent);
+            }
           } else {
             // the row's last, partial unit: slot j of the words holds logit
             // 8 * (j < 8 ? h : 1 - h) + (j & 7) of the unit
@@ -724,7 +742,8 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               if (8 * (j < 8 ? h : 1 - h) + (j & 7) < nv) vm |= 1u << j;
-            absorb_unit<true, false, TOPP>(st, w, c, vm, &ent);
+            if (nou) absorb_unit<true, false, TOPP, true>(st, w, c, vm, &ent);
+            else absorb_unit<true, false, TOPP>(st, w, c, vm, &ent);
           }
           if (TOPP) sk[u] = ent;
         }
@@ -736,6 +755,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
         const uint32_t slot = gs & (NSTAGE - 1);
         wait_full(smem_u32(&ctl.full[slot]), (gs / NSTAGE) & 1u, abort, g.wait_limit, a.status);
         c = ctl.rp[it % NRP].c;
+        nou = TOPP && ctl.rp[it % NRP].top_p < 1.0f;
       }
       for (int s = 0; s + 1 < g.nst; ++s) stage(s, false);
       stage(g.nst - 1, true);
@@ -758,6 +778,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
           ws_s = DF{__fmul_rn(st.S.hi, f), __fmul_rn(st.S.lo, f)};
           ws_u = __fmul_rn(f, __fmaf_rn(n, __fadd_rn(st.S.hi, st.S.lo), __fadd_rn(st.U.x, st.U.y)));
         }
+        if (nou && (bf16_lo(st.mn) == -INFINITY || bf16_hi(st.mn) == -INFINITY)) ws_u = NAN;
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
