@@ -24,6 +24,8 @@ STATUS_BAD_TOKEN_ID = 0x1
 STATUS_NONFINITE = 0x2
 OP_LOGPROB_ENTROPY, OP_GRPO_LOSS, OP_LMHEAD, OP_LMHEAD_BWD, OP_LMHEAD_TOPP = 0, 1, 2, 3, 4
 OP_CANONICAL = 5
+OP_CANONICAL_TOPP = 6
+SHARD_COUNTS_BYTES = 8224   # rlk_shard_counts: one row's window counts of one shard
 CANONICAL_TP, CANONICAL_VOCAB = 8, 152576
 SHARD_PARTIAL_WORDS = 8   # rlk_shard_partial: 32 bytes per (shard, row)
 AGG_TOKEN_MEAN, AGG_SEQ_MEAN_TOKEN_MEAN, AGG_PROMPT_MEAN = 0, 1, 2
@@ -51,6 +53,8 @@ EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logpro
            "rlk_lmhead_logprob_bwd", "rlk_shard_partials", "rlk_shard_combine",
            "rlk_shard_partials_support",
            "rlk_logprob_entropy_canonical", "rlk_sample_top_p",
+           "rlk_shard_window_counts", "rlk_shard_combine_topp",
+           "rlk_logprob_entropy_canonical_topp",
            "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
 DEBUG_EXPORTS = ("rlk_lmhead_logits_debug", "rlk_debug_inject_launch_failures",
@@ -59,6 +63,7 @@ STATUS_TIMEOUT = 0x4
 STATUS_BAD_SUPPORT = 0x8
 STATUS_NO_STATE = 0x10
 STATUS_BAD_PARAM = 0x20
+STATUS_UNRESOLVED = 0x40
 ROW_STATE_WORDS = 8   # rlk_row_state: 32 bytes per row
 
 _lock = threading.Lock()
@@ -139,6 +144,16 @@ def load(path: str | None = None):
         lib.rlk_logprob_entropy_canonical.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32, i32,
                                                       i64, vp, vp, vp, vp, sz, vp]
         lib.rlk_logprob_entropy_canonical.restype = ctypes.c_int
+        lib.rlk_shard_window_counts.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, i64, i32, vp,
+                                                f32, f32, vp, i32, vp, vp]
+        lib.rlk_shard_window_counts.restype = ctypes.c_int
+        lib.rlk_shard_combine_topp.argtypes = [vp, vp, i32, i64, i64, i64, vp, f32, f32, vp, vp,
+                                               vp, vp, vp]
+        lib.rlk_shard_combine_topp.restype = ctypes.c_int
+        lib.rlk_logprob_entropy_canonical_topp.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, f32,
+                                                           f32, i32, i64, vp, vp, vp, vp, vp, sz,
+                                                           vp]
+        lib.rlk_logprob_entropy_canonical_topp.restype = ctypes.c_int
         lib.rlk_lmhead_logprob_fwd.argtypes = [vp, vp, i64, i64, i64, vp, f32, f32, vp, vp, vp,
                                                vp, vp, sz, vp]
         lib.rlk_lmhead_logprob_fwd.restype = ctypes.c_int
@@ -650,6 +665,70 @@ def shard_combine(partials, token_ids, temperature, V, shard_width, *, status_wo
     return lp, ent
 
 
+def shard_window_counts(logits, token_ids, temperature, top_p, V, first_col, shard_width,
+                        n_shards, all_partials):
+    """rlk_shard_window_counts: [n_shards, T, 8224] uint8 window counts of this
+    rank's shards (bf16 ``logits`` [T, cols]), given every shard's partial
+    ([n_all, T, 8], canonical order)."""
+    lib = load()
+    _need_cuda(logits, token_ids, all_partials)
+    dt = _logits_dtype(logits)
+    T = logits.shape[0]
+    ld = logits.stride(0) if T > 1 else logits.shape[1]
+    if all_partials.dtype != torch.float32 or not all_partials.is_contiguous():
+        raise ValueError("all_partials must be contiguous fp32 [n_all, T, 8]")
+    out = torch.empty((n_shards, T, SHARD_COUNTS_BYTES), device=logits.device, dtype=torch.uint8)
+    code = lib.rlk_shard_window_counts(_ptr(logits), dt, T, int(V), ld, int(first_col),
+                                       int(shard_width), int(n_shards), _ptr(token_ids),
+                                       float(temperature), float(top_p), _ptr(all_partials),
+                                       int(all_partials.shape[0]), _ptr(out), _stream(logits.device))
+    _check("rlk_shard_window_counts", code)
+    return out
+
+
+def shard_combine_topp(partials, counts, token_ids, temperature, top_p, V, shard_width, *,
+                       status_word=None):
+    """rlk_shard_combine_topp: (logprob, entropy, nucleus size) from all shards'
+    partials and window counts (canonical order)."""
+    lib = load()
+    _need_cuda(partials, counts, token_ids)
+    n_shards, T = partials.shape[0], partials.shape[1]
+    if counts.shape[:2] != (n_shards, T) or not counts.is_contiguous():
+        raise ValueError("counts must be contiguous [n_shards, T, 8224]")
+    lp = torch.empty(T, device=partials.device, dtype=torch.float32)
+    ent = torch.empty(T, device=partials.device, dtype=torch.float32)
+    k = torch.empty(T, device=partials.device, dtype=torch.int32)
+    code = lib.rlk_shard_combine_topp(_ptr(partials), _ptr(counts), n_shards, T, int(V),
+                                      int(shard_width), _ptr(token_ids), float(temperature),
+                                      float(top_p), _ptr(lp), _ptr(ent), _ptr(k), _ptr(status_word),
+                                      _stream(partials.device))
+    _check("rlk_shard_combine_topp", code)
+    return lp, ent, k
+
+
+def logprob_entropy_canonical_topp(logits, token_ids, temperature, top_p, n_virtual=CANONICAL_TP,
+                                   padded_vocab=CANONICAL_VOCAB, *, status_word=None):
+    """The canonical partition on one device at top_p < 1: (logprob, entropy,
+    nucleus size)."""
+    lib = load()
+    _need_cuda(logits, token_ids)
+    dt = _logits_dtype(logits)
+    T, V = logits.shape
+    ld = logits.stride(0) if T > 1 else V
+    ws = torch.empty(max(int(lib.rlk_workspace_size(OP_CANONICAL_TOPP, T, n_virtual, 0)), 16),
+                     device=logits.device, dtype=torch.uint8)
+    lp = torch.empty(T, device=logits.device, dtype=torch.float32)
+    ent = torch.empty(T, device=logits.device, dtype=torch.float32)
+    k = torch.empty(T, device=logits.device, dtype=torch.int32)
+    code = lib.rlk_logprob_entropy_canonical_topp(_ptr(logits), dt, T, V, ld, _ptr(token_ids),
+                                                  float(temperature), float(top_p), int(n_virtual),
+                                                  int(padded_vocab), _ptr(lp), _ptr(ent), _ptr(k),
+                                                  _ptr(status_word), _ptr(ws), ws.numel(),
+                                                  _stream(logits.device))
+    _check("rlk_logprob_entropy_canonical_topp", code)
+    return lp, ent, k
+
+
 def logprob_entropy_canonical(logits, token_ids, temperature, n_virtual=CANONICAL_TP,
                               padded_vocab=CANONICAL_VOCAB, *, status_word=None):
     """The canonical partition on one device (top_p = 1)."""
@@ -671,9 +750,10 @@ def logprob_entropy_canonical(logits, token_ids, temperature, n_virtual=CANONICA
 
 
 def gather_shard_partials(local_partials, group=None):
-    """All ranks' partials ([n_local, T, 8] each) gathered in rank order, which
-    is canonical shard order: [n_local * world, T, 8].  The one exchange of the
-    vocabulary-parallel path."""
+    """All ranks' per-shard tensors ([n_local, T, ...] each: partials, or window
+    counts) gathered in rank order, which is canonical shard order:
+    [n_local * world, T, ...].  The exchange of the vocabulary-parallel path
+    (once at top_p = 1, twice at top_p < 1)."""
     import torch.distributed as dist
     world = dist.get_world_size(group)
     parts = [torch.empty_like(local_partials) for _ in range(world)]
@@ -682,17 +762,25 @@ def gather_shard_partials(local_partials, group=None):
 
 
 def vocab_parallel_logprob_entropy(local_logits, token_ids, temperature, V, group=None,
-                                   n_virtual=CANONICAL_TP, padded_vocab=CANONICAL_VOCAB):
-    """Tensor-parallel top_p = 1 log-probability and entropy: this rank's
-    canonical shards -> partials -> gather in rank order -> combine.  The result
-    is bitwise the same for every tensor-parallel degree."""
+                                   n_virtual=CANONICAL_TP, padded_vocab=CANONICAL_VOCAB,
+                                   top_p=1.0):
+    """Tensor-parallel log-probability and entropy: this rank's canonical
+    shards -> partials -> gather in rank order -> combine; at top_p < 1 the
+    gathered partials set every shard's window, whose counts are gathered too
+    and combined (returns (logprob, entropy, nucleus size) then).  The result is
+    bitwise the same for every tensor-parallel degree."""
     import torch.distributed as dist
     world = dist.get_world_size(group) if dist.is_initialized() else 1
     rank = dist.get_rank(group) if dist.is_initialized() else 0
     _, n, first_col, width = canonical_plan(world, rank, n_virtual, padded_vocab)
     part = shard_partials(local_logits, token_ids, temperature, V, first_col, width, n)
     allp = gather_shard_partials(part, group) if world > 1 else part
-    return shard_combine(allp, token_ids, temperature, V, width)
+    if top_p >= 1.0:
+        return shard_combine(allp, token_ids, temperature, V, width)
+    cnt = shard_window_counts(local_logits, token_ids, temperature, top_p, V, first_col, width, n,
+                              allp)
+    allc = gather_shard_partials(cnt, group) if world > 1 else cnt
+    return shard_combine_topp(allp, allc, token_ids, temperature, top_p, V, width)
 
 
 def sample_top_p(logits, temperature, top_p, uniforms, *, row_state=None, status_word=None):

@@ -153,6 +153,20 @@ struct ShardCombineArgs {
   float* out_logprob;
   float* out_entropy;
   uint32_t* status;
+  // top_p < 1: the shards' window counts ([n_shards][T], same order)
+  const void* counts = nullptr;
+  float top_p = 1.0f;
+  int32_t* out_k = nullptr;
+};
+struct ShardWindowArgs {
+  const void* logits;     // bf16: this rank's columns
+  int64_t T, V, ld, first_col, shard_width;
+  int n_shards;           // this rank's shards
+  const int32_t* ids;
+  float temperature, top_p;
+  const void* all_partials;   // [n_all][T]: every shard's partial, canonical order
+  int n_all;
+  void* counts;           // [n_shards][T]
 };
 struct SampleArgs {
   const void* logits;   // bf16
@@ -167,6 +181,8 @@ cudaError_t launch_sample(const SampleArgs& a, cudaStream_t stream);
 cudaError_t launch_shard_partials(const ShardArgs& a, cudaStream_t stream);
 cudaError_t launch_shard_combine(const ShardCombineArgs& a, cudaStream_t stream);
 cudaError_t launch_shard_support_partials(const ShardArgs& a, cudaStream_t stream);
+cudaError_t launch_shard_window(const ShardWindowArgs& a, cudaStream_t stream);
+cudaError_t launch_shard_combine_topp(const ShardCombineArgs& a, cudaStream_t stream);
 
 // Consumes one launch failure injected by rlk_debug_inject_launch_failures.
 bool take_injected_failure();

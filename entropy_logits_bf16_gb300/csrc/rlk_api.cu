@@ -136,6 +136,8 @@ size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H) {
     case RLK_OP_LMHEAD_TOPP: return rlk::lmhead_topp_workspace_bytes(T, V, H);
     case RLK_OP_CANONICAL:
       return V < 1 ? 0 : (size_t)V * (size_t)T * sizeof(rlk_shard_partial);
+    case RLK_OP_CANONICAL_TOPP:
+      return V < 1 ? 0 : (size_t)V * (size_t)T * (sizeof(rlk_shard_partial) + sizeof(rlk_shard_counts));
   }
   return 0;
 }
@@ -566,6 +568,112 @@ rlk_status rlk_logprob_entropy_canonical(const void* logits, rlk_dtype dtype, in
   if (st != RLK_OK) return st;
   return rlk_shard_combine(part, n_virtual, T, V, W, token_ids, temperature, out_logprob,
                            out_entropy, out_status_word, stream);
+}
+
+static_assert(sizeof(rlk_shard_counts) == 8224, "rlk_shard_counts is 8224 bytes");
+
+rlk_status rlk_shard_window_counts(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                   int64_t ld, int64_t first_col, int64_t shard_width,
+                                   int32_t n_shards, const int32_t* token_ids, float temperature,
+                                   float top_p, const rlk_shard_partial* all_partials,
+                                   int32_t n_all, rlk_shard_counts* out_counts, rlk_stream stream) {
+  if (dtype != RLK_BF16 && dtype != RLK_F32) return RLK_ERR_INVALID_ARG;
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || shard_width < 1 || n_shards < 1)
+    return RLK_ERR_INVALID_ARG;
+  if (first_col < 0 || first_col % shard_width != 0) return RLK_ERR_INVALID_ARG;
+  if (n_all < first_col / shard_width + n_shards || shard_width * (int64_t)n_all < V)
+    return RLK_ERR_INVALID_ARG;
+  const int64_t span = shard_width * (int64_t)n_shards;
+  int64_t cols = V - first_col < span ? V - first_col : span;
+  if (cols < 0) cols = 0;
+  if (ld < cols) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature) || !(top_p > 0.f && top_p < 1.f)) return RLK_ERR_INVALID_ARG;
+  if (dtype != RLK_BF16) return RLK_ERR_UNSUPPORTED;
+  if (T == 0) return RLK_OK;
+  if (!logits || !token_ids || !all_partials || !out_counts) return RLK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) % 2u != 0 ||
+      reinterpret_cast<uintptr_t>(all_partials) % 16u != 0 ||
+      reinterpret_cast<uintptr_t>(out_counts) % 16u != 0)
+    return RLK_ERR_INVALID_ARG;
+  rlk::ShardWindowArgs a{};
+  a.logits = logits;
+  a.T = T;
+  a.V = V;
+  a.ld = ld;
+  a.first_col = first_col;
+  a.shard_width = shard_width;
+  a.n_shards = n_shards;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.top_p = top_p;
+  a.all_partials = all_partials;
+  a.n_all = n_all;
+  a.counts = out_counts;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
+  return rlk::launch_shard_window(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_shard_combine_topp(const rlk_shard_partial* partials, const rlk_shard_counts* counts,
+                                  int32_t n_shards, int64_t T, int64_t V, int64_t shard_width,
+                                  const int32_t* token_ids, float temperature, float top_p,
+                                  float* out_logprob, float* out_entropy, int32_t* out_k,
+                                  uint32_t* out_status_word, rlk_stream stream) {
+  if (T < 0 || V < 1 || V > (int64_t(1) << 24) || shard_width < 1 || n_shards < 1)
+    return RLK_ERR_INVALID_ARG;
+  if (shard_width * (int64_t)n_shards < V) return RLK_ERR_INVALID_ARG;
+  if (!finite_positive(temperature) || !(top_p > 0.f && top_p < 1.f)) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  if (!partials || !counts || !token_ids || !out_logprob || !out_entropy)
+    return RLK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(partials) % 16u != 0 ||
+      reinterpret_cast<uintptr_t>(counts) % 16u != 0)
+    return RLK_ERR_INVALID_ARG;
+  rlk::ShardCombineArgs a{};
+  a.partials = partials;
+  a.n_shards = n_shards;
+  a.T = T;
+  a.V = V;
+  a.shard_width = shard_width;
+  a.ids = token_ids;
+  a.temperature = temperature;
+  a.out_logprob = out_logprob;
+  a.out_entropy = out_entropy;
+  a.status = out_status_word;
+  a.counts = counts;
+  a.top_p = top_p;
+  a.out_k = out_k;
+  if (rlk::take_injected_failure()) return RLK_ERR_CUDA;
+  return rlk::launch_shard_combine_topp(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RLK_OK
+             : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_logprob_entropy_canonical_topp(const void* logits, rlk_dtype dtype, int64_t T,
+                                              int64_t V, int64_t ld, const int32_t* token_ids,
+                                              float temperature, float top_p, int32_t n_virtual,
+                                              int64_t padded_vocab, float* out_logprob,
+                                              float* out_entropy, int32_t* out_k,
+                                              uint32_t* out_status_word, void* workspace,
+                                              size_t workspace_bytes, rlk_stream stream) {
+  if (n_virtual < 1 || padded_vocab < V || padded_vocab % n_virtual != 0 || ld < V)
+    return RLK_ERR_INVALID_ARG;
+  const size_t part_bytes = (size_t)n_virtual * (size_t)(T > 0 ? T : 0) * sizeof(rlk_shard_partial);
+  const size_t need = part_bytes + (size_t)n_virtual * (size_t)(T > 0 ? T : 0) * sizeof(rlk_shard_counts);
+  if (T > 0 && (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 16u != 0))
+    return RLK_ERR_WORKSPACE;
+  const int64_t W = padded_vocab / n_virtual;
+  rlk_shard_partial* part = static_cast<rlk_shard_partial*>(workspace);
+  rlk_shard_counts* cnt = reinterpret_cast<rlk_shard_counts*>(static_cast<char*>(workspace) + part_bytes);
+  rlk_status st = rlk_shard_partials(logits, dtype, T, V, ld, 0, W, n_virtual, token_ids,
+                                     temperature, part, stream);
+  if (st != RLK_OK) return st;
+  st = rlk_shard_window_counts(logits, dtype, T, V, ld, 0, W, n_virtual, token_ids, temperature,
+                               top_p, part, n_virtual, cnt, stream);
+  if (st != RLK_OK) return st;
+  return rlk_shard_combine_topp(part, cnt, n_virtual, T, V, W, token_ids, temperature, top_p,
+                                out_logprob, out_entropy, out_k, out_status_word, stream);
 }
 
 rlk_status rlk_sample_top_p(const void* logits, rlk_dtype dtype, int64_t T, int64_t V, int64_t ld,

@@ -1,4 +1,5 @@
-// The canonical vocabulary partition for the top_p = 1 path.
+// The canonical vocabulary partition: top_p = 1, a supplied retained set, and
+// top_p < 1 (window counts per shard after one exchange of the partials).
 //
 // RL-Kernel "Qwen3-8B VIME train-rollout consistency", section "Canonical
 // topology strategy": the launcher fixes a virtual tensor-parallel degree of 8
@@ -331,6 +332,338 @@ __global__ void __launch_bounds__(256) shard_combine_kernel(ShardCombineArgs a, 
   a.out_entropy[r] = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, st.u), zf));
 }
 
+
+// ------------------------------------------------------------- top_p < 1
+// The retained set at top_p < 1 under the same partition, with no supplied
+// set: every rank first gathers all shards' partials, so each one knows the
+// row's max m and Z.  From them every shard derives the same window
+// z >= m - L T with L = ln(V / ((1 - top_p) Z)) + 0.5 (Z relative to the
+// max's weight): below it lies less than V e^-L < (1 - top_p) Z of the mass,
+// so the nucleus boundary lies inside.  Each shard counts its logits in the
+// window per bf16 value -- every token of one value carries the same mass --
+// and the integer counts of all shards add up exactly, in any order.  Values
+// with |z| < 2^-12 share one bin whose mass each shard sums in a fixed order
+// (combined in shard order).  The combine scans the bins largest value first
+// with a fixed-order double-float prefix, as the single-device scorer does.
+
+constexpr int HBW = 4096;   // window bins (compressed keys below the row max)
+// Ordered 16-bit keys of the bf16 values with |z| < 2^-12 (exponent field
+// < 115) form the contiguous interval [MERGE_LO, MERGE_HI], compressed into
+// the single key MERGE_LO.
+constexpr uint32_t MERGE_LO = 0x4680u;
+constexpr uint32_t MERGE_HI = 0xB97Fu;
+constexpr uint32_t MERGE_SPAN = MERGE_HI - MERGE_LO;
+
+__device__ __forceinline__ uint32_t ckey(uint32_t k) {
+  return k < MERGE_LO ? k : (k <= MERGE_HI ? MERGE_LO : k - MERGE_SPAN);
+}
+__device__ __forceinline__ uint32_t ckey_expand(uint32_t ck) {   // ck != MERGE_LO
+  return ck < MERGE_LO ? ck : ck + MERGE_SPAN;
+}
+__device__ __forceinline__ uint32_t key_of_f(float v) { return okey16(__float_as_uint(v) >> 16); }
+
+struct ShardCounts {      // one row's window counts of one shard (8224 bytes)
+  uint32_t ties;          // tokens whose value is y's and whose id is below y
+  uint32_t merged_n;      // tokens in the near-zero bin
+  float merged_hi, merged_lo;   // their sum of 2^d, d = fma(z, c, -E), a double-float
+  float merged_u;         // their sum of 2^d d
+  uint32_t over;          // a bin of this shard passed 65535 tokens
+  uint32_t pad[2];
+  uint16_t cnt[HBW];      // bins 0..dmax
+};
+static_assert(sizeof(ShardCounts) == 8224, "the counts' layout is part of the ABI");
+
+struct Window {
+  float m, E, zf;         // the row max, E = fp32(m c), Z relative to 2^E
+  DF Z;
+  uint32_t key_m, key_lo, ck_m, dmax;
+  bool fits;              // the window has at most HBW bins and the row is finite
+};
+
+// Every shard and the combine derive the row's window from the gathered
+// partials (merged in shard order), so they all agree on it.
+__device__ Window row_window(const float4* p, int n_all, int64_t T, int64_t r, int64_t V, float c,
+                             float temp, float top_p) {
+  Part st{-INFINITY, 0.f, 0.f, 0.f};
+  for (int s = 0; s < n_all; ++s) {
+    const float4 q = p[2 * ((int64_t)s * T + r)];
+    st = part_merge(st, Part{q.x, q.y, q.z, q.w}, c);
+  }
+  Window w{};
+  w.m = st.m;
+  w.E = __fmul_rn(st.m, c);
+  w.Z = DF{st.hi, st.lo};
+  w.zf = __fadd_rn(st.hi, st.lo);
+  const float one_m_p = __fsub_rn(1.f, top_p);
+  const float L = fmaxf(logf(__fdiv_rn((float)V, __fmul_rn(one_m_p, w.zf))), 0.f) + 0.5f;
+  const float zlo = __fsub_rn(w.m, __fmul_rn(L, temp));
+  w.key_m = key_of_f(w.m);
+  const uint32_t kl = key_of_f(zlo);
+  w.key_lo = kl > 0u ? kl - 1u : 0u;
+  w.ck_m = ckey(w.key_m);
+  const uint32_t ck_lo = ckey(w.key_lo);
+  w.dmax = w.ck_m - ck_lo;
+  w.fits = isfinite(w.m) && isfinite(w.zf) && isfinite(st.u) && w.zf >= 1.f &&
+           w.key_lo <= w.key_m && w.dmax < (uint32_t)HBW;
+  return w;
+}
+
+// One CTA per (row, shard): the shard's window counts.
+__global__ void __launch_bounds__(NTP) shard_window_kernel(ShardWindowArgs a, float c) {
+  __shared__ uint32_t hist[HBW];
+  __shared__ Window win;
+  __shared__ float red_hi[NWP], red_lo[NWP], red_u[NWP];
+  __shared__ uint32_t red_n[NWP], red_t[NWP];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t n_pairs = a.T * (int64_t)a.n_shards;
+  for (int64_t pr = blockIdx.x; pr < n_pairs; pr += gridDim.x) {
+    const int64_t r = pr / a.n_shards;
+    const int s = (int)(pr % a.n_shards);
+    if (tid == 0)
+      win = row_window(reinterpret_cast<const float4*>(a.all_partials), a.n_all, a.T, r, a.V, c,
+                       a.temperature, a.top_p);
+    __syncthreads();
+    const Window w = win;
+    ShardCounts* out = reinterpret_cast<ShardCounts*>(a.counts) + ((int64_t)s * a.T + r);
+    const int64_t y = a.ids[r];
+    if (!w.fits || y < 0 || y >= a.V) {   // nothing to count (the combine reports the row)
+      if (tid == 0) {
+        out->ties = 0u;
+        out->merged_n = 0u;
+        out->merged_hi = out->merged_lo = out->merged_u = 0.f;
+        out->over = 0u;
+      }
+      __syncthreads();
+      continue;
+    }
+    for (uint32_t d = tid; d <= w.dmax; d += NTP) hist[d] = 0u;
+    __syncthreads();
+    const uint32_t fb = okey16_inverse(w.key_lo);
+    const __nv_bfloat162 f2 = bf2(fb | (fb << 16));
+    // y's logit, from the shard that holds it (every shard's partial is here)
+    const int ys = (int)(y / a.shard_width);
+    const float zy = ys < a.n_all ? reinterpret_cast<const float4*>(a.all_partials)[2 * ((int64_t)ys * a.T + r) + 1].x
+                                  : NAN;
+    const uint32_t key_y = isfinite(zy) ? key_of_f(zy) : 0xFFFFFFFFu;
+    const int64_t g0 = a.first_col + (int64_t)s * a.shard_width;   // global columns [g0, g1)
+    const int64_t l0 = (int64_t)s * a.shard_width;
+    int64_t l1 = l0 + a.shard_width;
+    if (g0 + a.shard_width > a.V) l1 = a.V - a.first_col;
+    if (l1 < l0) l1 = l0;
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(a.logits) + r * a.ld;
+    DF mz{0.f, 0.f};
+    float mu = 0.f;
+    uint32_t mn = 0u, tie = 0u;
+    auto take = [&](uint32_t bits, int64_t col) {   // one logit in the window
+      const uint32_t k = okey16(bits);
+      const uint32_t ck = ckey(k);
+      if (ck == MERGE_LO) {
+        const float d = __fmaf_rn(bf16_lo(bits), c, -w.E);
+        const float e = ex2(d);
+        mz = df_add_f(mz, e);
+        mu = __fmaf_rn(e, d, mu);
+        ++mn;
+      } else {
+        atomicAdd(&hist[w.ck_m - ck], 1u);
+      }
+      tie += (k == key_y && a.first_col + col < y) ? 1u : 0u;
+    };
+    const bool vec = ((reinterpret_cast<uintptr_t>(p + l0)) & 15u) == 0;
+    int64_t j = l0 + (int64_t)tid * 8;
+    if (vec) {
+      for (; j + 8 <= l1; j += (int64_t)NTP * 8) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(p + j));
+        const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t mk = __hge2_mask(bf2(v[i]), f2);
+          if (mk & 0xFFFFu) take(v[i] & 0xFFFFu, j + 2 * i);
+          if (mk >> 16) take(v[i] >> 16, j + 2 * i + 1);
+        }
+      }
+    }
+    for (; j < l1; j += (int64_t)NTP * 8) {
+      for (int i = 0; i < 8 && j + i < l1; ++i) {
+        const uint32_t bits = __ldg(p + j + i);
+        if (bf16_lo(bits) >= bf16_lo(fb)) take(bits, j + i);
+      }
+    }
+    // fixed-order reductions: lanes along a shuffle tree, then the warps in order
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const DF x{shfl_down(mz.hi, o), shfl_down(mz.lo, o)};
+      mz = df_add(mz, x);
+      mu = __fadd_rn(mu, shfl_down(mu, o));
+      mn += __shfl_down_sync(0xFFFFFFFFu, mn, o);
+      tie += __shfl_down_sync(0xFFFFFFFFu, tie, o);
+    }
+    if (lane == 0) {
+      red_hi[warp] = mz.hi;
+      red_lo[warp] = mz.lo;
+      red_u[warp] = mu;
+      red_n[warp] = mn;
+      red_t[warp] = tie;
+    }
+    __syncthreads();
+    uint32_t over = 0u;
+    for (uint32_t d = tid; d <= w.dmax; d += NTP) {
+      const uint32_t n = hist[d];
+      over |= n > 0xFFFFu ? 1u : 0u;
+      out->cnt[d] = (uint16_t)(n > 0xFFFFu ? 0xFFFFu : n);
+    }
+    over = __syncthreads_or(over);
+    if (tid == 0) {
+      DF z{0.f, 0.f};
+      float u = 0.f;
+      uint32_t n = 0u, t = 0u;
+      for (int k = 0; k < NWP; ++k) {
+        z = df_add(z, DF{red_hi[k], red_lo[k]});
+        u = __fadd_rn(u, red_u[k]);
+        n += red_n[k];
+        t += red_t[k];
+      }
+      out->ties = t;
+      out->merged_n = n;
+      out->merged_hi = z.hi;
+      out->merged_lo = z.lo;
+      out->merged_u = u;
+      out->over = over;
+    }
+    __syncthreads();
+  }
+}
+
+// One warp per row: the shards' counts added up, then the fixed-order scan.
+__global__ void __launch_bounds__(NTP) shard_combine_topp_kernel(ShardCombineArgs a, float c) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t r = (int64_t)blockIdx.x * NWP + warp;
+  if (r >= a.T) return;
+  const float4* P = reinterpret_cast<const float4*>(a.partials);
+  const ShardCounts* C = reinterpret_cast<const ShardCounts*>(a.counts);
+  const int64_t y = a.ids[r];
+  auto finish_bad = [&](uint32_t bit) {
+    if (lane == 0) {
+      a.out_logprob[r] = NAN;
+      a.out_entropy[r] = NAN;
+      if (a.out_k) a.out_k[r] = 0;
+      if (a.status) atomicOr(a.status, bit);
+    }
+  };
+  if (y < 0 || y >= a.V) return finish_bad(RLK_STATUS_BAD_TOKEN_ID);
+  const Window w = row_window(P, a.n_shards, a.T, r, a.V, c, a.temperature, a.top_p);
+  const int ys = (int)(y / a.shard_width);
+  const float4 py = ys < a.n_shards ? P[2 * ((int64_t)ys * a.T + r) + 1] : make_float4(NAN, 0.f, 0.f, 0.f);
+  const float zy = py.x;
+  if (!(isfinite(w.m) && isfinite(w.zf) && isfinite(zy))) return finish_bad(RLK_STATUS_NONFINITE);
+  {
+    bool fin = true;   // a non-finite logit in any shard leaves NaN in its partial
+    for (int s = 0; s < a.n_shards; ++s) fin = fin && !isnan(P[2 * ((int64_t)s * a.T + r)].w);
+    if (!fin) return finish_bad(RLK_STATUS_NONFINITE);
+  }
+  if (!w.fits) return finish_bad(RLK_STATUS_UNRESOLVED);
+  uint32_t ties = 0u, over = 0u, mn = 0u;
+  DF mz{0.f, 0.f};
+  float mu = 0.f;
+  for (int s = 0; s < a.n_shards; ++s) {
+    const ShardCounts& q = C[(int64_t)s * a.T + r];
+    ties += q.ties;
+    over |= q.over;
+    mn += q.merged_n;
+    mz = df_add(mz, DF{q.merged_hi, q.merged_lo});
+    mu = __fadd_rn(mu, q.merged_u);
+  }
+  if (over) return finish_bad(RLK_STATUS_UNRESOLVED);
+  const uint32_t key_y = key_of_f(zy);
+  const uint32_t d_merged = w.ck_m >= MERGE_LO ? w.ck_m - MERGE_LO : 0xFFFFFFFFu;
+  const uint32_t dmax = w.dmax;
+  const DF target = df_mul_f(w.Z, a.top_p);
+  // Bin d: the tokens of compressed key ck_m - d (d_merged: the near-zero bin).
+  auto bin = [&](uint32_t d, uint32_t& nb, DF& mass, float& um, float& wv, float& dv) {
+    nb = 0u; mass = DF{0.f, 0.f}; um = 0.f; wv = 0.f; dv = 0.f;
+    if (d > dmax) return;
+    if (d == d_merged) {
+      nb = mn; mass = mz; um = mu;
+      return;
+    }
+    for (int s = 0; s < a.n_shards; ++s) nb += C[(int64_t)s * a.T + r].cnt[d];
+    if (nb == 0u) return;
+    dv = __fmaf_rn(bf16_val(okey16_inverse(ckey_expand(w.ck_m - d))), c, -w.E);
+    wv = ex2(dv);
+    const float ms = __fmul_rn((float)nb, wv);
+    mass = DF{ms, 0.f};
+    um = __fmul_rn(ms, dv);
+  };
+  const uint32_t bpl = (dmax + 32u) / 32u;
+  const uint32_t d0 = (uint32_t)lane * bpl;
+  DF tot{0.f, 0.f};
+  uint32_t tcnt = 0u;
+  float tum = 0.f;
+  for (uint32_t j = 0; j < bpl; ++j) {
+    uint32_t nb; DF ms; float um, wv, dv;
+    bin(d0 + j, nb, ms, um, wv, dv);
+    tot = df_add(tot, ms);
+    tcnt += nb;
+    tum = __fadd_rn(tum, um);
+  }
+  DF inc = tot;
+  uint32_t icnt = tcnt;
+  float ium = tum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF lft{shfl_up(inc.hi, o), shfl_up(inc.lo, o)};
+    const uint32_t lc = __shfl_up_sync(0xFFFFFFFFu, icnt, o);
+    const float lu = shfl_up(ium, o);
+    if (lane >= o) {
+      inc = df_add(lft, inc);
+      icnt += lc;
+      ium = __fadd_rn(lu, ium);
+    }
+  }
+  DF P0{shfl_up(inc.hi, 1), shfl_up(inc.lo, 1)};
+  uint32_t pc = __shfl_up_sync(0xFFFFFFFFu, icnt, 1);
+  float pu = shfl_up(ium, 1);
+  if (lane == 0) { P0 = DF{0.f, 0.f}; pc = 0u; pu = 0.f; }
+  int my_d = -1;
+  DF pb{0.f, 0.f};
+  uint32_t cb = 0u, nt = 0u;
+  float ub = 0.f, wt = 0.f, dt = 0.f;
+  for (uint32_t j = 0; j < bpl; ++j) {
+    uint32_t nb; DF ms; float um, wv, dv;
+    bin(d0 + j, nb, ms, um, wv, dv);
+    const DF Pn = df_add(P0, ms);
+    if (nb > 0u && df_ge(Pn, target)) {
+      my_d = (int)(d0 + j);
+      pb = P0; cb = pc; ub = pu; wt = wv; dt = dv; nt = nb;
+      break;
+    }
+    P0 = Pn;
+    pc += nb;
+    pu = __fadd_rn(pu, um);
+  }
+  const uint32_t bal = __ballot_sync(0xFFFFFFFFu, my_d >= 0);
+  if (bal == 0u) return finish_bad(RLK_STATUS_UNRESOLVED);   // (the window holds the crossing)
+  const int win_lane = __ffs(bal) - 1;
+  const int cross = __shfl_sync(0xFFFFFFFFu, my_d, win_lane);
+  // A crossing inside the near-zero bin would need its values' order.
+  if ((uint32_t)cross == d_merged) return finish_bad(RLK_STATUS_UNRESOLVED);
+  if (lane == win_lane) {
+    const float need = df_sub_to_f(target, pb);
+    const float cf = ceilf(__fdiv_rn(need, wt));
+    const uint32_t cneed = cf < 1.f ? 1u : (cf > (float)nt ? nt : (uint32_t)cf);
+    const float wn = __fmul_rn((float)cneed, wt);
+    const DF zs = df_add_f(pb, wn);
+    const float us = __fmaf_rn(wn, dt, ub);
+    const uint32_t ck_y = ckey(key_y);
+    const uint32_t d_y = w.ck_m - ck_y;
+    const bool y_in = (d_y < (uint32_t)my_d) || (d_y == (uint32_t)my_d && ties < cneed);
+    const float zsf = __fadd_rn(zs.hi, zs.lo);
+    const float lz = logf(zsf);
+    a.out_logprob[r] = y_in ? __fsub_rn(__fmul_rn(kLn2, __fmaf_rn(zy, c, -w.E)), lz) : -INFINITY;
+    a.out_entropy[r] = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, us), zsf));
+    if (a.out_k) a.out_k[r] = (int32_t)(cb + cneed);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_shard_partials(const ShardArgs& a, cudaStream_t stream) {
@@ -348,6 +681,20 @@ cudaError_t launch_shard_support_partials(const ShardArgs& a, cudaStream_t strea
   const int64_t blocks = (n_pairs + NWP - 1) / NWP;
   const int64_t cap = (int64_t)8 * sm_count();
   shard_support_partial_kernel<<<(unsigned)(blocks < cap ? blocks : cap), NTP, 0, stream>>>(a, c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_window(const ShardWindowArgs& a, cudaStream_t stream) {
+  const float c = (float)(1.4426950408889634 / (double)a.temperature);
+  const int64_t n_pairs = a.T * (int64_t)a.n_shards;
+  const int64_t cap = (int64_t)16 * sm_count();
+  shard_window_kernel<<<(unsigned)(n_pairs < cap ? n_pairs : cap), NTP, 0, stream>>>(a, c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_combine_topp(const ShardCombineArgs& a, cudaStream_t stream) {
+  const float c = (float)(1.4426950408889634 / (double)a.temperature);
+  shard_combine_topp_kernel<<<(unsigned)((a.T + NWP - 1) / NWP), NTP, 0, stream>>>(a, c);
   return cudaGetLastError();
 }
 

@@ -85,7 +85,8 @@ typedef enum {
 
 /* Operation ids for rlk_workspace_size. */
 enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2,
-       RLK_OP_LMHEAD_BWD = 3, RLK_OP_LMHEAD_TOPP = 4, RLK_OP_CANONICAL = 5 };
+       RLK_OP_LMHEAD_BWD = 3, RLK_OP_LMHEAD_TOPP = 4, RLK_OP_CANONICAL = 5,
+       RLK_OP_CANONICAL_TOPP = 6 };
 
 /* Bits OR-ed into *out_status_word by the kernels. */
 #define RLK_STATUS_BAD_TOKEN_ID 0x1u   /* a token id outside [0, V)          */
@@ -99,6 +100,12 @@ enum { RLK_OP_LOGPROB_ENTROPY = 0, RLK_OP_GRPO_LOSS = 1, RLK_OP_LMHEAD = 2,
                                           offsets decrease                      */
 #define RLK_STATUS_NO_STATE     0x10u  /* a row state that no forward wrote
                                           (rlk_logprob_entropy_bwd)           */
+#define RLK_STATUS_UNRESOLVED   0x40u  /* rlk_shard_combine_topp: a row whose
+                                          window spans more than 4096 values,
+                                          whose nucleus boundary falls among the
+                                          logits with |z| < 2^-12, or with more
+                                          than 65535 equal logits in one shard's
+                                          window (NaN outputs)                 */
 #define RLK_STATUS_BAD_PARAM    0x20u  /* a per-row temperature that is not
                                           finite and > 0, or a per-row top_p
                                           outside (0, 1]                      */
@@ -141,6 +148,7 @@ const char* rlk_status_string(rlk_status status);
  *  RLK_OP_LMHEAD_BWD:      the same (rlk_lmhead_logprob_bwd)
  *  RLK_OP_LMHEAD_TOPP:     the same (rlk_lmhead_logprob with top_p < 1)
  *  RLK_OP_CANONICAL:       T rows, V = the number of virtual shards, H unused
+ *  RLK_OP_CANONICAL_TOPP:  the same (rlk_logprob_entropy_canonical_topp)
  * Returns 0 for an unknown op or negative sizes. */
 size_t rlk_workspace_size(int op, int64_t T, int64_t V, int64_t H);
 
@@ -710,6 +718,87 @@ rlk_status rlk_logprob_entropy_canonical(const void* logits, rlk_dtype dtype, in
                                          float* out_logprob, float* out_entropy,
                                          uint32_t* out_status_word, void* workspace,
                                          size_t workspace_bytes, rlk_stream stream);
+
+/*
+ * The canonical partition at top_p < 1, no retained set supplied.
+ *
+ * The retained set depends on the whole row, so the ranks exchange twice.
+ * (1) rlk_shard_partials on every rank, gathered in rank order: every rank
+ * now holds all shards' partials, hence the row's max m and Z.  (2)
+ * rlk_shard_window_counts: from those every shard derives the same window
+ * z >= m - L T, L = ln(V / ((1 - top_p) Z)) + 0.5 (Z relative to the max's
+ * weight) -- below it lies less than V e^-L < (1 - top_p) Z of the mass, so
+ * the nucleus boundary lies inside -- and counts its logits in the window per
+ * bf16 value (all logits of one value carry the same mass; the values with
+ * |z| < 2^-12 share one bin whose mass the shard sums in a fixed order),
+ * gathered in rank order too.  (3) rlk_shard_combine_topp adds the counts
+ * (integers: exact in any order), scans the bins largest value first with a
+ * fixed-order double-float prefix to the bin where the retained mass reaches
+ * top_p Z (tied logits kept lower id first, as rlk_logprob_entropy) and
+ * writes the log-probability of the selected token under the renormalised
+ * retained distribution (-inf when it is not retained) and the retained set's
+ * entropy.  The result is bitwise the same for any number of ranks, and within
+ * the parity tolerance of rlk_logprob_entropy.  bf16 logits only.
+ */
+
+/* One row's window counts of one shard.  Opaque, 8224 bytes. */
+typedef struct rlk_shard_counts {
+  uint32_t opaque[2056];
+} rlk_shard_counts;
+
+/*
+ * rlk_shard_window_counts -- step (2) above for this rank's n_shards shards.
+ *
+ *  logits          device bf16, the columns of this rank's shards (as
+ *                  rlk_shard_partials).
+ *  T, V, ld, first_col, shard_width, n_shards, token_ids, temperature
+ *                  as rlk_shard_partials.
+ *  top_p           in (0, 1).
+ *  all_partials    device rlk_shard_partial[n_all][T]: every shard's partial,
+ *                  shard 0 first (rlk_shard_partials of all ranks gathered in
+ *                  rank order), 16-byte aligned.
+ *  out_counts      device rlk_shard_counts[n_shards][T] (shard-major),
+ *                  16-byte aligned.
+ * Errors: as rlk_shard_partials, RLK_ERR_UNSUPPORTED for fp32 logits,
+ *  RLK_ERR_INVALID_ARG for top_p outside (0, 1) or n_all < first_col / W +
+ *  n_shards.  Rows with a bad id or a non-finite logit are left to the
+ *  combine, which reports them.
+ */
+rlk_status rlk_shard_window_counts(const void* logits, rlk_dtype dtype, int64_t T, int64_t V,
+                                   int64_t ld, int64_t first_col, int64_t shard_width,
+                                   int32_t n_shards, const int32_t* token_ids, float temperature,
+                                   float top_p, const rlk_shard_partial* all_partials,
+                                   int32_t n_all, rlk_shard_counts* out_counts, rlk_stream stream);
+
+/*
+ * rlk_shard_combine_topp -- step (3): log-probability, entropy and nucleus
+ * size from all shards' partials and window counts (both [n_shards][T], shard
+ * 0 first).
+ *
+ *  out_k           device int32[T] or NULL: the retained set's size.
+ * Data errors: NaN outputs (k = 0) with RLK_STATUS_BAD_TOKEN_ID,
+ *  RLK_STATUS_NONFINITE or RLK_STATUS_UNRESOLVED in the status word.
+ * Errors: as rlk_shard_combine, RLK_ERR_INVALID_ARG for top_p outside (0, 1).
+ */
+rlk_status rlk_shard_combine_topp(const rlk_shard_partial* partials, const rlk_shard_counts* counts,
+                                  int32_t n_shards, int64_t T, int64_t V, int64_t shard_width,
+                                  const int32_t* token_ids, float temperature, float top_p,
+                                  float* out_logprob, float* out_entropy, int32_t* out_k,
+                                  uint32_t* out_status_word, rlk_stream stream);
+
+/*
+ * rlk_logprob_entropy_canonical_topp -- the three steps on one device (all
+ * n_virtual shards): partials and counts go to the workspace,
+ * rlk_workspace_size(RLK_OP_CANONICAL_TOPP, T, n_virtual, 0) bytes, 16-byte
+ * aligned (8256 bytes per row and shard).
+ */
+rlk_status rlk_logprob_entropy_canonical_topp(const void* logits, rlk_dtype dtype, int64_t T,
+                                              int64_t V, int64_t ld, const int32_t* token_ids,
+                                              float temperature, float top_p, int32_t n_virtual,
+                                              int64_t padded_vocab, float* out_logprob,
+                                              float* out_entropy, int32_t* out_k,
+                                              uint32_t* out_status_word, void* workspace,
+                                              size_t workspace_bytes, rlk_stream stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

@@ -301,6 +301,33 @@ def test_canonical_rejects(lib):
     assert canon(P=999) == 1 and canon(P=1001) == 1 and canon(n=0) == 1
     assert canon(ws=None) == 3 and canon(wsb=16) == 3
     assert lib.rlk_workspace_size(5, 100, 8, 0) == 100 * 8 * 32
+    assert lib.rlk_workspace_size(6, 100, 8, 0) == 100 * 8 * (32 + 8224)
+    def win(**kw):
+        a = dict(dtype=0, T=4, V=1000, ld=1000, first=0, W=125, n=8, temp=0.7, p=0.9, nall=8,
+                 allp=FAKE, out=FAKE)
+        a.update(kw)
+        return lib.rlk_shard_window_counts(FAKE, a["dtype"], a["T"], a["V"], a["ld"], a["first"],
+                                           a["W"], a["n"], FAKE, a["temp"], a["p"], a["allp"],
+                                           a["nall"], a["out"], None)
+    for kw in (dict(p=1.0), dict(p=0.0), dict(nall=7), dict(W=0), dict(first=100), dict(ld=999),
+               dict(allp=None), dict(out=ctypes.c_void_p(0x10008)), dict(temp=-1.0)):
+        assert win(**kw) == 1, kw
+    assert win(dtype=1) == 2                    # fp32 logits: no per-value counts
+    assert win(T=0, out=None) == 0
+    def ctp(**kw):
+        a = dict(n=8, T=4, V=1000, W=125, p=0.9, cnt=FAKE)
+        a.update(kw)
+        return lib.rlk_shard_combine_topp(FAKE, a["cnt"], a["n"], a["T"], a["V"], a["W"], FAKE,
+                                          0.7, a["p"], FAKE, FAKE, None, None, None)
+    assert ctp(W=124) == 1 and ctp(p=1.0) == 1 and ctp(cnt=None) == 1
+    def ctopp(**kw):
+        a = dict(n=8, P=1000, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return lib.rlk_logprob_entropy_canonical_topp(FAKE, 0, 4, 1000, 1000, FAKE, 0.7, 0.9,
+                                                      a["n"], a["P"], FAKE, FAKE, None, None,
+                                                      a["ws"], a["wsb"], None)
+    assert ctopp(P=999) == 1 and ctopp(n=0) == 1
+    assert ctopp(ws=None) == 3 and ctopp(wsb=4 * 8 * (32 + 8224) - 1) == 3
 
 
 def test_injected_launch_failures_come_before_any_launch(lib):

@@ -147,3 +147,115 @@ def test_supplied_support_under_the_partition(cuda_lib, oracle):
     torch.cuda.synchronize()
     assert torch.isnan(lp2).cpu().tolist() == [False, True, True]
     assert int(stw.item()) == cuda_lib.STATUS_BAD_SUPPORT
+
+
+# ----------------------------------------------------------- top_p < 1
+# Two exchanges: every shard's partial reaches every rank, which sets the
+# row's window; each shard then counts its logits in the window per bf16 value
+# and the counts are combined in shard order (RL-Kernel "Qwen3-8B VIME
+# train-rollout consistency", section "Canonical topology strategy").
+
+def _emulate_ranks(cuda_lib, z, ids, T_, p, tp):
+    """tp ranks, each holding only its own columns: partials, the all-gather
+    (a concatenation in rank order), window counts, the second all-gather, and
+    the combine."""
+    V = z.shape[1]
+    plans = [cuda_lib.canonical_plan(tp, rank) for rank in range(tp)]
+    local = [z[:, c0:min(c0 + n * w, V)] for _, n, c0, w in plans]
+    parts = [cuda_lib.shard_partials(loc, ids, T_, V, c0, w, n)
+             for loc, (_, n, c0, w) in zip(local, plans)]
+    allp = torch.cat(parts, 0)
+    cnts = [cuda_lib.shard_window_counts(loc, ids, T_, p, V, c0, w, n, allp)
+            for loc, (_, n, c0, w) in zip(local, plans)]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = cuda_lib.shard_combine_topp(allp, torch.cat(cnts, 0), ids, T_, p, V, plans[0][3],
+                                      status_word=st)
+    torch.cuda.synchronize()
+    return out, int(st.item())
+
+
+@pytest.mark.parametrize("T_,p", [(0.7, 0.95), (0.7, 0.5), (1.8, 0.9)])
+def test_canonical_topp_matches_oracle(cuda_lib, oracle, T_, p):
+    from _parity import compare_rows
+    R, V = 48, workloads.VOCAB
+    z, _ = workloads.peaked_bf16(R, V=V, seed=41, device="cuda")
+    hz = workloads.bf16_bits(z)
+    ids = torch.from_numpy(oracle.sample_ids(hz, T_, p, workloads.uniforms(R, 9))).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lp, ent, k = cuda_lib.logprob_entropy_canonical_topp(z, ids, T_, p, status_word=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    compare_rows(oracle, hz, ids.cpu().numpy(), T_, p, lp.cpu().numpy(), ent.cpu().numpy(),
+                 k.cpu().numpy(), label=f"canonical top-p T{T_} p{p}")
+    # ids mostly outside the nucleus: -inf log-probabilities, same sizes
+    far = ((ids.long() + V // 2) % V).to(torch.int32)
+    lp2, ent2, k2 = cuda_lib.logprob_entropy_canonical_topp(z, far, T_, p)
+    torch.cuda.synchronize()
+    compare_rows(oracle, hz, far.cpu().numpy(), T_, p, lp2.cpu().numpy(), ent2.cpu().numpy(),
+                 k2.cpu().numpy(), label=f"canonical top-p far T{T_} p{p}")
+
+
+def test_canonical_topp_bits_for_every_degree(cuda_lib, oracle):
+    R, V = 40, workloads.VOCAB
+    z, _ = workloads.peaked_bf16(R, V=V, seed=43, device="cuda")
+    hz = workloads.bf16_bits(z)
+    ids = torch.from_numpy(oracle.sample_ids(hz, 0.7, 0.95, workloads.uniforms(R, 11))).cuda()
+    ref = cuda_lib.logprob_entropy_canonical_topp(z, ids, 0.7, 0.95)
+    torch.cuda.synchronize()
+    for tp in (1, 2, 4, 8):
+        (lp, ent, k), st = _emulate_ranks(cuda_lib, z, ids, 0.7, 0.95, tp)
+        assert st == 0
+        assert torch.equal(lp, ref[0]) and torch.equal(ent, ref[1]) and torch.equal(k, ref[2]), tp
+
+
+def test_canonical_topp_special_rows(cuda_lib, oracle):
+    """Windows that cross zero (the near-zero bin inside the window), flat
+    rows, wide tie groups, Zipf rows, and rows the path cannot resolve or must
+    refuse."""
+    from _parity import compare_rows
+    V = workloads.VOCAB
+    z, _ = workloads.peaked_bf16(12, V=V, seed=45)
+    z = z.float()
+    g = torch.Generator().manual_seed(45)
+    z[1] = torch.randn(V, generator=g) * 0.5              # flat, around zero
+    z[2] = torch.randn(V, generator=g) * 3 - 20.0         # all negative
+    z[3, :64] = z[3].max() + 0.5                           # a wide tie group at the top
+    zipf, _ = workloads.zipf_bf16(4, V=V, seed=46)
+    z[4:8] = zipf.float()
+    z[8] = 1.5                                             # all equal
+    z = z.to(torch.bfloat16).cuda()
+    hz = workloads.bf16_bits(z)
+    for T_, p in ((0.7, 0.95), (1.0, 0.9)):
+        ids_h = oracle.sample_ids(hz, T_, p, workloads.uniforms(12, 13))
+        ids = torch.from_numpy(ids_h).cuda()
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        lp, ent, k = cuda_lib.logprob_entropy_canonical_topp(z, ids, T_, p, status_word=st)
+        torch.cuda.synchronize()
+        lp, ent, k = lp.cpu().numpy(), ent.cpu().numpy(), k.cpu().numpy()
+        unresolved = np.isnan(lp)
+        # every row either matches the oracle or is reported unresolved
+        assert (int(st.item()) & ~cuda_lib.STATUS_UNRESOLVED) == 0
+        assert unresolved.sum() <= 2, f"rows left unresolved: {np.nonzero(unresolved)[0]}"
+        ok = ~unresolved
+        compare_rows(oracle, hz[ok], ids_h[ok], T_, p, lp[ok], ent[ok], k[ok],
+                     label=f"canonical special T{T_} p{p}")
+        for tp in (2, 8):
+            (lp2, ent2, k2), _ = _emulate_ranks(cuda_lib, z, ids, T_, p, tp)
+            assert np.array_equal(lp2.cpu().numpy().view(np.uint32), lp.view(np.uint32))
+            assert np.array_equal(ent2.cpu().numpy().view(np.uint32), ent.view(np.uint32))
+
+
+def test_canonical_topp_bad_rows(cuda_lib):
+    V = workloads.VOCAB
+    z, peaks = workloads.peaked_bf16(6, V=V, seed=47, device="cuda")
+    z[1, 5] = float("nan")
+    z[2, V - 1] = float("inf")
+    z[3, 400] = float("-inf")
+    ids = torch.tensor([int(peaks[0]), 1, 2, 3, V, -1], dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lp, ent, k = cuda_lib.logprob_entropy_canonical_topp(z, ids, 0.7, 0.9, status_word=st)
+    torch.cuda.synchronize()
+    lp, ent, k = lp.cpu().numpy(), ent.cpu().numpy(), k.cpu().numpy()
+    assert np.isfinite(lp[0]) and np.isfinite(ent[0]) and k[0] >= 1
+    assert np.all(np.isnan(lp[1:])) and np.all(np.isnan(ent[1:])) and np.all(k[1:] == 0)
+    assert int(st.item()) == (cuda_lib.STATUS_BAD_TOKEN_ID | cuda_lib.STATUS_NONFINITE)

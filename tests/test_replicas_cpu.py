@@ -91,15 +91,22 @@ def _gather_worker(rank, ws, port, q):
         # order can be read back
         local = torch.arange(s0, s0 + n, dtype=torch.float32).view(n, 1, 1).expand(n, T, 8)
         full = rlk.gather_shard_partials(local.contiguous())
-        q.put((rank, full[:, 0, 0].tolist(), tuple(full.shape)))
+        # the second exchange at top_p < 1: each shard's window counts (bytes)
+        cnt = torch.zeros((n, T, rlk.SHARD_COUNTS_BYTES), dtype=torch.uint8)
+        cnt[:, :, 0] = torch.arange(s0, s0 + n, dtype=torch.uint8).view(n, 1)
+        cnt[:, :, -1] = torch.arange(T, dtype=torch.uint8).view(1, T)
+        fullc = rlk.gather_shard_partials(cnt)
+        q.put((rank, full[:, 0, 0].tolist(), tuple(full.shape), fullc[:, 0, 0].tolist(),
+               fullc[:, :, -1].tolist(), tuple(fullc.shape)))
     finally:
         dist.destroy_process_group()
 
 
 @pytest.mark.parametrize("ws", [2, 4])
 def test_gather_shard_partials_in_canonical_order_over_gloo_ranks(ws):
-    """The vocabulary-parallel exchange: every rank ends with all eight shards'
-    partials in shard order, whatever rank computed them (TP 2 and TP 4)."""
+    """The vocabulary-parallel exchanges: every rank ends with all eight shards'
+    partials -- and, at top_p < 1, their window counts -- in shard order,
+    whatever rank computed them (TP 2 and TP 4)."""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
@@ -110,9 +117,11 @@ def test_gather_shard_partials_in_canonical_order_over_gloo_ranks(ws):
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    for _, order, shape in res:
+    for _, order, shape, corder, crow, cshape in res:
         assert order == [float(s) for s in range(8)]
         assert shape == (8, 5, 8)
+        assert corder == list(range(8)) and cshape == (8, 5, 8224)
+        assert crow == [list(range(5))] * 8                    # rows stay in place
 
 
 # ------------------------------------------------ the reference arm (the oracle on host cores)
