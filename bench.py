@@ -815,8 +815,8 @@ LMB_METRIC = ("tokens/s for the fused LM-head backward (dL/dhidden and dL/dW at 
 def run_lmhead_backward(args, ws, rank, dev, barrier):
     """--op lmhead_backward: rlk_lmhead_logprob_bwd on the LM-head benchmark
     shape (the forward, which saves each row's log-normaliser, runs once before
-    the timed region).  Three GEMMs of 2 T V H flops each: the recompute with
-    the gradient epilogue (tcgen05) and the two weight-side products."""
+    the timed region).  Three GEMMs of 2 T V H flops each, all tcgen05: the
+    recompute with the gradient epilogue and the two weight-side products."""
     import entropy_logits_bf16_gb300 as rlk
     import workloads
     stream = torch.cuda.current_stream(dev)
@@ -857,10 +857,9 @@ def run_lmhead_backward(args, ws, rank, dev, barrier):
                    "l2": "W (1.24 GB) and dW (2.49 GB) larger than L2; no flush between steps"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
-                     "kernel": "lmhead_kernel (gradient epilogue) + two cuBLASLt GEMMs per chunk",
+                     "kernel": "lmhead_kernel (gradient epilogue) + two gemm_kernel products per chunk",
                      "flops_per_launch": flops, "launch_ms": part_ms[0]},
-        "gpu_launches": n_chunks * args.steps,
-        "library_gemms_per_step": 2 * n_chunks,
+        "gpu_launches": 3 * n_chunks * args.steps,
         "clocks": clk,
     }
 

@@ -65,7 +65,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
     tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublasLt"], check=True)
+    subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
     os.replace(tmp, LIB)
     return LIB
 

@@ -37,7 +37,6 @@
 #include <atomic>
 #include <mutex>
 
-#include <cublasLt.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -523,6 +522,247 @@ __global__ void __launch_bounds__(256) lmhead_combine_kernel(LmParams p, float* 
   out_ent[row] = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, st.u), z));
 }
 
+// ------------------------------------------------------------ plain GEMM
+// D[M, N] (fp32, row-major, row stride ldd) = A[M, K] B[K, N] + beta D, with
+// bf16 operands brought in by TMA and the products on the tensor cores
+// (tcgen05, fp32 accumulators in TMEM), each tile's K in order (so the result
+// is deterministic).  A_MN: A is stored with M contiguous (a [K][M] array),
+// else with K contiguous ([M][K]); B_MN: B is stored with N contiguous
+// ([K][N]), else with K contiguous ([N][K]).  An MN-contiguous operand comes in
+// 64-element-wide TMA boxes of 64 K rows: 8-row groups of 128-byte swizzled
+// rows, 1024 bytes apart, and the 64-element blocks 8192 bytes apart.
+// Persistent: CTA b takes tiles b, b + grid, ...; warp 0 loads, one thread of
+// warp 1 issues the MMAs into one of two TMEM accumulators, warps 2-5 store.
+constexpr int GBM = 128, GBN = 256, GBK = 64, GSTAGES = 4;
+constexpr uint32_t GA_BYTES = GBM * GBK * 2;
+constexpr uint32_t GB_BYTES = GBN * GBK * 2;
+constexpr uint32_t GSTAGE_BYTES = GA_BYTES + GB_BYTES;
+constexpr uint32_t GMN_BLOCK = 64 * GBK * 2;   // one 64-element-wide MN block of a stage
+constexpr size_t GSMEM_BYTES = GSTAGES * GSTAGE_BYTES + 1024 + 256;
+
+struct GemmParams {
+  int64_t M, N, K;
+  int n_mt, n_nt, n_tiles, k_steps;
+  int m_fast;          // consecutive tiles walk M (else N): CTAs at work share the other operand in L2
+  float* D;
+  int64_t ldd;
+  float beta;
+  long long wait_limit;
+};
+
+// MN-contiguous operand: lbo = byte distance between 64-element blocks.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);   // start address
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;   // leading byte offset: next 64-element block
+  d |= (uint64_t)(1024u >> 4) << 32;         // stride byte offset: next 8-row group along K
+  d |= (uint64_t)1u << 46;                   // descriptor version
+  d |= (uint64_t)2u << 61;                   // 128-byte swizzle
+  return d;
+}
+
+template <bool A_MN, bool B_MN>
+constexpr uint32_t gemm_idesc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+         ((uint32_t)(GBN >> 3) << 17) | ((uint32_t)(GBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16_i(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void gemm_tile(const GemmParams& p, int t, int& mt, int& nt) {
+  if (p.m_fast) {
+    mt = t % p.n_mt;
+    nt = t / p.n_mt;
+  } else {
+    nt = t % p.n_nt;
+    mt = t / p.n_nt;
+  }
+}
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + GSTAGES * GSTAGE_BYTES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * GSTAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * GSTAGES + 5);
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * GSTAGES;
+  const uint32_t accf0 = empty0 + 8 * GSTAGES, acce0 = accf0 + 16;
+  const uint32_t drain_bar = smem_u32(bars + 2 * GSTAGES + 6);
+  constexpr uint32_t idesc = gemm_idesc<A_MN, B_MN>();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < GSTAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf0 + 8 * a, 1);
+      mbar_init(acce0 + 8 * a, 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0u, issued_parity = 0u;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+        int mt, nt;
+        gemm_tile(p, t, mt, nt);
+        for (int k = 0; k < p.k_steps; ++k) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.wait_limit)) { ok = false; break; }
+          if (*abort_flag) { ok = false; break; }
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_expect_tx(fb, GSTAGE_BYTES);
+          const uint32_t sa = base + stage * GSTAGE_BYTES, sb = sa + GA_BYTES;
+          if (A_MN) {
+#pragma unroll
+            for (int j = 0; j < GBM / 64; ++j) tma_load_2d(sa + j * GMN_BLOCK, &tmap_a, fb, mt * GBM + j * 64, k * GBK);
+          } else {
+            tma_load_2d(sa, &tmap_a, fb, k * GBK, mt * GBM);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < GBN / 64; ++j) tma_load_2d(sb + j * GMN_BLOCK, &tmap_b, fb, nt * GBN + j * 64, k * GBK);
+          } else {
+            tma_load_2d(sb, &tmap_b, fb, k * GBK, nt * GBN);
+          }
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == GSTAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok || *abort_flag) {   // let every issued copy land before the CTA exits
+        for (int s2 = 0; s2 < GSTAGES; ++s2) {
+          if (!(issued_mask & (1u << s2))) continue;
+          const uint32_t par = (issued_parity >> s2) & 1u;
+          for (uint32_t i = 0; i < SPIN_LIMIT; ++i)
+            if (mbar_try_wait(full0 + 8 * s2, par)) break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, tile = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++tile) {
+        const uint32_t acc = tile & 1u, accph = (tile >> 1) & 1u;
+        if (!mbar_wait(acce0 + 8 * acc, accph ^ 1u, abort_flag, p.wait_limit)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * GBN;
+        for (int k = 0; k < p.k_steps; ++k) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.wait_limit)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = base + stage * GSTAGE_BYTES, sb = sa + GA_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < GBK / 16; ++kk) {
+            // 16 K-elements: 32 bytes inside a K-contiguous row, 16 rows of an MN-contiguous block
+            const uint64_t da = A_MN ? smem_desc_mn_sw128(sa + kk * 2048, GMN_BLOCK)
+                                     : smem_desc_sw128(sa) + (uint64_t)(kk * 2);
+            const uint64_t db = B_MN ? smem_desc_mn_sw128(sb + kk * 2048, GMN_BLOCK)
+                                     : smem_desc_sw128(sb) + (uint64_t)(kk * 2);
+            mma_bf16_i(d_tmem, da, db, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(empty0 + 8 * stage);
+          if (++stage == GSTAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) mma_commit(accf0 + 8 * acc);
+      }
+      if (!ok) {
+        mma_commit(drain_bar);
+        for (uint32_t i = 0; i < SPIN_LIMIT; ++i)
+          if (mbar_try_wait(drain_bar, 0u)) break;
+      }
+    }
+  } else {
+    // ------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t tile = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++tile) {
+      int mt, nt;
+      gemm_tile(p, t, mt, nt);
+      const uint32_t acc = tile & 1u, accph = (tile >> 1) & 1u;
+      if (!mbar_wait(accf0 + 8 * acc, accph, abort_flag, p.wait_limit)) { ok = false; break; }
+      tc_fence_after();
+      const int64_t row = (int64_t)mt * GBM + q * 32 + lane;
+      float* drow = p.D + row * p.ldd;
+#pragma unroll 1
+      for (int ch = 0; ch < GBN / 32; ++ch) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + acc * GBN + ch * 32, v);
+        const int64_t col0 = (int64_t)nt * GBN + ch * 32;
+        if (row >= p.M || col0 >= p.N) continue;
+        const int n = (int)(p.N - col0 < 32 ? p.N - col0 : 32);
+        if (n == 32 && ((reinterpret_cast<uintptr_t>(drow + col0) & 15u) == 0)) {
+          float4* d4 = reinterpret_cast<float4*>(drow + col0);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+            if (p.beta != 0.f) {
+              const float4 old = d4[k];
+              o.x = __fmaf_rn(p.beta, old.x, o.x);
+              o.y = __fmaf_rn(p.beta, old.y, o.y);
+              o.z = __fmaf_rn(p.beta, old.z, o.z);
+              o.w = __fmaf_rn(p.beta, old.w, o.w);
+            }
+            d4[k] = o;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < n) drow[col0 + j] = p.beta != 0.f ? __fmaf_rn(p.beta, drow[col0 + j], v[j]) : v[j];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+    }
+    if (!ok && lane == 0) *abort_flag = 1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
 // ------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -554,6 +794,60 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, u
   return f(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A 2-D bf16 map over rows x cols (row stride ld elements) with a box of
+// box_inner columns by box_outer rows.
+bool make_map_box(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+                  uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return f(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// D = A B + beta D with the GEMM above.  A_MN / B_MN as there; a and b are
+// the stored arrays (a: [K][M] when A_MN else [M][K]; b: [K][N] when B_MN else
+// [N][K]), with row strides lda, ldb (elements, multiples of 8).
+template <bool A_MN, bool B_MN>
+cudaError_t gemm(const void* a, int64_t lda, const void* b, int64_t ldb, int64_t M, int64_t N,
+                 int64_t K, float* D, int64_t ldd, float beta, bool m_fast, cudaStream_t stream) {
+  static std::atomic<int> done[64];
+  const int ds = device_slot();
+  if (ds < 0 || !done[ds].load()) {
+    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<A_MN, B_MN>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)GSMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (ds >= 0) done[ds].store(1);
+  }
+  CUtensorMap ma, mb;
+  const bool oka = A_MN ? make_map_box(&ma, a, (uint64_t)K, (uint64_t)M, (uint64_t)lda, 64, GBK)
+                        : make_map_box(&ma, a, (uint64_t)M, (uint64_t)K, (uint64_t)lda, GBK, GBM);
+  const bool okb = B_MN ? make_map_box(&mb, b, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, 64, GBK)
+                        : make_map_box(&mb, b, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, GBK, GBN);
+  if (!oka || !okb) return cudaErrorInvalidValue;
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.n_mt = (int)((M + GBM - 1) / GBM);
+  p.n_nt = (int)((N + GBN - 1) / GBN);
+  p.n_tiles = p.n_mt * p.n_nt;
+  p.k_steps = (int)((K + GBK - 1) / GBK);
+  p.m_fast = m_fast ? 1 : 0;
+  p.D = D;
+  p.ldd = ldd;
+  p.beta = beta;
+  p.wait_limit = debug_wait_limit();
+  const int grid = p.n_tiles < sm_count() ? p.n_tiles : sm_count();
+  gemm_kernel<A_MN, B_MN><<<grid, THREADS, GSMEM_BYTES, stream>>>(ma, mb, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -612,12 +906,12 @@ cudaError_t launch_lmhead_impl(const LmheadArgs& a, float* debug_logits, cudaStr
 // the GEMM above (gradient epilogue) one chunk of rows at a time, so the
 // gradient logits exist for at most kBwdRows rows (the chunked-loss layout of
 // prime-rl v0.10.0 notes, "1. Trainer Performance").  The two weight-side
-// products are plain GEMMs with transposed operands: cuBLASLt, bf16 inputs,
-// fp32 accumulation and output, with the caller's workspace.
+// products are the tcgen05 GEMM above with MN-contiguous operands: bf16
+// inputs, fp32 accumulation and output, each tile's K and the chunks in a
+// fixed order.
 namespace {
 
 constexpr int64_t kBwdRows = 4096;
-constexpr size_t kLtWorkspace = (size_t)64 << 20;
 
 int64_t dz_ld(int64_t V) { return (V + 7) / 8 * 8; }   // 16-byte rows
 
@@ -626,67 +920,11 @@ size_t dz_bytes(int64_t T, int64_t V) {
   return ((size_t)rows * (size_t)dz_ld(V) * 2 + 255) & ~(size_t)255;
 }
 
-cublasLtHandle_t lt_handle() {
-  static cublasLtHandle_t h = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    if (cublasLtCreate(&h) != CUBLAS_STATUS_SUCCESS) h = nullptr;
-  });
-  return h;
-}
-
-// D[m, n] (column-major, ld ldd, fp32) = op(A) op(B) + beta D, A and B bf16
-// given by their stored column-major shapes.
-cudaError_t lt_gemm(cublasOperation_t opa, cublasOperation_t opb, int64_t m, int64_t n,
-                    int64_t k, const void* A, int64_t a_rows, int64_t a_cols, int64_t lda,
-                    const void* B, int64_t b_rows, int64_t b_cols, int64_t ldb, float* D,
-                    int64_t ldd, float beta, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)k;
-  cublasLtHandle_t h = lt_handle();
-  if (!h) return cudaErrorNotSupported;
-  cublasLtMatmulDesc_t op = nullptr;
-  cublasLtMatrixLayout_t la = nullptr, lb = nullptr, ld = nullptr;
-  cublasLtMatmulPreference_t pref = nullptr;
-  cudaError_t err = cudaErrorNotSupported;
-  cublasLtMatmulHeuristicResult_t res{};
-  int nres = 0;
-  const float alpha = 1.0f;
-  if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS) goto done;
-  if (cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &opa, sizeof(opa)) !=
-          CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &opb, sizeof(opb)) !=
-          CUBLAS_STATUS_SUCCESS)
-    goto done;
-  if (cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, a_rows, a_cols, lda) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, b_rows, b_cols, ldb) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatrixLayoutCreate(&ld, CUDA_R_32F, m, n, ldd) != CUBLAS_STATUS_SUCCESS)
-    goto done;
-  if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
-                                           &ws_bytes, sizeof(ws_bytes)) != CUBLAS_STATUS_SUCCESS)
-    goto done;
-  if (cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, ld, ld, pref, 1, &res, &nres) !=
-          CUBLAS_STATUS_SUCCESS ||
-      nres < 1)
-    goto done;
-  err = cublasLtMatmul(h, op, &alpha, A, la, B, lb, &beta, D, ld, D, ld, &res.algo, ws, ws_bytes,
-                       stream) == CUBLAS_STATUS_SUCCESS
-            ? cudaSuccess
-            : cudaErrorLaunchFailure;
-done:
-  if (pref) cublasLtMatmulPreferenceDestroy(pref);
-  if (ld) cublasLtMatrixLayoutDestroy(ld);
-  if (lb) cublasLtMatrixLayoutDestroy(lb);
-  if (la) cublasLtMatrixLayoutDestroy(la);
-  if (op) cublasLtMatmulDescDestroy(op);
-  return err;
-}
-
 }  // namespace
 
 size_t lmhead_bwd_workspace_bytes(int64_t T, int64_t V, int64_t H) {
   (void)H;
-  return dz_bytes(T, V) + kLtWorkspace;
+  return dz_bytes(T, V);
 }
 
 cudaError_t launch_lmhead_backward(const LmheadBwdArgs& a, cudaStream_t stream) {
@@ -695,7 +933,6 @@ cudaError_t launch_lmhead_backward(const LmheadBwdArgs& a, cudaStream_t stream) 
   if (!make_map(&mb, a.w_vocab, (uint64_t)a.V, (uint64_t)a.H, BN)) return cudaErrorInvalidValue;
   uint16_t* dz = static_cast<uint16_t*>(a.workspace);
   const int64_t ldz = dz_ld(a.V);
-  void* lt_ws = static_cast<char*>(a.workspace) + dz_bytes(a.T, a.V);
   const uint16_t* hid = static_cast<const uint16_t*>(a.hidden);
   for (int64_t r0 = 0; r0 < a.T; r0 += kBwdRows) {
     const int64_t rows = a.T - r0 < kBwdRows ? a.T - r0 : kBwdRows;
@@ -725,14 +962,17 @@ cudaError_t launch_lmhead_backward(const LmheadBwdArgs& a, cudaStream_t stream) 
     lmhead_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // dH[r0 : r0 + rows] = dZ W: column-major D[H, rows] = W^T[H, V] dZ^T[V, rows]
-    e = lt_gemm(CUBLAS_OP_N, CUBLAS_OP_N, a.H, rows, a.V, a.w_vocab, a.H, a.V, a.H, dz, a.V, rows,
-                ldz, a.grad_hidden + r0 * a.H, a.H, 0.0f, lt_ws, kLtWorkspace, stream);
+    // dH[r0 : r0 + rows] = dZ W: A = dZ [rows][V] (K contiguous), B = W [V][H]
+    // (N contiguous); consecutive tiles walk the rows, so the CTAs at work read
+    // the same columns of W
+    e = gemm<false, true>(dz, ldz, a.w_vocab, a.H, rows, a.H, a.V, a.grad_hidden + r0 * a.H, a.H,
+                          0.0f, true, stream);
     if (e != cudaSuccess) return e;
-    // dW (+)= dZ^T hidden: column-major D[H, V] = hidden^T[H, rows] dZ[rows, V]
+    // dW (+)= dZ^T hidden: A = dZ^T (M = V contiguous in dZ), B = hidden [rows][H]
+    // (N contiguous); consecutive tiles walk H, so the chunk's hidden stays in L2
     const float beta = (r0 > 0 || a.accumulate_w) ? 1.0f : 0.0f;
-    e = lt_gemm(CUBLAS_OP_N, CUBLAS_OP_T, a.H, a.V, rows, hid + r0 * a.H, a.H, rows, a.H, dz, a.V,
-                rows, ldz, a.grad_w, a.H, beta, lt_ws, kLtWorkspace, stream);
+    e = gemm<true, true>(dz, ldz, hid + r0 * a.H, a.H, a.V, a.H, rows, a.grad_w, a.H, beta, false,
+                         stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -273,7 +273,7 @@ def test_lmhead_fwd_bwd_reject(lib):
     assert bwd(ws=ctypes.c_void_p(0x10010)) == 3      # the workspace must be 256-byte aligned
     assert bwd(T=0, lse=None, ent=None, gh=None, gw=None, ws=None) == 0
     need = lib.rlk_workspace_size(3, 10000, 151936, 4096)
-    assert need >= 4096 * 151936 * 2 + (64 << 20)
+    assert need >= 4096 * 151936 * 2          # the gradient logits of one chunk of rows
 
 
 def test_canonical_rejects(lib):
