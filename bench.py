@@ -1099,9 +1099,14 @@ def main():
                          "gradient; backward: the dense top-p gradient; lmhead_backward: the "
                          "LM-head gradients")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lm-rows", type=int, default=None,
+                    help="rows of the LM-head workloads (default 16384; smaller for a profile)")
     ap.add_argument("--no-legs", action="store_true",
                     help="logits only: skip the long-response, packed GRPO and LM-head legs")
     args = ap.parse_args()
+    if args.lm_rows:
+        global LM_T
+        LM_T = int(args.lm_rows)
     if args.impl == "reference":
         run_reference(args)
         return
