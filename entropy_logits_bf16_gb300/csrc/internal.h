@@ -225,7 +225,6 @@ cudaError_t launch_lmhead(const LmheadArgs& a, cudaStream_t stream);
 size_t lmhead_bwd_workspace_bytes(int64_t T, int64_t V, int64_t H);
 size_t lmhead_topp_workspace_bytes(int64_t T, int64_t V, int64_t H);
 cudaError_t launch_lmhead_topp(const LmheadArgs& a, cudaStream_t stream);
-// Returns cudaErrorNotSupported when cuBLASLt finds no algorithm.
 cudaError_t launch_lmhead_backward(const LmheadBwdArgs& a, cudaStream_t stream);
 // Same, also writing the fp32 logits [T, V] to debug_logits (validation aid).
 cudaError_t launch_lmhead_impl(const LmheadArgs& a, float* debug_logits, cudaStream_t stream);

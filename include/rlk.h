@@ -560,9 +560,10 @@ rlk_status rlk_lmhead_logprob_fwd(const void* hidden, const void* w_vocab, int64
  * dz is recomputed by the same tensor-core GEMM as the forward, 4096 rows at a
  * time, rounded to bf16 and kept in the workspace (so the gradient logits of at
  * most 4096 rows exist at once: prime-rl v0.10.0 notes, "1. Trainer
- * Performance", the chunked loss); the two weight-side products are cuBLASLt
- * GEMMs (bf16 inputs, fp32 accumulation and outputs).  Deterministic for a
- * given T: grad_w sums the chunks in order.
+ * Performance", the chunked loss); the two weight-side products are tcgen05
+ * GEMMs of the library's own (bf16 inputs, fp32 accumulation and outputs, each
+ * tile's K in order).  Deterministic for a given T: grad_w sums the chunks in
+ * order.
  *
  * Arguments
  *  hidden, w_vocab, T, H, V, token_ids, temperature  the forward's.
@@ -572,12 +573,12 @@ rlk_status rlk_lmhead_logprob_fwd(const void* hidden, const void* w_vocab, int64
  *  grad_w          device float[V, H] row-major; overwritten, or added to when
  *                  accumulate_grad_w is non-zero.
  *  workspace       at least rlk_workspace_size(RLK_OP_LMHEAD_BWD, T, V, H)
- *                  bytes (4096 x V bf16 plus 64 MB), 16-byte aligned.
+ *                  bytes (the gradient logits of 4096 rows: 4096 x V bf16),
+ *                  16-byte aligned.
  * A row whose lse is NaN (a row the forward could not score) gives NaN in its
  * grad_hidden row and in all of grad_w.
  * Errors: as rlk_lmhead_logprob; RLK_ERR_INVALID_ARG for a NULL lse, entropy,
- *  grad_hidden or grad_w; RLK_ERR_UNSUPPORTED when cuBLASLt offers no
- *  algorithm.
+ *  grad_hidden or grad_w.
  */
 rlk_status rlk_lmhead_logprob_bwd(const void* hidden, const void* w_vocab, int64_t T, int64_t H,
                                   int64_t V, const int32_t* token_ids, float temperature,

@@ -1,6 +1,6 @@
 """CUDA-graph capture of the training-side chain: forward with row state,
 dense backward, sampler, the loss variants, and the LM-head forward and
-backward (whose weight-side products are cuBLASLt GEMMs).  After one eager
+backward (whose weight-side products are the library's tcgen05 GEMMs).  After one eager
 warm-up (lazy attribute and handle set-up happens there), a captured graph
 replays to the eager results bit for bit, and again after the inputs change
 in place: nothing in these calls synchronises, allocates on its own or
