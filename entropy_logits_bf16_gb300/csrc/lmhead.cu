@@ -230,6 +230,28 @@ struct LmParams {
   long long withhold;    // debug: the k-step copy the first CTA never issues (-1: none)
 };
 
+// Work unit u -> (row tile mt, vocabulary slice sl).  The slices go in blocks of
+// SLICE_BLOCK and, inside a block, the row tiles: the CTAs at work at any time
+// cover many row tiles of a few slices, so each W tile they read serves many
+// row tiles from L2 while their hidden tiles stay resident too.  The order only
+// changes which CTA runs a unit, never what it computes.
+constexpr int SLICE_BLOCK = 4;
+__device__ __forceinline__ void unit_coords(int u, int n_mt, int& mt, int& sl) {
+  const int full = n_mt * SLICE_BLOCK;                 // units of a whole block of slices
+  const int nfb = NSLICE / SLICE_BLOCK;                // whole blocks
+  const int b = u / full;
+  if (b < nfb) {
+    const int r = u - b * full;
+    mt = r / SLICE_BLOCK;
+    sl = b * SLICE_BLOCK + r % SLICE_BLOCK;
+  } else {                                             // the last, partial block
+    const int last = NSLICE - nfb * SLICE_BLOCK;
+    const int r = u - nfb * full;
+    mt = r / last;
+    sl = nfb * SLICE_BLOCK + r % last;
+  }
+}
+
 __device__ __forceinline__ void slice_bounds(int n_nt, int sl, int& nt0, int& nt1) {
   nt0 = (int)((int64_t)sl * n_nt / NSLICE);
   nt1 = (int)((int64_t)(sl + 1) * n_nt / NSLICE);
@@ -287,7 +309,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       long long n_issue = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-        const int mt = u / NSLICE, sl = u % NSLICE;
+        int mt, sl;
+        unit_coords(u, p.n_mt, mt, sl);
         int nt0, nt1;
         slice_bounds(p.n_nt, sl, nt0, nt1);
         for (int nt = nt0; nt < nt1 && ok; ++nt) {
@@ -328,7 +351,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t tile = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-        const int sl = u % NSLICE;
+        int mt_unused, sl;
+        unit_coords(u, p.n_mt, mt_unused, sl);
         int nt0, nt1;
         slice_bounds(p.n_nt, sl, nt0, nt1);
         for (int nt = nt0; nt < nt1 && ok; ++nt, ++tile) {
@@ -369,7 +393,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     int u_fail = p.n_units;
     for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
       u_fail = u;
-      const int mt = u / NSLICE, sl = u % NSLICE;
+      int mt, sl;
+      unit_coords(u, p.n_mt, mt, sl);
       int nt0, nt1;
       slice_bounds(p.n_nt, sl, nt0, nt1);
       const int64_t row = (int64_t)mt * BM + q * 32 + lane;
@@ -457,13 +482,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       // A wait ran out: every unit this CTA has not finished is marked, so
       // its rows come out NaN instead of normal-looking values.
       for (int u = u_fail; u < p.n_units; u += gridDim.x) {
-        const int64_t row = (int64_t)(u / NSLICE) * BM + q * 32 + lane;
+        int umt, usl;
+        unit_coords(u, p.n_mt, umt, usl);
+        const int64_t row = (int64_t)umt * BM + q * 32 + lane;
         if (row >= p.T) continue;
         if (!p.grad) {
-          p.part[(int64_t)(u % NSLICE) * p.T + row] = make_float4(0.f, kTimedOutSum, 0.f, 0.f);
+          p.part[(int64_t)usl * p.T + row] = make_float4(0.f, kTimedOutSum, 0.f, 0.f);
         } else {   // NaN logits or gradients: every result built on them is NaN
           int nt0, nt1;
-          slice_bounds(p.n_nt, u % NSLICE, nt0, nt1);
+          slice_bounds(p.n_nt, usl, nt0, nt1);
           const int64_t c1 = (int64_t)nt1 * BN < p.V ? (int64_t)nt1 * BN : p.V;
           for (int64_t col = (int64_t)nt0 * BN; col < c1; ++col) p.dz[row * p.ldz + col] = 0x7FC0u;
         }

@@ -82,9 +82,17 @@ def test_lmhead_withheld_copy_times_out_and_the_next_call_is_clean(cuda_lib):
         rlk.set_wait_limit(0)
     assert old > 2_000_000
     assert int(st.item()) & rlk.STATUS_TIMEOUT
+    n_mt = (T + BM - 1) // BM
+
+    def unit_tile(u, block=4):              # the kernel's unit order: slices in blocks of 4
+        full, nfb = n_mt * block, NSLICE // block
+        if u // full < nfb:
+            return (u % full) // block
+        return (u - nfb * full) // (NSLICE - nfb * block)
+
     bad = np.zeros(T, bool)
     for u in range(0, n_units, grid):       # the units of CTA 0, all unfinished
-        mt = u // NSLICE
+        mt = unit_tile(u)
         bad[mt * BM:(mt + 1) * BM] = True
     lp_h, ent_h = lp.cpu().numpy(), ent.cpu().numpy()
     assert np.all(np.isnan(lp_h[bad])) and np.all(np.isnan(ent_h[bad]))
