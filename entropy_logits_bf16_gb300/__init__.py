@@ -58,7 +58,8 @@ EXPORTS = ("rlk_version", "rlk_status_string", "rlk_workspace_size", "rlk_logpro
            "rlk_grpo_loss_noalloc")
 NOALLOC_MAX_SEQ = 16384
 DEBUG_EXPORTS = ("rlk_lmhead_logits_debug", "rlk_debug_inject_launch_failures",
-                 "rlk_debug_set_wait_limit", "rlk_debug_withhold_copy")
+                 "rlk_debug_set_wait_limit", "rlk_debug_withhold_copy",
+                 "rlk_debug_set_sampler_mode")
 STATUS_TIMEOUT = 0x4
 STATUS_BAD_SUPPORT = 0x8
 STATUS_NO_STATE = 0x10
@@ -133,6 +134,8 @@ def load(path: str | None = None):
         lib.rlk_debug_set_wait_limit.restype = ctypes.c_longlong
         lib.rlk_debug_withhold_copy.argtypes = [ctypes.c_longlong]
         lib.rlk_debug_withhold_copy.restype = ctypes.c_int
+        lib.rlk_debug_set_sampler_mode.argtypes = [ctypes.c_int]
+        lib.rlk_debug_set_sampler_mode.restype = ctypes.c_int
         lib.rlk_shard_partials.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, i64, i32, vp, f32,
                                            vp, vp]
         lib.rlk_shard_partials.restype = ctypes.c_int
@@ -836,3 +839,10 @@ def withhold_copy(stage: int) -> None:
     of the given stage in its first CTA, so the wait on it runs out; < 0
     clears it."""
     load().rlk_debug_withhold_copy(int(stage))
+
+
+def set_sampler_mode(mode: int) -> int:
+    """Debug: the ways rlk_sample_top_p may take to a draw: 1 the direct mode
+    with its member list (default), 2 the direct mode without the list, 0 the
+    radix descent only.  Returns the previous mode."""
+    return int(load().rlk_debug_set_sampler_mode(int(mode)))

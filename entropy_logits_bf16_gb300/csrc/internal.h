@@ -204,6 +204,7 @@ cudaError_t launch_lpe_stream(const LpeArgs& a, cudaStream_t stream, long long w
 // Debug settings of the bounded device waits (rlk_debug.h).
 long long debug_wait_limit();       // clock cycles (default about 2^31)
 long long debug_take_withheld();    // the stage to withhold in the next launch, or -1
+int debug_sampler_mode();           // 1 direct mode (default), 2 direct without its list, 0 radix only
 
 cudaError_t launch_support(const SupportArgs& a, cudaStream_t stream);
 cudaError_t launch_logprob_entropy_backward(const LpeBwdArgs& a, cudaStream_t stream);

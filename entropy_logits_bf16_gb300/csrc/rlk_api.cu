@@ -60,6 +60,9 @@ static std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
 static std::atomic<long long> g_withhold{-1};
 long long debug_wait_limit() { return g_wait_limit.load(); }
 long long debug_take_withheld() { return g_withhold.exchange(-1); }
+// rlk_debug_set_sampler_mode: the ways the sampler may take to a draw
+static std::atomic<int> g_sampler_mode{1};
+int debug_sampler_mode() { return g_sampler_mode.load(); }
 
 int grpo_loss_args(const float* logp_new, const float* logp_old, const float* logp_rollout,
                    const float* logp_ref, const uint8_t* loss_mask, const float* rewards,
@@ -111,6 +114,10 @@ long long rlk_debug_set_wait_limit(long long cycles) {
 int rlk_debug_withhold_copy(long long stage) {
   rlk::g_withhold.store(stage >= 0 ? stage : -1);
   return 0;
+}
+
+int rlk_debug_set_sampler_mode(int mode) {
+  return rlk::g_sampler_mode.exchange(mode == 0 || mode == 2 ? mode : 1);
 }
 
 const char* rlk_status_string(rlk_status status) {

@@ -8,15 +8,17 @@
 // sparse performance" notes: a deterministic top-p sampler).  u is supplied
 // per row; S is the one rlk_logprob_entropy_fwd selected (its row state).
 //
-// Instead of a sort and a prefix scan over the vocabulary, one CTA per row.
-// Direct mode, when the members' keys lie within NBD of the boundary key (the
-// top key is known to within a bf16 step from the saved E = fp32(m c)): one
-// pass counts members into bins by key - boundary with exact fixed-point
-// masses and the smallest id per bin; a block scan from the top finds the
-// draw's key; when the draw needs the first token of that key its id is the
-// bin's smallest, else a scan in id order finds it.  Otherwise (or when a
-// member lands above the estimate) a radix descent on the 16-bit
-// order-preserving key of the bf16 logits:
+// Instead of a sort and a prefix scan over the vocabulary, one CTA per row,
+// several rows in flight per SM, each thread keeping four 16-byte loads in
+// flight.  Direct mode, when the members' keys lie within NBD of the boundary
+// key (the top key is known to within a bf16 step from the saved E =
+// fp32(m c)): one read of the row counts members into bins by key - boundary
+// with exact fixed-point masses and lists each member's position; a block
+// scan from the top finds the draw's key, and the member list gives the
+// need-th lowest position holding it (a scan of the row in id order only when
+// the list ran out of room or the key's tie group is too large to rank).
+// Otherwise (or when a member lands above the estimate) a radix descent on the
+// 16-bit order-preserving key of the bf16 logits:
 //  1. members (key > boundary, or == boundary among the kept ties) counted
 //     into 256 bins by key >> 8, with masses w = 2^(z c - E) as fixed-point
 //     integers (w 2^40, truncated), so every sum is exact and order-free;
@@ -43,6 +45,10 @@ constexpr float kFix = 1099511627776.0f;   // 2^40
 constexpr int NBD = 2048;   // direct mode: members' keys within NBD of the boundary key
 // the direct-mode scan gives each thread exactly 8 consecutive bins
 static_assert(NBD == 8 * NTM, "direct-mode bins: 8 per thread");
+constexpr uint32_t LCAP = 4096;   // direct mode: members listed per row
+constexpr uint32_t GCAP = 1024;   // largest tie group ranked from the list
+constexpr int64_t kListMaxV = int64_t(1) << 21;   // a position and a bin in 32 bits
+constexpr int NLD = 4;            // 16-byte loads in flight per thread
 
 struct MSmem {
   union {
@@ -53,9 +59,12 @@ struct MSmem {
     struct {                        // direct mode: bin = key - boundary key
       unsigned long long dmass[NBD];
       uint32_t dcnt[NBD];
-      uint32_t dmin[NBD];           // the smallest id holding the bin's key
     };
+    uint32_t grp[GCAP];             // direct mode, after the scan: the draw's tie group
   };
+  uint32_t lst[LCAP];             // direct mode: members, position << 11 | bin
+  uint32_t lcnt;                  // members listed (may exceed LCAP)
+  uint32_t gn;                    // tie group gathered
   unsigned long long wsum[NWM];   // per-warp sums (direct-mode scan)
   uint32_t n_thr;                 // tokens holding the boundary key
   int ovf;                        // direct mode: a member above the estimated top key
@@ -129,7 +138,7 @@ __device__ void scan256(MSmem& sm, unsigned long long base, unsigned long long t
   }
 }
 
-__global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
+__global__ void __launch_bounds__(NTM, 5) sample_kernel(SampleArgs a, float c0, int mode) {
   __shared__ MSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ngroups = (a.V + 7) / 8;
@@ -152,74 +161,133 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
     const float E = st.E;
     float u = a.uniforms[r];
     u = u < 0.f ? 0.f : (u < 1.f ? u : 0.99999994f);
-    // the 16-bit key k of each element of group g, through f(k, z, index)
-    // (groups whose largest value is below `gate` hold no token the pass wants:
-    // one packed max skips them)
-    auto for_row = [&](float gate, auto&& f) {
-      for (int64_t g = tid; g < ngroups; g += NTM) {
-        uint32_t w4[4];
-        if (vec && g * 8 + 8 <= a.V) {
-          const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + g);
-          w4[0] = q.x; w4[1] = q.y; w4[2] = q.z; w4[3] = q.w;
-        } else {
+    // The elements of the row whose keys lie in [klo, khi], each through
+    // f(has, k, z, index), called by every lane of the warp together (has:
+    // this lane holds an element this round).  A thread takes groups g,
+    // g + NTM, ..., NLD of them per step, all loads issued before any is used;
+    // a group whose largest value is below the range is skipped after one
+    // packed max, the others are tested two elements at a time by packed bf16
+    // compares against the range's end values (-0 == +0, as the keys have
+    // it), and the elements found are handed out in rounds, one per lane and
+    // round, so a warp spends one pass of f per round rather than one per
+    // element of every passing group.
+    auto for_row = [&](uint32_t klo, uint32_t khi, auto&& f) {
+      // the range as values (keys below 0x7F are NaN, above 0xFF80 too; 0x7FFF
+      // is the key -0 would have without its mapping to +0)
+      const float lo_val = klo > 0x7Fu ? bf16_val(okey16_inverse(klo)) : -INFINITY;
+      const float hi_val = khi >= 0xFF80u ? INFINITY : bf16_val(okey16_inverse(khi == 0x7FFFu ? 0x7FFEu : khi));
+      const bool bounded = hi_val != INFINITY;
+      const __nv_bfloat162 lo2 = __float2bfloat162_rn(lo_val), hi2 = __float2bfloat162_rn(hi_val);
+      for (int64_t g0 = tid; g0 < ngroups; g0 += (int64_t)NLD * NTM) {
+        uint32_t w4[NLD][4];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int64_t i0 = g * 8 + 2 * h;
-            const uint32_t lo = i0 < a.V ? __ldg(p + i0) : 0u;
-            const uint32_t hi = i0 + 1 < a.V ? __ldg(p + i0 + 1) : 0u;
-            w4[h] = lo | (hi << 16);
+        for (int j = 0; j < NLD; ++j) {
+          const int64_t g = g0 + (int64_t)j * NTM;
+          if (vec && g * 8 + 8 <= a.V) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + g);
+            w4[j][0] = q.x; w4[j][1] = q.y; w4[j][2] = q.z; w4[j][3] = q.w;
+          } else {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int64_t i0 = g * 8 + 2 * h;
+              const uint32_t lo = i0 < a.V ? __ldg(p + i0) : 0xFF80u;
+              const uint32_t hi = i0 + 1 < a.V ? __ldg(p + i0 + 1) : 0xFF80u;
+              w4[j][h] = lo | (hi << 16);
+            }
           }
         }
-        const __nv_bfloat162 m2 = __hmax2(__hmax2(bf2(w4[0]), bf2(w4[1])),
-                                          __hmax2(bf2(w4[2]), bf2(w4[3])));
-        if (fmaxf(__low2float(m2), __high2float(m2)) < gate) continue;
+        uint32_t mm = 0u;   // bit 8 j + e: element e of group g0 + j NTM is in the range
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int64_t i = g * 8 + e;
-          if (i >= a.V) break;
-          const uint32_t bits = (w4[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-          f(okey16(bits), bf16_val(bits), i);
+        for (int j = 0; j < NLD; ++j) {
+          const int64_t g = g0 + (int64_t)j * NTM;
+          if (g >= ngroups) break;
+          const __nv_bfloat162 m2 = __hmax2(__hmax2(bf2(w4[j][0]), bf2(w4[j][1])),
+                                            __hmax2(bf2(w4[j][2]), bf2(w4[j][3])));
+          if (fmaxf(__low2float(m2), __high2float(m2)) < lo_val) continue;
+          uint32_t m8 = 0u;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            uint32_t mk = __hge2_mask(bf2(w4[j][h]), lo2);
+            if (bounded) mk &= __hle2_mask(bf2(w4[j][h]), hi2);
+            m8 |= ((mk & 1u) | ((mk >> 15) & 2u)) << (2 * h);
+          }
+          const int64_t left = a.V - g * 8;   // elements of the group inside the row
+          if (left < 8) m8 &= (1u << left) - 1u;
+          mm |= m8 << (8 * j);
+        }
+        while (__any_sync(0xFFFFFFFFu, mm != 0u)) {
+          const bool has = mm != 0u;
+          uint32_t bits = 0u;
+          int64_t i = 0;
+          if (has) {
+            const int b = __ffs(mm) - 1;
+            mm &= mm - 1u;
+            // word b >> 1 of the step's 16 by a select tree on its bits (no
+            // indexing: the words stay in registers)
+            static_assert(NLD == 4, "select tree over 16 words");
+            const bool s0 = b & 2, s1 = b & 4, s2 = b & 8, s3 = b & 16;
+            uint32_t l1[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) l1[q] = s0 ? w4[q >> 1][2 * (q & 1) + 1] : w4[q >> 1][2 * (q & 1)];
+            uint32_t l2[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) l2[q] = s1 ? l1[2 * q + 1] : l1[2 * q];
+            const uint32_t l3a = s2 ? l2[1] : l2[0], l3b = s2 ? l2[3] : l2[2];
+            const uint32_t word = s3 ? l3b : l3a;
+            bits = (word >> (16 * (b & 1))) & 0xFFFFu;
+            i = (g0 + (int64_t)(b >> 3) * NTM) * 8 + (b & 7);
+          }
+          f(has, okey16(bits), bf16_val(bits), i);
         }
       }
     };
     const float zt = bf16_val(okey16_inverse(thr));
     const uint64_t w_thr = thr == 0u ? 0ull : fixed_w(zt, c, E);
-    const float gate = thr == 0u ? -INFINITY : zt;   // members are z >= the boundary value
     uint32_t key_sel = 0u, n_sel = 0u, need = 1u;
     bool have = false;          // key_sel / need found (block-uniform)
-    int32_t direct_id = -1;     // direct mode, need == 1: the answer
+    bool direct_done = false;   // direct mode: the answer is written (block-uniform)
     {
       const float m_est = __fdiv_rn(E, c);   // the row max to within rounding
       uint32_t kmax = okey16(__float_as_uint(m_est) >> 16) + 4u;
       kmax = kmax > 0xFFFFu ? 0xFFFFu : kmax;
-      if (thr != 0u && kmax >= thr && kmax - thr < (uint32_t)NBD) {
+      if (mode >= 1 && thr != 0u && kmax >= thr && kmax - thr < (uint32_t)NBD) {
+        const bool listing = mode == 1 && a.V <= kListMaxV;
         for (int i = tid; i < NBD; i += NTM) {
           sm.dmass[i] = 0ull;
           sm.dcnt[i] = 0u;
-          sm.dmin[i] = 0xFFFFFFFFu;
         }
         if (tid == 0) {
-          sm.n_thr = 0u;
           sm.ovf = 0;
           sm.dsel = 0x7FFFFFFF;
+          sm.lcnt = 0u;
+          sm.gn = 0u;
         }
         __syncthreads();
-        for_row(gate, [&](uint32_t k, float z, int64_t i) {
-          if (k < thr) return;
+        for_row(thr, 0xFFFFu, [&](bool has, uint32_t k, float z, int64_t i) {
           const uint32_t d = k - thr;
-          if (d >= (uint32_t)NBD) {
-            sm.ovf = 1;
-            return;
+          const bool in = has && d < (uint32_t)NBD;
+          if (has && !in) sm.ovf = 1;
+          if (in) {
+            atomicAdd(&sm.dcnt[d], 1u);
+            atomicAdd(&sm.dmass[d], fixed_w(z, c, E));
           }
-          atomicAdd(&sm.dcnt[d], 1u);
-          atomicAdd(&sm.dmass[d], fixed_w(z, c, E));
-          atomicMin(&sm.dmin[d], (uint32_t)i);
-          if (d == 0u) atomicAdd(&sm.n_thr, 1u);
+          if (listing) {   // one list slot reservation per warp and round
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, in);
+            if (bal) {
+              const int lead = __ffs(bal) - 1;
+              uint32_t base = 0u;
+              if (lane == lead) base = atomicAdd(&sm.lcnt, (uint32_t)__popc(bal));
+              base = __shfl_sync(0xFFFFFFFFu, base, lead);
+              const uint32_t idx = base + (uint32_t)__popc(bal & ((1u << lane) - 1u));
+              if (in && idx < LCAP) sm.lst[idx] = ((uint32_t)i << 11) | d;
+            }
+          }
         });
         __syncthreads();
         if (!sm.ovf) {
+          const uint32_t n_thr = sm.dcnt[0];   // tokens holding the boundary key
           uint32_t drop = 0u;
-          if (st.ties != kTiesAll && sm.n_thr > st.ties) drop = sm.n_thr - st.ties;
+          if (st.ties != kTiesAll && n_thr > st.ties) drop = n_thr - st.ties;
           // thread t owns distances 8t .. 8t + 7 from the top (bin NBD - 1 - distance)
           unsigned long long own = 0ull;
 #pragma unroll
@@ -263,7 +331,8 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
           __syncthreads();
           if (dsel != 0x7FFFFFFF) {
             const int b = NBD - 1 - dsel;
-            n_sel = sm.dcnt[b] - (b == 0 ? drop : 0u);
+            const uint32_t n_all = sm.dcnt[b];   // tokens holding the key, kept or not
+            n_sel = n_all - (b == 0 ? drop : 0u);
             const unsigned long long w_sel =
                 (sm.dmass[b] - (b == 0 ? (unsigned long long)drop * w_thr : 0ull)) / n_sel;
             need = 1u;
@@ -272,18 +341,37 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
               need = q < 1ull ? 1u : (q > n_sel ? n_sel : (uint32_t)q);
             }
             key_sel = thr + (uint32_t)b;
-            if (need == 1u) direct_id = (int32_t)sm.dmin[b];
             have = true;
+            const uint32_t nl = sm.lcnt;
+            if (listing && nl <= LCAP && n_all <= GCAP) {
+              // every member is listed: gather the key's tie group (its
+              // positions; the kept ties of the boundary key are its lowest)
+              // and take the need-th lowest
+              if (tid == 0) a.out_ids[r] = -1;   // overwritten below (the group holds need tokens)
+              __syncthreads();   // the bins are read: grp overlays them
+              for (uint32_t k = tid; k < nl; k += NTM) {
+                const uint32_t e = sm.lst[k];
+                if ((e & 2047u) == (uint32_t)b) {
+                  const uint32_t gi = atomicAdd(&sm.gn, 1u);
+                  if (gi < GCAP) sm.grp[gi] = e >> 11;
+                }
+              }
+              __syncthreads();
+              const uint32_t gn = min(sm.gn, GCAP);   // == n_all
+              for (uint32_t t = tid; t < gn; t += NTM) {
+                const uint32_t pos = sm.grp[t];
+                uint32_t rank = 0u;
+                for (uint32_t j = 0; j < gn; ++j) rank += sm.grp[j] < pos ? 1u : 0u;
+                if (rank == need - 1u) a.out_ids[r] = (int32_t)pos;
+              }
+              direct_done = true;
+            }
           }
         }
         __syncthreads();
       }
     }
-    if (have && direct_id >= 0) {
-      if (tid == 0) a.out_ids[r] = direct_id;
-      __syncthreads();
-      continue;
-    }
+    if (direct_done) continue;
     if (!have) {
     // ---- pass 1: bins by key >> 8
     for (int i = tid; i < 256; i += NTM) {
@@ -292,8 +380,8 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
     }
     if (tid == 0) sm.n_thr = 0u;
     __syncthreads();
-    for_row(gate, [&](uint32_t k, float z, int64_t) {
-      if (k < thr) return;
+    for_row(thr, 0xFFFFu, [&](bool has, uint32_t k, float z, int64_t) {
+      if (!has) return;
       atomicAdd(&sm.cnt[k >> 8], 1u);
       atomicAdd(&sm.mass[k >> 8], fixed_w(z, c, E));
       if (k == thr) atomicAdd(&sm.n_thr, 1u);
@@ -338,8 +426,9 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
       sm.cnt[i] = 0u;
     }
     __syncthreads();
-    for_row(gate, [&](uint32_t k, float z, int64_t) {
-      if (k < thr || (int)(k >> 8) != hi_bin) return;
+    for_row(max(thr, (uint32_t)hi_bin << 8), ((uint32_t)hi_bin << 8) | 255u,
+            [&](bool has, uint32_t k, float z, int64_t) {
+      if (!has) return;
       atomicAdd(&sm.cnt[k & 255u], 1u);
       atomicAdd(&sm.mass[k & 255u], fixed_w(z, c, E));
     });
@@ -442,9 +531,9 @@ __global__ void __launch_bounds__(NTM) sample_kernel(SampleArgs a, float c0) {
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t stream) {
   const float c = (float)(1.4426950408889634 / (double)a.temperature);
   // a row's serial phases (the scans, the barriers) are hidden by the other
-  // rows in flight: as many CTAs per SM as the registers allow
+  // rows in flight: five CTAs per SM (registers and shared memory allow five)
   const int64_t cap = (int64_t)5 * sm_count();
-  sample_kernel<<<(unsigned)(a.T < cap ? a.T : cap), NTM, 0, stream>>>(a, c);
+  sample_kernel<<<(unsigned)(a.T < cap ? a.T : cap), NTM, 0, stream>>>(a, c, debug_sampler_mode());
   return cudaGetLastError();
 }
 

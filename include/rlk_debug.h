@@ -58,6 +58,20 @@ long long rlk_debug_set_wait_limit(long long cycles);
  */
 int rlk_debug_withhold_copy(long long stage);
 
+/*
+ * rlk_debug_set_sampler_mode -- the ways rlk_sample_top_p may take to a draw.
+ * mode = 1 (the default, also for any value other than 0 and 2): the direct
+ * mode where it applies, which bins the retained set by key in one read of
+ * the row and ranks the draw's tie group from the list of members it kept;
+ * mode = 2: the direct mode without the member list (the tie group is found
+ * by a scan of the row in id order, as when the list runs out of room);
+ * mode = 0: every row by the radix descent over the 16-bit keys (up to three
+ * reads of the row).  All draw the same id (integer arithmetic); this lets
+ * tests compare them on the same inputs.  Returns the previous mode.  Not
+ * thread-safe with respect to concurrent launches.
+ */
+int rlk_debug_set_sampler_mode(int mode);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif
