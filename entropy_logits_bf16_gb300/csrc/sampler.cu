@@ -49,6 +49,7 @@ constexpr uint32_t LCAP = 4096;   // direct mode: members listed per row
 constexpr uint32_t GCAP = 1024;   // largest tie group ranked from the list
 constexpr int64_t kListMaxV = int64_t(1) << 21;   // a position and a bin in 32 bits
 constexpr int NLD = 4;            // 16-byte loads in flight per thread
+constexpr uint32_t QCAP = 64;     // a warp's queue of passing groups (at most 63 held)
 
 struct MSmem {
   union {
@@ -63,6 +64,7 @@ struct MSmem {
     uint32_t grp[GCAP];             // direct mode, after the scan: the draw's tie group
   };
   uint32_t lst[LCAP];             // direct mode: members, position << 11 | bin
+  uint32_t q[NWM][QCAP];          // each warp's queue of groups that reach the range
   uint32_t lcnt;                  // members listed (may exceed LCAP)
   uint32_t gn;                    // tie group gathered
   unsigned long long wsum[NWM];   // per-warp sums (direct-mode scan)
@@ -165,12 +167,14 @@ __global__ void __launch_bounds__(NTM, 5) sample_kernel(SampleArgs a, float c0, 
     // f(has, k, z, index), called by every lane of the warp together (has:
     // this lane holds an element this round).  A thread takes groups g,
     // g + NTM, ..., NLD of them per step, all loads issued before any is used;
-    // a group whose largest value is below the range is skipped after one
-    // packed max, the others are tested two elements at a time by packed bf16
-    // compares against the range's end values (-0 == +0, as the keys have
-    // it), and the elements found are handed out in rounds, one per lane and
-    // round, so a warp spends one pass of f per round rather than one per
-    // element of every passing group.
+    // a group whose largest value is below the range is dropped after one
+    // packed max.  The others go into the warp's queue (their indices), and
+    // every 32 queued groups are taken one per lane: the group read again
+    // (from L2), tested two elements at a time by packed bf16 compares
+    // against the range's end values (-0 == +0, as the keys have it), and its
+    // elements in the range handed to f in rounds, one per lane and round.
+    // The range test and the rounds thus run once per 32 passing groups, not
+    // once per lane slot that holds one.
     auto for_row = [&](uint32_t klo, uint32_t khi, auto&& f) {
       // the range as values (keys below 0x7F are NaN, above 0xFF80 too; 0x7FFF
       // is the key -0 would have without its mapping to +0)
@@ -178,14 +182,60 @@ __global__ void __launch_bounds__(NTM, 5) sample_kernel(SampleArgs a, float c0, 
       const float hi_val = khi >= 0xFF80u ? INFINITY : bf16_val(okey16_inverse(khi == 0x7FFFu ? 0x7FFEu : khi));
       const bool bounded = hi_val != INFINITY;
       const __nv_bfloat162 lo2 = __float2bfloat162_rn(lo_val), hi2 = __float2bfloat162_rn(hi_val);
+      uint32_t* q = sm.q[warp];
+      uint32_t head = 0u, tail = 0u;   // the warp's queue (warp-uniform counters, ring of QCAP)
+      // lanes below n take queue entries head + lane
+      auto drain = [&](uint32_t n) {
+        __syncwarp();   // the entries written by other lanes are visible
+        uint32_t m8 = 0u, w[4] = {0u, 0u, 0u, 0u};
+        int64_t g = 0;
+        if ((uint32_t)lane < n) {
+          g = q[(head + (uint32_t)lane) & (QCAP - 1)];
+          if (vec && g * 8 + 8 <= a.V) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + g);
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+          } else {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int64_t i0 = g * 8 + 2 * h;
+              const uint32_t lo = i0 < a.V ? __ldg(p + i0) : 0xFF80u;
+              const uint32_t hi = i0 + 1 < a.V ? __ldg(p + i0 + 1) : 0xFF80u;
+              w[h] = lo | (hi << 16);
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            uint32_t mk = __hge2_mask(bf2(w[h]), lo2);
+            if (bounded) mk &= __hle2_mask(bf2(w[h]), hi2);
+            m8 |= ((mk & 1u) | ((mk >> 15) & 2u)) << (2 * h);
+          }
+          const int64_t left = a.V - g * 8;   // elements of the group inside the row
+          if (left < 8) m8 &= (1u << left) - 1u;
+        }
+        head += n;
+        while (__any_sync(0xFFFFFFFFu, m8 != 0u)) {
+          const bool has = m8 != 0u;
+          uint32_t bits = 0u;
+          int64_t i = 0;
+          if (has) {
+            const int e = __ffs(m8) - 1;
+            m8 &= m8 - 1u;
+            const uint32_t wa = (e & 2) ? w[1] : w[0], wb = (e & 2) ? w[3] : w[2];
+            bits = (((e & 4) ? wb : wa) >> (16 * (e & 1))) & 0xFFFFu;
+            i = g * 8 + e;
+          }
+          f(has, okey16(bits), bf16_val(bits), i);
+        }
+        __syncwarp();   // the entries are read before later pushes reuse them
+      };
       for (int64_t g0 = tid; g0 < ngroups; g0 += (int64_t)NLD * NTM) {
         uint32_t w4[NLD][4];
 #pragma unroll
         for (int j = 0; j < NLD; ++j) {
           const int64_t g = g0 + (int64_t)j * NTM;
           if (vec && g * 8 + 8 <= a.V) {
-            const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + g);
-            w4[j][0] = q.x; w4[j][1] = q.y; w4[j][2] = q.z; w4[j][3] = q.w;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + g);
+            w4[j][0] = v.x; w4[j][1] = v.y; w4[j][2] = v.z; w4[j][3] = v.w;
           } else {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -196,50 +246,19 @@ __global__ void __launch_bounds__(NTM, 5) sample_kernel(SampleArgs a, float c0, 
             }
           }
         }
-        uint32_t mm = 0u;   // bit 8 j + e: element e of group g0 + j NTM is in the range
 #pragma unroll
         for (int j = 0; j < NLD; ++j) {
           const int64_t g = g0 + (int64_t)j * NTM;
-          if (g >= ngroups) break;
           const __nv_bfloat162 m2 = __hmax2(__hmax2(bf2(w4[j][0]), bf2(w4[j][1])),
                                             __hmax2(bf2(w4[j][2]), bf2(w4[j][3])));
-          if (fmaxf(__low2float(m2), __high2float(m2)) < lo_val) continue;
-          uint32_t m8 = 0u;
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            uint32_t mk = __hge2_mask(bf2(w4[j][h]), lo2);
-            if (bounded) mk &= __hle2_mask(bf2(w4[j][h]), hi2);
-            m8 |= ((mk & 1u) | ((mk >> 15) & 2u)) << (2 * h);
-          }
-          const int64_t left = a.V - g * 8;   // elements of the group inside the row
-          if (left < 8) m8 &= (1u << left) - 1u;
-          mm |= m8 << (8 * j);
-        }
-        while (__any_sync(0xFFFFFFFFu, mm != 0u)) {
-          const bool has = mm != 0u;
-          uint32_t bits = 0u;
-          int64_t i = 0;
-          if (has) {
-            const int b = __ffs(mm) - 1;
-            mm &= mm - 1u;
-            // word b >> 1 of the step's 16 by a select tree on its bits (no
-            // indexing: the words stay in registers)
-            static_assert(NLD == 4, "select tree over 16 words");
-            const bool s0 = b & 2, s1 = b & 4, s2 = b & 8, s3 = b & 16;
-            uint32_t l1[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) l1[q] = s0 ? w4[q >> 1][2 * (q & 1) + 1] : w4[q >> 1][2 * (q & 1)];
-            uint32_t l2[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) l2[q] = s1 ? l1[2 * q + 1] : l1[2 * q];
-            const uint32_t l3a = s2 ? l2[1] : l2[0], l3b = s2 ? l2[3] : l2[2];
-            const uint32_t word = s3 ? l3b : l3a;
-            bits = (word >> (16 * (b & 1))) & 0xFFFFu;
-            i = (g0 + (int64_t)(b >> 3) * NTM) * 8 + (b & 7);
-          }
-          f(has, okey16(bits), bf16_val(bits), i);
+          const bool pass = g < ngroups && fmaxf(__low2float(m2), __high2float(m2)) >= lo_val;
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
+          if (pass) q[(tail + (uint32_t)__popc(bal & ((1u << lane) - 1u))) & (QCAP - 1)] = (uint32_t)g;
+          tail += (uint32_t)__popc(bal);
+          if (tail - head >= 32u) drain(32u);
         }
       }
+      if (tail != head) drain(tail - head);
     };
     const float zt = bf16_val(okey16_inverse(thr));
     const uint64_t w_thr = thr == 0u ? 0ull : fixed_w(zt, c, E);
