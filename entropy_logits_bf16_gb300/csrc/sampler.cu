@@ -140,7 +140,7 @@ __device__ void scan256(MSmem& sm, unsigned long long base, unsigned long long t
   }
 }
 
-__global__ void __launch_bounds__(NTM, 5) sample_kernel(SampleArgs a, float c0, int mode) {
+__global__ void __launch_bounds__(NTM, 4) sample_kernel(SampleArgs a, float c0, int mode) {
   __shared__ MSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ngroups = (a.V + 7) / 8;
@@ -228,7 +228,10 @@ __global__ void __launch_bounds__(NTM, 5) sample_kernel(SampleArgs a, float c0, 
         }
         __syncwarp();   // the entries are read before later pushes reuse them
       };
-      for (int64_t g0 = tid; g0 < ngroups; g0 += (int64_t)NLD * NTM) {
+      // the bound is the warp's (its first lane's): every lane of a warp runs
+      // the same steps, as the ballots and the drains need; groups past the
+      // row load nothing and never pass
+      for (int64_t g0 = tid; g0 - lane < ngroups; g0 += (int64_t)NLD * NTM) {
         uint32_t w4[NLD][4];
 #pragma unroll
         for (int j = 0; j < NLD; ++j) {
@@ -550,8 +553,9 @@ __global__ void __launch_bounds__(NTM, 5) sample_kernel(SampleArgs a, float c0, 
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t stream) {
   const float c = (float)(1.4426950408889634 / (double)a.temperature);
   // a row's serial phases (the scans, the barriers) are hidden by the other
-  // rows in flight: five CTAs per SM (registers and shared memory allow five)
-  const int64_t cap = (int64_t)5 * sm_count();
+  // rows in flight: four CTAs per SM (64 registers a thread; five would fit
+  // in shared memory but spill at 48 registers, and measured slower)
+  const int64_t cap = (int64_t)4 * sm_count();
   sample_kernel<<<(unsigned)(a.T < cap ? a.T : cap), NTM, 0, stream>>>(a, c, debug_sampler_mode());
   return cudaGetLastError();
 }

@@ -121,12 +121,17 @@ def test_tie_groups_every_rank(cuda_lib):
 
 
 @pytest.mark.parametrize("V,ld,off", [(14335, 14336, 0), (151931, 151936, 0), (151936, 151939, 0),
-                                      (151936, 151944, 1), (174081, 174088, 0), (20000, 20480, 0)])
+                                      (151936, 151944, 1), (174081, 174088, 0), (20000, 20480, 0),
+                                      (148256, 148256, 0), (148255, 148256, 0), (2097153, 2097160, 0)])
 @pytest.mark.parametrize("p", [0.9, 1.0])
 def test_vocab_sizes_and_strides(cuda_lib, oracle, V, ld, off, p):
     """Partial last groups, padded strides that are not a multiple of 8
-    logits, and a base that is not 16-byte aligned (2-byte loads)."""
-    rows = 12
+    logits, a base that is not 16-byte aligned (2-byte loads), row lengths
+    whose groups do not fill the CTA's last step evenly (148,256 logits:
+    18,532 groups, 100 past a whole number of 1,024-group steps, so some lanes
+    of a warp hold groups in that step and others do not), and a vocabulary
+    past 2^21 (no member list: the tie group from the scan in id order)."""
+    rows = 12 if V < 1_000_000 else 3
     base, _ = workloads.peaked_bf16(rows, V=ld + off, seed=17, device="cuda")
     z = base[:, off:off + V]
     z[:, V - 3:] = 12.5   # kept tokens in the partial last group
@@ -134,7 +139,8 @@ def test_vocab_sizes_and_strides(cuda_lib, oracle, V, ld, off, p):
     a, b, sa, sb = _both(cuda_lib, z, 0.7, p, torch.from_numpy(u).cuda())
     assert sa == 0 and sb == 0
     assert np.array_equal(a, b), np.nonzero(a != b)[0]
-    _check(workloads.bf16_bits(z), a, u, 0.7, p, oracle)
+    if V < 1_000_000:
+        _check(workloads.bf16_bits(z), a, u, 0.7, p, oracle)
 
 
 def test_batches_and_per_row_parameters(cuda_lib):
