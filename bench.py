@@ -942,8 +942,8 @@ def run_sample(args, ws, rank, dev, barrier):
                      "traffic": profiled_traffic(os.path.join(CSRC, "sampler.cu"),
                                                  os.path.join(PROFILES, "sample_kernel_qwen_T4096.txt")),
                      "peak_source": peak_kind,
-                     "kernel": "sample_kernel (one rlk_sample_top_p call; rows re-read when a tie "
-                               "must be resolved)",
+                     "kernel": "sample_kernel (one rlk_sample_top_p call: each row read once, "
+                               "tie groups ranked from the member list)",
                      "algorithmic_bytes_per_launch": alg, "launch_ms": part_ms[0]},
         "gpu_launches": args.steps,
         "clocks": clk,
