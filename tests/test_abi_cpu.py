@@ -409,3 +409,15 @@ def test_shard_partials_support_rejects(lib, armed):
         assert part(**kw) == 1, kw
     assert part(T=0, off=None, out=None) == 0
     assert part() == 4                                         # checks passed: injected
+
+
+def test_debug_settings_round_trip(lib):
+    """The host-side debug settings return the previous value and restore
+    their defaults (no device work)."""
+    assert rlk.set_sampler_mode(0) == 1
+    assert rlk.set_sampler_mode(2) == 0
+    assert rlk.set_sampler_mode(7) == 2      # anything else: the default
+    assert rlk.set_sampler_mode(1) == 1
+    prev = rlk.set_wait_limit(1234)
+    assert rlk.set_wait_limit(0) == 1234     # <= 0 restores the default
+    assert rlk.set_wait_limit(prev) == prev

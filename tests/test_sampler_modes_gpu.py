@@ -187,3 +187,20 @@ def test_subnormal_and_signed_zero_order(cuda_lib, oracle):
     assert sa == 0 and sb == 0
     assert np.array_equal(a, b), np.nonzero(a != b)[0]
     _check(hz, a, u, 1.0, 0.5, oracle)
+
+
+@pytest.mark.parametrize("V", [1, 5, 8, 9, 100, 1000])
+@pytest.mark.parametrize("T_,p", [(0.7, 0.9), (1.0, 1.0)])
+def test_small_vocabularies(cuda_lib, oracle, V, T_, p):
+    """Rows shorter than one warp's groups (the loop bound, the queue and
+    its last drain with a handful of lanes), with ties, against the oracle."""
+    rng = np.random.default_rng(V)
+    zf = np.round(rng.normal(0.0, 2.0, (16, V)) * 4) / 4   # a 0.25 grid: ties
+    z = torch.from_numpy(zf.astype(np.float32)).to(torch.bfloat16).cuda()
+    u = workloads.uniforms(16, V + 1).astype(np.float32)
+    u[0] = 0.0
+    a, b, sa, sb = _both(cuda_lib, z, T_, p, torch.from_numpy(u).cuda())
+    assert sa == 0 and sb == 0
+    assert np.array_equal(a, b), np.nonzero(a != b)[0]
+    assert ((a >= 0) & (a < V)).all()
+    _check(workloads.bf16_bits(z), a, u, T_, p, oracle)
