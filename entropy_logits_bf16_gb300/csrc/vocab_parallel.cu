@@ -28,9 +28,41 @@ namespace {
 constexpr int NTP = 256;
 constexpr int NWP = NTP / 32;
 
+// A state's sums are relative to 2^E with E = ceil(fp32(m c)), an integer
+// fixed by its max m alone: every weight is 2^d with d = fma(z, c, -E) (one
+// rounding), states merge and rescale by exact powers of two, and the
+// window's bins, formed the same way against the row's E, carry the very
+// weights the sums hold for the row max's tokens.  (A reference of fp32(m c)
+// itself rescaled by ex2 of rounded differences, and left the bins and Z
+// apart by up to 2^-19 relative: enough to move a boundary whose gap is
+// 1e-6.)
 struct Part {
   float m, hi, lo, u;
+  float e = -INFINITY;   // part_ref(m): kept by the absorbs and merges (not stored)
 };
+
+__device__ __forceinline__ float part_ref(float m, float c) { return ceilf(__fmul_rn(m, c)); }
+
+// 2^n for an integer-valued n <= 0, exactly (0 below 2^-126).
+__device__ __forceinline__ float pow2_int(float n) {
+  return n >= -126.f ? __int_as_float(((int)n + 127) << 23) : 0.f;
+}
+
+// Moves a state's sums from the reference of max m to that of max gm > m.
+__device__ __forceinline__ void part_raise(Part& st, float gm, float c) {
+  const float En = part_ref(gm, c);
+  if (st.m != -INFINITY) {
+    const float k = __fsub_rn(En, st.e);   // an integer >= 0
+    if (k > 0.f) {
+      const float f = pow2_int(-k);
+      st.u = __fmul_rn(f, __fmaf_rn(-k, __fadd_rn(st.hi, st.lo), st.u));
+      st.hi = __fmul_rn(st.hi, f);
+      st.lo = __fmul_rn(st.lo, f);
+    }
+  }
+  st.m = gm;
+  st.e = En;
+}
 
 __device__ __forceinline__ bool part_empty(const Part& a) {
   return a.m == -INFINITY && a.hi == 0.f && a.lo == 0.f && a.u == 0.f;
@@ -41,13 +73,15 @@ __device__ __forceinline__ Part part_merge(const Part& a, const Part& b, float c
   if (part_empty(b)) return a;
   if (part_empty(a)) return b;
   const float M = fmaxf(a.m, b.m);
-  const float da = __fmul_rn(__fsub_rn(M, a.m), c);
-  const float db = __fmul_rn(__fsub_rn(M, b.m), c);
-  const float fa = (a.m == M) ? 1.f : ex2(-da);
-  const float fb = (b.m == M) ? 1.f : ex2(-db);
+  const float E = part_ref(M, c);
+  const float da = __fsub_rn(E, part_ref(a.m, c));   // integers >= 0
+  const float db = __fsub_rn(E, part_ref(b.m, c));
+  const float fa = pow2_int(-da);
+  const float fb = pow2_int(-db);
   const float sa = __fadd_rn(a.hi, a.lo), sb = __fadd_rn(b.hi, b.lo);
   Part r;
   r.m = M;
+  r.e = E;
   r.u = __fadd_rn(__fmul_rn(fa, __fmaf_rn(-da, sa, a.u)), __fmul_rn(fb, __fmaf_rn(-db, sb, b.u)));
   float s, e;
   two_sum(__fmul_rn(a.hi, fa), __fmul_rn(b.hi, fb), s, e);
@@ -73,20 +107,12 @@ __device__ __forceinline__ void part_absorb8(Part& st, const float (&v)[8], int 
     return;
   }
   if (gm == -INFINITY) return;
-  if (gm > st.m) {
-    if (st.m != -INFINITY) {
-      const float delta = __fmul_rn(__fsub_rn(gm, st.m), c);
-      const float f = ex2(-delta);
-      st.u = __fmul_rn(f, __fmaf_rn(-delta, __fadd_rn(st.hi, st.lo), st.u));
-      st.hi = __fmul_rn(st.hi, f);
-      st.lo = __fmul_rn(st.lo, f);
-    }
-    st.m = gm;
-  }
+  if (gm > st.m) part_raise(st, gm, c);
+  const float E = st.e;
   float w[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const float d = k < n ? __fmul_rn(__fsub_rn(v[k], st.m), c) : 0.f;
+    const float d = k < n ? __fmaf_rn(v[k], c, -E) : 0.f;
     w[k] = k < n ? ex2(d) : 0.f;
     st.u = __fmaf_rn(w[k], d, st.u);
   }
@@ -100,7 +126,7 @@ __device__ __forceinline__ void part_absorb8(Part& st, const float (&v)[8], int 
 
 // Fold one packed group of eight bf16 into the state with packed arithmetic:
 // bf16x2 max / min (the NaN-propagating max flags NaN, the extremes flag
-// +-inf), then d = z c - E with E = fp32(m c) as fp32x2 fmas.
+// +-inf), then d = z c - E as fp32x2 fmas.
 __device__ __forceinline__ void part_absorb_packed(Part& st, const uint4 q, float c) {
   const __nv_bfloat162 mx = __hmax2_nan(__hmax2_nan(bf2(q.x), bf2(q.y)),
                                         __hmax2_nan(bf2(q.z), bf2(q.w)));
@@ -111,19 +137,8 @@ __device__ __forceinline__ void part_absorb_packed(Part& st, const uint4 q, floa
     st.u = NAN;   // a non-finite logit: the row has no distribution
     return;
   }
-  if (gm > st.m) {
-    if (st.m != -INFINITY) {
-      const float delta = __fmul_rn(__fsub_rn(gm, st.m), c);
-      const float f = ex2(-delta);
-      st.u = __fmul_rn(f, __fmaf_rn(-delta, __fadd_rn(st.hi, st.lo), st.u));
-      st.hi = __fmul_rn(st.hi, f);
-      st.lo = __fmul_rn(st.lo, f);
-    }
-    st.m = gm;
-  }
-  // d relative to m itself: E = fp32(m c), and fma(z, c, -E) differs from
-  // (z - m) c by the rounding of E, which every term and the rescales share
-  const float E = __fmul_rn(st.m, c);
+  if (gm > st.m) part_raise(st, gm, c);
+  const float E = st.e;
   const float2 c2 = make_float2(c, c), nE2 = make_float2(-E, -E);
   const float2 d0 = __ffma2_rn(bf16x2_to_f2(q.x), c2, nE2);
   const float2 d1 = __ffma2_rn(bf16x2_to_f2(q.y), c2, nE2);
@@ -146,7 +161,7 @@ __device__ __forceinline__ void part_absorb_packed(Part& st, const uint4 q, floa
 // One warp per (row, shard) pair; lane l takes the 8-column groups l, l + 32,
 // ... of the shard (four 16-byte loads in flight), and the lanes' states
 // merge along a fixed shuffle tree.
-__global__ void __launch_bounds__(NTP) shard_partial_kernel(ShardArgs a, float c) {
+__global__ void __launch_bounds__(NTP, 5) shard_partial_kernel(ShardArgs a, float c) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t n_pairs = a.T * (int64_t)a.n_shards;
   const int64_t nwarps = (int64_t)gridDim.x * NWP;
@@ -221,17 +236,8 @@ __device__ __forceinline__ void part_absorb1(Part& st, float z, float c) {
     st.u = NAN;
     return;
   }
-  if (z > st.m) {
-    if (st.m != -INFINITY) {
-      const float delta = __fmul_rn(__fsub_rn(z, st.m), c);
-      const float f = ex2(-delta);
-      st.u = __fmul_rn(f, __fmaf_rn(-delta, __fadd_rn(st.hi, st.lo), st.u));
-      st.hi = __fmul_rn(st.hi, f);
-      st.lo = __fmul_rn(st.lo, f);
-    }
-    st.m = z;
-  }
-  const float d = __fmul_rn(__fsub_rn(z, st.m), c);
+  if (z > st.m) part_raise(st, z, c);
+  const float d = __fmaf_rn(z, c, -st.e);
   const float w = ex2(d);
   float s, e;
   two_sum(st.hi, w, s, e);
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(256) shard_combine_kernel(ShardCombineArgs a, 
     return;
   }
   const float lz = logf(zf);
-  a.out_logprob[r] = y_in ? __fsub_rn(__fdiv_rn(__fsub_rn(py.x, st.m), a.temperature), lz)
+  a.out_logprob[r] = y_in ? __fsub_rn(__fmul_rn(kLn2, __fmaf_rn(py.x, c, -part_ref(st.m, c))), lz)
                           : -INFINITY;
   a.out_entropy[r] = __fsub_rn(lz, __fdiv_rn(__fmul_rn(kLn2, st.u), zf));
 }
@@ -374,7 +380,7 @@ struct ShardCounts {      // one row's window counts of one shard (8224 bytes)
 static_assert(sizeof(ShardCounts) == 8224, "the counts' layout is part of the ABI");
 
 struct Window {
-  float m, E, zf;         // the row max, E = fp32(m c), Z relative to 2^E
+  float m, E, zf;         // the row max, E = ceil(fp32(m c)), Z relative to 2^E
   DF Z;
   uint32_t key_m, key_lo, ck_m, dmax;
   bool fits;              // the window has at most HBW bins and the row is finite
@@ -391,11 +397,13 @@ __device__ Window row_window(const float4* p, int n_all, int64_t T, int64_t r, i
   }
   Window w{};
   w.m = st.m;
-  w.E = __fmul_rn(st.m, c);
+  w.E = part_ref(st.m, c);
   w.Z = DF{st.hi, st.lo};
   w.zf = __fadd_rn(st.hi, st.lo);
   const float one_m_p = __fsub_rn(1.f, top_p);
-  const float L = fmaxf(logf(__fdiv_rn((float)V, __fmul_rn(one_m_p, w.zf))), 0.f) + 0.5f;
+  // Z relative to the max's own weight 2^(m c - E), in (1/2, 1]
+  const float zmax = __fdiv_rn(w.zf, ex2(__fmaf_rn(st.m, c, -w.E)));
+  const float L = fmaxf(logf(__fdiv_rn((float)V, __fmul_rn(one_m_p, zmax))), 0.f) + 0.5f;
   const float zlo = __fsub_rn(w.m, __fmul_rn(L, temp));
   w.key_m = key_of_f(w.m);
   const uint32_t kl = key_of_f(zlo);
@@ -403,7 +411,7 @@ __device__ Window row_window(const float4* p, int n_all, int64_t T, int64_t r, i
   w.ck_m = ckey(w.key_m);
   const uint32_t ck_lo = ckey(w.key_lo);
   w.dmax = w.ck_m - ck_lo;
-  w.fits = isfinite(w.m) && isfinite(w.zf) && isfinite(st.u) && w.zf >= 1.f &&
+  w.fits = isfinite(w.m) && isfinite(w.zf) && isfinite(st.u) && w.zf > 0.f &&
            w.key_lo <= w.key_m && w.dmax < (uint32_t)HBW;
   return w;
 }

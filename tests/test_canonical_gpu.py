@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import workloads
-from _parity import LP_REL, LP_TOL, ENT_TOL
+from _parity import LP_REL, LP_TOL, ENT_TOL, compare_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -259,3 +259,20 @@ def test_canonical_topp_bad_rows(cuda_lib):
     assert np.isfinite(lp[0]) and np.isfinite(ent[0]) and k[0] >= 1
     assert np.all(np.isnan(lp[1:])) and np.all(np.isnan(ent[1:])) and np.all(k[1:] == 0)
     assert int(st.item()) == (cuda_lib.STATUS_BAD_TOKEN_ID | cuda_lib.STATUS_NONFINITE)
+
+
+def test_canonical_topp_boundaries_near_the_gap_threshold(cuda_lib, oracle):
+    """Three peaked rows (V = 58,644, temperature 0.5, top_p 0.999) whose
+    boundaries lie 0.7e-6, 1.18e-6 and 1.67e-6 from a cumulative step.  The
+    combine's bin weights and the shards' sums must use one reference: a
+    common factor between them as small as 2^-19 (a reference exponent
+    rounded to fp32 on one side and not on the other) moves the second row's
+    boundary by one token, outside the gap exemption."""
+    z, _ = workloads.peaked_bf16(3, V=58644, seed=268817604, device="cuda")
+    hz = workloads.bf16_bits(z)
+    ids_h = oracle.sample_ids(hz, 0.5, 0.999, workloads.uniforms(3, 5))
+    ids = torch.from_numpy(ids_h).cuda()
+    lp, ent, k = cuda_lib.logprob_entropy_canonical_topp(z, ids, 0.5, 0.999)
+    torch.cuda.synchronize()
+    compare_rows(oracle, hz, ids_h, 0.5, 0.999, lp.cpu().numpy(), ent.cpu().numpy(), k.cpu().numpy(),
+                 label="canonical near-threshold rows")
