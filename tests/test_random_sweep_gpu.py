@@ -89,3 +89,54 @@ def test_random_sweep(cuda_lib, oracle, seed):
         row_sum = g.double().sum(1).abs().cpu().numpy()[fin]
         row_abs = g.double().abs().sum(1).cpu().numpy()[fin]
         assert np.all(row_sum <= 1e-4 * row_abs + 2e-5), f"{label}: row sum {row_sum.max():.3e}"
+
+
+def test_random_lmhead_shapes(cuda_lib, oracle):
+    """Random LM-head shapes (T from 1 to 513 rows across 128-row tiles, H
+    from 64 to 1024, V from 1 to 20,000 across 256-column tiles): the fused
+    forward at top_p = 1 against the oracle on sampled rows, dL/dhidden and
+    dL/dW row by row (relative 4e-3 of the row's norm, the bf16 rounding of
+    dz, with an absolute floor for the all-zero gradients of V = 1), and at
+    top_p < 1 the same bits as the scorer on the GEMM's own logits rounded
+    to bf16."""
+    rng = np.random.default_rng(41)
+    for case in range(24):
+        T = int(rng.choice([1, 7, 127, 128, 129, 300, 513]))
+        H = int(rng.choice([64, 128, 192, 512, 1024]))
+        V = int(rng.choice([1, 3, 255, 256, 257, 4097, 20000]))
+        temp = float(rng.choice([0.5, 0.7, 1.0]))
+        p = float(rng.choice([1.0, 1.0, 0.9]))
+        g = torch.Generator().manual_seed(int(rng.integers(1 << 30)))
+        hidden = torch.randn(T, H, generator=g).to(torch.bfloat16).cuda()
+        w = (torch.randn(V, H, generator=g) * float(rng.choice([0.02, 0.1]))).to(torch.bfloat16).cuda()
+        ids = torch.randint(0, V, (T,), generator=g, dtype=torch.int32).cuda()
+        label = f"case {case}: T={T} H={H} V={V} temp={temp} top_p={p}"
+        lse = torch.empty(T, device="cuda") if p == 1.0 else None
+        lp, ent = cuda_lib.lmhead_logprob(hidden, w, ids, temp, p, out_lse=lse)
+        torch.cuda.synchronize()
+        if p < 1.0:
+            logits, _, _ = cuda_lib.lmhead_logits_debug(hidden, w, ids, temp)
+            slp, sent = cuda_lib.logprob_entropy(logits.to(torch.bfloat16).contiguous(), ids, temp, p)
+            torch.cuda.synchronize()
+            assert torch.equal(slp.view(torch.int32), lp.view(torch.int32)), label
+            assert torch.equal(sent.view(torch.int32), ent.view(torch.int32)), label
+            continue
+        hb, wb = workloads.bf16_bits(hidden), workloads.bf16_bits(w)
+        rows = np.unique(np.concatenate([[0, T - 1], rng.integers(0, T, 6)])).astype(np.int64)
+        olp, oent, _ = oracle.lmhead_rows(hb, wb, rows, ids.cpu().numpy(), temp, 1.0)
+        glp, gent = lp.cpu().numpy()[rows], ent.cpu().numpy()[rows]
+        assert np.all(np.abs(glp - olp) <= 2e-4 + 2.0 ** -22 * np.abs(olp)), label
+        assert np.all(np.abs(gent - oent) <= 2e-4), label
+        if T * V * H > 4e8:
+            continue   # the oracle's fp64 backward is O(T V H)
+        ones = torch.ones(T, device="cuda")
+        dh, dw = cuda_lib.lmhead_backward(hidden, w, ids, temp, lse, ent, ones, ones)
+        torch.cuda.synchronize()
+        odh, odw = oracle.lmhead_backward(hb, wb, ids.cpu().numpy(), temp, 1.0,
+                                          np.ones(T, np.float32), np.ones(T, np.float32))
+        for name, got, want in (("dL/dhidden", dh, odh), ("dL/dW", dw, odw)):
+            got = got.double().cpu().numpy()
+            floor = (1e-5 * np.sqrt(np.mean(want ** 2)) + 2e-5) * np.sqrt(want.shape[1])
+            err = np.linalg.norm(got - want, axis=1)
+            ref = np.linalg.norm(want, axis=1)
+            assert np.all(err <= 4e-3 * ref + floor), f"{label}: {name}"
