@@ -276,6 +276,7 @@ GRPO_SEQ, GRPO_LEN, GRPO_G = 64, 64, 8          # 64 responses x 64 tokens, grou
 LOSS_CFG = (f"GRPO/DAPO loss on the step's log-probs: {GRPO_SEQ} sequences x {GRPO_LEN} tokens, "
             f"group {GRPO_G}, eps 0.2/0.28, TIS cap 2.0, k3 KL 0.01, token mean")
 LM_T, LM_H = 16384, 4096
+ZIPF_ROWS = 8 * 6912   # the long-response batch: 8 responses x 6912 tokens
 LM_METRIC = "tokens/s for fused LM-head logprob+entropy (top_p 1) at V=151936, H=4096 bf16; % of bf16 peak"
 
 
@@ -487,7 +488,7 @@ def leg_zipf(args, ws, rank, dev, barrier, kappa):
     per-row kernel's reference exponent is not an integer)."""
     import entropy_logits_bf16_gb300 as rlk
     import workloads
-    rows = 8 * 6912
+    rows = ZIPF_ROWS
     k = workloads.ZIPF_KAPPA_CALIBRATED if kappa is None else kappa
     z, _ = workloads.zipf_bf16(rows, seed=2 + 100 * rank, kappa=k, sigma=workloads.ZIPF_SIGMA,
                                device=dev)
@@ -510,7 +511,7 @@ def leg_zipf(args, ws, rank, dev, barrier, kappa):
     achieved = rows * BYTES_PER_TOKEN / (part_ms[0] / 1e3) / 1e9
     out = {"metric": "tokens/s", "value": whole_job_rate(rows, la.steps, ws, elapsed_ms),
            "unit": "tokens/s", "steps": la.steps, "ms_per_step": elapsed_ms / la.steps,
-           "config": {"workload": (f"long-response batch 8 x 6912 = {rows} rows, V={VOCAB} bf16, "
+           "config": {"workload": (f"long-response batch of {rows} rows (8 x 6912 = 55296 in full), V={VOCAB} bf16, "
                                    f"z = bf16(-kappa s ln rank + sigma N(0,1)), s ~ U(0.8,1.4), "
                                    f"kappa {k}, sigma {workloads.ZIPF_SIGMA}, temperature "
                                    f"{TEMPERATURE}, top_p {TOP_P}; ids from the truncated "
@@ -518,7 +519,7 @@ def leg_zipf(args, ws, rank, dev, barrier, kappa):
                       "T": rows, "V": VOCAB, "kappa": k, "sigma": workloads.ZIPF_SIGMA,
                       "nucleus_size_quantiles_0_50_90_99_100": [round(x) for x in kq],
                       "rows_recomputed_by_per_row_kernel": recomputed,
-                      "l2": "inputs (16.8 GB) larger than L2"},
+                      "l2": f"inputs ({rows * VOCAB * 2 / 1e9:.1f} GB) larger than L2"},
            "roofline": hbm_roofline(achieved, peaks, peak_kind, part_ms[0], clk,
                                     kernel="one rlk_logprob_entropy call (streaming kernel + "
                                            "per-row recompute pass)",
@@ -540,6 +541,19 @@ def leg_zipf(args, ws, rank, dev, barrier, kappa):
                                "sample": f"{len(sel)} evenly spaced rows, fp64 oracle, {threads} "
                                          f"threads, {dt:.2f} s"}
     del z
+    return out
+
+
+def run_zipf(args, ws, rank, dev, barrier):
+    """--op zipf: the calibrated long-response leg on its own (--zipf-rows
+    rows; 55,296 by default, fewer for a profile)."""
+    out = leg_zipf(args, ws, rank, dev, barrier, None)
+    if rank != 0:
+        return None
+    out.update({"metric": "tokens/s for top-p logprob+entropy on the calibrated long-response rows "
+                          "at V=151936 bf16", "n_gpus": ws, "warmup": args.warmup,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic", "gpu_launches": 2 * out["steps"]})
     return out
 
 
@@ -1093,7 +1107,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "lmhead_backward", "support",
                                                        "support_backward", "backward",
-                                                       "lmhead_topp", "canonical", "sample"],
+                                                       "lmhead_topp", "canonical", "sample", "zipf"],
                     help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused "
                          "LM-head; support: the supplied-support scorer; support_backward: its "
                          "gradient; backward: the dense top-p gradient; lmhead_backward: the "
@@ -1101,12 +1115,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lm-rows", type=int, default=None,
                     help="rows of the LM-head workloads (default 16384; smaller for a profile)")
+    ap.add_argument("--zipf-rows", type=int, default=None,
+                    help="rows of the long-response workloads (default 55296; smaller for a profile)")
     ap.add_argument("--no-legs", action="store_true",
                     help="logits only: skip the long-response, packed GRPO and LM-head legs")
     args = ap.parse_args()
+    global LM_T, ZIPF_ROWS
     if args.lm_rows:
-        global LM_T
         LM_T = int(args.lm_rows)
+    if args.zipf_rows:
+        ZIPF_ROWS = int(args.zipf_rows)
     if args.impl == "reference":
         run_reference(args)
         return
@@ -1132,7 +1150,7 @@ def main():
            "support_backward": lambda *a: run_support(*a, backward=True),
            "backward": run_backward, "lmhead_backward": run_lmhead_backward,
            "lmhead_topp": lambda *a: run_lmhead(*a, top_p=TOP_P),
-           "canonical": run_canonical, "sample": run_sample}[args.op]
+           "canonical": run_canonical, "sample": run_sample, "zipf": run_zipf}[args.op]
     line = run(args, ws, rank, dev, barrier)
     if line is not None:
         print(json.dumps(line), flush=True)
