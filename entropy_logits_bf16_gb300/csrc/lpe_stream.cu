@@ -69,6 +69,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -105,10 +106,13 @@ struct RowParam {
 
 // What the merge warp decides for a row.
 enum : uint32_t { REC_DONE = 0, REC_COUNT = 1, REC_MARK = 2, REC_BAD = 3 };
+constexpr uint32_t MGCAP = 24;    // entries of a row's shared near-zero bin kept (see ck_of)
 struct RowRec {
   uint32_t mode, bad_bit;
   uint32_t zf2;          // window floor, a bf16 value in both halves
   uint32_t key_m, dmax, key_y;
+  uint32_t cz;           // the window crosses zero: bins by compressed key (ck_of)
+  uint32_t ckm, key_lo;  // the max's compressed key (bins are ckm - ck); the floor's key
   int32_t y;
   float E, c, U, zy, top_p, row_t;
   float zhi, zlo;        // Z as a double-float
@@ -123,6 +127,8 @@ struct __align__(16) Ctrl {
   unsigned long long floorpub[2];   // merge warp -> compute warps, scan warp: the row's record
   unsigned long long counted[2];    // compute warps -> scan warp: the row's window counted
   unsigned long long hclear[2];     // scan warp -> merge warp: the row's counts consumed
+  uint32_t mgn[2];                  // the shared near-zero bin's entries (may exceed MGCAP)
+  uint32_t mgv[2][MGCAP];           // bf16 value | 1 << 16 for a token taken out again
   RowParam rp[NRP];
   RowRec rec[2];
   uint32_t wkey[2][NWC];
@@ -177,6 +183,71 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 
 __device__ __forceinline__ float value_of_key(uint32_t k) { return bf16_val(okey16_inverse(k)); }
 __device__ __forceinline__ uint32_t key_of(float v) { return okey16(__float_as_uint(v) >> 16); }
+
+// Windows that cross zero.  The bf16 keys between -2^-4 and 2^-4 (bits
+// 0xBD7F .. 0x3D7F, the zeros included) are ~31,000 keys of which a window
+// would need a bin each; such a row's bins are indexed by compressed keys
+// instead: those keys share one bin, MG_LO, and the keys above them move down
+// by MG_W.  The shared bin's tokens differ in value, so its mass and its
+// entropy term are sums over the tokens, kept in fixed point (w 2^40 and
+// -w d 2^36, truncated: exact and independent of the order of the atomics);
+// a crossing inside it cannot be placed by counts and hands the row on.
+constexpr uint32_t MG_LO = 0x4280u, MG_HI = 0xBD7Fu, MG_W = MG_HI - MG_LO;
+constexpr float kFixW = 1099511627776.0f;   // 2^40
+constexpr float kFixU = 68719476736.0f;     // 2^36
+// The code that counts and scans a row comes in two instantiations: CZ for
+// rows whose window crosses zero, and the plain one (keys as they are) for
+// every other row, which thus runs no extra instruction.
+template <bool CZ>
+__device__ __forceinline__ uint32_t ck_of(uint32_t k) {
+  if (!CZ) return k;
+  return k > MG_HI ? k - MG_W : (k >= MG_LO ? MG_LO : k);
+}
+template <bool CZ>
+__device__ __forceinline__ uint32_t raw_of(uint32_t ck) {
+  return (CZ && ck > MG_LO) ? ck + MG_W : ck;
+}
+// An entry of the shared near-zero bin's list: a token (bf16 bits) counted,
+// or (remove) taken out again.
+__device__ __forceinline__ void mg_list(Ctrl& ctl, int sb, uint32_t bits, bool remove) {
+  const uint32_t i = atomicAdd(&ctl.mgn[sb], 1u);
+  if (i < MGCAP) ctl.mgv[sb][i] = bits | (remove ? 0x10000u : 0u);
+}
+
+// Counts one window token (bf16 bits) into the bins of buffer sb; a token of
+// the shared near-zero bin also goes to that bin's list.
+template <bool CZ>
+__device__ __forceinline__ void count_token(uint32_t* hist, uint32_t ckm, uint32_t bits, Ctrl& ctl,
+                                            int sb) {
+  const uint32_t ck = ck_of<CZ>(okey16(bits));
+  atomicAdd(&hist[ckm - ck], 1u);
+  if (CZ && ck == MG_LO) mg_list(ctl, sb, bits, false);
+}
+
+// The shared bin's mass and entropy term, sum w and sum w d over its listed
+// tokens (less those taken out again), summed by one warp in fixed point
+// (w 2^40, -w d 2^36, truncated: exact in any order, modulo 2^64).
+__device__ __forceinline__ void mg_sums(const Ctrl& ctl, int sb, int lane, float c, float E,
+                                        float& mass, float& um) {
+  const uint32_t n = ctl.mgn[sb] < MGCAP ? ctl.mgn[sb] : MGCAP;
+  unsigned long long sw = 0ull, su = 0ull;
+  for (uint32_t k = (uint32_t)lane; k < n; k += 32u) {
+    const uint32_t e = ctl.mgv[sb][k];
+    const float d = __fmaf_rn(bf16_val(e & 0xFFFFu), c, -E);   // < 0: m >= 2^-4 > |v|
+    const float w = ex2(d);
+    const unsigned long long fw = __float2ull_rz(__fmul_rn(w, kFixW));
+    const unsigned long long fu = __float2ull_rz(__fmul_rn(__fmul_rn(w, -d), kFixU));
+    sw += (e >> 16) ? 0ull - fw : fw;
+    su += (e >> 16) ? 0ull - fu : fu;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sw += __shfl_xor_sync(0xFFFFFFFFu, sw, o);
+    su += __shfl_xor_sync(0xFFFFFFFFu, su, o);
+  }
+  mass = (float)((double)sw * (1.0 / 1099511627776.0));
+  um = -(float)((double)su * (1.0 / 68719476736.0));
+}
 
 // The running state of one compute thread for one row.
 struct Acc {
@@ -348,17 +419,26 @@ struct ScanOut {
 // first), Z_S and the entropy numerator.  Lane l owns the contiguous bins
 // [l b, (l+1) b).  Returns false (on every lane) when the window's mass falls
 // short; else the results are valid on every lane.
+template <bool CZ>
 __device__ bool warp_scan_window(int lane, uint32_t dmax, uint32_t key_m, float c, float E,
                                  DF target, const uint32_t* hist, uint32_t key_y, uint32_t tie_y,
-                                 ScanOut& out) {
+                                 ScanOut& out, float mg_mass = 0.f, float mg_um = 0.f) {
+  // key_m: the max's key, compressed when cz (bin d holds compressed key key_m - d)
   const uint32_t bpl = (dmax + 32u) / 32u;
   const uint32_t d0 = (uint32_t)lane * bpl;
+  // the shared near-zero bin (its mass and entropy term given, as fp32)
+  const uint32_t d_mg = CZ ? key_m - MG_LO : 0xFFFFFFFFu;
   auto bin = [&](uint32_t d, uint32_t& nb, float& mass, float& um, float& wv, float& dv) {
     nb = 0u; mass = 0.f; um = 0.f; wv = 0.f; dv = 0.f;
     if (d > dmax) return;
     nb = hist[d];
     if (nb == 0u) return;
-    dv = __fmaf_rn(value_of_key(key_m - d), c, -E);
+    if (CZ && d == d_mg) {
+      mass = mg_mass;
+      um = mg_um;
+      return;
+    }
+    dv = __fmaf_rn(value_of_key(raw_of<CZ>(key_m - d)), c, -E);
     wv = ex2(dv);
     mass = __fmul_rn((float)nb, wv);
     um = __fmul_rn(mass, dv);
@@ -411,6 +491,8 @@ __device__ bool warp_scan_window(int lane, uint32_t dmax, uint32_t key_m, float 
   const uint32_t bal = __ballot_sync(0xFFFFFFFFu, my_d >= 0);
   if (bal == 0u) return false;
   const int win = __ffs(bal) - 1;   // the lowest lane holds the lowest crossing bin
+  // a crossing inside the shared near-zero bin needs its tokens' order
+  if (CZ && (uint32_t)__shfl_sync(0xFFFFFFFFu, my_d, win) == d_mg) return false;
   uint32_t kstar = 0u, ties = 0u;
   int y_in = 0;
   float lz = 0.f, h = 0.f;
@@ -421,7 +503,7 @@ __device__ bool warp_scan_window(int lane, uint32_t dmax, uint32_t key_m, float 
     const float wn = __fmul_rn((float)cneed, wt);
     const DF zs = df_add_f(pb, wn);
     const float us = __fmaf_rn(wn, dt, ub);
-    const uint32_t d_y = key_m - key_y;
+    const uint32_t d_y = key_m - ck_of<CZ>(key_y);
     kstar = cb + cneed;
     ties = cneed == nt ? kTiesAll : cneed;
     y_in = (d_y < (uint32_t)my_d) || (d_y == (uint32_t)my_d && tie_y < cneed);
@@ -431,7 +513,7 @@ __device__ bool warp_scan_window(int lane, uint32_t dmax, uint32_t key_m, float 
   }
   out.kstar = __shfl_sync(0xFFFFFFFFu, kstar, win);
   out.ties = __shfl_sync(0xFFFFFFFFu, ties, win);
-  out.key_thr = key_m - (uint32_t)__shfl_sync(0xFFFFFFFFu, my_d, win);
+  out.key_thr = raw_of<CZ>(key_m - (uint32_t)__shfl_sync(0xFFFFFFFFu, my_d, win));
   out.y_in = __shfl_sync(0xFFFFFFFFu, y_in, win) != 0;
   out.lz = __shfl_sync(0xFFFFFFFFu, lz, win);
   out.h = __shfl_sync(0xFFFFFFFFu, h, win);
@@ -479,9 +561,10 @@ __device__ __forceinline__ bool wait_full_warp(uint32_t bar, uint32_t parity, vo
 // bf16 value in both halves) into hist (bins below key_m); ny receives how
 // many carry key_y.  The unit is read again (whole with two 16-byte loads from
 // a 16-byte aligned row, else with scalar loads; absent logits read as -inf).
+template <bool CZ>
 __device__ __forceinline__ void count_unit(const uint16_t* row, int64_t V, int u, bool aligned_full,
                                            uint32_t zf2w, uint32_t key_m, uint32_t key_y,
-                                           uint32_t* hist, uint32_t& ny) {
+                                           uint32_t* hist, uint32_t& ny, Ctrl& ctl, int sb) {
   uint32_t w[8];
   if (aligned_full) {
     const uint4* q = reinterpret_cast<const uint4*>(row) + 2 * u;
@@ -499,9 +582,9 @@ __device__ __forceinline__ void count_unit(const uint16_t* row, int64_t V, int u
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
       if ((hm >> (16 * hf)) & 1u) {
-        const uint32_t kk = okey16((w[k] >> (16 * hf)) & 0xFFFFu);
-        atomicAdd(&hist[key_m - kk], 1u);
-        ny += kk == key_y ? 1u : 0u;
+        const uint32_t bits = (w[k] >> (16 * hf)) & 0xFFFFu;
+        count_token<CZ>(hist, key_m, bits, ctl, sb);
+        ny += okey16(bits) == key_y ? 1u : 0u;
       }
     }
   }
@@ -513,9 +596,10 @@ __device__ __forceinline__ void count_unit(const uint16_t* row, int64_t V, int u
 // loads; absent logits beyond V read as -inf) and adds its other tokens whose
 // key reaches the one of kv (a bf16 value in both halves).  Returns how many
 // were added; ny receives how many of them carry key_y.
+template <bool CZ>
 __device__ __forceinline__ uint32_t recount_unit(const uint16_t* row, int64_t V, int u, bool aligned_full,
                                                  uint32_t kv2w, uint32_t key_m, uint32_t key_y,
-                                                 uint32_t* hist, uint32_t& ny) {
+                                                 uint32_t* hist, uint32_t& ny, Ctrl& ctl, int sb) {
   uint32_t w[8];
   if (aligned_full) {
     const uint4* q = reinterpret_cast<const uint4*>(row) + 2 * u;
@@ -543,17 +627,19 @@ __device__ __forceinline__ uint32_t recount_unit(const uint16_t* row, int64_t V,
         m2 = fmaxf(m2, f);
       }
       if ((hm >> (16 * hf)) & 1u) {
-        const uint32_t kk = okey16(bits);
-        atomicAdd(&hist[key_m - kk], 1u);
+        count_token<CZ>(hist, key_m, bits, ctl, sb);
         ++n;
-        ny += kk == key_y ? 1u : 0u;
+        ny += okey16(bits) == key_y ? 1u : 0u;
       }
     }
   }
   // the two largest were counted from the sketch
   const uint32_t k1 = key_of(m1), k2 = key_of(m2);
-  atomicAdd(&hist[key_m - k1], 0xFFFFFFFFu);
-  atomicAdd(&hist[key_m - k2], 0xFFFFFFFFu);
+  const uint32_t c1 = ck_of<CZ>(k1), c2 = ck_of<CZ>(k2);
+  atomicAdd(&hist[key_m - c1], 0xFFFFFFFFu);
+  atomicAdd(&hist[key_m - c2], 0xFFFFFFFFu);
+  if (CZ && c1 == MG_LO) mg_list(ctl, sb, __float_as_uint(m1) >> 16, true);
+  if (CZ && c2 == MG_LO) mg_list(ctl, sb, __float_as_uint(m2) >> 16, true);
   ny -= (k1 == key_y ? 1u : 0u) + (k2 == key_y ? 1u : 0u);
   return n - 2u;
 }
@@ -583,6 +669,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       mbar_init(smem_u32(&ctl.hclear[b]), 1u);
       ctl.tie[b] = 0u;
       ctl.lcnt[b] = 0u;
+      ctl.mgn[b] = 0u;
     }
     ctl.abort = 0;
     fence_mbar_init();
@@ -615,83 +702,88 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       ready = __shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0) != 0;
       uint32_t tie = 0u;
       if (ready && ctl.rec[sb].mode == REC_COUNT && !*abort) {
-        const uint32_t zf2w = ctl.rec[sb].zf2;
-        const __nv_bfloat162 zf2 = bf2(zf2w);
-        const uint32_t key_m = ctl.rec[sb].key_m, key_y = ctl.rec[sb].key_y;
-        const int uy = ctl.rec[sb].y >> 4;
-        uint32_t* hist = hist0 + sb * HBC;
-        const uint32_t* sk = reinterpret_cast<const uint32_t*>(skb + (size_t)sb * g.skb);
-        uint32_t sm = 0u, cm = 0u;   // bit j: unit t + j NTC holds one / several window tokens
+        auto count_row = [&](auto czc) {
+          constexpr bool CZ = decltype(czc)::value;
+            const uint32_t zf2w = ctl.rec[sb].zf2;
+            const __nv_bfloat162 zf2 = bf2(zf2w);
+            const uint32_t key_m = ctl.rec[sb].ckm, key_y = ctl.rec[sb].key_y;   // key_m compressed
+            const int uy = ctl.rec[sb].y >> 4;
+            uint32_t* hist = hist0 + sb * HBC;
+            const uint32_t* sk = reinterpret_cast<const uint32_t*>(skb + (size_t)sb * g.skb);
+            uint32_t sm = 0u, cm = 0u;   // bit j: unit t + j NTC holds one / several window tokens
 #pragma unroll
-        for (int j = 0; j < NSTM; ++j) {
-          const int u = t + j * NTC;
-          if (u < g.nunits) {
-            const uint32_t mk = __hge2_mask(bf2(sk[u]), zf2);
-            if ((mk & 1u) && u != uy) {
-              if (mk >> 16) cm |= 1u << j;
-              else sm |= 1u << j;
-            }
-          }
-        }
-        // Candidates are handed out warp-densely, one per lane and round:
-        // candidate k of the warp belongs to the lane whose inclusive count
-        // first exceeds k, as that lane's (k - exclusive count)-th set bit.
-        const int ns = __popc(sm), nc = __popc(cm);
-        int is = ns, ic = nc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int vs = __shfl_up_sync(0xFFFFFFFFu, is, o), vc = __shfl_up_sync(0xFFFFFFFFu, ic, o);
-          if (lane >= o) { is += vs; ic += vc; }
-        }
-        const int tot_s = __shfl_sync(0xFFFFFFFFu, is, 31), tot_c = __shfl_sync(0xFFFFFFFFu, ic, 31);
-        auto pick = [&](int k, int incl, int n, uint32_t mask) -> int {   // the unit, or -1
-          int L = 0;
-#pragma unroll
-          for (int st = 16; st > 0; st >>= 1) {
-            const int v = __shfl_sync(0xFFFFFFFFu, incl, L + st - 1);
-            if (v <= k) L += st;
-          }
-          const int x = __shfl_sync(0xFFFFFFFFu, incl - n, L);
-          const uint32_t mL = __shfl_sync(0xFFFFFFFFu, mask, L);
-          if (L > 31) return -1;
-          const int j = (int)__fns(mL, 0u, k - x + 1);
-          return warp * 32 + L + j * NTC;
-        };
-        for (int k0 = 0; k0 < tot_s; k0 += 32) {
-          const int k = k0 + lane;
-          const int u = pick(k, is, ns, sm);
-          if (k < tot_s) {
-            const uint32_t kk = okey16(sk[u] & 0xFFFFu);
-            atomicAdd(&hist[key_m - kk], 1u);
-            tie += (kk == key_y && u < uy) ? 1u : 0u;
-          }
-        }
-        if (tot_c) {
-          uint32_t base = 0u;
-          if (lane == 0) base = atomicAdd(&ctl.lcnt[sb], (uint32_t)tot_c);
-          base = __shfl_sync(0xFFFFFFFFu, base, 0);
-          uint32_t* lst = reinterpret_cast<uint32_t*>(smem + g.off_list) + sb * LCAP;
-          const uint16_t* srow = logits + (int64_t)(blockIdx.x + (int64_t)rs * gridDim.x) * a.ld;
-          for (int k0 = 0; k0 < tot_c; k0 += 32) {
-            const int k = k0 + lane;
-            const int u = pick(k, ic, nc, cm);
-            if (k < tot_c) {
-              const uint32_t idx = base + (uint32_t)k;
-              if (idx < LCAP) {
-                const uint32_t e = sk[u];
-                const uint32_t kg = okey16(e & 0xFFFFu), k2 = okey16(e >> 16);
-                atomicAdd(&hist[key_m - kg], 1u);
-                atomicAdd(&hist[key_m - k2], 1u);
-                if (u < uy) tie += (kg == key_y ? 1u : 0u) + (k2 == key_y ? 1u : 0u);
-                lst[idx] = (uint32_t)u | (e & 0xFFFF0000u);
-              } else {   // no room in the list: counted whole here
-                uint32_t ny;
-                count_unit(srow, a.V, u, TMA && u < g.nfull, zf2w, key_m, key_y, hist, ny);
-                if (u < uy) tie += ny;
+            for (int j = 0; j < NSTM; ++j) {
+              const int u = t + j * NTC;
+              if (u < g.nunits) {
+                const uint32_t mk = __hge2_mask(bf2(sk[u]), zf2);
+                if ((mk & 1u) && u != uy) {
+                  if (mk >> 16) cm |= 1u << j;
+                  else sm |= 1u << j;
+                }
               }
             }
-          }
-        }
+            // Candidates are handed out warp-densely, one per lane and round:
+            // candidate k of the warp belongs to the lane whose inclusive count
+            // first exceeds k, as that lane's (k - exclusive count)-th set bit.
+            const int ns = __popc(sm), nc = __popc(cm);
+            int is = ns, ic = nc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int vs = __shfl_up_sync(0xFFFFFFFFu, is, o), vc = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+              if (lane >= o) { is += vs; ic += vc; }
+            }
+            const int tot_s = __shfl_sync(0xFFFFFFFFu, is, 31), tot_c = __shfl_sync(0xFFFFFFFFu, ic, 31);
+            auto pick = [&](int k, int incl, int n, uint32_t mask) -> int {   // the unit, or -1
+              int L = 0;
+#pragma unroll
+              for (int st = 16; st > 0; st >>= 1) {
+                const int v = __shfl_sync(0xFFFFFFFFu, incl, L + st - 1);
+                if (v <= k) L += st;
+              }
+              const int x = __shfl_sync(0xFFFFFFFFu, incl - n, L);
+              const uint32_t mL = __shfl_sync(0xFFFFFFFFu, mask, L);
+              if (L > 31) return -1;
+              const int j = (int)__fns(mL, 0u, k - x + 1);
+              return warp * 32 + L + j * NTC;
+            };
+            for (int k0 = 0; k0 < tot_s; k0 += 32) {
+              const int k = k0 + lane;
+              const int u = pick(k, is, ns, sm);
+              if (k < tot_s) {
+                const uint32_t kk = okey16(sk[u] & 0xFFFFu);
+                count_token<CZ>(hist, key_m, sk[u] & 0xFFFFu, ctl, sb);
+                tie += (kk == key_y && u < uy) ? 1u : 0u;
+              }
+            }
+            if (tot_c) {
+              uint32_t base = 0u;
+              if (lane == 0) base = atomicAdd(&ctl.lcnt[sb], (uint32_t)tot_c);
+              base = __shfl_sync(0xFFFFFFFFu, base, 0);
+              uint32_t* lst = reinterpret_cast<uint32_t*>(smem + g.off_list) + sb * LCAP;
+              const uint16_t* srow = logits + (int64_t)(blockIdx.x + (int64_t)rs * gridDim.x) * a.ld;
+              for (int k0 = 0; k0 < tot_c; k0 += 32) {
+                const int k = k0 + lane;
+                const int u = pick(k, ic, nc, cm);
+                if (k < tot_c) {
+                  const uint32_t idx = base + (uint32_t)k;
+                  if (idx < LCAP) {
+                    const uint32_t e = sk[u];
+                    const uint32_t kg = okey16(e & 0xFFFFu), k2 = okey16(e >> 16);
+                    count_token<CZ>(hist, key_m, e & 0xFFFFu, ctl, sb);
+                    count_token<CZ>(hist, key_m, e >> 16, ctl, sb);
+                    if (u < uy) tie += (kg == key_y ? 1u : 0u) + (k2 == key_y ? 1u : 0u);
+                    lst[idx] = (uint32_t)u | (e & 0xFFFF0000u);
+                  } else {   // no room in the list: counted whole here
+                    uint32_t ny;
+                    count_unit<CZ>(srow, a.V, u, TMA && u < g.nfull, zf2w, key_m, key_y, hist, ny, ctl, sb);
+                    if (u < uy) tie += ny;
+                  }
+                }
+              }
+            }
+        };
+        if (ctl.rec[sb].cz) count_row(std::true_type{});
+        else count_row(std::false_type{});
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) tie += __shfl_down_sync(0xFFFFFFFFu, tie, o);
@@ -920,7 +1012,14 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
           const uint32_t key_m = key_of(m);
           const uint32_t kl = key_of(zlo);
           const uint32_t key_lo = kl > 0u ? kl - 1u : 0u;
-          const uint32_t dmax = key_m - key_lo;
+          uint32_t dmax = key_m - key_lo;
+          uint32_t cz = 0u, ckm = key_m;
+          if (key_lo <= key_m && dmax >= (uint32_t)HBC && key_m > MG_HI && key_lo <= MG_HI) {
+            // the window crosses the near-zero keys: bins by compressed key
+            cz = 1u;
+            ckm = key_m - MG_W;
+            dmax = ckm - ck_of<true>(key_lo);
+          }
           if (key_lo <= key_m && dmax < (uint32_t)HBC) {
             rc.mode = REC_COUNT;
             const uint32_t fb = okey16_inverse(key_lo);
@@ -928,6 +1027,9 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
             rc.key_m = key_m;
             rc.dmax = dmax;
             rc.key_y = key_of(zy);
+            rc.cz = cz;
+            rc.ckm = ckm;
+            rc.key_lo = key_lo;
           } else {
             rc.mode = REC_MARK;
           }
@@ -982,79 +1084,90 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
       } else if (rc.mode == REC_MARK) {
         if (lane == 0) a.out_logprob[r] = __uint_as_float(kRecomputeMark);
       } else {
-        // The counts so far are exact for every token but the third and
-        // later largest of the listed units.  A first scan on them bounds the
-        // crossing from below; the listed units whose second largest logit
-        // reaches that bound are read again and their other tokens above it
-        // added; a second scan then sees exact counts above the bound.
-        const DF Z{rc.zhi, rc.zlo};
-        const DF target = df_mul_f(Z, rc.top_p);
-        uint32_t ty = 0u;
-        if (lane < UNIT && bf16_lo(ybits) >= bf16_lo(rc.zf2)) {
-          const uint32_t kk = okey16(ybits);
-          atomicAdd(&hist[rc.key_m - kk], 1u);
-          ty = (kk == rc.key_y && ypos < rc.y) ? 1u : 0u;
-        }
+        auto scan_row = [&](auto czc) {
+          constexpr bool CZ = decltype(czc)::value;
+            // The counts so far are exact for every token but the third and
+            // later largest of the listed units.  A first scan on them bounds the
+            // crossing from below; the listed units whose second largest logit
+            // reaches that bound are read again and their other tokens above it
+            // added; a second scan then sees exact counts above the bound.
+            const DF Z{rc.zhi, rc.zlo};
+            const DF target = df_mul_f(Z, rc.top_p);
+            uint32_t ty = 0u;
+            if (lane < UNIT && bf16_lo(ybits) >= bf16_lo(rc.zf2)) {
+              const uint32_t kk = okey16(ybits);
+              count_token<CZ>(hist, rc.ckm, ybits, ctl, b);
+              ty = (kk == rc.key_y && ypos < rc.y) ? 1u : 0u;
+            }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ty += __shfl_xor_sync(0xFFFFFFFFu, ty, o);
-        uint32_t tie_all = ctl.tie[b] + ty;
-        __syncwarp();
-        ScanOut so{};
-        bool found = warp_scan_window(lane, rc.dmax, rc.key_m, rc.c, rc.E, target, hist, rc.key_y,
-                                      tie_all, so);
-        // (units beyond the list's room were counted whole by the compute warps)
-        const uint32_t ncx = ctl.lcnt[b] < LCAP ? ctl.lcnt[b] : LCAP;
-        if (ncx > 0u) {
-          const uint32_t kap = found ? so.key_thr : rc.key_m - rc.dmax;
-          const uint32_t kvb = okey16_inverse(kap);
-          const uint32_t* lst = reinterpret_cast<const uint32_t*>(smem + g.off_list) + b * LCAP;
-          const int uy = rc.y >> 4;
-          uint32_t* lstw = reinterpret_cast<uint32_t*>(smem + g.off_list) + b * LCAP;
-          // keep the listed units whose second largest reaches kap (in place, in order)
-          uint32_t nneed = 0u;
-          for (uint32_t k0 = 0u; k0 < ncx; k0 += 32u) {
-            const uint32_t k = k0 + (uint32_t)lane;
-            const uint32_t item = k < ncx ? lst[k] : 0u;
-            const bool need = k < ncx && okey16(item >> 16) >= kap;
-            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, need);
+            for (int o = 16; o > 0; o >>= 1) ty += __shfl_xor_sync(0xFFFFFFFFu, ty, o);
+            uint32_t tie_all = ctl.tie[b] + ty;
             __syncwarp();
-            if (need) lstw[nneed + __popc(bal & ((1u << lane) - 1u))] = item;
-            nneed += __popc(bal);
-          }
-          __syncwarp();
-          uint32_t added = 0u, tx = 0u;
-          for (uint32_t k = (uint32_t)lane; k < nneed; k += 32u) {
-            const uint32_t item = lstw[k];
-            const int u = (int)(item & 0xFFFFu);
-            uint32_t ny;
-            added += recount_unit(row, a.V, u, TMA && u < g.nfull, kvb | (kvb << 16), rc.key_m,
-                                  rc.key_y, hist, ny);
-            if (u < uy) tx += ny;
-          }
-          if (__any_sync(0xFFFFFFFFu, added != 0u)) {
+            ScanOut so{};
+            float mg_mass = 0.f, mg_um = 0.f;
+            if (CZ) mg_sums(ctl, b, lane, rc.c, rc.E, mg_mass, mg_um);
+            bool found = warp_scan_window<CZ>(lane, rc.dmax, rc.ckm, rc.c, rc.E, target, hist, rc.key_y,
+                                          tie_all, so, mg_mass, mg_um);
+            // (units beyond the list's room were counted whole by the compute warps)
+            const uint32_t ncx = ctl.lcnt[b] < LCAP ? ctl.lcnt[b] : LCAP;
+            if (ncx > 0u) {
+              const uint32_t kap = found ? so.key_thr : rc.key_lo;
+              const uint32_t kvb = okey16_inverse(kap);
+              const uint32_t* lst = reinterpret_cast<const uint32_t*>(smem + g.off_list) + b * LCAP;
+              const int uy = rc.y >> 4;
+              uint32_t* lstw = reinterpret_cast<uint32_t*>(smem + g.off_list) + b * LCAP;
+              // keep the listed units whose second largest reaches kap (in place, in order)
+              uint32_t nneed = 0u;
+              for (uint32_t k0 = 0u; k0 < ncx; k0 += 32u) {
+                const uint32_t k = k0 + (uint32_t)lane;
+                const uint32_t item = k < ncx ? lst[k] : 0u;
+                const bool need = k < ncx && okey16(item >> 16) >= kap;
+                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, need);
+                __syncwarp();
+                if (need) lstw[nneed + __popc(bal & ((1u << lane) - 1u))] = item;
+                nneed += __popc(bal);
+              }
+              __syncwarp();
+              uint32_t added = 0u, tx = 0u;
+              for (uint32_t k = (uint32_t)lane; k < nneed; k += 32u) {
+                const uint32_t item = lstw[k];
+                const int u = (int)(item & 0xFFFFu);
+                uint32_t ny;
+                added += recount_unit<CZ>(row, a.V, u, TMA && u < g.nfull, kvb | (kvb << 16), rc.ckm,
+                                      rc.key_y, hist, ny, ctl, b);
+                if (u < uy) tx += ny;
+              }
+              if (__any_sync(0xFFFFFFFFu, added != 0u)) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) tx += __shfl_xor_sync(0xFFFFFFFFu, tx, o);
-            tie_all += tx;
-            __syncwarp();
-            found = warp_scan_window(lane, rc.dmax, rc.key_m, rc.c, rc.E, target, hist, rc.key_y,
-                                     tie_all, so);
-          }
-        }
-        if (lane == 0) {
-          if (!found) {
-            a.out_logprob[r] = __uint_as_float(kRecomputeMark);
-          } else {
-            a.out_logprob[r] = so.y_in
-                                   ? __fsub_rn(__fmul_rn(kLn2, __fmaf_rn(rc.zy, rc.c, -rc.E)), so.lz)
-                                   : -INFINITY;
-            a.out_entropy[r] = so.h;
-            if (a.out_k) a.out_k[r] = (int32_t)so.kstar;
-            if (a.state)
-              a.state[r] = RowState{rc.E, so.lz, so.h, so.key_thr, so.ties,
-                                    kStateValid | (so.y_in ? kStateYIn : 0u), (int32_t)so.kstar,
-                                    rc.row_t};
-          }
-        }
+                for (int o = 16; o > 0; o >>= 1) tx += __shfl_xor_sync(0xFFFFFFFFu, tx, o);
+                tie_all += tx;
+                __syncwarp();
+                __syncwarp();
+                if (CZ) mg_sums(ctl, b, lane, rc.c, rc.E, mg_mass, mg_um);
+                found = warp_scan_window<CZ>(lane, rc.dmax, rc.ckm, rc.c, rc.E, target, hist, rc.key_y,
+                                         tie_all, so, mg_mass, mg_um);
+              }
+            }
+            // a shared near-zero bin whose list ran out of room has no exact mass
+            if (CZ && ctl.mgn[b] > MGCAP) found = false;
+            if (lane == 0) {
+              if (!found) {
+                a.out_logprob[r] = __uint_as_float(kRecomputeMark);
+              } else {
+                a.out_logprob[r] = so.y_in
+                                       ? __fsub_rn(__fmul_rn(kLn2, __fmaf_rn(rc.zy, rc.c, -rc.E)), so.lz)
+                                       : -INFINITY;
+                a.out_entropy[r] = so.h;
+                if (a.out_k) a.out_k[r] = (int32_t)so.kstar;
+                if (a.state)
+                  a.state[r] = RowState{rc.E, so.lz, so.h, so.key_thr, so.ties,
+                                        kStateValid | (so.y_in ? kStateYIn : 0u), (int32_t)so.kstar,
+                                        rc.row_t};
+              }
+            }
+        };
+        if (rc.cz) scan_row(std::true_type{});
+        else scan_row(std::false_type{});
       }
       if (TOPP && rc.mode == REC_COUNT) {
         __syncwarp();
@@ -1062,6 +1175,7 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
         if (lane == 0) {
           ctl.tie[b] = 0u;
           ctl.lcnt[b] = 0u;
+          ctl.mgn[b] = 0u;
         }
       }
       __syncwarp();
