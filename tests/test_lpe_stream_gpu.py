@@ -121,3 +121,40 @@ def test_stream_bad_rows(cuda_lib):
         assert np.all(np.isnan(lp[1:7])) and np.all(np.isnan(ent[1:7]))
         assert np.all(k[1:7] == 0)
         assert int(st.item()) == (cuda_lib.STATUS_BAD_TOKEN_ID | cuda_lib.STATUS_NONFINITE)
+
+
+@pytest.mark.parametrize("p", [0.9, 0.95])
+def test_stream_windows_across_zero(cuda_lib, oracle, p):
+    """Rows whose window z >= m - L T crosses zero.  The long-response rows
+    (Zipf-tilted means) are counted by the streaming kernel itself with
+    compressed keys (the values within 2^-4 of zero share one bin summed in
+    fixed point): at least four in five of them must not be handed on.  Rows
+    whose boundary falls inside that shared bin (a tie group at 0.01, at -0.03)
+    and rows with more near-zero tokens than its list holds must be handed on,
+    and every row must match the oracle."""
+    V = workloads.VOCAB
+    z, _ = workloads.zipf_bf16(256, seed=9, kappa=workloads.ZIPF_KAPPA_CALIBRATED,
+                               sigma=workloads.ZIPF_SIGMA)
+    z = z.float()
+    g = torch.Generator().manual_seed(10)
+    for r, v in ((0, 0.01), (1, -0.03)):   # boundaries inside the shared bin
+        z[r] = torch.randn(V, generator=g) - 12.0
+        z[r, :3] = 2.0
+        z[r, 1000:1400] = v
+    z[2] = torch.randn(V, generator=g) * 0.02 - 30.0   # far below, and ...
+    z[2, :500] = torch.randn(500, generator=g) * 0.03  # ... 500 tokens near zero
+    z[2, 600] = 1.0
+    z = z.to(torch.bfloat16).cuda()
+    hz = workloads.bf16_bits(z)
+    ids_h = oracle.sample_ids(hz, 0.7, p, workloads.uniforms(256, 12))
+    ids = torch.from_numpy(ids_h).cuda()
+    st = cuda_lib.new_row_state(256, z.device)
+    lp, ent, k = cuda_lib.logprob_entropy(z, ids, 0.7, p, return_nucleus_size=True, row_state=st)
+    torch.cuda.synchronize()
+    compare_rows(oracle, hz, ids_h, 0.7, p, lp.cpu().numpy(), ent.cpu().numpy(), k.cpu().numpy(),
+                 label=f"across zero p{p}")
+    # the streaming kernel's reference exponent is an integer, the per-row kernel's is not
+    E = st[:, 0].contiguous().view(torch.float32).cpu().numpy()
+    streamed = E == np.floor(E)
+    assert streamed[3:].mean() >= 0.8, streamed[3:].mean()
+    assert not streamed[:2].any()
