@@ -773,7 +773,10 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
                     count_token<CZ>(hist, key_m, e >> 16, ctl, sb);
                     if (u < uy) tie += (kg == key_y ? 1u : 0u) + (k2 == key_y ? 1u : 0u);
                     lst[idx] = (uint32_t)u | (e & 0xFFFF0000u);
-                  } else {   // no room in the list: counted whole here
+                  } else if (!CZ || *reinterpret_cast<volatile const uint32_t*>(&ctl.mgn[sb]) <= MGCAP) {
+                    // no room in the list: counted whole here (unless the
+                    // shared near-zero bin's list has run out of room: such a
+                    // row is handed on, so its count can stop)
                     uint32_t ny;
                     count_unit<CZ>(srow, a.V, u, TMA && u < g.nfull, zf2w, key_m, key_y, hist, ny, ctl, sb);
                     if (u < uy) tie += ny;
@@ -1105,50 +1108,57 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
             __syncwarp();
             ScanOut so{};
             float mg_mass = 0.f, mg_um = 0.f;
-            if (CZ) mg_sums(ctl, b, lane, rc.c, rc.E, mg_mass, mg_um);
-            bool found = warp_scan_window<CZ>(lane, rc.dmax, rc.ckm, rc.c, rc.E, target, hist, rc.key_y,
-                                          tie_all, so, mg_mass, mg_um);
-            // (units beyond the list's room were counted whole by the compute warps)
-            const uint32_t ncx = ctl.lcnt[b] < LCAP ? ctl.lcnt[b] : LCAP;
-            if (ncx > 0u) {
-              const uint32_t kap = found ? so.key_thr : rc.key_lo;
-              const uint32_t kvb = okey16_inverse(kap);
-              const uint32_t* lst = reinterpret_cast<const uint32_t*>(smem + g.off_list) + b * LCAP;
-              const int uy = rc.y >> 4;
-              uint32_t* lstw = reinterpret_cast<uint32_t*>(smem + g.off_list) + b * LCAP;
-              // keep the listed units whose second largest reaches kap (in place, in order)
-              uint32_t nneed = 0u;
-              for (uint32_t k0 = 0u; k0 < ncx; k0 += 32u) {
-                const uint32_t k = k0 + (uint32_t)lane;
-                const uint32_t item = k < ncx ? lst[k] : 0u;
-                const bool need = k < ncx && okey16(item >> 16) >= kap;
-                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, need);
+            // A shared near-zero bin whose list ran out of room has no exact
+            // mass: the row is handed on without a scan (the compute warps
+            // stopped counting it too).
+            const bool lost = CZ && ctl.mgn[b] > MGCAP;
+            bool found = false;
+            if (!lost) {
+              if (CZ) mg_sums(ctl, b, lane, rc.c, rc.E, mg_mass, mg_um);
+              found = warp_scan_window<CZ>(lane, rc.dmax, rc.ckm, rc.c, rc.E, target, hist, rc.key_y,
+                                           tie_all, so, mg_mass, mg_um);
+              // (units beyond the list's room were counted whole by the compute warps)
+              const uint32_t ncx = ctl.lcnt[b] < LCAP ? ctl.lcnt[b] : LCAP;
+              if (ncx > 0u) {
+                const uint32_t kap = found ? so.key_thr : rc.key_lo;
+                const uint32_t kvb = okey16_inverse(kap);
+                const uint32_t* lst = reinterpret_cast<const uint32_t*>(smem + g.off_list) + b * LCAP;
+                const int uy = rc.y >> 4;
+                uint32_t* lstw = reinterpret_cast<uint32_t*>(smem + g.off_list) + b * LCAP;
+                // keep the listed units whose second largest reaches kap (in place, in order)
+                uint32_t nneed = 0u;
+                for (uint32_t k0 = 0u; k0 < ncx; k0 += 32u) {
+                  const uint32_t k = k0 + (uint32_t)lane;
+                  const uint32_t item = k < ncx ? lst[k] : 0u;
+                  const bool need = k < ncx && okey16(item >> 16) >= kap;
+                  const uint32_t bal = __ballot_sync(0xFFFFFFFFu, need);
+                  __syncwarp();
+                  if (need) lstw[nneed + __popc(bal & ((1u << lane) - 1u))] = item;
+                  nneed += __popc(bal);
+                }
                 __syncwarp();
-                if (need) lstw[nneed + __popc(bal & ((1u << lane) - 1u))] = item;
-                nneed += __popc(bal);
-              }
-              __syncwarp();
-              uint32_t added = 0u, tx = 0u;
-              for (uint32_t k = (uint32_t)lane; k < nneed; k += 32u) {
-                const uint32_t item = lstw[k];
-                const int u = (int)(item & 0xFFFFu);
-                uint32_t ny;
-                added += recount_unit<CZ>(row, a.V, u, TMA && u < g.nfull, kvb | (kvb << 16), rc.ckm,
-                                      rc.key_y, hist, ny, ctl, b);
-                if (u < uy) tx += ny;
-              }
-              if (__any_sync(0xFFFFFFFFu, added != 0u)) {
+                uint32_t added = 0u, tx = 0u;
+                for (uint32_t k = (uint32_t)lane; k < nneed; k += 32u) {
+                  const uint32_t item = lstw[k];
+                  const int u = (int)(item & 0xFFFFu);
+                  uint32_t ny;
+                  added += recount_unit<CZ>(row, a.V, u, TMA && u < g.nfull, kvb | (kvb << 16), rc.ckm,
+                                        rc.key_y, hist, ny, ctl, b);
+                  if (u < uy) tx += ny;
+                }
+                if (__any_sync(0xFFFFFFFFu, added != 0u)) {
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) tx += __shfl_xor_sync(0xFFFFFFFFu, tx, o);
-                tie_all += tx;
-                __syncwarp();
-                __syncwarp();
-                if (CZ) mg_sums(ctl, b, lane, rc.c, rc.E, mg_mass, mg_um);
-                found = warp_scan_window<CZ>(lane, rc.dmax, rc.ckm, rc.c, rc.E, target, hist, rc.key_y,
-                                         tie_all, so, mg_mass, mg_um);
+                  for (int o = 16; o > 0; o >>= 1) tx += __shfl_xor_sync(0xFFFFFFFFu, tx, o);
+                  tie_all += tx;
+                  __syncwarp();
+                  __syncwarp();
+                  if (CZ) mg_sums(ctl, b, lane, rc.c, rc.E, mg_mass, mg_um);
+                  found = warp_scan_window<CZ>(lane, rc.dmax, rc.ckm, rc.c, rc.E, target, hist, rc.key_y,
+                                           tie_all, so, mg_mass, mg_um);
+                }
               }
             }
-            // a shared near-zero bin whose list ran out of room has no exact mass
+            // the second look can fill the shared bin's list too
             if (CZ && ctl.mgn[b] > MGCAP) found = false;
             if (lane == 0) {
               if (!found) {
