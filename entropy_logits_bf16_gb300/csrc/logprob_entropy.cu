@@ -36,7 +36,8 @@
 //     V e^-L < (1 - top_p) Z of the mass -- is counted by a second pass over
 //     the row (an L2 hit) and scanned the same way.  The same pass serves rows
 //     the fast path cannot take (a window touching the near-zero bin, or more
-//     than 65535 counted tokens).  Every path feeds identical bins to the same
+//     than 65535 counted tokens); on rows where a quarter of the groups or
+//     more hold window tokens it counts each thread's groups in place.  Every path feeds identical bins to the same
 //     scan, so the result does not depend on which path ran.
 //   - Rows whose window spans more than the histogram, rows whose threshold
 //     falls in the near-zero bin, and fp32 rows bisect on the value key with
@@ -517,11 +518,72 @@ __device__ __forceinline__ void pass1_packed(const RowBf16& row, int tid, float 
 }
 
 // ------------------------------------------------------------ second pass
+// Counts one window token (bf16 bits): into the distance histogram (bin =
+// ck_m - ck), or, in the near-zero bin, into its fixed-point sums.  Every
+// window pass counts through here, so they all build the same integers.
+__device__ __forceinline__ void count_window_token(uint32_t ck, uint32_t bits, float m, float c,
+                                                   float inv_t, uint32_t ck_m, Smem& sm) {
+  if (ck == MERGE_LO) {
+    const float dd = __fsub_rn(bf16_val(bits), m);
+    const float w = ex2(__fmul_rn(dd, c));
+    atomicAdd(&sm.merged_w, __float2ull_rn(__fmul_rn(w, 1099511627776.0f)));      // 2^40
+    atomicAdd(&sm.merged_u, __float2ull_rn(__fmul_rn(-__fmul_rn(w, __fmul_rn(dd, inv_t)),
+                                                     4294967296.0f)));                  // 2^32
+    atomicAdd(&sm.merged_n, 1u);
+  } else {
+    atomicAdd(&sm.hist.rel[ck_m - ck], 1u);
+  }
+}
+
+// The window pass for rows where a quarter of the groups or more hold window
+// tokens (flat rows, wide nuclei): each thread counts the tokens of its own
+// groups in place, unrolled, without the queue.  Same counts and sums as
+// window_pass (absent tail logits read as -inf, below any window floor).
+__device__ __forceinline__ uint32_t window_pass_dense(const RowBf16& row, int tid, float zlo, float m,
+                                                   float c, float inv_t, uint32_t ck_m,
+                                                   uint32_t key_y, int64_t y, Smem& sm) {
+  const int64_t nfull = row.V / 8;
+  const int64_t ngroups = (row.V + 7) / 8;
+  uint32_t tie = 0;
+  auto group = [&](const uint4 q, int64_t g) {
+    if (group_max(q) < zlo) return;
+    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+    // ids of this group ahead of y: 0..8
+    const int64_t ahead64 = y - g * 8;
+    const int ahead = ahead64 < 0 ? 0 : (ahead64 > 8 ? 8 : (int)ahead64);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t bits = (w4[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+      if (bf16_val(bits) >= zlo) {
+        const uint32_t key = okey16(bits);
+        count_window_token(compress_key(key), bits, m, c, inv_t, ck_m, sm);
+        tie += (key == key_y && k < ahead) ? 1u : 0u;
+      }
+    }
+  };
+  constexpr int B = 4;
+  int64_t g = tid;
+  if (row.aligned) {   // whole batches of full groups: plain vector loads
+    const uint4* base = reinterpret_cast<const uint4*>(row.p);
+    for (; g + (B - 1) * NT < nfull; g += B * NT) {
+      uint4 q[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) q[b] = __ldg(base + g + b * NT);
+#pragma unroll
+      for (int b = 0; b < B; ++b) group(q[b], g + b * NT);
+    }
+  }
+  for (; g < ngroups; g += NT) group(row.packed(g, nfull), g);
+  return tie;
+}
+
 // Counts the tokens with z >= zlo into the distance histogram (bin = ck_m - ck),
-// the near-zero bin into fixed-point sums, and the ties of y ahead of it.
+// the near-zero bin into fixed-point sums, and the ties of y ahead of it
+// (dense: by window_pass_dense).
 __device__ __noinline__ uint32_t window_pass(const RowBf16& row, int tid, float zlo, float m, float c,
                                 float inv_t, uint32_t ck_m, uint32_t key_y, int64_t y,
-                                Smem& sm) {
+                                Smem& sm, bool dense) {
+  if (dense) return window_pass_dense(row, tid, zlo, m, c, inv_t, ck_m, key_y, y, sm);
   const int lane = tid & 31, warp = tid >> 5;
   const int64_t nfull = row.V / 8;
   const int64_t ngroups = (row.V + 7) / 8;
@@ -531,17 +593,7 @@ __device__ __noinline__ uint32_t window_pass(const RowBf16& row, int tid, float 
   auto process = [&](const uint4 q, uint32_t g) {
     for_candidates(q, g, row.V, zlo, [&](uint32_t bits, int64_t i) {
       const uint32_t key = okey16(bits);
-      const uint32_t ck = compress_key(key);
-      if (ck == MERGE_LO) {
-        const float dd = __fsub_rn(bf16_val(bits), m);
-        const float w = ex2(__fmul_rn(dd, c));
-        atomicAdd(&sm.merged_w, __float2ull_rn(__fmul_rn(w, 1099511627776.0f)));      // 2^40
-        atomicAdd(&sm.merged_u, __float2ull_rn(__fmul_rn(-__fmul_rn(w, __fmul_rn(dd, inv_t)),
-                                                         4294967296.0f)));                  // 2^32
-        atomicAdd(&sm.merged_n, 1u);
-      } else {
-        atomicAdd(&sm.hist.rel[ck_m - ck], 1u);
-      }
+      count_window_token(compress_key(key), bits, m, c, inv_t, ck_m, sm);
       if (key == key_y && i < y) ++tie;
     });
   };
@@ -588,17 +640,7 @@ __device__ __forceinline__ uint32_t sketch_pass(const RowBf16& row, int tid, flo
   auto expand = [&](const uint4 q, uint32_t g) {
     for_candidates(q, g, row.V, zlo, [&](uint32_t bits, int64_t i) {
       const uint32_t key = okey16(bits);
-      const uint32_t ck = compress_key(key);
-      if (ck == MERGE_LO) {
-        const float dd = __fsub_rn(bf16_val(bits), m);
-        const float w = ex2(__fmul_rn(dd, c));
-        atomicAdd(&sm.merged_w, __float2ull_rn(__fmul_rn(w, 1099511627776.0f)));      // 2^40
-        atomicAdd(&sm.merged_u, __float2ull_rn(__fmul_rn(-__fmul_rn(w, __fmul_rn(dd, inv_t)),
-                                                         4294967296.0f)));                  // 2^32
-        atomicAdd(&sm.merged_n, 1u);
-      } else {
-        atomicAdd(&sm.hist.rel[ck_m - ck], 1u);
-      }
+      count_window_token(compress_key(key), bits, m, c, inv_t, ck_m, sm);
       if (key == key_y && i < y) ++tie;
     });
   };
@@ -1060,9 +1102,12 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c0, float i
         __syncthreads();
         // The sketch pass lists the candidate groups and reloads only those:
         // worth it while they are sparse.  When a quarter of the groups or
-        // more are candidates (flat rows, wide nuclei) the streaming window
-        // pass is about twice as fast.  Both build the same integer counts.
-        bool use_sketch = (a.V + 8 * NT - 1) / (8 * NT) <= SK_ROUNDS;
+        // more are candidates (flat rows, wide nuclei) the window pass reads
+        // the row whole and counts each thread's groups in place (dense);
+        // rows too long for the sketch take the window pass with its queue.
+        // All three build the same integer counts.
+        const bool has_sketch = (a.V + 8 * NT - 1) / (8 * NT) <= SK_ROUNDS;
+        bool use_sketch = has_sketch;
         if (use_sketch) {
           const int64_t ngroups = (a.V + 7) / 8;
           uint32_t cc[4] = {0u, 0u, 0u, 0u};
@@ -1073,7 +1118,7 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c0, float i
         }
         uint32_t cnt2[4] = {0u, 0u, 0u, 0u};
         cnt2[0] = use_sketch ? sketch_pass(row, tid, zlo, m, c, inv_t, ck_m, key_y, y, sm)
-                             : window_pass(row, tid, zlo, m, c, inv_t, ck_m, key_y, y, sm);
+                             : window_pass(row, tid, zlo, m, c, inv_t, ck_m, key_y, y, sm, has_sketch);
         block_sum_u32(cnt2, sm, tid);  // also the barrier after the histogram
         int dstar;
         const bool found = scan_bins(tid, dmax, d_merged, ck_m, m, c, inv_t, target, sm, dstar);
