@@ -1168,6 +1168,8 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c0, float i
 
 }  // namespace
 
+constexpr int64_t kMarkedRowsPerCta = 8;   // rows per CTA of the recompute pass
+
 cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
   // c = log2(e) / T rounded once; inv_t = 1 / T.
   const float c = (float)(1.4426950408889634 / (double)a.temperature);
@@ -1200,7 +1202,16 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess || !topp) return e;
     LpeArgs b = a;   // rows the streaming kernel marked for recomputation
     b.only_marked = 1;
-    lpe_kernel<RowBf16, true><<<grid, block, smem, stream>>>(b, c, inv_t);
+    // About a CTA for every 8 rows, in whole multiples of the usual grid: a
+    // CTA without marked rows ends at once, so the block scheduler hands the
+    // marked rows to the SMs as they free up, and when every row is marked
+    // the waves stay full.  (With only the usual grid, each CTA taking every
+    // 456th row, a few CTAs got several marked rows and set the launch's
+    // time.)
+    const int64_t waves = (a.T + grid64 * kMarkedRowsPerCta - 1) / (grid64 * kMarkedRowsPerCta);
+    const int64_t rg = grid64 * waves;
+    const dim3 rgrid((unsigned)(rg < 0x7FFFFFFF ? rg : 0x7FFFFFFF));
+    lpe_kernel<RowBf16, true><<<rgrid, block, smem, stream>>>(b, c, inv_t);
     return cudaGetLastError();
   }
   if (a.dtype == 0) {
