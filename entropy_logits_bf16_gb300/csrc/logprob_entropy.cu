@@ -37,8 +37,9 @@
 //     the row (an L2 hit) and scanned the same way.  The same pass serves rows
 //     the fast path cannot take (a window touching the near-zero bin, or more
 //     than 65535 counted tokens); on rows where a quarter of the groups or
-//     more hold window tokens it counts each thread's groups in place.  Every path feeds identical bins to the same
-//     scan, so the result does not depend on which path ran.
+//     more hold window tokens it counts each thread's groups in place.
+//     Every path feeds identical bins to the same scan, so the result does
+//     not depend on which path ran.
 //   - Rows whose window spans more than the histogram, rows whose threshold
 //     falls in the near-zero bin, and fp32 rows bisect on the value key with
 //     fixed-order passes over the row (exact, slower).  This choice depends
