@@ -919,6 +919,50 @@ def run_canonical(args, ws, rank, dev, barrier):
     }
 
 
+CAN_TOPP_METRIC = ("tokens/s for top-p logprob+entropy over the canonical vocabulary partition "
+                   "(virtual TP 8, padded vocabulary 152576) at V=151936 bf16")
+
+
+def run_canonical_topp(args, ws, rank, dev, barrier):
+    """--op canonical_topp: rlk_logprob_entropy_canonical_topp on the benchmark
+    rows at top_p 0.95 -- the eight virtual shards' partials, their window
+    counts per bf16 value (a second read of each shard's logits, after the
+    partials fix the row's max and Z), then the fixed-order combine."""
+    import entropy_logits_bf16_gb300 as rlk
+    stream = torch.cuda.current_stream(dev)
+    z, ids = make_workload(dev, seed=rank_seed(rank))
+
+    def call():
+        rlk.logprob_entropy_canonical_topp(z, ids, TEMPERATURE, TOP_P)
+
+    elapsed_ms, part_ms, clk = timed_steps(args, ws, dev, stream, [call], barrier)
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    n = rlk.CANONICAL_TP
+    # per row: the logits read twice (partials, then the window counts), the id,
+    # the outputs (logprob, entropy, k*), the partials and the window counts
+    # each written once and read once
+    alg = T_ROWS * (2 * VOCAB * 2 + 4 + 12 + 2 * n * 32 + 2 * n * 8224)
+    achieved = alg / (part_ms[0] / 1e3) / 1e9
+    return {
+        "metric": CAN_TOPP_METRIC, "value": whole_job_rate(T_ROWS, args.steps, ws, elapsed_ms),
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_ROWS, "V": VOCAB, "virtual_tp": n,
+                   "padded_vocab": rlk.CANONICAL_VOCAB, "global_batch": T_ROWS * ws,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peak_kind,
+                     "kernel": "shard_partial_kernel + shard_window_kernel + shard_combine_topp_kernel "
+                               "(one rlk_logprob_entropy_canonical_topp call)",
+                     "algorithmic_bytes_per_launch": alg, "launch_ms": part_ms[0]},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+
+
 SMP_METRIC = ("tokens/s for deterministic top-p sampling (inverse CDF over the retained set "
               "in ranking order) at V=151936 bf16")
 
@@ -1107,7 +1151,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--op", default="logits", choices=["logits", "lmhead", "lmhead_backward", "support",
                                                        "support_backward", "backward",
-                                                       "lmhead_topp", "canonical", "sample", "zipf"],
+                                                       "lmhead_topp", "canonical", "canonical_topp", "sample",
+                                                       "zipf"],
                     help="logits: the benchmark (logprob/entropy + loss); lmhead: the fused "
                          "LM-head; support: the supplied-support scorer; support_backward: its "
                          "gradient; backward: the dense top-p gradient; lmhead_backward: the "
@@ -1150,7 +1195,8 @@ def main():
            "support_backward": lambda *a: run_support(*a, backward=True),
            "backward": run_backward, "lmhead_backward": run_lmhead_backward,
            "lmhead_topp": lambda *a: run_lmhead(*a, top_p=TOP_P),
-           "canonical": run_canonical, "sample": run_sample, "zipf": run_zipf}[args.op]
+           "canonical": run_canonical, "canonical_topp": run_canonical_topp,
+           "sample": run_sample, "zipf": run_zipf}[args.op]
     line = run(args, ws, rank, dev, barrier)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -387,13 +387,21 @@ struct Window {
 };
 
 // Every shard and the combine derive the row's window from the gathered
-// partials (merged in shard order), so they all agree on it.
+// partials (merged in shard order), so they all agree on it.  Called by a
+// whole warp: lane k loads shard k's partial (32 at a time) and every lane
+// merges them all in shard order, so each lane returns the same window.
 __device__ Window row_window(const float4* p, int n_all, int64_t T, int64_t r, int64_t V, float c,
-                             float temp, float top_p) {
+                             float temp, float top_p, int lane) {
   Part st{-INFINITY, 0.f, 0.f, 0.f};
-  for (int s = 0; s < n_all; ++s) {
-    const float4 q = p[2 * ((int64_t)s * T + r)];
-    st = part_merge(st, Part{q.x, q.y, q.z, q.w}, c);
+  for (int s0 = 0; s0 < n_all; s0 += 32) {
+    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (s0 + lane < n_all) q = p[2 * ((int64_t)(s0 + lane) * T + r)];
+    const int n = n_all - s0 < 32 ? n_all - s0 : 32;
+    for (int k = 0; k < n; ++k) {
+      const Part b{__shfl_sync(0xFFFFFFFFu, q.x, k), __shfl_sync(0xFFFFFFFFu, q.y, k),
+                   __shfl_sync(0xFFFFFFFFu, q.z, k), __shfl_sync(0xFFFFFFFFu, q.w, k)};
+      st = part_merge(st, b, c);
+    }
   }
   Window w{};
   w.m = st.m;
@@ -417,7 +425,7 @@ __device__ Window row_window(const float4* p, int n_all, int64_t T, int64_t r, i
 }
 
 // One CTA per (row, shard): the shard's window counts.
-__global__ void __launch_bounds__(NTP) shard_window_kernel(ShardWindowArgs a, float c) {
+__global__ void __launch_bounds__(NTP, 8) shard_window_kernel(ShardWindowArgs a, float c) {
   __shared__ uint32_t hist[HBW];
   __shared__ Window win;
   __shared__ float red_hi[NWP], red_lo[NWP], red_u[NWP];
@@ -427,9 +435,11 @@ __global__ void __launch_bounds__(NTP) shard_window_kernel(ShardWindowArgs a, fl
   for (int64_t pr = blockIdx.x; pr < n_pairs; pr += gridDim.x) {
     const int64_t r = pr / a.n_shards;
     const int s = (int)(pr % a.n_shards);
-    if (tid == 0)
-      win = row_window(reinterpret_cast<const float4*>(a.all_partials), a.n_all, a.T, r, a.V, c,
-                       a.temperature, a.top_p);
+    if (warp == 0) {
+      const Window w0 = row_window(reinterpret_cast<const float4*>(a.all_partials), a.n_all, a.T, r,
+                                   a.V, c, a.temperature, a.top_p, lane);
+      if (lane == 0) win = w0;
+    }
     __syncthreads();
     const Window w = win;
     ShardCounts* out = reinterpret_cast<ShardCounts*>(a.counts) + ((int64_t)s * a.T + r);
@@ -462,6 +472,7 @@ __global__ void __launch_bounds__(NTP) shard_window_kernel(ShardWindowArgs a, fl
     DF mz{0.f, 0.f};
     float mu = 0.f;
     uint32_t mn = 0u, tie = 0u;
+    const int64_t ylim = y - a.first_col;   // columns below this one precede y
     auto take = [&](uint32_t bits, int64_t col) {   // one logit in the window
       const uint32_t k = okey16(bits);
       const uint32_t ck = ckey(k);
@@ -474,19 +485,28 @@ __global__ void __launch_bounds__(NTP) shard_window_kernel(ShardWindowArgs a, fl
       } else {
         atomicAdd(&hist[w.ck_m - ck], 1u);
       }
-      tie += (k == key_y && a.first_col + col < y) ? 1u : 0u;
+      tie += (k == key_y && col < ylim) ? 1u : 0u;
     };
     const bool vec = ((reinterpret_cast<uintptr_t>(p + l0)) & 15u) == 0;
     int64_t j = l0 + (int64_t)tid * 8;
     if (vec) {
       for (; j + 8 <= l1; j += (int64_t)NTP * 8) {
         const uint4 q = __ldg(reinterpret_cast<const uint4*>(p + j));
-        const uint32_t v[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t mk = __hge2_mask(bf2(v[i]), f2);
-          if (mk & 0xFFFFu) take(v[i] & 0xFFFFu, j + 2 * i);
-          if (mk >> 16) take(v[i] >> 16, j + 2 * i + 1);
+        // bit k: logit k of the eight reaches the floor (two packed compares a word)
+        uint32_t cand = 0u;
+        cand |= (__hge2_mask(bf2(q.x), f2) & 0x00010001u) * 1u;
+        cand |= (__hge2_mask(bf2(q.y), f2) & 0x00010001u) * 4u;
+        cand |= (__hge2_mask(bf2(q.z), f2) & 0x00010001u) * 16u;
+        cand |= (__hge2_mask(bf2(q.w), f2) & 0x00010001u) * 64u;
+        cand = (cand & 0xFFu) | ((cand >> 15) & 0x1FEu);
+        // the window's logits only, in column order (a loop of each lane's own
+        // length, not a branch per logit that the warp takes for all eight)
+        while (cand) {
+          const int k = __ffs(cand) - 1;
+          cand &= cand - 1u;
+          const int h = k >> 1;
+          const uint32_t wsel = h == 0 ? q.x : (h == 1 ? q.y : (h == 2 ? q.z : q.w));
+          take((wsel >> (16 * (k & 1))) & 0xFFFFu, j + k);
         }
       }
     }
@@ -558,7 +578,7 @@ __global__ void __launch_bounds__(NTP) shard_combine_topp_kernel(ShardCombineArg
     }
   };
   if (y < 0 || y >= a.V) return finish_bad(RLK_STATUS_BAD_TOKEN_ID);
-  const Window w = row_window(P, a.n_shards, a.T, r, a.V, c, a.temperature, a.top_p);
+  const Window w = row_window(P, a.n_shards, a.T, r, a.V, c, a.temperature, a.top_p, lane);
   const int ys = (int)(y / a.shard_width);
   const float4 py = ys < a.n_shards ? P[2 * ((int64_t)ys * a.T + r) + 1] : make_float4(NAN, 0.f, 0.f, 0.f);
   const float zy = py.x;

@@ -17,7 +17,7 @@ import torch
 
 import bench
 import workloads
-from _parity import ENT_TOL, LP_REL, LP_TOL, check_nucleus_sizes
+from _parity import ENT_TOL, LP_REL, LP_TOL, check_nucleus_sizes, compare_rows
 from test_backward_gpu import _check as check_dense_grad
 from test_sampler_gpu import _check as check_draws
 
@@ -120,6 +120,20 @@ def test_canonical_partition_bench_shape(cuda_lib, oracle, batch):
     olp, oent, _, _ = oracle.logprob_entropy(hz, ids.cpu().numpy()[rows], TEMP, 1.0)
     _close(lp.cpu().numpy()[rows].astype(np.float64), ent.cpu().numpy()[rows].astype(np.float64),
            olp, oent, "bench canonical")
+
+
+def test_canonical_topp_bench_shape(cuda_lib, oracle, batch):
+    """--op canonical_topp: top_p 0.95 over the eight virtual shards (partials,
+    window counts, combine) on sampled rows, k* included; rows on both sides
+    of the window kernel's grid-stride boundary (2432 CTAs, a (row, shard)
+    pair each per round: 304 rows)."""
+    z, ids, _, _ = batch
+    lp, ent, k = cuda_lib.logprob_entropy_canonical_topp(z, ids, TEMP, P)
+    torch.cuda.synchronize()
+    rows = _rows(16 * 152 // 8, extra=range(0, T, 257))
+    hz = workloads.bf16_bits(z[torch.from_numpy(rows).cuda()])
+    compare_rows(oracle, hz, ids.cpu().numpy()[rows], TEMP, P, lp.cpu().numpy()[rows],
+                 ent.cpu().numpy()[rows], k.cpu().numpy()[rows], label="bench canonical top-p")
 
 
 @pytest.fixture(scope="module")
