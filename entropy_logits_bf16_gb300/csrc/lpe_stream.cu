@@ -233,7 +233,7 @@ __device__ __forceinline__ void mg_sums(const Ctrl& ctl, int sb, int lane, float
   unsigned long long sw = 0ull, su = 0ull;
   for (uint32_t k = (uint32_t)lane; k < n; k += 32u) {
     const uint32_t e = ctl.mgv[sb][k];
-    const float d = __fmaf_rn(bf16_val(e & 0xFFFFu), c, -E);   // < 0: m >= 2^-4 > |v|
+    const float d = __fmaf_rn(bf16_val(e & 0xFFFFu), c, -E);   // <= 0: E >= m c >= v c
     const float w = ex2(d);
     const unsigned long long fw = __float2ull_rz(__fmul_rn(w, kFixW));
     const unsigned long long fu = __float2ull_rz(__fmul_rn(__fmul_rn(w, -d), kFixU));
@@ -1017,10 +1017,11 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
           const uint32_t key_lo = kl > 0u ? kl - 1u : 0u;
           uint32_t dmax = key_m - key_lo;
           uint32_t cz = 0u, ckm = key_m;
-          if (key_lo <= key_m && dmax >= (uint32_t)HBC && key_m > MG_HI && key_lo <= MG_HI) {
-            // the window crosses the near-zero keys: bins by compressed key
+          if (key_lo <= key_m && dmax >= (uint32_t)HBC && key_m >= MG_LO && key_lo <= MG_HI) {
+            // the window reaches into the near-zero keys (from above them, or
+            // from a max among them): bins by compressed key
             cz = 1u;
-            ckm = key_m - MG_W;
+            ckm = ck_of<true>(key_m);
             dmax = ckm - ck_of<true>(key_lo);
           }
           if (key_lo <= key_m && dmax < (uint32_t)HBC) {

@@ -158,3 +158,49 @@ def test_stream_windows_across_zero(cuda_lib, oracle, p):
     streamed = E == np.floor(E)
     assert streamed[3:].mean() >= 0.8, streamed[3:].mean()
     assert not streamed[:2].any()
+
+
+@pytest.mark.parametrize("p", [0.5, 0.95])
+def test_stream_max_near_zero(cuda_lib, oracle, p):
+    """Rows whose max lies within 2^-4 of zero.  A max just above zero makes
+    the window cross zero from inside the shared near-zero bin: where the
+    boundary lies below that bin the streaming kernel counts the row itself
+    (the bin, max included, summed in fixed point); where the bin holds the
+    boundary it hands the row on.  A max just below zero needs no shared bin
+    (the window does not cross zero).  Every row against the oracle."""
+    V = workloads.VOCAB
+    g = torch.Generator().manual_seed(23)
+    z = torch.randn(12, V, generator=g) - 6.0                 # the bulk, well below the max
+    z[0, 100] = 0.03                                           # max just above zero
+    z[1, 7] = 0.05; z[1, 9] = 0.01; z[1, 11] = -0.02          # a few near-zero tokens at the top
+    z[2, V - 1] = -0.02                                        # max just below zero
+    z[3, 0] = 0.0; z[3, 1] = -0.0; z[3, 2] = 0.001            # zeros of both signs at the top
+    z[4] = torch.randn(V, generator=g) - 20.0                  # the bin holds nearly all the mass:
+    z[4, 1000:1300] = 0.04                                     # the boundary lies in it
+    z[4, 2000:2300] = -0.03
+    z[5] = torch.randn(V, generator=g) * 1.5 - 8.0             # a wider bulk
+    z[5, 50] = 0.06
+    for r in range(6, 12):                                     # tilted like the long-response rows
+        z[r] = -1.2 * torch.log(torch.randperm(V, generator=g).float() + 1.0) + \
+               0.5 * torch.randn(V, generator=g) - 3.0
+        z[r, r * 97] = 0.02 * (r - 8)
+    z = z.to(torch.bfloat16).cuda()
+    hz = workloads.bf16_bits(z)
+    ids_h = oracle.sample_ids(hz, 0.7, p, workloads.uniforms(12, 24))
+    ids_h[0], ids_h[2] = 100, V - 1                            # the max itself selected
+    ids = torch.from_numpy(ids_h).cuda()
+    st = cuda_lib.new_row_state(12, z.device)
+    lp, ent, k = cuda_lib.logprob_entropy(z, ids, 0.7, p, return_nucleus_size=True, row_state=st)
+    torch.cuda.synchronize()
+    compare_rows(oracle, hz, ids_h, 0.7, p, lp.cpu().numpy(), ent.cpu().numpy(), k.cpu().numpy(),
+                 label=f"max near zero p{p}")
+    # the streaming kernel's reference exponent is an integer, the per-row
+    # kernel's is not (row 8, whose max is 0, is left out: both are 0 there)
+    E = st[:, 0].contiguous().view(torch.float32).cpu().numpy()
+    streamed = E == np.floor(E)
+    # streamed: boundaries far below the bin, and the rows whose max is below
+    # zero; handed on: the bin holds the boundary (row 4's tie groups, and the
+    # tilted rows with a positive max that alone is the nucleus)
+    on = [0, 1, 2, 3, 6, 7] + ([5] if p < 0.9 else [])
+    off = [4, 9, 10, 11]
+    assert streamed[on].all() and not streamed[off].any(), streamed
