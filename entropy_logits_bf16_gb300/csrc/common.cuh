@@ -17,6 +17,15 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Programmatic dependent launch.  A kernel launched after another on the same
+// stream with the programmatic-serialization attribute may start while the
+// other is still running: pdl_wait() returns once that grid has completed and
+// its memory is visible (at once when there is no such grid), so it comes
+// before the first read of the other's outputs.  pdl_trigger() lets the next
+// such kernel be scheduled once every CTA of this grid has issued it or ended.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // bf16 halves of a 32-bit word as fp32 (exact widening).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -102,6 +102,8 @@ __device__ __forceinline__ bool seq_range(const LossArgs& a, int s, int64_t& t0,
 }
 
 __global__ void __launch_bounds__(LT) loss_seq_kernel(LossArgs a) {
+  pdl_trigger();
+  pdl_wait();   // the log-probabilities may come from the kernel before
   __shared__ float s_adv;
   __shared__ float s_red[LWARP][NP];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -218,6 +220,8 @@ __device__ void cta_sum_df(DF (&acc)[NV], DF (*s_red)[NV], float (&out)[NV]) {
 // One CTA: fixed-order sums over the sequences' partials, then (the MIS scale
 // being known) over the aggregation units: the batch, sequences or groups.
 __global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
+  pdl_trigger();
+  pdl_wait();   // the sequences' partials
   __shared__ DF s_red1[LWARP][NP];
   __shared__ DF s_red2[LWARP][2];
   __shared__ float s_t[NP];
@@ -290,6 +294,7 @@ __global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
 // Each token's gradient with its weight in the loss, recomputed from the
 // inputs (the weight and the MIS scale are known only after the reduction).
 __global__ void __launch_bounds__(LT) loss_grad_kernel(LossArgs a) {
+  pdl_wait();   // the batch sums
   const float* sc = a.workspace + (int64_t)a.n_seq * NP;
   const bool mis = a.is_method == RLK_IS_MIS;
   for (int s = blockIdx.x; s < a.n_seq; s += gridDim.x) {
@@ -331,10 +336,14 @@ size_t loss_workspace_bytes(int64_t n_seq) {
 cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t stream) {
   const int cap = 8 * sm_count();
   const int grid = a.n_seq < cap ? (a.n_seq > 0 ? a.n_seq : 1) : cap;
-  if (a.n_seq > 0) loss_seq_kernel<<<grid, LT, 0, stream>>>(a);
-  loss_finalize_kernel<<<1, LT, 0, stream>>>(a);
-  if (a.out_grad && a.n_seq > 0) loss_grad_kernel<<<grid, LT, 0, stream>>>(a);
-  return cudaGetLastError();
+  // each launch overlaps the end of the kernel before it (programmatic
+  // dependent launch; every kernel waits for its predecessor's writes)
+  cudaError_t e = cudaSuccess;
+  if (a.n_seq > 0) e = launch_after(loss_seq_kernel, dim3(grid), dim3(LT), 0, stream, a);
+  if (e == cudaSuccess) e = launch_after(loss_finalize_kernel, dim3(1), dim3(LT), 0, stream, a);
+  if (e == cudaSuccess && a.out_grad && a.n_seq > 0)
+    e = launch_after(loss_grad_kernel, dim3(grid), dim3(LT), 0, stream, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace rlk

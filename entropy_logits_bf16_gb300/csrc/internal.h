@@ -194,6 +194,25 @@ int sm_count();
 // callers then redo the work on every call).
 int device_slot();
 
+// Launches kernel k as a programmatic dependent of the previous kernel on the
+// stream: its launch overlaps that kernel's end, and k calls pdl_wait()
+// before it reads anything that kernel wrote.
+template <class... KArgs, class... Args>
+cudaError_t launch_after(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream);
 // Streaming kernel for every bf16 batch of a large vocabulary (lpe_stream.cu).
 // wait_limit: clock cycles a device wait may take; withhold: a debug stage

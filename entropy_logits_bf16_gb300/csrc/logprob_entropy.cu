@@ -954,6 +954,8 @@ __device__ __forceinline__ void write_bad_state(const LpeArgs& a, int64_t r, uin
 // --------------------------------------------------------------- kernel
 template <class Row, bool TOPP>
 __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c0, float inv_t0) {
+  pdl_trigger();
+  pdl_wait();   // as the recompute pass, the streaming kernel's marks and outputs
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
@@ -1212,8 +1214,8 @@ cudaError_t launch_logprob_entropy(const LpeArgs& a, cudaStream_t stream) {
     const int64_t waves = (a.T + grid64 * kMarkedRowsPerCta - 1) / (grid64 * kMarkedRowsPerCta);
     const int64_t rg = grid64 * waves;
     const dim3 rgrid((unsigned)(rg < 0x7FFFFFFF ? rg : 0x7FFFFFFF));
-    lpe_kernel<RowBf16, true><<<rgrid, block, smem, stream>>>(b, c, inv_t);
-    return cudaGetLastError();
+    cudaError_t le = launch_after(lpe_kernel<RowBf16, true>, rgrid, block, smem, stream, b, c, inv_t);
+    return le != cudaSuccess ? le : cudaGetLastError();
   }
   if (a.dtype == 0) {
     if (topp) lpe_kernel<RowBf16, true><<<grid, block, smem, stream>>>(a, c, inv_t);

@@ -647,6 +647,7 @@ __device__ __forceinline__ uint32_t recount_unit(const uint16_t* row, int64_t V,
 // --------------------------------------------------------------- kernel
 template <bool TOPP, bool TMA>
 __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, float c0) {
+  pdl_trigger();   // the recompute pass may be scheduled (it waits for this grid)
   extern __shared__ __align__(128) uint8_t smem[];
   Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem);
   float* part = reinterpret_cast<float*>(smem + g.off_part);         // [2][4][32]: E, S hi, S lo, U
