@@ -8,8 +8,9 @@
 // VIME train-rollout consistency", section "Canonical topology strategy"), so
 // the gradient written here already carries the aggregation weight.
 //
-// Launches (all on the caller's stream, no atomics on floats, no inter-CTA
-// waits, every sum in a fixed order):
+// Launches (all on the caller's stream, each a programmatic dependent of the
+// one before, which it waits for before reading; no atomics on floats, no
+// waits between CTAs of one launch, every sum in a fixed order):
 //  1. seq kernel, one CTA per sequence: the sequence's advantage from its
 //     group's rewards, then per-token terms; per-sequence partial sums (and
 //     the advantage) go to the workspace.
