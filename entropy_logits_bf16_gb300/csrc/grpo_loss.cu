@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(LT) loss_finalize_kernel(LossArgs a) {
 // Each token's gradient with its weight in the loss, recomputed from the
 // inputs (the weight and the MIS scale are known only after the reduction).
 __global__ void __launch_bounds__(LT) loss_grad_kernel(LossArgs a) {
+  pdl_trigger();
   pdl_wait();   // the batch sums
   const float* sc = a.workspace + (int64_t)a.n_seq * NP;
   const bool mis = a.is_method == RLK_IS_MIS;

@@ -648,6 +648,7 @@ __device__ __forceinline__ uint32_t recount_unit(const uint16_t* row, int64_t V,
 template <bool TOPP, bool TMA>
 __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, float c0) {
   pdl_trigger();   // the recompute pass may be scheduled (it waits for this grid)
+  pdl_wait();      // the logits may come from the kernel before
   extern __shared__ __align__(128) uint8_t smem[];
   Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem);
   float* part = reinterpret_cast<float*>(smem + g.off_part);         // [2][4][32]: E, S hi, S lo, U
@@ -1253,13 +1254,12 @@ cudaError_t launch_lpe_stream(const LpeArgs& a, cudaStream_t stream, long long w
   }
   const int nsm = sm_count();
   const int64_t grid = a.T < (int64_t)nsm ? a.T : (int64_t)nsm;
-  switch (vi) {
-    case 0: lpe_stream_kernel<false, false><<<(unsigned)grid, NTB, smem, stream>>>(a, g, c); break;
-    case 1: lpe_stream_kernel<false, true><<<(unsigned)grid, NTB, smem, stream>>>(a, g, c); break;
-    case 2: lpe_stream_kernel<true, false><<<(unsigned)grid, NTB, smem, stream>>>(a, g, c); break;
-    default: lpe_stream_kernel<true, true><<<(unsigned)grid, NTB, smem, stream>>>(a, g, c); break;
-  }
-  return cudaGetLastError();
+  // a programmatic dependent of the kernel before it on the stream (it waits
+  // for that kernel's writes before reading anything)
+  void (*const ks[4])(LpeArgs, Geom, float) = {lpe_stream_kernel<false, false>, lpe_stream_kernel<false, true>,
+                                               lpe_stream_kernel<true, false>, lpe_stream_kernel<true, true>};
+  e = launch_after(ks[vi], dim3((unsigned)grid), dim3(NTB), smem, stream, a, g, c);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace rlk
