@@ -33,7 +33,7 @@ struct LpeArgs {
   float* out_entropy;
   int32_t* out_k;
   uint32_t* status;
-  int only_marked;  // per-row kernel: process only rows whose out_logprob holds kRecomputeMark
+  int only_marked;  // per-row kernel: process only rows whose out_logprob holds a recompute mark
   RowState* state;  // [T] or NULL
   // per-row sampling parameters (NULL: the scalars above for every row)
   const float* temps = nullptr;
@@ -55,9 +55,12 @@ struct LpeBwdArgs {
   uint32_t* status;
 };
 
-// A quiet-NaN payload that no arithmetic produces: the streaming kernel leaves it
-// in out_logprob for rows that the per-row kernel must recompute.
+// Quiet-NaN payloads that no arithmetic produces: the streaming kernel leaves
+// one in out_logprob for each row that the per-row kernel must recompute --
+// the second for a row whose speculative window held too little mass, which
+// the per-row kernel then scores in its guaranteed window at once.
 constexpr uint32_t kRecomputeMark = 0x7FC0DEADu;
+constexpr uint32_t kRecomputeMarkWide = 0x7FC0DEAEu;
 
 struct SupportArgs {
   const void* logits;

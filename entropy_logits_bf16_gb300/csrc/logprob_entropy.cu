@@ -334,7 +334,8 @@ struct __align__(16) Smem {
   unsigned long long merged_w, merged_u;  // fixed-point sums of the near-zero bin
   uint32_t merged_n;
   uint32_t gmin_key;                      // ordered key of the row's smallest value
-  uint32_t marked[NWARP];                 // recompute pass: which of the next NT rows are marked
+  uint32_t marked[NWARP];                 // recompute pass: which of the next NT rows are marked,
+  uint32_t wide[NWARP];                   // and which of them take the guaranteed window at once
   int dstar;
   // result of the scan, written by the thread owning the threshold bin
   float r_pb_hi, r_pb_lo, r_um_before, r_w, r_x;
@@ -963,17 +964,23 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c0, float i
   constexpr bool HIST = TOPP && BF;   // histogram select (else bisection at top_p < 1)
   int64_t i_row = 0;   // this CTA's row count (the recompute pass reads its marks NT at a time)
   for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x, ++i_row) {
+    bool wide_first = false;   // the streaming kernel found its window's mass short
     if (a.only_marked) {
       const int slot = (int)(i_row % NT);
       if (slot == 0) {
         __syncthreads();
         const int64_t rr = r + (int64_t)tid * gridDim.x;
-        const bool mk = rr < a.T && __float_as_uint(a.out_logprob[rr]) == kRecomputeMark;
-        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, mk);
-        if ((tid & 31) == 0) sm.marked[tid >> 5] = bal;
+        const uint32_t mb = rr < a.T ? __float_as_uint(a.out_logprob[rr]) : 0u;
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, mb == kRecomputeMark || mb == kRecomputeMarkWide);
+        const uint32_t wbal = __ballot_sync(0xFFFFFFFFu, mb == kRecomputeMarkWide);
+        if ((tid & 31) == 0) {
+          sm.marked[tid >> 5] = bal;
+          sm.wide[tid >> 5] = wbal;
+        }
         __syncthreads();
       }
       if (((sm.marked[slot >> 5] >> (slot & 31)) & 1u) == 0u) continue;
+      wide_first = ((sm.wide[slot >> 5] >> (slot & 31)) & 1u) != 0u;
     }
     Row row;
     row.p = reinterpret_cast<decltype(row.p)>(a.logits) + r * a.ld;
@@ -1086,9 +1093,10 @@ __global__ void __launch_bounds__(NT, 3) lpe_kernel(LpeArgs a, float c0, float i
       const uint32_t ck_m = compress_key(Row::key(m));
       bool done = false;
       // Second pass over the row (served from L2): the speculative window,
-      // then, if its mass falls short, the worst-case window.
+      // then, if its mass falls short, the worst-case window (at once for a
+      // row whose speculative window the streaming kernel found short).
       for (int att = 0; att < 2 && !done && !use_bisect; ++att) {
-        if (att == 0 && !(L_spec < L_worst)) continue;
+        if (att == 0 && (!(L_spec < L_worst) || wide_first)) continue;
         const float L = att == 0 ? L_spec : L_worst;
         const float zlo = __fsub_rn(m, __fmul_rn(L, temp));
         bool merged_in;

@@ -422,7 +422,8 @@ struct ScanOut {
 template <bool CZ>
 __device__ bool warp_scan_window(int lane, uint32_t dmax, uint32_t key_m, float c, float E,
                                  DF target, const uint32_t* hist, uint32_t key_y, uint32_t tie_y,
-                                 ScanOut& out, float mg_mass = 0.f, float mg_um = 0.f) {
+                                 ScanOut& out, bool& short_mass, float mg_mass = 0.f,
+                                 float mg_um = 0.f) {
   // key_m: the max's key, compressed when cz (bin d holds compressed key key_m - d)
   const uint32_t bpl = (dmax + 32u) / 32u;
   const uint32_t d0 = (uint32_t)lane * bpl;
@@ -489,6 +490,7 @@ __device__ bool warp_scan_window(int lane, uint32_t dmax, uint32_t key_m, float 
     pu = __fadd_rn(pu, um);
   }
   const uint32_t bal = __ballot_sync(0xFFFFFFFFu, my_d >= 0);
+  short_mass = bal == 0u;   // no bin reaches the target: the window holds too little
   if (bal == 0u) return false;
   const int win = __ffs(bal) - 1;   // the lowest lane holds the lowest crossing bin
   // a crossing inside the shared near-zero bin needs its tokens' order
@@ -1115,11 +1117,11 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
             // mass: the row is handed on without a scan (the compute warps
             // stopped counting it too).
             const bool lost = CZ && ctl.mgn[b] > MGCAP;
-            bool found = false;
+            bool found = false, short_mass = false;
             if (!lost) {
               if (CZ) mg_sums(ctl, b, lane, rc.c, rc.E, mg_mass, mg_um);
               found = warp_scan_window<CZ>(lane, rc.dmax, rc.ckm, rc.c, rc.E, target, hist, rc.key_y,
-                                           tie_all, so, mg_mass, mg_um);
+                                           tie_all, so, short_mass, mg_mass, mg_um);
               // (units beyond the list's room were counted whole by the compute warps)
               const uint32_t ncx = ctl.lcnt[b] < LCAP ? ctl.lcnt[b] : LCAP;
               if (ncx > 0u) {
@@ -1157,15 +1159,15 @@ __global__ void __launch_bounds__(NTB, 1) lpe_stream_kernel(LpeArgs a, Geom g, f
                   __syncwarp();
                   if (CZ) mg_sums(ctl, b, lane, rc.c, rc.E, mg_mass, mg_um);
                   found = warp_scan_window<CZ>(lane, rc.dmax, rc.ckm, rc.c, rc.E, target, hist, rc.key_y,
-                                           tie_all, so, mg_mass, mg_um);
+                                           tie_all, so, short_mass, mg_mass, mg_um);
                 }
               }
             }
             // the second look can fill the shared bin's list too
-            if (CZ && ctl.mgn[b] > MGCAP) found = false;
+            if (CZ && ctl.mgn[b] > MGCAP) found = short_mass = false;
             if (lane == 0) {
               if (!found) {
-                a.out_logprob[r] = __uint_as_float(kRecomputeMark);
+                a.out_logprob[r] = __uint_as_float(short_mass ? kRecomputeMarkWide : kRecomputeMark);
               } else {
                 a.out_logprob[r] = so.y_in
                                        ? __fsub_rn(__fmul_rn(kLn2, __fmaf_rn(rc.zy, rc.c, -rc.E)), so.lz)

@@ -25,7 +25,7 @@ from _parity import compare_rows
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-MARK = 0x7FC0DEAD
+MARKS = (0x7FC0DEAD, 0x7FC0DEAE)   # the recompute marks
 T_CFG2 = 8 * 6912
 TEMP, TOP_P = 0.7, 0.95
 
@@ -72,7 +72,7 @@ def test_long_response_batch_full_size(cuda_lib, oracle):
     lp, ent, k, status = _run(cuda_lib, z, ids)
     assert status == 0
     # properties of every row
-    assert not np.any(lp.view(np.uint32) == MARK)
+    assert not np.isin(lp.view(np.uint32), MARKS).any()
     assert np.all(np.isfinite(lp) | np.isneginf(lp)) and np.all(np.isfinite(ent))
     assert np.all((k >= 1) & (k <= V))
     assert np.all(ent >= -1e-5) and np.all(ent <= np.log(k) + 1e-4)
